@@ -1,0 +1,426 @@
+"""Pins for the CPU oracle, against what the format definitions and the mathematics fix.
+
+Each test ties one oracle function to something other than itself: the closed-form definition
+of a format, a printed landmark value (tests/golden), IEEE float32 arithmetic as numpy performs
+it, a library routine (numpy matmul, scipy softmax), an invariant, or a closed-form special
+case. A plausible slip in the oracle (a dropped term, a wrong sign, a transposed operand, a
+wrong tie rule) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import softmax
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "nvfp4_formats.txt")
+
+
+# ------------------------------------------------------------------ formats
+def _e2m1_closed(code):
+    s = -1.0 if code & 8 else 1.0
+    e = (code >> 1) & 3
+    m = code & 1
+    mag = 0.5 * m if e == 0 else 2.0 ** (e - 1) * (1 + m / 2)
+    return s * mag
+
+
+def _e4m3_closed(byte):
+    s = -1.0 if byte & 0x80 else 1.0
+    e = (byte >> 3) & 0xF
+    m = byte & 7
+    if e == 15 and m == 7:
+        return math.nan
+    mag = (m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+    return s * mag
+
+
+def test_e2m1_exhaustive_decode_matches_closed_form():
+    for code in range(16):
+        assert oracle.e2m1_value(code) == _e2m1_closed(code)
+
+
+def test_e4m3_exhaustive_decode_matches_closed_form():
+    for b in range(256):
+        v, ref = oracle.e4m3_value(b), _e4m3_closed(b)
+        if math.isnan(ref):
+            assert math.isnan(v)
+        else:
+            assert v == ref and math.copysign(1, v) == math.copysign(1, ref)
+
+
+def test_formats_golden_landmarks():
+    n = 0
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        fmt, code, val = line.split()
+        code = int(code, 16)
+        got = oracle.e2m1_value(code) if fmt == "e2m1" else oracle.e4m3_value(code)
+        if val == "nan":
+            assert math.isnan(got)
+        else:
+            ref = float(val)
+            assert got == ref and math.copysign(1, got) == math.copysign(1, ref), (fmt, code)
+        n += 1
+    assert n == 26
+
+
+def _nearest_brute(values, v, codes):
+    """Nearest representable magnitude by exhaustive search, ties to the even code."""
+    best = None
+    for c, m in zip(codes, values):
+        d = abs(m - abs(v))
+        if best is None or d < best[0] or (d == best[0] and c % 2 == 0 and best[1] % 2 == 1):
+            best = (d, c)
+    return best[1]
+
+
+def test_e2m1_encode_textbook_ties_and_saturation():
+    # ties go to the even code (RNE), values above 6 saturate to 6
+    cases = [(0.25, 0x0), (0.75, 0x2), (1.25, 0x2), (1.75, 0x4), (2.5, 0x4), (3.5, 0x6),
+             (5.0, 0x6), (0.2499, 0x0), (0.2501, 0x1), (5.0001, 0x7), (6.0, 0x7), (7.0, 0x7),
+             (1e30, 0x7), (-0.75, 0xA), (-1e-9, 0x8), (0.0, 0x0), (-0.0, 0x8)]
+    for v, c in cases:
+        assert oracle.e2m1_encode(v) == c, v
+
+
+def test_e2m1_encode_brute_force():
+    rng = np.random.default_rng(1)
+    mags = [abs(_e2m1_closed(c)) for c in range(8)]
+    vals = list(rng.uniform(-7, 7, 400).astype(np.float32))
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    for m in mids:
+        for d in (-1, 0, 1):
+            vals.append(np.nextafter(np.float32(m), np.float32(np.inf if d > 0 else -np.inf))
+                        if d else np.float32(m))
+    for v in vals:
+        v = float(np.float32(v))
+        want = _nearest_brute(mags, min(abs(v), 6.0), list(range(8)))
+        want |= 8 if math.copysign(1, v) < 0 else 0
+        assert oracle.e2m1_encode(v) == want, v
+
+
+def test_e4m3_encode_brute_force_and_ties():
+    mags = [_e4m3_closed(b) for b in range(0x7F)]
+    rng = np.random.default_rng(2)
+    vals = list(np.exp(rng.uniform(np.log(1e-4), np.log(500), 500)).astype(np.float32))
+    for b in range(0x7E):   # every midpoint and its float neighbours
+        mid = np.float32((mags[b] + mags[b + 1]) / 2)
+        vals += [mid, np.nextafter(mid, np.float32(0)), np.nextafter(mid, np.float32(1e9))]
+    for v in vals:
+        v = float(v)
+        want = 0x7E if v >= 448 else _nearest_brute(mags, v, list(range(0x7F)))
+        assert oracle.e4m3_encode(v) == want, v
+    assert oracle.e4m3_encode(1.0625) == 0x38   # tie between 1 (0x38) and 1.125 -> even
+    assert oracle.e4m3_encode(1.1875) == 0x3A   # tie between 1.125 and 1.25 -> even
+    assert oracle.e4m3_encode(2.0 ** -10) == 0  # tie between 0 and 2^-9 -> even (0)
+    assert oracle.e4m3_encode(464.0) == 0x7E    # satfinite
+    assert oracle.e4m3_encode(1e30) == 0x7E
+
+
+def test_f32_ops_match_numpy_ieee_float32():
+    rng = np.random.default_rng(3)
+    a = (rng.standard_normal(3000) * np.exp(rng.uniform(-60, 60, 3000))).astype(np.float32)
+    b = (rng.standard_normal(3000) * np.exp(rng.uniform(-60, 60, 3000))).astype(np.float32)
+    a[:10] = np.float32(1e-42)   # subnormals
+    with np.errstate(all="ignore"):
+        pm = a * b
+        pd = a / b
+    for i in range(len(a)):
+        m = oracle.f32_mul(float(a[i]), float(b[i]))
+        d = oracle.f32_div(float(a[i]), float(b[i]))
+        assert np.float32(m).tobytes() == pm[i].tobytes()
+        assert np.float32(d).tobytes() == pd[i].tobytes()
+
+
+def test_double_to_bf16_against_independent_rounding():
+    rng = np.random.default_rng(4)
+    f = (rng.standard_normal(5000) * np.exp(rng.uniform(-30, 30, 5000))).astype(np.float32)
+    ref = synth.bf16_bits(f)   # integer rounding of the float32 pattern
+    got = np.array([oracle.double_to_bf16(float(v)) for v in f], np.uint16)
+    assert np.array_equal(ref, got)
+    # ties in double precision: exactly halfway between two BF16 values
+    assert oracle.double_to_bf16(1.0 + 2.0 ** -8) == 0x3F80            # tie -> even (1.0)
+    assert oracle.double_to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82        # tie -> even
+    assert oracle.double_to_bf16(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81  # just above the tie
+
+
+# ------------------------------------------------------------------ quantiser
+def test_quantizer_steps_match_numpy_float32():
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        S = np.float32(np.exp(rng.uniform(-12, 2)))
+        v = (rng.standard_normal(16) * np.exp(rng.uniform(-3, 3))).astype(np.float32)
+        st = oracle.quantize_block_steps(v, float(S))
+        inv6S = np.float32(1) / (np.float32(6) * S)
+        assert np.float32(st["inv6S"]) == inv6S
+        t = np.float32(np.abs(v).max()) * inv6S
+        assert np.float32(st["t"]) == t
+        assert st["sf"] == oracle.e4m3_encode(float(t))
+        sfv = np.float32(oracle.e4m3_value(st["sf"]))
+        if sfv == 0:
+            assert np.all(st["codes"] == 0)
+            continue
+        r = np.float32(1) / (sfv * S)
+        assert np.float32(st["r"]) == r
+        assert np.array_equal(st["scaled"], v * r)
+        for i in range(16):
+            assert st["codes"][i] == oracle.e2m1_encode(float(v[i] * r))
+
+
+def _dec_block(codes, sf, S):
+    return np.array([oracle.e2m1_value(c) for c in codes]) * oracle.e4m3_value(sf) * S
+
+
+def test_quantizer_round_trip_on_representable_blocks():
+    rng = np.random.default_rng(6)
+    for _ in range(300):
+        S = float(np.float32(np.exp(rng.uniform(-12, 0))))
+        sf = int(rng.integers(0x08, 0x7E))          # a normal, unsaturated scale
+        codes = rng.integers(0, 16, 16)
+        codes[rng.integers(0, 16)] = 7 | (8 * int(rng.integers(0, 2)))   # the amax -> 6
+        v = _dec_block(codes, sf, S).astype(np.float32)
+        if not np.all(v.astype(np.float64) == _dec_block(codes, sf, S)):
+            continue   # not exactly representable in float32 at this S
+        c, s = oracle.quantize_nvfp4(v[None, :], S)
+        assert s[0, 0] == sf
+        dec_codes = [(c[0, i // 2] >> (4 * (i % 2))) & 0xF for i in range(16)]
+        # zero codes may carry either sign; compare decoded values for them
+        assert np.array_equal(_dec_block(dec_codes, sf, S), _dec_block(codes, sf, S))
+
+
+def test_quantizer_error_and_amax_invariants():
+    rng = np.random.default_rng(7)
+    rows = (rng.standard_normal((200, 64)) * np.exp(rng.uniform(-2, 2, (200, 1)))).astype(
+        np.float32)
+    S = float(np.float32(np.abs(rows).max() / 2688.0))
+    codes, scales = oracle.quantize_nvfp4(rows, S)
+    for r in range(rows.shape[0]):
+        for b in range(4):
+            v = rows[r, b * 16:(b + 1) * 16].astype(np.float64)
+            sf = scales[r, b]
+            cs = [(codes[r, b * 8 + i // 2] >> (4 * (i % 2))) & 0xF for i in range(16)]
+            dec = _dec_block(cs, sf, S)
+            unit = oracle.e4m3_value(sf) * S
+            # every element within half a step of the grid it was rounded on (steps 0.5/1/2)
+            for i in range(16):
+                mag = abs(v[i]) / unit
+                step = 0.5 if mag <= 2 else (1.0 if mag <= 4 else 2.0)
+                assert abs(dec[i] - v[i]) <= (step / 2) * unit * (1 + 1e-6) + 1e-30
+                assert np.sign(dec[i]) in (0, np.sign(v[i]))
+            amax_i = int(np.argmax(np.abs(v)))
+            if 0x08 <= sf < 0x7E:
+                assert cs[amax_i] & 7 == 7     # the block maximum maps to +-6
+
+
+def test_quantizer_zero_and_saturated_blocks():
+    c, s = oracle.quantize_nvfp4(np.zeros((1, 16), np.float32), 0.01)
+    assert s[0, 0] == 0 and np.all(c == 0)
+    v = np.full((1, 16), 1e6, np.float32)
+    v[0, 3] = -1e6
+    c, s = oracle.quantize_nvfp4(v, 1e-3)
+    assert s[0, 0] == 0x7E
+    assert c[0, 0] == 0x77 and c[0, 1] == 0xF7
+
+
+# ------------------------------------------------------------------ routing
+def _tiny_route_inputs(seed, T, E, H):
+    x = synth.activations(seed, 0, T, H)
+    wr = synth.router_weight(seed, 0, E, H)
+    return x, wr
+
+
+def test_route_topk_brute_force_and_tie_rule():
+    T, E, H, k = 5, 9, 64, 3
+    x, wr = _tiny_route_inputs(11, T, E, H)
+    wr[4] = wr[2]     # experts 2 and 4 have equal logits: 2 must come first
+    wr[7] = wr[2]
+    r = oracle.route(x, wr, k)
+    l64 = synth.bf16_to_f32(x).astype(np.float64) @ synth.bf16_to_f32(wr).astype(np.float64).T
+    assert np.allclose(r["logits"], l64, rtol=1e-13, atol=1e-13)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-l64[t, e], e))
+        assert list(r["idx"][t]) == order[:k]
+        sel = set(order[:k])
+        assert min(l64[t, e] for e in sel) >= max(l64[t, e] for e in range(E) if e not in sel)
+    np.testing.assert_allclose(r["w"].sum(1), 1.0, rtol=1e-14)
+    for t in range(T):
+        for a in range(k):
+            for b in range(k):
+                ia, ib = r["idx"][t, a], r["idx"][t, b]
+                assert math.isclose(r["w"][t, a] / r["w"][t, b],
+                                    math.exp(l64[t, ia] - l64[t, ib]), rel_tol=1e-12)
+
+
+def test_route_k1_and_k_equals_E():
+    T, E, H = 4, 6, 32
+    x, wr = _tiny_route_inputs(12, T, E, H)
+    r1 = oracle.route(x, wr, 1)
+    assert np.all(r1["w"] == 1.0)
+    rE = oracle.route(x, wr, E)
+    full = softmax(rE["logits"], axis=1)
+    for t in range(T):
+        np.testing.assert_allclose(rE["w"][t], full[t, rE["idx"][t]], rtol=1e-13)
+
+
+def test_route_permutation_is_a_stable_counting_sort():
+    T, E, H, k = 37, 16, 64, 4
+    x, wr = _tiny_route_inputs(13, T, E, H)
+    r = oracle.route(x, wr, k)
+    assert r["counts"].sum() == T * k
+    assert np.array_equal(r["offsets"], np.concatenate([[0], np.cumsum(r["counts"])]))
+    pairs = sorted((int(r["idx"][t, j]), t) for t in range(T) for j in range(k))
+    assert list(r["perm"]) == [t for _, t in pairs]
+    for t in range(T):
+        for j in range(k):
+            s = r["slot_of"][t, j]
+            e = r["idx"][t, j]
+            assert r["perm"][s] == t and r["offsets"][e] <= s < r["offsets"][e + 1]
+    assert sorted(r["slot_of"].ravel().tolist()) == list(range(T * k))
+
+
+# ------------------------------------------------------------------ expert FFN
+def _make_experts(seed, E, H, I, down_scales=None):
+    ex = oracle.ExpertSet(E, H, I)
+    for e in range(E):
+        gq = oracle.quantize_weight_bf16(synth.expert_weight(seed, 0, e, "gate", H, I))
+        uq = oracle.quantize_weight_bf16(synth.expert_weight(seed, 0, e, "up", H, I))
+        dq = oracle.quantize_weight_bf16(synth.expert_weight(seed, 0, e, "down", H, I))
+        xs = synth.activation_input_scale(H)
+        ds = 14.0 / 2688 if down_scales is None else down_scales[e]
+        ex.set(e, gq[:2], uq[:2], dq[:2], (gq[2], uq[2], dq[2]), (xs, xs, ds))
+    return ex
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    wl = synth.WORKLOADS["tiny"]
+    x = synth.activations(0, 0, wl.T, wl.H)
+    wr = synth.router_weight(0, 0, wl.E, wl.H)
+    ex = _make_experts(0, wl.E, wl.H, wl.I, synth.down_input_scales(0, 0, wl.E))
+    return wl, x, wr, ex
+
+
+def test_forward_matches_numpy_float64_pipeline(tiny):
+    wl, x, wr, ex = tiny
+    res = oracle.forward(x, wr, ex, wl.k, oracle.W4A16,
+                         want=("out64", "idx", "w", "slot_of", "perm", "g", "u", "h", "y"))
+    xf = synth.bf16_to_f32(x).astype(np.float64)
+    for s in range(wl.T * wl.k):
+        t = res["perm"][s]
+        e = int(np.searchsorted(np.cumsum(np.bincount(res["idx"].ravel(), minlength=wl.E)), s,
+                                side="right"))
+        Wg = oracle.dequantize_nvfp4(*ex.gate[e], ex.mult[e, 0])
+        Wu = oracle.dequantize_nvfp4(*ex.up[e], ex.mult[e, 1])
+        Wd = oracle.dequantize_nvfp4(*ex.down[e], ex.mult[e, 2])
+        g = Wg @ xf[t]
+        u = Wu @ xf[t]
+        np.testing.assert_allclose(res["g"][s], g, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(res["u"][s], u, rtol=1e-12, atol=1e-12)
+        h = g * (1 / (1 + np.exp(-g))) * u
+        np.testing.assert_allclose(res["h"][s], h, rtol=1e-12, atol=1e-12)
+        hb = synth.bf16_to_f32(np.array([oracle.double_to_bf16(v) for v in h], np.uint16))
+        y = Wd @ hb.astype(np.float64)
+        yb = synth.bf16_to_f32(np.array([oracle.double_to_bf16(v) for v in y], np.uint16))
+        np.testing.assert_allclose(res["y"][s], yb, rtol=0, atol=0)
+    for t in range(wl.T):
+        acc = sum(res["w"][t, j] * res["y"][res["slot_of"][t, j]] for j in range(wl.k))
+        np.testing.assert_allclose(res["out64"][t], acc, rtol=1e-13, atol=1e-13)
+
+
+def test_forward_one_hot_weights_closed_form():
+    E, H, I, k, T = 4, 64, 32, 1, 3
+    x = synth.activations(21, 0, T, H)
+    wr = synth.router_weight(21, 0, E, H)
+    ex = oracle.ExpertSet(E, H, I)
+    rng = np.random.default_rng(21)
+    sf = 0x38   # scale 1.0
+    for e in range(E):
+        cols = rng.integers(0, H, I)
+        gc = np.zeros((I, H // 2), np.uint8)
+        for i in range(I):
+            c = cols[i]
+            gc[i, c // 2] |= 7 << (4 * (c % 2))      # code +6 at one column per row
+        gs = np.full((I, H // 16), sf, np.uint8)
+        ex.set(e, (gc, gs), (gc, gs), (np.zeros((H, I // 2), np.uint8),
+                                        np.zeros((H, I // 16), np.uint8)), (0.25, 0.5, 1.0))
+        ex.cols = getattr(ex, "cols", {})
+        ex.cols[e] = cols
+    res = oracle.forward(x, wr, ex, k, oracle.W4A16, want=("g", "u", "perm", "idx", "counts"))
+    xf = synth.bf16_to_f32(x).astype(np.float64)
+    offs = np.concatenate([[0], np.cumsum(res["counts"])])
+    for s in range(T * k):
+        t = res["perm"][s]
+        e = int(np.searchsorted(offs, s, side="right") - 1)
+        np.testing.assert_array_equal(res["g"][s], 6 * 0.25 * xf[t, ex.cols[e]])
+        np.testing.assert_array_equal(res["u"][s], 6 * 0.5 * xf[t, ex.cols[e]])
+
+
+def test_forward_identical_experts_give_one_expert(tiny):
+    wl, x, wr, ex = tiny
+    same = oracle.ExpertSet(wl.E, wl.H, wl.I)
+    for e in range(wl.E):
+        same.set(e, ex.gate[0], ex.up[0], ex.down[0], ex.mult[0], ex.in_scale[0])
+    res = oracle.forward(x, wr, same, wl.k, oracle.W4A16, want=("y", "slot_of"))
+    for t in range(wl.T):
+        y0 = res["y"][res["slot_of"][t, 0]]
+        assert np.array_equal(synth.bf16_to_f32(res["out_bf16"][t]).astype(np.float64), y0)
+
+
+def test_forward_zero_gate_gives_zero(tiny):
+    wl, x, wr, ex = tiny
+    z = oracle.ExpertSet(wl.E, wl.H, wl.I)
+    zc = (np.zeros((wl.I, wl.H // 2), np.uint8), np.zeros((wl.I, wl.H // 16), np.uint8))
+    for e in range(wl.E):
+        z.set(e, zc, ex.up[e], ex.down[e], ex.mult[e], ex.in_scale[e])
+    res = oracle.forward(x, wr, z, wl.k, oracle.W4A16, want=("h",))
+    assert np.all(res["h"] == 0) and np.all(synth.bf16_to_f32(res["out_bf16"]) == 0)
+
+
+def test_forward_w4a4_equals_w4a16_before_h_on_representable_x(tiny):
+    wl, _, wr, ex0 = tiny
+    rng = np.random.default_rng(31)
+    S = 2.0 ** -9          # a power of two, so code * scale * S is exactly BF16
+    ex = oracle.ExpertSet(wl.E, wl.H, wl.I)
+    for e in range(wl.E):
+        ex.set(e, ex0.gate[e], ex0.up[e], ex0.down[e], ex0.mult[e],
+               (S, S, ex0.in_scale[e, 2]))
+    codes = rng.integers(0, 16, (wl.T, wl.H))
+    codes[:, ::16] = 7
+    sfs = rng.integers(0x30, 0x48, (wl.T, wl.H // 16))
+    xv = np.array([[oracle.e2m1_value(c) for c in row] for row in codes]) * \
+        np.repeat(np.vectorize(oracle.e4m3_value)(sfs), 16, axis=1) * S
+    x = synth.bf16_bits(xv.astype(np.float32))
+    assert np.array_equal(synth.bf16_to_f32(x).astype(np.float64), xv)  # exactly BF16
+    a = oracle.forward(x, wr, ex, wl.k, oracle.W4A16, want=("g", "u"))
+    b = oracle.forward(x, wr, ex, wl.k, oracle.W4A4, want=("g", "u", "xq_codes", "xq_scales"))
+    assert np.array_equal(a["g"], b["g"]) and np.array_equal(a["u"], b["u"])
+    qc, qs = oracle.quantize_nvfp4(synth.bf16_to_f32(x), S)
+    assert np.array_equal(qs, b["xq_scales"]) and np.array_equal(qc, b["xq_codes"])
+
+
+def test_forward_w4a4_h_codes_are_q_of_h(tiny):
+    wl, x, wr, ex = tiny
+    res = oracle.forward(x, wr, ex, wl.k, oracle.W4A4,
+                         want=("h", "hq_codes", "hq_scales", "idx", "counts", "h_amb_elem"))
+    offs = np.concatenate([[0], np.cumsum(res["counts"])])
+    for s in range(wl.T * wl.k):
+        e = int(np.searchsorted(offs, s, side="right") - 1)
+        c, sc = oracle.quantize_nvfp4(res["h"][s][None, :].astype(np.float32),
+                                      float(ex.in_scale[e, 2]))
+        assert np.array_equal(c[0], res["hq_codes"][s]) and np.array_equal(sc[0],
+                                                                          res["hq_scales"][s])
+    assert np.all(res["h_amb_elem"] >= 0)
+
+
+def test_synth_streams_are_deterministic_and_independent():
+    a = synth.expert_weight(0, 3, 7, "gate", 64, 32)
+    b = synth.expert_weight(0, 3, 7, "gate", 64, 32)
+    c = synth.expert_weight(0, 3, 8, "gate", 64, 32)
+    assert np.array_equal(a, b) and not np.array_equal(a, c)
+    assert synth.activations(0, 0, 4, 64).shape == (4, 64)
