@@ -1,0 +1,481 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 NVFP4 routed-expert MoE step (one JSON line on stdout).
+
+Headline workload (``decode1``): one decode step of a 48-layer stack, 1 token per layer, W4A16,
+hidden 4096, 512 experts, top-10, expert intermediate 384; every layer has its own router and its
+own 512-expert NVFP4 pack (65 GB resident), so a step streams 48 x 10 selected experts
+(1.27 GB) and nothing is reused from L2 between steps. A "step" = the 48 layers, captured in
+one CUDA graph (PDL-chained kernels). ``value`` = layer-tokens per second = T * layers / step
+time. Inputs are seeded synthetic (``synth``), resident in HBM before timing starts.
+
+Also reported in the same line: the roofline of the dominant kernel (gate/up) from CUDA events
+recorded around it on its stream, the end-to-end number through the C ABI with host buffers
+(host->device copy of x and device->host copy of out inside the timed region), the SM clocks
+sampled during the timed region, a secondary table (8-token verify W4A16/W4A4 and the
+8192-token prefill), and the CPU oracle timed on a bounded sample as a reported baseline.
+
+``--impl reference`` times the CPU oracle alone (the reference arm of this comparison).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer tokens/s + HBM GB/s (decode), NVFP4 TFLOPS (prefill), % roofline"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--workload", default="decode1", choices=list(synth.WORKLOADS))
+    p.add_argument("--layers", type=int, default=None)
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=smax,
+                    reasons=sorted(reasons), samples=len(sm))
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_mixture_experts_bf16_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    d = json.load(open(path)).get(f"{kernel}:{workload}")
+    if not d or d.get("source_sha") != source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def bytes_gateup(U, H, I):
+    return U * (2 * I * H // 2 + 2 * I * H // 16)
+
+
+def bytes_down(U, H, I):
+    return U * (H * I // 2 + H * I // 16)
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline arm)
+def oracle_sample(wl, seed, n_tokens, threads):
+    """A bounded sample of the workload for the CPU oracle: n_tokens tokens of layer 0 with the
+    experts they select (generated and quantised outside the timed region)."""
+    import oracle
+    H, E, k, I = wl.H, wl.E, wl.k, wl.I
+    x = synth.activations(seed, 0, n_tokens, H, wl.zipf)
+    wr = synth.router_weight(seed, 0, E, H, wl.zipf)
+    r = oracle.route(x, wr, k, nthreads=threads)
+    ex = oracle.ExpertSet(E, H, I)
+    xs = synth.activation_input_scale(H)
+    ds = synth.down_input_scales(seed, 0, E)
+    for e in sorted(set(r["idx"].ravel().tolist())):
+        q = [oracle.quantize_weight_bf16(synth.expert_weight(seed, 0, e, w, H, I), nthreads=threads)
+             for w in ("gate", "up", "down")]
+        ex.set(e, q[0][:2], q[1][:2], q[2][:2], (q[0][2], q[1][2], q[2][2]), (xs, xs, float(ds[e])))
+    return x, wr, ex
+
+
+def time_oracle(wl, seed, steps, budget_s, threads, n_tokens):
+    import oracle
+    x, wr, ex = oracle_sample(wl, seed, n_tokens, threads)
+    times = []
+    t_end = time.time() + budget_s
+    for _ in range(max(1, steps)):
+        t0 = time.perf_counter()
+        oracle.forward(x, wr, ex, wl.k, wl.mode, nthreads=threads, want=("out_bf16",))
+        times.append(time.perf_counter() - t0)
+        if time.time() > t_end:
+            break
+    t = statistics.median(times)
+    return dict(value=n_tokens / t, unit="layer-tokens/s", cores=threads, kind="oracle",
+                sample=f"{n_tokens} tokens of layer 0 of '{wl.name}' (T={wl.T} workload shapes), "
+                       f"{len(times)} timed calls, median", calls=len(times))
+
+
+def run_reference(args, rank, world):
+    wl = synth.WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    n_tok = 4 if wl.T <= 8 else 8
+    cb = time_oracle(wl, args.seed, args.steps, budget_s=120, threads=threads, n_tokens=n_tok)
+    line = dict(impl="reference", metric=METRIC, value=cb["value"], unit=cb["unit"], n_gpus=0,
+                steps=cb["calls"], warmup=0, ms_per_step=1e3 * n_tok / cb["value"],
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic", config=dict(workload=wl.name, T=wl.T, hidden=wl.H,
+                                              experts=wl.E, top_k=wl.k, inter=wl.I,
+                                              mode=["W4A16", "W4A4"][wl.mode]),
+                cpu_baseline=cb,
+                e2e=dict(value=cb["value"], unit=cb["unit"], h2d_bytes_per_step=0,
+                         d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ native arm
+class Layer:
+    def __init__(self, x, wr, pack, U):
+        self.x, self.wr, self.pack, self.U = x, wr, pack, U
+
+
+def quantized_experts(seed, layer, E, H, I, device):
+    """Synthetic checkpoint of one layer drawn on the device and quantised with the library's
+    own NVFP4 quantiser (multiplier = global amax / 2688 per matrix)."""
+    import torch
+    import nvfp4_mixture_experts_bf16_gb300 as moe
+    mats = {}
+    for w in ("gate", "up", "down"):
+        W = synth.torch_expert_weights(seed, layer, w, E, H, I, device)
+        S = (W.float().abs().amax(dim=(1, 2)) / 2688.0).float().cpu().numpy()
+        rows, cols = W.shape[1], W.shape[2]
+        codes = torch.empty((E, rows, cols // 2), dtype=torch.uint8, device=device)
+        scales = torch.empty((E, rows, cols // 16), dtype=torch.uint8, device=device)
+        for e in range(E):
+            moe.moe_quantize_act_nvfp4(W[e], float(S[e]), codes[e], scales[e])
+        del W
+        mats[w] = (codes, scales, S)
+    return mats
+
+
+def dev_bf16(u16, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def build_stack(wl, layers, seed, device, packs=None):
+    """layers x (x, router, pack); packs may be reused from another workload of equal shapes."""
+    import torch
+    import nvfp4_mixture_experts_bf16_gb300 as moe
+    out = []
+    xs = synth.activation_input_scale(wl.H)
+    for l in range(layers):
+        x = dev_bf16(synth.activations(seed, l, wl.T, wl.H, wl.zipf), device)
+        wr = dev_bf16(synth.router_weight(seed, l, wl.E, wl.H, wl.zipf), device)
+        if packs is None:
+            m = quantized_experts(seed, l, wl.E, wl.H, wl.I, device)
+            ds = synth.down_input_scales(seed, l, wl.E)
+            args = []
+            for w in ("gate", "up", "down"):
+                codes, scales, S = m[w]
+                ins = [xs] * wl.E if w != "down" else [float(v) for v in ds]
+                args.append([(codes[e], scales[e], float(S[e]), ins[e]) for e in range(wl.E)])
+            pack = moe.moe_pack_nvfp4(args[0], args[1], args[2], wl.H, wl.I)
+            del m, args
+            torch.cuda.synchronize()
+        else:
+            pack = packs[l % len(packs)]
+        r = moe.moe_route_topk(x, wr, wl.k)
+        U = int((r["counts"] > 0).sum().item())
+        out.append(Layer(x, wr, pack, U))
+    return out
+
+
+def measure(wl, stack, steps, warmup, use_graph, device, clocks=None):
+    """Time `steps` steps (all layers) on one stream; returns per-step ms and the launch count."""
+    import torch
+    import nvfp4_mixture_experts_bf16_gb300 as moe
+    s = torch.cuda.Stream(device=device)
+    ws = moe.new_workspace(moe.moe_workspace_size(stack[0].pack, wl.T, wl.k, wl.mode), device)
+    outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in stack]
+    launches = [0]
+
+    def step():
+        n = 0
+        for L, o in zip(stack, outs):
+            moe.moe_forward(L.x, L.wr, L.pack, wl.k, wl.mode, out=o, ws=ws, stream=s)
+            n += moe.moe_last_launch_count()
+        launches[0] = n
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step()
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else step
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            run()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.start()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(steps):
+            run()
+        e1.record(s)
+    torch.cuda.synchronize()
+    info = clocks.stop() if clocks else None
+    status = moe.moe_read_device_status(ws, stream=s)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    return e0.elapsed_time(e1) / steps, launches[0], info, (s, ws, outs, graph)
+
+
+def stage_times(wl, stack, reps, device):
+    """Mean duration of each stage (route, gate/up, down, combine) per layer, from CUDA events
+    recorded around each stage on the launching stream (PDL off while profiling)."""
+    import torch
+    import nvfp4_mixture_experts_bf16_gb300 as moe
+    s = torch.cuda.Stream(device=device)
+    ws = moe.new_workspace(moe.moe_workspace_size(stack[0].pack, wl.T, wl.k, wl.mode), device)
+    outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in stack]
+    acc = np.zeros(4)
+    n = 0
+    with torch.cuda.stream(s):
+        for rep in range(reps + 1):
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in stack]
+            for L, o, ev in zip(stack, outs, evs):
+                moe.moe_profile_next_forward(ev)
+                moe.moe_forward(L.x, L.wr, L.pack, wl.k, wl.mode, out=o, ws=ws, stream=s)
+            torch.cuda.synchronize()
+            if rep == 0:
+                continue  # warm-up
+            for ev in evs:
+                acc += [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(4)]
+                n += 1
+    return acc / n  # ms per layer
+
+
+def e2e_measure(wl, stack, steps, state, device):
+    """Same metric through the public API with host buffers: per step, copy every layer's x
+    host->device (pinned), run the step, copy every layer's out device->host."""
+    import torch
+    s, ws, outs, graph = state
+    hx = [L.x.cpu().pin_memory() for L in stack]
+    ho = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory() for _ in stack]
+    run = graph.replay
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for it in range(steps + 2):
+            if it == 2:
+                e0.record(s)
+            for L, h in zip(stack, hx):
+                L.x.copy_(h, non_blocking=True)
+            run()
+            for o, h in zip(outs, ho):
+                h.copy_(o, non_blocking=True)
+        e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = len(stack) * wl.T * wl.H * 2
+    return ms, nbytes
+
+
+def run_native(args, rank, world, local_rank):
+    import torch
+    import nvfp4_mixture_experts_bf16_gb300 as moe
+    moe.build()
+    moe.lib()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    wl = synth.WORKLOADS[args.workload]
+    layers = args.layers or wl.layers
+    pk = peaks()
+    t_setup = time.time()
+    stack = build_stack(wl, layers, args.seed + 1000 * rank, device)
+    setup_s = time.time() - t_setup
+
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = Clocks(local_rank) if rank == 0 else None
+    ms, launches, clk, state = measure(wl, stack, args.steps, args.warmup, not args.no_graph,
+                                       device, clocks)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_step = wl.T * layers
+    value = world * tokens_per_step / (ms / 1e3)
+
+    st = stage_times(wl, stack, reps=3, device=device)
+    U_mean = float(np.mean([L.U for L in stack]))
+    gu_bytes = bytes_gateup(U_mean, wl.H, wl.I)
+    dn_bytes = bytes_down(U_mean, wl.H, wl.I)
+    gu_gbs = gu_bytes / (st[1] * 1e-3) / 1e9
+    layer_bytes = gu_bytes + dn_bytes
+    layer_gbs = layer_bytes / (ms / layers * 1e-3) / 1e9
+    roofline = dict(bound="hbm", kernel="k_gateup (gate/up + SiLU*up)",
+                    achieved=round(gu_gbs, 1), peak=pk["hbm"], unit="GB/s",
+                    frac=round(gu_gbs / pk["hbm"], 4),
+                    traffic=committed_traffic("k_gateup", wl.name),
+                    algorithmic_bytes_per_launch=int(gu_bytes),
+                    peak_source=f"{pk['src']} hbm_gbs (MEASURED_PEAKS.json)"
+                    if pk["src"] == "measured" else "fallback 6.8 TB/s")
+    e2e_ms, io_bytes = e2e_measure(wl, stack, max(3, args.steps // 2), state, device)
+
+    extra = {}
+    if not args.no_extra and rank == 0:
+        packs = [L.pack for L in stack]
+        for name in ("verify8", "verify8_w4a4"):
+            w2 = synth.WORKLOADS[name]
+            st2 = build_stack(w2, layers, args.seed, device, packs=packs)
+            ms2, _, _, _ = measure(w2, st2, max(3, args.steps // 2), 3, not args.no_graph, device)
+            U2 = float(np.mean([L.U for L in st2]))
+            b2 = bytes_gateup(U2, w2.H, w2.I) + bytes_down(U2, w2.H, w2.I)
+            extra[name] = dict(tokens_per_s=round(w2.T * layers / (ms2 / 1e3), 1),
+                               us_per_layer=round(ms2 / layers * 1e3, 2),
+                               unique_experts=round(U2, 2),
+                               hbm_gbs=round(b2 / (ms2 / layers * 1e-3) / 1e9, 1),
+                               frac_hbm=round(b2 / (ms2 / layers * 1e-3) / 1e9 / pk["hbm"], 4))
+        for mode in (1, 0):
+            name = "prefill8192"
+            w3 = synth.Workload(name, 8192, wl.H, wl.E, wl.k, wl.I, mode, 1, True)
+            st3 = build_stack(w3, 1, args.seed, device, packs=packs[:1])
+            ms3, _, _, _ = measure(w3, st3, 3, 2, False, device)
+            flops = 2 * w3.T * w3.k * 3 * w3.I * w3.H
+            extra[f"prefill8192_{['w4a16', 'w4a4'][mode]}"] = dict(
+                tokens_per_s=round(w3.T / (ms3 / 1e3), 1), ms=round(ms3, 3),
+                expert_tflops=round(flops / (ms3 * 1e-3) / 1e12, 2),
+                note="grouped fallback path (mma.sync); tcgen05 path pending")
+        torch.cuda.synchronize()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        cpu = time_oracle(wl, args.seed, 10, budget_s=25, threads=threads, n_tokens=4)
+
+    if rank != 0:
+        return
+    line = dict(
+        metric=METRIC, value=round(value, 2), unit="layer-tokens/s", n_gpus=world,
+        steps=args.steps, warmup=args.warmup, ms_per_step=round(ms, 5), higher_is_better=True,
+        scaling="weak", vs_baseline=None, dtype="nvfp4 weights, bf16/f16 operands, f32 accum",
+        data="synthetic", impl="native",
+        config=dict(workload=wl.name, T=wl.T, layers=layers, hidden=wl.H, experts=wl.E,
+                    top_k=wl.k, inter=wl.I, mode=["W4A16", "W4A4"][wl.mode],
+                    parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                    l2="no flush: a step streams 48 layers x 10 experts = 1.27 GB > 129 MB L2",
+                    graph=not args.no_graph, setup_s=round(setup_s, 1)),
+        gpu_launches=launches * args.steps,
+        roofline=roofline,
+        layer=dict(us=round(ms / layers * 1e3, 3), stage_us=dict(
+            route=round(st[0] * 1e3, 2), gateup=round(st[1] * 1e3, 2), down=round(st[2] * 1e3, 2),
+            combine=round(st[3] * 1e3, 2)), hbm_gbs=round(layer_gbs, 1),
+            frac_hbm=round(layer_gbs / pk["hbm"], 4), unique_experts=U_mean),
+        e2e=dict(value=round(world * tokens_per_step / (e2e_ms / 1e3), 2), unit="layer-tokens/s",
+                 h2d_bytes_per_step=io_bytes, d2h_bytes_per_step=io_bytes),
+        clocks=clk, cpu_baseline=cpu, secondary=extra)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "native":
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_native(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+/* moe_nvfp4.h — C ABI of the GB300 (sm_103a) NVFP4 routed-expert MoE feed-forward library.
+ *
+ * The operation is the routed-expert MoE feed-forward step of a Qwen-style sparse model as
+ * the pages describe it:
+ *   - the model card "Qwen3.8-Flash-Next NVIDIA NVFP4 for Infernix (bit-exact)", first
+ *     paragraph (512 routed experts per layer, top-10) and section "What is bit-exact and what
+ *     is quantized" (each routed expert matrix stored as E2M1 codes, one E4M3 scale per 16
+ *     weights, an FP32 multiplier and an FP32 activation input scale per matrix; the router
+ *     stored BF16);
+ *   - the Infernix README, section "Activation precision" (routed experts run W4A4 with the
+ *     checkpoint's calibrated input scales, or with 16-bit activations on the same 4-bit
+ *     weights), and the release notes "Infernix windows-2026.10.11", section "Highlights"
+ *     (narrow expert calls of up to eight columns; the down pass launched as a dependent of
+ *     gate/up).
+ * Readings taken where the pages are silent: the router keeps the k largest logits (equal
+ * logits: the lower expert index first) and weights them by the softmax over those k logits;
+ * an expert computes down(SiLU(gate x) * up x); h = SiLU(gate)*up is rounded to BF16 (W4A16)
+ * or quantised to NVFP4 with the down matrix's input scale (W4A4); each expert output Y is
+ * rounded to BF16; out = BF16(sum_j w_j * Y_j) summed in rank order j = 0..k-1 in FP32.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are row-major. "device" pointers must be device memory of the current
+ *     device, 16-byte aligned. BF16 tensors are passed as uint16_t bit patterns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; 0 = legacy default stream). No call
+ *     except moe_pack_nvfp4 / moe_pack_destroy / moe_pack_get_matrix / moe_read_device_status
+ *     allocates, frees or synchronises.
+ *   - Argument errors return before anything is launched. A launch failure returns
+ *     MOE_ERR_CUDA. Faults during execution surface on the caller's next synchronisation.
+ *   - Kernels never wait without bound: an internal wait that exceeds ~2 s records
+ *     MOE_ERR_TIMEOUT in the workspace status word (see moe_read_device_status) and the kernel
+ *     returns; the outputs of that call are then undefined.
+ *   - The caller owns x, router weights, outputs and the workspace. The library owns a pack
+ *     from moe_pack_nvfp4 until moe_pack_destroy.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* a null/misaligned pointer, a bad size, k > E, ...             */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. W4A4 with unequal x scales)  */
+  MOE_ERR_OOM = 3,          /* device allocation failed (moe_pack_nvfp4 only)               */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed                          */
+  MOE_ERR_TIMEOUT = 5,      /* a device-side wait gave up (reported via the status word)     */
+  MOE_ERR_WORKSPACE = 6     /* the workspace is smaller than moe_workspace_size reported     */
+} moe_status;
+
+typedef enum {
+  MOE_W4A16 = 0,  /* BF16 activations on NVFP4 weights ("--a16-activations" route)          */
+  MOE_W4A4 = 1    /* activations quantised to NVFP4 with the per-matrix input scale         */
+} moe_mode;
+
+/* Opaque, device-resident, library-owned set of one layer's routed experts. */
+typedef struct moe_expert_pack moe_expert_pack;
+
+/* One NVFP4 matrix in checkpoint layout (model card, "What is bit-exact and what is
+ * quantized"): rows x cols weights, cols being the reduction dimension.
+ *   codes  [rows][cols/2] bytes; element (r, c) is the low nibble of byte (r, c/2) when c is
+ *          even and the high nibble when c is odd; bit 3 of a nibble is the sign (E2M1).
+ *   scales [rows][cols/16] E4M3 bytes; scale (r, b) applies to columns 16b..16b+15.
+ *   decoded weight = E2M1(code) * E4M3(scale) * multiplier.
+ *   input_scale: the FP32 activation scale of the matrix (W4A4); ignored in W4A16.
+ * codes/scales may be host or device pointers; they are only read during moe_pack_nvfp4. */
+typedef struct {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  float multiplier;
+  float input_scale;
+} moe_nvfp4_matrix;
+
+/* Build a pack from num_experts experts, each given as gate [inter x hidden], up
+ * [inter x hidden] and down [hidden x inter] matrices (arrays of num_experts descriptors).
+ * The codes are kept bit for bit; the scales are re-laid out for the kernels (bit-preserving:
+ * moe_pack_get_matrix returns the input bytes). Requirements: hidden % 128 == 0,
+ * inter % 64 == 0, hidden <= 8192, inter <= 2048, 1 <= num_experts <= 1024, every multiplier
+ * and input_scale finite and > 0. Allocates device memory (MOE_ERR_OOM on failure) and
+ * synchronises `stream` before returning. On success *out owns that memory. */
+moe_status moe_pack_nvfp4(const moe_nvfp4_matrix* gate, const moe_nvfp4_matrix* up,
+                          const moe_nvfp4_matrix* down, int num_experts, int hidden, int inter,
+                          void* stream, moe_expert_pack** out);
+
+/* Free a pack (null is accepted). The pack must not be in use by queued work. */
+moe_status moe_pack_destroy(moe_expert_pack* pack);
+
+/* Sizes of a pack, and its device bytes. Any output pointer may be null. */
+moe_status moe_pack_info(const moe_expert_pack* pack, int* num_experts, int* hidden,
+                         int* inter, size_t* device_bytes);
+
+/* Copy one matrix of one expert back in checkpoint layout (which: 0 gate, 1 up, 2 down) into
+ * host buffers codes [rows][cols/2] and scales [rows][cols/16], plus its multiplier and input
+ * scale. Synchronous. For tests of the bit-preserving repack. */
+moe_status moe_pack_get_matrix(const moe_expert_pack* pack, int expert, int which,
+                               uint8_t* codes, uint8_t* scales, float* multiplier,
+                               float* input_scale);
+
+/* Workspace bytes moe_forward needs for (pack, T, k, mode). The workspace must be zero-filled
+ * before its first use; every call leaves its counters at zero again, so a workspace can be
+ * reused by later calls (with any T, k, mode whose size fits) without re-zeroing. After a call
+ * that reported an error through the status word, zero it again. */
+moe_status moe_workspace_size(const moe_expert_pack* pack, int T, int k, moe_mode mode,
+                              size_t* bytes);
+
+/* Workspace bytes moe_route_topk needs (same zero-fill rule). */
+moe_status moe_route_workspace_size(int T, int H, int E, int k, size_t* bytes);
+
+/* Router, top-k, softmax weights, histogram and permutation (the first steps of the MoE
+ * step; model card: BF16 router, 512 experts, top-10).
+ *   x        device [T][H] BF16;  router_w device [E][H] BF16.
+ *   idx      device [T][k] int32: the selected experts of each token, by descending logit.
+ *   w        device [T][k] float: softmax of the selected logits (sums to 1 per token).
+ *   counts   device [E] int32: slots routed to each expert.
+ *   offsets  device [E+1] int32: exclusive prefix sum of counts.
+ *   perm     device [T*k] int32: token ids grouped by expert (ascending expert, then token).
+ * Logits are accumulated in FP32 from exact BF16 products. Requirements: 1 <= T <= 65536,
+ * H % 128 == 0, H <= 8192, 1 <= k <= min(E, 32), E <= 1024. */
+moe_status moe_route_topk(const uint16_t* x, const uint16_t* router_w, int T, int H, int E,
+                          int k, int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, void* ws, size_t ws_bytes, void* stream);
+
+/* The whole MoE feed-forward step: out [T][H] BF16 (device) from x [T][H] BF16 and router_w
+ * [E][H] BF16 (device), using the experts of `pack` in `mode`. T <= 8 runs the narrow decode
+ * kernels; larger T runs the grouped (prefill) kernels. W4A4 requires every gate and up
+ * matrix of the pack to share one input scale (else MOE_ERR_UNSUPPORTED). out must not alias
+ * x. ws/ws_bytes: see moe_workspace_size. */
+moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_expert_pack* pack,
+                       int T, int k, moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/* Byte offsets inside a moe_forward workspace of intermediate results, for tests:
+ * the per-call routing tables and the quantised activations and h of the last call. */
+typedef struct {
+  size_t idx;        /* int32 [T][k]      */
+  size_t w;          /* float [T][k]      */
+  size_t counts;     /* int32 [E]         */
+  size_t offsets;    /* int32 [E+1]       */
+  size_t perm;       /* int32 [T*k]       */
+  size_t slot_of;    /* int32 [T][k]: position of (t, idx[t][j]) in perm */
+  size_t x_codes;    /* uint8 [T][H/2]   (W4A4: Q(x) codes, checkpoint nibble order) */
+  size_t x_scales;   /* uint8 [T][H/16]  (W4A4: Q(x) E4M3 scales)                    */
+  size_t h_bf16;     /* uint16 [T*k][I]  (W4A16: h rounded to BF16, rows = perm slots) */
+  size_t h_codes;    /* uint8 [T*k][I/2] (W4A4: Q(h) codes)                          */
+  size_t h_scales;   /* uint8 [T*k][I/16] (W4A4: Q(h) scales)                        */
+  size_t y;          /* uint16 [T*k][H]  BF16 expert outputs Y, rows = perm slots     */
+} moe_ws_offsets;
+
+moe_status moe_workspace_offsets(const moe_expert_pack* pack, int T, int k, moe_mode mode,
+                                 moe_ws_offsets* offsets);
+
+/* NVFP4 quantiser Q (test hook, also usable to build checkpoints): rows x cols BF16 values
+ * (device, cols % 16 == 0) -> codes [rows][cols/2] and E4M3 scales [rows][cols/16] (device),
+ * with per-matrix FP32 scale S = input_scale (> 0, finite). Steps, per 16-element block:
+ * inv6S = fl32(1/fl32(6 S)); sf = E4M3_RNE_satfinite(fl32(amax * inv6S)); sf == 0 -> codes +0;
+ * otherwise r = fl32(1/fl32(sf * S)) and q = E2M1_RNE_satfinite(fl32(v * r)) (ties to even,
+ * sign kept, so negative values rounding to zero encode as -0). */
+moe_status moe_quantize_act_nvfp4(const uint16_t* x, int rows, int cols, float input_scale,
+                                  uint8_t* codes, uint8_t* scales, void* stream);
+
+/* Read and clear the device status word of a workspace (synchronises `stream`). *status is
+ * MOE_OK or the first error a kernel recorded (MOE_ERR_TIMEOUT). */
+moe_status moe_read_device_status(void* ws, void* stream, moe_status* status);
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status status);
+
+/* Number of CUDA kernels the last moe_forward call on this host thread launched. */
+int moe_last_launch_count(void);
+
+/* Profiling hook (measurement only; not needed for computing): for the NEXT moe_forward call
+ * on this host thread, record cudaEvent_t events[2i] before and events[2i+1] after stage i on
+ * the call's stream, stage 0 = routing and activation preparation, 1 = gate/up + SiLU*up,
+ * 2 = down, 3 = combine (count <= 8 uses the first count/2 stages). While profiling, the
+ * stages are not overlapped by programmatic dependent launch. count = 0 cancels. */
+moe_status moe_profile_next_forward(void* const* events, int count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

@@ -1,0 +1,450 @@
+// moe_api.cu — the C ABI (include/moe_nvfp4.h): argument validation, the expert pack, the
+// workspace layout and the launch sequence of the NVFP4 routed-expert MoE step on sm_103a.
+#include "../../include/moe_nvfp4.h"
+#include "moe_internal.cuh"
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+namespace moe {
+size_t route_narrow_smem_bytes(int T, int H, int E, int k);
+}
+
+struct moe_expert_pack {
+  int E, H, I, device;
+  unsigned char* buf;
+  size_t bytes;
+  moe::PackView view;
+  float x_scale;
+  float x_inv6S;
+  int x_scale_uniform;
+  std::vector<float> mult_h;      // [E][3]
+  std::vector<float> in_scale_h;  // [E][3]
+};
+
+namespace {
+
+thread_local int g_last_launches = 0;
+// One-shot profiling events for the next moe_forward on this thread: events[2i] / events[2i+1]
+// are recorded on the call's stream before / after its i-th kernel launch.
+thread_local cudaEvent_t g_prof_events[32];
+thread_local int g_prof_count = 0;
+
+cudaError_t prof_mark(cudaStream_t s, int i) {
+  if (i < g_prof_count && g_prof_events[i]) return cudaEventRecord(g_prof_events[i], s);
+  return cudaSuccess;
+}
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool finite_pos(float v) { return std::isfinite(v) && v > 0.0f; }
+
+// fl32(1 / fl32(6 * S)), evaluated with IEEE single-precision operations.
+float inv6S_of(float S) {
+  volatile float six_s = 6.0f * S;
+  volatile float r = 1.0f / six_s;
+  return r;
+}
+
+int num_sms_of_current_device() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+struct WsLayout {
+  size_t ctl, logits, idx, w, slot_of, counts, offsets, perm, grp_expert, grp_slot, grp_n,
+      chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, total;
+  int G;
+};
+
+// mode: 0 W4A16, 1 W4A4, -1 routing only (no expert buffers).
+WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
+  WsLayout L;
+  const long long S = (long long)T * k;
+  L.G = (int)((S + moe::kGroup - 1) / moe::kGroup + (S < E ? S : E));
+  const int nchunk = (T + 31) / 32;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+  L.ctl = take(moe::kCtlWords * 4);
+  L.logits = take((size_t)T * E * 4);
+  L.idx = take((size_t)S * 4);
+  L.w = take((size_t)S * 4);
+  L.slot_of = take((size_t)S * 4);
+  L.counts = take((size_t)E * 4);
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.perm = take((size_t)S * 4);
+  L.grp_expert = take((size_t)L.G * 4);
+  L.grp_slot = take((size_t)L.G * 4);
+  L.grp_n = take((size_t)L.G * 4);
+  L.chunk_base = take(T > moe::kNarrowT ? (size_t)nchunk * E * 4 : 0);
+  L.xh = take(mode >= 0 ? (size_t)T * H * 2 : 0);
+  L.xfac = take(mode >= 0 ? (size_t)T * 4 : 0);
+  L.xq = take(mode == 1 ? (size_t)T * H / 2 : 0);
+  L.xsf = take(mode == 1 ? (size_t)T * H / 16 : 0);
+  L.h16 = take(mode == 0 ? (size_t)S * I * 2 : 0);
+  L.hq = take(mode == 1 ? (size_t)S * I / 2 : 0);
+  L.hsf = take(mode == 1 ? (size_t)S * I / 16 : 0);
+  L.y = take(mode >= 0 ? (size_t)S * H * 2 : 0);
+  L.total = o;
+  return L;
+}
+
+moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int I) {
+  unsigned char* b = static_cast<unsigned char*>(ws);
+  moe::WsView v;
+  v.ctl = reinterpret_cast<uint32_t*>(b + L.ctl);
+  v.logits = reinterpret_cast<float*>(b + L.logits);
+  v.idx = reinterpret_cast<int32_t*>(b + L.idx);
+  v.w = reinterpret_cast<float*>(b + L.w);
+  v.slot_of = reinterpret_cast<int32_t*>(b + L.slot_of);
+  v.counts = reinterpret_cast<int32_t*>(b + L.counts);
+  v.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+  v.perm = reinterpret_cast<int32_t*>(b + L.perm);
+  v.grp_expert = reinterpret_cast<int32_t*>(b + L.grp_expert);
+  v.grp_slot = reinterpret_cast<int32_t*>(b + L.grp_slot);
+  v.grp_n = reinterpret_cast<int32_t*>(b + L.grp_n);
+  v.chunk_base = reinterpret_cast<int32_t*>(b + L.chunk_base);
+  v.xh = reinterpret_cast<__half*>(b + L.xh);
+  v.xfac = reinterpret_cast<float*>(b + L.xfac);
+  v.xq = b + L.xq;
+  v.xsf = b + L.xsf;
+  v.h16 = reinterpret_cast<uint16_t*>(b + L.h16);
+  v.hq = b + L.hq;
+  v.hsf = b + L.hsf;
+  v.y = reinterpret_cast<uint16_t*>(b + L.y);
+  v.T = T; v.H = H; v.E = E; v.k = k; v.I = I; v.G = L.G;
+  return v;
+}
+
+moe_status from_cuda(cudaError_t e) {
+  return e == cudaSuccess ? MOE_OK : (e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA);
+}
+
+bool route_shape_ok(int T, int H, int E, int k) {
+  return T >= 1 && T <= 65536 && H >= 128 && H % 128 == 0 && H <= 8192 && E >= 1 && E <= 1024 &&
+         k >= 1 && k <= E && k <= 32;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_OOM: return "MOE_ERR_OOM";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+int moe_last_launch_count(void) { return g_last_launches; }
+
+moe_status moe_profile_next_forward(void* const* events, int count) {
+  if (count < 0 || count > 32 || (count > 0 && !events)) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) g_prof_events[i] = static_cast<cudaEvent_t>(events[i]);
+  g_prof_count = count;
+  return MOE_OK;
+}
+
+moe_status moe_pack_nvfp4(const moe_nvfp4_matrix* gate, const moe_nvfp4_matrix* up,
+                          const moe_nvfp4_matrix* down, int num_experts, int hidden, int inter,
+                          void* stream, moe_expert_pack** out) {
+  if (!gate || !up || !down || !out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  const int E = num_experts, H = hidden, I = inter;
+  if (E < 1 || E > 1024 || H < 128 || H % 128 || H > 8192 || I < 64 || I % 64 || I > 2048)
+    return MOE_ERR_INVALID_ARG;
+  for (int e = 0; e < E; ++e) {
+    const moe_nvfp4_matrix* m[3] = {&gate[e], &up[e], &down[e]};
+    for (auto* p : m)
+      if (!p->codes || !p->scales || !finite_pos(p->multiplier) || !finite_pos(p->input_scale))
+        return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t mat_codes = (size_t)I * H / 2;   // codes of one gate/up/down matrix
+  const size_t mat_scales = (size_t)I * H / 16;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+  const size_t off_gc = take(mat_codes * E), off_uc = take(mat_codes * E),
+               off_dc = take(mat_codes * E), off_gus = take(2 * mat_scales * E),
+               off_ds = take(mat_scales * E), off_mult = take((size_t)E * 12),
+               off_dsc = take((size_t)E * 4), off_dinv = take((size_t)E * 4);
+  moe_expert_pack* pk = new (std::nothrow) moe_expert_pack();
+  if (!pk) return MOE_ERR_OOM;
+  pk->E = E; pk->H = H; pk->I = I;
+  cudaGetDevice(&pk->device);
+  pk->bytes = o;
+  if (cudaMalloc(&pk->buf, o) != cudaSuccess) {
+    cudaGetLastError();
+    delete pk;
+    return MOE_ERR_OOM;
+  }
+  unsigned char* raw = nullptr;
+  if (cudaMalloc(&raw, 3 * mat_scales * E) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(pk->buf);
+    delete pk;
+    return MOE_ERR_OOM;
+  }
+  cudaError_t err = cudaSuccess;
+  for (int e = 0; e < E && err == cudaSuccess; ++e) {
+    err = cudaMemcpyAsync(pk->buf + off_gc + e * mat_codes, gate[e].codes, mat_codes,
+                          cudaMemcpyDefault, s);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync(pk->buf + off_uc + e * mat_codes, up[e].codes, mat_codes,
+                            cudaMemcpyDefault, s);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync(pk->buf + off_dc + e * mat_codes, down[e].codes, mat_codes,
+                            cudaMemcpyDefault, s);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync(raw + e * mat_scales, gate[e].scales, mat_scales, cudaMemcpyDefault, s);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync(raw + (E + e) * mat_scales, up[e].scales, mat_scales,
+                            cudaMemcpyDefault, s);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync(raw + (2 * E + e) * mat_scales, down[e].scales, mat_scales,
+                            cudaMemcpyDefault, s);
+  }
+  pk->mult_h.resize((size_t)E * 3);
+  pk->in_scale_h.resize((size_t)E * 3);
+  std::vector<float> dsc(E), dinv(E);
+  pk->x_scale = gate[0].input_scale;
+  pk->x_scale_uniform = 1;
+  for (int e = 0; e < E; ++e) {
+    pk->mult_h[e * 3 + 0] = gate[e].multiplier;
+    pk->mult_h[e * 3 + 1] = up[e].multiplier;
+    pk->mult_h[e * 3 + 2] = down[e].multiplier;
+    pk->in_scale_h[e * 3 + 0] = gate[e].input_scale;
+    pk->in_scale_h[e * 3 + 1] = up[e].input_scale;
+    pk->in_scale_h[e * 3 + 2] = down[e].input_scale;
+    if (gate[e].input_scale != pk->x_scale || up[e].input_scale != pk->x_scale)
+      pk->x_scale_uniform = 0;
+    dsc[e] = down[e].input_scale;
+    dinv[e] = inv6S_of(down[e].input_scale);
+  }
+  pk->x_inv6S = inv6S_of(pk->x_scale);
+  if (err == cudaSuccess)
+    err = moe::launch_pack_scales(s, raw, raw + E * mat_scales, raw + 2 * E * mat_scales, E, H, I,
+                                  pk->buf + off_gus, pk->buf + off_ds);
+  if (err == cudaSuccess)
+    err = cudaMemcpyAsync(pk->buf + off_mult, pk->mult_h.data(), (size_t)E * 12,
+                          cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess)
+    err = cudaMemcpyAsync(pk->buf + off_dsc, dsc.data(), (size_t)E * 4, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess)
+    err = cudaMemcpyAsync(pk->buf + off_dinv, dinv.data(), (size_t)E * 4, cudaMemcpyHostToDevice, s);
+  cudaError_t se = cudaStreamSynchronize(s);
+  if (err == cudaSuccess) err = se;
+  cudaFree(raw);
+  if (err != cudaSuccess) {
+    cudaFree(pk->buf);
+    delete pk;
+    return from_cuda(err);
+  }
+  moe::PackView& v = pk->view;
+  v.gate_codes = pk->buf + off_gc;
+  v.up_codes = pk->buf + off_uc;
+  v.down_codes = pk->buf + off_dc;
+  v.gu_scales = pk->buf + off_gus;
+  v.down_scales = pk->buf + off_ds;
+  v.mult = reinterpret_cast<const float*>(pk->buf + off_mult);
+  v.down_in_scale = reinterpret_cast<const float*>(pk->buf + off_dsc);
+  v.down_inv6S = reinterpret_cast<const float*>(pk->buf + off_dinv);
+  v.E = E; v.H = H; v.I = I;
+  *out = pk;
+  return MOE_OK;
+}
+
+moe_status moe_pack_destroy(moe_expert_pack* pack) {
+  if (!pack) return MOE_OK;
+  cudaError_t e = cudaFree(pack->buf);
+  delete pack;
+  return from_cuda(e);
+}
+
+moe_status moe_pack_info(const moe_expert_pack* pack, int* num_experts, int* hidden, int* inter,
+                         size_t* device_bytes) {
+  if (!pack) return MOE_ERR_INVALID_ARG;
+  if (num_experts) *num_experts = pack->E;
+  if (hidden) *hidden = pack->H;
+  if (inter) *inter = pack->I;
+  if (device_bytes) *device_bytes = pack->bytes;
+  return MOE_OK;
+}
+
+moe_status moe_pack_get_matrix(const moe_expert_pack* pack, int expert, int which, uint8_t* codes,
+                               uint8_t* scales, float* multiplier, float* input_scale) {
+  if (!pack || expert < 0 || expert >= pack->E || which < 0 || which > 2 || !codes || !scales)
+    return MOE_ERR_INVALID_ARG;
+  const size_t mat_codes = (size_t)pack->I * pack->H / 2;
+  const size_t mat_scales = (size_t)pack->I * pack->H / 16;
+  const uint8_t* src = which == 0 ? pack->view.gate_codes
+                       : which == 1 ? pack->view.up_codes : pack->view.down_codes;
+  cudaError_t e = cudaMemcpy(codes, src + expert * mat_codes, mat_codes, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return from_cuda(e);
+  unsigned char* tmp = nullptr;
+  if (cudaMalloc(&tmp, mat_scales) != cudaSuccess) { cudaGetLastError(); return MOE_ERR_OOM; }
+  e = moe::launch_unpack_scales(0, pack->view.gu_scales, pack->view.down_scales, pack->E, pack->H,
+                                pack->I, expert, which, tmp);
+  if (e == cudaSuccess) e = cudaMemcpy(scales, tmp, mat_scales, cudaMemcpyDeviceToHost);
+  cudaFree(tmp);
+  if (multiplier) *multiplier = pack->mult_h[expert * 3 + which];
+  if (input_scale) *input_scale = pack->in_scale_h[expert * 3 + which];
+  return from_cuda(e);
+}
+
+moe_status moe_workspace_size(const moe_expert_pack* pack, int T, int k, moe_mode mode,
+                              size_t* bytes) {
+  if (!pack || !bytes || (mode != MOE_W4A16 && mode != MOE_W4A4) ||
+      !route_shape_ok(T, pack->H, pack->E, k))
+    return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(T, pack->H, pack->E, k, pack->I, (int)mode).total;
+  return MOE_OK;
+}
+
+moe_status moe_route_workspace_size(int T, int H, int E, int k, size_t* bytes) {
+  if (!bytes || !route_shape_ok(T, H, E, k)) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(T, H, E, k, 0, -1).total;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_offsets(const moe_expert_pack* pack, int T, int k, moe_mode mode,
+                                 moe_ws_offsets* off) {
+  if (!pack || !off || (mode != MOE_W4A16 && mode != MOE_W4A4) ||
+      !route_shape_ok(T, pack->H, pack->E, k))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, pack->H, pack->E, k, pack->I, (int)mode);
+  off->idx = L.idx; off->w = L.w; off->counts = L.counts; off->offsets = L.offsets;
+  off->perm = L.perm; off->slot_of = L.slot_of; off->x_codes = L.xq; off->x_scales = L.xsf;
+  off->h_bf16 = L.h16; off->h_codes = L.hq; off->h_scales = L.hsf; off->y = L.y;
+  return MOE_OK;
+}
+
+moe_status moe_route_topk(const uint16_t* x, const uint16_t* router_w, int T, int H, int E, int k,
+                          int32_t* idx, float* w, int32_t* counts, int32_t* offsets, int32_t* perm,
+                          void* ws, size_t ws_bytes, void* stream) {
+  g_last_launches = 0;
+  if (!x || !router_w || !idx || !w || !counts || !offsets || !perm || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (!route_shape_ok(T, H, E, k)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(T, H, E, k, 0, -1);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  moe::WsView v = ws_view(ws, L, T, H, E, k, 0);
+  moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
+  cudaError_t e;
+  if (T <= moe::kNarrowT) {
+    e = moe::launch_route_narrow(lc, x, router_w, v, -1, 1.0f, 1.0f, idx, w, counts, offsets, perm);
+    g_last_launches = 1;
+  } else {
+    int n = 0;
+    e = moe::launch_route_wide(lc, x, router_w, v, idx, w, counts, offsets, perm, &n);
+    g_last_launches = n;
+  }
+  return from_cuda(e);
+}
+
+moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_expert_pack* pack,
+                       int T, int k, moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
+                       void* stream) {
+  g_last_launches = 0;
+  if (!x || !router_w || !pack || !out || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(out) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_W4A16 && mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
+  const int H = pack->H, E = pack->E, I = pack->I;
+  if (!route_shape_ok(T, H, E, k)) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<const void*>(out) == reinterpret_cast<const void*>(x))
+    return MOE_ERR_INVALID_ARG;
+  if (mode == MOE_W4A4 && !pack->x_scale_uniform) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(T, H, E, k, I, (int)mode);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  moe::WsView v = ws_view(ws, L, T, H, E, k, I);
+  moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
+  const int m = (int)mode;
+  const bool narrow = T <= moe::kNarrowT;
+  cudaError_t e;
+  int n = 0;
+  // stage i of the profile covers: 0 routing (+ activation prep), 1 gate/up, 2 down, 3 combine
+  if (g_prof_count) lc.pdl = false;
+  e = prof_mark(lc.stream, 0);
+  if (narrow) {
+    if (e == cudaSuccess)
+      e = moe::launch_route_narrow(lc, x, router_w, v, m, pack->x_scale, pack->x_inv6S, v.idx,
+                                   v.w, v.counts, v.offsets, v.perm);
+    n += 1;
+  } else {
+    if (e == cudaSuccess)
+      e = moe::launch_route_wide(lc, x, router_w, v, v.idx, v.w, v.counts, v.offsets, v.perm, &n);
+    if (e == cudaSuccess) {
+      e = moe::launch_xprep_wide(lc, x, v, m, pack->x_scale, pack->x_inv6S);
+      n += 1;
+    }
+  }
+  if (e == cudaSuccess) e = prof_mark(lc.stream, 1);
+  if (e == cudaSuccess) e = prof_mark(lc.stream, 2);
+  if (e == cudaSuccess) {
+    e = moe::launch_gateup(lc, pack->view, v, m, narrow);
+    n += 1;
+  }
+  if (e == cudaSuccess) e = prof_mark(lc.stream, 3);
+  if (e == cudaSuccess) e = prof_mark(lc.stream, 4);
+  if (e == cudaSuccess) {
+    const long long S = (long long)T * k;
+    const bool h_res = narrow && S * (2LL * I + 16) <= 96 * 1024;
+    e = moe::launch_down(lc, pack->view, v, m, h_res);
+    n += 1;
+  }
+  if (e == cudaSuccess) e = prof_mark(lc.stream, 5);
+  if (e == cudaSuccess) e = prof_mark(lc.stream, 6);
+  if (e == cudaSuccess) {
+    e = moe::launch_combine(lc, v, out);
+    n += 1;
+  }
+  if (e == cudaSuccess) e = prof_mark(lc.stream, 7);
+  g_prof_count = 0;
+  g_last_launches = n;
+  return from_cuda(e);
+}
+
+moe_status moe_quantize_act_nvfp4(const uint16_t* x, int rows, int cols, float input_scale,
+                                  uint8_t* codes, uint8_t* scales, void* stream) {
+  if (!x || !codes || !scales || rows < 1 || cols < 16 || cols % 16 || !finite_pos(input_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return MOE_ERR_INVALID_ARG;
+  moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
+  return from_cuda(moe::launch_quantize_rows(lc, x, rows, cols, input_scale, inv6S_of(input_scale),
+                                             codes, scales));
+}
+
+moe_status moe_read_device_status(void* ws, void* stream, moe_status* status) {
+  if (!ws || !status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  uint32_t* word = static_cast<uint32_t*>(ws) + moe::kCtlStatus;
+  cudaError_t e = cudaMemcpyAsync(&v, word, 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(word, 0, 4, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return from_cuda(e);
+  *status = static_cast<moe_status>(v);
+  return MOE_OK;
+}
+
+}  // extern "C"

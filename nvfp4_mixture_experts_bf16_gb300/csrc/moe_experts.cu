@@ -1,0 +1,668 @@
+// moe_experts.cu — NVFP4 expert kernels of the routed-expert MoE step (sm_103a):
+// gate/up with fused SiLU*up (and NVFP4 quantisation of h in W4A4), down, and the
+// deterministic fixed-order combine.
+//
+// The expert matrices are NVFP4 (model card "Qwen3.8-Flash-Next NVIDIA NVFP4 for Infernix
+// (bit-exact)", section "What is bit-exact and what is quantized": E2M1 codes, one E4M3 scale
+// per 16 weights, FP32 multiplier and activation input scale per matrix). The release notes
+// "Infernix windows-2026.10.11", section "Highlights", describe the sm_120a design these
+// kernels replace: narrow calls of up to 8 columns on one-column kernels that convert FP4 to
+// half2 in one instruction, and a down pass chained to gate/up with programmatic dependent
+// launch. Here:
+//   * One producer warp per CTA streams weight tiles HBM -> shared memory with TMA bulk copies
+//     (cp.async.bulk) into a ring of stages guarded by mbarriers; consumer warps never issue
+//     global loads for weights. Every wait is bounded.
+//   * Consumers decode E2M1 -> f16x2 and E4M3 -> f16x2 with the hardware conversions
+//     (code * scale is exact in f16) and multiply with m16n8k16 tensor-core MMAs, 8 tokens as N,
+//     FP32 accumulation. Decode (<= 8 tokens) would otherwise be ALU-bound on CUDA cores.
+//   * Tasks are (token group, row tile); groups hold <= 8 tokens of one expert, so the same
+//     kernels serve decode (one group per expert) and the grouped prefill fallback.
+#include "moe_internal.cuh"
+
+#include <cuda_bf16.h>
+
+namespace moe {
+namespace {
+
+constexpr int kGuConsumers = 8;
+constexpr int kGuThreads = (kGuConsumers + 1) * 32;
+constexpr int kDnConsumers = 4;
+constexpr int kDnThreads = (kDnConsumers + 1) * 32;
+constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block
+
+struct GuGeom {
+  int KC;          // reduction columns per stage
+  int nkc;         // stages per task (H / KC)
+  int row_stride;  // bytes per code row in shared memory (KC/2 + pad, == 32 mod 128)
+  int stage_bytes;
+  int stages;
+  int x_stride;    // bytes per activation row in shared memory (2H + 16)
+  int x_rows;      // rows of the activation region (T if resident else 8)
+  int tiles;       // I / 16
+};
+
+struct DnGeom {
+  int stage_bytes;  // 64 rows * I/2 codes + 4*I scales
+  int stages;
+  int h_stride;     // 2I + 16
+  int h_rows;       // slots if resident else 8
+  int tiles;        // H / 64
+};
+
+__host__ __device__ inline int pick_kc(int H) {
+  return (H % 1024 == 0) ? 1024 : (H % 512 == 0) ? 512 : (H % 256 == 0) ? 256
+                                                                         : (H % 128 == 0) ? 128 : 64;
+}
+
+GuGeom gu_geom(int H, int I, bool x_resident, int T) {
+  GuGeom g;
+  g.KC = pick_kc(H);
+  g.nkc = H / g.KC;
+  const int half = g.KC / 2;
+  g.row_stride = half + ((32 - (half % 128)) + 128) % 128;
+  g.stage_bytes = 32 * g.row_stride + 2 * g.KC;
+  g.x_stride = 2 * H + 16;
+  g.x_rows = x_resident ? T : kGroup;
+  g.tiles = I / 16;
+  const int fixed = g.x_rows * g.x_stride + kGuConsumers * 2 * 32 * 16 + 1024;
+  int st = (kMaxSmem - fixed) / g.stage_bytes;
+  g.stages = st > 6 ? 6 : st;
+  return g;
+}
+
+size_t gu_smem(const GuGeom& g) {
+  return (size_t)g.stages * g.stage_bytes + (size_t)g.x_rows * g.x_stride +
+         kGuConsumers * 2 * 32 * 16 + 2 * 8 * g.stages + 64;
+}
+
+DnGeom dn_geom(int H, int I, bool h_resident, int slots) {
+  DnGeom d;
+  d.stage_bytes = 64 * (I / 2) + 4 * I;
+  d.h_stride = 2 * I + 16;
+  d.h_rows = h_resident ? slots : kGroup;
+  d.tiles = H / 64;
+  const int fixed = d.h_rows * d.h_stride + d.h_rows * 4 + 1024;
+  int st = (kMaxSmem - fixed) / d.stage_bytes;
+  d.stages = st > 8 ? 8 : st;
+  return d;
+}
+
+size_t dn_smem(const DnGeom& d) {
+  return (size_t)d.stages * d.stage_bytes + (size_t)d.h_rows * d.h_stride + d.h_rows * 4 +
+         2 * 8 * d.stages + 64;
+}
+
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint2 lds64(const unsigned char* p) {
+  return *reinterpret_cast<const uint2*>(p);
+}
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ uint32_t lds16(const unsigned char* p) {
+  return *reinterpret_cast<const uint16_t*>(p);
+}
+
+// Balanced contiguous task range of this CTA.
+__device__ __forceinline__ void task_range(int ntasks, int& q0, int& q1) {
+  q0 = (int)(((long long)ntasks * blockIdx.x) / gridDim.x);
+  q1 = (int)(((long long)ntasks * (blockIdx.x + 1)) / gridDim.x);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return (g / (1.0f + expf(-g))) * u;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// ------------------------------------------------------------------ gate/up
+// grid: persistent; block: 8 consumer warps + 1 producer warp.
+// A task is (token group gi, 16-row tile `it` of the intermediate dimension): it computes
+// gate and up rows it*16..+15 for the group's tokens over the full hidden dimension.
+__global__ void __launch_bounds__(kGuThreads, 1)
+    k_gateup(PackView pk, WsView ws, GuGeom geo, int mode, int x_resident) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* stages = smem;
+  unsigned char* xs = stages + (size_t)geo.stages * geo.stage_bytes;
+  float* red = reinterpret_cast<float*>(xs + (size_t)geo.x_rows * geo.x_stride);
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + kGuConsumers * 2 * 32 * 4);
+  uint64_t* empty = full + geo.stages;
+  __shared__ volatile int abort_s;
+  __shared__ int cur_group_s;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = pk.H, I = pk.I;
+  if (tid == 0) {
+    for (int s = 0; s < geo.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kGuConsumers);
+    }
+    fence_mbar_init();
+    abort_s = 0;
+    cur_group_s = -1;
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int G = (int)ws.ctl[kCtlGroups];
+  const int ntasks = G * geo.tiles;
+  int q0, q1;
+  task_range(ntasks, q0, q1);
+
+  if (warp == kGuConsumers) {
+    // ---------------- producer
+    if (lane != 0) return;
+    int chunk = 0;
+    for (int q = q0; q < q1 && !abort_s; ++q) {
+      const int gi = q / geo.tiles, it = q % geo.tiles;
+      const int e = ws.grp_expert[gi];
+      const size_t row0 = (size_t)e * I + (size_t)it * 16;
+      const uint8_t* gsrc = pk.gate_codes + row0 * (H / 2);
+      const uint8_t* usrc = pk.up_codes + row0 * (H / 2);
+      const uint8_t* gsc = pk.gu_scales + (((size_t)0 * pk.E + e) * geo.tiles + it) * (size_t)H;
+      const uint8_t* usc = pk.gu_scales + (((size_t)1 * pk.E + e) * geo.tiles + it) * (size_t)H;
+      for (int kc = 0; kc < geo.nkc; ++kc, ++chunk) {
+        const int s = chunk % geo.stages, n = chunk / geo.stages;
+        if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+          break;
+        }
+        unsigned char* st = stages + (size_t)s * geo.stage_bytes;
+        const uint32_t half = geo.KC / 2;
+        mbar_arrive_expect_tx(&full[s], 32 * half + 2 * geo.KC);
+        for (int r = 0; r < 16; ++r) {
+          bulk_g2s(st + r * geo.row_stride, gsrc + (size_t)r * (H / 2) + (size_t)kc * half, half,
+                   &full[s]);
+          bulk_g2s(st + (16 + r) * geo.row_stride, usrc + (size_t)r * (H / 2) + (size_t)kc * half,
+                   half, &full[s]);
+        }
+        bulk_g2s(st + 32 * geo.row_stride, gsc + (size_t)kc * geo.KC, geo.KC, &full[s]);
+        bulk_g2s(st + 32 * geo.row_stride + geo.KC, usc + (size_t)kc * geo.KC, geo.KC, &full[s]);
+      }
+    }
+    // Do not leave while copies into this CTA's shared memory may still be in flight.
+    const int used = chunk < geo.stages ? chunk : geo.stages;
+    for (int i = 0; i < used; ++i) {
+      const int c = chunk - 1 - i;
+      (void)mbar_wait(&full[c % geo.stages], (c / geo.stages) & 1);
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int g = lane >> 2, c = lane & 3;
+  const int ncons = kGuConsumers * 32;
+  if (x_resident) {
+    // all T tokens' activations, row t at t * x_stride
+    const int T = ws.T;
+    const int words = H / 8;  // uint4 per row
+    for (int i = tid; i < T * words; i += ncons) {
+      const int t = i / words, w = i % words;
+      *reinterpret_cast<uint4*>(xs + (size_t)t * geo.x_stride + w * 16) =
+          reinterpret_cast<const uint4*>(ws.xh + (size_t)t * H)[w];
+    }
+    consumer_sync(ncons);
+  }
+  int chunk = 0;
+  const int kb_per_chunk = geo.KC / 64;
+  for (int q = q0; q < q1; ++q) {
+    const int gi = q / geo.tiles, it = q % geo.tiles;
+    const int e = ws.grp_expert[gi];
+    const int slot0 = ws.grp_slot[gi];
+    const int n = ws.grp_n[gi];
+    if (!x_resident && gi != cur_group_s) {
+      consumer_sync(ncons);
+      const int words = H / 8;
+      for (int i = tid; i < kGroup * words; i += ncons) {
+        const int r = i / words, w = i % words;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < n) v = reinterpret_cast<const uint4*>(ws.xh + (size_t)ws.perm[slot0 + r] * H)[w];
+        *reinterpret_cast<uint4*>(xs + (size_t)r * geo.x_stride + w * 16) = v;
+      }
+      consumer_sync(ncons);
+      if (tid == 0) cur_group_s = gi;
+    }
+    // activation row of this lane's token column g
+    const bool gvalid = g < n;
+    const int xrow = x_resident ? (gvalid ? ws.perm[slot0 + g] : 0) : g;
+    const unsigned char* xr = xs + (size_t)xrow * geo.x_stride + c * 32;
+
+    float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kc = 0; kc < geo.nkc; ++kc, ++chunk) {
+      const int s = chunk % geo.stages, nn = chunk / geo.stages;
+      if (!abort_s && !mbar_wait(&full[s], nn & 1)) {
+        record_status(ws.ctl, kStTimeout);
+        abort_s = 1;
+      }
+      const unsigned char* st = stages + (size_t)s * geo.stage_bytes;
+      for (int jb = warp; jb < kb_per_chunk; jb += kGuConsumers) {
+        const int off = jb * 32 + c * 8;
+        const uint2 gr = lds64(st + g * geo.row_stride + off);
+        const uint2 gr8 = lds64(st + (g + 8) * geo.row_stride + off);
+        const uint2 ur = lds64(st + (16 + g) * geo.row_stride + off);
+        const uint2 ur8 = lds64(st + (24 + g) * geo.row_stride + off);
+        const unsigned char* scb = st + 32 * geo.row_stride + jb * 64 + c * 16 + g * 2;
+        const uint32_t scg = lds16(scb);
+        const uint32_t scu = lds16(scb + geo.KC);
+        uint4 xb0 = make_uint4(0, 0, 0, 0), xb1 = xb0;
+        if (gvalid || !x_resident) {
+          const unsigned char* xp = xr + (size_t)(kc * kb_per_chunk + jb) * 128;
+          xb0 = lds128(xp);
+          xb1 = lds128(xp + 16);
+        }
+        kblock_mma(accg, gr, gr8, scg, xb0, xb1);
+        kblock_mma(accu, ur, ur8, scu, xb0, xb1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // fixed-order reduction over the consumer warps
+    float* myred = red + (size_t)(warp * 2) * 32 * 4;
+    *reinterpret_cast<float4*>(myred + lane * 4) = make_float4(accg[0], accg[1], accg[2], accg[3]);
+    *reinterpret_cast<float4*>(myred + 128 + lane * 4) =
+        make_float4(accu[0], accu[1], accu[2], accu[3]);
+    consumer_sync(ncons);
+    if (warp == 0) {
+      float G4[4] = {0.f, 0.f, 0.f, 0.f}, U4[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int w = 0; w < kGuConsumers; ++w) {
+        const float4 a = *reinterpret_cast<const float4*>(red + (size_t)(w * 2) * 128 + lane * 4);
+        const float4 b =
+            *reinterpret_cast<const float4*>(red + (size_t)(w * 2) * 128 + 128 + lane * 4);
+        G4[0] += a.x; G4[1] += a.y; G4[2] += a.z; G4[3] += a.w;
+        U4[0] += b.x; U4[1] += b.y; U4[2] += b.z; U4[3] += b.w;
+      }
+      const float mg = pk.mult[e * 3 + 0], mu = pk.mult[e * 3 + 1];
+      float hv[4];  // (row g, col 2c), (row g, col 2c+1), (row g+8, col 2c), (row g+8, col 2c+1)
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2) {
+        const int col = 2 * c + (q2 & 1);
+        const float xf = col < n ? ws.xfac[ws.perm[slot0 + col]] : 0.0f;
+        const float gv = G4[q2] * mg * xf;
+        const float uv = U4[q2] * mu * xf;
+        hv[q2] = col < n ? silu_mul(gv, uv) : 0.0f;
+      }
+      const int i0 = it * 16 + g;
+      if (mode == 0) {
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          const int col = 2 * c + (q2 & 1);
+          if (col < n) {
+            const int row = i0 + ((q2 >> 1) << 3);
+            ws.h16[(size_t)(slot0 + col) * I + row] = f32_to_bf16_rn(hv[q2]);
+          }
+        }
+      } else {
+        const float Sd = pk.down_in_scale[e], i6 = pk.down_inv6S[e];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {  // token column 2c + cc
+          const float v_lo = hv[cc], v_hi = hv[2 + cc];  // elements g and g+8 of the block
+          float a = fmaxf(fabsf(v_lo), fabsf(v_hi));
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+          const uint32_t sf = e4m3_encode_rn(__fmul_rn(a, i6));
+          uint32_t lo = 0, hi = 0;
+          if (sf != 0u) {
+            const float r = __frcp_rn(__fmul_rn(e4m3_value_nonneg(sf), Sd));
+            const uint32_t q_lo = e2m1_encode_rn(__fmul_rn(v_lo, r));
+            const uint32_t q_hi = e2m1_encode_rn(__fmul_rn(v_hi, r));
+            lo = q_lo << (4 * g);  // elements 0..7 -> word 0
+            hi = q_hi << (4 * g);  // elements 8..15 -> word 1
+          }
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            lo |= __shfl_xor_sync(0xFFFFFFFFu, lo, off);
+            hi |= __shfl_xor_sync(0xFFFFFFFFu, hi, off);
+          }
+          const int col = 2 * c + cc;
+          if (g == 0 && col < n) {
+            const size_t slot = (size_t)(slot0 + col);
+            *reinterpret_cast<uint2*>(ws.hq + slot * (I / 2) + it * 8) = make_uint2(lo, hi);
+            ws.hsf[slot * (I / 16) + it] = static_cast<uint8_t>(sf);
+          }
+        }
+      }
+    }
+    consumer_sync(ncons);
+  }
+}
+
+// ------------------------------------------------------------------ down
+// A task is (token group gi, 64-row tile ht of the hidden dimension); consumer warp w owns
+// rows ht*64 + 16w .. +15. Y (BF16) goes to the slot-major buffer for the combine.
+__global__ void __launch_bounds__(kDnThreads, 1)
+    k_down(PackView pk, WsView ws, DnGeom geo, int mode, int h_resident) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* stages = smem;
+  unsigned char* hs = stages + (size_t)geo.stages * geo.stage_bytes;
+  float* hfac = reinterpret_cast<float*>(hs + (size_t)geo.h_rows * geo.h_stride);
+  uint64_t* full = reinterpret_cast<uint64_t*>(hfac + geo.h_rows + (geo.h_rows & 1));
+  uint64_t* empty = full + geo.stages;
+  __shared__ volatile int abort_s;
+  __shared__ int cur_group_s;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = pk.H, I = pk.I;
+  if (tid == 0) {
+    for (int s = 0; s < geo.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kDnConsumers);
+    }
+    fence_mbar_init();
+    abort_s = 0;
+    cur_group_s = -1;
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int G = (int)ws.ctl[kCtlGroups];
+  const int ntasks = G * geo.tiles;
+  int q0, q1;
+  task_range(ntasks, q0, q1);
+  const uint32_t code_bytes = 64u * (I / 2);
+
+  if (warp == kDnConsumers) {
+    if (lane != 0) return;
+    int chunk = 0;
+    for (int q = q0; q < q1 && !abort_s; ++q, ++chunk) {
+      const int gi = q / geo.tiles, ht = q % geo.tiles;
+      const int e = ws.grp_expert[gi];
+      const int s = chunk % geo.stages, n = chunk / geo.stages;
+      if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
+        record_status(ws.ctl, kStTimeout);
+        abort_s = 1;
+        break;
+      }
+      unsigned char* st = stages + (size_t)s * geo.stage_bytes;
+      mbar_arrive_expect_tx(&full[s], code_bytes + 4u * I);
+      bulk_g2s(st, pk.down_codes + ((size_t)e * H + (size_t)ht * 64) * (I / 2), code_bytes,
+               &full[s]);
+      bulk_g2s(st + code_bytes, pk.down_scales + ((size_t)e * geo.tiles + ht) * (4 * (size_t)I),
+               4u * I, &full[s]);
+    }
+    const int used = chunk < geo.stages ? chunk : geo.stages;
+    for (int i = 0; i < used; ++i) {
+      const int c2 = chunk - 1 - i;
+      (void)mbar_wait(&full[c2 % geo.stages], (c2 / geo.stages) & 1);
+    }
+    return;
+  }
+
+  const int g = lane >> 2, c = lane & 3;
+  const int ncons = kDnConsumers * 32;
+  // Stage h as the f16 operand: rows = perm slots (resident) or the group's slots.
+  auto stage_h = [&](int row, int slot, int e) {
+    // one warp per row
+    unsigned char* dst = hs + (size_t)row * geo.h_stride;
+    if (mode == 0) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(ws.h16 + (size_t)slot * I);
+      float m = 0.0f;
+      for (int i = lane; i < I / 2; i += 32) {
+        const uint32_t v = src[i];
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(v << 16)), fabsf(__uint_as_float(v & 0xFFFF0000u))));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+      int sh = 0;
+      if (m > 0.0f) {
+        int ex;
+        frexpf(m, &ex);
+        sh = ex - 15;
+        sh = sh < -110 ? -110 : (sh > 110 ? 110 : sh);
+      }
+      const float f = __int_as_float((127 - sh) << 23);
+      for (int i = lane; i < I / 2; i += 32) {
+        const uint32_t v = src[i];
+        const __half2 h2 = __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), f),
+                                             __fmul_rn(__uint_as_float(v & 0xFFFF0000u), f));
+        *reinterpret_cast<__half2*>(dst + i * 4) = h2;
+      }
+      if (lane == 0) hfac[row] = __int_as_float((127 + sh) << 23);
+    } else {
+      const uint8_t* cq = ws.hq + (size_t)slot * (I / 2);
+      const uint8_t* sq = ws.hsf + (size_t)slot * (I / 16);
+      for (int i = lane; i < I / 2; i += 32) {
+        const uint32_t byte = cq[i];
+        const float sv = e4m3_value_nonneg(sq[i / 8]);
+        const __half2 h2 = __floats2half2_rn(e2m1_value(byte & 0xF) * sv, e2m1_value(byte >> 4) * sv);
+        *reinterpret_cast<__half2*>(dst + i * 4) = h2;
+      }
+      if (lane == 0) hfac[row] = pk.down_in_scale[e];
+    }
+  };
+  if (h_resident) {
+    const int S = ws.T * ws.k;
+    for (int sl = warp; sl < S; sl += kDnConsumers) {
+      // expert of the slot: the group that contains it
+      int e = 0;
+      for (int gi = 0; gi < G; ++gi)
+        if (sl >= ws.grp_slot[gi] && sl < ws.grp_slot[gi] + ws.grp_n[gi]) e = ws.grp_expert[gi];
+      stage_h(sl, sl, e);
+    }
+    consumer_sync(ncons);
+  }
+  int chunk = 0;
+  for (int q = q0; q < q1; ++q, ++chunk) {
+    const int gi = q / geo.tiles, ht = q % geo.tiles;
+    const int e = ws.grp_expert[gi];
+    const int slot0 = ws.grp_slot[gi];
+    const int n = ws.grp_n[gi];
+    if (!h_resident && gi != cur_group_s) {
+      consumer_sync(ncons);
+      for (int r = warp; r < kGroup; r += kDnConsumers) {
+        if (r < n) stage_h(r, slot0 + r, e);
+      }
+      consumer_sync(ncons);
+      if (tid == 0) cur_group_s = gi;
+    }
+    const int s = chunk % geo.stages, nn = chunk / geo.stages;
+    if (!abort_s && !mbar_wait(&full[s], nn & 1)) {
+      record_status(ws.ctl, kStTimeout);
+      abort_s = 1;
+    }
+    const unsigned char* st = stages + (size_t)s * geo.stage_bytes;
+    const bool gvalid = g < n;
+    const int hrow = h_resident ? slot0 + (gvalid ? g : 0) : g;
+    const unsigned char* hr = hs + (size_t)hrow * geo.h_stride + c * 32;
+    const int nkb = I / 64;
+    const unsigned char* rg = st + (size_t)(warp * 16 + g) * (I / 2) + c * 8;
+    const unsigned char* rg8 = rg + 8 * (I / 2);
+    const unsigned char* scb = st + code_bytes + (size_t)warp * nkb * 64 + c * 16 + g * 2;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < nkb; ++j) {
+      const uint2 a0 = lds64(rg + j * 32);
+      const uint2 a1 = lds64(rg8 + j * 32);
+      const uint32_t sc = lds16(scb + j * 64);
+      uint4 xb0 = make_uint4(0, 0, 0, 0), xb1 = xb0;
+      if (gvalid) {
+        xb0 = lds128(hr + j * 128);
+        xb1 = lds128(hr + j * 128 + 16);
+      }
+      kblock_mma(acc, a0, a1, sc, xb0, xb1);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    const float md = pk.mult[e * 3 + 2];
+#pragma unroll
+    for (int q2 = 0; q2 < 4; ++q2) {
+      const int col = 2 * c + (q2 & 1);
+      if (col < n) {
+        const int hsrow = h_resident ? slot0 + col : col;
+        const float y = acc[q2] * md * hfac[hsrow];
+        const int row = ht * 64 + warp * 16 + g + ((q2 >> 1) << 3);
+        ws.y[(size_t)(slot0 + col) * H + row] = f32_to_bf16_rn(y);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ combine
+// out[t][r] = BF16( sum_{j=0..k-1} w[t][j] * Y[slot_of[t][j]][r] ), FP32, j in rank order.
+__global__ void __launch_bounds__(256) k_combine(WsView ws, uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int H = ws.H, k = ws.k;
+  const long long n8 = (long long)ws.T * (H / 8);
+  for (long long it = (long long)blockIdx.x * 256 + threadIdx.x; it < n8;
+       it += (long long)gridDim.x * 256) {
+    const int t = (int)(it / (H / 8)), r8 = (int)(it % (H / 8));
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const float wj = ws.w[(size_t)t * k + j];
+      const int slot = ws.slot_of[(size_t)t * k + j];
+      const uint4 v = reinterpret_cast<const uint4*>(ws.y + (size_t)slot * H)[r8];
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += wj * __uint_as_float(wd[q] << 16);
+        acc[2 * q + 1] += wj * __uint_as_float(wd[q] & 0xFFFF0000u);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = (uint32_t)f32_to_bf16_rn(acc[2 * q]) | ((uint32_t)f32_to_bf16_rn(acc[2 * q + 1]) << 16);
+    reinterpret_cast<uint4*>(out + (size_t)t * H)[r8] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ------------------------------------------------------------------ scale re-layout
+// checkpoint [E][rows][cols/16] -> fragment order (see PackView).
+__global__ void k_pack_scales(const uint8_t* __restrict__ rg, const uint8_t* __restrict__ ru,
+                              const uint8_t* __restrict__ rd, int E, int H, int I,
+                              uint8_t* __restrict__ gu, uint8_t* __restrict__ dn, int inverse,
+                              int only_expert, int only_which, uint8_t* __restrict__ raw_out) {
+  // gate/up part: index over [mat][E][I/16][H/64][4][8][2]
+  const long long n_gu = 2ll * E * I * (H / 16);
+  const long long n_dn = (long long)E * H * (I / 16);
+  for (long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x; o < n_gu + n_dn;
+       o += (long long)gridDim.x * blockDim.x) {
+    if (o < n_gu) {
+      long long r = o;
+      const int h = (int)(r & 1); r >>= 1;
+      const int g = (int)(r & 7); r >>= 3;
+      const int c = (int)(r & 3); r >>= 2;
+      const int j = (int)(r % (H / 64)); r /= (H / 64);
+      const int tile = (int)(r % (I / 16)); r /= (I / 16);
+      const int e = (int)(r % E); r /= E;
+      const int mat = (int)r;
+      const int row = tile * 16 + g + 8 * h;
+      const int blk = 4 * j + c;
+      const size_t src = ((size_t)e * I + row) * (H / 16) + blk;
+      if (!inverse) {
+        gu[o] = (mat == 0 ? rg : ru)[src];
+      } else if (e == only_expert && mat == only_which) {
+        raw_out[(size_t)row * (H / 16) + blk] = gu[o];
+      }
+    } else {
+      long long r = o - n_gu;
+      const int h = (int)(r & 1); r >>= 1;
+      const int g = (int)(r & 7); r >>= 3;
+      const int c = (int)(r & 3); r >>= 2;
+      const int j = (int)(r % (I / 64)); r /= (I / 64);
+      const int mt = (int)(r & 3); r >>= 2;
+      const int ht = (int)(r % (H / 64)); r /= (H / 64);
+      const int e = (int)r;
+      const int row = ht * 64 + mt * 16 + g + 8 * h;
+      const int blk = 4 * j + c;
+      const size_t src = ((size_t)e * H + row) * (I / 16) + blk;
+      if (!inverse) {
+        dn[o - n_gu] = rd[src];
+      } else if (e == only_expert && only_which == 2) {
+        raw_out[(size_t)row * (I / 16) + blk] = dn[o - n_gu];
+      }
+    }
+  }
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
+                   Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace
+
+size_t gateup_smem_bytes(int H, bool x_resident, int T) {
+  return gu_smem(gu_geom(H, 64, x_resident, T));
+}
+
+size_t down_smem_bytes(int I, bool h_resident, int slots) {
+  return dn_smem(dn_geom(64, I, h_resident, slots));
+}
+
+cudaError_t launch_gateup(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
+                          bool x_resident) {
+  const GuGeom geo = gu_geom(pk.H, pk.I, x_resident, ws.T);
+  if (geo.stages < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = gu_smem(geo);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int max_tasks = ws.G * geo.tiles;
+  int grid = lc.num_sms < max_tasks ? lc.num_sms : max_tasks;
+  if (grid < 1) grid = 1;
+  return launch(lc, k_gateup, dim3(grid), dim3(kGuThreads), smem, pk, ws, geo, mode,
+                x_resident ? 1 : 0);
+}
+
+cudaError_t launch_down(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
+                        bool h_resident) {
+  const DnGeom geo = dn_geom(pk.H, pk.I, h_resident, ws.T * ws.k);
+  if (geo.stages < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = dn_smem(geo);
+  cudaError_t e =
+      cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int max_tasks = ws.G * geo.tiles;
+  int grid = lc.num_sms < max_tasks ? lc.num_sms : max_tasks;
+  if (grid < 1) grid = 1;
+  return launch(lc, k_down, dim3(grid), dim3(kDnThreads), smem, pk, ws, geo, mode,
+                h_resident ? 1 : 0);
+}
+
+cudaError_t launch_combine(const LaunchCfg& lc, const WsView& ws, uint16_t* out) {
+  const long long n8 = (long long)ws.T * (ws.H / 8);
+  long long grid = (n8 + 255) / 256;
+  const long long cap = (long long)lc.num_sms * 8;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  return launch(lc, k_combine, dim3((unsigned)grid), dim3(256), 0, ws, out);
+}
+
+cudaError_t launch_pack_scales(cudaStream_t s, const uint8_t* raw_gate, const uint8_t* raw_up,
+                               const uint8_t* raw_down, int E, int H, int I, uint8_t* gu_scales,
+                               uint8_t* down_scales) {
+  k_pack_scales<<<1024, 256, 0, s>>>(raw_gate, raw_up, raw_down, E, H, I, gu_scales, down_scales,
+                                     0, -1, -1, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_scales(cudaStream_t s, const uint8_t* gu_scales,
+                                 const uint8_t* down_scales, int E, int H, int I, int expert,
+                                 int which, uint8_t* raw_out) {
+  k_pack_scales<<<1024, 256, 0, s>>>(nullptr, nullptr, nullptr, E, H, I,
+                                     const_cast<uint8_t*>(gu_scales),
+                                     const_cast<uint8_t*>(down_scales), 1, expert, which, raw_out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

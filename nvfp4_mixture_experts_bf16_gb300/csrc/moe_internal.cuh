@@ -1,0 +1,317 @@
+// moe_internal.cuh — device helpers and views shared by the sm_103a kernels of the NVFP4
+// routed-expert MoE library. Internal to the library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Device status codes (values equal the public moe_status codes).
+constexpr uint32_t kStOk = 0;
+constexpr uint32_t kStTimeout = 5;
+
+// A wait that takes longer than this gives up, records kStTimeout and returns.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Narrow (decode) path: tokens per call at most this many; also the token-group width of the
+// grouped path (the N of one m16n8k16 MMA).
+constexpr int kNarrowT = 8;
+constexpr int kGroup = 8;
+
+// ------------------------------------------------------------------ workspace view
+// Control words at the start of the workspace (zero-filled before first use).
+enum : int {
+  kCtlRouteTicket = 0,  // last-block-done ticket of the narrow router (self-resetting)
+  kCtlStatus = 1,       // first device error (sticky until read by the host)
+  kCtlGroups = 2,       // number of token groups of the current call
+  kCtlUnique = 3,       // number of distinct experts of the current call
+  kCtlWords = 64
+};
+
+struct WsView {
+  uint32_t* ctl;
+  float* logits;       // [T][E]
+  int32_t* idx;        // [T][k]
+  float* w;            // [T][k]
+  int32_t* slot_of;    // [T][k]
+  int32_t* counts;     // [E]
+  int32_t* offsets;    // [E+1]
+  int32_t* perm;       // [T*k]
+  int32_t* grp_expert; // [G]
+  int32_t* grp_slot;   // [G] first perm slot of the group
+  int32_t* grp_n;      // [G] tokens in the group (1..8)
+  int32_t* chunk_base; // [nchunk][E] (grouped routing)
+  __half* xh;          // [T][H] activations as the f16 B operand of gate/up
+  float* xfac;         // [T] factor restoring xh's scale (2^shift in W4A16, S_x in W4A4)
+  uint8_t* xq;         // [T][H/2]  W4A4 activation codes
+  uint8_t* xsf;        // [T][H/16] W4A4 activation scales
+  uint16_t* h16;       // [T*k][I] W4A16 h (BF16)
+  uint8_t* hq;         // [T*k][I/2] W4A4 h codes
+  uint8_t* hsf;        // [T*k][I/16] W4A4 h scales
+  uint16_t* y;         // [T*k][H] BF16 expert outputs
+  int T, H, E, k, I, G;
+};
+
+// ------------------------------------------------------------------ pack view
+// Codes keep the checkpoint layout ([rows][cols/2] per matrix, experts contiguous).
+// Scales are stored in the "fragment" order the narrow/grouped kernels read:
+//   gate/up: [mat(2)][E][I/16 row tiles][H/64 k-blocks][c(4)][g(8)][2]
+//            byte (c, g, h) of k-block j is the scale of row 16*tile + g + 8h, block 4j + c.
+//   down:    [E][H/64 row tiles][4 m16 tiles][I/64 k-blocks][c(4)][g(8)][2]
+struct PackView {
+  const uint8_t* gate_codes;   // [E][I][H/2]
+  const uint8_t* up_codes;     // [E][I][H/2]
+  const uint8_t* down_codes;   // [E][H][I/2]
+  const uint8_t* gu_scales;    // see above
+  const uint8_t* down_scales;  // see above
+  const float* mult;           // [E][3]
+  const float* down_in_scale;  // [E]
+  const float* down_inv6S;     // [E] fl32(1 / fl32(6 * S_down))
+  int E, H, I;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase: false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// One TMA bulk copy global -> shared (16-byte aligned, bytes % 16 == 0), completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void record_status(uint32_t* ctl, uint32_t code) {
+  atomicCAS(&ctl[kCtlStatus], 0u, code);
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's results / let the next
+// kernel start its prologue.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ format conversions
+// Four bytes of E2M1 codes -> four f16x2 (byte b -> out[b]; low nibble -> low half). Exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t src, uint32_t (&out)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}\n"
+      : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+      : "r"(src));
+}
+
+// Two E4M3 bytes (low byte -> low half) -> f16x2. Exact (every E4M3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t out;
+  uint16_t in = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(in));
+  return out;
+}
+
+// E4M3 scale byte broadcast to both halves of an f16x2.
+__device__ __forceinline__ uint32_t e4m3_bcast_f16x2(uint32_t byte) {
+  return e4m3x2_to_f16x2(byte * 0x0101u);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Exact decoded values.
+__device__ __forceinline__ float e2m1_value(uint32_t code) {
+  const uint32_t e = (code >> 1) & 3u, m = code & 1u;
+  // exponent field 0: 0 or 0.5; otherwise (1 + m/2) * 2^(e-1)
+  const float v = (e == 0u) ? 0.5f * static_cast<float>(m) : __uint_as_float(((126u + e) << 23) | (m << 22));
+  return (code & 8u) ? -v : v;
+}
+
+__device__ __forceinline__ float e4m3_value_nonneg(uint32_t byte) {
+  uint32_t e = (byte >> 3) & 0xF, mnt = byte & 7;
+  if (e == 0) return static_cast<float>(mnt) * 0.001953125f;  // m/8 * 2^-6
+  return __uint_as_float(((e + 120u) << 23) | (mnt << 20));   // (1+m/8) * 2^(e-7)
+}
+
+// Round-to-nearest-even encoders of the quantiser, in exact integer/compare steps.
+// E2M1: nearest of {0,.5,1,1.5,2,3,4,6}, ties to the even code, above 6 -> 6; sign kept.
+__device__ __forceinline__ uint32_t e2m1_encode_rn(float v) {
+  const float a = fabsf(v);
+  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+               (a >= 3.5f) + (a > 5.0f);
+  return c | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// E4M3 of a non-negative finite float: nearest, ties to even, above 448 -> 448 (0x7E).
+__device__ __forceinline__ uint32_t e4m3_encode_rn(float t) {
+  if (!(t > 0.0f)) return 0u;
+  if (t >= 448.0f) return 0x7Eu;
+  if (t < 0.015625f) {  // subnormal range: multiples of 2^-9
+    return static_cast<uint32_t>(__float2int_rn(t * 512.0f));  // 0..8 (8 == 2^-6, normal)
+  }
+  const uint32_t bits = __float_as_uint(t);
+  const int e = static_cast<int>((bits >> 23) & 0xFF) - 127;   // t in [2^e, 2^(e+1))
+  const float frac = __uint_as_float((bits & 0x7FFFFFu) | 0x3F800000u);  // in [1, 2)
+  uint32_t m = static_cast<uint32_t>(__float2int_rn((frac - 1.0f) * 8.0f));
+  uint32_t ef = static_cast<uint32_t>(e + 7);
+  if (m == 8) { m = 0; ef += 1; }
+  uint32_t r = (ef << 3) | m;
+  return r > 0x7Eu ? 0x7Eu : r;
+}
+
+// Quantise 16 FP32 values with per-matrix scale S (inv6S = fl32(1/fl32(6 S))).
+// Writes 8 code bytes (even element in the low nibble) and returns the scale byte.
+// Every step is one IEEE single-precision operation, as in the public quantiser definition.
+__device__ __forceinline__ uint32_t quantize16(const float (&v)[16], float S, float inv6S,
+                                               uint32_t (&codes)[2]) {
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(v[i]));
+  const uint32_t sf = e4m3_encode_rn(__fmul_rn(a, inv6S));
+  codes[0] = codes[1] = 0u;
+  if (sf == 0u) return 0u;
+  const float r = __frcp_rn(__fmul_rn(e4m3_value_nonneg(sf), S));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t q = e2m1_encode_rn(__fmul_rn(v[i], r));
+    codes[i >> 3] |= q << (4 * (i & 7));
+  }
+  return sf;
+}
+
+// ------------------------------------------------------------------ MMA
+// D (16x8 f32) += A (16x16 f16, row) * B (16x8 f16, col).
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The product of one 64-wide k-block for one m16 row tile and one 8-token group:
+//   rowg / rowg8: the thread's 8 code bytes of rows g and g+8 (codes k = 64j+16c .. +15),
+//   sc:           the two scale bytes (rows g, g+8) of block 4j + c,
+//   xb0, xb1:     the thread's 16 B operand values x[g][64j+16c .. +15] as 2 x uint4.
+// The k order inside an MMA is permuted consistently for A and B (thread c of MMA m holds
+// k = 64j + 16c + 4m + {0,1,2,3}), so both operands come from contiguous bytes.
+__device__ __forceinline__ void kblock_mma(float (&acc)[4], uint2 rowg, uint2 rowg8, uint32_t sc,
+                                           const uint4& xb0, const uint4& xb1) {
+  const uint32_t s0 = e4m3_bcast_f16x2(sc & 0xFFu);
+  const uint32_t s1 = e4m3_bcast_f16x2((sc >> 8) & 0xFFu);
+  uint32_t ga[4], gb[4], ha[4], hb[4];
+  e2m1x8_to_f16x2x4(rowg.x, ga);   // row g, k 0..7
+  e2m1x8_to_f16x2x4(rowg.y, gb);   // row g, k 8..15
+  e2m1x8_to_f16x2x4(rowg8.x, ha);  // row g+8
+  e2m1x8_to_f16x2x4(rowg8.y, hb);
+  const uint32_t xs[8] = {xb0.x, xb0.y, xb0.z, xb0.w, xb1.x, xb1.y, xb1.z, xb1.w};
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t* g4 = (m < 2) ? ga : gb;
+    const uint32_t* h4 = (m < 2) ? ha : hb;
+    const int o = (m & 1) * 2;
+    uint32_t a[4];
+    a[0] = hmul2_u32(g4[o], s0);
+    a[1] = hmul2_u32(h4[o], s1);
+    a[2] = hmul2_u32(g4[o + 1], s0);
+    a[3] = hmul2_u32(h4[o + 1], s1);
+    mma_16816(acc, a, xs[2 * m], xs[2 * m + 1]);
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+struct LaunchCfg {
+  cudaStream_t stream;
+  int num_sms;
+  bool pdl;
+};
+
+cudaError_t launch_route_narrow(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
+                                const WsView& ws, int mode, float xS, float x_inv6S,
+                                int32_t* out_idx, float* out_w, int32_t* out_counts,
+                                int32_t* out_offsets, int32_t* out_perm);
+cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
+                              const WsView& ws, int32_t* out_idx, float* out_w,
+                              int32_t* out_counts, int32_t* out_offsets, int32_t* out_perm,
+                              int* launches);
+cudaError_t launch_xprep_wide(const LaunchCfg& lc, const uint16_t* x, const WsView& ws, int mode,
+                              float xS, float x_inv6S);
+cudaError_t launch_quantize_rows(const LaunchCfg& lc, const uint16_t* x, int rows, int cols,
+                                 float S, float inv6S, uint8_t* codes, uint8_t* scales);
+cudaError_t launch_gateup(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
+                          bool x_resident);
+cudaError_t launch_down(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
+                        bool h_resident);
+cudaError_t launch_combine(const LaunchCfg& lc, const WsView& ws, uint16_t* out);
+cudaError_t launch_pack_scales(cudaStream_t s, const uint8_t* raw_gate, const uint8_t* raw_up,
+                               const uint8_t* raw_down, int E, int H, int I, uint8_t* gu_scales,
+                               uint8_t* down_scales);
+cudaError_t launch_unpack_scales(cudaStream_t s, const uint8_t* gu_scales,
+                                 const uint8_t* down_scales, int E, int H, int I, int expert,
+                                 int which, uint8_t* raw_out);
+
+// Dynamic shared memory the expert kernels need (host side, for validation).
+size_t gateup_smem_bytes(int H, bool x_resident, int T);
+size_t down_smem_bytes(int I, bool h_resident, int slots);
+
+}  // namespace moe

@@ -1,0 +1,690 @@
+// moe_route.cu — router, top-k + softmax, histogram + permutation, and activation preparation
+// for the NVFP4 routed-expert MoE step (sm_103a).
+//
+// Model card "Qwen3.8-Flash-Next NVIDIA NVFP4 for Infernix (bit-exact)": the router is stored
+// BF16 and each token keeps the top-10 of 512 routed experts. Weights are the softmax over the
+// selected logits; ties go to the lower expert index.
+//
+// Narrow calls (T <= 8, the decode / speculative-verification case of the Infernix release
+// notes "windows-2026.10.11", "Highlights") run in ONE kernel: every CTA computes 4 router rows
+// (a GEMV: the 4 MiB router is read once, coalesced) and prepares its share of the activations;
+// the last CTA to finish (a ticket, no spinning) selects the top-k, the softmax weights, the
+// histogram, the permutation and the token groups. Wide calls (prefill) run a tensor-core
+// router GEMM followed by small top-k / histogram / scan / scatter kernels.
+#include "moe_internal.cuh"
+
+#include <cuda_bf16.h>
+#include <float.h>
+
+namespace moe {
+namespace {
+
+struct RouteOut {
+  int32_t* idx;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Sum of the 8 exact BF16 products of two uint4 chunks, as a fixed pairwise tree.
+__device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
+  const float p0 = bf16_lo(a.x) * bf16_lo(b.x), p1 = bf16_hi(a.x) * bf16_hi(b.x);
+  const float p2 = bf16_lo(a.y) * bf16_lo(b.y), p3 = bf16_hi(a.y) * bf16_hi(b.y);
+  const float p4 = bf16_lo(a.z) * bf16_lo(b.z), p5 = bf16_hi(a.z) * bf16_hi(b.z);
+  const float p6 = bf16_lo(a.w) * bf16_lo(b.w), p7 = bf16_hi(a.w) * bf16_hi(b.w);
+  return ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7));
+}
+
+// Power-of-two shift that puts a token's amax in [2^14, 2^15) for the f16 operand.
+__device__ __forceinline__ int token_shift(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int e;
+  frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
+  int s = e - 15;
+  return s < -110 ? -110 : (s > 110 ? 110 : s);
+}
+
+__device__ __forceinline__ float pow2f(int s) { return __int_as_float((127 + s) << 23); }
+
+// Prepare one 16-element block of token t: the f16 B operand (and the W4A4 codes/scales).
+__device__ __forceinline__ void prep_block(const uint16_t* xrow, int b, int t, const WsView& ws,
+                                           int mode, float xS, float x_inv6S, int shift) {
+  const int H = ws.H;
+  const uint4* src = reinterpret_cast<const uint4*>(xrow + b * 16);
+  const uint4 u0 = src[0], u1 = src[1];
+  const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = bf16_lo(words[i]);
+    v[2 * i + 1] = bf16_hi(words[i]);
+  }
+  __half hv[16];
+  if (mode == 0) {
+    const float f = pow2f(-shift);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) hv[i] = __float2half_rn(__fmul_rn(v[i], f));
+  } else {
+    uint32_t codes[2];
+    const uint32_t sf = quantize16(v, xS, x_inv6S, codes);
+    *reinterpret_cast<uint2*>(ws.xq + (size_t)t * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
+    ws.xsf[(size_t)t * (H / 16) + b] = static_cast<uint8_t>(sf);
+    const float sfv = e4m3_value_nonneg(sf);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      hv[i] = __float2half_rn(e2m1_value((codes[i >> 3] >> (4 * (i & 7))) & 0xF) * sfv);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(ws.xh + (size_t)t * H + b * 16);
+  dst[0] = *reinterpret_cast<uint4*>(&hv[0]);
+  dst[1] = *reinterpret_cast<uint4*>(&hv[8]);
+}
+
+// Warp-level top-k of one token's logits held in shared memory (entries are overwritten with
+// NaN once taken). Selection order: larger logit first, equal logits -> lower index first.
+__device__ void warp_topk(float* vals, int E, int k, int lane, int32_t* sel_idx,
+                          float* sel_val) {
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int e = lane; e < E; e += 32) {
+      const float v = vals[e];
+      if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) {
+      sel_idx[j] = bi;
+      sel_val[j] = bv;
+      if (bi < E) vals[bi] = __int_as_float(0x7FC00000);
+    }
+    __syncwarp();
+  }
+}
+
+// Softmax over the k selected logits (descending), FP32, fixed order.
+__device__ void topk_softmax(const float* sel_val, int k, float* w_out) {
+  const float m = sel_val[0];
+  float z = 0.0f;
+  for (int j = 0; j < k; ++j) z += expf(sel_val[j] - m);
+  for (int j = 0; j < k; ++j) w_out[j] = expf(sel_val[j] - m) / z;
+}
+
+// Block-wide exclusive scan of n <= 4 * blockDim ints in shared memory (in place); returns
+// the total. blockDim.x must be 256.
+__device__ int block_exclusive_scan(int32_t* a, int n, int32_t* scratch /*[8]*/) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int v[4], s = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = tid * 4 + i;
+    v[i] = idx < n ? a[idx] : 0;
+    s += v[i];
+  }
+  int incl = s;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  int wbase = 0, total = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) wbase += scratch[w];
+    total += scratch[w];
+  }
+  int run = wbase + incl - s;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = tid * 4 + i;
+    if (idx < n) a[idx] = run;
+    run += v[i];
+  }
+  __syncthreads();
+  return total;
+}
+
+// ------------------------------------------------------------------ narrow router
+constexpr int kRouteRows = 4;  // router rows per CTA (2 warps per row, one per half of H)
+
+__global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict__ x,
+                                                      const uint16_t* __restrict__ wr, WsView ws,
+                                                      int mode, float xS, float x_inv6S,
+                                                      RouteOut out) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ float part[kRouteRows][2][kNarrowT];
+  __shared__ int shift_s[kNarrowT];
+  __shared__ int last_s;
+  __shared__ int32_t scan_scratch[8];
+
+  const int T = ws.T, H = ws.H, E = ws.E, k = ws.k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // Stage the activations (T x H BF16) in shared memory.
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    for (int i = tid; i < T * H / 8; i += 256) dst[i] = src[i];
+  }
+
+  // Issue this warp's router loads before waiting for the staged activations.
+  const int row = blockIdx.x * kRouteRows + (warp >> 1);
+  const int half = warp & 1;
+  const int nchunk = H / 16;  // uint4 chunks in half a row
+  constexpr int kMaxChunks = 16;  // H <= 8192
+  uint4 wv[kMaxChunks];
+  if (row < E) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)row * H) + half * nchunk;
+#pragma unroll
+    for (int i = 0; i < kMaxChunks; ++i)
+      if (lane + 32 * i < nchunk) wv[i] = __ldg(wrow + lane + 32 * i);
+  }
+  __syncthreads();
+
+  float acc[kNarrowT];
+#pragma unroll
+  for (int t = 0; t < kNarrowT; ++t) acc[t] = 0.0f;
+  if (row < E) {
+#pragma unroll
+    for (int i = 0; i < kMaxChunks; ++i) {
+      if (lane + 32 * i < nchunk) {
+#pragma unroll
+        for (int t = 0; t < kNarrowT; ++t) {
+          if (t < T) {
+            const uint4 xv =
+                reinterpret_cast<const uint4*>(xs + (size_t)t * H)[half * nchunk + lane + 32 * i];
+            acc[t] += dot8_bf16(wv[i], xv);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kNarrowT; ++t) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], off);
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < kNarrowT; ++t) part[warp >> 1][half][t] = acc[t];
+  }
+
+  // Per-token power-of-two shift of the f16 operand (W4A16): one warp per token.
+  if (mode == 0 && warp < T) {
+    float m = 0.0f;
+    const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs + (size_t)warp * H);
+    for (int i = lane; i < H / 2; i += 32) {
+      const uint32_t v = xr[i];
+      m = fmaxf(m, fmaxf(fabsf(bf16_lo(v)), fabsf(bf16_hi(v))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    if (lane == 0) shift_s[warp] = token_shift(m);
+  }
+  __syncthreads();
+
+  if (tid < kRouteRows * T) {
+    const int r = tid / T, t = tid % T;
+    const int rr = blockIdx.x * kRouteRows + r;
+    if (rr < E) ws.logits[(size_t)t * E + rr] = part[r][0][t] + part[r][1][t];
+  }
+
+  // This CTA's share of the activation preparation (skipped for routing-only calls).
+  if (mode >= 0) {
+    const int nblk = T * (H / 16);
+    for (int it = blockIdx.x * 256 + tid; it < nblk; it += gridDim.x * 256) {
+      const int t = it / (H / 16), b = it % (H / 16);
+      prep_block(xs + (size_t)t * H, b, t, ws, mode, xS, x_inv6S, mode == 0 ? shift_s[t] : 0);
+    }
+    if (blockIdx.x == 0 && tid < T) ws.xfac[tid] = mode == 0 ? pow2f(shift_s[tid]) : xS;
+  }
+
+  // Last CTA to arrive finishes the routing.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t ticket = atomicAdd(&ws.ctl[kCtlRouteTicket], 1u);
+    last_s = (ticket == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+
+  const int S = T * k;
+  float* lg = reinterpret_cast<float*>(smem);              // [T][E]
+  int32_t* sel_idx = reinterpret_cast<int32_t*>(lg + (size_t)T * E);   // [S]
+  float* sel_val = reinterpret_cast<float*>(sel_idx + S);             // [S]
+  float* sel_w = sel_val + S;                                         // [S]
+  int32_t* cnt = reinterpret_cast<int32_t*>(sel_w + S);               // [E+1]
+  int32_t* uq = cnt + (E + 1);                                        // [E+1]
+
+  for (int i = tid; i < T * E; i += 256) lg[i] = __ldcg(ws.logits + i);
+  for (int e = tid; e <= E; e += 256) cnt[e] = 0;
+  __syncthreads();
+  if (warp < T) {
+    warp_topk(lg + (size_t)warp * E, E, k, lane, sel_idx + warp * k, sel_val + warp * k);
+    if (lane == 0) topk_softmax(sel_val + warp * k, k, sel_w + warp * k);
+  }
+  __syncthreads();
+  if (tid < S) atomicAdd(&cnt[sel_idx[tid]], 1);
+  __syncthreads();
+  for (int e = tid; e < E; e += 256) {
+    uq[e] = cnt[e] > 0 ? 1 : 0;
+    out.counts[e] = cnt[e];
+    ws.counts[e] = cnt[e];
+  }
+  __syncthreads();
+  block_exclusive_scan(cnt, E, scan_scratch);   // cnt -> offsets
+  const int U = block_exclusive_scan(uq, E, scan_scratch);
+  for (int e = tid; e < E; e += 256) {
+    out.offsets[e] = cnt[e];
+    ws.offsets[e] = cnt[e];
+    const int c = ((e + 1 < E) ? cnt[e + 1] : S) - cnt[e];
+    if (c > 0) {
+      const int u = uq[e];
+      ws.grp_expert[u] = e;
+      ws.grp_slot[u] = cnt[e];
+      ws.grp_n[u] = c;
+    }
+  }
+  if (tid == 0) {
+    out.offsets[E] = S;
+    ws.offsets[E] = S;
+    ws.ctl[kCtlGroups] = U;
+    ws.ctl[kCtlUnique] = U;
+  }
+  if (tid < S) {
+    const int t = tid / k, e = sel_idx[tid];
+    int rank = 0;
+    for (int s2 = 0; s2 < t * k; ++s2) rank += (sel_idx[s2] == e) ? 1 : 0;
+    const int pos = cnt[e] + rank;
+    out.perm[pos] = t;
+    ws.perm[pos] = t;
+    ws.slot_of[tid] = pos;
+    out.idx[tid] = e;
+    out.w[tid] = sel_w[tid];
+    ws.idx[tid] = e;
+    ws.w[tid] = sel_w[tid];
+  }
+  if (tid == 0) ws.ctl[kCtlRouteTicket] = 0u;
+}
+
+// ------------------------------------------------------------------ wide router GEMM
+// logits[T][E] = x[T][H] . Wr[E][H]^T, BF16 mma.sync m16n8k16 with FP32 accumulation.
+// CTA tile 128 tokens x 128 experts, k-step 32, two cp.async stages.
+constexpr int kGM = 128, kGN = 128, kGK = 32, kGLd = 40;  // padded row (bf16 elements)
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool pred) {
+  const uint32_t d = smem_u32(dst);
+  const int n = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(256) k_router_gemm(const uint16_t* __restrict__ x,
+                                                     const uint16_t* __restrict__ wr, WsView ws) {
+  __shared__ __align__(16) uint16_t As[2][kGM][kGLd];
+  __shared__ __align__(16) uint16_t Bs[2][kGN][kGLd];
+  const int T = ws.T, H = ws.H, E = ws.E;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int m0 = blockIdx.y * kGM, n0 = blockIdx.x * kGN;
+  const int wm = (warp >> 1) * 32, wn = (warp & 1) * 64;  // warp tile 32 x 64
+
+  pdl_wait();
+  pdl_launch_dependents();
+
+  auto load_stage = [&](int st, int k0) {
+    // 128 rows x 32 bf16 = 512 chunks of 16 B per operand; 2 per thread per operand.
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int c = tid + 256 * i, r = c >> 2, q = c & 3;
+      const bool pa = (m0 + r) < T;
+      const bool pb = (n0 + r) < E;
+      cp_async16(&As[st][r][q * 8], x + (size_t)(pa ? m0 + r : 0) * H + k0 + q * 8, pa);
+      cp_async16(&Bs[st][r][q * 8], wr + (size_t)(pb ? n0 + r : 0) * H + k0 + q * 8, pb);
+    }
+    cp_async_commit();
+  };
+
+  float acc[2][8][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i][j][q] = 0.0f;
+
+  const int nk = H / kGK;
+  load_stage(0, 0);
+  for (int kt = 0; kt < nk; ++kt) {
+    cp_async_wait_all();
+    __syncthreads();
+    if (kt + 1 < nk) load_stage((kt + 1) & 1, (kt + 1) * kGK);
+    const int st = kt & 1;
+#pragma unroll
+    for (int kk = 0; kk < kGK; kk += 16) {
+      uint32_t a[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int r = wm + i * 16 + (lane & 15);
+        const int c = kk + (lane >> 4) * 8;
+        ldmatrix_x4(a[i], &As[st][r][c]);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; j += 2) {
+        uint32_t b[4];
+        // matrices: (n j, k lo), (n j, k hi), (n j+1, k lo), (n j+1, k hi)
+        const int r = wn + j * 8 + (lane & 7) + ((lane >> 4) << 3);
+        const int c = kk + ((lane >> 3) & 1) * 8;
+        ldmatrix_x4(b, &Bs[st][r][c]);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          mma_bf16_16816(acc[i][j], a[i], b[0], b[1]);
+          mma_bf16_16816(acc[i][j + 1], a[i], b[2], b[3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = m0 + wm + i * 16 + (lane >> 2);
+      const int c = n0 + wn + j * 8 + (lane & 3) * 2;
+      if (c + 1 < E + 1) {
+        if (r < T && c < E) ws.logits[(size_t)r * E + c] = acc[i][j][0];
+        if (r < T && c + 1 < E) ws.logits[(size_t)r * E + c + 1] = acc[i][j][1];
+        if (r + 8 < T && c < E) ws.logits[(size_t)(r + 8) * E + c] = acc[i][j][2];
+        if (r + 8 < T && c + 1 < E) ws.logits[(size_t)(r + 8) * E + c + 1] = acc[i][j][3];
+      }
+    }
+}
+
+// ------------------------------------------------------------------ wide top-k
+__global__ void __launch_bounds__(256) k_topk_wide(WsView ws, RouteOut out) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int E = ws.E, k = ws.k, T = ws.T;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  float* vals = reinterpret_cast<float*>(smem) + (size_t)warp * (E + 2 * 32 + 32);
+  int32_t* sidx = reinterpret_cast<int32_t*>(vals + E);
+  float* sval = reinterpret_cast<float*>(sidx + 32);
+  float* sw = sval + 32;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  for (int e = lane; e < E; e += 32) vals[e] = ws.logits[(size_t)t * E + e];
+  __syncwarp();
+  warp_topk(vals, E, k, lane, sidx, sval);
+  if (lane == 0) topk_softmax(sval, k, sw);
+  __syncwarp();
+  for (int j = lane; j < k; j += 32) {
+    out.idx[(size_t)t * k + j] = sidx[j];
+    out.w[(size_t)t * k + j] = sw[j];
+    ws.idx[(size_t)t * k + j] = sidx[j];
+    ws.w[(size_t)t * k + j] = sw[j];
+  }
+}
+
+// ------------------------------------------------------------------ wide histogram / scan
+constexpr int kChunkTok = 32;
+
+__global__ void __launch_bounds__(256) k_hist_wide(WsView ws) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  int32_t* cnt = reinterpret_cast<int32_t*>(smem);
+  const int E = ws.E, k = ws.k, T = ws.T;
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int e = threadIdx.x; e < E; e += 256) cnt[e] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kChunkTok;
+  const int n = min(kChunkTok, T - t0) * k;
+  for (int s = threadIdx.x; s < n; s += 256) atomicAdd(&cnt[ws.idx[(size_t)t0 * k + s]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += 256) ws.chunk_base[(size_t)blockIdx.x * E + e] = cnt[e];
+}
+
+// One CTA of 1024 threads: per-expert chunk prefix sums, offsets, and the token groups.
+__global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, RouteOut out, int nchunk) {
+  __shared__ int32_t tot[1024 + 1];
+  __shared__ int32_t wsum[32];
+  const int E = ws.E;
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  int run = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunk; ++c) {
+      int32_t* p = ws.chunk_base + (size_t)c * E + e;
+      const int v = *p;
+      *p = run;
+      run += v;
+    }
+  }
+  const int cnt_e = e < E ? run : 0;
+  const int ng_e = (cnt_e + kGroup - 1) / kGroup;
+  // two block-wide exclusive scans (counts, group counts)
+  int a = cnt_e, b = ng_e;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int oa = __shfl_up_sync(0xFFFFFFFFu, a, off);
+    const int ob = __shfl_up_sync(0xFFFFFFFFu, b, off);
+    if (lane >= off) { a += oa; b += ob; }
+  }
+  if (lane == 31) { wsum[warp] = a; tot[warp] = b; }
+  __syncthreads();
+  int ba = 0, bb = 0, ta = 0, tb = 0;
+  for (int w = 0; w < 32; ++w) {
+    if (w < warp) { ba += wsum[w]; bb += tot[w]; }
+    ta += wsum[w];
+    tb += tot[w];
+  }
+  const int off_e = ba + a - cnt_e;
+  const int gbase = bb + b - ng_e;
+  __syncthreads();
+  if (e < E) {
+    out.counts[e] = cnt_e;
+    out.offsets[e] = off_e;
+    ws.counts[e] = cnt_e;
+    ws.offsets[e] = off_e;
+    for (int q = 0; q < ng_e; ++q) {
+      ws.grp_expert[gbase + q] = e;
+      ws.grp_slot[gbase + q] = off_e + q * kGroup;
+      ws.grp_n[gbase + q] = min(kGroup, cnt_e - q * kGroup);
+    }
+  }
+  if (e == 0) {
+    out.offsets[E] = ta;
+    ws.offsets[E] = ta;
+    ws.ctl[kCtlGroups] = tb;
+  }
+}
+
+__global__ void __launch_bounds__(256) k_scatter_wide(WsView ws, RouteOut out) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int E = ws.E, k = ws.k, T = ws.T;
+  int32_t* sidx = reinterpret_cast<int32_t*>(smem);  // [kChunkTok * k]
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t0 = blockIdx.x * kChunkTok;
+  const int ntok = min(kChunkTok, T - t0);
+  const int n = ntok * k;
+  for (int s = threadIdx.x; s < n; s += 256) sidx[s] = ws.idx[(size_t)t0 * k + s];
+  __syncthreads();
+  for (int s = threadIdx.x; s < n; s += 256) {
+    const int tl = s / k, e = sidx[s];
+    int rank = 0;
+    for (int s2 = 0; s2 < tl * k; ++s2) rank += (sidx[s2] == e) ? 1 : 0;
+    const int pos = ws.offsets[e] + ws.chunk_base[(size_t)blockIdx.x * E + e] + rank;
+    out.perm[pos] = t0 + tl;
+    ws.perm[pos] = t0 + tl;
+    ws.slot_of[(size_t)t0 * k + s] = pos;
+  }
+}
+
+// ------------------------------------------------------------------ wide activation prep
+__global__ void __launch_bounds__(256) k_xprep_wide(const uint16_t* __restrict__ x, WsView ws,
+                                                    int mode, float xS, float x_inv6S) {
+  __shared__ float red[8];
+  const int H = ws.H;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  const uint16_t* xr = x + (size_t)t * H;
+  int shift = 0;
+  if (mode == 0) {
+    float m = 0.0f;
+    const uint32_t* xw = reinterpret_cast<const uint32_t*>(xr);
+    for (int i = tid; i < H / 2; i += 256) {
+      const uint32_t v = xw[i];
+      m = fmaxf(m, fmaxf(fabsf(bf16_lo(v)), fabsf(bf16_hi(v))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w]);
+    shift = token_shift(m);
+  }
+  for (int b = tid; b < H / 16; b += 256) prep_block(xr, b, t, ws, mode, xS, x_inv6S, shift);
+  if (tid == 0) ws.xfac[t] = mode == 0 ? pow2f(shift) : xS;
+}
+
+// ------------------------------------------------------------------ quantiser hook
+__global__ void __launch_bounds__(256) k_quantize_rows(const uint16_t* __restrict__ x, int rows,
+                                                       int cols, float S, float inv6S,
+                                                       uint8_t* __restrict__ codes,
+                                                       uint8_t* __restrict__ scales) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const long long nblk = (long long)rows * (cols / 16);
+  for (long long it = (long long)blockIdx.x * 256 + threadIdx.x; it < nblk;
+       it += (long long)gridDim.x * 256) {
+    const long long r = it / (cols / 16), b = it % (cols / 16);
+    const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + b * 16);
+    const uint4 u0 = src[0], u1 = src[1];
+    const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_lo(words[i]);
+      v[2 * i + 1] = bf16_hi(words[i]);
+    }
+    uint32_t c[2];
+    const uint32_t sf = quantize16(v, S, inv6S, c);
+    *reinterpret_cast<uint2*>(codes + r * (cols / 2) + b * 8) = make_uint2(c[0], c[1]);
+    scales[r * (cols / 16) + b] = static_cast<uint8_t>(sf);
+  }
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
+                   Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace
+
+size_t route_narrow_smem_bytes(int T, int H, int E, int k) {
+  const size_t xbytes = (size_t)T * H * 2;
+  const size_t fin = (size_t)T * E * 4 + (size_t)T * k * 12 + (size_t)(E + 1) * 8 + 64;
+  return xbytes > fin ? xbytes : fin;
+}
+
+cudaError_t launch_route_narrow(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
+                                const WsView& ws, int mode, float xS, float x_inv6S,
+                                int32_t* out_idx, float* out_w, int32_t* out_counts,
+                                int32_t* out_offsets, int32_t* out_perm) {
+  const size_t smem = route_narrow_smem_bytes(ws.T, ws.H, ws.E, ws.k);
+  cudaError_t e = cudaFuncSetAttribute(k_route_narrow, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  RouteOut out{out_idx, out_w, out_counts, out_offsets, out_perm};
+  const int grid = (ws.E + kRouteRows - 1) / kRouteRows;
+  return launch(lc, k_route_narrow, dim3(grid), dim3(256), smem, x, wr, ws, mode, xS, x_inv6S,
+                out);
+}
+
+cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
+                              const WsView& ws, int32_t* out_idx, float* out_w,
+                              int32_t* out_counts, int32_t* out_offsets, int32_t* out_perm,
+                              int* launches) {
+  RouteOut out{out_idx, out_w, out_counts, out_offsets, out_perm};
+  cudaError_t e;
+  dim3 gg((ws.E + kGN - 1) / kGN, (ws.T + kGM - 1) / kGM);
+  e = launch(lc, k_router_gemm, gg, dim3(256), 0, x, wr, ws);
+  if (e != cudaSuccess) return e;
+  const size_t tk_smem = (size_t)8 * (ws.E + 96) * 4;
+  e = cudaFuncSetAttribute(k_topk_wide, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tk_smem);
+  if (e != cudaSuccess) return e;
+  e = launch(lc, k_topk_wide, dim3((ws.T + 7) / 8), dim3(256), tk_smem, ws, out);
+  if (e != cudaSuccess) return e;
+  const int nchunk = (ws.T + kChunkTok - 1) / kChunkTok;
+  e = launch(lc, k_hist_wide, dim3(nchunk), dim3(256), (size_t)ws.E * 4, ws);
+  if (e != cudaSuccess) return e;
+  e = launch(lc, k_scan_wide, dim3(1), dim3(1024), 0, ws, out, nchunk);
+  if (e != cudaSuccess) return e;
+  e = launch(lc, k_scatter_wide, dim3(nchunk), dim3(256), (size_t)kChunkTok * ws.k * 4, ws, out);
+  if (launches) *launches += 5;
+  return e;
+}
+
+cudaError_t launch_xprep_wide(const LaunchCfg& lc, const uint16_t* x, const WsView& ws, int mode,
+                              float xS, float x_inv6S) {
+  return launch(lc, k_xprep_wide, dim3(ws.T), dim3(256), 0, x, ws, mode, xS, x_inv6S);
+}
+
+cudaError_t launch_quantize_rows(const LaunchCfg& lc, const uint16_t* x, int rows, int cols,
+                                 float S, float inv6S, uint8_t* codes, uint8_t* scales) {
+  const long long nblk = (long long)rows * (cols / 16);
+  long long grid = (nblk + 255) / 256;
+  const long long cap = (long long)lc.num_sms * 16;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  return launch(lc, k_quantize_rows, dim3((unsigned)grid), dim3(256), 0, x, rows, cols, S, inv6S,
+                codes, scales);
+}
+
+}  // namespace moe

@@ -1,0 +1,313 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded
+inputs. Rules and tolerances are stated in tests/_gpu_fixtures.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import nvfp4_mixture_experts_bf16_gb300 as moe
+from _gpu_fixtures import (GAMMA_NARROW, GAMMA_WIDE, FullLayer, check_topk, compare_outputs,
+                           dev_bf16, h_flip_allowance, host_u16, pack_from_experts, slot_map,
+                           small_layer, stable_perm, ws_array)
+
+pytestmark = pytest.mark.gpu
+
+ALL = ("out_bf16", "out64", "logits", "abssum", "idx", "w", "counts", "offsets", "perm",
+       "slot_of", "h_bf16", "hq_codes", "hq_scales", "h_amb_elem", "h_amb_block", "y",
+       "xq_codes", "xq_scales")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    moe.build()
+    moe.lib()
+
+
+def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None):
+    """Run moe_forward on the GPU and check every stage against the oracle."""
+    T, H = x.shape
+    E, I = ex.E, ex.I
+    S = T * k
+    ws = moe.new_workspace(moe.moe_workspace_size(pack, T, k, mode))
+    out = moe.moe_forward(dev_bf16(x), dev_bf16(wr), pack, k, mode, ws=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    off = moe.moe_workspace_offsets(pack, T, k, mode)
+    g_idx = ws_array(ws, off["idx"], S * 4, np.int32).reshape(T, k)
+    g_w = ws_array(ws, off["w"], S * 4, np.float32).reshape(T, k)
+    g_counts = ws_array(ws, off["counts"], E * 4, np.int32)
+    g_offsets = ws_array(ws, off["offsets"], (E + 1) * 4, np.int32)
+    g_perm = ws_array(ws, off["perm"], S * 4, np.int32)
+    g_slot_of = ws_array(ws, off["slot_of"], S * 4, np.int32).reshape(T, k)
+    ref = oracle.forward(x, wr, ex, k, mode, nthreads=nthreads, want=ALL)
+
+    differ = check_topk(g_idx, g_w, ref, GAMMA_NARROW if T <= 8 else GAMMA_WIDE)
+    c, o, p = stable_perm(g_idx, E)
+    assert np.array_equal(g_counts, c) and np.array_equal(g_offsets, o)
+    assert np.array_equal(g_perm, p)
+    if not differ:
+        assert np.array_equal(g_perm, ref["perm"]) and np.array_equal(g_counts, ref["counts"])
+    for t in range(T):
+        for j in range(k):
+            s = g_slot_of[t, j]
+            assert g_perm[s] == t and g_offsets[g_idx[t, j]] <= s < g_offsets[g_idx[t, j] + 1]
+
+    if mode == 1:
+        assert np.array_equal(ws_array(ws, off["x_codes"], T * H // 2, np.uint8).reshape(T, -1),
+                              ref["xq_codes"])
+        assert np.array_equal(ws_array(ws, off["x_scales"], T * H // 16, np.uint8).reshape(T, -1),
+                              ref["xq_scales"])
+    gm = slot_map(g_perm, g_offsets)
+    rm = slot_map(ref["perm"], ref["offsets"])
+    allowance = {}
+    flips = 0
+    if mode == 0:
+        gh = synth.bf16_to_f32(ws_array(ws, off["h_bf16"], S * I * 2, np.uint16).reshape(S, I))
+        rh = synth.bf16_to_f32(ref["h_bf16"])
+        gy = synth.bf16_to_f32(ws_array(ws, off["y"], S * H * 2, np.uint16).reshape(S, H))
+    else:
+        gq = ws_array(ws, off["h_codes"], S * I // 2, np.uint8).reshape(S, I // 2)
+        gsf = ws_array(ws, off["h_scales"], S * I // 16, np.uint8).reshape(S, I // 16)
+    for t in range(T):
+        if t in differ:
+            continue
+        for j in range(k):
+            e = int(g_idx[t, j])
+            gs, rs = gm[(t, e)], rm[(t, e)]
+            if mode == 0:
+                a, b = gh[gs].astype(np.float64), rh[rs].astype(np.float64)
+                scale = np.sqrt(np.mean(b * b)) + 1e-30
+                assert np.all(np.abs(a - b) <= 2.0 ** -8 * np.maximum(np.abs(a), np.abs(b))
+                              + 1e-5 * scale), (t, j)
+                ya, yb = gy[gs].astype(np.float64), ref["y"][rs]
+                assert np.linalg.norm(ya - yb) <= 2e-3 * np.linalg.norm(yb) + 1e-30, (t, j)
+            else:
+                a, f = h_flip_allowance(gq[gs], gsf[gs], ref, rs, I)
+                allowance[t] = allowance.get(t, 0.0) + float(g_w[t, j]) * a
+                flips += f
+    toks = [t for t in range(T) if t not in differ] if tokens is None else tokens
+    worst = compare_outputs(host_u16(out), ref, mode, toks, allowance)
+    return dict(out=out, ws=ws, differ=differ, flips=flips, worst=worst, ref=ref, g_idx=g_idx)
+
+
+# ------------------------------------------------------------------ quantiser
+def _q_case(rows, cols, S, rng):
+    v = rng.standard_normal((rows, cols)) * np.exp(rng.uniform(-4, 4, (rows, 1)))
+    v[0, :16] = 0.0                       # a zero block
+    v[1, :16] = 1e30                      # saturating block
+    v[1, 3] = -1e30
+    return synth.bf16_bits(v.astype(np.float32))
+
+
+def test_quantizer_bit_exact_random():
+    rng = np.random.default_rng(0)
+    for S in (1e-3, 0.37, 2.0 ** -9, 5e-6):
+        xb = _q_case(96, 1024, S, rng)
+        gc, gs = moe.moe_quantize_act_nvfp4(dev_bf16(xb), S)
+        rc, rs = oracle.quantize_nvfp4(synth.bf16_to_f32(xb), S)
+        assert np.array_equal(gs.cpu().numpy(), rs), S
+        assert np.array_equal(gc.cpu().numpy(), rc), S
+
+
+def test_quantizer_bit_exact_on_rounding_ties():
+    # S and the block scale are powers of two, so v * r lands exactly on E2M1 midpoints.
+    S = 2.0 ** -9
+    rows = []
+    rng = np.random.default_rng(1)
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 6.0, 0.0]
+    for k2 in range(-6, 7):
+        blk = np.array([6.0] + list(rng.choice(mids, 15)), np.float64) * 2.0 ** k2
+        blk *= np.where(rng.random(16) < 0.5, -1, 1)
+        rows.append(blk)
+    xb = synth.bf16_bits(np.array(rows, np.float32))
+    assert np.array_equal(synth.bf16_to_f32(xb), np.array(rows, np.float32))
+    gc, gs = moe.moe_quantize_act_nvfp4(dev_bf16(xb), S)
+    rc, rs = oracle.quantize_nvfp4(synth.bf16_to_f32(xb), S)
+    assert np.array_equal(gs.cpu().numpy(), rs)
+    assert np.array_equal(gc.cpu().numpy(), rc)
+
+
+# ------------------------------------------------------------------ pack
+def test_pack_is_bit_preserving():
+    x, wr, ex = small_layer(1, 256, 5, 2, 64)
+    pack = pack_from_experts(ex)
+    for e in range(ex.E):
+        for which, m in ((0, ex.gate), (1, ex.up), (2, ex.down)):
+            c, s, mult, ins = pack.get_matrix(e, which)
+            assert np.array_equal(c, m[e][0]) and np.array_equal(s, m[e][1])
+            assert np.float32(mult) == ex.mult[e, which]
+            assert np.float32(ins) == ex.in_scale[e, which]
+    pack.close()
+
+
+# ------------------------------------------------------------------ routing
+@pytest.mark.parametrize("T", [1, 5, 8, 9, 37, 300])
+def test_route_topk(T):
+    H, E, k = 512, 96, 6
+    x = synth.activations(3, 0, T, H, zipf=True)
+    wr = synth.router_weight(3, 0, E, H, zipf=True)
+    g = moe.moe_route_topk(dev_bf16(x), dev_bf16(wr), k)
+    torch.cuda.synchronize()
+    ref = oracle.route(x, wr, k, nthreads=8)
+    gi = g["idx"].cpu().numpy()
+    differ = check_topk(gi, g["w"].cpu().numpy(), ref, GAMMA_NARROW if T <= 8 else GAMMA_WIDE)
+    c, o, p = stable_perm(gi, E)
+    assert np.array_equal(g["counts"].cpu().numpy(), c)
+    assert np.array_equal(g["offsets"].cpu().numpy(), o)
+    assert np.array_equal(g["perm"].cpu().numpy(), p)
+    if not differ:
+        assert np.array_equal(p, ref["perm"])
+
+
+def test_route_topk_full_size_router():
+    for T in (1, 8):
+        x = synth.activations(0, 7, T, 4096, zipf=T == 8)
+        wr = synth.router_weight(0, 7, 512, 4096, zipf=T == 8)
+        g = moe.moe_route_topk(dev_bf16(x), dev_bf16(wr), 10)
+        torch.cuda.synchronize()
+        ref = oracle.route(x, wr, 10, nthreads=8)
+        differ = check_topk(g["idx"].cpu().numpy(), g["w"].cpu().numpy(), ref, GAMMA_NARROW)
+        assert not differ
+
+
+def test_route_ties_go_to_lower_index():
+    T, H, E, k = 3, 256, 32, 5
+    x = synth.activations(5, 0, T, H)
+    wr = np.tile(synth.router_weight(5, 0, 1, H), (E, 1))  # all logits equal
+    g = moe.moe_route_topk(dev_bf16(x), dev_bf16(wr), k)
+    gi = g["idx"].cpu().numpy()
+    assert np.array_equal(gi, np.tile(np.arange(k), (T, 1)))
+    assert np.allclose(g["w"].cpu().numpy(), 1.0 / k, rtol=1e-6)
+
+
+# ------------------------------------------------------------------ forward, small shapes
+@pytest.mark.parametrize("mode", [0, 1])
+def test_forward_tiny_workload(mode):
+    wl = synth.WORKLOADS["tiny"]
+    x, wr, ex = small_layer(wl.T, wl.H, wl.E, wl.k, wl.I)
+    pack = pack_from_experts(ex)
+    r = run_and_check(x, wr, ex, pack, wl.k, mode)
+    assert r["worst"] < {0: 2e-3, 1: 5e-3}[mode]
+    pack.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("T", [1, 3, 8, 9, 50, 203])
+def test_forward_ragged_shapes(T, mode):
+    # several row tiles, k-blocks and token groups, with ragged tails
+    H, E, k, I = 1536, 24, 4, 192
+    x, wr, ex = small_layer(T, H, E, k, I, zipf=True, seed=11)
+    pack = pack_from_experts(ex)
+    run_and_check(x, wr, ex, pack, k, mode)
+    pack.close()
+
+
+def test_forward_twice_is_deterministic_and_counters_reset():
+    x, wr, ex = small_layer(8, 512, 32, 4, 128, seed=4)
+    pack = pack_from_experts(ex)
+    ws = moe.new_workspace(moe.moe_workspace_size(pack, 8, 4, 0))
+    a = moe.moe_forward(dev_bf16(x), dev_bf16(wr), pack, 4, 0, ws=ws).clone()
+    b = moe.moe_forward(dev_bf16(x), dev_bf16(wr), pack, 4, 0, ws=ws).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert moe.moe_read_device_status(ws) == 0
+    assert int(ws[:4].view(torch.int32).item()) == 0     # router ticket back at zero
+    pack.close()
+
+
+def test_forward_identical_experts_equal_one_expert():
+    x, wr, ex = small_layer(4, 512, 16, 3, 128, seed=6)
+    same = oracle.ExpertSet(ex.E, ex.H, ex.I)
+    for e in range(ex.E):
+        same.set(e, ex.gate[0], ex.up[0], ex.down[0], ex.mult[0], ex.in_scale[0])
+    pack = pack_from_experts(same)
+    r = run_and_check(x, wr, same, pack, 3, 0)
+    # every slot of a token holds the same Y; the weights sum to 1
+    ref = r["ref"]
+    for t in range(4):
+        y0 = ref["y"][ref["slot_of"][t, 0]]
+        assert np.array_equal(synth.bf16_to_f32(ref["out_bf16"][t]).astype(np.float64), y0)
+    pack.close()
+
+
+def test_forward_zero_activations():
+    x = np.zeros((3, 512), np.uint16)
+    _, wr, ex = small_layer(3, 512, 16, 3, 128, seed=8)
+    pack = pack_from_experts(ex)
+    for mode in (0, 1):
+        out = moe.moe_forward(dev_bf16(x), dev_bf16(wr), pack, 3, mode)
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(out.float()).item() == 0
+    pack.close()
+
+
+def test_forward_rejects_bad_arguments():
+    x, wr, ex = small_layer(2, 256, 8, 2, 64)
+    pack = pack_from_experts(ex)
+    xd, wd = dev_bf16(x), dev_bf16(wr)
+    with pytest.raises(moe.MoeError):
+        moe.moe_forward(xd, wd, pack, 9, 0)            # k > E
+    ws = moe.new_workspace(64)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward(xd, wd, pack, 2, 0, ws=ws)      # workspace too small
+    assert e.value.code == 6
+    pack.close()
+
+
+# ------------------------------------------------------------------ full-size decode
+@pytest.mark.parametrize("name", ["decode1", "verify8", "verify8_w4a4"])
+def test_forward_full_size_decode(name):
+    wl = synth.WORKLOADS[name]
+    lay = FullLayer(0, 0, wl.T, wl.zipf)
+    ref_route = oracle.route(lay.x, lay.wr, wl.k, nthreads=8)
+    ex = lay.oracle_experts(ref_route["idx"].ravel())
+    r = run_and_check(lay.x, lay.wr, ex, lay.pack, wl.k, wl.mode)
+    assert not r["differ"]
+    lay.close()
+
+
+# ------------------------------------------------------------------ full-size prefill, sampled
+@pytest.mark.parametrize("mode", [1, 0])
+def test_forward_prefill_8192_sampled(mode):
+    wl = synth.WORKLOADS["prefill8192"]
+    lay = FullLayer(0, 0, wl.T, wl.zipf)
+    T, k = wl.T, wl.k
+    ws = moe.new_workspace(moe.moe_workspace_size(lay.pack, T, k, mode))
+    out = moe.moe_forward(dev_bf16(lay.x), dev_bf16(lay.wr), lay.pack, k, mode, ws=ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    off = moe.moe_workspace_offsets(lay.pack, T, k, mode)
+    g_idx = ws_array(ws, off["idx"], T * k * 4, np.int32).reshape(T, k)
+    g_w = ws_array(ws, off["w"], T * k * 4, np.float32).reshape(T, k)
+    ref_route = oracle.route(lay.x, lay.wr, k, nthreads=16)
+    differ = check_topk(g_idx, g_w, ref_route, GAMMA_WIDE)
+    c, o, p = stable_perm(g_idx, lay.E)
+    assert np.array_equal(ws_array(ws, off["perm"], T * k * 4, np.int32), p)
+    assert c.max() > 1000  # the Zipf popularity reaches the thousands
+    if mode == 1:
+        rc, rs = oracle.quantize_nvfp4(synth.bf16_to_f32(lay.x), lay.xs, nthreads=16)
+        assert np.array_equal(ws_array(ws, off["x_codes"], T * 2048, np.uint8).reshape(T, -1), rc)
+        assert np.array_equal(ws_array(ws, off["x_scales"], T * 256, np.uint8).reshape(T, -1), rs)
+    rng = np.random.default_rng(0)
+    sample = [int(t) for t in rng.choice(T, 24, replace=False) if t not in differ]
+    sample += [t for t in (0, T - 1) if t not in differ and t not in sample]
+    ex = lay.oracle_experts(ref_route["idx"][sample].ravel(), nthreads=16)
+    ref = oracle.forward(lay.x[sample], lay.wr, ex, k, mode, nthreads=16,
+                         want=("out_bf16", "out64", "idx", "perm", "offsets", "hq_codes",
+                               "hq_scales", "h_amb_elem", "h_amb_block"))
+    allowance = {}
+    if mode == 1:
+        g_perm = ws_array(ws, off["perm"], T * k * 4, np.int32)
+        gm = slot_map(g_perm, o)
+        rm = slot_map(ref["perm"], ref["offsets"])
+        gq = ws_array(ws, off["h_codes"], T * k * lay.I // 2, np.uint8).reshape(T * k, -1)
+        gsf = ws_array(ws, off["h_scales"], T * k * lay.I // 16, np.uint8).reshape(T * k, -1)
+        for i, t in enumerate(sample):
+            for j in range(k):
+                e = int(g_idx[t, j])
+                a, _ = h_flip_allowance(gq[gm[(t, e)]], gsf[gm[(t, e)]], ref, rm[(i, e)], lay.I)
+                allowance[i] = allowance.get(i, 0.0) + float(g_w[t, j]) * a
+    got = host_u16(out)[sample]
+    compare_outputs(got, ref, mode, list(range(len(sample))), allowance)
+    lay.close()
