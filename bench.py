@@ -46,6 +46,8 @@ def parse_args():
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--workload", default="decode1", choices=list(synth.WORKLOADS))
     p.add_argument("--layers", type=int, default=None)
+    p.add_argument("--experts", type=int, default=None,
+                   help="experts per layer (smaller packs for profiler captures)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -213,7 +215,8 @@ def quantized_experts(seed, layer, E, H, I, device):
     mats = {}
     for w in ("gate", "up", "down"):
         W = synth.torch_expert_weights(seed, layer, w, E, H, I, device)
-        S = (W.float().abs().amax(dim=(1, 2)) / 2688.0).float().cpu().numpy()
+        # multiplier = fl32(amax / 2688) by an IEEE float32 division on the host
+        S = W.float().abs().amax(dim=(1, 2)).cpu().numpy().astype(np.float32) / np.float32(2688.0)
         rows, cols = W.shape[1], W.shape[2]
         codes = torch.empty((E, rows, cols // 2), dtype=torch.uint8, device=device)
         scales = torch.empty((E, rows, cols // 16), dtype=torch.uint8, device=device)
@@ -318,6 +321,9 @@ def stage_times(wl, stack, reps, device):
     with torch.cuda.stream(s):
         for rep in range(reps + 1):
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in stack]
+            for ev in evs:          # torch creates the CUDA event at its first record
+                for e in ev:
+                    e.record(s)
             for L, o, ev in zip(stack, outs, evs):
                 moe.moe_profile_next_forward(ev)
                 moe.moe_forward(L.x, L.wr, L.pack, wl.k, wl.mode, out=o, ws=ws, stream=s)
@@ -365,6 +371,9 @@ def run_native(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     wl = synth.WORKLOADS[args.workload]
+    if args.experts:
+        wl = synth.Workload(wl.name, wl.T, wl.H, args.experts, wl.k, wl.I, wl.mode, wl.layers,
+                            wl.zipf)
     layers = args.layers or wl.layers
     pk = peaks()
     t_setup = time.time()

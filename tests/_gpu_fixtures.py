@@ -78,12 +78,12 @@ class FullLayer:
                   for w in ("gate", "up", "down")}
         self.q = {}
         for w, W in self.W.items():
-            amax = W.float().abs().amax(dim=(1, 2))
-            S = (amax / 2688.0).float()
+            amax = W.float().abs().amax(dim=(1, 2)).cpu().numpy().astype(np.float32)
+            # IEEE float32 division (torch divides a tensor by a scalar via a reciprocal)
+            Sh = amax / np.float32(2688.0)
             rows, cols = W.shape[1], W.shape[2]
             codes = torch.empty((E, rows, cols // 2), dtype=torch.uint8, device="cuda")
             scales = torch.empty((E, rows, cols // 16), dtype=torch.uint8, device="cuda")
-            Sh = S.cpu().numpy()
             for e in range(E):
                 moe.moe_quantize_act_nvfp4(W[e], float(Sh[e]), codes[e], scales[e])
             self.q[w] = (codes, scales, Sh)

@@ -78,8 +78,11 @@ def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None):
             if mode == 0:
                 a, b = gh[gs].astype(np.float64), rh[rs].astype(np.float64)
                 scale = np.sqrt(np.mean(b * b)) + 1e-30
-                assert np.all(np.abs(a - b) <= 2.0 ** -8 * np.maximum(np.abs(a), np.abs(b))
-                              + 1e-5 * scale), (t, j)
+                # at most one BF16 ulp (<= 2^-7 of the larger magnitude) where the FP32 h and
+                # the FP64 h round to different neighbours
+                assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b))
+                              + 1e-5 * scale), (t, j, np.flatnonzero(np.abs(a - b) > 2.0 ** -7 *
+                                                np.maximum(np.abs(a), np.abs(b)) + 1e-5 * scale))
                 ya, yb = gy[gs].astype(np.float64), ref["y"][rs]
                 assert np.linalg.norm(ya - yb) <= 2e-3 * np.linalg.norm(yb) + 1e-30, (t, j)
             else:
