@@ -65,8 +65,9 @@ int num_sms_of_current_device() {
 }
 
 struct WsLayout {
-  size_t ctl, logits, idx, w, slot_of, counts, offsets, perm, grp_expert, grp_slot, grp_n,
+  size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm, grp_expert, grp_slot, grp_n,
       chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, total;
+  size_t slot_amax_bytes;
   int G;
 };
 
@@ -79,6 +80,9 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
   L.ctl = take(moe::kCtlWords * 4);
+  L.gmeta = take((size_t)L.G * sizeof(moe::GroupMeta));
+  L.slot_amax_bytes = mode == 0 ? (size_t)S * 4 : 0;
+  L.slot_amax = take(L.slot_amax_bytes);
   L.logits = take((size_t)T * E * 4);
   L.idx = take((size_t)S * 4);
   L.w = take((size_t)S * 4);
@@ -106,6 +110,8 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   unsigned char* b = static_cast<unsigned char*>(ws);
   moe::WsView v;
   v.ctl = reinterpret_cast<uint32_t*>(b + L.ctl);
+  v.gmeta = reinterpret_cast<moe::GroupMeta*>(b + L.gmeta);
+  v.slot_amax = L.slot_amax_bytes ? reinterpret_cast<uint32_t*>(b + L.slot_amax) : nullptr;
   v.logits = reinterpret_cast<float*>(b + L.logits);
   v.idx = reinterpret_cast<int32_t*>(b + L.idx);
   v.w = reinterpret_cast<float*>(b + L.w);
@@ -351,11 +357,12 @@ moe_status moe_route_topk(const uint16_t* x, const uint16_t* router_w, int T, in
   moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
   cudaError_t e;
   if (T <= moe::kNarrowT) {
-    e = moe::launch_route_narrow(lc, x, router_w, v, -1, 1.0f, 1.0f, idx, w, counts, offsets, perm);
+    e = moe::launch_route_narrow(lc, x, router_w, v, nullptr, -1, 1.0f, 1.0f, idx, w, counts,
+                                 offsets, perm);
     g_last_launches = 1;
   } else {
     int n = 0;
-    e = moe::launch_route_wide(lc, x, router_w, v, idx, w, counts, offsets, perm, &n);
+    e = moe::launch_route_wide(lc, x, router_w, v, nullptr, idx, w, counts, offsets, perm, &n);
     g_last_launches = n;
   }
   return from_cuda(e);
@@ -387,12 +394,13 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
   e = prof_mark(lc.stream, 0);
   if (narrow) {
     if (e == cudaSuccess)
-      e = moe::launch_route_narrow(lc, x, router_w, v, m, pack->x_scale, pack->x_inv6S, v.idx,
-                                   v.w, v.counts, v.offsets, v.perm);
+      e = moe::launch_route_narrow(lc, x, router_w, v, &pack->view, m, pack->x_scale,
+                                   pack->x_inv6S, v.idx, v.w, v.counts, v.offsets, v.perm);
     n += 1;
   } else {
     if (e == cudaSuccess)
-      e = moe::launch_route_wide(lc, x, router_w, v, v.idx, v.w, v.counts, v.offsets, v.perm, &n);
+      e = moe::launch_route_wide(lc, x, router_w, v, &pack->view, v.idx, v.w, v.counts, v.offsets,
+                                 v.perm, &n);
     if (e == cudaSuccess) {
       e = moe::launch_xprep_wide(lc, x, v, m, pack->x_scale, pack->x_inv6S);
       n += 1;

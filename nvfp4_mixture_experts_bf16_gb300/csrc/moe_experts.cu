@@ -31,14 +31,15 @@ constexpr int kDnThreads = (kDnConsumers + 1) * 32;
 constexpr int kMaxSmem = 232448;  // 227 KB opt-in per block
 
 struct GuGeom {
-  int KC;          // reduction columns per stage
+  int KC;          // reduction columns per stage (== H when a whole task fits one stage)
   int nkc;         // stages per task (H / KC)
-  int row_stride;  // bytes per code row in shared memory (KC/2 + pad, == 32 mod 128)
-  int stage_bytes;
+  int row_bytes;   // KC / 2: code bytes per row in a stage (rows packed, no padding)
+  int stage_bytes; // 32 rows of codes + gate/up scales
   int stages;
-  int x_stride;    // bytes per activation row in shared memory (2H + 16)
-  int x_rows;      // rows of the activation region (T if resident else 8)
+  int x_stride;    // bytes per activation row in shared memory (2H + 64)
+  int x_rows;      // T if resident else 8
   int tiles;       // I / 16
+  int meta_cap;    // group records staged per CTA
 };
 
 struct DnGeom {
@@ -47,32 +48,32 @@ struct DnGeom {
   int h_stride;     // 2I + 16
   int h_rows;       // slots if resident else 8
   int tiles;        // H / 64
+  int meta_cap;
 };
 
-__host__ __device__ inline int pick_kc(int H) {
-  return (H % 1024 == 0) ? 1024 : (H % 512 == 0) ? 512 : (H % 256 == 0) ? 256
-                                                                         : (H % 128 == 0) ? 128 : 64;
-}
+constexpr int kMetaCap = 8;   // group records staged per CTA (a CTA's task range spans few groups)
 
 GuGeom gu_geom(int H, int I, bool x_resident, int T) {
   GuGeom g;
-  g.KC = pick_kc(H);
+  g.KC = H <= 4096 ? H : 4096;
+  while (H % g.KC) g.KC -= 128;
   g.nkc = H / g.KC;
-  const int half = g.KC / 2;
-  g.row_stride = half + ((32 - (half % 128)) + 128) % 128;
-  g.stage_bytes = 32 * g.row_stride + 2 * g.KC;
-  g.x_stride = 2 * H + 16;
+  g.row_bytes = g.KC / 2;
+  g.stage_bytes = 32 * g.row_bytes + 2 * g.KC;
+  g.x_stride = 2 * H + 64;
   g.x_rows = x_resident ? T : kGroup;
   g.tiles = I / 16;
-  const int fixed = g.x_rows * g.x_stride + kGuConsumers * 2 * 32 * 16 + 1024;
+  g.meta_cap = kMetaCap;
+  const int fixed = g.x_rows * g.x_stride + kGuConsumers * 2 * 32 * 16 +
+                    g.meta_cap * (int)sizeof(GroupMeta) + 1024;
   int st = (kMaxSmem - fixed) / g.stage_bytes;
-  g.stages = st > 6 ? 6 : st;
+  g.stages = st > 3 ? 3 : st;
   return g;
 }
 
 size_t gu_smem(const GuGeom& g) {
   return (size_t)g.stages * g.stage_bytes + (size_t)g.x_rows * g.x_stride +
-         kGuConsumers * 2 * 32 * 16 + 2 * 8 * g.stages + 64;
+         kGuConsumers * 2 * 32 * 16 + g.meta_cap * sizeof(GroupMeta) + 2 * 8 * g.stages + 64;
 }
 
 DnGeom dn_geom(int H, int I, bool h_resident, int slots) {
@@ -81,7 +82,8 @@ DnGeom dn_geom(int H, int I, bool h_resident, int slots) {
   d.h_stride = 2 * I + 16;
   d.h_rows = h_resident ? slots : kGroup;
   d.tiles = H / 64;
-  const int fixed = d.h_rows * d.h_stride + d.h_rows * 4 + 1024;
+  d.meta_cap = kMetaCap;
+  const int fixed = d.h_rows * d.h_stride + d.h_rows * 4 + d.meta_cap * (int)sizeof(GroupMeta) + 1024;
   int st = (kMaxSmem - fixed) / d.stage_bytes;
   d.stages = st > 8 ? 8 : st;
   return d;
@@ -89,7 +91,7 @@ DnGeom dn_geom(int H, int I, bool h_resident, int slots) {
 
 size_t dn_smem(const DnGeom& d) {
   return (size_t)d.stages * d.stage_bytes + (size_t)d.h_rows * d.h_stride + d.h_rows * 4 +
-         2 * 8 * d.stages + 64;
+         d.meta_cap * sizeof(GroupMeta) + 2 * 8 * d.stages + 64;
 }
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
@@ -105,11 +107,23 @@ __device__ __forceinline__ uint4 lds128(const unsigned char* p) {
 __device__ __forceinline__ uint32_t lds16(const unsigned char* p) {
   return *reinterpret_cast<const uint16_t*>(p);
 }
+__device__ __forceinline__ uint32_t lds32(const unsigned char* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
+}
 
 // Balanced contiguous task range of this CTA.
 __device__ __forceinline__ void task_range(int ntasks, int& q0, int& q1) {
   q0 = (int)(((long long)ntasks * blockIdx.x) / gridDim.x);
   q1 = (int)(((long long)ntasks * (blockIdx.x + 1)) / gridDim.x);
+}
+
+// Stage the group records of groups [g0, g0 + n) into shared memory (n <= kMetaCap).
+__device__ __forceinline__ void stage_meta(GroupMeta* dst, const GroupMeta* src, int g0, int n,
+                                           int tid, int nthreads) {
+  const int words = n * (int)(sizeof(GroupMeta) / 16);
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + g0);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (int i = tid; i < words; i += nthreads) d4[i] = s4[i];
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
@@ -122,16 +136,19 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
 }
 
 // ------------------------------------------------------------------ gate/up
-// grid: persistent; block: 8 consumer warps + 1 producer warp.
-// A task is (token group gi, 16-row tile `it` of the intermediate dimension): it computes
-// gate and up rows it*16..+15 for the group's tokens over the full hidden dimension.
+// grid: persistent, one CTA per SM; block: 8 consumer warps + 1 producer warp.
+// A task is (token group gi, 16-row tile `it` of the intermediate dimension): gate and up rows
+// it*16..+15 for the group's tokens over the full hidden dimension. The rows of a 16-row tile
+// are contiguous in the pack, so a whole task is 4 TMA bulk copies (gate codes, up codes, gate
+// scales, up scales) when it fits one stage.
 __global__ void __launch_bounds__(kGuThreads, 1)
     k_gateup(PackView pk, WsView ws, GuGeom geo, int mode, int x_resident) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* stages = smem;
   unsigned char* xs = stages + (size_t)geo.stages * geo.stage_bytes;
   float* red = reinterpret_cast<float*>(xs + (size_t)geo.x_rows * geo.x_stride);
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + kGuConsumers * 2 * 32 * 4);
+  GroupMeta* meta = reinterpret_cast<GroupMeta*>(red + kGuConsumers * 2 * 32 * 4);
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + geo.meta_cap);
   uint64_t* empty = full + geo.stages;
   __shared__ volatile int abort_s;
   __shared__ int cur_group_s;
@@ -155,14 +172,17 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   const int ntasks = G * geo.tiles;
   int q0, q1;
   task_range(ntasks, q0, q1);
+  const int gfirst = q0 / geo.tiles;
+  const int glast = q1 > q0 ? (q1 - 1) / geo.tiles : gfirst - 1;
 
   if (warp == kGuConsumers) {
     // ---------------- producer
     if (lane != 0) return;
     int chunk = 0;
+    const uint32_t half = geo.row_bytes;
     for (int q = q0; q < q1 && !abort_s; ++q) {
       const int gi = q / geo.tiles, it = q % geo.tiles;
-      const int e = ws.grp_expert[gi];
+      const int e = __ldg(&ws.gmeta[gi].expert);
       const size_t row0 = (size_t)e * I + (size_t)it * 16;
       const uint8_t* gsrc = pk.gate_codes + row0 * (H / 2);
       const uint8_t* usrc = pk.up_codes + row0 * (H / 2);
@@ -176,16 +196,19 @@ __global__ void __launch_bounds__(kGuThreads, 1)
           break;
         }
         unsigned char* st = stages + (size_t)s * geo.stage_bytes;
-        const uint32_t half = geo.KC / 2;
         mbar_arrive_expect_tx(&full[s], 32 * half + 2 * geo.KC);
-        for (int r = 0; r < 16; ++r) {
-          bulk_g2s(st + r * geo.row_stride, gsrc + (size_t)r * (H / 2) + (size_t)kc * half, half,
-                   &full[s]);
-          bulk_g2s(st + (16 + r) * geo.row_stride, usrc + (size_t)r * (H / 2) + (size_t)kc * half,
-                   half, &full[s]);
+        if (geo.nkc == 1) {
+          bulk_g2s(st, gsrc, 16 * half, &full[s]);
+          bulk_g2s(st + 16 * half, usrc, 16 * half, &full[s]);
+        } else {
+          for (int r = 0; r < 16; ++r) {
+            bulk_g2s(st + r * half, gsrc + (size_t)r * (H / 2) + (size_t)kc * half, half, &full[s]);
+            bulk_g2s(st + (16 + r) * half, usrc + (size_t)r * (H / 2) + (size_t)kc * half, half,
+                     &full[s]);
+          }
         }
-        bulk_g2s(st + 32 * geo.row_stride, gsc + (size_t)kc * geo.KC, geo.KC, &full[s]);
-        bulk_g2s(st + 32 * geo.row_stride + geo.KC, usc + (size_t)kc * geo.KC, geo.KC, &full[s]);
+        bulk_g2s(st + 32 * half, gsc + (size_t)kc * geo.KC, geo.KC, &full[s]);
+        bulk_g2s(st + 32 * half + geo.KC, usc + (size_t)kc * geo.KC, geo.KC, &full[s]);
       }
     }
     // Do not leave while copies into this CTA's shared memory may still be in flight.
@@ -200,40 +223,52 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   // ---------------- consumers
   const int g = lane >> 2, c = lane & 3;
   const int ncons = kGuConsumers * 32;
-  if (x_resident) {
-    // all T tokens' activations, row t at t * x_stride
-    const int T = ws.T;
-    const int words = H / 8;  // uint4 per row
-    for (int i = tid; i < T * words; i += ncons) {
-      const int t = i / words, w = i % words;
-      *reinterpret_cast<uint4*>(xs + (size_t)t * geo.x_stride + w * 16) =
-          reinterpret_cast<const uint4*>(ws.xh + (size_t)t * H)[w];
+  const int nmeta = glast - gfirst + 1;
+  if (nmeta > 0) stage_meta(meta, ws.gmeta, gfirst, nmeta < geo.meta_cap ? nmeta : geo.meta_cap,
+                            tid, ncons);
+  // Activation rows in shared memory, permuted inside each 128-wide k-block so that thread c
+  // reads its 32 values as 4 x 16 B: element 128J + 32c + 8p + q -> 128J + 32p + 8c + q.
+  auto stage_x_row = [&](int row, const __half* src, int word0, int step) {
+    unsigned char* dst = xs + (size_t)row * geo.x_stride;
+    for (int w = word0; w < H / 8; w += step) {   // w = 16-B word of the natural row
+      const int J = w >> 4, cc = (w >> 2) & 3, p = w & 3;
+      *reinterpret_cast<uint4*>(dst + J * 256 + p * 64 + cc * 16) =
+          reinterpret_cast<const uint4*>(src)[w];
     }
-    consumer_sync(ncons);
+  };
+  if (x_resident) {
+    const int T = ws.T;
+    for (int i = tid; i < T * (H / 8); i += ncons) {
+      const int t = i / (H / 8), w = i % (H / 8);
+      stage_x_row(t, ws.xh + (size_t)t * H, w, H / 8);
+    }
   }
+  consumer_sync(ncons);
   int chunk = 0;
-  const int kb_per_chunk = geo.KC / 64;
+  const int jb_per_chunk = geo.KC / 128;
   for (int q = q0; q < q1; ++q) {
     const int gi = q / geo.tiles, it = q % geo.tiles;
-    const int e = ws.grp_expert[gi];
-    const int slot0 = ws.grp_slot[gi];
-    const int n = ws.grp_n[gi];
+    const int mi = gi - gfirst;
+    const GroupMeta& gm = (mi < geo.meta_cap) ? meta[mi] : ws.gmeta[gi];
+    const int slot0 = gm.slot0, n = gm.n;
     if (!x_resident && gi != cur_group_s) {
       consumer_sync(ncons);
-      const int words = H / 8;
-      for (int i = tid; i < kGroup * words; i += ncons) {
-        const int r = i / words, w = i % words;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < n) v = reinterpret_cast<const uint4*>(ws.xh + (size_t)ws.perm[slot0 + r] * H)[w];
-        *reinterpret_cast<uint4*>(xs + (size_t)r * geo.x_stride + w * 16) = v;
+      for (int i = tid; i < kGroup * (H / 8); i += ncons) {
+        const int r = i / (H / 8), w = i % (H / 8);
+        if (r < n) {
+          stage_x_row(r, ws.xh + (size_t)ws.perm[slot0 + r] * H, w, H / 8);
+        } else {
+          const int J = w >> 4, cc = (w >> 2) & 3, p = w & 3;
+          *reinterpret_cast<uint4*>(xs + (size_t)r * geo.x_stride + J * 256 + p * 64 + cc * 16) =
+              make_uint4(0, 0, 0, 0);
+        }
       }
       consumer_sync(ncons);
       if (tid == 0) cur_group_s = gi;
     }
-    // activation row of this lane's token column g
     const bool gvalid = g < n;
-    const int xrow = x_resident ? (gvalid ? ws.perm[slot0 + g] : 0) : g;
-    const unsigned char* xr = xs + (size_t)xrow * geo.x_stride + c * 32;
+    const int xrow = x_resident ? (gvalid ? gm.tok[g] : 0) : g;
+    const unsigned char* xr = xs + (size_t)xrow * geo.x_stride + c * 16;
 
     float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
     for (int kc = 0; kc < geo.nkc; ++kc, ++chunk) {
@@ -243,23 +278,26 @@ __global__ void __launch_bounds__(kGuThreads, 1)
         abort_s = 1;
       }
       const unsigned char* st = stages + (size_t)s * geo.stage_bytes;
-      for (int jb = warp; jb < kb_per_chunk; jb += kGuConsumers) {
-        const int off = jb * 32 + c * 8;
-        const uint2 gr = lds64(st + g * geo.row_stride + off);
-        const uint2 gr8 = lds64(st + (g + 8) * geo.row_stride + off);
-        const uint2 ur = lds64(st + (16 + g) * geo.row_stride + off);
-        const uint2 ur8 = lds64(st + (24 + g) * geo.row_stride + off);
-        const unsigned char* scb = st + 32 * geo.row_stride + jb * 64 + c * 16 + g * 2;
-        const uint32_t scg = lds16(scb);
-        const uint32_t scu = lds16(scb + geo.KC);
-        uint4 xb0 = make_uint4(0, 0, 0, 0), xb1 = xb0;
+      const unsigned char* scb = st + 32 * geo.row_bytes + c * 32 + g * 4;
+      for (int jb = warp; jb < jb_per_chunk; jb += kGuConsumers) {
+        const int off = jb * 64 + c * 16;
+        const uint4 gr = lds128(st + g * geo.row_bytes + off);
+        const uint4 gr8 = lds128(st + (g + 8) * geo.row_bytes + off);
+        const uint4 ur = lds128(st + (16 + g) * geo.row_bytes + off);
+        const uint4 ur8 = lds128(st + (24 + g) * geo.row_bytes + off);
+        const uint32_t scg = lds32(scb + jb * 128);
+        const uint32_t scu = lds32(scb + geo.KC + jb * 128);
+        uint4 xb[4];
         if (gvalid || !x_resident) {
-          const unsigned char* xp = xr + (size_t)(kc * kb_per_chunk + jb) * 128;
-          xb0 = lds128(xp);
-          xb1 = lds128(xp + 16);
+          const unsigned char* xp = xr + (size_t)(kc * jb_per_chunk + jb) * 256;
+#pragma unroll
+          for (int p = 0; p < 4; ++p) xb[p] = lds128(xp + p * 64);
+        } else {
+#pragma unroll
+          for (int p = 0; p < 4; ++p) xb[p] = make_uint4(0, 0, 0, 0);
         }
-        kblock_mma(accg, gr, gr8, scg, xb0, xb1);
-        kblock_mma(accu, ur, ur8, scu, xb0, xb1);
+        kblock128_mma(accg, gr, gr8, scg, xb);
+        kblock128_mma(accu, ur, ur8, scu, xb);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -279,28 +317,36 @@ __global__ void __launch_bounds__(kGuThreads, 1)
         G4[0] += a.x; G4[1] += a.y; G4[2] += a.z; G4[3] += a.w;
         U4[0] += b.x; U4[1] += b.y; U4[2] += b.z; U4[3] += b.w;
       }
-      const float mg = pk.mult[e * 3 + 0], mu = pk.mult[e * 3 + 1];
       float hv[4];  // (row g, col 2c), (row g, col 2c+1), (row g+8, col 2c), (row g+8, col 2c+1)
 #pragma unroll
       for (int q2 = 0; q2 < 4; ++q2) {
         const int col = 2 * c + (q2 & 1);
-        const float xf = col < n ? ws.xfac[ws.perm[slot0 + col]] : 0.0f;
-        const float gv = G4[q2] * mg * xf;
-        const float uv = U4[q2] * mu * xf;
+        const int tok = col < n ? (x_resident ? gm.tok[col] : ws.perm[slot0 + col]) : 0;
+        const float xf = col < n ? ws.xfac[tok] : 0.0f;
+        const float gv = G4[q2] * gm.mg * xf;
+        const float uv = U4[q2] * gm.mu * xf;
         hv[q2] = col < n ? silu_mul(gv, uv) : 0.0f;
       }
       const int i0 = it * 16 + g;
       if (mode == 0) {
 #pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-          const int col = 2 * c + (q2 & 1);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int col = 2 * c + cc;
+          const uint16_t b0 = f32_to_bf16_rn(hv[cc]), b1 = f32_to_bf16_rn(hv[2 + cc]);
+          // |h| of the BF16 values, for the down stage's per-slot f16 scaling
+          float a = fmaxf(fabsf(__uint_as_float((uint32_t)b0 << 16)),
+                          fabsf(__uint_as_float((uint32_t)b1 << 16)));
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
           if (col < n) {
-            const int row = i0 + ((q2 >> 1) << 3);
-            ws.h16[(size_t)(slot0 + col) * I + row] = f32_to_bf16_rn(hv[q2]);
+            const size_t slot = (size_t)(slot0 + col);
+            ws.h16[slot * I + i0] = b0;
+            ws.h16[slot * I + i0 + 8] = b1;
+            if (g == 0) atomicMax(&ws.slot_amax[slot], __float_as_uint(a));
           }
         }
       } else {
-        const float Sd = pk.down_in_scale[e], i6 = pk.down_inv6S[e];
+        const float Sd = gm.sd, i6 = gm.i6d;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {  // token column 2c + cc
           const float v_lo = hv[cc], v_hi = hv[2 + cc];  // elements g and g+8 of the block
@@ -311,10 +357,8 @@ __global__ void __launch_bounds__(kGuThreads, 1)
           uint32_t lo = 0, hi = 0;
           if (sf != 0u) {
             const float r = __frcp_rn(__fmul_rn(e4m3_value_nonneg(sf), Sd));
-            const uint32_t q_lo = e2m1_encode_rn(__fmul_rn(v_lo, r));
-            const uint32_t q_hi = e2m1_encode_rn(__fmul_rn(v_hi, r));
-            lo = q_lo << (4 * g);  // elements 0..7 -> word 0
-            hi = q_hi << (4 * g);  // elements 8..15 -> word 1
+            lo = e2m1_encode_rn(__fmul_rn(v_lo, r)) << (4 * g);  // elements 0..7 -> word 0
+            hi = e2m1_encode_rn(__fmul_rn(v_hi, r)) << (4 * g);  // elements 8..15 -> word 1
           }
 #pragma unroll
           for (int off = 4; off < 32; off <<= 1) {
@@ -337,13 +381,22 @@ __global__ void __launch_bounds__(kGuThreads, 1)
 // ------------------------------------------------------------------ down
 // A task is (token group gi, 64-row tile ht of the hidden dimension); consumer warp w owns
 // rows ht*64 + 16w .. +15. Y (BF16) goes to the slot-major buffer for the combine.
+__device__ __forceinline__ int amax_shift(float m) {
+  if (!(m > 0.0f)) return 0;
+  int ex;
+  frexpf(m, &ex);
+  const int sh = ex - 15;
+  return sh < -110 ? -110 : (sh > 110 ? 110 : sh);
+}
+
 __global__ void __launch_bounds__(kDnThreads, 1)
     k_down(PackView pk, WsView ws, DnGeom geo, int mode, int h_resident) {
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* stages = smem;
   unsigned char* hs = stages + (size_t)geo.stages * geo.stage_bytes;
   float* hfac = reinterpret_cast<float*>(hs + (size_t)geo.h_rows * geo.h_stride);
-  uint64_t* full = reinterpret_cast<uint64_t*>(hfac + geo.h_rows + (geo.h_rows & 1));
+  GroupMeta* meta = reinterpret_cast<GroupMeta*>(hfac + geo.h_rows + ((4 - (geo.h_rows & 3)) & 3));
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + geo.meta_cap);
   uint64_t* empty = full + geo.stages;
   __shared__ volatile int abort_s;
   __shared__ int cur_group_s;
@@ -368,13 +421,15 @@ __global__ void __launch_bounds__(kDnThreads, 1)
   int q0, q1;
   task_range(ntasks, q0, q1);
   const uint32_t code_bytes = 64u * (I / 2);
+  const int gfirst = q0 / geo.tiles;
+  const int glast = q1 > q0 ? (q1 - 1) / geo.tiles : gfirst - 1;
 
   if (warp == kDnConsumers) {
     if (lane != 0) return;
     int chunk = 0;
     for (int q = q0; q < q1 && !abort_s; ++q, ++chunk) {
       const int gi = q / geo.tiles, ht = q % geo.tiles;
-      const int e = ws.grp_expert[gi];
+      const int e = __ldg(&ws.gmeta[gi].expert);
       const int s = chunk % geo.stages, n = chunk / geo.stages;
       if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
         record_status(ws.ctl, kStTimeout);
@@ -398,68 +453,58 @@ __global__ void __launch_bounds__(kDnThreads, 1)
 
   const int g = lane >> 2, c = lane & 3;
   const int ncons = kDnConsumers * 32;
-  // Stage h as the f16 operand: rows = perm slots (resident) or the group's slots.
-  auto stage_h = [&](int row, int slot, int e) {
-    // one warp per row
-    unsigned char* dst = hs + (size_t)row * geo.h_stride;
+  const int nmeta = glast - gfirst + 1;
+  if (nmeta > 0) stage_meta(meta, ws.gmeta, gfirst, nmeta < geo.meta_cap ? nmeta : geo.meta_cap,
+                            tid, ncons);
+  // Stage h as the f16 operand: per-row factors first, then every (row, word) in one sweep so
+  // that all loads are in flight together.
+  auto row_factor = [&](int row, int slot, float sd) {
     if (mode == 0) {
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(ws.h16 + (size_t)slot * I);
-      float m = 0.0f;
-      for (int i = lane; i < I / 2; i += 32) {
-        const uint32_t v = src[i];
-        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(v << 16)), fabsf(__uint_as_float(v & 0xFFFF0000u))));
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-      int sh = 0;
-      if (m > 0.0f) {
-        int ex;
-        frexpf(m, &ex);
-        sh = ex - 15;
-        sh = sh < -110 ? -110 : (sh > 110 ? 110 : sh);
-      }
-      const float f = __int_as_float((127 - sh) << 23);
-      for (int i = lane; i < I / 2; i += 32) {
-        const uint32_t v = src[i];
-        const __half2 h2 = __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), f),
-                                             __fmul_rn(__uint_as_float(v & 0xFFFF0000u), f));
-        *reinterpret_cast<__half2*>(dst + i * 4) = h2;
-      }
-      if (lane == 0) hfac[row] = __int_as_float((127 + sh) << 23);
+      // BF16 h scaled by 2^-s puts the slot's amax in [2^14, 2^15): exact in f16
+      hfac[row] = __int_as_float((127 + amax_shift(__uint_as_float(ws.slot_amax[slot]))) << 23);
     } else {
-      const uint8_t* cq = ws.hq + (size_t)slot * (I / 2);
-      const uint8_t* sq = ws.hsf + (size_t)slot * (I / 16);
-      for (int i = lane; i < I / 2; i += 32) {
-        const uint32_t byte = cq[i];
-        const float sv = e4m3_value_nonneg(sq[i / 8]);
-        const __half2 h2 = __floats2half2_rn(e2m1_value(byte & 0xF) * sv, e2m1_value(byte >> 4) * sv);
-        *reinterpret_cast<__half2*>(dst + i * 4) = h2;
-      }
-      if (lane == 0) hfac[row] = pk.down_in_scale[e];
+      hfac[row] = sd;
+    }
+  };
+  auto stage_word = [&](int row, int slot, int i) {
+    unsigned char* dst = hs + (size_t)row * geo.h_stride + i * 4;
+    if (mode == 0) {
+      const float f = 1.0f / hfac[row];  // exact: a power of two
+      const uint32_t v = reinterpret_cast<const uint32_t*>(ws.h16 + (size_t)slot * I)[i];
+      *reinterpret_cast<__half2*>(dst) =
+          __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), f),
+                            __fmul_rn(__uint_as_float(v & 0xFFFF0000u), f));
+    } else {
+      const uint32_t byte = ws.hq[(size_t)slot * (I / 2) + i];
+      const float sv = e4m3_value_nonneg(ws.hsf[(size_t)slot * (I / 16) + i / 8]);
+      *reinterpret_cast<__half2*>(dst) =
+          __floats2half2_rn(e2m1_value(byte & 0xF) * sv, e2m1_value(byte >> 4) * sv);
     }
   };
   if (h_resident) {
-    const int S = ws.T * ws.k;
-    for (int sl = warp; sl < S; sl += kDnConsumers) {
-      // expert of the slot: the group that contains it
-      int e = 0;
-      for (int gi = 0; gi < G; ++gi)
-        if (sl >= ws.grp_slot[gi] && sl < ws.grp_slot[gi] + ws.grp_n[gi]) e = ws.grp_expert[gi];
-      stage_h(sl, sl, e);
+    for (int gi = tid; gi < G; gi += ncons) {
+      const GroupMeta& gm = ws.gmeta[gi];
+      const int s0 = gm.slot0, nn = gm.n;
+      const float sd = gm.sd;
+      for (int r = 0; r < nn; ++r) row_factor(s0 + r, s0 + r, sd);
     }
     consumer_sync(ncons);
+    const int S = ws.T * ws.k;
+    for (int i = tid; i < S * (I / 2); i += ncons) stage_word(i / (I / 2), i / (I / 2), i % (I / 2));
   }
+  consumer_sync(ncons);
   int chunk = 0;
   for (int q = q0; q < q1; ++q, ++chunk) {
     const int gi = q / geo.tiles, ht = q % geo.tiles;
-    const int e = ws.grp_expert[gi];
-    const int slot0 = ws.grp_slot[gi];
-    const int n = ws.grp_n[gi];
+    const int mi = gi - gfirst;
+    const GroupMeta& gm = (mi < geo.meta_cap) ? meta[mi] : ws.gmeta[gi];
+    const int slot0 = gm.slot0, n = gm.n;
     if (!h_resident && gi != cur_group_s) {
       consumer_sync(ncons);
-      for (int r = warp; r < kGroup; r += kDnConsumers) {
-        if (r < n) stage_h(r, slot0 + r, e);
-      }
+      if (tid < n) row_factor(tid, slot0 + tid, gm.sd);
+      consumer_sync(ncons);
+      for (int i = tid; i < n * (I / 2); i += ncons)
+        stage_word(i / (I / 2), slot0 + i / (I / 2), i % (I / 2));
       consumer_sync(ncons);
       if (tid == 0) cur_group_s = gi;
     }
@@ -490,7 +535,7 @@ __global__ void __launch_bounds__(kDnThreads, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    const float md = pk.mult[e * 3 + 2];
+    const float md = gm.md;
 #pragma unroll
     for (int q2 = 0; q2 < 4; ++q2) {
       const int col = 2 * c + (q2 & 1);
@@ -506,6 +551,8 @@ __global__ void __launch_bounds__(kDnThreads, 1)
 
 // ------------------------------------------------------------------ combine
 // out[t][r] = BF16( sum_{j=0..k-1} w[t][j] * Y[slot_of[t][j]][r] ), FP32, j in rank order.
+// All k weight/slot loads are issued before the Y loads (no dependent load chain per j).
+
 __global__ void __launch_bounds__(256) k_combine(WsView ws, uint16_t* __restrict__ out) {
   pdl_wait();
   pdl_launch_dependents();
@@ -515,15 +562,30 @@ __global__ void __launch_bounds__(256) k_combine(WsView ws, uint16_t* __restrict
        it += (long long)gridDim.x * 256) {
     const int t = (int)(it / (H / 8)), r8 = (int)(it % (H / 8));
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const float wj = ws.w[(size_t)t * k + j];
-      const int slot = ws.slot_of[(size_t)t * k + j];
-      const uint4 v = reinterpret_cast<const uint4*>(ws.y + (size_t)slot * H)[r8];
-      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      // the weights and slots of 8 ranks, then their 8 Y loads, all issued before use
+      float wj[8];
+      int sj[8];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[2 * q] += wj * __uint_as_float(wd[q] << 16);
-        acc[2 * q + 1] += wj * __uint_as_float(wd[q] & 0xFFFF0000u);
+      for (int q = 0; q < 8; ++q) {
+        const bool ok = j0 + q < k;
+        wj[q] = ok ? ws.w[(size_t)t * k + j0 + q] : 0.0f;
+        sj[q] = ok ? ws.slot_of[(size_t)t * k + j0 + q] : -1;
+      }
+      uint4 v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[q] = sj[q] >= 0 ? reinterpret_cast<const uint4*>(ws.y + (size_t)sj[q] * H)[r8]
+                          : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (sj[q] < 0) break;   // ranks in order: stop at the first past k
+        const uint32_t wd[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          acc[2 * u] += wj[q] * __uint_as_float(wd[u] << 16);
+          acc[2 * u + 1] += wj[q] * __uint_as_float(wd[u] & 0xFFFF0000u);
+        }
       }
     }
     uint32_t o[4];
@@ -546,16 +608,18 @@ __global__ void k_pack_scales(const uint8_t* __restrict__ rg, const uint8_t* __r
   for (long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x; o < n_gu + n_dn;
        o += (long long)gridDim.x * blockDim.x) {
     if (o < n_gu) {
+      // [mat][E][I/16][H/128][c 4][g 8][4]: byte 2h + b = row 16*tile + g + 8h, block 8J+2c+b
       long long r = o;
+      const int b = (int)(r & 1); r >>= 1;
       const int h = (int)(r & 1); r >>= 1;
       const int g = (int)(r & 7); r >>= 3;
       const int c = (int)(r & 3); r >>= 2;
-      const int j = (int)(r % (H / 64)); r /= (H / 64);
+      const int J = (int)(r % (H / 128)); r /= (H / 128);
       const int tile = (int)(r % (I / 16)); r /= (I / 16);
       const int e = (int)(r % E); r /= E;
       const int mat = (int)r;
       const int row = tile * 16 + g + 8 * h;
-      const int blk = 4 * j + c;
+      const int blk = 8 * J + 2 * c + b;
       const size_t src = ((size_t)e * I + row) * (H / 16) + blk;
       if (!inverse) {
         gu[o] = (mat == 0 ? rg : ru)[src];
@@ -612,7 +676,7 @@ size_t down_smem_bytes(int I, bool h_resident, int slots) {
 cudaError_t launch_gateup(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
                           bool x_resident) {
   const GuGeom geo = gu_geom(pk.H, pk.I, x_resident, ws.T);
-  if (geo.stages < 2) return cudaErrorInvalidConfiguration;
+  if (geo.stages < 1) return cudaErrorInvalidConfiguration;
   const size_t smem = gu_smem(geo);
   cudaError_t e =
       cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

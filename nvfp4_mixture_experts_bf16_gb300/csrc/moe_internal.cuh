@@ -30,8 +30,20 @@ enum : int {
   kCtlWords = 64
 };
 
+// Per token group (<= 8 tokens of one expert): everything the expert kernels need about it,
+// written by the routing stage so that the expert kernels stage it with one load.
+struct GroupMeta {
+  int32_t expert, slot0, n, pad0;
+  int32_t tok[8];        // token ids of the group's columns (-1 past n)
+  float mg, mu, md, sd;  // gate/up/down multipliers, down input scale
+  float i6d, pad1, pad2, pad3;  // fl32(1/fl32(6*sd))
+};
+static_assert(sizeof(GroupMeta) == 80, "GroupMeta layout");
+
 struct WsView {
   uint32_t* ctl;
+  GroupMeta* gmeta;    // [G]
+  uint32_t* slot_amax; // [T*k] bits of max|h| per slot (W4A16), zeroed by the routing stage
   float* logits;       // [T][E]
   int32_t* idx;        // [T][k]
   float* w;            // [T][k]
@@ -57,8 +69,8 @@ struct WsView {
 // ------------------------------------------------------------------ pack view
 // Codes keep the checkpoint layout ([rows][cols/2] per matrix, experts contiguous).
 // Scales are stored in the "fragment" order the narrow/grouped kernels read:
-//   gate/up: [mat(2)][E][I/16 row tiles][H/64 k-blocks][c(4)][g(8)][2]
-//            byte (c, g, h) of k-block j is the scale of row 16*tile + g + 8h, block 4j + c.
+//   gate/up: [mat(2)][E][I/16 row tiles][H/128 k-blocks][c(4)][g(8)][4]
+//            bytes (c, g, 2h + b) of k-block J: the scale of row 16*tile + g + 8h, block 8J+2c+b.
 //   down:    [E][H/64 row tiles][4 m16 tiles][I/64 k-blocks][c(4)][g(8)][2]
 struct PackView {
   const uint8_t* gate_codes;   // [E][I][H/2]
@@ -279,6 +291,41 @@ __device__ __forceinline__ void kblock_mma(float (&acc)[4], uint2 rowg, uint2 ro
   }
 }
 
+// The product of one 128-wide k-block for one m16 row tile and one 8-token group:
+//   rowg / rowg8: the thread's 16 code bytes of rows g and g+8 (codes k = 128J + 32c .. +31),
+//   sc4:          scale bytes (row g, block 2c), (row g, block 2c+1), (row g+8, 2c), (row g+8, 2c+1),
+//   xb[p]:        the thread's B operand x[g][128J + 32c + 8p .. +7], p = 0..3.
+// MMA m (0..7) holds k = 128J + 32c + 4m + {0,1,2,3}: the k order inside an MMA is permuted
+// consistently for A and B so that each operand comes from contiguous bytes.
+__device__ __forceinline__ void kblock128_mma(float (&acc)[4], const uint4& rowg, const uint4& rowg8,
+                                              uint32_t sc4, const uint4 (&xb)[4]) {
+  const uint32_t s_g0 = e4m3_bcast_f16x2(sc4 & 0xFFu);
+  const uint32_t s_g1 = e4m3_bcast_f16x2((sc4 >> 8) & 0xFFu);
+  const uint32_t s_h0 = e4m3_bcast_f16x2((sc4 >> 16) & 0xFFu);
+  const uint32_t s_h1 = e4m3_bcast_f16x2(sc4 >> 24);
+  const uint32_t gw[4] = {rowg.x, rowg.y, rowg.z, rowg.w};
+  const uint32_t hw[4] = {rowg8.x, rowg8.y, rowg8.z, rowg8.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {   // word w = codes 8w..8w+7 -> MMAs 2w, 2w+1
+    uint32_t gf[4], hf[4];
+    e2m1x8_to_f16x2x4(gw[w], gf);
+    e2m1x8_to_f16x2x4(hw[w], hf);
+    const uint32_t sg = (w < 2) ? s_g0 : s_g1;
+    const uint32_t sh = (w < 2) ? s_h0 : s_h1;
+    const uint4& xv = xb[w];
+    {
+      uint32_t a[4] = {hmul2_u32(gf[0], sg), hmul2_u32(hf[0], sh), hmul2_u32(gf[1], sg),
+                       hmul2_u32(hf[1], sh)};
+      mma_16816(acc, a, xv.x, xv.y);
+    }
+    {
+      uint32_t a[4] = {hmul2_u32(gf[2], sg), hmul2_u32(hf[2], sh), hmul2_u32(gf[3], sg),
+                       hmul2_u32(hf[3], sh)};
+      mma_16816(acc, a, xv.z, xv.w);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ launchers
 struct LaunchCfg {
   cudaStream_t stream;
@@ -287,11 +334,12 @@ struct LaunchCfg {
 };
 
 cudaError_t launch_route_narrow(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
-                                const WsView& ws, int mode, float xS, float x_inv6S,
+                                const WsView& ws, const PackView* pk, int mode, float xS,
+                                float x_inv6S,
                                 int32_t* out_idx, float* out_w, int32_t* out_counts,
                                 int32_t* out_offsets, int32_t* out_perm);
 cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
-                              const WsView& ws, int32_t* out_idx, float* out_w,
+                              const WsView& ws, const PackView* pk, int32_t* out_idx, float* out_w,
                               int32_t* out_counts, int32_t* out_offsets, int32_t* out_perm,
                               int* launches);
 cudaError_t launch_xprep_wide(const LaunchCfg& lc, const uint16_t* x, const WsView& ws, int mode,

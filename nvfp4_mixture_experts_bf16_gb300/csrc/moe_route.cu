@@ -155,10 +155,34 @@ __device__ int block_exclusive_scan(int32_t* a, int n, int32_t* scratch /*[8]*/)
 // ------------------------------------------------------------------ narrow router
 constexpr int kRouteRows = 4;  // router rows per CTA (2 warps per row, one per half of H)
 
+// Fill the record of group u (expert e, slots [slot0, slot0 + n)); pk may be null (routing only).
+__device__ __forceinline__ void write_group(const WsView& ws, const PackView* pk, int u, int e,
+                                            int slot0, int n, const int32_t* perm_s) {
+  GroupMeta m;
+  m.expert = e;
+  m.slot0 = slot0;
+  m.n = n;
+  m.pad0 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m.tok[i] = (perm_s && i < n) ? perm_s[slot0 + i] : -1;
+  if (pk) {
+    m.mg = pk->mult[e * 3 + 0];
+    m.mu = pk->mult[e * 3 + 1];
+    m.md = pk->mult[e * 3 + 2];
+    m.sd = pk->down_in_scale[e];
+    m.i6d = pk->down_inv6S[e];
+  } else {
+    m.mg = m.mu = m.md = m.sd = m.i6d = 0.0f;
+  }
+  m.pad1 = m.pad2 = m.pad3 = 0.0f;
+  ws.gmeta[u] = m;
+}
+
 __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict__ x,
                                                       const uint16_t* __restrict__ wr, WsView ws,
-                                                      int mode, float xS, float x_inv6S,
-                                                      RouteOut out) {
+                                                      PackView pkv, int has_pack, int mode,
+                                                      float xS, float x_inv6S, RouteOut out) {
+  const PackView* pk = has_pack ? &pkv : nullptr;
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ float part[kRouteRows][2][kNarrowT];
   __shared__ int shift_s[kNarrowT];
@@ -269,6 +293,7 @@ __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict
   float* sel_w = sel_val + S;                                         // [S]
   int32_t* cnt = reinterpret_cast<int32_t*>(sel_w + S);               // [E+1]
   int32_t* uq = cnt + (E + 1);                                        // [E+1]
+  int32_t* perm_s = uq + (E + 1);                                     // [S]
 
   for (int i = tid; i < T * E; i += 256) lg[i] = __ldcg(ws.logits + i);
   for (int e = tid; e <= E; e += 256) cnt[e] = 0;
@@ -291,13 +316,6 @@ __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict
   for (int e = tid; e < E; e += 256) {
     out.offsets[e] = cnt[e];
     ws.offsets[e] = cnt[e];
-    const int c = ((e + 1 < E) ? cnt[e + 1] : S) - cnt[e];
-    if (c > 0) {
-      const int u = uq[e];
-      ws.grp_expert[u] = e;
-      ws.grp_slot[u] = cnt[e];
-      ws.grp_n[u] = c;
-    }
   }
   if (tid == 0) {
     out.offsets[E] = S;
@@ -310,6 +328,7 @@ __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict
     int rank = 0;
     for (int s2 = 0; s2 < t * k; ++s2) rank += (sel_idx[s2] == e) ? 1 : 0;
     const int pos = cnt[e] + rank;
+    perm_s[pos] = t;
     out.perm[pos] = t;
     ws.perm[pos] = t;
     ws.slot_of[tid] = pos;
@@ -317,6 +336,19 @@ __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict
     out.w[tid] = sel_w[tid];
     ws.idx[tid] = e;
     ws.w[tid] = sel_w[tid];
+    if (ws.slot_amax) ws.slot_amax[tid] = 0u;
+  }
+  __syncthreads();
+  // one group per distinct expert (a narrow call has at most 8 tokens per expert)
+  for (int e = tid; e < E; e += 256) {
+    const int c = ((e + 1 < E) ? cnt[e + 1] : S) - cnt[e];
+    if (c > 0) {
+      const int u = uq[e];
+      ws.grp_expert[u] = e;
+      ws.grp_slot[u] = cnt[e];
+      ws.grp_n[u] = c;
+      write_group(ws, pk, u, e, cnt[e], c, perm_s);
+    }
   }
   if (tid == 0) ws.ctl[kCtlRouteTicket] = 0u;
 }
@@ -476,7 +508,9 @@ __global__ void __launch_bounds__(256) k_hist_wide(WsView ws) {
 }
 
 // One CTA of 1024 threads: per-expert chunk prefix sums, offsets, and the token groups.
-__global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, RouteOut out, int nchunk) {
+__global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, PackView pkv, int has_pack,
+                                                    RouteOut out, int nchunk) {
+  const PackView* pk = has_pack ? &pkv : nullptr;
   __shared__ int32_t tot[1024 + 1];
   __shared__ int32_t wsum[32];
   const int E = ws.E;
@@ -522,8 +556,12 @@ __global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, RouteOut out, int
       ws.grp_expert[gbase + q] = e;
       ws.grp_slot[gbase + q] = off_e + q * kGroup;
       ws.grp_n[gbase + q] = min(kGroup, cnt_e - q * kGroup);
+      write_group(ws, pk, gbase + q, e, off_e + q * kGroup, min(kGroup, cnt_e - q * kGroup),
+                  nullptr);
     }
   }
+  if (ws.slot_amax)
+    for (int i = e; i < ws.T * ws.k; i += 1024) ws.slot_amax[i] = 0u;
   if (e == 0) {
     out.offsets[E] = ta;
     ws.offsets[E] = ta;
@@ -629,28 +667,30 @@ cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t
 
 size_t route_narrow_smem_bytes(int T, int H, int E, int k) {
   const size_t xbytes = (size_t)T * H * 2;
-  const size_t fin = (size_t)T * E * 4 + (size_t)T * k * 12 + (size_t)(E + 1) * 8 + 64;
+  const size_t fin = (size_t)T * E * 4 + (size_t)T * k * 16 + (size_t)(E + 1) * 8 + 64;
   return xbytes > fin ? xbytes : fin;
 }
 
 cudaError_t launch_route_narrow(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
-                                const WsView& ws, int mode, float xS, float x_inv6S,
-                                int32_t* out_idx, float* out_w, int32_t* out_counts,
+                                const WsView& ws, const PackView* pk, int mode, float xS,
+                                float x_inv6S, int32_t* out_idx, float* out_w, int32_t* out_counts,
                                 int32_t* out_offsets, int32_t* out_perm) {
+  const PackView pkv = pk ? *pk : PackView{};
   const size_t smem = route_narrow_smem_bytes(ws.T, ws.H, ws.E, ws.k);
   cudaError_t e = cudaFuncSetAttribute(k_route_narrow, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   RouteOut out{out_idx, out_w, out_counts, out_offsets, out_perm};
   const int grid = (ws.E + kRouteRows - 1) / kRouteRows;
-  return launch(lc, k_route_narrow, dim3(grid), dim3(256), smem, x, wr, ws, mode, xS, x_inv6S,
-                out);
+  return launch(lc, k_route_narrow, dim3(grid), dim3(256), smem, x, wr, ws, pkv, pk ? 1 : 0,
+                mode, xS, x_inv6S, out);
 }
 
 cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
-                              const WsView& ws, int32_t* out_idx, float* out_w,
+                              const WsView& ws, const PackView* pk, int32_t* out_idx, float* out_w,
                               int32_t* out_counts, int32_t* out_offsets, int32_t* out_perm,
                               int* launches) {
+  const PackView pkv = pk ? *pk : PackView{};
   RouteOut out{out_idx, out_w, out_counts, out_offsets, out_perm};
   cudaError_t e;
   dim3 gg((ws.E + kGN - 1) / kGN, (ws.T + kGM - 1) / kGM);
@@ -664,7 +704,7 @@ cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint
   const int nchunk = (ws.T + kChunkTok - 1) / kChunkTok;
   e = launch(lc, k_hist_wide, dim3(nchunk), dim3(256), (size_t)ws.E * 4, ws);
   if (e != cudaSuccess) return e;
-  e = launch(lc, k_scan_wide, dim3(1), dim3(1024), 0, ws, out, nchunk);
+  e = launch(lc, k_scan_wide, dim3(1), dim3(1024), 0, ws, pkv, pk ? 1 : 0, out, nchunk);
   if (e != cudaSuccess) return e;
   e = launch(lc, k_scatter_wide, dim3(nchunk), dim3(256), (size_t)kChunkTok * ws.k * 4, ws, out);
   if (launches) *launches += 5;

@@ -99,6 +99,9 @@ class FullLayer:
         """ExpertSet with the given experts, quantised by the oracle from the same BF16 draws;
         asserts bit equality with the product quantiser's codes."""
         ex = oracle.ExpertSet(self.E, self.H, self.I)
+        ex.in_scale[:, 0] = self.xs       # every expert carries the layer's input scales, also
+        ex.in_scale[:, 1] = self.xs       # the ones that are not supplied
+        ex.in_scale[:, 2] = self.ds
         for e in sorted(set(int(v) for v in experts)):
             got = {}
             for w in ("gate", "up", "down"):
