@@ -66,9 +66,10 @@ int num_sms_of_current_device() {
 
 struct WsLayout {
   size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm, grp_expert, grp_slot, grp_n,
-      chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, total;
+      chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
+      xsf_atoms, hq_perm, hsf_atoms, total;
   size_t slot_amax_bytes;
-  int G;
+  int G, NT;
 };
 
 // mode: 0 W4A16, 1 W4A4, -1 routing only (no expert buffers).
@@ -102,6 +103,18 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
   L.hq = take(mode == 1 ? (size_t)S * I / 2 : 0);
   L.hsf = take(mode == 1 ? (size_t)S * I / 16 : 0);
   L.y = take(mode >= 0 ? (size_t)S * H * 2 : 0);
+  // grouped tensor-core path (wide W4A4): 128-slot token tiles in a padded permuted space
+  const bool tc = mode == 1 && T > moe::kNarrowT;
+  L.NT = tc ? (int)((S + 127) / 128 + (S < E ? S : E)) : 0;
+  const size_t P = (size_t)L.NT * 128;
+  L.tt_expert = take((size_t)L.NT * 4);
+  L.tt_slot0 = take((size_t)L.NT * 4);
+  L.tt_n = take((size_t)L.NT * 4);
+  L.ttbase = take(tc ? (size_t)(E + 1) * 4 : 0);
+  L.xq_perm = take(P * H / 2);
+  L.xsf_atoms = take((size_t)L.NT * (H / 64) * 512);
+  L.hq_perm = take(P * I / 2);
+  L.hsf_atoms = take((size_t)L.NT * (I / 64 > 0 ? I / 64 : 1) * 512);
   L.total = o;
   return L;
 }
@@ -131,7 +144,16 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   v.hq = b + L.hq;
   v.hsf = b + L.hsf;
   v.y = reinterpret_cast<uint16_t*>(b + L.y);
-  v.T = T; v.H = H; v.E = E; v.k = k; v.I = I; v.G = L.G;
+  v.T = T; v.H = H; v.E = E; v.k = k; v.I = I; v.G = L.G; v.NT = L.NT;
+  const bool tc = L.NT > 0;
+  v.tt_expert = tc ? reinterpret_cast<int32_t*>(b + L.tt_expert) : nullptr;
+  v.tt_slot0 = reinterpret_cast<int32_t*>(b + L.tt_slot0);
+  v.tt_n = reinterpret_cast<int32_t*>(b + L.tt_n);
+  v.ttbase = reinterpret_cast<int32_t*>(b + L.ttbase);
+  v.xq_perm = b + L.xq_perm;
+  v.xsf_atoms = b + L.xsf_atoms;
+  v.hq_perm = b + L.hq_perm;
+  v.hsf_atoms = b + L.hsf_atoms;
   return v;
 }
 
@@ -191,7 +213,8 @@ moe_status moe_pack_nvfp4(const moe_nvfp4_matrix* gate, const moe_nvfp4_matrix* 
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
   const size_t off_gc = take(mat_codes * E), off_uc = take(mat_codes * E),
                off_dc = take(mat_codes * E), off_gus = take(2 * mat_scales * E),
-               off_ds = take(mat_scales * E), off_mult = take((size_t)E * 12),
+               off_ds = take(mat_scales * E), off_agu = take(2 * mat_scales * E),
+               off_adn = take(mat_scales * E), off_mult = take((size_t)E * 12),
                off_dsc = take((size_t)E * 4), off_dinv = take((size_t)E * 4);
   moe_expert_pack* pk = new (std::nothrow) moe_expert_pack();
   if (!pk) return MOE_ERR_OOM;
@@ -249,7 +272,8 @@ moe_status moe_pack_nvfp4(const moe_nvfp4_matrix* gate, const moe_nvfp4_matrix* 
   pk->x_inv6S = inv6S_of(pk->x_scale);
   if (err == cudaSuccess)
     err = moe::launch_pack_scales(s, raw, raw + E * mat_scales, raw + 2 * E * mat_scales, E, H, I,
-                                  pk->buf + off_gus, pk->buf + off_ds);
+                                  pk->buf + off_gus, pk->buf + off_ds, pk->buf + off_agu,
+                                  pk->buf + off_adn);
   if (err == cudaSuccess)
     err = cudaMemcpyAsync(pk->buf + off_mult, pk->mult_h.data(), (size_t)E * 12,
                           cudaMemcpyHostToDevice, s);
@@ -274,6 +298,8 @@ moe_status moe_pack_nvfp4(const moe_nvfp4_matrix* gate, const moe_nvfp4_matrix* 
   v.mult = reinterpret_cast<const float*>(pk->buf + off_mult);
   v.down_in_scale = reinterpret_cast<const float*>(pk->buf + off_dsc);
   v.down_inv6S = reinterpret_cast<const float*>(pk->buf + off_dinv);
+  v.sfa_gu = pk->buf + off_agu;
+  v.sfa_down = pk->buf + off_adn;
   v.E = E; v.H = H; v.I = I;
   *out = pk;
   return MOE_OK;
@@ -408,17 +434,28 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
   }
   if (e == cudaSuccess) e = prof_mark(lc.stream, 1);
   if (e == cudaSuccess) e = prof_mark(lc.stream, 2);
-  if (e == cudaSuccess) {
-    e = moe::launch_gateup(lc, pack->view, v, m, narrow);
-    n += 1;
-  }
-  if (e == cudaSuccess) e = prof_mark(lc.stream, 3);
-  if (e == cudaSuccess) e = prof_mark(lc.stream, 4);
-  if (e == cudaSuccess) {
-    const long long S = (long long)T * k;
-    const bool h_res = narrow && S * (2LL * I + 16) <= 96 * 1024;
-    e = moe::launch_down(lc, pack->view, v, m, h_res);
-    n += 1;
+  const bool use_tc = !narrow && m == 1 && v.NT > 0 && H % 256 == 0 && moe::tc_supported();
+  if (use_tc) {
+    // x permutation + gate/up + down on tcgen05 (stage 1 covers all three)
+    if (e == cudaSuccess) {
+      e = moe::launch_tc_experts(lc, pack->view, v, pack->x_scale);
+      n += 3;
+    }
+    if (e == cudaSuccess) e = prof_mark(lc.stream, 3);
+    if (e == cudaSuccess) e = prof_mark(lc.stream, 4);
+  } else {
+    if (e == cudaSuccess) {
+      e = moe::launch_gateup(lc, pack->view, v, m, narrow);
+      n += 1;
+    }
+    if (e == cudaSuccess) e = prof_mark(lc.stream, 3);
+    if (e == cudaSuccess) e = prof_mark(lc.stream, 4);
+    if (e == cudaSuccess) {
+      const long long S = (long long)T * k;
+      const bool h_res = narrow && S * (2LL * I + 16) <= 96 * 1024;
+      e = moe::launch_down(lc, pack->view, v, m, h_res);
+      n += 1;
+    }
   }
   if (e == cudaSuccess) e = prof_mark(lc.stream, 5);
   if (e == cudaSuccess) e = prof_mark(lc.stream, 6);

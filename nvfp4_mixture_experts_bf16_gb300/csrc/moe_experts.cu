@@ -49,6 +49,7 @@ struct DnGeom {
   int h_rows;       // slots if resident else 8
   int tiles;        // H / 64
   int meta_cap;
+  int raw_bytes;    // raw h staging area (resident h only)
 };
 
 constexpr int kMetaCap = 8;   // group records staged per CTA (a CTA's task range spans few groups)
@@ -76,22 +77,25 @@ size_t gu_smem(const GuGeom& g) {
          kGuConsumers * 2 * 32 * 16 + g.meta_cap * sizeof(GroupMeta) + 2 * 8 * g.stages + 64;
 }
 
-DnGeom dn_geom(int H, int I, bool h_resident, int slots) {
+DnGeom dn_geom(int H, int I, bool h_resident, int slots, int mode) {
   DnGeom d;
   d.stage_bytes = 64 * (I / 2) + 4 * I;
   d.h_stride = 2 * I + 16;
   d.h_rows = h_resident ? slots : kGroup;
   d.tiles = H / 64;
   d.meta_cap = kMetaCap;
-  const int fixed = d.h_rows * d.h_stride + d.h_rows * 4 + d.meta_cap * (int)sizeof(GroupMeta) + 1024;
+  const int raw = mode == 0 ? slots * I * 2 : slots * (I / 2) + ((slots * (I / 16) + 15) / 16) * 16;
+  d.raw_bytes = h_resident ? raw : 0;
+  const int fixed = d.h_rows * d.h_stride + d.raw_bytes + d.h_rows * 4 +
+                    d.meta_cap * (int)sizeof(GroupMeta) + 1024;
   int st = (kMaxSmem - fixed) / d.stage_bytes;
   d.stages = st > 8 ? 8 : st;
   return d;
 }
 
 size_t dn_smem(const DnGeom& d) {
-  return (size_t)d.stages * d.stage_bytes + (size_t)d.h_rows * d.h_stride + d.h_rows * 4 +
-         d.meta_cap * sizeof(GroupMeta) + 2 * 8 * d.stages + 64;
+  return (size_t)d.stages * d.stage_bytes + (size_t)d.h_rows * d.h_stride + d.raw_bytes +
+         d.h_rows * 4 + d.meta_cap * sizeof(GroupMeta) + 2 * 8 * d.stages + 64;
 }
 
 __device__ __forceinline__ void consumer_sync(int nthreads) {
@@ -152,6 +156,7 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   uint64_t* empty = full + geo.stages;
   __shared__ volatile int abort_s;
   __shared__ int cur_group_s;
+  __shared__ uint64_t xbar;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = pk.H, I = pk.I;
@@ -160,6 +165,7 @@ __global__ void __launch_bounds__(kGuThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kGuConsumers);
     }
+    mbar_init(&xbar, 1);
     fence_mbar_init();
     abort_s = 0;
     cur_group_s = -1;
@@ -178,6 +184,12 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   if (warp == kGuConsumers) {
     // ---------------- producer
     if (lane != 0) return;
+    if (x_resident) {
+      // the T activation rows (already in the permuted operand layout), one copy per row
+      mbar_arrive_expect_tx(&xbar, (uint32_t)ws.T * H * 2);
+      for (int t = 0; t < ws.T; ++t)
+        bulk_g2s(xs + (size_t)t * geo.x_stride, ws.xh + (size_t)t * H, (uint32_t)H * 2, &xbar);
+    }
     int chunk = 0;
     const uint32_t half = geo.row_bytes;
     for (int q = q0; q < q1 && !abort_s; ++q) {
@@ -217,6 +229,7 @@ __global__ void __launch_bounds__(kGuThreads, 1)
       const int c = chunk - 1 - i;
       (void)mbar_wait(&full[c % geo.stages], (c / geo.stages) & 1);
     }
+    if (x_resident) (void)mbar_wait(&xbar, 0);
     return;
   }
 
@@ -226,24 +239,11 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   const int nmeta = glast - gfirst + 1;
   if (nmeta > 0) stage_meta(meta, ws.gmeta, gfirst, nmeta < geo.meta_cap ? nmeta : geo.meta_cap,
                             tid, ncons);
-  // Activation rows in shared memory, permuted inside each 128-wide k-block so that thread c
-  // reads its 32 values as 4 x 16 B: element 128J + 32c + 8p + q -> 128J + 32p + 8c + q.
-  auto stage_x_row = [&](int row, const __half* src, int word0, int step) {
-    unsigned char* dst = xs + (size_t)row * geo.x_stride;
-    for (int w = word0; w < H / 8; w += step) {   // w = 16-B word of the natural row
-      const int J = w >> 4, cc = (w >> 2) & 3, p = w & 3;
-      *reinterpret_cast<uint4*>(dst + J * 256 + p * 64 + cc * 16) =
-          reinterpret_cast<const uint4*>(src)[w];
-    }
-  };
-  if (x_resident) {
-    const int T = ws.T;
-    for (int i = tid; i < T * (H / 8); i += ncons) {
-      const int t = i / (H / 8), w = i % (H / 8);
-      stage_x_row(t, ws.xh + (size_t)t * H, w, H / 8);
-    }
-  }
   consumer_sync(ncons);
+  if (x_resident && !mbar_wait(&xbar, 0)) {
+    record_status(ws.ctl, kStTimeout);
+    abort_s = 1;
+  }
   int chunk = 0;
   const int jb_per_chunk = geo.KC / 128;
   for (int q = q0; q < q1; ++q) {
@@ -253,14 +253,22 @@ __global__ void __launch_bounds__(kGuThreads, 1)
     const int slot0 = gm.slot0, n = gm.n;
     if (!x_resident && gi != cur_group_s) {
       consumer_sync(ncons);
-      for (int i = tid; i < kGroup * (H / 8); i += ncons) {
-        const int r = i / (H / 8), w = i % (H / 8);
-        if (r < n) {
-          stage_x_row(r, ws.xh + (size_t)ws.perm[slot0 + r] * H, w, H / 8);
-        } else {
-          const int J = w >> 4, cc = (w >> 2) & 3, p = w & 3;
-          *reinterpret_cast<uint4*>(xs + (size_t)r * geo.x_stride + J * 256 + p * 64 + cc * 16) =
-              make_uint4(0, 0, 0, 0);
+      // the group's activation rows (already in the permuted operand layout), 4 loads in flight
+      // per thread
+      for (int i0 = tid; i0 < kGroup * (H / 8); i0 += 4 * ncons) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * ncons, r = i / (H / 8), w = i % (H / 8);
+          v[u] = (i < kGroup * (H / 8) && r < n)
+                     ? reinterpret_cast<const uint4*>(ws.xh + (size_t)ws.perm[slot0 + r] * H)[w]
+                     : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * ncons, r = i / (H / 8), w = i % (H / 8);
+          if (i < kGroup * (H / 8))
+            *reinterpret_cast<uint4*>(xs + (size_t)r * geo.x_stride + w * 16) = v[u];
         }
       }
       consumer_sync(ncons);
@@ -394,12 +402,14 @@ __global__ void __launch_bounds__(kDnThreads, 1)
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* stages = smem;
   unsigned char* hs = stages + (size_t)geo.stages * geo.stage_bytes;
-  float* hfac = reinterpret_cast<float*>(hs + (size_t)geo.h_rows * geo.h_stride);
+  unsigned char* raw = hs + (size_t)geo.h_rows * geo.h_stride;
+  float* hfac = reinterpret_cast<float*>(raw + geo.raw_bytes);
   GroupMeta* meta = reinterpret_cast<GroupMeta*>(hfac + geo.h_rows + ((4 - (geo.h_rows & 3)) & 3));
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + geo.meta_cap);
   uint64_t* empty = full + geo.stages;
   __shared__ volatile int abort_s;
   __shared__ int cur_group_s;
+  __shared__ uint64_t hbar;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = pk.H, I = pk.I;
@@ -408,6 +418,7 @@ __global__ void __launch_bounds__(kDnThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kDnConsumers);
     }
+    mbar_init(&hbar, 1);
     fence_mbar_init();
     abort_s = 0;
     cur_group_s = -1;
@@ -424,8 +435,22 @@ __global__ void __launch_bounds__(kDnThreads, 1)
   const int gfirst = q0 / geo.tiles;
   const int glast = q1 > q0 ? (q1 - 1) / geo.tiles : gfirst - 1;
 
+  const int S = ws.T * ws.k;
   if (warp == kDnConsumers) {
     if (lane != 0) return;
+    if (h_resident) {
+      // every slot's raw h in one or two copies (W4A16: BF16 rows; W4A4: codes, then scales)
+      if (mode == 0) {
+        mbar_arrive_expect_tx(&hbar, (uint32_t)S * I * 2);
+        bulk_g2s(raw, ws.h16, (uint32_t)S * I * 2, &hbar);
+      } else {
+        const uint32_t cb = (uint32_t)S * (I / 2);
+        const uint32_t sb = (uint32_t)((S * (I / 16) + 15) / 16) * 16;
+        mbar_arrive_expect_tx(&hbar, cb + sb);
+        bulk_g2s(raw, ws.hq, cb, &hbar);
+        bulk_g2s(raw + cb, ws.hsf, sb, &hbar);
+      }
+    }
     int chunk = 0;
     for (int q = q0; q < q1 && !abort_s; ++q, ++chunk) {
       const int gi = q / geo.tiles, ht = q % geo.tiles;
@@ -448,6 +473,7 @@ __global__ void __launch_bounds__(kDnThreads, 1)
       const int c2 = chunk - 1 - i;
       (void)mbar_wait(&full[c2 % geo.stages], (c2 / geo.stages) & 1);
     }
+    if (h_resident) (void)mbar_wait(&hbar, 0);
     return;
   }
 
@@ -488,9 +514,28 @@ __global__ void __launch_bounds__(kDnThreads, 1)
       const float sd = gm.sd;
       for (int r = 0; r < nn; ++r) row_factor(s0 + r, s0 + r, sd);
     }
+    if (!mbar_wait(&hbar, 0)) {
+      record_status(ws.ctl, kStTimeout);
+      abort_s = 1;
+    }
     consumer_sync(ncons);
-    const int S = ws.T * ws.k;
-    for (int i = tid; i < S * (I / 2); i += ncons) stage_word(i / (I / 2), i / (I / 2), i % (I / 2));
+    // convert the raw copy to the f16 operand rows, shared memory to shared memory
+    for (int i = tid; i < S * (I / 2); i += ncons) {
+      const int row = i / (I / 2), w = i % (I / 2);
+      unsigned char* dst = hs + (size_t)row * geo.h_stride + w * 4;
+      if (mode == 0) {
+        const float f = 1.0f / hfac[row];  // exact: a power of two
+        const uint32_t v = reinterpret_cast<const uint32_t*>(raw)[i];
+        *reinterpret_cast<__half2*>(dst) =
+            __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), f),
+                              __fmul_rn(__uint_as_float(v & 0xFFFF0000u), f));
+      } else {
+        const uint32_t byte = raw[i];
+        const float sv = e4m3_value_nonneg(raw[(size_t)S * (I / 2) + (size_t)row * (I / 16) + w / 8]);
+        *reinterpret_cast<__half2*>(dst) =
+            __floats2half2_rn(e2m1_value(byte & 0xF) * sv, e2m1_value(byte >> 4) * sv);
+      }
+    }
   }
   consumer_sync(ncons);
   int chunk = 0;
@@ -647,6 +692,36 @@ __global__ void k_pack_scales(const uint8_t* __restrict__ rg, const uint8_t* __r
   }
 }
 
+// checkpoint scales -> tensor-core scale-factor atoms (see PackView).
+__global__ void k_pack_sf_atoms(const uint8_t* __restrict__ rg, const uint8_t* __restrict__ ru,
+                                const uint8_t* __restrict__ rd, int E, int H, int I,
+                                uint8_t* __restrict__ at_gu, uint8_t* __restrict__ at_dn) {
+  const long long n_gu = (long long)E * (I / 64) * (H / 64) * 512;
+  const long long n_dn = (long long)E * (H / 128) * (I / 64) * 512;
+  for (long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x; o < n_gu + n_dn;
+       o += (long long)gridDim.x * blockDim.x) {
+    const bool gu = o < n_gu;
+    long long q = gu ? o : o - n_gu;
+    const int byte = (int)(q & 511); q >>= 9;
+    const int r = (byte >> 4) + 32 * ((byte & 15) >> 2);   // row inside the 128-row tile
+    const int b = byte & 3;                                // block inside the K step
+    if (gu) {
+      const int ks = (int)(q % (H / 64)); q /= (H / 64);
+      const int mt = (int)(q % (I / 64)); q /= (I / 64);
+      const int e = (int)q;
+      const int row = mt * 64 + (r & 63);
+      const uint8_t* src = r < 64 ? rg : ru;
+      at_gu[o] = src[((size_t)e * I + row) * (H / 16) + ks * 4 + b];
+    } else {
+      const int ks = (int)(q % (I / 64)); q /= (I / 64);
+      const int mt = (int)(q % (H / 128)); q /= (H / 128);
+      const int e = (int)q;
+      const int row = mt * 128 + r;
+      at_dn[o - n_gu] = rd[((size_t)e * H + row) * (I / 16) + ks * 4 + b];
+    }
+  }
+}
+
 template <typename Kern, typename... Args>
 cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
                    Args... args) {
@@ -670,7 +745,7 @@ size_t gateup_smem_bytes(int H, bool x_resident, int T) {
 }
 
 size_t down_smem_bytes(int I, bool h_resident, int slots) {
-  return dn_smem(dn_geom(64, I, h_resident, slots));
+  return dn_smem(dn_geom(64, I, h_resident, slots, 0));
 }
 
 cudaError_t launch_gateup(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
@@ -690,7 +765,11 @@ cudaError_t launch_gateup(const LaunchCfg& lc, const PackView& pk, const WsView&
 
 cudaError_t launch_down(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
                         bool h_resident) {
-  const DnGeom geo = dn_geom(pk.H, pk.I, h_resident, ws.T * ws.k);
+  DnGeom geo = dn_geom(pk.H, pk.I, h_resident, ws.T * ws.k, mode);
+  if (h_resident && geo.stages < 2) {  // not enough room to keep every slot's h: stage per group
+    h_resident = false;
+    geo = dn_geom(pk.H, pk.I, false, ws.T * ws.k, mode);
+  }
   if (geo.stages < 2) return cudaErrorInvalidConfiguration;
   const size_t smem = dn_smem(geo);
   cudaError_t e =
@@ -714,9 +793,12 @@ cudaError_t launch_combine(const LaunchCfg& lc, const WsView& ws, uint16_t* out)
 
 cudaError_t launch_pack_scales(cudaStream_t s, const uint8_t* raw_gate, const uint8_t* raw_up,
                                const uint8_t* raw_down, int E, int H, int I, uint8_t* gu_scales,
-                               uint8_t* down_scales) {
+                               uint8_t* down_scales, uint8_t* sfa_gu, uint8_t* sfa_down) {
   k_pack_scales<<<1024, 256, 0, s>>>(raw_gate, raw_up, raw_down, E, H, I, gu_scales, down_scales,
                                      0, -1, -1, nullptr);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || H % 128) return e;
+  k_pack_sf_atoms<<<1024, 256, 0, s>>>(raw_gate, raw_up, raw_down, E, H, I, sfa_gu, sfa_down);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@ enum : int {
   kCtlStatus = 1,       // first device error (sticky until read by the host)
   kCtlGroups = 2,       // number of token groups of the current call
   kCtlUnique = 3,       // number of distinct experts of the current call
+  kCtlTokenTiles = 4,   // number of 128-slot token tiles (grouped tensor-core path)
   kCtlWords = 64
 };
 
@@ -63,7 +64,17 @@ struct WsView {
   uint8_t* hq;         // [T*k][I/2] W4A4 h codes
   uint8_t* hsf;        // [T*k][I/16] W4A4 h scales
   uint16_t* y;         // [T*k][H] BF16 expert outputs
-  int T, H, E, k, I, G;
+  // grouped tensor-core path: token tiles of <= 128 slots of one expert; tile j occupies padded
+  // rows ("pslots") 128j .. 128j+127 of the permuted operands
+  int32_t* tt_expert;  // [NT]
+  int32_t* tt_slot0;   // [NT] first (unpadded) slot of the tile
+  int32_t* tt_n;       // [NT] slots in the tile (1..128)
+  int32_t* ttbase;     // [E+1] first token tile of each expert
+  uint8_t* xq_perm;    // [128*NT][H/2]  activation codes by pslot (W4A4)
+  uint8_t* xsf_atoms;  // [NT][H/64][512] activation scales in tensor-core scale-factor atoms
+  uint8_t* hq_perm;    // [128*NT][I/2]  h codes by pslot
+  uint8_t* hsf_atoms;  // [NT][I/64][512]
+  int T, H, E, k, I, G, NT;
 };
 
 // ------------------------------------------------------------------ pack view
@@ -81,6 +92,12 @@ struct PackView {
   const float* mult;           // [E][3]
   const float* down_in_scale;  // [E]
   const float* down_inv6S;     // [E] fl32(1 / fl32(6 * S_down))
+  // tensor-core scale-factor atoms (512 B = 128 rows x 4 blocks of 16; byte
+  // (r % 32) * 16 + (r / 32) * 4 + b), one per (row tile, K step of 64):
+  //   sfa_gu:   [E][I/64][H/64]: rows 0..63 = gate rows 64*mt.., rows 64..127 = the up rows
+  //   sfa_down: [E][H/128][I/64]
+  const uint8_t* sfa_gu;
+  const uint8_t* sfa_down;
   int E, H, I;
 };
 
@@ -353,7 +370,10 @@ cudaError_t launch_down(const LaunchCfg& lc, const PackView& pk, const WsView& w
 cudaError_t launch_combine(const LaunchCfg& lc, const WsView& ws, uint16_t* out);
 cudaError_t launch_pack_scales(cudaStream_t s, const uint8_t* raw_gate, const uint8_t* raw_up,
                                const uint8_t* raw_down, int E, int H, int I, uint8_t* gu_scales,
-                               uint8_t* down_scales);
+                               uint8_t* down_scales, uint8_t* sfa_gu, uint8_t* sfa_down);
+// Grouped tensor-core experts (W4A4, wide calls): activation permutation, gate/up, down.
+bool tc_supported();
+cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws, float xS);
 cudaError_t launch_unpack_scales(cudaStream_t s, const uint8_t* gu_scales,
                                  const uint8_t* down_scales, int E, int H, int I, int expert,
                                  int which, uint8_t* raw_out);

@@ -78,9 +78,12 @@ __device__ __forceinline__ void prep_block(const uint16_t* xrow, int b, int t, c
     for (int i = 0; i < 16; ++i)
       hv[i] = __float2half_rn(e2m1_value((codes[i >> 3] >> (4 * (i & 7))) & 0xF) * sfv);
   }
-  uint4* dst = reinterpret_cast<uint4*>(ws.xh + (size_t)t * H + b * 16);
-  dst[0] = *reinterpret_cast<uint4*>(&hv[0]);
-  dst[1] = *reinterpret_cast<uint4*>(&hv[8]);
+  // permuted inside each 128-wide k-block: element 128J + 32c + 8p + q is stored at
+  // 128J + 32p + 8c + q, so that the expert kernels read a thread's 32 values as 4 x 16 B
+  const int J = b >> 3, c = (b & 7) >> 1, p0 = 2 * (b & 1);
+  __half* row = ws.xh + (size_t)t * H + J * 128 + 8 * c;
+  *reinterpret_cast<uint4*>(row + 32 * p0) = *reinterpret_cast<uint4*>(&hv[0]);
+  *reinterpret_cast<uint4*>(row + 32 * (p0 + 1)) = *reinterpret_cast<uint4*>(&hv[8]);
 }
 
 // Warp-level top-k of one token's logits held in shared memory (entries are overwritten with
@@ -178,6 +181,7 @@ __device__ __forceinline__ void write_group(const WsView& ws, const PackView* pk
   ws.gmeta[u] = m;
 }
 
+template <int NT>
 __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict__ x,
                                                       const uint16_t* __restrict__ wr, WsView ws,
                                                       PackView pkv, int has_pack, int mode,
@@ -188,61 +192,56 @@ __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict
   __shared__ int shift_s[kNarrowT];
   __shared__ int last_s;
   __shared__ int32_t scan_scratch[8];
+  __shared__ uint64_t bar;
 
-  const int T = ws.T, H = ws.H, E = ws.E, k = ws.k;
+  const int T = NT, H = ws.H, E = ws.E, k = ws.k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                       // [NT][H]
+  const uint16_t* wrs = reinterpret_cast<const uint16_t*>(smem + (size_t)NT * H * 2);  // [4][H]
+  const int row0 = blockIdx.x * kRouteRows;
+  const int nrows = min(kRouteRows, E - row0);
 
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
 
-  // Stage the activations (T x H BF16) in shared memory.
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(x);
-    uint4* dst = reinterpret_cast<uint4*>(xs);
-    for (int i = tid; i < T * H / 8; i += 256) dst[i] = src[i];
+  // Two TMA bulk copies: the activations and this CTA's router rows (contiguous).
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar, (uint32_t)(NT + nrows) * H * 2);
+    bulk_g2s(xs, x, (uint32_t)NT * H * 2, &bar);
+    bulk_g2s(const_cast<uint16_t*>(wrs), wr + (size_t)row0 * H, (uint32_t)nrows * H * 2, &bar);
   }
+  if (!mbar_wait(&bar, 0)) record_status(ws.ctl, kStTimeout);
 
-  // Issue this warp's router loads before waiting for the staged activations.
-  const int row = blockIdx.x * kRouteRows + (warp >> 1);
-  const int half = warp & 1;
-  const int nchunk = H / 16;  // uint4 chunks in half a row
-  constexpr int kMaxChunks = 16;  // H <= 8192
-  uint4 wv[kMaxChunks];
-  if (row < E) {
-    const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)row * H) + half * nchunk;
+  const int r = warp >> 1, half = warp & 1;
+  float acc[NT];
 #pragma unroll
-    for (int i = 0; i < kMaxChunks; ++i)
-      if (lane + 32 * i < nchunk) wv[i] = __ldg(wrow + lane + 32 * i);
-  }
-  __syncthreads();
-
-  float acc[kNarrowT];
+  for (int t = 0; t < NT; ++t) acc[t] = 0.0f;
+  if (r < nrows) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(wrs + (size_t)r * H) + half * (H / 16);
+    const int nchunk = H / 16;  // uint4 chunks in half a row
+#pragma unroll 2
+    for (int i = lane; i < nchunk; i += 32) {
+      const uint4 wv = wrow[i];
 #pragma unroll
-  for (int t = 0; t < kNarrowT; ++t) acc[t] = 0.0f;
-  if (row < E) {
-#pragma unroll
-    for (int i = 0; i < kMaxChunks; ++i) {
-      if (lane + 32 * i < nchunk) {
-#pragma unroll
-        for (int t = 0; t < kNarrowT; ++t) {
-          if (t < T) {
-            const uint4 xv =
-                reinterpret_cast<const uint4*>(xs + (size_t)t * H)[half * nchunk + lane + 32 * i];
-            acc[t] += dot8_bf16(wv[i], xv);
-          }
-        }
+      for (int t = 0; t < NT; ++t) {
+        const uint4 xv = reinterpret_cast<const uint4*>(xs + (size_t)t * H)[half * nchunk + i];
+        acc[t] += dot8_bf16(wv, xv);
       }
     }
   }
 #pragma unroll
-  for (int t = 0; t < kNarrowT; ++t) {
+  for (int t = 0; t < NT; ++t) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], off);
   }
   if (lane == 0) {
 #pragma unroll
-    for (int t = 0; t < kNarrowT; ++t) part[warp >> 1][half][t] = acc[t];
+    for (int t = 0; t < NT; ++t) part[r][half][t] = acc[t];
   }
 
   // Per-token power-of-two shift of the f16 operand (W4A16): one warp per token.
@@ -260,9 +259,9 @@ __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict
   __syncthreads();
 
   if (tid < kRouteRows * T) {
-    const int r = tid / T, t = tid % T;
-    const int rr = blockIdx.x * kRouteRows + r;
-    if (rr < E) ws.logits[(size_t)t * E + rr] = part[r][0][t] + part[r][1][t];
+    const int rl = tid / T, t = tid % T;
+    const int rr = row0 + rl;
+    if (rr < E) ws.logits[(size_t)t * E + rr] = part[rl][0][t] + part[rl][1][t];
   }
 
   // This CTA's share of the activation preparation (skipped for routing-only calls).
@@ -528,24 +527,29 @@ __global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, PackView pkv, int
   }
   const int cnt_e = e < E ? run : 0;
   const int ng_e = (cnt_e + kGroup - 1) / kGroup;
-  // two block-wide exclusive scans (counts, group counts)
-  int a = cnt_e, b = ng_e;
+  const int nt_e = (cnt_e + 127) / 128;
+  // three block-wide exclusive scans: slots, token groups, 128-slot token tiles
+  int a = cnt_e, b = ng_e, c3 = nt_e;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const int oa = __shfl_up_sync(0xFFFFFFFFu, a, off);
     const int ob = __shfl_up_sync(0xFFFFFFFFu, b, off);
-    if (lane >= off) { a += oa; b += ob; }
+    const int oc = __shfl_up_sync(0xFFFFFFFFu, c3, off);
+    if (lane >= off) { a += oa; b += ob; c3 += oc; }
   }
-  if (lane == 31) { wsum[warp] = a; tot[warp] = b; }
+  __shared__ int32_t tsum[32];
+  if (lane == 31) { wsum[warp] = a; tot[warp] = b; tsum[warp] = c3; }
   __syncthreads();
-  int ba = 0, bb = 0, ta = 0, tb = 0;
+  int ba = 0, bb = 0, bc = 0, ta = 0, tb = 0, tc = 0;
   for (int w = 0; w < 32; ++w) {
-    if (w < warp) { ba += wsum[w]; bb += tot[w]; }
+    if (w < warp) { ba += wsum[w]; bb += tot[w]; bc += tsum[w]; }
     ta += wsum[w];
     tb += tot[w];
+    tc += tsum[w];
   }
   const int off_e = ba + a - cnt_e;
   const int gbase = bb + b - ng_e;
+  const int tbase = bc + c3 - nt_e;
   __syncthreads();
   if (e < E) {
     out.counts[e] = cnt_e;
@@ -559,6 +563,18 @@ __global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, PackView pkv, int
       write_group(ws, pk, gbase + q, e, off_e + q * kGroup, min(kGroup, cnt_e - q * kGroup),
                   nullptr);
     }
+    if (ws.tt_expert) {
+      ws.ttbase[e] = tbase;
+      for (int q = 0; q < nt_e; ++q) {
+        ws.tt_expert[tbase + q] = e;
+        ws.tt_slot0[tbase + q] = off_e + q * 128;
+        ws.tt_n[tbase + q] = min(128, cnt_e - q * 128);
+      }
+    }
+  }
+  if (e == 0) {
+    if (ws.tt_expert) ws.ttbase[E] = tc;
+    ws.ctl[kCtlTokenTiles] = tc;
   }
   if (ws.slot_amax)
     for (int i = e; i < ws.T * ws.k; i += 1024) ws.slot_amax[i] = 0u;
@@ -666,7 +682,7 @@ cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t
 }  // namespace
 
 size_t route_narrow_smem_bytes(int T, int H, int E, int k) {
-  const size_t xbytes = (size_t)T * H * 2;
+  const size_t xbytes = (size_t)T * H * 2 + (size_t)kRouteRows * H * 2;
   const size_t fin = (size_t)T * E * 4 + (size_t)T * k * 16 + (size_t)(E + 1) * 8 + 64;
   return xbytes > fin ? xbytes : fin;
 }
@@ -677,13 +693,25 @@ cudaError_t launch_route_narrow(const LaunchCfg& lc, const uint16_t* x, const ui
                                 int32_t* out_offsets, int32_t* out_perm) {
   const PackView pkv = pk ? *pk : PackView{};
   const size_t smem = route_narrow_smem_bytes(ws.T, ws.H, ws.E, ws.k);
-  cudaError_t e = cudaFuncSetAttribute(k_route_narrow, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
   RouteOut out{out_idx, out_w, out_counts, out_offsets, out_perm};
   const int grid = (ws.E + kRouteRows - 1) / kRouteRows;
-  return launch(lc, k_route_narrow, dim3(grid), dim3(256), smem, x, wr, ws, pkv, pk ? 1 : 0,
-                mode, xS, x_inv6S, out);
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch(lc, kern, dim3(grid), dim3(256), smem, x, wr, ws, pkv, pk ? 1 : 0, mode, xS,
+                  x_inv6S, out);
+  };
+  switch (ws.T) {
+    case 1: return go(k_route_narrow<1>);
+    case 2: return go(k_route_narrow<2>);
+    case 3: return go(k_route_narrow<3>);
+    case 4: return go(k_route_narrow<4>);
+    case 5: return go(k_route_narrow<5>);
+    case 6: return go(k_route_narrow<6>);
+    case 7: return go(k_route_narrow<7>);
+    default: return go(k_route_narrow<8>);
+  }
 }
 
 cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,

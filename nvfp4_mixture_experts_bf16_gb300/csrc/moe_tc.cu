@@ -1,0 +1,485 @@
+// moe_tc.cu — grouped NVFP4 expert GEMMs on the 5th-generation tensor cores (tcgen05) for wide
+// (prefill) calls in W4A4 mode.
+//
+// Model card "Qwen3.8-Flash-Next NVIDIA NVFP4 for Infernix (bit-exact)", section "What is
+// bit-exact and what is quantized": E2M1 codes with one E4M3 scale per 16 weights, an FP32
+// multiplier and an FP32 activation input scale per matrix. The Infernix README, section
+// "Activation precision", reads prompts in W4A4 on the FP4 tensor cores. Here that is
+// tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (E2M1 x E2M1, UE4M3 scale per 16), M = 128
+// weight rows, N = 128 tokens, K = 64 per instruction, FP32 accumulators in tensor memory:
+//
+//   * tokens are grouped per expert into tiles of <= 128 slots ("token tiles"), laid out in a
+//     padded permuted space (tile j = rows 128j..128j+127), so that a tile's activation codes
+//     and scale-factor atoms are contiguous;
+//   * warp 0 issues TMA loads (tensor maps, 128-byte swizzle) of the weight and activation tiles
+//     and bulk copies of the scale-factor atoms into a ring of stages guarded by mbarriers;
+//   * warp 1 copies the scale factors into tensor memory (tcgen05.cp) and issues the MMAs; a
+//     commit per stage releases the stage and a commit per tile hands the accumulator to
+//   * warps 2..5, the epilogue: tensor memory -> registers, then SiLU*up and the NVFP4
+//     quantisation of h (gate/up) or the BF16 expert output Y (down). Accumulators are double
+//     buffered so the epilogue of one tile overlaps the main loop of the next.
+//
+// Scale-factor atom (512 B, one K step of 64 for 128 rows): byte (r % 32) * 16 + (r / 32) * 4 + b
+// holds the scale of row r, 16-element block b. After tcgen05.cp.32x128b.warpx4 row m's scales
+// sit at tensor-memory lane m, column (base + m / 32), the layout the block-scaled MMA reads.
+#include "moe_internal.cuh"
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+namespace moe {
+namespace tc {
+
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+constexpr int kStageK = 256;                    // FP4 elements per stage = 128 bytes per row
+constexpr int kTileBytes = kTileM * 128;        // 16 KB: one 128-row x 128-byte SW128 tile
+constexpr int kSfStage = 4 * 512;               // 4 K steps of scale-factor atoms
+constexpr int kStageBytes = 2 * kTileBytes + 2 * kSfStage;   // A, B, SFA, SFB = 36 KB
+constexpr int kStages = 5;
+constexpr int kThreads = 192;                   // producer, MMA, 4 epilogue warps
+constexpr int kTmemCols = 512;
+constexpr int kSfCol = 256;                     // scale factors after two 128-column accumulators
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
+                            ((uint32_t)(kTileM >> 4) << 24);   // E2M1 x E2M1, UE4M3, 128x128
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Source descriptor of a 32-row x 16-byte scale-factor atom (rows 16 B apart, no swizzle).
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(16 >> 4) << 16) |
+         ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                       uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_nvf4(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void epi_sync() {  // the 4 epilogue warps
+  asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// Byte offset of (row r, 16-element block b) inside a scale-factor atom.
+__device__ __forceinline__ int sf_atom_byte(int r, int b) {
+  return (r & 31) * 16 + (r >> 5) * 4 + b;
+}
+
+struct TcParams {
+  const uint8_t* sfa;    // weight scale-factor atoms (pack)
+  const uint8_t* sfb;    // activation scale-factor atoms (workspace)
+  const float* mult;     // [E][3]
+  const float* dscale;   // [E] down input scale
+  const float* dinv6;    // [E]
+  float xS;              // activation input scale of gate/up
+  int H, I, E;
+  int MT;                // m tiles per token tile
+  int nks;               // stages per tile
+  int last_k4;           // K steps (of 64) in the last stage
+};
+
+// ------------------------------------------------------------------ shared pipeline skeleton
+// Kernel body shared by gate/up and down: DOWN selects the operands, K and the epilogue.
+template <bool DOWN>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+              const __grid_constant__ CUtensorMap tm_b, TcParams prm, WsView ws) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_s;
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* smem = smem_raw + pad;
+  float* xch = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // [64][33] gate<->up
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    fence_mbar_init();
+    abort_s = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base_s)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_s;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int NT = (int)ws.ctl[kCtlTokenTiles];
+  const int ntiles = NT * prm.MT;
+  const int H = prm.H, I = prm.I;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles && !abort_s; t += gridDim.x) {
+        const int j = t / prm.MT, mt = t % prm.MT;
+        const int e = __ldg(&ws.tt_expert[j]);
+        for (int ks = 0; ks < prm.nks; ++ks, ++it) {
+          const int s = it % kStages, n = it / kStages;
+          if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+            break;
+          }
+          unsigned char* st = smem + s * kStageBytes;
+          const int k4 = (ks == prm.nks - 1) ? prm.last_k4 : 4;
+          mbar_arrive_expect_tx(&full[s], 2 * kTileBytes + 2 * 512 * k4);
+          if (!DOWN) {
+            // A = 64 gate rows over 64 up rows of intermediate tile mt
+            tma_2d(st, &tm_a0, ks * 128, e * I + mt * 64, &full[s]);
+            tma_2d(st + kTileBytes / 2, &tm_a1, ks * 128, e * I + mt * 64, &full[s]);
+          } else {
+            tma_2d(st, &tm_a0, ks * 128, e * H + mt * 128, &full[s]);
+          }
+          tma_2d(st + kTileBytes, &tm_b, ks * 128, j * 128, &full[s]);
+          const int katoms = DOWN ? I / 64 : H / 64;
+          bulk_g2s(st + 2 * kTileBytes,
+                   prm.sfa + (((size_t)e * prm.MT + mt) * katoms + 4 * ks) * 512, 512 * k4,
+                   &full[s]);
+          bulk_g2s(st + 2 * kTileBytes + kSfStage, prm.sfb + ((size_t)j * katoms + 4 * ks) * 512,
+                   512 * k4, &full[s]);
+        }
+      }
+      const int used = it < kStages ? it : kStages;
+      for (int i = 0; i < used; ++i) {
+        const int c = it - 1 - i;
+        (void)mbar_wait(&full[c % kStages], (c / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
+        const int buf = tcount & 1, use = tcount >> 1;
+        if (use > 0 && !abort_s && !mbar_wait(&acc_empty[buf], (use - 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        fence_after();
+        const uint32_t dacc = tmem + buf * kTileN;
+        for (int ks = 0; ks < prm.nks; ++ks, ++it) {
+          const int s = it % kStages, n = it / kStages;
+          if (!abort_s && !mbar_wait(&full[s], n & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          fence_after();
+          unsigned char* st = smem + s * kStageBytes;
+          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + kTileBytes);
+          const uint32_t sfa0 = smem_u32(st + 2 * kTileBytes);
+          const uint32_t sfb0 = smem_u32(st + 2 * kTileBytes + kSfStage);
+          const uint32_t sfcol = tmem + kSfCol + (it & 1) * 32;
+          const int k4 = (ks == prm.nks - 1) ? prm.last_k4 : 4;
+          for (int q = 0; q < k4; ++q) {
+            cp_sf(sfcol + 4 * q, desc_sf(sfa0 + q * 512));
+            cp_sf(sfcol + 16 + 4 * q, desc_sf(sfb0 + q * 512));
+          }
+          for (int q = 0; q < k4; ++q) {
+            mma_nvf4(dacc, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32), sfcol + 4 * q,
+                     sfcol + 16 + 4 * q, (ks > 0 || q > 0) ? 1u : 0u);
+          }
+          commit(&empty[s]);
+        }
+        commit(&acc_full[buf]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    const int quad = warp & 3;            // tensor-memory lanes 32*quad .. +31
+    const int row = quad * 32 + lane;     // accumulator row of this thread
+    int tcount = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
+      const int j = t / prm.MT, mt = t % prm.MT;
+      const int buf = tcount & 1, use = tcount >> 1;
+      if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
+        record_status(ws.ctl, kStTimeout);
+        abort_s = 1;
+      }
+      __syncwarp();
+      fence_after();
+      const int e = ws.tt_expert[j];
+      const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
+      const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN;
+      if (!DOWN) {
+        // rows 0..63: gate rows mt*64 + row; rows 64..127: the matching up rows
+        const float mg = prm.mult[e * 3 + 0] * prm.xS, mu = prm.mult[e * 3 + 1] * prm.xS;
+        const float Sd = prm.dscale[e], i6 = prm.dinv6[e];
+        const bool is_gate = quad < 2;
+        const int il = is_gate ? row : row - 64;       // intermediate index inside the tile
+        for (int c0 = 0; c0 < kTileN; c0 += 32) {
+          uint32_t r[32];
+          ld32(tbase + c0, r);
+          if (!is_gate) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) xch[il * 33 + q] = __uint_as_float(r[q]) * mu;
+          }
+          epi_sync();
+          if (is_gate) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const int col = c0 + q;
+              const float g = __uint_as_float(r[q]) * mg;
+              const float u = xch[il * 33 + q];
+              const float h = (g / (1.0f + expf(-g))) * u;
+              // NVFP4 block of 16 consecutive intermediate rows = 16 consecutive lanes
+              float a = fabsf(h);
+#pragma unroll
+              for (int off = 1; off < 16; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+              const uint32_t sf = e4m3_encode_rn(__fmul_rn(a, i6));
+              uint32_t code = 0;
+              if (sf != 0u) code = e2m1_encode_rn(__fmul_rn(h, __frcp_rn(__fmul_rn(e4m3_value_nonneg(sf), Sd))));
+              const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, code, 1);
+              if (col < nval) {
+                const int ig = mt * 64 + il;          // intermediate index
+                const size_t pslot = (size_t)j * 128 + col;
+                const size_t slot = (size_t)slot0 + col;
+                if ((lane & 1) == 0) {
+                  const uint8_t byte = (uint8_t)(code | (other << 4));
+                  ws.hq_perm[pslot * (I / 2) + ig / 2] = byte;
+                  ws.hq[slot * (I / 2) + ig / 2] = byte;
+                }
+                if ((il & 15) == 0) {
+                  const int blk = ig / 16;                 // block along I
+                  ws.hsf_atoms[((size_t)j * (I / 64) + blk / 4) * 512 + sf_atom_byte(col, blk & 3)] =
+                      (uint8_t)sf;
+                  ws.hsf[slot * (I / 16) + blk] = (uint8_t)sf;
+                }
+              }
+            }
+          }
+          epi_sync();
+        }
+      } else {
+        const float md = prm.mult[e * 3 + 2] * prm.dscale[e];
+        const int hrow = mt * 128 + row;
+        for (int c0 = 0; c0 < kTileN; c0 += 32) {
+          uint32_t r[32];
+          ld32(tbase + c0, r);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int col = c0 + q;
+            if (col < nval)
+              ws.y[(size_t)(slot0 + col) * H + hrow] = f32_to_bf16_rn(__uint_as_float(r[q]) * md);
+          }
+        }
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+}
+
+// ------------------------------------------------------------------ activations by pslot
+// For every slot: copy the token's NVFP4 codes to its padded permuted row and scatter its scales
+// into the scale-factor atoms of its token tile. One 128-thread CTA per slot.
+__global__ void __launch_bounds__(128) k_x_perm(WsView ws) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int s = blockIdx.x;
+  const int H = ws.H, E = ws.E;
+  if (s >= ws.T * ws.k) return;
+  // expert of slot s: last e with offsets[e] <= s (binary search over E+1 offsets)
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (ws.offsets[mid] <= s) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int rank = s - ws.offsets[e];
+  const int j = ws.ttbase[e] + rank / 128, r = rank % 128;
+  const int t = ws.perm[s];
+  const uint4* src = reinterpret_cast<const uint4*>(ws.xq + (size_t)t * (H / 2));
+  uint4* dst = reinterpret_cast<uint4*>(ws.xq_perm + ((size_t)j * 128 + r) * (H / 2));
+  for (int i = threadIdx.x; i < H / 32; i += 128) dst[i] = src[i];
+  for (int b = threadIdx.x; b < H / 16; b += 128)
+    ws.xsf_atoms[((size_t)j * (H / 64) + b / 4) * 512 + sf_atom_byte(r, b & 3)] =
+        ws.xsf[(size_t)t * (H / 16) + b];
+}
+
+}  // namespace tc
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows][row_bytes] with a box of 128 bytes x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
+              uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
+                   Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace
+
+bool tc_supported() { return encode_fn() != nullptr; }
+
+size_t tc_smem_bytes() {
+  return (size_t)tc::kStages * tc::kStageBytes + 64 * 33 * 4 + 1024;
+}
+
+cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
+                              float xS) {
+  const int H = pk.H, I = pk.I, E = pk.E;
+  const uint64_t P = (uint64_t)ws.NT * 128;
+  CUtensorMap m_gate, m_up, m_x, m_down, m_h;
+  if (!make_map(&m_gate, pk.gate_codes, H / 2, (uint64_t)E * I, 64) ||
+      !make_map(&m_up, pk.up_codes, H / 2, (uint64_t)E * I, 64) ||
+      !make_map(&m_x, ws.xq_perm, H / 2, P, 128) ||
+      !make_map(&m_down, pk.down_codes, I / 2, (uint64_t)E * H, 128) ||
+      !make_map(&m_h, ws.hq_perm, I / 2, P, 128))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch(lc, tc::k_x_perm, dim3(ws.T * ws.k), dim3(128), 0, ws);
+  if (e != cudaSuccess) return e;
+  const size_t smem = tc_smem_bytes();
+  e = cudaFuncSetAttribute(tc::k_tc_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::k_tc_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  tc::TcParams pg;
+  pg.sfa = pk.sfa_gu;
+  pg.sfb = ws.xsf_atoms;
+  pg.mult = pk.mult;
+  pg.dscale = pk.down_in_scale;
+  pg.dinv6 = pk.down_inv6S;
+  pg.xS = xS;
+  pg.H = H; pg.I = I; pg.E = E;
+  pg.MT = I / 64;
+  pg.nks = H / tc::kStageK;
+  pg.last_k4 = 4;
+  const int grid = lc.num_sms;
+  e = launch(lc, tc::k_tc_gemm<false>, dim3(grid), dim3(tc::kThreads), smem, m_gate, m_up, m_x, pg,
+             ws);
+  if (e != cudaSuccess) return e;
+  tc::TcParams pd = pg;
+  pd.sfa = pk.sfa_down;
+  pd.sfb = ws.hsf_atoms;
+  pd.MT = H / 128;
+  pd.nks = (I + tc::kStageK - 1) / tc::kStageK;
+  pd.last_k4 = ((I % tc::kStageK) ? (I % tc::kStageK) : tc::kStageK) / 64;
+  return launch(lc, tc::k_tc_gemm<true>, dim3(grid), dim3(tc::kThreads), smem, m_down, m_down, m_h,
+                pd, ws);
+}
+
+}  // namespace moe

@@ -206,6 +206,18 @@ def test_forward_ragged_shapes(T, mode):
     pack.close()
 
 
+@pytest.mark.parametrize("mode", [1, 0])
+def test_forward_multi_tile_experts(mode):
+    # every expert receives more than 128 slots: several token tiles per expert on the grouped
+    # tensor-core path (W4A4), several 8-token groups on the grouped CUDA-core path (W4A16)
+    T, H, E, k, I = 600, 512, 8, 2, 128
+    x, wr, ex = small_layer(T, H, E, k, I, seed=21)
+    pack = pack_from_experts(ex)
+    r = run_and_check(x, wr, ex, pack, k, mode)
+    assert np.bincount(r["g_idx"].ravel(), minlength=E).max() > 128
+    pack.close()
+
+
 def test_forward_twice_is_deterministic_and_counters_reset():
     x, wr, ex = small_layer(8, 512, 32, 4, 128, seed=4)
     pack = pack_from_experts(ex)
