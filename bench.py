@@ -46,6 +46,7 @@ def parse_args():
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--workload", default="decode1", choices=list(synth.WORKLOADS))
     p.add_argument("--layers", type=int, default=None)
+    p.add_argument("--tokens", type=int, default=None, help="tokens per layer (profiling)")
     p.add_argument("--experts", type=int, default=None,
                    help="experts per layer (smaller packs for profiler captures)")
     p.add_argument("--seed", type=int, default=0)
@@ -371,9 +372,9 @@ def run_native(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     wl = synth.WORKLOADS[args.workload]
-    if args.experts:
-        wl = synth.Workload(wl.name, wl.T, wl.H, args.experts, wl.k, wl.I, wl.mode, wl.layers,
-                            wl.zipf)
+    if args.experts or args.tokens:
+        wl = synth.Workload(wl.name, args.tokens or wl.T, wl.H, args.experts or wl.E, wl.k, wl.I,
+                            wl.mode, wl.layers, wl.zipf)
     layers = args.layers or wl.layers
     pk = peaks()
     t_setup = time.time()
@@ -431,7 +432,8 @@ def run_native(args, rank, world, local_rank):
             extra[f"prefill8192_{['w4a16', 'w4a4'][mode]}"] = dict(
                 tokens_per_s=round(w3.T / (ms3 / 1e3), 1), ms=round(ms3, 3),
                 expert_tflops=round(flops / (ms3 * 1e-3) / 1e12, 2),
-                note="grouped fallback path (mma.sync); tcgen05 path pending")
+                note=("tcgen05 block-scaled FP4 grouped GEMMs" if mode == 1 else
+                      "grouped mma.sync path (CUDA-core dequant)"))
         torch.cuda.synchronize()
 
     cpu = None
