@@ -306,7 +306,7 @@ def measure(wl, stack, steps, warmup, use_graph, device, clocks=None):
     status = moe.moe_read_device_status(ws, stream=s)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    return e0.elapsed_time(e1) / steps, launches[0], info, (s, ws, outs, graph)
+    return e0.elapsed_time(e1) / steps, launches[0], info, (s, ws, outs, run)
 
 
 def stage_times(wl, stack, reps, device):
@@ -341,10 +341,9 @@ def e2e_measure(wl, stack, steps, state, device):
     """Same metric through the public API with host buffers: per step, copy every layer's x
     host->device (pinned), run the step, copy every layer's out device->host."""
     import torch
-    s, ws, outs, graph = state
+    s, ws, outs, run = state
     hx = [L.x.cpu().pin_memory() for L in stack]
     ho = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory() for _ in stack]
-    run = graph.replay
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
