@@ -36,8 +36,10 @@ constexpr int kStageK = 256;                    // FP4 elements per stage = 128 
 constexpr int kTileBytes = kTileM * 128;        // 16 KB: one 128-row x 128-byte SW128 tile
 constexpr int kSfStage = 4 * 512;               // 4 K steps of scale-factor atoms
 constexpr int kStageBytes = 2 * kTileBytes + 2 * kSfStage;   // A, B, SFA, SFB = 36 KB
-constexpr int kStages = 5;
-constexpr int kThreads = 192;                   // producer, MMA, 4 epilogue warps
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 8;                    // two per tensor-memory lane quadrant
+constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue warps
+constexpr int kStageF = kTileN + 4;             // padded row of the epilogue staging (floats)
 constexpr int kTmemCols = 512;
 constexpr int kSfCol = 256;                     // scale factors after two 128-column accumulators
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
@@ -106,8 +108,8 @@ __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void epi_sync() {  // the 4 epilogue warps
-  asm volatile("bar.sync 2, 128;" ::: "memory");
+__device__ __forceinline__ void epi_sync() {  // the epilogue warps
+  asm volatile("bar.sync 2, %0;" ::"r"(kEpiWarps * 32) : "memory");
 }
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
@@ -145,7 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int abort_s;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* smem = smem_raw + pad;
-  float* xch = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // [64][33] gate<->up
+  // epilogue staging: the gate and up accumulators of a tile, [128 rows][kStageF] floats
+  float* acc_s = reinterpret_cast<float*>(smem + kStages * kStageBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -155,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], kEpiWarps);
     }
     fence_mbar_init();
     abort_s = 0;
@@ -256,88 +259,87 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------------------------------------------------------- epilogue (warps 2..5)
-    const int quad = warp & 3;            // tensor-memory lanes 32*quad .. +31
+    // ---------------------------------------------------------------- epilogue (warps 2..9)
+    const int ew = warp - 2;              // epilogue warp 0..7
+    const int quad = warp & 3;            // tensor-memory lanes 32*quad .. +31 (hardware rule)
+    const int chalf = ew >> 2;            // column half handled by this warp in the TMEM read
     const int row = quad * 32 + lane;     // accumulator row of this thread
+    const int etid = ew * 32 + lane;      // 0..255
     int tcount = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
       const int j = t / prm.MT, mt = t % prm.MT;
       const int buf = tcount & 1, use = tcount >> 1;
+      // tile metadata (independent loads, issued before the wait)
+      const int e = ws.tt_expert[j];
+      const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
       if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
       }
       __syncwarp();
       fence_after();
-      const int e = ws.tt_expert[j];
-      const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
       const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN;
-      if (!DOWN) {
-        // rows 0..63: gate rows mt*64 + row; rows 64..127: the matching up rows
-        const float mg = prm.mult[e * 3 + 0] * prm.xS, mu = prm.mult[e * 3 + 1] * prm.xS;
-        const float Sd = prm.dscale[e], i6 = prm.dinv6[e];
-        const bool is_gate = quad < 2;
-        const int il = is_gate ? row : row - 64;       // intermediate index inside the tile
-        for (int c0 = 0; c0 < kTileN; c0 += 32) {
-          uint32_t r[32];
-          ld32(tbase + c0, r);
-          if (!is_gate) {
+      // accumulators -> shared memory (this warp: its 32 rows x 64 columns), then release TMEM
+      for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
+        uint32_t r[32];
+        ld32(tbase + c0, r);
+        float4* dst = reinterpret_cast<float4*>(acc_s + row * kStageF + c0);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) xch[il * 33 + q] = __uint_as_float(r[q]) * mu;
-          }
-          epi_sync();
-          if (is_gate) {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-              const int col = c0 + q;
-              const float g = __uint_as_float(r[q]) * mg;
-              const float u = xch[il * 33 + q];
-              const float h = (g / (1.0f + expf(-g))) * u;
-              // NVFP4 block of 16 consecutive intermediate rows = 16 consecutive lanes
-              float a = fabsf(h);
-#pragma unroll
-              for (int off = 1; off < 16; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
-              const uint32_t sf = e4m3_encode_rn(__fmul_rn(a, i6));
-              uint32_t code = 0;
-              if (sf != 0u) code = e2m1_encode_rn(__fmul_rn(h, __frcp_rn(__fmul_rn(e4m3_value_nonneg(sf), Sd))));
-              const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, code, 1);
-              if (col < nval) {
-                const int ig = mt * 64 + il;          // intermediate index
-                const size_t pslot = (size_t)j * 128 + col;
-                const size_t slot = (size_t)slot0 + col;
-                if ((lane & 1) == 0) {
-                  const uint8_t byte = (uint8_t)(code | (other << 4));
-                  ws.hq_perm[pslot * (I / 2) + ig / 2] = byte;
-                  ws.hq[slot * (I / 2) + ig / 2] = byte;
-                }
-                if ((il & 15) == 0) {
-                  const int blk = ig / 16;                 // block along I
-                  ws.hsf_atoms[((size_t)j * (I / 64) + blk / 4) * 512 + sf_atom_byte(col, blk & 3)] =
-                      (uint8_t)sf;
-                  ws.hsf[slot * (I / 16) + blk] = (uint8_t)sf;
-                }
-              }
-            }
-          }
-          epi_sync();
-        }
-      } else {
-        const float md = prm.mult[e * 3 + 2] * prm.dscale[e];
-        const int hrow = mt * 128 + row;
-        for (int c0 = 0; c0 < kTileN; c0 += 32) {
-          uint32_t r[32];
-          ld32(tbase + c0, r);
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int col = c0 + q;
-            if (col < nval)
-              ws.y[(size_t)(slot0 + col) * H + hrow] = f32_to_bf16_rn(__uint_as_float(r[q]) * md);
-          }
-        }
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
       }
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      epi_sync();
+      if (!DOWN) {
+        // rows 0..63: gate rows mt*64 + i; rows 64..127: the matching up rows. A task is one
+        // 16-row NVFP4 block of h for one token: SiLU*up and the quantiser, all in one thread.
+        const float mg = prm.mult[e * 3 + 0] * prm.xS, mu = prm.mult[e * 3 + 1] * prm.xS;
+        const float Sd = prm.dscale[e], i6 = prm.dinv6[e];
+        for (int task = etid; task < 4 * kTileN; task += kEpiWarps * 32) {
+          const int col = task % kTileN, blk = task / kTileN;   // consecutive threads: columns
+          if (col >= nval) continue;
+          float h[16];
+          float a = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g = acc_s[(blk * 16 + i) * kStageF + col] * mg;
+            const float u = acc_s[(64 + blk * 16 + i) * kStageF + col] * mu;
+            h[i] = (g / (1.0f + expf(-g))) * u;
+            a = fmaxf(a, fabsf(h[i]));
+          }
+          const uint32_t sf = e4m3_encode_rn(__fmul_rn(a, i6));
+          uint32_t lo = 0, hi = 0;
+          if (sf != 0u) {
+            const float rr = __frcp_rn(__fmul_rn(e4m3_value_nonneg(sf), Sd));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              lo |= e2m1_encode_rn(__fmul_rn(h[i], rr)) << (4 * i);
+              hi |= e2m1_encode_rn(__fmul_rn(h[8 + i], rr)) << (4 * i);
+            }
+          }
+          const int ib = mt * 4 + blk;                 // 16-element block index along I
+          const size_t pslot = (size_t)j * 128 + col;
+          const size_t slot = (size_t)slot0 + col;
+          *reinterpret_cast<uint2*>(ws.hq_perm + pslot * (I / 2) + ib * 8) = make_uint2(lo, hi);
+          *reinterpret_cast<uint2*>(ws.hq + slot * (I / 2) + ib * 8) = make_uint2(lo, hi);
+          ws.hsf_atoms[((size_t)j * (I / 64) + ib / 4) * 512 + sf_atom_byte(col, ib & 3)] =
+              (uint8_t)sf;
+          ws.hsf[slot * (I / 16) + ib] = (uint8_t)sf;
+        }
+      } else {
+        // Y[slot][row] for this tile's 128 rows: a warp writes 32 consecutive rows of one slot
+        const float md = prm.mult[e * 3 + 2] * prm.dscale[e];
+        for (int idx = etid; idx < kTileM * kTileN; idx += kEpiWarps * 32) {
+          const int col = idx / kTileM, r = idx % kTileM;
+          if (col < nval)
+            ws.y[(size_t)(slot0 + col) * H + mt * 128 + r] =
+                f32_to_bf16_rn(acc_s[r * kStageF + col] * md);
+        }
+      }
+      epi_sync();   // the staging buffer is reused by the next tile
     }
   }
   fence_before();
@@ -434,7 +436,7 @@ cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t
 bool tc_supported() { return encode_fn() != nullptr; }
 
 size_t tc_smem_bytes() {
-  return (size_t)tc::kStages * tc::kStageBytes + 64 * 33 * 4 + 1024;
+  return (size_t)tc::kStages * tc::kStageBytes + (size_t)tc::kTileM * tc::kStageF * 4 + 1024;
 }
 
 cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
