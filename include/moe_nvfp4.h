@@ -124,6 +124,22 @@ moe_status moe_route_topk(const uint16_t* x, const uint16_t* router_w, int T, in
                           int k, int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
                           int32_t* perm, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_route_topk without a workspace argument, for callers that cannot allocate device memory:
+ * code that runs while a stream is being captured into a CUDA graph (cudaMalloc is not allowed
+ * there), runtimes whose allocator is frozen after start-up, and embedders that own no device
+ * allocator. The pages have no counterpart to this entry point; it exists only for such callers.
+ * Arguments, outputs and requirements are those of moe_route_topk. Its workspace is a fixed
+ * 4 MiB device array inside the library, held by every GPU that loads the library until the
+ * process exits; shapes whose moe_route_workspace_size exceeds 4 MiB return MOE_ERR_WORKSPACE
+ * before anything is launched. No call allocates or frees memory. The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress): make that first call before any
+ * stream capture. Each call clears the array's control words (cudaMemsetAsync on `stream`). All
+ * calls share the one array: calls that overlap on the GPU (e.g. on two streams) race, so the
+ * caller must serialise them. */
+moe_status moe_route_topk_noalloc(const uint16_t* x, const uint16_t* router_w, int T, int H, int E,
+                                  int k, int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
+                                  int32_t* perm, void* stream);
+
 /* The whole MoE feed-forward step: out [T][H] BF16 (device) from x [T][H] BF16 and router_w
  * [E][H] BF16 (device), using the experts of `pack` in `mode`. T <= 8 runs the narrow decode
  * kernels; larger T runs the grouped (prefill) kernels. W4A4 requires every gate and up

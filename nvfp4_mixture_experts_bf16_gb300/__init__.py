@@ -26,7 +26,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTED = ["moe_pack_nvfp4", "moe_pack_destroy", "moe_pack_info", "moe_pack_get_matrix",
             "moe_workspace_size", "moe_route_workspace_size", "moe_route_topk", "moe_forward",
             "moe_workspace_offsets", "moe_quantize_act_nvfp4", "moe_read_device_status",
-            "moe_status_string", "moe_last_launch_count", "moe_profile_next_forward"]
+            "moe_status_string", "moe_last_launch_count", "moe_profile_next_forward",
+            "moe_route_topk_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -83,6 +84,7 @@ def lib() -> ctypes.CDLL:
             L.moe_status_string.restype = ctypes.c_char_p
             L.moe_last_launch_count.argtypes = []
             L.moe_profile_next_forward.argtypes = [vp, i32]
+            L.moe_route_topk_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
             for n in EXPORTED:
                 if n not in ("moe_status_string",):
                     getattr(L, n).restype = ctypes.c_int
@@ -215,6 +217,24 @@ def moe_route_topk(x, router_w, k: int, ws=None, stream=None):
         _bits(x), _bits(router_w), T, H, E, k, _ptr(out["idx"]), _ptr(out["w"]),
         _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(ws), ws.numel(),
         _stream(stream)))
+    return out
+
+
+def moe_route_topk_noalloc(x, router_w, k: int, stream=None):
+    """moe_route_topk with the library's fixed device workspace (no workspace argument): for
+    callers that cannot allocate device memory. Calls that overlap on the GPU race."""
+    import torch
+    T, H = x.shape
+    E = router_w.shape[0]
+    dev = x.device
+    out = dict(idx=torch.empty((T, k), dtype=torch.int32, device=dev),
+               w=torch.empty((T, k), dtype=torch.float32, device=dev),
+               counts=torch.empty(E, dtype=torch.int32, device=dev),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+               perm=torch.empty(T * k, dtype=torch.int32, device=dev))
+    _check("moe_route_topk_noalloc", lib().moe_route_topk_noalloc(
+        _bits(x), _bits(router_w), T, H, E, k, _ptr(out["idx"]), _ptr(out["w"]),
+        _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]), _stream(stream)))
     return out
 
 
