@@ -65,7 +65,7 @@ int num_sms_of_current_device() {
 }
 
 struct WsLayout {
-  size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm, grp_expert, grp_slot, grp_n,
+  size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm,
       chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
       xsf_atoms, hq_perm, hsf_atoms, total;
   size_t slot_amax_bytes;
@@ -91,9 +91,6 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
   L.counts = take((size_t)E * 4);
   L.offsets = take((size_t)(E + 1) * 4);
   L.perm = take((size_t)S * 4);
-  L.grp_expert = take((size_t)L.G * 4);
-  L.grp_slot = take((size_t)L.G * 4);
-  L.grp_n = take((size_t)L.G * 4);
   L.chunk_base = take(T > moe::kNarrowT ? (size_t)nchunk * E * 4 : 0);
   L.xh = take(mode >= 0 ? (size_t)T * H * 2 : 0);
   L.xfac = take(mode >= 0 ? (size_t)T * 4 : 0);
@@ -132,9 +129,6 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   v.counts = reinterpret_cast<int32_t*>(b + L.counts);
   v.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
   v.perm = reinterpret_cast<int32_t*>(b + L.perm);
-  v.grp_expert = reinterpret_cast<int32_t*>(b + L.grp_expert);
-  v.grp_slot = reinterpret_cast<int32_t*>(b + L.grp_slot);
-  v.grp_n = reinterpret_cast<int32_t*>(b + L.grp_n);
   v.chunk_base = reinterpret_cast<int32_t*>(b + L.chunk_base);
   v.xh = reinterpret_cast<__half*>(b + L.xh);
   v.xfac = reinterpret_cast<float*>(b + L.xfac);
@@ -418,27 +412,37 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
   // stage i of the profile covers: 0 routing (+ activation prep), 1 gate/up, 2 down, 3 combine
   if (g_prof_count) lc.pdl = false;
   e = prof_mark(lc.stream, 0);
+  if (narrow && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
+    // the whole step in one persistent kernel; the profile's later stages are empty
+    if (e == cudaSuccess)
+      e = moe::launch_decode(lc, pack->view, v, m, pack->x_scale, pack->x_inv6S, x, router_w, out);
+    for (int i = 1; i < 8 && e == cudaSuccess; ++i) e = prof_mark(lc.stream, i);
+    g_prof_count = 0;
+    g_last_launches = 1;
+    return from_cuda(e);
+  }
   if (narrow) {
     if (e == cudaSuccess)
       e = moe::launch_route_narrow(lc, x, router_w, v, &pack->view, m, pack->x_scale,
                                    pack->x_inv6S, v.idx, v.w, v.counts, v.offsets, v.perm);
     n += 1;
-  } else {
+  }
+  const bool use_tc = !narrow && m == 1 && v.NT > 0 && H % 256 == 0 && moe::tc_supported();
+  if (!narrow) {
     if (e == cudaSuccess)
       e = moe::launch_route_wide(lc, x, router_w, v, &pack->view, v.idx, v.w, v.counts, v.offsets,
                                  v.perm, &n);
-    if (e == cudaSuccess) {
+    if (e == cudaSuccess && !use_tc) {   // the tensor-core path quantises x itself
       e = moe::launch_xprep_wide(lc, x, v, m, pack->x_scale, pack->x_inv6S);
       n += 1;
     }
   }
   if (e == cudaSuccess) e = prof_mark(lc.stream, 1);
   if (e == cudaSuccess) e = prof_mark(lc.stream, 2);
-  const bool use_tc = !narrow && m == 1 && v.NT > 0 && H % 256 == 0 && moe::tc_supported();
   if (use_tc) {
-    // x permutation + gate/up + down on tcgen05 (stage 1 covers all three)
+    // x quantisation + permutation, gate/up, down on tcgen05 (stage 1 covers all three)
     if (e == cudaSuccess) {
-      e = moe::launch_tc_experts(lc, pack->view, v, pack->x_scale);
+      e = moe::launch_tc_experts(lc, pack->view, v, x, pack->x_scale, pack->x_inv6S);
       n += 3;
     }
     if (e == cudaSuccess) e = prof_mark(lc.stream, 3);

@@ -98,23 +98,6 @@ size_t dn_smem(const DnGeom& d) {
          d.h_rows * 4 + d.meta_cap * sizeof(GroupMeta) + 2 * 8 * d.stages + 64;
 }
 
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ uint2 lds64(const unsigned char* p) {
-  return *reinterpret_cast<const uint2*>(p);
-}
-__device__ __forceinline__ uint4 lds128(const unsigned char* p) {
-  return *reinterpret_cast<const uint4*>(p);
-}
-__device__ __forceinline__ uint32_t lds16(const unsigned char* p) {
-  return *reinterpret_cast<const uint16_t*>(p);
-}
-__device__ __forceinline__ uint32_t lds32(const unsigned char* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
-}
-
 // Balanced contiguous task range of this CTA.
 __device__ __forceinline__ void task_range(int ntasks, int& q0, int& q1) {
   q0 = (int)(((long long)ntasks * blockIdx.x) / gridDim.x);
@@ -128,15 +111,6 @@ __device__ __forceinline__ void stage_meta(GroupMeta* dst, const GroupMeta* src,
   const uint4* s4 = reinterpret_cast<const uint4*>(src + g0);
   uint4* d4 = reinterpret_cast<uint4*>(dst);
   for (int i = tid; i < words; i += nthreads) d4[i] = s4[i];
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return (g / (1.0f + expf(-g))) * u;
-}
-
-__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
-  __nv_bfloat16 b = __float2bfloat16_rn(v);
-  return *reinterpret_cast<uint16_t*>(&b);
 }
 
 // ------------------------------------------------------------------ gate/up
@@ -389,14 +363,6 @@ __global__ void __launch_bounds__(kGuThreads, 1)
 // ------------------------------------------------------------------ down
 // A task is (token group gi, 64-row tile ht of the hidden dimension); consumer warp w owns
 // rows ht*64 + 16w .. +15. Y (BF16) goes to the slot-major buffer for the combine.
-__device__ __forceinline__ int amax_shift(float m) {
-  if (!(m > 0.0f)) return 0;
-  int ex;
-  frexpf(m, &ex);
-  const int sh = ex - 15;
-  return sh < -110 ? -110 : (sh > 110 ? 110 : sh);
-}
-
 __global__ void __launch_bounds__(kDnThreads, 1)
     k_down(PackView pk, WsView ws, DnGeom geo, int mode, int h_resident) {
   extern __shared__ __align__(128) unsigned char smem[];

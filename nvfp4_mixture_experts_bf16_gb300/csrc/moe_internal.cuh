@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace moe {
@@ -28,7 +29,11 @@ enum : int {
   kCtlGroups = 2,       // number of token groups of the current call
   kCtlUnique = 3,       // number of distinct experts of the current call
   kCtlTokenTiles = 4,   // number of 128-slot token tiles (grouped tensor-core path)
-  kCtlWords = 64
+  kCtlBar1 = 8,         // fused decode kernel: grid barrier after the router logits
+  kCtlBar2 = 9,         //   grid barrier after h
+  kCtlDone = 10,        //   CTAs finished (the last one resets the fused kernel's words)
+  kCtlTiles = 64,       //   per 128-row output tile: down tasks finished (64 words)
+  kCtlWords = 128
 };
 
 // Per token group (<= 8 tokens of one expert): everything the expert kernels need about it,
@@ -52,9 +57,6 @@ struct WsView {
   int32_t* counts;     // [E]
   int32_t* offsets;    // [E+1]
   int32_t* perm;       // [T*k]
-  int32_t* grp_expert; // [G]
-  int32_t* grp_slot;   // [G] first perm slot of the group
-  int32_t* grp_n;      // [G] tokens in the group (1..8)
   int32_t* chunk_base; // [nchunk][E] (grouped routing)
   __half* xh;          // [T][H] activations as the f16 B operand of gate/up
   float* xfac;         // [T] factor restoring xh's scale (2^shift in W4A16, S_x in W4A4)
@@ -343,6 +345,134 @@ __device__ __forceinline__ void kblock128_mma(float (&acc)[4], const uint4& rowg
   }
 }
 
+// ------------------------------------------------------------------ shared arithmetic helpers
+// BF16 halves of a 32-bit word, the router dot product, the f16 operand's power-of-two
+// scaling, the warp top-k, and small shared-memory / conversion helpers of the expert kernels.
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// Sum of the 8 exact BF16 products of two uint4 chunks, as a fixed pairwise tree.
+__device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
+  const float p0 = bf16_lo(a.x) * bf16_lo(b.x), p1 = bf16_hi(a.x) * bf16_hi(b.x);
+  const float p2 = bf16_lo(a.y) * bf16_lo(b.y), p3 = bf16_hi(a.y) * bf16_hi(b.y);
+  const float p4 = bf16_lo(a.z) * bf16_lo(b.z), p5 = bf16_hi(a.z) * bf16_hi(b.z);
+  const float p6 = bf16_lo(a.w) * bf16_lo(b.w), p7 = bf16_hi(a.w) * bf16_hi(b.w);
+  return ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7));
+}
+
+// Power-of-two shift that puts a token's amax in [2^14, 2^15) for the f16 operand.
+__device__ __forceinline__ int token_shift(float amax) {
+  if (!(amax > 0.0f)) return 0;
+  int e;
+  frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
+  int s = e - 15;
+  return s < -110 ? -110 : (s > 110 ? 110 : s);
+}
+
+__device__ __forceinline__ float pow2f(int s) { return __int_as_float((127 + s) << 23); }
+
+// Orderable 32-bit key of an FP32 logit: a larger logit gives a larger key, and -0 and +0 give
+// the same key. Key 0 lies below every logit and marks a taken or absent entry.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  uint32_t f = __float_as_uint(v);
+  if (f == 0x80000000u) f = 0u;
+  return (f & 0x80000000u) ? ~f : (f | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Top-k of one token's E <= 32 V logits (global memory, read through L2) by one warp, followed by
+// the softmax over the k selected logits. Lane e % 32 holds logit e in register e / 32. Each
+// round takes the warp's largest key (redux.sync max) and, among lanes holding it, the lowest
+// expert index (redux.sync min): larger logit first, equal logits -> lower index first. Only the
+// winning lane drops its entry and rescans its registers. Lane j < k returns the j-th selection
+// and its softmax weight; the sum of exponentials is a fixed butterfly, identical in all lanes.
+template <int V>
+__device__ __forceinline__ void warp_topk_softmax(const float* row, int E, int k, int lane,
+                                                  int& e_out, float& w_out) {
+  uint32_t key[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? logit_key(__ldcg(row + e)) : 0u;
+  }
+  uint32_t bk = 0u;
+  int bp = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+    if (key[i] > bk) { bk = key[i]; bp = i; }
+  e_out = 0;
+  float v = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const uint32_t ew =
+        __reduce_min_sync(0xFFFFFFFFu, bk == m ? (uint32_t)(lane + 32 * bp) : 0xFFFFFFFFu);
+    if (lane == j) {
+      e_out = (int)ew;
+      v = key_logit(m);
+    }
+    if ((int)(ew & 31u) == lane) {
+      const int taken = bp;
+      bk = 0u;
+      bp = 0;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        if (i == taken) key[i] = 0u;
+        if (key[i] > bk) { bk = key[i]; bp = i; }
+      }
+    }
+  }
+  const float m0 = __shfl_sync(0xFFFFFFFFu, v, 0);
+  const float ex = lane < k ? expf(v - m0) : 0.0f;
+  float z = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
+  w_out = ex / z;
+}
+
+__device__ __forceinline__ void topk_row(const float* row, int E, int k, int lane, int& e_out,
+                                         float& w_out) {
+  if (E <= 128) warp_topk_softmax<4>(row, E, k, lane, e_out, w_out);
+  else if (E <= 256) warp_topk_softmax<8>(row, E, k, lane, e_out, w_out);
+  else if (E <= 512) warp_topk_softmax<16>(row, E, k, lane, e_out, w_out);
+  else warp_topk_softmax<32>(row, E, k, lane, e_out, w_out);
+}
+
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint2 lds64(const unsigned char* p) {
+  return *reinterpret_cast<const uint2*>(p);
+}
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ uint32_t lds16(const unsigned char* p) {
+  return *reinterpret_cast<const uint16_t*>(p);
+}
+__device__ __forceinline__ uint32_t lds32(const unsigned char* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return (g / (1.0f + expf(-g))) * u;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+
+__device__ __forceinline__ int amax_shift(float m) {
+  if (!(m > 0.0f)) return 0;
+  int ex;
+  frexpf(m, &ex);
+  const int sh = ex - 15;
+  return sh < -110 ? -110 : (sh > 110 ? 110 : sh);
+}
+
 // ------------------------------------------------------------------ launchers
 struct LaunchCfg {
   cudaStream_t stream;
@@ -368,12 +498,23 @@ cudaError_t launch_gateup(const LaunchCfg& lc, const PackView& pk, const WsView&
 cudaError_t launch_down(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
                         bool h_resident);
 cudaError_t launch_combine(const LaunchCfg& lc, const WsView& ws, uint16_t* out);
+// Fused narrow-call kernel (router .. combine in one launch): whether a shape fits it, and the
+// launch.
+bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom);
+cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
+                          float xS, float x_inv6S, const uint16_t* x, const uint16_t* wr,
+                          uint16_t* out);
 cudaError_t launch_pack_scales(cudaStream_t s, const uint8_t* raw_gate, const uint8_t* raw_up,
                                const uint8_t* raw_down, int E, int H, int I, uint8_t* gu_scales,
                                uint8_t* down_scales, uint8_t* sfa_gu, uint8_t* sfa_down);
 // Grouped tensor-core experts (W4A4, wide calls): activation permutation, gate/up, down.
 bool tc_supported();
-cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws, float xS);
+// W4A4 grouped experts on tcgen05: activation quantisation + permutation, gate/up, down.
+cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
+                              const uint16_t* x, float xS, float x_inv6S);
+// Router logits of a wide call on tcgen05 (BF16 x BF16 -> FP32).
+cudaError_t launch_tc_router(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
+                             const WsView& ws);
 cudaError_t launch_unpack_scales(cudaStream_t s, const uint8_t* gu_scales,
                                  const uint8_t* down_scales, int E, int H, int I, int expert,
                                  int which, uint8_t* raw_out);

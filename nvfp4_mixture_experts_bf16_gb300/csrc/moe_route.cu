@@ -27,29 +27,6 @@ struct RouteOut {
   int32_t* perm;
 };
 
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-
-// Sum of the 8 exact BF16 products of two uint4 chunks, as a fixed pairwise tree.
-__device__ __forceinline__ float dot8_bf16(const uint4& a, const uint4& b) {
-  const float p0 = bf16_lo(a.x) * bf16_lo(b.x), p1 = bf16_hi(a.x) * bf16_hi(b.x);
-  const float p2 = bf16_lo(a.y) * bf16_lo(b.y), p3 = bf16_hi(a.y) * bf16_hi(b.y);
-  const float p4 = bf16_lo(a.z) * bf16_lo(b.z), p5 = bf16_hi(a.z) * bf16_hi(b.z);
-  const float p6 = bf16_lo(a.w) * bf16_lo(b.w), p7 = bf16_hi(a.w) * bf16_hi(b.w);
-  return ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7));
-}
-
-// Power-of-two shift that puts a token's amax in [2^14, 2^15) for the f16 operand.
-__device__ __forceinline__ int token_shift(float amax) {
-  if (!(amax > 0.0f)) return 0;
-  int e;
-  frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
-  int s = e - 15;
-  return s < -110 ? -110 : (s > 110 ? 110 : s);
-}
-
-__device__ __forceinline__ float pow2f(int s) { return __int_as_float((127 + s) << 23); }
-
 // Prepare one 16-element block of token t: the f16 B operand (and the W4A4 codes/scales).
 __device__ __forceinline__ void prep_block(const uint16_t* xrow, int b, int t, const WsView& ws,
                                            int mode, float xS, float x_inv6S, int shift) {
@@ -84,40 +61,6 @@ __device__ __forceinline__ void prep_block(const uint16_t* xrow, int b, int t, c
   __half* row = ws.xh + (size_t)t * H + J * 128 + 8 * c;
   *reinterpret_cast<uint4*>(row + 32 * p0) = *reinterpret_cast<uint4*>(&hv[0]);
   *reinterpret_cast<uint4*>(row + 32 * (p0 + 1)) = *reinterpret_cast<uint4*>(&hv[8]);
-}
-
-// Warp-level top-k of one token's logits held in shared memory (entries are overwritten with
-// NaN once taken). Selection order: larger logit first, equal logits -> lower index first.
-__device__ void warp_topk(float* vals, int E, int k, int lane, int32_t* sel_idx,
-                          float* sel_val) {
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-    for (int e = lane; e < E; e += 32) {
-      const float v = vals[e];
-      if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, off);
-      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-    }
-    if (lane == 0) {
-      sel_idx[j] = bi;
-      sel_val[j] = bv;
-      if (bi < E) vals[bi] = __int_as_float(0x7FC00000);
-    }
-    __syncwarp();
-  }
-}
-
-// Softmax over the k selected logits (descending), FP32, fixed order.
-__device__ void topk_softmax(const float* sel_val, int k, float* w_out) {
-  const float m = sel_val[0];
-  float z = 0.0f;
-  for (int j = 0; j < k; ++j) z += expf(sel_val[j] - m);
-  for (int j = 0; j < k; ++j) w_out[j] = expf(sel_val[j] - m) / z;
 }
 
 // Block-wide exclusive scan of n <= 4 * blockDim ints in shared memory (in place); returns
@@ -286,23 +229,31 @@ __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict
   __threadfence();
 
   const int S = T * k;
-  float* lg = reinterpret_cast<float*>(smem);              // [T][E]
-  int32_t* sel_idx = reinterpret_cast<int32_t*>(lg + (size_t)T * E);   // [S]
-  float* sel_val = reinterpret_cast<float*>(sel_idx + S);             // [S]
-  float* sel_w = sel_val + S;                                         // [S]
+  int32_t* sel_idx = reinterpret_cast<int32_t*>(smem);                // [S]
+  float* sel_w = reinterpret_cast<float*>(sel_idx + S);               // [S]
   int32_t* cnt = reinterpret_cast<int32_t*>(sel_w + S);               // [E+1]
   int32_t* uq = cnt + (E + 1);                                        // [E+1]
-  int32_t* perm_s = uq + (E + 1);                                     // [S]
+  uint32_t* tmask = reinterpret_cast<uint32_t*>(uq + (E + 1));        // [E] tokens per expert
+  int32_t* perm_s = reinterpret_cast<int32_t*>(tmask + E);            // [S]
 
-  for (int i = tid; i < T * E; i += 256) lg[i] = __ldcg(ws.logits + i);
-  for (int e = tid; e <= E; e += 256) cnt[e] = 0;
-  __syncthreads();
+  for (int e = tid; e <= E; e += 256) {
+    cnt[e] = 0;
+    if (e < E) tmask[e] = 0u;
+  }
   if (warp < T) {
-    warp_topk(lg + (size_t)warp * E, E, k, lane, sel_idx + warp * k, sel_val + warp * k);
-    if (lane == 0) topk_softmax(sel_val + warp * k, k, sel_w + warp * k);
+    int e_sel;
+    float w_sel;
+    topk_row(ws.logits + (size_t)warp * E, E, k, lane, e_sel, w_sel);
+    if (lane < k) {
+      sel_idx[warp * k + lane] = e_sel;
+      sel_w[warp * k + lane] = w_sel;
+    }
   }
   __syncthreads();
-  if (tid < S) atomicAdd(&cnt[sel_idx[tid]], 1);
+  if (tid < S) {
+    atomicAdd(&cnt[sel_idx[tid]], 1);
+    atomicOr(&tmask[sel_idx[tid]], 1u << (tid / k));
+  }
   __syncthreads();
   for (int e = tid; e < E; e += 256) {
     uq[e] = cnt[e] > 0 ? 1 : 0;
@@ -323,10 +274,10 @@ __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict
     ws.ctl[kCtlUnique] = U;
   }
   if (tid < S) {
+    // a token selects an expert at most once: its rank among the expert's slots is the number
+    // of earlier tokens that selected the same expert
     const int t = tid / k, e = sel_idx[tid];
-    int rank = 0;
-    for (int s2 = 0; s2 < t * k; ++s2) rank += (sel_idx[s2] == e) ? 1 : 0;
-    const int pos = cnt[e] + rank;
+    const int pos = cnt[e] + __popc(tmask[e] & ((1u << t) - 1u));
     perm_s[pos] = t;
     out.perm[pos] = t;
     ws.perm[pos] = t;
@@ -343,9 +294,6 @@ __global__ void __launch_bounds__(256) k_route_narrow(const uint16_t* __restrict
     const int c = ((e + 1 < E) ? cnt[e + 1] : S) - cnt[e];
     if (c > 0) {
       const int u = uq[e];
-      ws.grp_expert[u] = e;
-      ws.grp_slot[u] = cnt[e];
-      ws.grp_n[u] = c;
       write_group(ws, pk, u, e, cnt[e], c, perm_s);
     }
   }
@@ -464,27 +412,20 @@ __global__ void __launch_bounds__(256) k_router_gemm(const uint16_t* __restrict_
 
 // ------------------------------------------------------------------ wide top-k
 __global__ void __launch_bounds__(256) k_topk_wide(WsView ws, RouteOut out) {
-  extern __shared__ __align__(16) unsigned char smem[];
   const int E = ws.E, k = ws.k, T = ws.T;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();
   pdl_launch_dependents();
-  float* vals = reinterpret_cast<float*>(smem) + (size_t)warp * (E + 2 * 32 + 32);
-  int32_t* sidx = reinterpret_cast<int32_t*>(vals + E);
-  float* sval = reinterpret_cast<float*>(sidx + 32);
-  float* sw = sval + 32;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
-  for (int e = lane; e < E; e += 32) vals[e] = ws.logits[(size_t)t * E + e];
-  __syncwarp();
-  warp_topk(vals, E, k, lane, sidx, sval);
-  if (lane == 0) topk_softmax(sval, k, sw);
-  __syncwarp();
-  for (int j = lane; j < k; j += 32) {
-    out.idx[(size_t)t * k + j] = sidx[j];
-    out.w[(size_t)t * k + j] = sw[j];
-    ws.idx[(size_t)t * k + j] = sidx[j];
-    ws.w[(size_t)t * k + j] = sw[j];
+  int e_sel;
+  float w_sel;
+  topk_row(ws.logits + (size_t)t * E, E, k, lane, e_sel, w_sel);
+  if (lane < k) {
+    out.idx[(size_t)t * k + lane] = e_sel;
+    out.w[(size_t)t * k + lane] = w_sel;
+    ws.idx[(size_t)t * k + lane] = e_sel;
+    ws.w[(size_t)t * k + lane] = w_sel;
   }
 }
 
@@ -518,11 +459,17 @@ __global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, PackView pkv, int
   pdl_launch_dependents();
   int run = 0;
   if (e < E) {
-    for (int c = 0; c < nchunk; ++c) {
-      int32_t* p = ws.chunk_base + (size_t)c * E + e;
-      const int v = *p;
-      *p = run;
-      run += v;
+    // in place: chunk counts -> chunk prefixes of expert e, 16 loads in flight per round
+    int32_t* col = ws.chunk_base + e;
+    for (int c0 = 0; c0 < nchunk; c0 += 16) {
+      int v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) v[u] = c0 + u < nchunk ? col[(size_t)(c0 + u) * E] : 0;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        if (c0 + u < nchunk) col[(size_t)(c0 + u) * E] = run;
+        run += v[u];
+      }
     }
   }
   const int cnt_e = e < E ? run : 0;
@@ -556,13 +503,12 @@ __global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, PackView pkv, int
     out.offsets[e] = off_e;
     ws.counts[e] = cnt_e;
     ws.offsets[e] = off_e;
-    for (int q = 0; q < ng_e; ++q) {
-      ws.grp_expert[gbase + q] = e;
-      ws.grp_slot[gbase + q] = off_e + q * kGroup;
-      ws.grp_n[gbase + q] = min(kGroup, cnt_e - q * kGroup);
-      write_group(ws, pk, gbase + q, e, off_e + q * kGroup, min(kGroup, cnt_e - q * kGroup),
-                  nullptr);
-    }
+    // token groups of <= 8 slots feed the mma.sync expert kernels; the tensor-core path
+    // reads the 128-slot token tiles instead
+    if (!ws.tt_expert)
+      for (int q = 0; q < ng_e; ++q)
+        write_group(ws, pk, gbase + q, e, off_e + q * kGroup, min(kGroup, cnt_e - q * kGroup),
+                    nullptr);
     if (ws.tt_expert) {
       ws.ttbase[e] = tbase;
       for (int q = 0; q < nt_e; ++q) {
@@ -683,7 +629,7 @@ cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t
 
 size_t route_narrow_smem_bytes(int T, int H, int E, int k) {
   const size_t xbytes = (size_t)T * H * 2 + (size_t)kRouteRows * H * 2;
-  const size_t fin = (size_t)T * E * 4 + (size_t)T * k * 16 + (size_t)(E + 1) * 8 + 64;
+  const size_t fin = (size_t)T * k * 12 + (size_t)(E + 1) * 12 + 64;
   return xbytes > fin ? xbytes : fin;
 }
 
@@ -721,13 +667,17 @@ cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint
   const PackView pkv = pk ? *pk : PackView{};
   RouteOut out{out_idx, out_w, out_counts, out_offsets, out_perm};
   cudaError_t e;
-  dim3 gg((ws.E + kGN - 1) / kGN, (ws.T + kGM - 1) / kGM);
-  e = launch(lc, k_router_gemm, gg, dim3(256), 0, x, wr, ws);
+  const bool tc = ws.H % 64 == 0 && ((reinterpret_cast<uintptr_t>(x) |
+                                       reinterpret_cast<uintptr_t>(wr)) & 15) == 0 &&
+                  tc_supported();
+  if (tc) {
+    e = launch_tc_router(lc, x, wr, ws);
+  } else {
+    dim3 gg((ws.E + kGN - 1) / kGN, (ws.T + kGM - 1) / kGM);
+    e = launch(lc, k_router_gemm, gg, dim3(256), 0, x, wr, ws);
+  }
   if (e != cudaSuccess) return e;
-  const size_t tk_smem = (size_t)8 * (ws.E + 96) * 4;
-  e = cudaFuncSetAttribute(k_topk_wide, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tk_smem);
-  if (e != cudaSuccess) return e;
-  e = launch(lc, k_topk_wide, dim3((ws.T + 7) / 8), dim3(256), tk_smem, ws, out);
+  e = launch(lc, k_topk_wide, dim3((ws.T + 7) / 8), dim3(256), 0, ws, out);
   if (e != cudaSuccess) return e;
   const int nchunk = (ws.T + kChunkTok - 1) / kChunkTok;
   e = launch(lc, k_hist_wide, dim3(nchunk), dim3(256), (size_t)ws.E * 4, ws);

@@ -40,6 +40,7 @@ constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;                    // two per tensor-memory lane quadrant
 constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue warps
 constexpr int kStageF = kTileN + 4;             // padded row of the epilogue staging (floats)
+constexpr int kYStride = kTileM + 8;            // padded slot column of the down staging (BF16)
 constexpr int kTmemCols = 512;
 constexpr int kSfCol = 256;                     // scale factors after two 128-column accumulators
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
@@ -279,16 +280,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN;
-      // accumulators -> shared memory (this warp: its 32 rows x 64 columns), then release TMEM
-      for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
-        uint32_t r[32];
-        ld32(tbase + c0, r);
-        float4* dst = reinterpret_cast<float4*>(acc_s + row * kStageF + c0);
+      if (!DOWN) {
+        // accumulators -> shared memory (this warp: its 32 rows x 64 columns)
+        for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
+          uint32_t r[32];
+          ld32(tbase + c0, r);
+          float4* dst = reinterpret_cast<float4*>(acc_s + row * kStageF + c0);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        }
+      } else {
+        // Y = BF16(acc * md), transposed into shared memory as [slot column][row] so that each
+        // slot's 128 rows leave as contiguous 16-byte stores; lanes (rows) write consecutive
+        // 2-byte words of one column, free of bank conflicts
+        const float md = prm.mult[e * 3 + 2] * prm.dscale[e];
+        uint16_t* yt = reinterpret_cast<uint16_t*>(acc_s);
+        for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
+          uint32_t r[32];
+          ld32(tbase + c0, r);
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            yt[(c0 + q) * kYStride + row] = f32_to_bf16_rn(__uint_as_float(r[q]) * md);
+        }
       }
+      // release the accumulator buffer to the MMA warp
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -330,13 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ws.hsf[slot * (I / 16) + ib] = (uint8_t)sf;
         }
       } else {
-        // Y[slot][row] for this tile's 128 rows: a warp writes 32 consecutive rows of one slot
-        const float md = prm.mult[e * 3 + 2] * prm.dscale[e];
-        for (int idx = etid; idx < kTileM * kTileN; idx += kEpiWarps * 32) {
-          const int col = idx / kTileM, r = idx % kTileM;
+        // Y[slot0 + col][mt*128 .. +127]: 16 chunks of 8 rows per slot, one 16-byte store each
+        const uint16_t* yt = reinterpret_cast<const uint16_t*>(acc_s);
+        for (int id = etid; id < kTileN * (kTileM / 8); id += kEpiWarps * 32) {
+          const int col = id >> 4, r8 = id & 15;
           if (col < nval)
-            ws.y[(size_t)(slot0 + col) * H + mt * 128 + r] =
-                f32_to_bf16_rn(acc_s[r * kStageF + col] * md);
+            *reinterpret_cast<uint4*>(ws.y + (size_t)(slot0 + col) * H + mt * 128 + r8 * 8) =
+                *reinterpret_cast<const uint4*>(yt + col * kYStride + r8 * 8);
         }
       }
       epi_sync();   // the staging buffer is reused by the next tile
@@ -351,31 +368,210 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
 }
 
-// ------------------------------------------------------------------ activations by pslot
-// For every slot: copy the token's NVFP4 codes to its padded permuted row and scatter its scales
-// into the scale-factor atoms of its token tile. One 128-thread CTA per slot.
-__global__ void __launch_bounds__(128) k_x_perm(WsView ws) {
+// ------------------------------------------------------------------ router GEMM (BF16)
+// logits[T][E] = x[T][H] . Wr[E][H]^T on tcgen05.mma kind::f16 (BF16 x BF16 -> FP32 in tensor
+// memory): A = 128 router rows, B = 128 tokens, K = 64 per stage (one 128-byte swizzle atom),
+// four K = 16 instructions per stage. Warp 0: TMA producer; warp 1: MMA; warps 2..5: epilogue.
+constexpr int kRStages = 4;
+constexpr int kRThreads = 192;
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(kIdescBf16), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kRThreads, 1)
+    k_tc_router(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+                WsView ws) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t full[kRStages], empty[kRStages], acc_full[2], acc_empty[2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_s;
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* smem = smem_raw + pad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = ws.T, H = ws.H, E = ws.E;
+  if (tid == 0) {
+    for (int s = 0; s < kRStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    fence_mbar_init();
+    abort_s = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base_s)),
+                 "r"(256)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_s;
   pdl_wait();
   pdl_launch_dependents();
-  const int s = blockIdx.x;
-  const int H = ws.H, E = ws.E;
-  if (s >= ws.T * ws.k) return;
-  // expert of slot s: last e with offsets[e] <= s (binary search over E+1 offsets)
-  int lo = 0, hi = E;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (ws.offsets[mid] <= s) lo = mid; else hi = mid;
+  const int ME = (E + kTileM - 1) / kTileM, NTk = (T + kTileN - 1) / kTileN;
+  const int ntiles = ME * NTk;
+  const int nks = H / 64;
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles && !abort_s; t += gridDim.x) {
+        const int me = t % ME, nt = t / ME;   // consecutive tiles share the token tile
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % kRStages, n = it / kRStages;
+          if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+            break;
+          }
+          unsigned char* st = smem + s * 2 * kTileBytes;
+          mbar_arrive_expect_tx(&full[s], 2 * kTileBytes);
+          tma_2d(st, &tm_w, ks * 128, me * kTileM, &full[s]);
+          tma_2d(st + kTileBytes, &tm_x, ks * 128, nt * kTileN, &full[s]);
+        }
+      }
+      const int used = it < kRStages ? it : kRStages;
+      for (int i = 0; i < used; ++i) {
+        const int c = it - 1 - i;
+        (void)mbar_wait(&full[c % kRStages], (c / kRStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
+        const int buf = tcount & 1, use = tcount >> 1;
+        if (use > 0 && !abort_s && !mbar_wait(&acc_empty[buf], (use - 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        fence_after();
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % kRStages, n = it / kRStages;
+          if (!abort_s && !mbar_wait(&full[s], n & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          fence_after();
+          const uint32_t a0 = smem_u32(smem + s * 2 * kTileBytes);
+          const uint32_t b0 = a0 + kTileBytes;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            mma_bf16(tmem + buf * kTileN, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32),
+                     (ks > 0 || q > 0) ? 1u : 0u);
+          commit(&empty[s]);
+        }
+        commit(&acc_full[buf]);
+      }
+    }
+  } else {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;     // router row inside the tile
+    int tcount = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
+      const int me = t % ME, nt = t / ME;
+      const int buf = tcount & 1, use = tcount >> 1;
+      if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
+        record_status(ws.ctl, kStTimeout);
+        abort_s = 1;
+      }
+      __syncwarp();
+      fence_after();
+      const int e = me * kTileM + row;
+      const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN;
+      for (int c0 = 0; c0 < kTileN; c0 += 32) {
+        uint32_t r[32];
+        ld32(tbase + c0, r);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int tok = nt * kTileN + c0 + q;
+          if (tok < T && e < E) ws.logits[(size_t)tok * E + e] = __uint_as_float(r[q]);
+        }
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
   }
-  const int e = lo;
-  const int rank = s - ws.offsets[e];
-  const int j = ws.ttbase[e] + rank / 128, r = rank % 128;
-  const int t = ws.perm[s];
-  const uint4* src = reinterpret_cast<const uint4*>(ws.xq + (size_t)t * (H / 2));
-  uint4* dst = reinterpret_cast<uint4*>(ws.xq_perm + ((size_t)j * 128 + r) * (H / 2));
-  for (int i = threadIdx.x; i < H / 32; i += 128) dst[i] = src[i];
-  for (int b = threadIdx.x; b < H / 16; b += 128)
-    ws.xsf_atoms[((size_t)j * (H / 64) + b / 4) * 512 + sf_atom_byte(r, b & 3)] =
-        ws.xsf[(size_t)t * (H / 16) + b];
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256)
+                 : "memory");
+}
+
+// ------------------------------------------------------------------ activations by pslot
+// W4A4 activations of the grouped path in one pass: 64 threads per token quantise its row
+// (four 16-element blocks per thread, the quantiser Q with the gate/up input scale), publish the
+// codes and scales by token, and write the token's k copies into the padded permuted operand
+// ("pslot" = 128 * token tile + rank in the tile) with their scale-factor atom words.
+constexpr int kXqTok = 4;   // tokens per CTA
+
+__global__ void __launch_bounds__(64 * kXqTok) k_xquant_perm(const uint16_t* __restrict__ x,
+                                                             WsView ws, float xS, float x_inv6S) {
+  __shared__ int pslot_s[kXqTok][32];
+  const int H = ws.H, k = ws.k;
+  const int tl = threadIdx.x >> 6, q = threadIdx.x & 63;
+  const int t = blockIdx.x * kXqTok + tl;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (t < ws.T && q < k) {
+    const int s = ws.slot_of[(size_t)t * k + q], e = ws.idx[(size_t)t * k + q];
+    pslot_s[tl][q] = ws.ttbase[e] * 128 + (s - ws.offsets[e]);
+  }
+  __syncthreads();
+  if (t >= ws.T) return;
+  for (int g = q; g < H / 64; g += 64) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + (size_t)g * 64);
+    uint4 u[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[i] = src[i];
+    uint32_t cw[8], sfw = 0;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+      const uint32_t w8[8] = {u[2 * blk].x, u[2 * blk].y, u[2 * blk].z, u[2 * blk].w,
+                              u[2 * blk + 1].x, u[2 * blk + 1].y, u[2 * blk + 1].z,
+                              u[2 * blk + 1].w};
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_lo(w8[i]);
+        v[2 * i + 1] = bf16_hi(w8[i]);
+      }
+      uint32_t c2[2];
+      const uint32_t sf = quantize16(v, xS, x_inv6S, c2);
+      cw[2 * blk] = c2[0];
+      cw[2 * blk + 1] = c2[1];
+      sfw |= sf << (8 * blk);
+    }
+    const uint4 c_lo = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    const uint4 c_hi = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    uint4* xd = reinterpret_cast<uint4*>(ws.xq + (size_t)t * (H / 2) + (size_t)g * 32);
+    xd[0] = c_lo;
+    xd[1] = c_hi;
+    *reinterpret_cast<uint32_t*>(ws.xsf + (size_t)t * (H / 16) + (size_t)g * 4) = sfw;
+    for (int j = 0; j < k; ++j) {
+      const int row = pslot_s[tl][j], tile = row >> 7, r = row & 127;
+      uint4* pd = reinterpret_cast<uint4*>(ws.xq_perm + (size_t)row * (H / 2) + (size_t)g * 32);
+      pd[0] = c_lo;
+      pd[1] = c_hi;
+      *reinterpret_cast<uint32_t*>(ws.xsf_atoms + ((size_t)tile * (H / 64) + g) * 512 +
+                                   sf_atom_byte(r, 0)) = sfw;
+    }
+  }
 }
 
 }  // namespace tc
@@ -439,8 +635,23 @@ size_t tc_smem_bytes() {
   return (size_t)tc::kStages * tc::kStageBytes + (size_t)tc::kTileM * tc::kStageF * 4 + 1024;
 }
 
+cudaError_t launch_tc_router(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
+                             const WsView& ws) {
+  CUtensorMap m_w, m_x;
+  if (!make_map(&m_w, wr, (uint64_t)ws.H * 2, (uint64_t)ws.E, 128) ||
+      !make_map(&m_x, x, (uint64_t)ws.H * 2, (uint64_t)ws.T, 128))
+    return cudaErrorInvalidValue;
+  const size_t smem = (size_t)tc::kRStages * 2 * tc::kTileBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(tc::k_tc_router, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = ((ws.E + 127) / 128) * ((ws.T + 127) / 128);
+  const int grid = tiles < lc.num_sms ? tiles : lc.num_sms;
+  return launch(lc, tc::k_tc_router, dim3(grid), dim3(tc::kRThreads), smem, m_w, m_x, ws);
+}
+
 cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
-                              float xS) {
+                              const uint16_t* x, float xS, float x_inv6S) {
   const int H = pk.H, I = pk.I, E = pk.E;
   const uint64_t P = (uint64_t)ws.NT * 128;
   CUtensorMap m_gate, m_up, m_x, m_down, m_h;
@@ -450,7 +661,8 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
       !make_map(&m_down, pk.down_codes, I / 2, (uint64_t)E * H, 128) ||
       !make_map(&m_h, ws.hq_perm, I / 2, P, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch(lc, tc::k_x_perm, dim3(ws.T * ws.k), dim3(128), 0, ws);
+  cudaError_t e = launch(lc, tc::k_xquant_perm, dim3((ws.T + tc::kXqTok - 1) / tc::kXqTok),
+                         dim3(64 * tc::kXqTok), 0, x, ws, xS, x_inv6S);
   if (e != cudaSuccess) return e;
   const size_t smem = tc_smem_bytes();
   e = cudaFuncSetAttribute(tc::k_tc_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
