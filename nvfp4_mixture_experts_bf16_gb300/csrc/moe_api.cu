@@ -66,7 +66,7 @@ int num_sms_of_current_device() {
 
 struct WsLayout {
   size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm,
-      chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
+      chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, htag, ytag, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
       xsf_atoms, hq_perm, hsf_atoms, total;
   size_t slot_amax_bytes;
   int G, NT;
@@ -84,7 +84,8 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
   L.gmeta = take((size_t)L.G * sizeof(moe::GroupMeta));
   L.slot_amax_bytes = mode == 0 ? (size_t)S * 4 : 0;
   L.slot_amax = take(L.slot_amax_bytes);
-  L.logits = take((size_t)T * E * 4);
+  const bool narrow = T <= moe::kNarrowT;
+  L.logits = take((size_t)T * E * (narrow ? 8 : 4));
   L.idx = take((size_t)S * 4);
   L.w = take((size_t)S * 4);
   L.slot_of = take((size_t)S * 4);
@@ -100,6 +101,8 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
   L.hq = take(mode == 1 ? (size_t)S * I / 2 : 0);
   L.hsf = take(mode == 1 ? (size_t)S * I / 16 : 0);
   L.y = take(mode >= 0 ? (size_t)S * H * 2 : 0);
+  L.htag = take(mode >= 0 && narrow ? (size_t)S * (I / 16) * 9 * 8 : 0);
+  L.ytag = take(mode >= 0 && narrow ? (size_t)S * (H / 2) * 8 : 0);
   // grouped tensor-core path (wide W4A4): 128-slot token tiles in a padded permuted space
   const bool tc = mode == 1 && T > moe::kNarrowT;
   L.NT = tc ? (int)((S + 127) / 128 + (S < E ? S : E)) : 0;
@@ -138,6 +141,8 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   v.hq = b + L.hq;
   v.hsf = b + L.hsf;
   v.y = reinterpret_cast<uint16_t*>(b + L.y);
+  v.htag = reinterpret_cast<unsigned long long*>(b + L.htag);
+  v.ytag = reinterpret_cast<unsigned long long*>(b + L.ytag);
   v.T = T; v.H = H; v.E = E; v.k = k; v.I = I; v.G = L.G; v.NT = L.NT;
   const bool tc = L.NT > 0;
   v.tt_expert = tc ? reinterpret_cast<int32_t*>(b + L.tt_expert) : nullptr;

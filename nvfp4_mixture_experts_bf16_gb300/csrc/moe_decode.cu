@@ -4,26 +4,28 @@
 // The pages' engine runs this step as a chain of small kernels joined by programmatic dependent
 // launch (release notes "Infernix windows-2026.10.11", section "Highlights"). At one token the
 // step moves ~26 MB, about 4 us of HBM time, while every kernel boundary costs a few
-// microseconds of drain, launch and first-copy latency. Here one CTA per SM runs every phase,
-// and CTAs meet only at two grid-wide barriers (bounded spins on counters in the workspace):
+// microseconds of drain, launch and first-copy latency, and every grid-wide barrier a couple of
+// global round trips. Here one CTA per SM runs every phase, and CTAs never meet at a barrier:
+// data that another CTA produces (logits, h, Y) is also written as 64-bit words {data, epoch of
+// the call}, single-copy atomic, and the consumer polls the data itself (bounded) until it
+// carries the current epoch. The epoch lives in the workspace; the last CTA of a call advances
+// it.
 //
 //   1. router: each CTA copies its 3-4 router rows (TMA bulk copy, issued before waiting for
 //      the preceding kernel: the router does not depend on it) and the T activation rows, and
-//      writes its logits.                                                    -> barrier 1
-//      While waiting, each CTA converts the activations into the f16 (W4A16) or NVFP4-decoded
-//      (W4A4) MMA operand in its own shared memory, and writes its share of the W4A4 codes.
-//   2. routing: every CTA selects the top-k of every token itself (one warp per token) and
-//      builds the expert groups in shared memory; no second barrier is needed. CTA 0 publishes
-//      idx / w / counts / offsets / perm / slot_of.
-//   3. gate/up + SiLU*up: tasks (group, 16-row tile of I), as in the multi-kernel path.
-//      As soon as its last gate/up stage is free, the producer warp streams this CTA's down
-//      weights into the same shared memory, so they load while h is finished elsewhere.
-//                                                                            -> barrier 2
-//   4. down: tasks (group, 128-row tile of H); each task writes Y (BF16). The CTA that finishes
-//      the last task of a 128-row tile (a ticket per tile) forms out for those rows: the
-//      fixed-order weighted sum over each token's k experts (rank order, FP32, then BF16).
-//
-// Every product, rounding and summation order is the one of the multi-kernel path.
+//      writes its tagged logits. Then it converts the activations into the f16 (W4A16) or
+//      NVFP4-decoded (W4A4) MMA operand in its own shared memory and writes its share of the
+//      W4A4 codes.
+//   2. routing: every CTA selects the top-k of every token itself (one warp per token, from the
+//      tagged logits), sorts the T*k selections by expert and builds the expert groups in shared
+//      memory. CTA 0 publishes idx / w / counts / offsets / perm / slot_of.
+//   3. gate/up + SiLU*up: tasks (group, 16-row tile of I), as in the multi-kernel path; h is
+//      written plain and tagged. As soon as its last gate/up stage is free, the producer warp
+//      streams this CTA's down weights into the same shared memory.
+//   4. down: tasks (group, 128-row tile of H); a task waits only for its own group's tagged h.
+//      Each task writes Y (BF16), plain and tagged.
+//   5. combine: CTA j (mod the grid) forms 128-row tile j of out once its tagged Y has arrived:
+//      the fixed-order weighted sum over each token's k experts (rank order, FP32, then BF16).
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -34,17 +36,14 @@ constexpr int kDcThreads = (kDcWarps + 1) * 32;   // + one producer warp
 constexpr int kDcCons = kDcWarps * 32;
 constexpr int kDnRows = 128;                      // rows of H per down task (16 per warp)
 constexpr int kDcSmemMax = 232448;                // 227 KB opt-in per block
-constexpr int kDcStatic = 512;                    // static shared memory allowance
+constexpr int kDcStatic = 1024;                   // static shared memory allowance
 
 // One expert's token group (<= 8 tokens) of the current call.
 struct DcGroup {
   int expert, slot0, n;
   uint32_t toks;          // token of column c in bits 4c .. 4c+3
-  float mg, mu, md, sd;   // gate/up/down multipliers, down input scale
-  float i6d;              // fl32(1 / fl32(6 * sd))
-  int pad[3];
 };
-static_assert(sizeof(DcGroup) == 48, "DcGroup layout");
+static_assert(sizeof(DcGroup) == 16, "DcGroup layout");
 
 struct DcGeom {
   int rows_max;                 // router rows of one CTA, at most
@@ -53,6 +52,7 @@ struct DcGeom {
   int gu_stage, gu_stages;
   int dn_stage, dn_stages;
   int arena;                    // router rows + raw x | routing scratch | gate/up ring | down ring
+                                // | combine staging
   int x_stride;                 // 2H + 64: one x operand row
   int h_stride;                 // 2I + 16: one h operand row
   int xop;                      // x operand rows, later the h operand rows of one group
@@ -60,55 +60,112 @@ struct DcGeom {
   int smem;
 };
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// Tagged words: {data in the low 32 bits, epoch of the writing call in the high 32 bits}, stored
+// and loaded as single 64-bit accesses, which are single-copy atomic: a reader that sees the
+// current epoch sees the data written with it, with no fence or barrier on either side.
+__device__ __forceinline__ void st_tag(unsigned long long* p, uint32_t data, uint32_t ep) {
+  const unsigned long long v = ((unsigned long long)ep << 32) | data;
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_tag(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t tag_of(unsigned long long v) { return (uint32_t)(v >> 32); }
+__device__ __forceinline__ uint32_t data_of(unsigned long long v) { return (uint32_t)v; }
 
-// Grid barrier halves (thread 0 of the CTA; the callers synchronise the CTA around them).
-__device__ __forceinline__ void grid_arrive(uint32_t* ctr) {
-  __threadfence();
-  atomicAdd(ctr, 1u);
+__device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t* ctr) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(ctr), "r"(1u)
+               : "memory");
+  return old;
 }
-__device__ __forceinline__ bool grid_wait(const uint32_t* ctr, uint32_t target) {
-  if (ld_acquire(ctr) >= target) return true;
+
+// Top-k + softmax of one token from its tagged logits: polls (bounded) until every logit of
+// the current epoch has arrived. False on timeout.
+template <int V>
+__device__ __forceinline__ bool topk_tagged_v(const unsigned long long* row, int E, int k,
+                                              int lane, uint32_t ep, int& e_out, float& w_out) {
+  uint32_t key[V];
+  uint32_t pending = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = 0u;
+    if (e < E) {
+      const unsigned long long w = ld_tag(row + e);
+      if (tag_of(w) == ep) key[i] = logit_key(__uint_as_float(data_of(w)));
+      else pending |= 1u << i;
+    }
+  }
+  bool ok = true;
+  if (__any_sync(0xFFFFFFFFu, pending != 0u)) {
+    const uint64_t t0 = globaltimer_ns();
+    while (__any_sync(0xFFFFFFFFu, pending != 0u)) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        if (pending & (1u << i)) {
+          const unsigned long long w = ld_tag(row + lane + 32 * i);
+          if (tag_of(w) == ep) {
+            key[i] = logit_key(__uint_as_float(data_of(w)));
+            pending &= ~(1u << i);
+          }
+        }
+      }
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  warp_select_softmax<V>(key, k, lane, e_out, w_out);
+  return ok;
+}
+
+__device__ __forceinline__ bool topk_tagged(const unsigned long long* row, int E, int k, int lane,
+                                            uint32_t ep, int& e_out, float& w_out) {
+  if (E <= 128) return topk_tagged_v<4>(row, E, k, lane, ep, e_out, w_out);
+  if (E <= 256) return topk_tagged_v<8>(row, E, k, lane, ep, e_out, w_out);
+  if (E <= 512) return topk_tagged_v<16>(row, E, k, lane, ep, e_out, w_out);
+  return topk_tagged_v<32>(row, E, k, lane, ep, e_out, w_out);
+}
+
+// Polls n tagged words (bounded) until all carry epoch ep. False on timeout.
+template <int n>
+__device__ __forceinline__ bool poll_tags(const unsigned long long* p, uint32_t ep,
+                                          unsigned long long (&out)[n]) {
+  bool all = true;
+#pragma unroll
+  for (int i = 0; i < n; ++i) {
+    out[i] = ld_tag(p + i);
+    all &= tag_of(out[i]) == ep;
+  }
+  if (all) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    for (int i = 0; i < 16; ++i)
-      if (ld_acquire(ctr) >= target) return true;
+    all = true;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      if (tag_of(out[i]) != ep) out[i] = ld_tag(p + i);
+      all &= tag_of(out[i]) == ep;
+    }
+    if (all) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 
 __device__ __forceinline__ int group_tok(uint32_t toks, int c) { return (toks >> (4 * c)) & 0xF; }
 
-// Exclusive scan of a[0..n) in place by one warp; returns the total.
-__device__ __forceinline__ int warp_exclusive_scan(int32_t* a, int n, int lane) {
-  const int per = (n + 31) / 32;
-  const int b0 = lane * per, b1 = min(n, b0 + per);
-  int s = 0;
-  for (int i = b0; i < b1; ++i) s += a[i];
-  int incl = s;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  int run = incl - s;
-  for (int i = b0; i < b1; ++i) {
-    const int v = a[i];
-    a[i] = run;
-    run += v;
-  }
-  return __shfl_sync(0xFFFFFFFFu, incl, 31);
-}
-
+// Contiguous share of ntasks for this CTA (ntasks * gridDim.x < 2^31 for every valid shape).
 __device__ __forceinline__ void balanced_range(int ntasks, int& q0, int& q1) {
-  q0 = (int)(((long long)ntasks * blockIdx.x) / gridDim.x);
-  q1 = (int)(((long long)ntasks * (blockIdx.x + 1)) / gridDim.x);
+  q0 = (int)(((unsigned)ntasks * blockIdx.x) / gridDim.x);
+  q1 = (int)(((unsigned)ntasks * (blockIdx.x + 1)) / gridDim.x);
 }
 
+template <int NT>
 __global__ void __launch_bounds__(kDcThreads, 1)
     k_decode(PackView pk, WsView ws, DcGeom geo, const uint16_t* __restrict__ x,
              const uint16_t* __restrict__ wr, int mode, float xS, float x_inv6S,
@@ -129,17 +186,19 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   uint64_t* dempty = dfull + geo.dn_stages;
   uint64_t* rbar = dempty + geo.dn_stages;
   uint64_t* xbar = rbar + 1;
-  __shared__ float xfac_s[kNarrowT];
-  __shared__ int shift_s[kNarrowT];
-  __shared__ float hfac_s[kGroup], hinv_s[kGroup];
-  __shared__ int U_s, last_s;
+  __shared__ float xfac_s[NT];
+  __shared__ int shift_s[NT];
+  __shared__ float hfac_s[kGroup];
+  __shared__ uint32_t hamax_s[kGroup];
+  __shared__ int wcount_s[kDcWarps + 1];
   __shared__ volatile int abort_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int T = ws.T, H = ws.H, E = ws.E, k = ws.k, I = ws.I, S = T * k;
+  constexpr int T = NT;
+  const int H = ws.H, E = ws.E, k = ws.k, I = ws.I, S = T * k;
   const int G = gridDim.x, b = blockIdx.x;
-  const int row0 = (int)(((long long)E * b) / G);
-  const int nrows = (int)(((long long)E * (b + 1)) / G) - row0;
+  const int row0 = (E * b) / G;
+  const int nrows = (E * (b + 1)) / G - row0;
   uint16_t* wrs = reinterpret_cast<uint16_t*>(arena);                            // [rows][H]
   uint16_t* xraw = reinterpret_cast<uint16_t*>(arena + (size_t)geo.rows_max * H * 2);  // [T][H]
 
@@ -169,19 +228,22 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     mbar_arrive_expect_tx(xbar, (uint32_t)T * H * 2);
     bulk_g2s(xraw, x, (uint32_t)T * H * 2, xbar);
   }
-  if (b == 0 && mode == 0)
-    for (int i = tid; i < S; i += kDcThreads) ws.slot_amax[i] = 0u;
+  // this call's epoch: one past the last completed call's (never 0, the zeroed workspace's tag)
+  uint32_t ep = __ldcg(&ws.ctl[kCtlEpoch]) + 1u;
+  if (ep == 0u) ep = 1u;
   if ((nrows > 0 && !mbar_wait(rbar, 0)) || !mbar_wait(xbar, 0)) {
     record_status(ws.ctl, kStTimeout);
     abort_s = 1;
   }
 
-  // ---------------- 1. router rows (warps 0..7; warp w: row w / wpr, part w % wpr of H)
+  // ---------------- 1. router rows (warps 0..7; warp w: row w / wpr, part w % wpr of H); the
+  // warps of row 0 also take each token's max |x| over their part (for the f16 scaling)
+  float* amax_part = red + kDcWarps * NT;   // [wpr][NT]
   if (warp < kDcWarps) {
     const int r = warp / geo.wpr, part = warp % geo.wpr;
-    float acc[kNarrowT];
+    float acc[NT], am[NT];
 #pragma unroll
-    for (int t = 0; t < kNarrowT; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < NT; ++t) acc[t] = am[t] = 0.0f;
     if (r < nrows) {
       const int nchunk = H / (8 * geo.wpr);  // uint4 chunks of this warp's part of the row
       const uint4* wrow = reinterpret_cast<const uint4*>(wrs + (size_t)r * H) + part * nchunk;
@@ -189,50 +251,63 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       for (int i = lane; i < nchunk; i += 32) {
         const uint4 wv = wrow[i];
 #pragma unroll
-        for (int t = 0; t < kNarrowT; ++t) {
-          if (t < T) {
-            const uint4 xv = reinterpret_cast<const uint4*>(xraw + (size_t)t * H)[part * nchunk + i];
-            acc[t] += dot8_bf16(wv, xv);
+        for (int t = 0; t < NT; ++t) {
+          const uint4 xv = reinterpret_cast<const uint4*>(xraw + (size_t)t * H)[part * nchunk + i];
+          acc[t] += dot8_bf16(wv, xv);
+          if (r == 0) {
+            const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              am[t] = fmaxf(am[t], fmaxf(fabsf(bf16_lo(w4[q])), fabsf(bf16_hi(w4[q]))));
           }
         }
       }
+    } else if (nrows == 0 && warp < T) {
+      // no router row in this CTA: warp t takes token t's max |x| over the whole row
+      const uint32_t* xr = reinterpret_cast<const uint32_t*>(xraw + (size_t)warp * H);
+      for (int i = lane; i < H / 2; i += 32) {
+        const uint32_t v = xr[i];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          if (t == warp) am[t] = fmaxf(am[t], fmaxf(fabsf(bf16_lo(v)), fabsf(bf16_hi(v))));
+      }
     }
 #pragma unroll
-    for (int t = 0; t < kNarrowT; ++t) {
+    for (int t = 0; t < NT; ++t) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], off);
+      for (int off = 16; off > 0; off >>= 1) {
+        acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], off);
+        am[t] = fmaxf(am[t], __shfl_xor_sync(0xFFFFFFFFu, am[t], off));
+      }
     }
     if (lane == 0) {
 #pragma unroll
-      for (int t = 0; t < kNarrowT; ++t) red[warp * kNarrowT + t] = acc[t];
+      for (int t = 0; t < NT; ++t) {
+        red[warp * NT + t] = acc[t];
+        if (nrows > 0 && r == 0) amax_part[part * NT + t] = am[t];
+        if (nrows == 0 && warp == t) amax_part[t] = am[t];
+      }
     }
   }
   __syncthreads();
   if (tid < nrows * T) {
     const int rl = tid / T, t = tid % T;
-    float s = red[(rl * geo.wpr) * kNarrowT + t];
-    for (int p = 1; p < geo.wpr; ++p) s += red[(rl * geo.wpr + p) * kNarrowT + t];
-    ws.logits[(size_t)t * E + row0 + rl] = s;
+    float s = red[(rl * geo.wpr) * NT + t];
+    for (int p = 1; p < geo.wpr; ++p) s += red[(rl * geo.wpr + p) * NT + t];
+    st_tag(reinterpret_cast<unsigned long long*>(ws.logits) + (size_t)t * E + row0 + rl,
+           __float_as_uint(s), ep);
+  } else if (tid >= kDcCons && tid - kDcCons < T) {
+    const int t = tid - kDcCons;
+    const int parts = nrows > 0 ? geo.wpr : 1;
+    float m = amax_part[t];
+    for (int p = 1; p < parts; ++p) m = fmaxf(m, amax_part[p * NT + t]);
+    shift_s[t] = token_shift(m);
+    xfac_s[t] = mode == 0 ? pow2f(shift_s[t]) : xS;
   }
   __syncthreads();
-  if (tid == 0) grid_arrive(&ws.ctl[kCtlBar1]);
 
-  // ---------------- activation operand of every token, in this CTA's shared memory
-  if (warp < T) {
-    float m = 0.0f;
-    const uint32_t* xr = reinterpret_cast<const uint32_t*>(xraw + (size_t)warp * H);
-    for (int i = lane; i < H / 2; i += 32) {
-      const uint32_t v = xr[i];
-      m = fmaxf(m, fmaxf(fabsf(bf16_lo(v)), fabsf(bf16_hi(v))));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    if (lane == 0) {
-      shift_s[warp] = token_shift(m);
-      xfac_s[warp] = mode == 0 ? pow2f(shift_s[warp]) : xS;
-    }
-  }
-  __syncthreads();
+  // ---------------- activation operand of every token, in this CTA's shared memory (while the
+  // other CTAs finish their logits)
   {
     const int nb = H / 16;
     for (int blk = tid; blk < T * nb; blk += kDcThreads) {
@@ -271,26 +346,21 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       *reinterpret_cast<uint4*>(row + 64 * (p0 + 1)) = *reinterpret_cast<uint4*>(&hv[8]);
     }
   }
-  if (tid == 0 && !grid_wait(&ws.ctl[kCtlBar1], (uint32_t)G)) {
-    record_status(ws.ctl, kStTimeout);
-    abort_s = 1;
-  }
   __syncthreads();
-  __threadfence();
 
   // ---------------- 2. routing, in every CTA
-  int32_t* cnt = reinterpret_cast<int32_t*>(arena);          // [E+1] counts -> offsets
-  int32_t* uq = cnt + (E + 1);                               // [E+1] distinct -> group ids
-  uint32_t* tmask = reinterpret_cast<uint32_t*>(uq + (E + 1));   // [E] tokens per expert
-  for (int e = tid; e <= E; e += kDcThreads) {
-    cnt[e] = 0;
-    uq[e] = 0;
-    if (e < E) tmask[e] = 0u;
-  }
+  // top-k + softmax of every token (warp t), then a stable sort of the S = T*k selections by
+  // expert: entry s = t*k + j goes to slot #{s' : e_s' < e_s} + #{s' < s : e_s' == e_s}
+  int32_t* sorted_e = reinterpret_cast<int32_t*>(arena);   // [S] expert of slot p
+  int32_t* sorted_t = sorted_e + geo.smax;                  // [S] token of slot p
   if (warp < T) {
     int e_sel;
     float w_sel;
-    topk_row(ws.logits + (size_t)warp * E, E, k, lane, e_sel, w_sel);
+    if (!topk_tagged(reinterpret_cast<const unsigned long long*>(ws.logits) + (size_t)warp * E, E,
+                     k, lane, ep, e_sel, w_sel) && lane == 0) {
+      record_status(ws.ctl, kStTimeout);
+      abort_s = 1;
+    }
     if (lane < k) {
       sel_idx[warp * k + lane] = e_sel;
       sel_w[warp * k + lane] = w_sel;
@@ -298,54 +368,57 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   }
   __syncthreads();
   if (tid < S) {
-    atomicAdd(&cnt[sel_idx[tid]], 1);
-    atomicOr(&tmask[sel_idx[tid]], 1u << (tid / k));
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += kDcThreads) uq[e] = cnt[e] > 0 ? 1 : 0;
-  __syncthreads();
-  if (warp == 0) {
-    warp_exclusive_scan(cnt, E, lane);
-  } else if (warp == 1) {
-    const int U = warp_exclusive_scan(uq, E, lane);
-    if (lane == 0) U_s = U;
-  }
-  __syncthreads();
-  for (int e = tid; e < E; e += kDcThreads) {
-    const uint32_t tm = tmask[e];
-    if (tm) {
-      DcGroup gr;
-      gr.expert = e;
-      gr.slot0 = cnt[e];
-      gr.n = __popc(tm);
-      uint32_t toks = 0, mm = tm;
-      for (int r = 0; mm; ++r) {
-        const int t = __ffs(mm) - 1;
-        toks |= (uint32_t)t << (4 * r);
-        mm &= mm - 1;
-      }
-      gr.toks = toks;
-      gr.mg = __ldg(&pk.mult[e * 3 + 0]);
-      gr.mu = __ldg(&pk.mult[e * 3 + 1]);
-      gr.md = __ldg(&pk.mult[e * 3 + 2]);
-      gr.sd = __ldg(&pk.down_in_scale[e]);
-      gr.i6d = __ldg(&pk.down_inv6S[e]);
-      gr.pad[0] = gr.pad[1] = gr.pad[2] = 0;
-      grp[uq[e]] = gr;
+    const int e = sel_idx[tid];
+    int p = 0;
+    for (int s2 = 0; s2 < S; ++s2) {
+      const int e2 = sel_idx[s2];
+      p += (e2 < e) || (e2 == e && s2 < tid);
     }
-  }
-  if (tid < S) {
-    // a token selects an expert at most once: its rank among the expert's slots is the
-    // number of earlier tokens that selected the same expert
-    const int t = tid / k, e = sel_idx[tid];
-    sel_slot[tid] = cnt[e] + __popc(tmask[e] & ((1u << t) - 1u));
+    sel_slot[tid] = p;
+    sorted_e[p] = e;
+    sorted_t[p] = tid / k;
   }
   __syncthreads();
-  const int U = U_s;
+  // one group per distinct expert (at most T <= 8 slots each), numbered in slot order
+  const bool gstart = tid < S && (tid == 0 || sorted_e[tid] != sorted_e[tid - 1]);
+  const unsigned gbal = __ballot_sync(0xFFFFFFFFu, gstart);
+  if (lane == 0) wcount_s[warp] = __popc(gbal);
+  __syncthreads();
+  int U = 0, ubase = 0;
+#pragma unroll
+  for (int w = 0; w <= kDcWarps; ++w) {
+    if (w < warp) ubase += wcount_s[w];
+    U += wcount_s[w];
+  }
+  if (gstart) {
+    const int e = sorted_e[tid];
+    int n = 1;
+    while (tid + n < S && sorted_e[tid + n] == e) ++n;
+    uint32_t toks = 0;
+    for (int r = 0; r < n; ++r) toks |= (uint32_t)sorted_t[tid + r] << (4 * r);
+    DcGroup gr;
+    gr.expert = e;
+    gr.slot0 = tid;
+    gr.n = n;
+    gr.toks = toks;
+    grp[ubase + __popc(gbal & ((1u << lane) - 1u))] = gr;
+  }
   if (b == 0) {
+    // CTA 0 publishes the routing: counts/offsets of every expert (binary search in the
+    // sorted selections), the per-token experts, weights and slots, and the permutation
     for (int e = tid; e < E; e += kDcThreads) {
-      ws.counts[e] = __popc(tmask[e]);
-      ws.offsets[e] = cnt[e];
+      int lo = 0, hi = S;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sorted_e[mid] < e) lo = mid + 1; else hi = mid;
+      }
+      int lo2 = lo, hi2 = S;
+      while (lo2 < hi2) {
+        const int mid = (lo2 + hi2) >> 1;
+        if (sorted_e[mid] <= e) lo2 = mid + 1; else hi2 = mid;
+      }
+      ws.offsets[e] = lo;
+      ws.counts[e] = lo2 - lo;
     }
     if (tid < S) {
       ws.idx[tid] = sel_idx[tid];
@@ -448,8 +521,13 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     const int jb_per_chunk = geo.KC / 128;
     for (int q = q0; q < q1; ++q) {
       const int gi = q / gu_tiles, it = q % gu_tiles;
-      const DcGroup& gm = grp[gi];
+      const DcGroup gm = grp[gi];
       const int slot0 = gm.slot0, n = gm.n;
+      // this task's multipliers: the loads overlap the MMA loop
+      const float mg = __ldg(&pk.mult[gm.expert * 3 + 0]);
+      const float mu = __ldg(&pk.mult[gm.expert * 3 + 1]);
+      const float sd = mode == 1 ? __ldg(&pk.down_in_scale[gm.expert]) : 0.0f;
+      const float i6d = mode == 1 ? __ldg(&pk.down_inv6S[gm.expert]) : 0.0f;
       const bool gvalid = g < n;
       const int xrow = gvalid ? group_tok(gm.toks, g) : 0;
       const unsigned char* xr = xop + (size_t)xrow * geo.x_stride + c * 16;
@@ -485,77 +563,63 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&gempty[s]);
       }
-      // fixed-order reduction over the consumer warps
+      // partial sums of the 8 warps -> shared memory; 128 threads each finish one h element
       float* myred = red + (size_t)(warp * 2) * 128;
       *reinterpret_cast<float4*>(myred + lane * 4) =
           make_float4(accg[0], accg[1], accg[2], accg[3]);
       *reinterpret_cast<float4*>(myred + 128 + lane * 4) =
           make_float4(accu[0], accu[1], accu[2], accu[3]);
       consumer_sync(kDcCons);
-      if (warp == 0) {
-        float G4[4] = {0.f, 0.f, 0.f, 0.f}, U4[4] = {0.f, 0.f, 0.f, 0.f};
+      if (tid < 128) {
+        // thread = (column col, row r of the 16-row tile); the 16 rows of a column are 16
+        // consecutive lanes. Accumulator element of (r, col): lane 4 (r % 8) + col / 2,
+        // register (col % 2) + 2 (r / 8).
+        const int col = tid >> 4, r = tid & 15;
+        const int e_idx = (4 * (r & 7) + (col >> 1)) * 4 + (col & 1) + 2 * (r >> 3);
+        float gs = 0.0f, us = 0.0f;
+#pragma unroll
         for (int w = 0; w < kDcWarps; ++w) {
-          const float4 a = *reinterpret_cast<const float4*>(red + (size_t)(w * 2) * 128 + lane * 4);
-          const float4 bq =
-              *reinterpret_cast<const float4*>(red + (size_t)(w * 2) * 128 + 128 + lane * 4);
-          G4[0] += a.x; G4[1] += a.y; G4[2] += a.z; G4[3] += a.w;
-          U4[0] += bq.x; U4[1] += bq.y; U4[2] += bq.z; U4[3] += bq.w;
+          gs += red[(size_t)(w * 2) * 128 + e_idx];
+          us += red[(size_t)(w * 2) * 128 + 128 + e_idx];
         }
-        float hv[4];  // (row g, col 2c), (row g, col 2c+1), (row g+8, col 2c), (row g+8, col 2c+1)
-#pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-          const int col = 2 * c + (q2 & 1);
-          const float xf = col < n ? xfac_s[group_tok(gm.toks, col)] : 0.0f;
-          const float gv = G4[q2] * gm.mg * xf;
-          const float uv = U4[q2] * gm.mu * xf;
-          hv[q2] = col < n ? silu_mul(gv, uv) : 0.0f;
-        }
-        const int i0 = it * 16 + g;
+        const bool cvalid = col < n;
+        const float xf = cvalid ? xfac_s[group_tok(gm.toks, col)] : 0.0f;
+        const float hv = cvalid ? silu_mul(gs * mg * xf, us * mu * xf) : 0.0f;
+        const size_t slot = (size_t)(slot0 + (cvalid ? col : 0));
+        unsigned long long* htp = ws.htag + (slot * (I / 16) + it) * 9;
         if (mode == 0) {
+          const uint16_t hb = f32_to_bf16_rn(hv);
+          // |h| of the BF16 values over the column's 16 rows, for the down stage's f16 scaling
+          float a = fabsf(__uint_as_float((uint32_t)hb << 16));
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int col = 2 * c + cc;
-            const uint16_t b0 = f32_to_bf16_rn(hv[cc]), b1 = f32_to_bf16_rn(hv[2 + cc]);
-            // |h| of the BF16 values, for the down stage's per-slot f16 scaling
-            float a = fmaxf(fabsf(__uint_as_float((uint32_t)b0 << 16)),
-                            fabsf(__uint_as_float((uint32_t)b1 << 16)));
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1)
-              a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
-            if (col < n) {
-              const size_t slot = (size_t)(slot0 + col);
-              ws.h16[slot * I + i0] = b0;
-              ws.h16[slot * I + i0 + 8] = b1;
-              if (g == 0) atomicMax(&ws.slot_amax[slot], __float_as_uint(a));
-            }
+          for (int off = 1; off < 16; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+          const uint32_t hb_next = __shfl_down_sync(0xFFFFFFFFu, (uint32_t)hb, 1);
+          if (cvalid) {
+            ws.h16[slot * I + it * 16 + r] = hb;
+            // tagged for the down stage: BF16 pairs (rows r, r+1) and the block's max |h|
+            if ((r & 1) == 0) st_tag(htp + r / 2, (uint32_t)hb | (hb_next << 16), ep);
+            if (r == 0) st_tag(htp + 8, __float_as_uint(a), ep);
           }
         } else {
-          const float Sd = gm.sd, i6 = gm.i6d;
+          // the quantiser Q of this 16-element block of h (down input scale)
+          float a = fabsf(hv);
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {  // token column 2c + cc
-            const float v_lo = hv[cc], v_hi = hv[2 + cc];  // elements g and g+8 of the block
-            float a = fmaxf(fabsf(v_lo), fabsf(v_hi));
+          for (int off = 1; off < 16; off <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+          const uint32_t sf = e4m3_encode_rn(__fmul_rn(a, i6d));
+          uint32_t nib = 0;
+          if (sf != 0u) {
+            const float rr = __frcp_rn(__fmul_rn(e4m3_value_nonneg(sf), sd));
+            nib = e2m1_encode_rn(__fmul_rn(hv, rr)) << (4 * (r & 7));
+          }
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1)
-              a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
-            const uint32_t sf = e4m3_encode_rn(__fmul_rn(a, i6));
-            uint32_t lo = 0, hi = 0;
-            if (sf != 0u) {
-              const float r = __frcp_rn(__fmul_rn(e4m3_value_nonneg(sf), Sd));
-              lo = e2m1_encode_rn(__fmul_rn(v_lo, r)) << (4 * g);
-              hi = e2m1_encode_rn(__fmul_rn(v_hi, r)) << (4 * g);
-            }
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-              lo |= __shfl_xor_sync(0xFFFFFFFFu, lo, off);
-              hi |= __shfl_xor_sync(0xFFFFFFFFu, hi, off);
-            }
-            const int col = 2 * c + cc;
-            if (g == 0 && col < n) {
-              const size_t slot = (size_t)(slot0 + col);
-              *reinterpret_cast<uint2*>(ws.hq + slot * (I / 2) + it * 8) = make_uint2(lo, hi);
-              ws.hsf[slot * (I / 16) + it] = static_cast<uint8_t>(sf);
-            }
+          for (int off = 1; off < 8; off <<= 1) nib |= __shfl_xor_sync(0xFFFFFFFFu, nib, off);
+          const uint32_t hi_word = __shfl_down_sync(0xFFFFFFFFu, nib, 8);
+          if (cvalid && r == 0) {
+            *reinterpret_cast<uint2*>(ws.hq + slot * (I / 2) + it * 8) = make_uint2(nib, hi_word);
+            ws.hsf[slot * (I / 16) + it] = static_cast<uint8_t>(sf);
+            st_tag(htp + 0, nib, ep);
+            st_tag(htp + 1, hi_word, ep);
+            st_tag(htp + 2, sf, ep);
           }
         }
       }
@@ -563,79 +627,80 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     }
   }
 
-  // ---------------- barrier 2: every CTA's h is written
-  if (tid == 0) {
-    grid_arrive(&ws.ctl[kCtlBar2]);
-    if (!grid_wait(&ws.ctl[kCtlBar2], (uint32_t)G)) {
-      record_status(ws.ctl, kStTimeout);
-      abort_s = 1;
-    }
-    __threadfence();
-  }
-  consumer_sync(kDcCons);
-
-  // ---------------- 4. down + combine (consumer warps)
+  // ---------------- 4. down (consumer warps): each task waits only for its own group's h
   {
-    const int nkb = I / 64;
+    const int nkb = I / 64, ntile = I / 16;
     const uint32_t code_bytes = (uint32_t)kDnRows * (I / 2);
     int cur = -1, dchunk = 0;
+    float md = 0.0f;
     for (int q = d0; q < d1; ++q, ++dchunk) {
       const int gi = q / dn_tiles, ht = q % dn_tiles;
-      const DcGroup& gm = grp[gi];
+      const DcGroup gm = grp[gi];
       const int slot0 = gm.slot0, n = gm.n;
       if (gi != cur) {
         // the group's h rows as the f16 operand: BF16 h * 2^-s (W4A16; s from the slot's
-        // amax, exact), or the decoded NVFP4 code * scale (W4A4, exact)
+        // max |h|, exact) or the decoded NVFP4 code * scale (W4A4, exact). One (row, 16-block)
+        // per thread: poll its tagged words, then convert.
+        if (tid < kGroup) hamax_s[tid] = 0u;
         consumer_sync(kDcCons);
-        if (tid < n) {
+        md = __ldg(&pk.mult[gm.expert * 3 + 2]);
+        const float sd = mode == 1 ? __ldg(&pk.down_in_scale[gm.expert]) : 0.0f;
+        const int nent = n * ntile;
+        for (int ent = tid; ent < nent; ent += kDcCons) {
+          const int row = ent / ntile, it = ent % ntile;
+          const unsigned long long* src = ws.htag + ((size_t)(slot0 + row) * ntile + it) * 9;
+          unsigned long long w[9];
+          bool ok;
           if (mode == 0) {
-            const int sh = amax_shift(__uint_as_float(__ldcg(&ws.slot_amax[slot0 + tid])));
-            hfac_s[tid] = pow2f(sh);
-            hinv_s[tid] = pow2f(-sh);
+            ok = poll_tags<9>(src, ep, w);
           } else {
-            hfac_s[tid] = gm.sd;
+            unsigned long long w3[3];
+            ok = poll_tags<3>(src, ep, w3);
+            w[0] = w3[0];
+            w[1] = w3[1];
+            w[2] = w3[2];
+          }
+          if (!ok) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          uint32_t* dst = reinterpret_cast<uint32_t*>(xop + (size_t)row * geo.h_stride) + it * 8;
+          if (mode == 0) {
+            // raw BF16 pairs for now; converted once the row's max |h| is known
+#pragma unroll
+            for (int p2 = 0; p2 < 8; ++p2) dst[p2] = data_of(w[p2]);
+            atomicMax(&hamax_s[row], data_of(w[8]));
+          } else {
+            const float sv = e4m3_value_nonneg(data_of(w[2]));
+            const uint32_t cw[2] = {data_of(w[0]), data_of(w[1])};
+#pragma unroll
+            for (int p2 = 0; p2 < 8; ++p2) {
+              const uint32_t byte = (cw[p2 >> 2] >> (8 * (p2 & 3))) & 0xFFu;
+              const __half2 hh = __floats2half2_rn(e2m1_value(byte & 0xF) * sv,
+                                                   e2m1_value(byte >> 4) * sv);
+              dst[p2] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
+            if (it == 0) hfac_s[row] = sd;
           }
         }
         consumer_sync(kDcCons);
-        const int words = n * (I / 2);
-        for (int i0 = tid; i0 < words; i0 += 4 * kDcCons) {
-          uint32_t v[4], sc[4];
+        if (mode == 0) {
+          for (int ent = tid; ent < nent; ent += kDcCons) {
+            const int row = ent / ntile, it = ent % ntile;
+            const int sh = amax_shift(__uint_as_float(hamax_s[row]));
+            const float f = pow2f(-sh);
+            if (it == 0) hfac_s[row] = pow2f(sh);
+            uint32_t* dst = reinterpret_cast<uint32_t*>(xop + (size_t)row * geo.h_stride) + it * 8;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * kDcCons;
-            const int row = i / (I / 2), wd = i % (I / 2);
-            v[u] = 0u;
-            sc[u] = 0u;
-            if (i < words) {
-              if (mode == 0) {
-                v[u] = __ldcg(reinterpret_cast<const unsigned int*>(ws.h16 +
-                                                                   (size_t)(slot0 + row) * I) + wd);
-              } else {
-                v[u] = __ldcg(ws.hq + (size_t)(slot0 + row) * (I / 2) + wd);
-                sc[u] = __ldcg(ws.hsf + (size_t)(slot0 + row) * (I / 16) + wd / 8);
-              }
+            for (int p2 = 0; p2 < 8; ++p2) {
+              const uint32_t v = dst[p2];
+              const __half2 hh = __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), f),
+                                                   __fmul_rn(__uint_as_float(v & 0xFFFF0000u), f));
+              dst[p2] = *reinterpret_cast<const uint32_t*>(&hh);
             }
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int i = i0 + u * kDcCons;
-            if (i < words) {
-              const int row = i / (I / 2), wd = i % (I / 2);
-              unsigned char* dst = xop + (size_t)row * geo.h_stride + wd * 4;
-              if (mode == 0) {
-                const float f = hinv_s[row];
-                *reinterpret_cast<__half2*>(dst) =
-                    __floats2half2_rn(__fmul_rn(__uint_as_float(v[u] << 16), f),
-                                      __fmul_rn(__uint_as_float(v[u] & 0xFFFF0000u), f));
-              } else {
-                const float sv = e4m3_value_nonneg(sc[u]);
-                *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(
-                    e2m1_value(v[u] & 0xF) * sv, e2m1_value((v[u] >> 4) & 0xF) * sv);
-              }
-            }
-          }
+          consumer_sync(kDcCons);
         }
-        consumer_sync(kDcCons);
         cur = gi;
       }
       const int s = dchunk % geo.dn_stages, nn = dchunk / geo.dn_stages;
@@ -651,6 +716,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       const unsigned char* scb = st + code_bytes + (size_t)(warp >> 2) * (4 * I) +
                                  (size_t)(warp & 3) * nkb * 64 + c * 16 + g * 2;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 3
       for (int j = 0; j < nkb; ++j) {
         const uint2 a0 = lds64(rg + j * 32);
         const uint2 a1 = lds64(rg8 + j * 32);
@@ -664,75 +730,61 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&dempty[s]);
-      const float md = gm.md;
+      // Y = BF16(acc * md * factor): plain (slot-major rows) and tagged pairs of rows (r, r+1),
+      // r even, for the combine; row g's partner g+1 is the lane 4 above
 #pragma unroll
       for (int q2 = 0; q2 < 4; ++q2) {
         const int col = 2 * c + (q2 & 1);
+        const int row = ht * kDnRows + warp * 16 + g + ((q2 >> 1) << 3);
+        const uint16_t yb = f32_to_bf16_rn(acc[q2] * md * hfac_s[col < n ? col : 0]);
+        const uint32_t yb_next = __shfl_down_sync(0xFFFFFFFFu, (uint32_t)yb, 4);
         if (col < n) {
-          const float y = acc[q2] * md * hfac_s[col];
-          const int row = ht * kDnRows + warp * 16 + g + ((q2 >> 1) << 3);
-          ws.y[(size_t)(slot0 + col) * H + row] = f32_to_bf16_rn(y);
-        }
-      }
-      // the last task of output tile ht (one per group) forms out for its rows
-      consumer_sync(kDcCons);
-      if (tid == 0) {
-        __threadfence();
-        last_s = atomicAdd(&ws.ctl[kCtlTiles + ht], 1u) == (uint32_t)(U - 1) ? 1 : 0;
-        __threadfence();
-      }
-      consumer_sync(kDcCons);
-      if (last_s) {
-        for (int it2 = tid; it2 < T * (kDnRows / 8); it2 += kDcCons) {
-          const int t = it2 / (kDnRows / 8), r8 = ht * (kDnRows / 8) + it2 % (kDnRows / 8);
-          float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          for (int j0 = 0; j0 < k; j0 += 8) {
-            float wj[8];
-            int sj[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const bool ok = j0 + u < k;
-              wj[u] = ok ? sel_w[t * k + j0 + u] : 0.0f;
-              sj[u] = ok ? sel_slot[t * k + j0 + u] : -1;
-            }
-            uint4 v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              v[u] = sj[u] >= 0 ? __ldcg(reinterpret_cast<const uint4*>(ws.y + (size_t)sj[u] * H) + r8)
-                                : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              if (sj[u] < 0) break;
-              const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-              for (int z = 0; z < 4; ++z) {
-                acc8[2 * z] += wj[u] * __uint_as_float(wd[z] << 16);
-                acc8[2 * z + 1] += wj[u] * __uint_as_float(wd[z] & 0xFFFF0000u);
-              }
-            }
-          }
-          uint32_t o[4];
-#pragma unroll
-          for (int z = 0; z < 4; ++z)
-            o[z] = (uint32_t)f32_to_bf16_rn(acc8[2 * z]) |
-                   ((uint32_t)f32_to_bf16_rn(acc8[2 * z + 1]) << 16);
-          reinterpret_cast<uint4*>(out + (size_t)t * H)[r8] = make_uint4(o[0], o[1], o[2], o[3]);
+          const size_t slot = (size_t)(slot0 + col);
+          ws.y[slot * H + row] = yb;
+          if ((g & 1) == 0)
+            st_tag(ws.ytag + slot * (H / 2) + row / 2, (uint32_t)yb | (yb_next << 16), ep);
         }
       }
     }
   }
 
-  // ---------------- the last CTA to finish resets the kernel's control words
-  consumer_sync(kDcCons);
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(&ws.ctl[kCtlDone], 1u) == (uint32_t)(G - 1)) {
-      ws.ctl[kCtlBar1] = 0u;
-      ws.ctl[kCtlBar2] = 0u;
-      for (int i = 0; i < dn_tiles; ++i) ws.ctl[kCtlTiles + i] = 0u;
-      ws.ctl[kCtlDone] = 0u;
+  // ---------------- 5. combine: 128-row tile ht of out is formed by CTA ht (mod the grid) once
+  // all of its Y pairs carry this epoch: the fixed-order weighted sum over each token's k
+  // experts (rank order, FP32, then BF16)
+  {
+    uint32_t* ysm = reinterpret_cast<uint32_t*>(arena);   // [T][k][64] BF16 pairs of the tile
+    for (int ht = b; ht < dn_tiles; ht += G) {
+      consumer_sync(kDcCons);
+      for (int it2 = tid; it2 < S * 64; it2 += kDcCons) {
+        const int sj = it2 >> 6, p2 = it2 & 63;
+        unsigned long long w[1];
+        if (!poll_tags<1>(ws.ytag + (size_t)sel_slot[sj] * (H / 2) + ht * 64 + p2, ep, w)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        ysm[it2] = data_of(w[0]);
+      }
+      consumer_sync(kDcCons);
+      for (int it2 = tid; it2 < T * 64; it2 += kDcCons) {
+        const int t = it2 >> 6, p2 = it2 & 63;
+        float a0 = 0.0f, a1 = 0.0f;
+        for (int j = 0; j < k; ++j) {
+          const float wj = sel_w[t * k + j];
+          const uint32_t v = ysm[(t * k + j) * 64 + p2];
+          a0 += wj * __uint_as_float(v << 16);
+          a1 += wj * __uint_as_float(v & 0xFFFF0000u);
+        }
+        reinterpret_cast<uint32_t*>(out + (size_t)t * H)[ht * 64 + p2] =
+            (uint32_t)f32_to_bf16_rn(a0) | ((uint32_t)f32_to_bf16_rn(a1) << 16);
+      }
     }
   }
+
+  // ---------------- the last CTA of the call publishes its epoch (after every CTA read it)
+  consumer_sync(kDcCons);
+  if (tid == 0 && (ticket_acq_rel(&ws.ctl[kCtlDone]) + 1u) % (uint32_t)G == 0u)
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(&ws.ctl[kCtlEpoch]), "r"(ep)
+                 : "memory");
 }
 
 template <typename Kern, typename... Args>
@@ -757,7 +809,7 @@ cudaError_t launch_pdl(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, si
 // memory (the multi-kernel path serves such shapes).
 bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom) {
   DcGeom g{};
-  if (T < 1 || T > kNarrowT || num_ctas < 1 || H / kDnRows > kCtlWords - kCtlTiles) return false;
+  if (T < 1 || T > kNarrowT || num_ctas < 1) return false;
   g.rows_max = (E + num_ctas - 1) / num_ctas;
   if (g.rows_max > kDcWarps) return false;
   g.wpr = g.rows_max <= kDcWarps / 2 ? 2 : 1;
@@ -773,7 +825,7 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   g.smax = T * k;
   g.gmax = g.smax < E ? g.smax : E;
   const int route_bytes = g.rows_max * H * 2 + T * H * 2;
-  const int scratch = (3 * E + 2) * 4;
+  const int scratch = T * k * 64 * 4;  // sorted selections; Y pairs of one tile for the combine
   const int fixed = g.xop + kDcWarps * 2 * 128 * 4 + g.gmax * (int)sizeof(DcGroup) +
                     g.smax * 12 + 8 + 8 * (2 * 3 + 2 * 16 + 2) + kDcStatic;
   const int avail = kDcSmemMax - fixed;
@@ -794,18 +846,28 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   return true;
 }
 
-size_t decode_geom_bytes() { return sizeof(DcGeom); }
-
 cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
                           float xS, float x_inv6S, const uint16_t* x, const uint16_t* wr,
                           uint16_t* out) {
   DcGeom geo;
   if (!decode_geom(ws.T, ws.H, ws.E, ws.k, ws.I, lc.num_sms, &geo)) return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(lc, k_decode, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, pk, ws,
-                    geo, x, wr, mode, xS, x_inv6S, out);
+  auto go = [&](auto kern) -> cudaError_t {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(lc, kern, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, pk, ws,
+                      geo, x, wr, mode, xS, x_inv6S, out);
+  };
+  switch (ws.T) {
+    case 1: return go(k_decode<1>);
+    case 2: return go(k_decode<2>);
+    case 3: return go(k_decode<3>);
+    case 4: return go(k_decode<4>);
+    case 5: return go(k_decode<5>);
+    case 6: return go(k_decode<6>);
+    case 7: return go(k_decode<7>);
+    default: return go(k_decode<8>);
+  }
 }
 
 }  // namespace moe

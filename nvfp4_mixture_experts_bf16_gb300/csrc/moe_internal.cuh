@@ -29,11 +29,9 @@ enum : int {
   kCtlGroups = 2,       // number of token groups of the current call
   kCtlUnique = 3,       // number of distinct experts of the current call
   kCtlTokenTiles = 4,   // number of 128-slot token tiles (grouped tensor-core path)
-  kCtlBar1 = 8,         // fused decode kernel: grid barrier after the router logits
-  kCtlBar2 = 9,         //   grid barrier after h
-  kCtlDone = 10,        //   CTAs finished (the last one resets the fused kernel's words)
-  kCtlTiles = 64,       //   per 128-row output tile: down tasks finished (64 words)
-  kCtlWords = 128
+  kCtlEpoch = 8,        // fused narrow kernel: epoch of the last completed call (tags its data)
+  kCtlDone = 9,         //   CTAs finished, over all calls (the last of a call advances the epoch)
+  kCtlWords = 64
 };
 
 // Per token group (<= 8 tokens of one expert): everything the expert kernels need about it,
@@ -50,7 +48,7 @@ struct WsView {
   uint32_t* ctl;
   GroupMeta* gmeta;    // [G]
   uint32_t* slot_amax; // [T*k] bits of max|h| per slot (W4A16), zeroed by the routing stage
-  float* logits;       // [T][E]
+  float* logits;       // [T][E] (fused narrow kernel: [T][E] 64-bit {logit bits, epoch})
   int32_t* idx;        // [T][k]
   float* w;            // [T][k]
   int32_t* slot_of;    // [T][k]
@@ -66,6 +64,10 @@ struct WsView {
   uint8_t* hq;         // [T*k][I/2] W4A4 h codes
   uint8_t* hsf;        // [T*k][I/16] W4A4 h scales
   uint16_t* y;         // [T*k][H] BF16 expert outputs
+  // fused narrow kernel: 64-bit words {data, epoch} that other CTAs poll instead of a barrier
+  unsigned long long* htag;  // [T*k][I/16][9]: h of one 16-element block (W4A16: 8 BF16 pairs +
+                             // max |h|; W4A4: code words lo, hi + scale byte)
+  unsigned long long* ytag;  // [T*k][H/2]: BF16 pairs of Y
   // grouped tensor-core path: token tiles of <= 128 slots of one expert; tile j occupies padded
   // rows ("pslots") 128j .. 128j+127 of the permuted operands
   int32_t* tt_expert;  // [NT]
@@ -382,21 +384,16 @@ __device__ __forceinline__ float key_logit(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// Top-k of one token's E <= 32 V logits (global memory, read through L2) by one warp, followed by
-// the softmax over the k selected logits. Lane e % 32 holds logit e in register e / 32. Each
-// round takes the warp's largest key (redux.sync max) and, among lanes holding it, the lowest
-// expert index (redux.sync min): larger logit first, equal logits -> lower index first. Only the
-// winning lane drops its entry and rescans its registers. Lane j < k returns the j-th selection
-// and its softmax weight; the sum of exponentials is a fixed butterfly, identical in all lanes.
+// Top-k of one token's logits by one warp, followed by the softmax over the k selected logits.
+// Lane e % 32 holds the key of logit e in key[e / 32] (0 for e >= E). Each round takes the
+// warp's largest key (redux.sync max) and, among lanes holding it, the lowest expert index
+// (redux.sync min): larger logit first, equal logits -> lower index first. The winning lane
+// drops its entry; every lane rescans its registers (predicated, no divergent branch, which
+// measured faster). Lane j < k returns the j-th selection and its softmax weight; the sum of
+// exponentials is a fixed butterfly, identical in all lanes.
 template <int V>
-__device__ __forceinline__ void warp_topk_softmax(const float* row, int E, int k, int lane,
-                                                  int& e_out, float& w_out) {
-  uint32_t key[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = e < E ? logit_key(__ldcg(row + e)) : 0u;
-  }
+__device__ __forceinline__ void warp_select_softmax(uint32_t (&key)[V], int k, int lane,
+                                                    int& e_out, float& w_out) {
   uint32_t bk = 0u;
   int bp = 0;
 #pragma unroll
@@ -412,16 +409,16 @@ __device__ __forceinline__ void warp_topk_softmax(const float* row, int E, int k
       e_out = (int)ew;
       v = key_logit(m);
     }
-    if ((int)(ew & 31u) == lane) {
-      const int taken = bp;
-      bk = 0u;
-      bp = 0;
+    const int taken = (int)(ew & 31u) == lane ? bp : -1;
+    uint32_t nb = 0u;
+    int np = 0;
 #pragma unroll
-      for (int i = 0; i < V; ++i) {
-        if (i == taken) key[i] = 0u;
-        if (key[i] > bk) { bk = key[i]; bp = i; }
-      }
+    for (int i = 0; i < V; ++i) {
+      key[i] = i == taken ? 0u : key[i];
+      if (key[i] > nb) { nb = key[i]; np = i; }
     }
+    bk = nb;
+    bp = np;
   }
   const float m0 = __shfl_sync(0xFFFFFFFFu, v, 0);
   const float ex = lane < k ? expf(v - m0) : 0.0f;
@@ -429,6 +426,19 @@ __device__ __forceinline__ void warp_topk_softmax(const float* row, int E, int k
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
   w_out = ex / z;
+}
+
+// The same for E <= 32 V FP32 logits in global memory (read through L2).
+template <int V>
+__device__ __forceinline__ void warp_topk_softmax(const float* row, int E, int k, int lane,
+                                                  int& e_out, float& w_out) {
+  uint32_t key[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? logit_key(__ldcg(row + e)) : 0u;
+  }
+  warp_select_softmax<V>(key, k, lane, e_out, w_out);
 }
 
 __device__ __forceinline__ void topk_row(const float* row, int E, int k, int lane, int& e_out,
