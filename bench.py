@@ -8,8 +8,9 @@ own 512-expert NVFP4 pack (65 GB resident), so a step streams 48 x 10 selected e
 one CUDA graph (PDL-chained kernels). ``value`` = layer-tokens per second = T * layers / step
 time. Inputs are seeded synthetic (``synth``), resident in HBM before timing starts.
 
-Also reported in the same line: the roofline of the dominant kernel (gate/up) from CUDA events
-recorded around it on its stream, the end-to-end number through the C ABI with host buffers
+Also reported in the same line: the roofline of the dominant kernel from CUDA events on its
+stream (for narrow calls the whole step is one persistent kernel, ``k_decode``, so its mean
+launch time is the timed step / layers), the end-to-end number through the C ABI with host buffers
 (host->device copy of x and device->host copy of out inside the timed region), the SM clocks
 sampled during the timed region, a secondary table (8-token verify W4A16/W4A4 and the
 8192-token prefill), and the CPU oracle timed on a bounded sample as a reported baseline.
@@ -145,6 +146,12 @@ def bytes_gateup(U, H, I):
 
 def bytes_down(U, H, I):
     return U * (H * I // 2 + H * I // 16)
+
+
+def bytes_decode_launch(U, T, H, E, I):
+    """Algorithmic DRAM bytes of one fused narrow-call launch: the router (read once), every
+    selected expert's NVFP4 codes + scales + 3 multipliers (each read once), x in and out out."""
+    return E * H * 2 + bytes_gateup(U, H, I) + bytes_down(U, H, I) + U * 12 + 2 * T * H * 2
 
 
 # ------------------------------------------------------------------ CPU oracle (baseline arm)
@@ -392,20 +399,36 @@ def run_native(args, rank, world, local_rank):
     tokens_per_step = wl.T * layers
     value = world * tokens_per_step / (ms / 1e3)
 
-    st = stage_times(wl, stack, reps=3, device=device)
     U_mean = float(np.mean([L.U for L in stack]))
     gu_bytes = bytes_gateup(U_mean, wl.H, wl.I)
     dn_bytes = bytes_down(U_mean, wl.H, wl.I)
-    gu_gbs = gu_bytes / (st[1] * 1e-3) / 1e9
     layer_bytes = gu_bytes + dn_bytes
-    layer_gbs = layer_bytes / (ms / layers * 1e-3) / 1e9
-    roofline = dict(bound="hbm", kernel="k_gateup (gate/up + SiLU*up)",
-                    achieved=round(gu_gbs, 1), peak=pk["hbm"], unit="GB/s",
-                    frac=round(gu_gbs / pk["hbm"], 4),
-                    traffic=committed_traffic("k_gateup", wl.name),
-                    algorithmic_bytes_per_launch=int(gu_bytes),
-                    peak_source=f"{pk['src']} hbm_gbs (MEASURED_PEAKS.json)"
-                    if pk["src"] == "measured" else "fallback 6.8 TB/s")
+    layer_s = ms / layers * 1e-3
+    layer_gbs = layer_bytes / layer_s / 1e9
+    peak_src = (f"{pk['src']} hbm_gbs (MEASURED_PEAKS.json)" if pk["src"] == "measured"
+                else "fallback 6.8 TB/s")
+    fused = launches == layers   # one launch per layer: the persistent narrow-call kernel
+    stages = None
+    if fused:
+        # the only kernel of the step: mean launch duration = event-timed step / launches
+        dec_bytes = bytes_decode_launch(U_mean, wl.T, wl.H, wl.E, wl.I)
+        gbs = dec_bytes / layer_s / 1e9
+        roofline = dict(bound="hbm", kernel="k_decode (whole narrow-call step, one launch)",
+                        achieved=round(gbs, 1), peak=pk["hbm"], unit="GB/s",
+                        frac=round(gbs / pk["hbm"], 4),
+                        traffic=committed_traffic("k_decode", wl.name),
+                        algorithmic_bytes_per_launch=int(dec_bytes),
+                        launch_us=round(layer_s * 1e6, 3), peak_source=peak_src)
+    else:
+        st = stage_times(wl, stack, reps=3, device=device)
+        gu_gbs = gu_bytes / (st[1] * 1e-3) / 1e9
+        stages = dict(route=round(st[0] * 1e3, 2), gateup=round(st[1] * 1e3, 2),
+                      down=round(st[2] * 1e3, 2), combine=round(st[3] * 1e3, 2))
+        roofline = dict(bound="hbm", kernel="k_gateup (gate/up + SiLU*up)",
+                        achieved=round(gu_gbs, 1), peak=pk["hbm"], unit="GB/s",
+                        frac=round(gu_gbs / pk["hbm"], 4),
+                        traffic=committed_traffic("k_gateup", wl.name),
+                        algorithmic_bytes_per_launch=int(gu_bytes), peak_source=peak_src)
     e2e_ms, io_bytes = e2e_measure(wl, stack, max(3, args.steps // 2), state, device)
 
     extra = {}
@@ -454,10 +477,10 @@ def run_native(args, rank, world, local_rank):
                     graph=not args.no_graph, setup_s=round(setup_s, 1)),
         gpu_launches=launches * args.steps,
         roofline=roofline,
-        layer=dict(us=round(ms / layers * 1e3, 3), stage_us=dict(
-            route=round(st[0] * 1e3, 2), gateup=round(st[1] * 1e3, 2), down=round(st[2] * 1e3, 2),
-            combine=round(st[3] * 1e3, 2)), hbm_gbs=round(layer_gbs, 1),
-            frac_hbm=round(layer_gbs / pk["hbm"], 4), unique_experts=U_mean),
+        layer=dict(us=round(ms / layers * 1e3, 3), launches=launches // layers,
+                   stage_us=stages, hbm_gbs=round(layer_gbs, 1),
+                   frac_hbm=round(layer_gbs / pk["hbm"], 4), unique_experts=U_mean,
+                   note="hbm_gbs: selected experts' bytes (U x B_e) per layer time, router excluded"),
         e2e=dict(value=round(world * tokens_per_step / (e2e_ms / 1e3), 2), unit="layer-tokens/s",
                  h2d_bytes_per_step=io_bytes, d2h_bytes_per_step=io_bytes),
         clocks=clk, cpu_baseline=cpu, secondary=extra)

@@ -85,7 +85,7 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
   L.slot_amax_bytes = mode == 0 ? (size_t)S * 4 : 0;
   L.slot_amax = take(L.slot_amax_bytes);
   const bool narrow = T <= moe::kNarrowT;
-  L.logits = take((size_t)T * E * (narrow ? 8 : 4));
+  L.logits = take((size_t)T * E * (narrow ? 8 * moe::kLogitReplicas : 4));
   L.idx = take((size_t)S * 4);
   L.w = take((size_t)S * 4);
   L.slot_of = take((size_t)S * 4);

@@ -47,7 +47,8 @@ static_assert(sizeof(DcGroup) == 16, "DcGroup layout");
 
 struct DcGeom {
   int rows_max;                 // router rows of one CTA, at most
-  int wpr;                      // warps per router row (2: each warp half a row)
+  int rs;                       // bytes per staged router / activation row: 2H + 16 (padded so
+                                // that 8 rows' fragment loads hit distinct banks)
   int KC, nkc, row_bytes;       // gate/up stage: KC reduction columns, nkc stages per task
   int gu_stage, gu_stages;
   int dn_stage, dn_stages;
@@ -157,6 +158,16 @@ __device__ __forceinline__ bool poll_tags(const unsigned long long* p, uint32_t 
   }
 }
 
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a2,
+                                               uint32_t b0, uint32_t b1) {
+  // rows 8..15 of A are zero (a router CTA has at most 8 rows)
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ int group_tok(uint32_t toks, int c) { return (toks >> (4 * c)) & 0xF; }
 
 // Contiguous share of ntasks for this CTA (ntasks * gridDim.x < 2^31 for every valid shape).
@@ -199,8 +210,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   const int G = gridDim.x, b = blockIdx.x;
   const int row0 = (E * b) / G;
   const int nrows = (E * (b + 1)) / G - row0;
-  uint16_t* wrs = reinterpret_cast<uint16_t*>(arena);                            // [rows][H]
-  uint16_t* xraw = reinterpret_cast<uint16_t*>(arena + (size_t)geo.rows_max * H * 2);  // [T][H]
+  unsigned char* wrs = arena;                                            // [rows][rs bytes]
+  unsigned char* xraw = arena + (size_t)geo.rows_max * geo.rs;           // [T][rs bytes]
 
   if (tid == 0) {
     for (int s = 0; s < geo.gu_stages; ++s) {
@@ -218,7 +229,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     // the router rows are weights: copy them before waiting for the preceding kernel
     if (nrows > 0) {
       mbar_arrive_expect_tx(rbar, (uint32_t)nrows * H * 2);
-      bulk_g2s(wrs, wr + (size_t)row0 * H, (uint32_t)nrows * H * 2, rbar);
+      for (int r = 0; r < nrows; ++r)
+        bulk_g2s(wrs + (size_t)r * geo.rs, wr + (size_t)(row0 + r) * H, (uint32_t)H * 2, rbar);
     }
   }
   __syncthreads();
@@ -226,7 +238,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   pdl_launch_dependents();
   if (tid == 0) {
     mbar_arrive_expect_tx(xbar, (uint32_t)T * H * 2);
-    bulk_g2s(xraw, x, (uint32_t)T * H * 2, xbar);
+    for (int t = 0; t < T; ++t)
+      bulk_g2s(xraw + (size_t)t * geo.rs, x + (size_t)t * H, (uint32_t)H * 2, xbar);
   }
   // this call's epoch: one past the last completed call's (never 0, the zeroed workspace's tag)
   uint32_t ep = __ldcg(&ws.ctl[kCtlEpoch]) + 1u;
@@ -236,71 +249,61 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     abort_s = 1;
   }
 
-  // ---------------- 1. router rows (warps 0..7; warp w: row w / wpr, part w % wpr of H); the
-  // warps of row 0 also take each token's max |x| over their part (for the f16 scaling)
-  float* amax_part = red + kDcWarps * NT;   // [wpr][NT]
+  // ---------------- 1. router rows on the tensor cores: logits[t][row0 + r] = W[r] . x[t] as one
+  // m16n8k16 BF16 MMA chain per warp over an eighth of H (A = the CTA's <= 8 router rows,
+  // B = the T tokens, FP32 accumulation; the products are exact). The B fragments also give each
+  // token's max |x| (for the f16 operand's scaling).
+  float* amax_part = red + kDcWarps * 64;   // [8 warps][8 tokens]
   if (warp < kDcWarps) {
-    const int r = warp / geo.wpr, part = warp % geo.wpr;
-    float acc[NT], am[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) acc[t] = am[t] = 0.0f;
-    if (r < nrows) {
-      const int nchunk = H / (8 * geo.wpr);  // uint4 chunks of this warp's part of the row
-      const uint4* wrow = reinterpret_cast<const uint4*>(wrs + (size_t)r * H) + part * nchunk;
-#pragma unroll 2
-      for (int i = lane; i < nchunk; i += 32) {
-        const uint4 wv = wrow[i];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const uint4 xv = reinterpret_cast<const uint4*>(xraw + (size_t)t * H)[part * nchunk + i];
-          acc[t] += dot8_bf16(wv, xv);
-          if (r == 0) {
-            const uint32_t w4[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              am[t] = fmaxf(am[t], fmaxf(fabsf(bf16_lo(w4[q])), fabsf(bf16_hi(w4[q]))));
-          }
-        }
+    const int g = lane >> 2, c = lane & 3;
+    const bool arow = g < nrows, bcol = g < T;
+    const int kw = H / kDcWarps;                       // K range of this warp
+    const unsigned char* ap = wrs + (size_t)g * geo.rs + (size_t)(warp * kw + 2 * c) * 2;
+    const unsigned char* bp = xraw + (size_t)g * geo.rs + (size_t)(warp * kw + 2 * c) * 2;
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    float am = 0.0f;
+    for (int ks = 0; ks < kw / 16; ks += 2) {
+      uint32_t a[4] = {0u, 0u, 0u, 0u}, bb[4] = {0u, 0u, 0u, 0u};
+      if (arow) {
+        a[0] = lds32(ap + ks * 32);
+        a[1] = lds32(ap + ks * 32 + 16);
+        a[2] = lds32(ap + ks * 32 + 32);
+        a[3] = lds32(ap + ks * 32 + 48);
       }
-    } else if (nrows == 0 && warp < T) {
-      // no router row in this CTA: warp t takes token t's max |x| over the whole row
-      const uint32_t* xr = reinterpret_cast<const uint32_t*>(xraw + (size_t)warp * H);
-      for (int i = lane; i < H / 2; i += 32) {
-        const uint32_t v = xr[i];
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-          if (t == warp) am[t] = fmaxf(am[t], fmaxf(fabsf(bf16_lo(v)), fabsf(bf16_hi(v))));
+      if (bcol) {
+        bb[0] = lds32(bp + ks * 32);
+        bb[1] = lds32(bp + ks * 32 + 16);
+        bb[2] = lds32(bp + ks * 32 + 32);
+        bb[3] = lds32(bp + ks * 32 + 48);
       }
+      mma_bf16_16816(d0, a[0], a[1], bb[0], bb[1]);
+      mma_bf16_16816(d1, a[2], a[3], bb[2], bb[3]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        am = fmaxf(am, fmaxf(fabsf(bf16_lo(bb[q])), fabsf(bf16_hi(bb[q]))));
     }
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        acc[t] += __shfl_xor_sync(0xFFFFFFFFu, acc[t], off);
-        am[t] = fmaxf(am[t], __shfl_xor_sync(0xFFFFFFFFu, am[t], off));
-      }
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        red[warp * NT + t] = acc[t];
-        if (nrows > 0 && r == 0) amax_part[part * NT + t] = am[t];
-        if (nrows == 0 && warp == t) amax_part[t] = am[t];
-      }
-    }
+    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+    // D[row g][token 2c, 2c+1]
+    red[(warp * 8 + g) * 8 + 2 * c] = d0[0] + d1[0];
+    red[(warp * 8 + g) * 8 + 2 * c + 1] = d0[1] + d1[1];
+    if (c == 0) amax_part[warp * 8 + g] = am;
   }
   __syncthreads();
   if (tid < nrows * T) {
     const int rl = tid / T, t = tid % T;
-    float s = red[(rl * geo.wpr) * NT + t];
-    for (int p = 1; p < geo.wpr; ++p) s += red[(rl * geo.wpr + p) * NT + t];
-    st_tag(reinterpret_cast<unsigned long long*>(ws.logits) + (size_t)t * E + row0 + rl,
-           __float_as_uint(s), ep);
+    float s = red[rl * 8 + t];
+#pragma unroll
+    for (int w = 1; w < kDcWarps; ++w) s += red[(w * 8 + rl) * 8 + t];
+    unsigned long long* lg = reinterpret_cast<unsigned long long*>(ws.logits);
+#pragma unroll
+    for (int rep = 0; rep < kLogitReplicas; ++rep)
+      st_tag(lg + ((size_t)rep * T + t) * E + row0 + rl, __float_as_uint(s), ep);
   } else if (tid >= kDcCons && tid - kDcCons < T) {
     const int t = tid - kDcCons;
-    const int parts = nrows > 0 ? geo.wpr : 1;
     float m = amax_part[t];
-    for (int p = 1; p < parts; ++p) m = fmaxf(m, amax_part[p * NT + t]);
+#pragma unroll
+    for (int w = 1; w < kDcWarps; ++w) m = fmaxf(m, amax_part[w * 8 + t]);
     shift_s[t] = token_shift(m);
     xfac_s[t] = mode == 0 ? pow2f(shift_s[t]) : xS;
   }
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     const int nb = H / 16;
     for (int blk = tid; blk < T * nb; blk += kDcThreads) {
       const int t = blk / nb, bb = blk % nb;
-      const uint4* src = reinterpret_cast<const uint4*>(xraw + (size_t)t * H + bb * 16);
+      const uint4* src = reinterpret_cast<const uint4*>(xraw + (size_t)t * geo.rs + bb * 32);
       const uint4 u0 = src[0], u1 = src[1];
       const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
       float v[16];
@@ -356,8 +359,9 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   if (warp < T) {
     int e_sel;
     float w_sel;
-    if (!topk_tagged(reinterpret_cast<const unsigned long long*>(ws.logits) + (size_t)warp * E, E,
-                     k, lane, ep, e_sel, w_sel) && lane == 0) {
+    const unsigned long long* lg = reinterpret_cast<const unsigned long long*>(ws.logits) +
+                                   ((size_t)(b % kLogitReplicas) * T + warp) * E;
+    if (!topk_tagged(lg, E, k, lane, ep, e_sel, w_sel) && lane == 0) {
       record_status(ws.ctl, kStTimeout);
       abort_s = 1;
     }
@@ -812,7 +816,8 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   if (T < 1 || T > kNarrowT || num_ctas < 1) return false;
   g.rows_max = (E + num_ctas - 1) / num_ctas;
   if (g.rows_max > kDcWarps) return false;
-  g.wpr = g.rows_max <= kDcWarps / 2 ? 2 : 1;
+  g.rs = 2 * H + 16;
+  if (H % (kDcWarps * 32)) return false;            // whole k-step pairs per warp
   g.KC = H <= 4096 ? H : 4096;
   while (H % g.KC) g.KC -= 128;
   g.nkc = H / g.KC;
@@ -824,7 +829,7 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   g.xop = T * g.x_stride > kGroup * g.h_stride ? T * g.x_stride : kGroup * g.h_stride;
   g.smax = T * k;
   g.gmax = g.smax < E ? g.smax : E;
-  const int route_bytes = g.rows_max * H * 2 + T * H * 2;
+  const int route_bytes = (g.rows_max + T) * g.rs;
   const int scratch = T * k * 64 * 4;  // sorted selections; Y pairs of one tile for the combine
   const int fixed = g.xop + kDcWarps * 2 * 128 * 4 + g.gmax * (int)sizeof(DcGroup) +
                     g.smax * 12 + 8 + 8 * (2 * 3 + 2 * 16 + 2) + kDcStatic;

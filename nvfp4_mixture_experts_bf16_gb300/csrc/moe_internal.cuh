@@ -20,6 +20,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // grouped path (the N of one m16n8k16 MMA).
 constexpr int kNarrowT = 8;
 constexpr int kGroup = 8;
+// The fused narrow kernel writes its tagged logits this many times ([replica][T][E]); CTA b
+// polls replica b % kLogitReplicas, which spreads the 152 readers over more L2 lines.
+constexpr int kLogitReplicas = 8;
 
 // ------------------------------------------------------------------ workspace view
 // Control words at the start of the workspace (zero-filled before first use).
@@ -48,7 +51,7 @@ struct WsView {
   uint32_t* ctl;
   GroupMeta* gmeta;    // [G]
   uint32_t* slot_amax; // [T*k] bits of max|h| per slot (W4A16), zeroed by the routing stage
-  float* logits;       // [T][E] (fused narrow kernel: [T][E] 64-bit {logit bits, epoch})
+  float* logits;       // [T][E] (fused narrow kernel: [replica][T][E] 64-bit {logit, epoch})
   int32_t* idx;        // [T][k]
   float* w;            // [T][k]
   int32_t* slot_of;    // [T][k]

@@ -25,8 +25,12 @@ import nvfp4_mixture_experts_bf16_gb300 as moe
 
 TOL = {0: 2e-3, 1: 5e-3}
 U = 2.0 ** -24
-GAMMA_NARROW = 32     # summation depth bound of the narrow router GEMV
-GAMMA_WIDE = 300      # summation depth bound of the grouped router GEMM
+# Summation-depth bounds n of the FP32 router accumulation (error <= gamma(n) * sum|x*w|).
+# Narrow calls: per warp one tensor-core chain of 16-product MMA steps over H/8 (16 steps at
+# H = 4096, two interleaved chains), then 8 warp partials: n <= 16*16 + 1 + 8 < 300. The
+# route-only kernel (FMA tree) is far below that. Wide calls: tcgen05 over 64 K-steps.
+GAMMA_NARROW = 300
+GAMMA_WIDE = 300
 
 
 def gamma(n):
