@@ -70,7 +70,7 @@ __device__ __forceinline__ void st_tag(unsigned long long* p, uint32_t data, uin
 }
 __device__ __forceinline__ unsigned long long ld_tag(const unsigned long long* p) {
   unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p));
   return v;
 }
 __device__ __forceinline__ uint32_t tag_of(unsigned long long v) { return (uint32_t)(v >> 32); }
@@ -92,13 +92,15 @@ __device__ __forceinline__ bool topk_tagged_v(const unsigned long long* row, int
                                               int lane, uint32_t ep, int& e_out, float& w_out) {
   uint32_t key[V];
   uint32_t pending = 0;
+  unsigned long long w[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i)   // every load in flight before any is examined
+    w[i] = lane + 32 * i < E ? ld_tag(row + lane + 32 * i) : 0ull;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int e = lane + 32 * i;
     key[i] = 0u;
-    if (e < E) {
-      const unsigned long long w = ld_tag(row + e);
-      if (tag_of(w) == ep) key[i] = logit_key(__uint_as_float(data_of(w)));
+    if (lane + 32 * i < E) {
+      if (tag_of(w[i]) == ep) key[i] = logit_key(__uint_as_float(data_of(w[i])));
       else pending |= 1u << i;
     }
   }
@@ -759,14 +761,32 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     uint32_t* ysm = reinterpret_cast<uint32_t*>(arena);   // [T][k][64] BF16 pairs of the tile
     for (int ht = b; ht < dn_tiles; ht += G) {
       consumer_sync(kDcCons);
-      for (int it2 = tid; it2 < S * 64; it2 += kDcCons) {
-        const int sj = it2 >> 6, p2 = it2 & 63;
-        unsigned long long w[1];
-        if (!poll_tags<1>(ws.ytag + (size_t)sel_slot[sj] * (H / 2) + ht * 64 + p2, ep, w)) {
-          record_status(ws.ctl, kStTimeout);
-          abort_s = 1;
+      // 8 pairs per thread in flight at a time: (selection sj, pair p2) = it2 + u * 256
+      for (int base = 0; base < S * 64; base += 8 * kDcCons) {
+        unsigned long long w[8];
+        bool have[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int it2 = base + tid + u * kDcCons;
+          have[u] = it2 < S * 64;
+          w[u] = have[u] ? ld_tag(ws.ytag + (size_t)sel_slot[it2 >> 6] * (H / 2) + ht * 64 +
+                                  (it2 & 63))
+                         : 0ull;
         }
-        ysm[it2] = data_of(w[0]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int it2 = base + tid + u * kDcCons;
+          if (have[u] && tag_of(w[u]) != ep) {
+            unsigned long long w1[1];
+            if (!poll_tags<1>(ws.ytag + (size_t)sel_slot[it2 >> 6] * (H / 2) + ht * 64 +
+                                  (it2 & 63), ep, w1)) {
+              record_status(ws.ctl, kStTimeout);
+              abort_s = 1;
+            }
+            w[u] = w1[0];
+          }
+          if (have[u]) ysm[it2] = data_of(w[u]);
+        }
       }
       consumer_sync(kDcCons);
       for (int it2 = tid; it2 < T * 64; it2 += kDcCons) {
