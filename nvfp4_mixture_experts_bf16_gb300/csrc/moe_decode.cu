@@ -52,7 +52,7 @@ struct DcGeom {
   int KC, nkc, row_bytes;       // gate/up stage: KC reduction columns, nkc stages per task
   int gu_stage, gu_stages;
   int dn_stage, dn_stages;
-  int arena;                    // router rows + raw x | routing scratch | gate/up ring | down ring
+  int arena;                    // router rows + raw x | gate/up ring | down ring
                                 // | combine staging
   int x_stride;                 // 2H + 64: one x operand row
   int h_stride;                 // 2I + 16: one h operand row
@@ -191,8 +191,12 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   int32_t* sel_idx = reinterpret_cast<int32_t*>(grp + geo.gmax);        // [S]
   float* sel_w = reinterpret_cast<float*>(sel_idx + geo.smax);          // [S]
   int32_t* sel_slot = reinterpret_cast<int32_t*>(sel_w + geo.smax);     // [S]
+  // the selections sorted by expert (own region: the arena only ever receives TMA writes and
+  // the combine's staging, so no proxy fence is needed before the first weight copy)
+  int32_t* sorted_e = sel_slot + geo.smax;                               // [S] expert of slot p
+  int32_t* sorted_t = sorted_e + geo.smax;                               // [S] token of slot p
   uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(sel_slot + geo.smax) + 7) & ~uintptr_t(7));
+      (reinterpret_cast<uintptr_t>(sorted_t + geo.smax) + 7) & ~uintptr_t(7));
   uint64_t* gfull = bars;
   uint64_t* gempty = gfull + geo.gu_stages;
   uint64_t* dfull = gempty + geo.gu_stages;
@@ -356,8 +360,6 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   // ---------------- 2. routing, in every CTA
   // top-k + softmax of every token (warp t), then a stable sort of the S = T*k selections by
   // expert: entry s = t*k + j goes to slot #{s' : e_s' < e_s} + #{s' < s : e_s' == e_s}
-  int32_t* sorted_e = reinterpret_cast<int32_t*>(arena);   // [S] expert of slot p
-  int32_t* sorted_t = sorted_e + geo.smax;                  // [S] token of slot p
   if (warp < T) {
     int e_sel;
     float w_sel;
@@ -438,7 +440,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       ws.ctl[kCtlUnique] = (uint32_t)U;
     }
   }
-  __syncthreads();   // the routing scratch in the arena is dead from here on
+  __syncthreads();   // groups and selections are final from here on
 
   const int gu_tiles = I / 16, dn_tiles = H / kDnRows;
   int q0, q1, d0, d1;
@@ -448,7 +450,6 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   if (warp == kDcWarps) {
     // ---------------- producer: gate/up tasks, then this CTA's down tasks
     if (lane != 0) return;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     const uint32_t half = geo.row_bytes;
     int chunk = 0;
     for (int q = q0; q < q1 && !abort_s; ++q) {
@@ -850,9 +851,9 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   g.smax = T * k;
   g.gmax = g.smax < E ? g.smax : E;
   const int route_bytes = (g.rows_max + T) * g.rs;
-  const int scratch = T * k * 64 * 4;  // sorted selections; Y pairs of one tile for the combine
+  const int scratch = T * k * 64 * 4;  // Y pairs of one tile for the combine
   const int fixed = g.xop + kDcWarps * 2 * 128 * 4 + g.gmax * (int)sizeof(DcGroup) +
-                    g.smax * 12 + 8 + 8 * (2 * 3 + 2 * 16 + 2) + kDcStatic;
+                    g.smax * 20 + 8 + 8 * (2 * 3 + 2 * 16 + 2) + kDcStatic;
   const int avail = kDcSmemMax - fixed;
   g.gu_stages = avail / g.gu_stage;
   if (g.gu_stages > 3) g.gu_stages = 3;
