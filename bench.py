@@ -173,9 +173,11 @@ def oracle_sample(wl, seed, n_tokens, threads):
     return x, wr, ex
 
 
-def time_oracle(wl, seed, steps, budget_s, threads, n_tokens):
+def time_oracle(wl, seed, steps, budget_s, threads, n_tokens, warmup=1):
     import oracle
     x, wr, ex = oracle_sample(wl, seed, n_tokens, threads)
+    for _ in range(warmup):   # untimed: thread pool start-up and first-touch of the sample
+        oracle.forward(x, wr, ex, wl.k, wl.mode, nthreads=threads, want=("out_bf16",))
     times = []
     t_end = time.time() + budget_s
     for _ in range(max(1, steps)):
@@ -196,9 +198,11 @@ def run_reference(args, rank, world):
         return
     threads = os.cpu_count() or 1
     n_tok = 4 if wl.T <= 8 else 8
-    cb = time_oracle(wl, args.seed, args.steps, budget_s=120, threads=threads, n_tokens=n_tok)
-    line = dict(impl="reference", metric=METRIC, value=cb["value"], unit=cb["unit"], n_gpus=0,
-                steps=cb["calls"], warmup=0, ms_per_step=1e3 * n_tok / cb["value"],
+    cb = time_oracle(wl, args.seed, args.steps, budget_s=120, threads=threads, n_tokens=n_tok,
+                     warmup=args.warmup)
+    line = dict(impl="reference", metric=METRIC, value=cb["value"], unit=cb["unit"],
+                n_gpus=world, steps=cb["calls"], warmup=args.warmup,
+                ms_per_step=1e3 * n_tok / cb["value"],
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
                 data="synthetic", config=dict(workload=wl.name, T=wl.T, hidden=wl.H,
                                               experts=wl.E, top_k=wl.k, inter=wl.I,
