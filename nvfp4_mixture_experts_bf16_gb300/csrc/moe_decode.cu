@@ -130,8 +130,7 @@ __device__ __forceinline__ bool topk_tagged_v(const unsigned long long* row, int
 
 __device__ __forceinline__ bool topk_tagged(const unsigned long long* row, int E, int k, int lane,
                                             uint32_t ep, int& e_out, float& w_out) {
-  if (E <= 128) return topk_tagged_v<4>(row, E, k, lane, ep, e_out, w_out);
-  if (E <= 256) return topk_tagged_v<8>(row, E, k, lane, ep, e_out, w_out);
+  // two register widths only: every instantiation is code that each CTA fetches once per launch
   if (E <= 512) return topk_tagged_v<16>(row, E, k, lane, ep, e_out, w_out);
   return topk_tagged_v<32>(row, E, k, lane, ep, e_out, w_out);
 }
@@ -178,11 +177,12 @@ __device__ __forceinline__ void balanced_range(int ntasks, int& q0, int& q1) {
   q1 = (int)(((unsigned)ntasks * (blockIdx.x + 1)) / gridDim.x);
 }
 
-template <int NT>
+template <int NT, int MODE>
 __global__ void __launch_bounds__(kDcThreads, 1)
     k_decode(PackView pk, WsView ws, DcGeom geo, const uint16_t* __restrict__ x,
-             const uint16_t* __restrict__ wr, int mode, float xS, float x_inv6S,
+             const uint16_t* __restrict__ wr, float xS, float x_inv6S,
              uint16_t* __restrict__ out) {
+  constexpr int mode = MODE;   // 0: W4A16, 1: W4A4 (one instantiation each: smaller code)
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* arena = smem;
   unsigned char* xop = arena + geo.arena;
@@ -777,16 +777,23 @@ __global__ void __launch_bounds__(kDcThreads, 1)
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int it2 = base + tid + u * kDcCons;
-          if (have[u] && tag_of(w[u]) != ep) {
-            unsigned long long w1[1];
-            if (!poll_tags<1>(ws.ytag + (size_t)sel_slot[it2 >> 6] * (H / 2) + ht * 64 +
-                                  (it2 & 63), ep, w1)) {
-              record_status(ws.ctl, kStTimeout);
-              abort_s = 1;
-            }
-            w[u] = w1[0];
-          }
           if (have[u]) ysm[it2] = data_of(w[u]);
+        }
+        // words that had not arrived yet: poll them one at a time (rare)
+        uint32_t late = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) late |= (have[u] && tag_of(w[u]) != ep) ? 1u << u : 0u;
+#pragma unroll 1
+        for (int u = 0; u < 8; ++u) {
+          if (!(late & (1u << u))) continue;
+          const int it2 = base + tid + u * kDcCons;
+          unsigned long long w1[1];
+          if (!poll_tags<1>(ws.ytag + (size_t)sel_slot[it2 >> 6] * (H / 2) + ht * 64 +
+                                (it2 & 63), ep, w1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          ysm[it2] = data_of(w1[0]);
         }
       }
       consumer_sync(kDcCons);
@@ -882,17 +889,29 @@ cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(lc, kern, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, pk, ws,
-                      geo, x, wr, mode, xS, x_inv6S, out);
+                      geo, x, wr, xS, x_inv6S, out);
   };
+  if (mode == 1) {
+    switch (ws.T) {
+      case 1: return go(k_decode<1, 1>);
+      case 2: return go(k_decode<2, 1>);
+      case 3: return go(k_decode<3, 1>);
+      case 4: return go(k_decode<4, 1>);
+      case 5: return go(k_decode<5, 1>);
+      case 6: return go(k_decode<6, 1>);
+      case 7: return go(k_decode<7, 1>);
+      default: return go(k_decode<8, 1>);
+    }
+  }
   switch (ws.T) {
-    case 1: return go(k_decode<1>);
-    case 2: return go(k_decode<2>);
-    case 3: return go(k_decode<3>);
-    case 4: return go(k_decode<4>);
-    case 5: return go(k_decode<5>);
-    case 6: return go(k_decode<6>);
-    case 7: return go(k_decode<7>);
-    default: return go(k_decode<8>);
+    case 1: return go(k_decode<1, 0>);
+    case 2: return go(k_decode<2, 0>);
+    case 3: return go(k_decode<3, 0>);
+    case 4: return go(k_decode<4, 0>);
+    case 5: return go(k_decode<5, 0>);
+    case 6: return go(k_decode<6, 0>);
+    case 7: return go(k_decode<7, 0>);
+    default: return go(k_decode<8, 0>);
   }
 }
 
