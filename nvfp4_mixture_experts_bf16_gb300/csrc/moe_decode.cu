@@ -85,11 +85,84 @@ __device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t* ctr) {
   return old;
 }
 
+// Top-k + softmax of one token by one warp, with a 32-entry shared-memory scratch (cand):
+// threshold L = the k-th largest of the 32 lane maxima (a bitonic sort across lanes). The k lane
+// maxima >= L are k distinct logits, so every one of the top k has key >= L. The candidates
+// (keys >= L, about 12 of 512 for k = 10) are written to cand at their prefix position, each
+// candidate's exact rank by (key desc, index asc) is counted against the others, and ranks < k
+// are the selection. More than 32 candidates: the redux.sync rounds of warp_select_softmax.
+template <int V>
+__device__ __forceinline__ void warp_select_scratch(uint32_t (&key)[V], int k, int lane,
+                                                    unsigned long long* cand, int& e_out,
+                                                    float& w_out) {
+  uint32_t sv = 0u;
+#pragma unroll
+  for (int i = 0; i < V; ++i) sv = key[i] > sv ? key[i] : sv;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {   // ascending across lanes
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, sv, stride);
+      const bool asc = (lane & size) == 0, low = (lane & stride) == 0;
+      const uint32_t mn = sv < o ? sv : o, mx = sv < o ? o : sv;
+      sv = (asc == low) ? mn : mx;
+    }
+  }
+  uint32_t thr = __shfl_sync(0xFFFFFFFFu, sv, 32 - k);
+  if (thr == 0u) thr = 1u;   // fewer than k lanes hold logits: every logit is a candidate
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i) cnt += key[i] >= thr;
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  const int C = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  if (C > 32) {
+    warp_select_softmax<V>(key, k, lane, e_out, w_out);
+    return;
+  }
+  // candidate word: key in the high half, ~index in the low half, so that a larger word is a
+  // larger logit, and for equal logits the lower index
+  int pos = incl - cnt;
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+    if (key[i] >= thr) cand[pos++] = ((unsigned long long)key[i] << 32) | (uint32_t)~(lane + 32 * i);
+  __syncwarp();
+  e_out = 0;
+  float v = 0.0f;
+  int r = 32;
+  unsigned long long mine = 0ull;
+  if (lane < C) {
+    mine = cand[lane];
+    r = 0;
+    for (int j = 0; j < C; ++j) r += cand[j] > mine;
+  }
+  __syncwarp();
+  if (r < k) cand[r] = mine;   // cand[0..k) <- the selection in order
+  __syncwarp();
+  if (lane < k) {
+    const unsigned long long w = cand[lane];
+    e_out = (int)~(uint32_t)w;
+    v = key_logit((uint32_t)(w >> 32));
+  }
+  __syncwarp();
+  const float m0 = __shfl_sync(0xFFFFFFFFu, v, 0);
+  const float ex = lane < k ? expf(v - m0) : 0.0f;
+  float z = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
+  w_out = ex / z;
+}
+
 // Top-k + softmax of one token from its tagged logits: polls (bounded) until every logit of
 // the current epoch has arrived. False on timeout.
 template <int V>
 __device__ __forceinline__ bool topk_tagged_v(const unsigned long long* row, int E, int k,
-                                              int lane, uint32_t ep, int& e_out, float& w_out) {
+                                              int lane, uint32_t ep, int& e_out, float& w_out,
+                                              unsigned long long* cand) {
   uint32_t key[V];
   uint32_t pending = 0;
   unsigned long long w[V];
@@ -124,15 +197,16 @@ __device__ __forceinline__ bool topk_tagged_v(const unsigned long long* row, int
       }
     }
   }
-  warp_select_softmax<V>(key, k, lane, e_out, w_out);
+  warp_select_scratch<V>(key, k, lane, cand, e_out, w_out);
   return ok;
 }
 
 __device__ __forceinline__ bool topk_tagged(const unsigned long long* row, int E, int k, int lane,
-                                            uint32_t ep, int& e_out, float& w_out) {
+                                            uint32_t ep, int& e_out, float& w_out,
+                                            unsigned long long* cand) {
   // two register widths only: every instantiation is code that each CTA fetches once per launch
-  if (E <= 512) return topk_tagged_v<16>(row, E, k, lane, ep, e_out, w_out);
-  return topk_tagged_v<32>(row, E, k, lane, ep, e_out, w_out);
+  if (E <= 512) return topk_tagged_v<16>(row, E, k, lane, ep, e_out, w_out, cand);
+  return topk_tagged_v<32>(row, E, k, lane, ep, e_out, w_out, cand);
 }
 
 // Polls n tagged words (bounded) until all carry epoch ep. False on timeout.
@@ -268,6 +342,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     const unsigned char* bp = xraw + (size_t)g * geo.rs + (size_t)(warp * kw + 2 * c) * 2;
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
     float am = 0.0f;
+#pragma unroll 2
     for (int ks = 0; ks < kw / 16; ks += 2) {
       uint32_t a[4] = {0u, 0u, 0u, 0u}, bb[4] = {0u, 0u, 0u, 0u};
       if (arow) {
@@ -365,7 +440,9 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     float w_sel;
     const unsigned long long* lg = reinterpret_cast<const unsigned long long*>(ws.logits) +
                                    ((size_t)(b % kLogitReplicas) * T + warp) * E;
-    if (!topk_tagged(lg, E, k, lane, ep, e_sel, w_sel) && lane == 0) {
+    // scratch: 32 words per warp in the GEMV partials buffer (free once the logits are out)
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(red) + warp * 32;
+    if (!topk_tagged(lg, E, k, lane, ep, e_sel, w_sel, cand) && lane == 0) {
       record_status(ws.ctl, kStTimeout);
       abort_s = 1;
     }
@@ -410,35 +487,6 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     gr.n = n;
     gr.toks = toks;
     grp[ubase + __popc(gbal & ((1u << lane) - 1u))] = gr;
-  }
-  if (b == 0) {
-    // CTA 0 publishes the routing: counts/offsets of every expert (binary search in the
-    // sorted selections), the per-token experts, weights and slots, and the permutation
-    for (int e = tid; e < E; e += kDcThreads) {
-      int lo = 0, hi = S;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (sorted_e[mid] < e) lo = mid + 1; else hi = mid;
-      }
-      int lo2 = lo, hi2 = S;
-      while (lo2 < hi2) {
-        const int mid = (lo2 + hi2) >> 1;
-        if (sorted_e[mid] <= e) lo2 = mid + 1; else hi2 = mid;
-      }
-      ws.offsets[e] = lo;
-      ws.counts[e] = lo2 - lo;
-    }
-    if (tid < S) {
-      ws.idx[tid] = sel_idx[tid];
-      ws.w[tid] = sel_w[tid];
-      ws.slot_of[tid] = sel_slot[tid];
-      ws.perm[sel_slot[tid]] = tid / k;
-    }
-    if (tid == 0) {
-      ws.offsets[E] = S;
-      ws.ctl[kCtlGroups] = (uint32_t)U;
-      ws.ctl[kCtlUnique] = (uint32_t)U;
-    }
   }
   __syncthreads();   // groups and selections are final from here on
 
@@ -809,6 +857,37 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         reinterpret_cast<uint32_t*>(out + (size_t)t * H)[ht * 64 + p2] =
             (uint32_t)f32_to_bf16_rn(a0) | ((uint32_t)f32_to_bf16_rn(a1) << 16);
       }
+    }
+  }
+
+  if (b == 0) {
+    // CTA 0 publishes the routing once its own work is done (no later phase reads it):
+    // counts/offsets of every expert (binary search in the sorted selections), the per-token
+    // experts, weights and slots, and the permutation
+    for (int e = tid; e < E; e += kDcCons) {
+      int lo = 0, hi = S;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sorted_e[mid] < e) lo = mid + 1; else hi = mid;
+      }
+      int lo2 = lo, hi2 = S;
+      while (lo2 < hi2) {
+        const int mid = (lo2 + hi2) >> 1;
+        if (sorted_e[mid] <= e) lo2 = mid + 1; else hi2 = mid;
+      }
+      ws.offsets[e] = lo;
+      ws.counts[e] = lo2 - lo;
+    }
+    if (tid < S) {
+      ws.idx[tid] = sel_idx[tid];
+      ws.w[tid] = sel_w[tid];
+      ws.slot_of[tid] = sel_slot[tid];
+      ws.perm[sel_slot[tid]] = tid / k;
+    }
+    if (tid == 0) {
+      ws.offsets[E] = S;
+      ws.ctl[kCtlGroups] = (uint32_t)U;
+      ws.ctl[kCtlUnique] = (uint32_t)U;
     }
   }
 
