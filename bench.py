@@ -459,7 +459,8 @@ def run_native(args, rank, world, local_rank):
                 tokens_per_s=round(w3.T / (ms3 / 1e3), 1), ms=round(ms3, 3),
                 expert_tflops=round(flops / (ms3 * 1e-3) / 1e12, 2),
                 note=("tcgen05 block-scaled FP4 grouped GEMMs" if mode == 1 else
-                      "grouped mma.sync path (CUDA-core dequant)"))
+                      "tcgen05 kind::f16 grouped GEMMs, weights dequantised to f16 in shared "
+                      "memory"))
         torch.cuda.synchronize()
 
     cpu = None

@@ -67,7 +67,7 @@ int num_sms_of_current_device() {
 struct WsLayout {
   size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm,
       chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, htag, ytag, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
-      xsf_atoms, hq_perm, hsf_atoms, total;
+      xsf_atoms, hq_perm, hsf_atoms, xh_perm, hf_perm, total;
   size_t slot_amax_bytes;
   int G, NT;
 };
@@ -103,18 +103,21 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
   L.y = take(mode >= 0 ? (size_t)S * H * 2 : 0);
   L.htag = take(mode >= 0 && narrow ? (size_t)S * (I / 16) * 9 * 8 : 0);
   L.ytag = take(mode >= 0 && narrow ? (size_t)S * (H / 2) * 8 : 0);
-  // grouped tensor-core path (wide W4A4): 128-slot token tiles in a padded permuted space
-  const bool tc = mode == 1 && T > moe::kNarrowT;
+  // grouped tensor-core path (wide calls): 128-slot token tiles in a padded permuted space
+  const bool tc = mode >= 0 && moe::tile_path(T, H, I, mode);
   L.NT = tc ? (int)((S + 127) / 128 + (S < E ? S : E)) : 0;
   const size_t P = (size_t)L.NT * 128;
+  const bool w4a4 = tc && mode == 1, w4a16 = tc && mode == 0;
   L.tt_expert = take((size_t)L.NT * 4);
   L.tt_slot0 = take((size_t)L.NT * 4);
   L.tt_n = take((size_t)L.NT * 4);
   L.ttbase = take(tc ? (size_t)(E + 1) * 4 : 0);
-  L.xq_perm = take(P * H / 2);
-  L.xsf_atoms = take((size_t)L.NT * (H / 64) * 512);
-  L.hq_perm = take(P * I / 2);
-  L.hsf_atoms = take((size_t)L.NT * (I / 64 > 0 ? I / 64 : 1) * 512);
+  L.xq_perm = take(w4a4 ? P * H / 2 : 0);
+  L.xsf_atoms = take(w4a4 ? (size_t)L.NT * (H / 64) * 512 : 0);
+  L.hq_perm = take(w4a4 ? P * I / 2 : 0);
+  L.hsf_atoms = take(w4a4 ? (size_t)L.NT * (I / 64 > 0 ? I / 64 : 1) * 512 : 0);
+  L.xh_perm = take(w4a16 ? P * H * 2 : 0);
+  L.hf_perm = take(w4a16 ? P * I * 2 : 0);
   L.total = o;
   return L;
 }
@@ -153,6 +156,8 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   v.xsf_atoms = b + L.xsf_atoms;
   v.hq_perm = b + L.hq_perm;
   v.hsf_atoms = b + L.hsf_atoms;
+  v.xh_perm = reinterpret_cast<__half*>(b + L.xh_perm);
+  v.hf_perm = reinterpret_cast<__half*>(b + L.hf_perm);
   return v;
 }
 
@@ -432,7 +437,8 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
                                    pack->x_inv6S, v.idx, v.w, v.counts, v.offsets, v.perm);
     n += 1;
   }
-  const bool use_tc = !narrow && m == 1 && v.NT > 0 && H % 256 == 0 && moe::tc_supported();
+  // wide calls run the tensor-core grouped path when the layout reserved its token tiles
+  const bool use_tc = !narrow && v.NT > 0;
   if (!narrow) {
     if (e == cudaSuccess)
       e = moe::launch_route_wide(lc, x, router_w, v, &pack->view, v.idx, v.w, v.counts, v.offsets,
@@ -445,10 +451,15 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
   if (e == cudaSuccess) e = prof_mark(lc.stream, 1);
   if (e == cudaSuccess) e = prof_mark(lc.stream, 2);
   if (use_tc) {
-    // x quantisation + permutation, gate/up, down on tcgen05 (stage 1 covers all three)
+    // x operand by padded slot, gate/up, (h operand,) down on tcgen05 (stage 1 covers all)
     if (e == cudaSuccess) {
-      e = moe::launch_tc_experts(lc, pack->view, v, x, pack->x_scale, pack->x_inv6S);
-      n += 3;
+      if (m == 1) {
+        e = moe::launch_tc_experts(lc, pack->view, v, x, pack->x_scale, pack->x_inv6S);
+        n += 3;
+      } else {
+        e = moe::launch_tc16_experts(lc, pack->view, v, x);
+        n += 4;
+      }
     }
     if (e == cudaSuccess) e = prof_mark(lc.stream, 3);
     if (e == cudaSuccess) e = prof_mark(lc.stream, 4);

@@ -81,6 +81,8 @@ struct WsView {
   uint8_t* xsf_atoms;  // [NT][H/64][512] activation scales in tensor-core scale-factor atoms
   uint8_t* hq_perm;    // [128*NT][I/2]  h codes by pslot
   uint8_t* hsf_atoms;  // [NT][I/64][512]
+  __half* xh_perm;     // W4A16 grouped path: [128*NT][H] f16(x * 2^-s) by pslot
+  __half* hf_perm;     // W4A16 grouped path: [128*NT][I] f16(h * 2^-s) by pslot
   int T, H, E, k, I, G, NT;
 };
 
@@ -526,6 +528,11 @@ bool tc_supported();
 // W4A4 grouped experts on tcgen05: activation quantisation + permutation, gate/up, down.
 cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
                               const uint16_t* x, float xS, float x_inv6S);
+// W4A16 grouped experts on tcgen05 kind::f16 (weights dequantised in shared memory).
+cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
+                                const uint16_t* x);
+// Whether a wide call runs the tensor-core grouped path (128-slot token tiles) for its mode.
+bool tile_path(int T, int H, int I, int mode);
 // Router logits of a wide call on tcgen05 (BF16 x BF16 -> FP32).
 cudaError_t launch_tc_router(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
                              const WsView& ws);

@@ -574,6 +574,373 @@ __global__ void __launch_bounds__(64 * kXqTok) k_xquant_perm(const uint16_t* __r
   }
 }
 
+// ------------------------------------------------------------------ W4A16 grouped experts
+// Tensor cores need both operands in one 16-bit type, and NVFP4 x BF16 has no MMA kind, so the
+// W4A16 grouped path runs tcgen05 kind::f16 on f16 operands that hold the values exactly:
+//   A (weights): E2M1 code x E4M3 scale (<= 6 significant bits, |v| <= 2688: exact in f16),
+//     dequantised in shared memory by converter warps from the TMA-staged FP4 codes;
+//   B (activations): x * 2^-s per token (gate/up) and BF16 h * 2^-s per slot (down), with s
+//     putting the row's max |value| in [2^14, 2^15) (exact, as in the narrow-call path);
+// the epilogues restore 2^s. Tiles: 128 weight rows x 128 padded slots, K = 64 per stage.
+// Gate/up issues two MMAs per K step (the 128 gate rows and the 128 up rows of the same
+// intermediate indices) into two accumulators, so one epilogue lane holds both g and u.
+constexpr int kT16Stages = 3;
+constexpr int kT16Threads = 10 * 32;   // producer, MMA, 4 converter warps, 4 epilogue warps
+constexpr uint32_t kIdescF16 = (1u << 4) | ((uint32_t)(kTileN >> 3) << 17) |
+                               ((uint32_t)(kTileM >> 4) << 24);   // f16 x f16 -> f32, 128x128
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(kIdescF16), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void t16_epi_sync() {  // the 4 epilogue warps
+  asm volatile("bar.sync 3, 128;" ::: "memory");
+}
+
+// Per-stage layout (bytes): conv A (f16, SW128; gate/up: gate 16 KB + up 16 KB), B (16 KB),
+// raw FP4 codes (gate/up: 2 x 128 rows x 32 B), scale-factor atoms (gate/up 2, down 1).
+template <bool DOWN>
+struct T16 {
+  static constexpr int kConv = DOWN ? 16384 : 32768;
+  static constexpr int kB = 16384;
+  static constexpr int kRaw = DOWN ? 4096 : 8192;
+  static constexpr int kSf = DOWN ? 512 : 1024;
+  static constexpr int kStage = ((kConv + kB + kRaw + kSf) + 1023) / 1024 * 1024;
+  static constexpr int kTmemCols = DOWN ? 256 : 512;
+  static constexpr int kYStage = kTileN * kYStride * 2;   // down: transposed BF16 Y tile
+  static constexpr int kSmem = kT16Stages * kStage + (DOWN ? kYStage : 0) + 2 * 512 + 1024;
+};
+
+template <bool DOWN>
+__global__ void __launch_bounds__(kT16Threads, 1)
+    k_tc16(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+           const __grid_constant__ CUtensorMap tm_b, TcParams prm, WsView ws) {
+  using L = T16<DOWN>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t full[kT16Stages], conv_full[kT16Stages], empty[kT16Stages];
+  __shared__ uint64_t acc_full[2], acc_empty[2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_s;
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* smem = smem_raw + pad;
+  unsigned char* ystage = smem + kT16Stages * L::kStage;            // down: Y tile
+  float* colfac = reinterpret_cast<float*>(ystage + (DOWN ? L::kYStage : 0));   // [128]
+  uint32_t* colmax = reinterpret_cast<uint32_t*>(colfac + kTileN);             // [128]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < kT16Stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&conv_full[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    fence_mbar_init();
+    abort_s = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base_s)),
+                 "r"(L::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_s;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int NT = (int)ws.ctl[kCtlTokenTiles];
+  const int ntiles = NT * prm.MT;
+  const int H = prm.H, I = prm.I;
+  const int nks = DOWN ? I / 64 : H / 64;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int it = 0;
+      for (int t = blockIdx.x; t < ntiles && !abort_s; t += gridDim.x) {
+        const int j = t / prm.MT, mt = t % prm.MT;
+        const int e = __ldg(&ws.tt_expert[j]);
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % kT16Stages, n = it / kT16Stages;
+          if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+            break;
+          }
+          unsigned char* st = smem + s * L::kStage;
+          unsigned char* bt = st + L::kConv;
+          unsigned char* raw = bt + L::kB;
+          unsigned char* sf = raw + L::kRaw;
+          mbar_arrive_expect_tx(&full[s], L::kB + L::kRaw + L::kSf);
+          if (!DOWN) {
+            tma_2d(raw, &tm_a0, ks * 32, e * I + mt * 128, &full[s]);
+            tma_2d(raw + 4096, &tm_a1, ks * 32, e * I + mt * 128, &full[s]);
+            // scale atoms of the two 64-row intermediate tiles (gate rows 0..63, up 64..127)
+            for (int h2 = 0; h2 < 2; ++h2)
+              bulk_g2s(sf + h2 * 512,
+                       prm.sfa + (((size_t)e * (I / 64) + 2 * mt + h2) * (H / 64) + ks) * 512, 512,
+                       &full[s]);
+          } else {
+            tma_2d(raw, &tm_a0, ks * 32, e * H + mt * 128, &full[s]);
+            bulk_g2s(sf, prm.sfa + (((size_t)e * (H / 128) + mt) * (I / 64) + ks) * 512, 512,
+                     &full[s]);
+          }
+          tma_2d(bt, &tm_b, ks * 128, j * 128, &full[s]);
+        }
+      }
+      const int used = it < kT16Stages ? it : kT16Stages;
+      for (int i = 0; i < used; ++i) {
+        const int c = it - 1 - i;
+        (void)mbar_wait(&full[c % kT16Stages], (c / kT16Stages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      const uint32_t bufcols = DOWN ? kTileN : 2 * kTileN;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
+        const int buf = tcount & 1, use = tcount >> 1;
+        if (use > 0 && !abort_s && !mbar_wait(&acc_empty[buf], (use - 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        fence_after();
+        const uint32_t d0 = tmem + buf * bufcols;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % kT16Stages, n = it / kT16Stages;
+          if (!abort_s && !mbar_wait(&conv_full[s], n & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          fence_after();
+          unsigned char* st = smem + s * L::kStage;
+          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + L::kConv);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t acc = (ks > 0 || q > 0) ? 1u : 0u;
+            mma_f16(d0, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32), acc);
+            if (!DOWN)
+              mma_f16(d0 + kTileN, desc_sw128(a0 + 16384 + q * 32), desc_sw128(b0 + q * 32), acc);
+          }
+          commit(&empty[s]);
+        }
+        commit(&acc_full[buf]);
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- converters (warps 2..5)
+    // thread ct owns A row ct (gate/up: gate row ct and up row ct) of every stage
+    const int ct = tid - 64;
+    int it = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        const int s = it % kT16Stages, n = it / kT16Stages;
+        if (!abort_s && !mbar_wait(&full[s], n & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        unsigned char* st = smem + s * L::kStage;
+        const unsigned char* raw = st + L::kConv + L::kB;
+        const unsigned char* sf = raw + L::kRaw;
+#pragma unroll
+        for (int mat = 0; mat < (DOWN ? 1 : 2); ++mat) {
+          const uint4* src = reinterpret_cast<const uint4*>(raw + mat * 4096 + ct * 32);
+          const uint4 c0 = src[0], c1 = src[1];
+          // the row's 4 scale bytes (blocks of 16 along this stage's 64 K)
+          const int rr = DOWN ? ct : mat * 64 + (ct & 63);
+          const unsigned char* atom = sf + (DOWN ? 0 : (ct >> 6) * 512);
+          const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(atom + (rr & 31) * 16 + (rr >> 5) * 4);
+          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          unsigned char* row = st + mat * 16384 + (ct >> 3) * 1024 + (ct & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {   // chunk c: elements 8c .. 8c+7 = code word c
+            const uint32_t sh = e4m3_bcast_f16x2((sc4 >> (8 * (c >> 1))) & 0xFFu);
+            uint32_t f[4];
+            e2m1x8_to_f16x2x4(w[c], f);
+            const uint4 o = make_uint4(hmul2_u32(f[0], sh), hmul2_u32(f[1], sh),
+                                       hmul2_u32(f[2], sh), hmul2_u32(f[3], sh));
+            *reinterpret_cast<uint4*>(row + ((c ^ (ct & 7)) << 4)) = o;
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv_full[s]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 6..9)
+    const int et = tid - 192;               // 0..127
+    const int quad = warp & 3;              // tensor-memory lanes 32*quad .. +31
+    const int row = quad * 32 + lane;       // accumulator row of this thread
+    int tcount = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
+      const int j = t / prm.MT, mt = t % prm.MT;
+      const int buf = tcount & 1, use = tcount >> 1;
+      const int e = ws.tt_expert[j];
+      const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
+      // per column (slot) factor 2^s: of the slot's token (gate/up) or of the slot (down)
+      {
+        float f = 0.0f;
+        if (et < nval) {
+          if (!DOWN) {
+            f = ws.xfac[ws.perm[slot0 + et]];
+          } else {
+            f = __int_as_float((127 + amax_shift(__uint_as_float(ws.slot_amax[slot0 + et]))) << 23);
+          }
+        }
+        colfac[et] = f;
+        if (!DOWN) colmax[et] = 0u;
+      }
+      t16_epi_sync();
+      if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
+        record_status(ws.ctl, kStTimeout);
+        abort_s = 1;
+      }
+      __syncwarp();
+      fence_after();
+      if (!DOWN) {
+        const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * (2 * kTileN);
+        const float mg = prm.mult[e * 3 + 0], mu = prm.mult[e * 3 + 1];
+        const int irow = mt * 128 + row;
+        for (int c0 = 0; c0 < kTileN; c0 += 32) {
+          uint32_t gr[32], ur[32];
+          ld32(tb + c0, gr);
+          ld32(tb + kTileN + c0, ur);
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int col = c0 + q;
+            const float fx = colfac[col];
+            const float gv = __uint_as_float(gr[q]) * mg * fx;
+            const float uv = __uint_as_float(ur[q]) * mu * fx;
+            const uint16_t hb = f32_to_bf16_rn((gv / (1.0f + expf(-gv))) * uv);
+            const uint32_t am = __reduce_max_sync(
+                0xFFFFFFFFu, __float_as_uint(fabsf(__uint_as_float((uint32_t)hb << 16))));
+            if (col < nval) {
+              ws.h16[(size_t)(slot0 + col) * I + irow] = hb;
+              if (lane == 0) atomicMax(&colmax[col], am);
+            }
+          }
+        }
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        t16_epi_sync();
+        if (et < nval) atomicMax(&ws.slot_amax[slot0 + et], colmax[et]);
+      } else {
+        const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN;
+        const float md = prm.mult[e * 3 + 2];
+        uint16_t* yt = reinterpret_cast<uint16_t*>(ystage);
+        for (int c0 = 0; c0 < kTileN; c0 += 32) {
+          uint32_t r[32];
+          ld32(tb + c0, r);
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            yt[(c0 + q) * kYStride + row] =
+                f32_to_bf16_rn(__uint_as_float(r[q]) * md * colfac[c0 + q]);
+        }
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        t16_epi_sync();
+        for (int id = et; id < kTileN * (kTileM / 8); id += 128) {
+          const int col = id >> 4, r8 = id & 15;
+          if (col < nval)
+            *reinterpret_cast<uint4*>(ws.y + (size_t)(slot0 + col) * H + mt * 128 + r8 * 8) =
+                *reinterpret_cast<const uint4*>(yt + col * kYStride + r8 * 8);
+        }
+      }
+      t16_epi_sync();   // colfac / colmax / the Y tile are reused by the next tile
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(L::kTmemCols)
+                 : "memory");
+}
+
+// W4A16 activations by padded slot: 64 threads per token find the token's max |x|, then write
+// f16(x * 2^-s) into each of its k slots' rows and 2^s to xfac (exact; see above).
+__global__ void __launch_bounds__(64 * kXqTok) k_xprep16_perm(const uint16_t* __restrict__ x,
+                                                              WsView ws) {
+  __shared__ int pslot_s[kXqTok][32];
+  __shared__ float am_s[kXqTok][2];
+  const int H = ws.H, k = ws.k;
+  const int tl = threadIdx.x >> 6, q = threadIdx.x & 63, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kXqTok + tl;
+  pdl_wait();
+  pdl_launch_dependents();
+  const bool live = t < ws.T;
+  if (live && q < k) {
+    const int s = ws.slot_of[(size_t)t * k + q], e = ws.idx[(size_t)t * k + q];
+    pslot_s[tl][q] = ws.ttbase[e] * 128 + (s - ws.offsets[e]);
+  }
+  float m = 0.0f;
+  if (live)
+    for (int g = q; g < H / 8; g += 64) {
+      const uint4 u = reinterpret_cast<const uint4*>(x + (size_t)t * H)[g];
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w4[i])), fabsf(bf16_hi(w4[i]))));
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  if (lane == 0) am_s[tl][q >> 5] = m;
+  __syncthreads();
+  if (!live) return;
+  const int sh = token_shift(fmaxf(am_s[tl][0], am_s[tl][1]));
+  const float f = pow2f(-sh);
+  if (q == 0) ws.xfac[t] = pow2f(sh);
+  for (int g = q; g < H / 8; g += 64) {
+    const uint4 u = reinterpret_cast<const uint4*>(x + (size_t)t * H)[g];
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 hh = __floats2half2_rn(__fmul_rn(bf16_lo(w4[i]), f), __fmul_rn(bf16_hi(w4[i]), f));
+      o[i] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int jj = 0; jj < k; ++jj)
+      reinterpret_cast<uint4*>(ws.xh_perm + (size_t)pslot_s[tl][jj] * H)[g] = ov;
+  }
+}
+
+// h of every slot as the down operand by padded slot: f16(h * 2^-s), s from the slot's max |h|.
+__global__ void __launch_bounds__(256) k_hprep16(WsView ws) {
+  const int I = ws.I;
+  const int j = blockIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (j >= (int)ws.ctl[kCtlTokenTiles]) return;
+  const int slot0 = ws.tt_slot0[j], n = ws.tt_n[j];
+  const int words = n * (I / 2);
+  for (int i = threadIdx.x; i < words; i += 256) {
+    const int r = i / (I / 2), wd = i % (I / 2);
+    const int sh = amax_shift(__uint_as_float(ws.slot_amax[slot0 + r]));
+    const float f = pow2f(-sh);
+    const uint32_t v = reinterpret_cast<const uint32_t*>(ws.h16 + (size_t)(slot0 + r) * I)[wd];
+    const __half2 hh = __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), f),
+                                         __fmul_rn(__uint_as_float(v & 0xFFFF0000u), f));
+    reinterpret_cast<uint32_t*>(ws.hf_perm + ((size_t)j * 128 + r) * I)[wd] =
+        *reinterpret_cast<const uint32_t*>(&hh);
+  }
+}
+
 }  // namespace tc
 
 // ------------------------------------------------------------------ host side
@@ -597,17 +964,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D byte tensor [rows][row_bytes] with a box of 128 bytes x box_rows, 128-byte swizzle.
+// 2-D byte tensor [rows][row_bytes] with a box of box_bytes x box_rows (128-byte swizzle for
+// 128-byte boxes, none for narrower ones).
 bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows,
-              uint32_t box_rows) {
+              uint32_t box_rows, uint32_t box_bytes = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {row_bytes, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t box[2] = {box_bytes, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -630,6 +999,13 @@ cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t
 }  // namespace
 
 bool tc_supported() { return encode_fn() != nullptr; }
+
+bool tile_path(int T, int H, int I, int mode) {
+  if (T <= kNarrowT || !tc_supported()) return false;
+  if (mode == 1) return H % 256 == 0 && I % 64 == 0;
+  if (mode == 0) return H % 128 == 0 && I % 128 == 0;
+  return false;
+}
 
 size_t tc_smem_bytes() {
   return (size_t)tc::kStages * tc::kStageBytes + (size_t)tc::kTileM * tc::kStageF * 4 + 1024;
@@ -694,6 +1070,55 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
   pd.last_k4 = ((I % tc::kStageK) ? (I % tc::kStageK) : tc::kStageK) / 64;
   return launch(lc, tc::k_tc_gemm<true>, dim3(grid), dim3(tc::kThreads), smem, m_down, m_down, m_h,
                 pd, ws);
+}
+
+}  // namespace moe
+
+namespace moe {
+
+cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
+                                const uint16_t* x) {
+  const int H = pk.H, I = pk.I, E = pk.E;
+  const uint64_t P = (uint64_t)ws.NT * 128;
+  CUtensorMap m_gate, m_up, m_x, m_down, m_h;
+  if (!make_map(&m_gate, pk.gate_codes, H / 2, (uint64_t)E * I, 128, 32) ||
+      !make_map(&m_up, pk.up_codes, H / 2, (uint64_t)E * I, 128, 32) ||
+      !make_map(&m_x, ws.xh_perm, (uint64_t)H * 2, P, 128) ||
+      !make_map(&m_down, pk.down_codes, I / 2, (uint64_t)E * H, 128, 32) ||
+      !make_map(&m_h, ws.hf_perm, (uint64_t)I * 2, P, 128))
+    return cudaErrorInvalidValue;
+  cudaError_t e = launch(lc, tc::k_xprep16_perm, dim3((ws.T + tc::kXqTok - 1) / tc::kXqTok),
+                         dim3(64 * tc::kXqTok), 0, x, ws);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::k_tc16<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::T16<false>::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::k_tc16<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::T16<true>::kSmem);
+  if (e != cudaSuccess) return e;
+  tc::TcParams pg;
+  pg.sfa = pk.sfa_gu;
+  pg.sfb = nullptr;
+  pg.mult = pk.mult;
+  pg.dscale = pk.down_in_scale;
+  pg.dinv6 = pk.down_inv6S;
+  pg.xS = 1.0f;
+  pg.H = H; pg.I = I; pg.E = E;
+  pg.MT = I / 128;
+  pg.nks = H / 64;
+  pg.last_k4 = 0;
+  const int grid = lc.num_sms;
+  e = launch(lc, tc::k_tc16<false>, dim3(grid), dim3(tc::kT16Threads), tc::T16<false>::kSmem,
+             m_gate, m_up, m_x, pg, ws);
+  if (e != cudaSuccess) return e;
+  e = launch(lc, tc::k_hprep16, dim3(ws.NT), dim3(256), 0, ws);
+  if (e != cudaSuccess) return e;
+  tc::TcParams pd = pg;
+  pd.sfa = pk.sfa_down;
+  pd.MT = H / 128;
+  pd.nks = I / 64;
+  return launch(lc, tc::k_tc16<true>, dim3(grid), dim3(tc::kT16Threads), tc::T16<true>::kSmem,
+                m_down, m_down, m_h, pd, ws);
 }
 
 }  // namespace moe
