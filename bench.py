@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--experts", type=int, default=None,
                    help="experts per layer (smaller packs for profiler captures)")
     p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--mode", default=None, choices=["w4a16", "w4a4"],
+                   help="override the workload's activation mode (profiling)")
     p.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
@@ -121,10 +123,19 @@ class Clocks:
                     reasons=sorted(reasons), samples=len(sm))
 
 
-def source_sha():
+# Sources each profiled kernel is compiled from; a committed DRAM count is quoted only while
+# these files are byte-identical to the ones the capture ran.
+KERNEL_SOURCES = {
+    "k_decode": ("moe_decode.cu", "moe_internal.cuh"),
+    "k_gateup": ("moe_experts.cu", "moe_internal.cuh"),
+}
+
+
+def source_sha(kernel=None):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_mixture_experts_bf16_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(csrc))
+    for n in names:
         h.update(open(os.path.join(csrc, n), "rb").read())
     return h.hexdigest()[:16]
 
@@ -135,7 +146,7 @@ def committed_traffic(kernel, workload):
     if not os.path.exists(path):
         return None
     d = json.load(open(path)).get(f"{kernel}:{workload}")
-    if not d or d.get("source_sha") != source_sha():
+    if not d or d.get("source_sha") != source_sha(kernel):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -382,9 +393,10 @@ def run_native(args, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
     wl = synth.WORKLOADS[args.workload]
-    if args.experts or args.tokens:
+    if args.experts or args.tokens or args.mode:
+        mode = wl.mode if args.mode is None else int(args.mode == "w4a4")
         wl = synth.Workload(wl.name, args.tokens or wl.T, wl.H, args.experts or wl.E, wl.k, wl.I,
-                            wl.mode, wl.layers, wl.zipf)
+                            mode, wl.layers, wl.zipf)
     layers = args.layers or wl.layers
     pk = peaks()
     t_setup = time.time()
