@@ -57,6 +57,8 @@ struct DcGeom {
   int x_stride;                 // 2H + 64: one x operand row
   int h_stride;                 // 2I + 16: one h operand row
   int xop;                      // x operand rows, later the h operand rows of one group
+  int xsep;                     // one token: bytes of its own activation staging row (outside
+                                // the arena, so the first weight copies can start early)
   int smax, gmax;               // slots T*k, groups min(T*k, E)
   int smem;
 };
@@ -86,50 +88,54 @@ __device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t* ctr) {
 }
 
 // Top-k + softmax of one token by one warp, with a 32-entry shared-memory scratch (cand):
-// threshold L = the k-th largest of the 32 lane maxima (a bitonic sort across lanes). The k lane
-// maxima >= L are k distinct logits, so every one of the top k has key >= L. The candidates
-// (keys >= L, about 12 of 512 for k = 10) are written to cand at their prefix position, each
+// threshold L = the k-th largest of the 32 lane maxima (counted with multiplicity). The k lane
+// maxima >= L are k distinct logits, so every one of the top k has key >= L. L is found without
+// a sort: each lane counts the lane maxima above its own (broadcast reads of the 32 maxima from
+// the scratch), and L is the smallest lane maximum with fewer than k above it. The candidates
+// (keys >= L, about 12 of 512 for k = 10) are packed into the scratch by ballots, each
 // candidate's exact rank by (key desc, index asc) is counted against the others, and ranks < k
 // are the selection. More than 32 candidates: the redux.sync rounds of warp_select_softmax.
 template <int V>
 __device__ __forceinline__ void warp_select_scratch(uint32_t (&key)[V], int k, int lane,
                                                     unsigned long long* cand, int& e_out,
                                                     float& w_out) {
-  uint32_t sv = 0u;
+  static_assert((V & (V - 1)) == 0, "V is a power of two");
+  uint32_t m[V];
 #pragma unroll
-  for (int i = 0; i < V; ++i) sv = key[i] > sv ? key[i] : sv;
+  for (int i = 0; i < V; ++i) m[i] = key[i];
 #pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {   // ascending across lanes
+  for (int w = V / 2; w > 0; w >>= 1)
 #pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, sv, stride);
-      const bool asc = (lane & size) == 0, low = (lane & stride) == 0;
-      const uint32_t mn = sv < o ? sv : o, mx = sv < o ? o : sv;
-      sv = (asc == low) ? mn : mx;
-    }
+    for (int i = 0; i < w; ++i) m[i] = m[i] > m[i + w] ? m[i] : m[i + w];
+  const uint32_t sv = m[0];
+  uint32_t* lm = reinterpret_cast<uint32_t*>(cand);
+  lm[lane] = sv;
+  __syncwarp();
+  int above = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 q = reinterpret_cast<const uint4*>(lm)[j];
+    above += (q.x > sv) + (q.y > sv) + (q.z > sv) + (q.w > sv);
   }
-  uint32_t thr = __shfl_sync(0xFFFFFFFFu, sv, 32 - k);
+  uint32_t thr = __reduce_min_sync(0xFFFFFFFFu, above < k ? sv : 0xFFFFFFFFu);
   if (thr == 0u) thr = 1u;   // fewer than k lanes hold logits: every logit is a candidate
-  int cnt = 0;
+  __syncwarp();              // every lane has read the maxima before the scratch is reused
+  const unsigned lt = (1u << lane) - 1u;
+  int C = 0;
 #pragma unroll
-  for (int i = 0; i < V; ++i) cnt += key[i] >= thr;
-  int incl = cnt;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-    if (lane >= off) incl += o;
+  for (int i = 0; i < V; ++i) {
+    const bool is = key[i] >= thr;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, is);
+    const int pos = C + __popc(bal & lt);
+    // candidate word: key in the high half, ~index in the low half, so that a larger word is a
+    // larger logit, and for equal logits the lower index
+    if (is && pos < 32) cand[pos] = ((unsigned long long)key[i] << 32) | (uint32_t)~(lane + 32 * i);
+    C += __popc(bal);
   }
-  const int C = __shfl_sync(0xFFFFFFFFu, incl, 31);
   if (C > 32) {
     warp_select_softmax<V>(key, k, lane, e_out, w_out);
     return;
   }
-  // candidate word: key in the high half, ~index in the low half, so that a larger word is a
-  // larger logit, and for equal logits the lower index
-  int pos = incl - cnt;
-#pragma unroll
-  for (int i = 0; i < V; ++i)
-    if (key[i] >= thr) cand[pos++] = ((unsigned long long)key[i] << 32) | (uint32_t)~(lane + 32 * i);
   __syncwarp();
   e_out = 0;
   float v = 0.0f;
@@ -138,7 +144,11 @@ __device__ __forceinline__ void warp_select_scratch(uint32_t (&key)[V], int k, i
   if (lane < C) {
     mine = cand[lane];
     r = 0;
-    for (int j = 0; j < C; ++j) r += cand[j] > mine;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {   // broadcast reads; entries >= C do not count
+      const ulonglong2 q = reinterpret_cast<const ulonglong2*>(cand)[j];
+      r += (2 * j < C && q.x > mine) + (2 * j + 1 < C && q.y > mine);
+    }
   }
   __syncwarp();
   if (r < k) cand[r] = mine;   // cand[0..k) <- the selection in order
@@ -191,7 +201,7 @@ __device__ __forceinline__ bool topk_tagged_v(const unsigned long long* row, int
           }
         }
       }
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (__any_sync(0xFFFFFFFFu, globaltimer_ns() - t0 > kWaitLimitNs)) {   // warp-uniform
         ok = false;
         break;
       }
@@ -243,6 +253,13 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 
+// max(a, |b|) per BF16 lane of two packed pairs (a holds magnitudes)
+__device__ __forceinline__ uint32_t bmax2_abs(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b & 0x7FFF7FFFu));
+  return d;
+}
+
 __device__ __forceinline__ int group_tok(uint32_t toks, int c) { return (toks >> (4 * c)) & 0xF; }
 
 // Contiguous share of ntasks for this CTA (ntasks * gridDim.x < 2^31 for every valid shape).
@@ -277,6 +294,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   uint64_t* dempty = dfull + geo.dn_stages;
   uint64_t* rbar = dempty + geo.dn_stages;
   uint64_t* xbar = rbar + 1;
+  unsigned char* xsep_row = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(xbar + 1) + 15) & ~uintptr_t(15));
   __shared__ float xfac_s[NT];
   __shared__ int shift_s[NT];
   __shared__ float hfac_s[kGroup];
@@ -291,7 +310,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   const int row0 = (E * b) / G;
   const int nrows = (E * (b + 1)) / G - row0;
   unsigned char* wrs = arena;                                            // [rows][rs bytes]
-  unsigned char* xraw = arena + (size_t)geo.rows_max * geo.rs;           // [T][rs bytes]
+  unsigned char* xraw = geo.xsep ? xsep_row                              // [T][rs bytes]
+                                 : arena + (size_t)geo.rows_max * geo.rs;
 
   if (tid == 0) {
     for (int s = 0; s < geo.gu_stages; ++s) {
@@ -334,14 +354,80 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   // B = the T tokens, FP32 accumulation; the products are exact). The B fragments also give each
   // token's max |x| (for the f16 operand's scaling).
   float* amax_part = red + kDcWarps * 64;   // [8 warps][8 tokens]
-  if (warp < kDcWarps) {
+  if (NT <= 2 && warp < kDcWarps) {
+    // one or two tokens: FP32 dot products on the CUDA cores (an MMA chain would leave 7 of
+    // its 8 columns empty): thread j takes 16-element chunks j, j + 256, ... of every row
+    // (exact BF16 products, FP32 sums), then a butterfly over the warp. Also each token's
+    // max |x| over the thread's chunks.
+    float acc[kDcWarps][NT];
+    float am[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      am[t] = 0.0f;
+#pragma unroll
+      for (int r = 0; r < kDcWarps; ++r) acc[r][t] = 0.0f;
+    }
+    for (int c16 = tid; c16 < H / 16; c16 += kDcCons) {
+      float xv[NT][16];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const uint4 u0 = lds128(xraw + (size_t)t * geo.rs + c16 * 32);
+        const uint4 u1 = lds128(xraw + (size_t)t * geo.rs + c16 * 32 + 16);
+        const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        uint32_t m2 = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          xv[t][2 * i] = bf16_lo(wd[i]);
+          xv[t][2 * i + 1] = bf16_hi(wd[i]);
+          m2 = bmax2_abs(m2, wd[i]);
+        }
+        am[t] = fmaxf(am[t], fmaxf(bf16_lo(m2), bf16_hi(m2)));
+      }
+#pragma unroll
+      for (int r = 0; r < kDcWarps; ++r) {
+        if (r < nrows) {
+          const uint4 u0 = lds128(wrs + (size_t)r * geo.rs + c16 * 32);
+          const uint4 u1 = lds128(wrs + (size_t)r * geo.rs + c16 * 32 + 16);
+          const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float w0 = bf16_lo(wd[i]), w1 = bf16_hi(wd[i]);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              acc[r][t] = fmaf(w0, xv[t][2 * i], acc[r][t]);
+              acc[r][t] = fmaf(w1, xv[t][2 * i + 1], acc[r][t]);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kDcWarps; ++r) {
+      if (r < nrows) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          float v = acc[r][t];
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+          if (lane == 0) red[(warp * 8 + r) * 8 + t] = v;
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float m = am[t];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+      if (lane == 0) amax_part[warp * 8 + t] = m;
+    }
+  } else if (warp < kDcWarps) {
     const int g = lane >> 2, c = lane & 3;
     const bool arow = g < nrows, bcol = g < T;
     const int kw = H / kDcWarps;                       // K range of this warp
     const unsigned char* ap = wrs + (size_t)g * geo.rs + (size_t)(warp * kw + 2 * c) * 2;
     const unsigned char* bp = xraw + (size_t)g * geo.rs + (size_t)(warp * kw + 2 * c) * 2;
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-    float am = 0.0f;
+    uint32_t am2 = 0u;   // running max |x| of the B fragments, two BF16 lanes
 #pragma unroll 2
     for (int ks = 0; ks < kw / 16; ks += 2) {
       uint32_t a[4] = {0u, 0u, 0u, 0u}, bb[4] = {0u, 0u, 0u, 0u};
@@ -360,9 +446,9 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       mma_bf16_16816(d0, a[0], a[1], bb[0], bb[1]);
       mma_bf16_16816(d1, a[2], a[3], bb[2], bb[3]);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        am = fmaxf(am, fmaxf(fabsf(bf16_lo(bb[q])), fabsf(bf16_hi(bb[q]))));
+      for (int q = 0; q < 4; ++q) am2 = bmax2_abs(am2, bb[q]);
     }
+    float am = fmaxf(bf16_lo(am2), bf16_hi(am2));
     am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
     am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
     // D[row g][token 2c, 2c+1]
@@ -390,11 +476,98 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   }
   __syncthreads();
 
-  // ---------------- activation operand of every token, in this CTA's shared memory (while the
-  // other CTAs finish their logits)
+  // ---------------- 2a. top-k + softmax of every token (warp t), from the tagged logits. With
+  // T <= 2 the selection runs while the other warps build the activation operand (below);
+  // with more tokens every warp takes part in the operand first.
+  constexpr bool kEarlyTopk = NT <= 2;
+  const int gu_tiles = I / 16, dn_tiles = H / kDnRows;
+  // this CTA's gate/up tasks [q0, q1) (one token: U = k groups, known before the routing)
+  int q0 = 0, q1 = 0;
+  if (T == 1) balanced_range(k * gu_tiles, q0, q1);
+  // one token: the selecting warp issues the first gate/up stages itself, right after the
+  // selection (the arena holds no staged activations then, and every router row is consumed)
+  const int npre = (T == 1 && geo.xsep) ? min((q1 - q0) * geo.nkc, geo.gu_stages) : 0;
+
+  // copies of gate/up stage `chunk` = (task q, k-chunk kc) of expert e into its ring slot
+  auto issue_gu = [&](int chunk, int q, int kc, int e) {
+    const int it = q % gu_tiles, s = chunk % geo.gu_stages;
+    const uint32_t half = geo.row_bytes;
+    const size_t grow0 = (size_t)e * I + (size_t)it * 16;
+    const uint8_t* gsrc = pk.gate_codes + grow0 * (H / 2);
+    const uint8_t* usrc = pk.up_codes + grow0 * (H / 2);
+    const uint8_t* gsc = pk.gu_scales + (((size_t)0 * pk.E + e) * gu_tiles + it) * (size_t)H;
+    const uint8_t* usc = pk.gu_scales + (((size_t)1 * pk.E + e) * gu_tiles + it) * (size_t)H;
+    unsigned char* st = arena + (size_t)s * geo.gu_stage;
+    mbar_arrive_expect_tx(&gfull[s], 32 * half + 2 * geo.KC);
+    if (geo.nkc == 1) {
+      bulk_g2s(st, gsrc, 16 * half, &gfull[s]);
+      bulk_g2s(st + 16 * half, usrc, 16 * half, &gfull[s]);
+    } else {
+      for (int r = 0; r < 16; ++r) {
+        bulk_g2s(st + r * half, gsrc + (size_t)r * (H / 2) + (size_t)kc * half, half, &gfull[s]);
+        bulk_g2s(st + (16 + r) * half, usrc + (size_t)r * (H / 2) + (size_t)kc * half, half,
+                 &gfull[s]);
+      }
+    }
+    bulk_g2s(st + 32 * half, gsc + (size_t)kc * geo.KC, geo.KC, &gfull[s]);
+    bulk_g2s(st + 32 * half + geo.KC, usc + (size_t)kc * geo.KC, geo.KC, &gfull[s]);
+  };
+
+  auto select_token = [&]() {
+    int e_sel;
+    float w_sel;
+    const unsigned long long* lg = reinterpret_cast<const unsigned long long*>(ws.logits) +
+                                   ((size_t)(b % kLogitReplicas) * T + warp) * E;
+    // scratch: 32 words per warp in the GEMV partials buffer (free once the logits are out)
+    unsigned long long* cand = reinterpret_cast<unsigned long long*>(red) + warp * 32;
+    const bool ok = topk_tagged(lg, E, k, lane, ep, e_sel, w_sel, cand);   // warp-uniform
+    if (!ok && lane == 0) {
+      record_status(ws.ctl, kStTimeout);
+      abort_s = 1;
+    }
+    if (T == 1) {
+      // one token: its k experts are distinct, so every selection is a group of one, and
+      // the slot of selection j is its rank by expert (k shuffles, no block barrier)
+      int p = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int ej = __shfl_sync(0xFFFFFFFFu, e_sel, j);
+        p += (j < k) && (ej < e_sel);
+      }
+      if (lane < k) {
+        sel_idx[lane] = e_sel;
+        sel_w[lane] = w_sel;
+        sel_slot[lane] = p;
+        sorted_e[p] = e_sel;
+        sorted_t[p] = 0;
+        DcGroup gr;
+        gr.expert = e_sel;
+        gr.slot0 = p;
+        gr.n = 1;
+        gr.toks = 0u;
+        grp[p] = gr;
+      }
+      if (__all_sync(0xFFFFFFFFu, ok && !abort_s)) {
+        for (int c = 0; c < npre; ++c) {
+          const int q = q0 + c / geo.nkc;
+          const unsigned src = __ballot_sync(0xFFFFFFFFu, lane < k && p == q / gu_tiles);
+          const int e = __shfl_sync(0xFFFFFFFFu, e_sel, __ffs(src) - 1);
+          if (lane == c) issue_gu(c, q, c % geo.nkc, e);
+        }
+      }
+    } else if (lane < k) {
+      sel_idx[warp * k + lane] = e_sel;
+      sel_w[warp * k + lane] = w_sel;
+    }
+  };
+  if (kEarlyTopk && warp < T) select_token();
+
+  // ---------------- 2b. activation operand of every token, in this CTA's shared memory
   {
     const int nb = H / 16;
-    for (int blk = tid; blk < T * nb; blk += kDcThreads) {
+    const int t0 = kEarlyTopk ? 32 * T : 0;
+    for (int blk = tid - t0; blk < T * nb; blk += kDcThreads - t0) {
+      if (blk < 0) break;
       const int t = blk / nb, bb = blk % nb;
       const uint4* src = reinterpret_cast<const uint4*>(xraw + (size_t)t * geo.rs + bb * 32);
       const uint4 u0 = src[0], u1 = src[1];
@@ -431,27 +604,16 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     }
   }
   __syncthreads();
+  if (!kEarlyTopk && warp < T) select_token();
 
-  // ---------------- 2. routing, in every CTA
-  // top-k + softmax of every token (warp t), then a stable sort of the S = T*k selections by
-  // expert: entry s = t*k + j goes to slot #{s' : e_s' < e_s} + #{s' < s : e_s' == e_s}
-  if (warp < T) {
-    int e_sel;
-    float w_sel;
-    const unsigned long long* lg = reinterpret_cast<const unsigned long long*>(ws.logits) +
-                                   ((size_t)(b % kLogitReplicas) * T + warp) * E;
-    // scratch: 32 words per warp in the GEMV partials buffer (free once the logits are out)
-    unsigned long long* cand = reinterpret_cast<unsigned long long*>(red) + warp * 32;
-    if (!topk_tagged(lg, E, k, lane, ep, e_sel, w_sel, cand) && lane == 0) {
-      record_status(ws.ctl, kStTimeout);
-      abort_s = 1;
-    }
-    if (lane < k) {
-      sel_idx[warp * k + lane] = e_sel;
-      sel_w[warp * k + lane] = w_sel;
-    }
-  }
-  __syncthreads();
+  // ---------------- 2c. groups, in every CTA: a stable sort of the S = T*k selections by
+  // expert (entry s = t*k + j goes to slot #{s' : e_s' < e_s} + #{s' < s : e_s' == e_s}) and one
+  // group per distinct expert, numbered in slot order. One token: done in the selecting warp.
+  int U = 0;
+  if (T == 1) {
+    U = k;
+  } else {
+  if (!kEarlyTopk) __syncthreads();
   if (tid < S) {
     const int e = sel_idx[tid];
     int p = 0;
@@ -469,7 +631,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   const unsigned gbal = __ballot_sync(0xFFFFFFFFu, gstart);
   if (lane == 0) wcount_s[warp] = __popc(gbal);
   __syncthreads();
-  int U = 0, ubase = 0;
+  int ubase = 0;
 #pragma unroll
   for (int w = 0; w <= kDcWarps; ++w) {
     if (w < warp) ubase += wcount_s[w];
@@ -488,48 +650,29 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     gr.toks = toks;
     grp[ubase + __popc(gbal & ((1u << lane) - 1u))] = gr;
   }
-  __syncthreads();   // groups and selections are final from here on
+  __syncthreads();
+  }
+  // groups and selections are final from here on (one token: since the operand barrier)
 
-  const int gu_tiles = I / 16, dn_tiles = H / kDnRows;
-  int q0, q1, d0, d1;
+  int d0, d1;
   balanced_range(U * gu_tiles, q0, q1);
   balanced_range(U * dn_tiles, d0, d1);
 
   if (warp == kDcWarps) {
     // ---------------- producer: gate/up tasks, then this CTA's down tasks
     if (lane != 0) return;
-    const uint32_t half = geo.row_bytes;
     int chunk = 0;
     for (int q = q0; q < q1 && !abort_s; ++q) {
-      const int gi = q / gu_tiles, it = q % gu_tiles;
-      const int e = grp[gi].expert;
-      const size_t grow0 = (size_t)e * I + (size_t)it * 16;
-      const uint8_t* gsrc = pk.gate_codes + grow0 * (H / 2);
-      const uint8_t* usrc = pk.up_codes + grow0 * (H / 2);
-      const uint8_t* gsc = pk.gu_scales + (((size_t)0 * pk.E + e) * gu_tiles + it) * (size_t)H;
-      const uint8_t* usc = pk.gu_scales + (((size_t)1 * pk.E + e) * gu_tiles + it) * (size_t)H;
+      const int e = grp[q / gu_tiles].expert;
       for (int kc = 0; kc < geo.nkc; ++kc, ++chunk) {
+        if (chunk < npre) continue;   // issued by the selecting warp
         const int s = chunk % geo.gu_stages, n = chunk / geo.gu_stages;
         if (n > 0 && !mbar_wait(&gempty[s], (n - 1) & 1)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
           break;
         }
-        unsigned char* st = arena + (size_t)s * geo.gu_stage;
-        mbar_arrive_expect_tx(&gfull[s], 32 * half + 2 * geo.KC);
-        if (geo.nkc == 1) {
-          bulk_g2s(st, gsrc, 16 * half, &gfull[s]);
-          bulk_g2s(st + 16 * half, usrc, 16 * half, &gfull[s]);
-        } else {
-          for (int r = 0; r < 16; ++r) {
-            bulk_g2s(st + r * half, gsrc + (size_t)r * (H / 2) + (size_t)kc * half, half,
-                     &gfull[s]);
-            bulk_g2s(st + (16 + r) * half, usrc + (size_t)r * (H / 2) + (size_t)kc * half, half,
-                     &gfull[s]);
-          }
-        }
-        bulk_g2s(st + 32 * half, gsc + (size_t)kc * geo.KC, geo.KC, &gfull[s]);
-        bulk_g2s(st + 32 * half + geo.KC, usc + (size_t)kc * geo.KC, geo.KC, &gfull[s]);
+        issue_gu(chunk, q, kc, e);
       }
     }
     // the arena becomes the down ring once the consumers have released every gate/up stage
@@ -586,7 +729,9 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       const bool gvalid = g < n;
       const int xrow = gvalid ? group_tok(gm.toks, g) : 0;
       const unsigned char* xr = xop + (size_t)xrow * geo.x_stride + c * 16;
+      // two accumulator sets (alternate k-blocks of a warp): two independent MMA chains each
       float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+      float accg2[4] = {0.f, 0.f, 0.f, 0.f}, accu2[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kc = 0; kc < geo.nkc; ++kc, ++chunk) {
         const int s = chunk % geo.gu_stages, nn = chunk / geo.gu_stages;
         if (!abort_s && !mbar_wait(&gfull[s], nn & 1)) {
@@ -595,7 +740,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         }
         const unsigned char* st = arena + (size_t)s * geo.gu_stage;
         const unsigned char* scb = st + 32 * geo.row_bytes + c * 32 + g * 4;
-        for (int jb = warp; jb < jb_per_chunk; jb += kDcWarps) {
+        auto kblock = [&](int jb, float (&ag)[4], float (&au)[4]) {
           const int off = jb * 64 + c * 16;
           const uint4 gr = lds128(st + g * geo.row_bytes + off);
           const uint4 gr8 = lds128(st + (g + 8) * geo.row_bytes + off);
@@ -612,11 +757,20 @@ __global__ void __launch_bounds__(kDcThreads, 1)
 #pragma unroll
             for (int p = 0; p < 4; ++p) xb[p] = make_uint4(0, 0, 0, 0);
           }
-          kblock128_mma(accg, gr, gr8, scg, xb);
-          kblock128_mma(accu, ur, ur8, scu, xb);
+          kblock128_mma(ag, gr, gr8, scg, xb);
+          kblock128_mma(au, ur, ur8, scu, xb);
+        };
+        for (int jb = warp; jb < jb_per_chunk; jb += 2 * kDcWarps) {
+          kblock(jb, accg, accu);
+          if (jb + kDcWarps < jb_per_chunk) kblock(jb + kDcWarps, accg2, accu2);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&gempty[s]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        accg[i] += accg2[i];
+        accu[i] += accu2[i];
       }
       // partial sums of the 8 warps -> shared memory; 128 threads each finish one h element
       float* myred = red + (size_t)(warp * 2) * 128;
@@ -770,9 +924,9 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       const unsigned char* rg8 = rg + 8 * (I / 2);
       const unsigned char* scb = st + code_bytes + (size_t)(warp >> 2) * (4 * I) +
                                  (size_t)(warp & 3) * nkb * 64 + c * 16 + g * 2;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 3
-      for (int j = 0; j < nkb; ++j) {
+      // two accumulators (even / odd k-blocks): two independent MMA chains
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+      auto dblock = [&](int j, float (&a)[4]) {
         const uint2 a0 = lds64(rg + j * 32);
         const uint2 a1 = lds64(rg8 + j * 32);
         const uint32_t sc = lds16(scb + j * 64);
@@ -781,8 +935,14 @@ __global__ void __launch_bounds__(kDcThreads, 1)
           xb0 = lds128(hr + j * 128);
           xb1 = lds128(hr + j * 128 + 16);
         }
-        kblock_mma(acc, a0, a1, sc, xb0, xb1);
+        kblock_mma(a, a0, a1, sc, xb0, xb1);
+      };
+      for (int j = 0; j < nkb; j += 2) {
+        dblock(j, acc);
+        if (j + 1 < nkb) dblock(j + 1, acc2);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] += acc2[i];
       __syncwarp();
       if (lane == 0) mbar_arrive(&dempty[s]);
       // Y = BF16(acc * md * factor): plain (slot-major rows) and tagged pairs of rows (r, r+1),
@@ -936,10 +1096,11 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   g.xop = T * g.x_stride > kGroup * g.h_stride ? T * g.x_stride : kGroup * g.h_stride;
   g.smax = T * k;
   g.gmax = g.smax < E ? g.smax : E;
-  const int route_bytes = (g.rows_max + T) * g.rs;
+  g.xsep = T == 1 ? g.rs : 0;
+  const int route_bytes = (g.rows_max + (g.xsep ? 0 : T)) * g.rs;
   const int scratch = T * k * 64 * 4;  // Y pairs of one tile for the combine
   const int fixed = g.xop + kDcWarps * 2 * 128 * 4 + g.gmax * (int)sizeof(DcGroup) +
-                    g.smax * 20 + 8 + 8 * (2 * 3 + 2 * 16 + 2) + kDcStatic;
+                    g.smax * 20 + 8 + 8 * (2 * 3 + 2 * 16 + 2) + 16 + g.xsep + kDcStatic;
   const int avail = kDcSmemMax - fixed;
   g.gu_stages = avail / g.gu_stage;
   if (g.gu_stages > 3) g.gu_stages = 3;

@@ -212,6 +212,19 @@ __device__ __forceinline__ uint32_t e4m3_bcast_f16x2(uint32_t byte) {
   return e4m3x2_to_f16x2(byte * 0x0101u);
 }
 
+// a * (low half of s), a * (high half of s): the half broadcast is an operand selector of the
+// f16x2 multiply, so two rows' scales share one conversion
+__device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t s) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                            __low2half2(*reinterpret_cast<const __half2*>(&s)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2_hi(uint32_t a, uint32_t s) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                            __high2half2(*reinterpret_cast<const __half2*>(&s)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
@@ -296,8 +309,7 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 // k = 64j + 16c + 4m + {0,1,2,3}), so both operands come from contiguous bytes.
 __device__ __forceinline__ void kblock_mma(float (&acc)[4], uint2 rowg, uint2 rowg8, uint32_t sc,
                                            const uint4& xb0, const uint4& xb1) {
-  const uint32_t s0 = e4m3_bcast_f16x2(sc & 0xFFu);
-  const uint32_t s1 = e4m3_bcast_f16x2((sc >> 8) & 0xFFu);
+  const uint32_t s01 = e4m3x2_to_f16x2(sc);   // {row g, row g+8}
   uint32_t ga[4], gb[4], ha[4], hb[4];
   e2m1x8_to_f16x2x4(rowg.x, ga);   // row g, k 0..7
   e2m1x8_to_f16x2x4(rowg.y, gb);   // row g, k 8..15
@@ -310,10 +322,10 @@ __device__ __forceinline__ void kblock_mma(float (&acc)[4], uint2 rowg, uint2 ro
     const uint32_t* h4 = (m < 2) ? ha : hb;
     const int o = (m & 1) * 2;
     uint32_t a[4];
-    a[0] = hmul2_u32(g4[o], s0);
-    a[1] = hmul2_u32(h4[o], s1);
-    a[2] = hmul2_u32(g4[o + 1], s0);
-    a[3] = hmul2_u32(h4[o + 1], s1);
+    a[0] = hmul2_lo(g4[o], s01);
+    a[1] = hmul2_hi(h4[o], s01);
+    a[2] = hmul2_lo(g4[o + 1], s01);
+    a[3] = hmul2_hi(h4[o + 1], s01);
     mma_16816(acc, a, xs[2 * m], xs[2 * m + 1]);
   }
 }
@@ -326,10 +338,9 @@ __device__ __forceinline__ void kblock_mma(float (&acc)[4], uint2 rowg, uint2 ro
 // consistently for A and B so that each operand comes from contiguous bytes.
 __device__ __forceinline__ void kblock128_mma(float (&acc)[4], const uint4& rowg, const uint4& rowg8,
                                               uint32_t sc4, const uint4 (&xb)[4]) {
-  const uint32_t s_g0 = e4m3_bcast_f16x2(sc4 & 0xFFu);
-  const uint32_t s_g1 = e4m3_bcast_f16x2((sc4 >> 8) & 0xFFu);
-  const uint32_t s_h0 = e4m3_bcast_f16x2((sc4 >> 16) & 0xFFu);
-  const uint32_t s_h1 = e4m3_bcast_f16x2(sc4 >> 24);
+  // {row g, row g+8} scales of block 2c and of block 2c+1
+  const uint32_t s_0 = e4m3x2_to_f16x2(__byte_perm(sc4, 0u, 0x0020u));
+  const uint32_t s_1 = e4m3x2_to_f16x2(__byte_perm(sc4, 0u, 0x0031u));
   const uint32_t gw[4] = {rowg.x, rowg.y, rowg.z, rowg.w};
   const uint32_t hw[4] = {rowg8.x, rowg8.y, rowg8.z, rowg8.w};
 #pragma unroll
@@ -337,17 +348,16 @@ __device__ __forceinline__ void kblock128_mma(float (&acc)[4], const uint4& rowg
     uint32_t gf[4], hf[4];
     e2m1x8_to_f16x2x4(gw[w], gf);
     e2m1x8_to_f16x2x4(hw[w], hf);
-    const uint32_t sg = (w < 2) ? s_g0 : s_g1;
-    const uint32_t sh = (w < 2) ? s_h0 : s_h1;
+    const uint32_t sp = (w < 2) ? s_0 : s_1;
     const uint4& xv = xb[w];
     {
-      uint32_t a[4] = {hmul2_u32(gf[0], sg), hmul2_u32(hf[0], sh), hmul2_u32(gf[1], sg),
-                       hmul2_u32(hf[1], sh)};
+      uint32_t a[4] = {hmul2_lo(gf[0], sp), hmul2_hi(hf[0], sp), hmul2_lo(gf[1], sp),
+                       hmul2_hi(hf[1], sp)};
       mma_16816(acc, a, xv.x, xv.y);
     }
     {
-      uint32_t a[4] = {hmul2_u32(gf[2], sg), hmul2_u32(hf[2], sh), hmul2_u32(gf[3], sg),
-                       hmul2_u32(hf[3], sh)};
+      uint32_t a[4] = {hmul2_lo(gf[2], sp), hmul2_hi(hf[2], sp), hmul2_lo(gf[3], sp),
+                       hmul2_hi(hf[3], sp)};
       mma_16816(acc, a, xv.z, xv.w);
     }
   }

@@ -764,13 +764,20 @@ __global__ void __launch_bounds__(kT16Threads, 1)
           const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(atom + (rr & 31) * 16 + (rr >> 5) * 4);
           const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
           unsigned char* row = st + mat * 16384 + (ct >> 3) * 1024 + (ct & 7) * 128;
+          const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {   // chunk c: elements 8c .. 8c+7 = code word c
-            const uint32_t sh = e4m3_bcast_f16x2((sc4 >> (8 * (c >> 1))) & 0xFFu);
+            const uint32_t sp = (c < 4) ? s01 : s23;
             uint32_t f[4];
             e2m1x8_to_f16x2x4(w[c], f);
-            const uint4 o = make_uint4(hmul2_u32(f[0], sh), hmul2_u32(f[1], sh),
-                                       hmul2_u32(f[2], sh), hmul2_u32(f[3], sh));
+            uint4 o;
+            if (c & 2) {   // blocks 1 and 3 of the stage: the high half of the pair
+              o = make_uint4(hmul2_hi(f[0], sp), hmul2_hi(f[1], sp), hmul2_hi(f[2], sp),
+                             hmul2_hi(f[3], sp));
+            } else {
+              o = make_uint4(hmul2_lo(f[0], sp), hmul2_lo(f[1], sp), hmul2_lo(f[2], sp),
+                             hmul2_lo(f[3], sp));
+            }
             *reinterpret_cast<uint4*>(row + ((c ^ (ct & 7)) << 4)) = o;
           }
         }
