@@ -356,7 +356,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   float* amax_part = red + kDcWarps * 64;   // [8 warps][8 tokens]
   if (NT <= 2 && warp < kDcWarps) {
     // one or two tokens: FP32 dot products on the CUDA cores (an MMA chain would leave 7 of
-    // its 8 columns empty): thread j takes 16-element chunks j, j + 256, ... of every row
+    // its 8 columns empty): lane l of warp w takes the 8-element chunks 32 (2w + h) + l,
+    // h = 0, 1 (and every 512 chunks further), so that a warp's loads are 512 contiguous bytes
     // (exact BF16 products, FP32 sums), then a butterfly over the warp. Also each token's
     // max |x| over the thread's chunks.
     float acc[kDcWarps][NT];
@@ -367,12 +368,14 @@ __global__ void __launch_bounds__(kDcThreads, 1)
 #pragma unroll
       for (int r = 0; r < kDcWarps; ++r) acc[r][t] = 0.0f;
     }
-    for (int c16 = tid; c16 < H / 16; c16 += kDcCons) {
+    for (int c8 = warp * 64 + lane; c8 < H / 8; c8 += kDcCons * 2) {
+      const int o0 = c8 * 16, o1 = (c8 + 32) * 16;   // byte offsets of the two chunks
+      const bool h1 = c8 + 32 < H / 8;                  // H % 512 != 0: a last half chunk
       float xv[NT][16];
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        const uint4 u0 = lds128(xraw + (size_t)t * geo.rs + c16 * 32);
-        const uint4 u1 = lds128(xraw + (size_t)t * geo.rs + c16 * 32 + 16);
+        const uint4 u0 = lds128(xraw + (size_t)t * geo.rs + o0);
+        const uint4 u1 = h1 ? lds128(xraw + (size_t)t * geo.rs + o1) : make_uint4(0, 0, 0, 0);
         const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
         uint32_t m2 = 0u;
 #pragma unroll
@@ -386,8 +389,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
 #pragma unroll
       for (int r = 0; r < kDcWarps; ++r) {
         if (r < nrows) {
-          const uint4 u0 = lds128(wrs + (size_t)r * geo.rs + c16 * 32);
-          const uint4 u1 = lds128(wrs + (size_t)r * geo.rs + c16 * 32 + 16);
+          const uint4 u0 = lds128(wrs + (size_t)r * geo.rs + o0);
+          const uint4 u1 = h1 ? lds128(wrs + (size_t)r * geo.rs + o1) : make_uint4(0, 0, 0, 0);
           const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
