@@ -880,6 +880,261 @@ __global__ void __launch_bounds__(kT16Threads, 1)
                  : "memory");
 }
 
+// W4A16 down GEMM with the operands' roles swapped: A = the h tile of one 128-slot token tile
+// (f16, all I columns, resident in shared memory while the CTA runs every 256-row weight tile of
+// that token tile), B = 256 dequantised down-weight rows x 64 K per stage, D = [slot][row]
+// (M = 128, N = 256) in tensor memory. The h tile is staged once per token tile instead of once
+// per weight tile, and each epilogue thread owns one slot, so Y rows are written directly.
+constexpr int kDnN = 256;
+constexpr uint32_t kIdescDn = (1u << 4) | ((uint32_t)(kDnN >> 3) << 17) |
+                              ((uint32_t)(kTileM >> 4) << 24);   // f16 x f16 -> f32, 128x256
+constexpr int kDnConv = kDnN * 128;                 // 256 rows x 128 B (64 f16), SW128
+constexpr int kDnRaw = kDnN * 32;                   // 256 rows x 64 FP4 codes
+constexpr int kDnSf = 2 * 512;                      // two 128-row scale-factor atoms
+constexpr int kDnStage = kDnConv + kDnRaw + kDnSf;  // 41 KB, a multiple of 1 KB
+constexpr int kDnMaxStages = 3;
+
+__device__ __forceinline__ void mma_f16_dn(uint32_t d, uint64_t a, uint64_t b,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(kIdescDn), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kT16Threads, 1)
+    k_tc16_dn(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_h,
+              TcParams prm, WsView ws, int nst) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t full[kDnMaxStages], conv_full[kDnMaxStages], empty[kDnMaxStages];
+  __shared__ uint64_t acc_full[2], acc_empty[2], a_full, a_empty;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_s;
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* smem = smem_raw + pad;
+  const int H = prm.H, I = prm.I;
+  const int nks = I / 64;
+  unsigned char* atile = smem;                                   // [nks][128 rows x 128 B]
+  unsigned char* stages = smem + (size_t)nks * 16384;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&conv_full[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(&a_full, 1);
+    mbar_init(&a_empty, 1);
+    fence_mbar_init();
+    abort_s = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base_s)),
+                 "r"(2 * kDnN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_s;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // units (token tile j, 256-row weight tile nt), a contiguous share per CTA so that consecutive
+  // units reuse the staged h tile
+  const int nts = H / kDnN;
+  const int nunits = (int)ws.ctl[kCtlTokenTiles] * nts;
+  const int u0 = (int)(((long long)nunits * blockIdx.x) / gridDim.x);
+  const int u1 = (int)(((long long)nunits * (blockIdx.x + 1)) / gridDim.x);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int it = 0, jprev = -1, jcount = 0;
+      for (int u = u0; u < u1 && !abort_s; ++u) {
+        const int j = u / nts, nt = u % nts;
+        const int e = __ldg(&ws.tt_expert[j]);
+        if (j != jprev) {
+          if (jcount > 0 && !mbar_wait(&a_empty, (jcount - 1) & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&a_full, (uint32_t)nks * 16384u);
+          for (int ks = 0; ks < nks; ++ks) tma_2d(atile + ks * 16384, &tm_h, ks * 128, j * 128, &a_full);
+          jprev = j;
+          ++jcount;
+        }
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % nst, n = it / nst;
+          if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+            break;
+          }
+          unsigned char* raw = stages + (size_t)s * kDnStage + kDnConv;
+          unsigned char* sf = raw + kDnRaw;
+          mbar_arrive_expect_tx(&full[s], kDnRaw + kDnSf);
+          tma_2d(raw, &tm_raw, ks * 32, e * H + nt * kDnN, &full[s]);
+          tma_2d(raw + 4096, &tm_raw, ks * 32, e * H + nt * kDnN + 128, &full[s]);
+          for (int h2 = 0; h2 < 2; ++h2)
+            bulk_g2s(sf + h2 * 512,
+                     prm.sfa + (((size_t)e * (H / 128) + 2 * nt + h2) * (I / 64) + ks) * 512, 512,
+                     &full[s]);
+        }
+      }
+      const int used = it < nst ? it : nst;
+      for (int i = 0; i < used; ++i) {
+        const int c = it - 1 - i;
+        (void)mbar_wait(&full[c % nst], (c / nst) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int it = 0, tcount = 0, jprev = -1, jcount = 0;
+      for (int u = u0; u < u1; ++u, ++tcount) {
+        const int j = u / nts;
+        if (j != jprev) {
+          if (!abort_s && !mbar_wait(&a_full, jcount & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          jprev = j;
+          ++jcount;
+        }
+        const int buf = tcount & 1, use = tcount >> 1;
+        if (use > 0 && !abort_s && !mbar_wait(&acc_empty[buf], (use - 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        fence_after();
+        const uint32_t d0 = tmem + buf * kDnN;
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const int s = it % nst, n = it / nst;
+          if (!abort_s && !mbar_wait(&conv_full[s], n & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          fence_after();
+          const uint32_t a0 = smem_u32(atile + ks * 16384);
+          const uint32_t b0 = smem_u32(stages + (size_t)s * kDnStage);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            mma_f16_dn(d0, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32),
+                       (ks > 0 || q > 0) ? 1u : 0u);
+          commit(&empty[s]);
+        }
+        commit(&acc_full[buf]);
+        // the h tile may be replaced once this token tile's last MMA has read it
+        if (u + 1 == u1 || (u + 1) / nts != j) commit(&a_empty);
+      }
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- converters (warps 2..5)
+    // thread ct owns B rows ct and ct + 128 of every stage
+    const int ct = tid - 64;
+    int it = 0;
+    for (int u = u0; u < u1; ++u) {
+      for (int ks = 0; ks < nks; ++ks, ++it) {
+        const int s = it % nst, n = it / nst;
+        if (!abort_s && !mbar_wait(&full[s], n & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        unsigned char* st = stages + (size_t)s * kDnStage;
+        const unsigned char* raw = st + kDnConv;
+        const unsigned char* sf = raw + kDnRaw;
+#pragma unroll
+        for (int mat = 0; mat < 2; ++mat) {
+          const uint4* src = reinterpret_cast<const uint4*>(raw + mat * 4096 + ct * 32);
+          const uint4 c0 = src[0], c1 = src[1];
+          // the row's 4 scale bytes (blocks of 16 along this stage's 64 K)
+          const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(sf + mat * 512 + (ct & 31) * 16 +
+                                                                  (ct >> 5) * 4);
+          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          unsigned char* row = st + mat * 16384 + (ct >> 3) * 1024 + (ct & 7) * 128;
+          const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {   // chunk c: elements 8c .. 8c+7 = code word c
+            const uint32_t sp = (c < 4) ? s01 : s23;
+            uint32_t f[4];
+            e2m1x8_to_f16x2x4(w[c], f);
+            uint4 o;
+            if (c & 2) {
+              o = make_uint4(hmul2_hi(f[0], sp), hmul2_hi(f[1], sp), hmul2_hi(f[2], sp),
+                             hmul2_hi(f[3], sp));
+            } else {
+              o = make_uint4(hmul2_lo(f[0], sp), hmul2_lo(f[1], sp), hmul2_lo(f[2], sp),
+                             hmul2_lo(f[3], sp));
+            }
+            *reinterpret_cast<uint4*>(row + ((c ^ (ct & 7)) << 4)) = o;
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv_full[s]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 6..9)
+    const int quad = warp & 3;              // tensor-memory lanes 32*quad .. +31
+    const int row = quad * 32 + lane;       // slot of the token tile
+    int tcount = 0;
+    for (int u = u0; u < u1; ++u, ++tcount) {
+      const int j = u / nts, nt = u % nts;
+      const int buf = tcount & 1, use = tcount >> 1;
+      const int e = ws.tt_expert[j];
+      const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
+      // Y = BF16(acc * md * 2^s of the slot)
+      float f = 0.0f;
+      if (row < nval)
+        f = prm.mult[e * 3 + 2] *
+            __int_as_float((127 + amax_shift(__uint_as_float(ws.slot_amax[slot0 + row]))) << 23);
+      if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
+        record_status(ws.ctl, kStTimeout);
+        abort_s = 1;
+      }
+      __syncwarp();
+      fence_after();
+      const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * kDnN;
+      uint4* yrow = reinterpret_cast<uint4*>(ws.y + (size_t)(slot0 + row) * H + nt * kDnN);
+      for (int c0 = 0; c0 < kDnN; c0 += 32) {
+        uint32_t r[32];
+        ld32(tb + c0, r);
+        uint32_t o[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          o[q] = (uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * q]) * f) |
+                 ((uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * q + 1]) * f) << 16);
+        if (row < nval) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            yrow[c0 / 8 + q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(2 * kDnN)
+                 : "memory");
+}
+
 // W4A16 activations by padded slot: 64 threads per token find the token's max |x|, then write
 // f16(x * 2^-s) into each of its k slots' rows and 2^s to xfac (exact; see above).
 __global__ void __launch_bounds__(64 * kXqTok) k_xprep16_perm(const uint16_t* __restrict__ x,
@@ -1124,6 +1379,17 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
   pd.sfa = pk.sfa_down;
   pd.MT = H / 128;
   pd.nks = I / 64;
+  // the down GEMM with the h tile resident when it and two weight stages fit in shared memory
+  const int abytes = (I / 64) * 16384;
+  int nst = (232448 - 2048 - abytes) / tc::kDnStage;
+  if (nst > tc::kDnMaxStages) nst = tc::kDnMaxStages;
+  if (H % tc::kDnN == 0 && nst >= 2) {
+    const int smem = abytes + nst * tc::kDnStage + 1024;
+    e = cudaFuncSetAttribute(tc::k_tc16_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch(lc, tc::k_tc16_dn, dim3(grid), dim3(tc::kT16Threads), (size_t)smem, m_down, m_h,
+                  pd, ws, nst);
+  }
   return launch(lc, tc::k_tc16<true>, dim3(grid), dim3(tc::kT16Threads), tc::T16<true>::kSmem,
                 m_down, m_down, m_h, pd, ws);
 }
