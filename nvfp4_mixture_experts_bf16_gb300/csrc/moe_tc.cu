@@ -637,25 +637,81 @@ __device__ __forceinline__ void t16_convert_row(const unsigned char* src, uint32
 
 // Gate/up + SiLU*up. Tile = (token tile j, 128 intermediate rows mt): two M = 128 accumulators
 // (the gate rows and the up rows of the same intermediate indices, so one epilogue lane holds
-// both g and u), N = 128 padded slots. TMA stage: the x tile (16 KB, SW128), the gate and up
-// codes (2 x 4 KB) and two scale-factor atoms (64-row intermediate tiles: gate rows 0..63, up
-// rows 64..127 of each atom).
+// both g and u), N = 128 padded slots. The dequantised weights are the MMAs' A operand in tensor
+// memory: a converter thread writes its row's 64 f16 of a stage into its own tensor-memory lane
+// (one tcgen05.st), so shared memory carries only what the TMA brings (the x tile, the codes,
+// the scales) and the x tile's MMA reads. Tensor memory: the gate and up accumulators (256
+// columns, one buffer: the next tile's first MMA waits for the epilogue to have read them) and a
+// three-stage ring of A (32 columns of gate and 32 of up per stage). TMA stage: the x tile (16 KB,
+// SW128), the gate and up codes (2 x 4 KB) and two scale-factor atoms (64-row intermediate tiles:
+// gate rows 0..63, up rows 64..127 of each atom).
 constexpr int kGuStage = 16384 + 8192 + 1024 + 1024;   // 26 KB (1 KB multiple: SW128 x tile)
+constexpr int kGuAStages = 3;
+constexpr int kGuEpiWarps = 8;          // two per tensor-memory lane quadrant (64 columns each)
+constexpr int kGuThreads = (2 + kT16ConvWarps + kGuEpiWarps) * 32;
 
-__global__ void __launch_bounds__(kT16Threads, 1)
+__device__ __forceinline__ void gu_epi_sync() {  // the epilogue warps
+  asm volatile("bar.sync 3, %0;" ::"r"(kGuEpiWarps * 32) : "memory");
+}
+constexpr uint32_t kGuACol = 2 * kTileN;                // first tensor-memory column of the A ring
+
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(kIdescF16), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// One weight row of a stage (64 E2M1 codes at src, the E4M3 scales of its four 16-element blocks
+// in sc4, block b in byte b) -> 32 f16x2 words in K order (word c holds elements 2c, 2c+1).
+__device__ __forceinline__ void t16_dequant_row(const unsigned char* src, uint32_t sc4,
+                                                uint32_t (&o)[32]) {
+  // consecutive rows' 32-byte code rows are read half by half, lanes 4..7 (mod 8) taking the
+  // second half first, so that each load of the warp touches every bank once per 128 bytes
+  const int h = (threadIdx.x >> 2) & 1;
+  const uint4 ca = reinterpret_cast<const uint4*>(src)[h];
+  const uint4 cb = reinterpret_cast<const uint4*>(src)[h ^ 1];
+  const uint4 c0 = h ? cb : ca, c1 = h ? ca : cb;
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {   // code word c: elements 8c .. 8c+7, block c / 2
+    const uint32_t sp = (c < 4) ? s01 : s23;
+    uint32_t f[4];
+    e2m1x8_to_f16x2x4(w[c], f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[4 * c + i] = (c & 2) ? hmul2_hi(f[i], sp) : hmul2_lo(f[i], sp);
+  }
+}
+
+__global__ void __launch_bounds__(kGuThreads, 1)
     k_tc16_gu(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
               const __grid_constant__ CUtensorMap tm_x, TcParams prm, WsView ws, int nring) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ uint64_t full[kT16MaxRing], empty[kT16MaxRing];
-  __shared__ uint64_t conv_full[2], conv_empty[2], acc_full[2], acc_empty[2];
+  __shared__ uint64_t conv_full[kGuAStages], conv_empty[kGuAStages], acc_full, acc_empty;
   __shared__ float colfac[kTileN];
   __shared__ uint32_t colmax[kTileN];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  unsigned char* smem = smem_raw + pad;
-  unsigned char* conv = smem;                              // [2][gate 16 KB | up 16 KB]
-  unsigned char* ring = smem + 2 * kT16Conv;               // [nring][x | codes | sf]
+  unsigned char* ring = smem_raw + pad;                    // [nring][x | codes | sf]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -663,12 +719,12 @@ __global__ void __launch_bounds__(kT16Threads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kT16ConvWarps + 1);   // the converter warps (codes), the MMA (x tile)
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kGuAStages; ++b) {
       mbar_init(&conv_full[b], kT16ConvWarps);
       mbar_init(&conv_empty[b], 1);
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
     }
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, kGuEpiWarps);
     fence_mbar_init();
     abort_s = 0;
   }
@@ -726,91 +782,102 @@ __global__ void __launch_bounds__(kT16Threads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int it = 0, tcount = 0;
+      int it = 0, tcount = 0, ca = 0, na = 0;   // ca / na: A ring slot and its use count
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
-        const int buf = tcount & 1, use = tcount >> 1;
-        if (use > 0 && !abort_s && !mbar_wait(&acc_empty[buf], (use - 1) & 1)) {
+        if (tcount > 0 && !abort_s && !mbar_wait(&acc_empty, (tcount - 1) & 1)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
         }
         fence_after();
-        const uint32_t d0 = tmem + buf * (2 * kTileN);
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % nring, cb = it & 1;
+          const int s = it % nring;
           if (!abort_s && (!mbar_wait(&full[s], (it / nring) & 1) ||
-                           !mbar_wait(&conv_full[cb], (it >> 1) & 1))) {
+                           !mbar_wait(&conv_full[ca], na & 1))) {
             record_status(ws.ctl, kStTimeout);
             abort_s = 1;
           }
           fence_after();
-          const uint32_t a0 = smem_u32(conv + cb * kT16Conv);
+          const uint32_t ag = tmem + kGuACol + ca * 64, au = ag + 32;
           const uint32_t b0 = smem_u32(ring + (size_t)s * kGuStage);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t acc = (ks > 0 || q > 0) ? 1u : 0u;
-            mma_f16(d0, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32), acc);
-            mma_f16(d0 + kTileN, desc_sw128(a0 + 16384 + q * 32), desc_sw128(b0 + q * 32), acc);
+            mma_f16_ts(tmem, ag + q * 8, desc_sw128(b0 + q * 32), acc);
+            mma_f16_ts(tmem + kTileN, au + q * 8, desc_sw128(b0 + q * 32), acc);
           }
           commit(&empty[s]);
-          commit(&conv_empty[cb]);
+          commit(&conv_empty[ca]);
+          if (++ca == kGuAStages) {
+            ca = 0;
+            ++na;
+          }
         }
-        commit(&acc_full[buf]);
+        commit(&acc_full);
       }
     }
   } else if (warp < 2 + kT16ConvWarps) {
     // ---------------------------------------------------------------- converters
-    // thread ct owns row ct & 127 of the gate (ct < 128) or up (ct >= 128) tile of every stage
-    const int ct = tid - 64, mat = ct >> 7, r = ct & 127;
+    // warps 2..5: gate rows, warps 6..9: up rows; a thread converts the row of its own
+    // tensor-memory lane (32 x (warp % 4) + lane) of every stage
+    const int mat = (warp - 2) >> 2, r = 32 * (warp & 3) + lane;
     const int rr = mat * 64 + (r & 63);   // row inside the scale atom of its 64-row tile
-    int it = 0;
+    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kGuACol + mat * 32;
+    int it = 0, ca = 0, na = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       for (int ks = 0; ks < nks; ++ks, ++it) {
-        const int s = it % nring, cb = it & 1;
+        const int s = it % nring;
         if (!abort_s && (!mbar_wait(&full[s], (it / nring) & 1) ||
-                         (it >= 2 && !mbar_wait(&conv_empty[cb], ((it >> 1) - 1) & 1)))) {
+                         (na > 0 && !mbar_wait(&conv_empty[ca], (na - 1) & 1)))) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
         }
+        fence_after();
         const unsigned char* raw = ring + (size_t)s * kGuStage + 16384;
         const unsigned char* sf = raw + 8192 + (r >> 6) * 512;
         const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(sf + (rr & 31) * 16 + (rr >> 5) * 4);
-        t16_convert_row(raw + mat * 4096 + r * 32, sc4, conv + cb * kT16Conv + mat * 16384, r);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        uint32_t o[32];
+        t16_dequant_row(raw + mat * 4096 + r * 32, sc4, o);
+        st32(tl + ca * 64, o);
+        fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&conv_full[cb]);
+          mbar_arrive(&conv_full[ca]);
           mbar_arrive(&empty[s]);
+        }
+        if (++ca == kGuAStages) {
+          ca = 0;
+          ++na;
         }
       }
     }
   } else {
-    // ---------------------------------------------------------------- epilogue (last 4 warps)
-    const int et = tid - (2 + kT16ConvWarps) * 32;   // 0..127
+    // ---------------------------------------------------------------- epilogue (last 8 warps)
+    // warp pair (w, w + 4) shares lane quadrant w & 3: columns 0..63 and 64..127
+    const int et = tid - (2 + kT16ConvWarps) * 32;   // 0..255
     const int quad = warp & 3;              // tensor-memory lanes 32*quad .. +31
     const int row = quad * 32 + lane;       // accumulator row of this thread
+    const int cbase = (et >> 7) * 64;
     int tcount = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
       const int j = t / prm.MT, mt = t % prm.MT;
-      const int buf = tcount & 1, use = tcount >> 1;
       const int e = ws.tt_expert[j];
       const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
       // per column (slot) factor 2^s of the slot's token
-      colfac[et] = et < nval ? ws.xfac[ws.perm[slot0 + et]] : 0.0f;
-      colmax[et] = 0u;
-      t16_epi_sync();
-      if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
+      if (et < kTileN) {
+        colfac[et] = et < nval ? ws.xfac[ws.perm[slot0 + et]] : 0.0f;
+        colmax[et] = 0u;
+      }
+      gu_epi_sync();
+      if (!abort_s && !mbar_wait(&acc_full, tcount & 1)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
       }
       __syncwarp();
       fence_after();
-      const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * (2 * kTileN);
+      const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + cbase;
       const float mg = prm.mult[e * 3 + 0], mu = prm.mult[e * 3 + 1];
       const int irow = mt * 128 + row;
-      for (int c0 = 0; c0 < kTileN; c0 += 32) {
-        uint32_t gr[32], ur[32];
-        ld32(tb + c0, gr);
-        ld32(tb + kTileN + c0, ur);
+      auto finish = [&](const uint32_t (&gr)[32], const uint32_t (&ur)[32], int c0) {
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           const int col = c0 + q;
@@ -825,13 +892,26 @@ __global__ void __launch_bounds__(kT16Threads, 1)
             if (lane == 0) atomicMax(&colmax[col], am);
           }
         }
+      };
+      {
+        uint32_t gr[32], ur[32];
+        ld32(tb, gr);
+        ld32(tb + kTileN, ur);
+        finish(gr, ur, cbase);
       }
-      fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
-      t16_epi_sync();
+      {
+        uint32_t gr[32], ur[32];
+        ld32(tb + 32, gr);
+        ld32(tb + kTileN + 32, ur);
+        // every accumulator column of this warp is in registers: the next tile may start
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty);
+        finish(gr, ur, cbase + 32);
+      }
+      gu_epi_sync();
       if (et < nval) atomicMax(&ws.slot_amax[slot0 + et], colmax[et]);
-      t16_epi_sync();   // colfac / colmax are reused by the next tile
+      gu_epi_sync();   // colfac / colmax are reused by the next tile
     }
   }
   fence_before();
@@ -1209,15 +1289,15 @@ bool tc_supported() { return encode_fn() != nullptr; }
 // TMA stages do not fit.
 bool tc16_geometry(int H, int I, int* gu_ring, int* gu_smem, int* dn_ring, int* dn_smem) {
   if (H % tc::kDnN || I % 128) return false;
-  const int budget = 232448 - 6144 - 2 * tc::kT16Conv - 1024;
+  const int budget = 232448 - 6144 - 1024;
   int g = budget / tc::kGuStage;
-  int d = (budget - (I / 64) * 16384) / tc::kDnStage;
+  int d = (budget - 2 * tc::kT16Conv - (I / 64) * 16384) / tc::kDnStage;
   if (g > tc::kT16MaxRing) g = tc::kT16MaxRing;
   if (d > tc::kT16MaxRing) d = tc::kT16MaxRing;
   if (g < 2 || d < 2) return false;
   if (gu_ring) *gu_ring = g;
   if (dn_ring) *dn_ring = d;
-  if (gu_smem) *gu_smem = 2 * tc::kT16Conv + g * tc::kGuStage + 1024;
+  if (gu_smem) *gu_smem = g * tc::kGuStage + 1024;
   if (dn_smem) *dn_smem = (I / 64) * 16384 + 2 * tc::kT16Conv + d * tc::kDnStage + 1024;
   return true;
 }
@@ -1330,7 +1410,7 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc::k_tc16_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, dn_smem);
   if (e != cudaSuccess) return e;
-  e = launch(lc, tc::k_tc16_gu, dim3(grid), dim3(tc::kT16Threads), (size_t)gu_smem, m_gate, m_up,
+  e = launch(lc, tc::k_tc16_gu, dim3(grid), dim3(tc::kGuThreads), (size_t)gu_smem, m_gate, m_up,
              m_x, pg, ws, gu_ring);
   if (e != cudaSuccess) return e;
   e = launch(lc, tc::k_hprep16, dim3(ws.NT), dim3(256), 0, ws);
