@@ -577,18 +577,15 @@ __global__ void __launch_bounds__(64 * kXqTok) k_xquant_perm(const uint16_t* __r
 // ------------------------------------------------------------------ W4A16 grouped experts
 // Tensor cores need both operands in one 16-bit type, and NVFP4 x BF16 has no MMA kind, so the
 // W4A16 grouped path runs tcgen05 kind::f16 on f16 operands that hold the values exactly:
-//   weights: E2M1 code x E4M3 scale (<= 6 significant bits, |v| <= 2688: exact in f16),
+//   A (weights): E2M1 code x E4M3 scale (<= 6 significant bits, |v| <= 2688: exact in f16),
 //     dequantised in shared memory by converter warps from the TMA-staged FP4 codes;
-//   activations: x * 2^-s per token (gate/up) and BF16 h * 2^-s per slot (down), with s
+//   B (activations): x * 2^-s per token (gate/up) and BF16 h * 2^-s per slot (down), with s
 //     putting the row's max |value| in [2^14, 2^15) (exact, as in the narrow-call path);
-// the epilogues restore 2^s. K = 64 per stage. The TMA-staged bytes of a stage and its
-// dequantised weights live in two rings: the TMA ring is deep (its slots are released as soon
-// as the converters have read them, so many HBM requests stay in flight) and the dequantised
-// ring has two slots (written by the converters, read by the MMAs).
-constexpr int kT16ConvWarps = 8;       // one dequantised row per thread and stage
-constexpr int kT16Threads = (2 + kT16ConvWarps + 4) * 32;   // producer, MMA, converters, epilogue
-constexpr int kT16MaxRing = 8;
-constexpr int kT16Conv = 32768;        // one dequantised slot: 256 rows x 64 f16, SW128
+// the epilogues restore 2^s. Tiles: 128 weight rows x 128 padded slots, K = 64 per stage.
+// Gate/up issues two MMAs per K step (the 128 gate rows and the 128 up rows of the same
+// intermediate indices) into two accumulators, so one epilogue lane holds both g and u.
+constexpr int kT16Stages = 3;
+constexpr int kT16Threads = 10 * 32;   // producer, MMA, 4 converter warps, 4 epilogue warps
 constexpr uint32_t kIdescF16 = (1u << 4) | ((uint32_t)(kTileN >> 3) << 17) |
                                ((uint32_t)(kTileM >> 4) << 24);   // f16 x f16 -> f32, 128x128
 
@@ -604,134 +601,54 @@ __device__ __forceinline__ void t16_epi_sync() {  // the 4 epilogue warps
   asm volatile("bar.sync 3, 128;" ::: "memory");
 }
 
-// One weight row of a stage: 64 E2M1 codes (32 bytes at src) times the E4M3 scales of its four
-// 16-element blocks (sc4, block b in byte b) -> f16 row `row` of an SW128 K-major tile (chunk c
-// of the row at chunk c ^ (row & 7)).
-__device__ __forceinline__ void t16_convert_row(const unsigned char* src, uint32_t sc4,
-                                                unsigned char* tile, int row) {
-  // consecutive rows' 32-byte code rows are read half by half, lanes 4..7 (mod 8) taking the
-  // second half first, so that each load of the warp touches every bank once per 128 bytes
-  const int h = (threadIdx.x >> 2) & 1;
-  const uint4 ca = reinterpret_cast<const uint4*>(src)[h];
-  const uint4 cb = reinterpret_cast<const uint4*>(src)[h ^ 1];
-  const uint4 c0 = h ? cb : ca, c1 = h ? ca : cb;
-  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  unsigned char* dst = tile + (row >> 3) * 1024 + (row & 7) * 128;
-  const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {   // chunk c: elements 8c .. 8c+7 = code word c, block c / 2
-    const uint32_t sp = (c < 4) ? s01 : s23;
-    uint32_t f[4];
-    e2m1x8_to_f16x2x4(w[c], f);
-    uint4 o;
-    if (c & 2) {
-      o = make_uint4(hmul2_hi(f[0], sp), hmul2_hi(f[1], sp), hmul2_hi(f[2], sp),
-                     hmul2_hi(f[3], sp));
-    } else {
-      o = make_uint4(hmul2_lo(f[0], sp), hmul2_lo(f[1], sp), hmul2_lo(f[2], sp),
-                     hmul2_lo(f[3], sp));
-    }
-    *reinterpret_cast<uint4*>(dst + ((c ^ (row & 7)) << 4)) = o;
-  }
-}
+// Per-stage layout (bytes): conv A (f16, SW128; gate/up: gate 16 KB + up 16 KB), B (16 KB),
+// raw FP4 codes (gate/up: 2 x 128 rows x 32 B), scale-factor atoms (gate/up 2, down 1).
+template <bool DOWN>
+struct T16 {
+  static constexpr int kConv = DOWN ? 16384 : 32768;
+  static constexpr int kB = 16384;
+  static constexpr int kRaw = DOWN ? 4096 : 8192;
+  static constexpr int kSf = DOWN ? 512 : 1024;
+  static constexpr int kStage = ((kConv + kB + kRaw + kSf) + 1023) / 1024 * 1024;
+  static constexpr int kTmemCols = DOWN ? 256 : 512;
+  static constexpr int kYStage = kTileN * kYStride * 2;   // down: transposed BF16 Y tile
+  static constexpr int kSmem = kT16Stages * kStage + (DOWN ? kYStage : 0) + 2 * 512 + 1024;
+};
 
-// Gate/up + SiLU*up. Tile = (token tile j, 128 intermediate rows mt): two M = 128 accumulators
-// (the gate rows and the up rows of the same intermediate indices, so one epilogue lane holds
-// both g and u), N = 128 padded slots. The dequantised weights are the MMAs' A operand in tensor
-// memory: a converter thread writes its row's 64 f16 of a stage into its own tensor-memory lane
-// (one tcgen05.st), so shared memory carries only what the TMA brings (the x tile, the codes,
-// the scales) and the x tile's MMA reads. Tensor memory: the gate and up accumulators (256
-// columns, one buffer: the next tile's first MMA waits for the epilogue to have read them) and a
-// three-stage ring of A (32 columns of gate and 32 of up per stage). TMA stage: the x tile (16 KB,
-// SW128), the gate and up codes (2 x 4 KB) and two scale-factor atoms (64-row intermediate tiles:
-// gate rows 0..63, up rows 64..127 of each atom).
-constexpr int kGuStage = 16384 + 8192 + 1024 + 1024;   // 26 KB (1 KB multiple: SW128 x tile)
-constexpr int kGuAStages = 3;
-constexpr int kGuEpiWarps = 8;          // two per tensor-memory lane quadrant (64 columns each)
-constexpr int kGuThreads = (2 + kT16ConvWarps + kGuEpiWarps) * 32;
-
-__device__ __forceinline__ void gu_epi_sync() {  // the epilogue warps
-  asm volatile("bar.sync 3, %0;" ::"r"(kGuEpiWarps * 32) : "memory");
-}
-constexpr uint32_t kGuACol = 2 * kTileN;                // first tensor-memory column of the A ring
-
-__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
-      "r"(a_tmem), "l"(b), "r"(kIdescF16), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// One weight row of a stage (64 E2M1 codes at src, the E4M3 scales of its four 16-element blocks
-// in sc4, block b in byte b) -> 32 f16x2 words in K order (word c holds elements 2c, 2c+1).
-__device__ __forceinline__ void t16_dequant_row(const unsigned char* src, uint32_t sc4,
-                                                uint32_t (&o)[32]) {
-  // consecutive rows' 32-byte code rows are read half by half, lanes 4..7 (mod 8) taking the
-  // second half first, so that each load of the warp touches every bank once per 128 bytes
-  const int h = (threadIdx.x >> 2) & 1;
-  const uint4 ca = reinterpret_cast<const uint4*>(src)[h];
-  const uint4 cb = reinterpret_cast<const uint4*>(src)[h ^ 1];
-  const uint4 c0 = h ? cb : ca, c1 = h ? ca : cb;
-  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-  const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {   // code word c: elements 8c .. 8c+7, block c / 2
-    const uint32_t sp = (c < 4) ? s01 : s23;
-    uint32_t f[4];
-    e2m1x8_to_f16x2x4(w[c], f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[4 * c + i] = (c & 2) ? hmul2_hi(f[i], sp) : hmul2_lo(f[i], sp);
-  }
-}
-
-__global__ void __launch_bounds__(kGuThreads, 1)
-    k_tc16_gu(const __grid_constant__ CUtensorMap tm_gate, const __grid_constant__ CUtensorMap tm_up,
-              const __grid_constant__ CUtensorMap tm_x, TcParams prm, WsView ws, int nring) {
+template <bool DOWN>
+__global__ void __launch_bounds__(kT16Threads, 1)
+    k_tc16(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+           const __grid_constant__ CUtensorMap tm_b, TcParams prm, WsView ws) {
+  using L = T16<DOWN>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t full[kT16MaxRing], empty[kT16MaxRing];
-  __shared__ uint64_t conv_full[kGuAStages], conv_empty[kGuAStages], acc_full, acc_empty;
-  __shared__ float colfac[kTileN];
-  __shared__ uint32_t colmax[kTileN];
+  __shared__ uint64_t full[kT16Stages], conv_full[kT16Stages], empty[kT16Stages];
+  __shared__ uint64_t acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  unsigned char* ring = smem_raw + pad;                    // [nring][x | codes | sf]
+  unsigned char* smem = smem_raw + pad;
+  unsigned char* ystage = smem + kT16Stages * L::kStage;            // down: Y tile
+  float* colfac = reinterpret_cast<float*>(ystage + (DOWN ? L::kYStage : 0));   // [128]
+  uint32_t* colmax = reinterpret_cast<uint32_t*>(colfac + kTileN);             // [128]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    for (int s = 0; s < nring; ++s) {
+    for (int s = 0; s < kT16Stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kT16ConvWarps + 1);   // the converter warps (codes), the MMA (x tile)
+      mbar_init(&conv_full[s], 4);
+      mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < kGuAStages; ++b) {
-      mbar_init(&conv_full[b], kT16ConvWarps);
-      mbar_init(&conv_empty[b], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
     }
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, kGuEpiWarps);
     fence_mbar_init();
     abort_s = 0;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&tmem_base_s)),
-                 "r"(4 * kTileN)
+                 "r"(L::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -742,9 +659,10 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
 
-  const int ntiles = (int)ws.ctl[kCtlTokenTiles] * prm.MT;
+  const int NT = (int)ws.ctl[kCtlTokenTiles];
+  const int ntiles = NT * prm.MT;
   const int H = prm.H, I = prm.I;
-  const int nks = H / 64;
+  const int nks = DOWN ? I / 64 : H / 64;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -754,164 +672,203 @@ __global__ void __launch_bounds__(kGuThreads, 1)
         const int j = t / prm.MT, mt = t % prm.MT;
         const int e = __ldg(&ws.tt_expert[j]);
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % nring, n = it / nring;
+          const int s = it % kT16Stages, n = it / kT16Stages;
           if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
             record_status(ws.ctl, kStTimeout);
             abort_s = 1;
             break;
           }
-          unsigned char* xt = ring + (size_t)s * kGuStage;
-          unsigned char* raw = xt + 16384;
-          unsigned char* sf = raw + 8192;
-          mbar_arrive_expect_tx(&full[s], 16384 + 8192 + 1024);
-          tma_2d(raw, &tm_gate, ks * 32, e * I + mt * 128, &full[s]);
-          tma_2d(raw + 4096, &tm_up, ks * 32, e * I + mt * 128, &full[s]);
-          for (int h2 = 0; h2 < 2; ++h2)
-            bulk_g2s(sf + h2 * 512,
-                     prm.sfa + (((size_t)e * (I / 64) + 2 * mt + h2) * (H / 64) + ks) * 512, 512,
+          unsigned char* st = smem + s * L::kStage;
+          unsigned char* bt = st + L::kConv;
+          unsigned char* raw = bt + L::kB;
+          unsigned char* sf = raw + L::kRaw;
+          mbar_arrive_expect_tx(&full[s], L::kB + L::kRaw + L::kSf);
+          if (!DOWN) {
+            tma_2d(raw, &tm_a0, ks * 32, e * I + mt * 128, &full[s]);
+            tma_2d(raw + 4096, &tm_a1, ks * 32, e * I + mt * 128, &full[s]);
+            // scale atoms of the two 64-row intermediate tiles (gate rows 0..63, up 64..127)
+            for (int h2 = 0; h2 < 2; ++h2)
+              bulk_g2s(sf + h2 * 512,
+                       prm.sfa + (((size_t)e * (I / 64) + 2 * mt + h2) * (H / 64) + ks) * 512, 512,
+                       &full[s]);
+          } else {
+            tma_2d(raw, &tm_a0, ks * 32, e * H + mt * 128, &full[s]);
+            bulk_g2s(sf, prm.sfa + (((size_t)e * (H / 128) + mt) * (I / 64) + ks) * 512, 512,
                      &full[s]);
-          tma_2d(xt, &tm_x, ks * 128, j * 128, &full[s]);
+          }
+          tma_2d(bt, &tm_b, ks * 128, j * 128, &full[s]);
         }
       }
-      const int used = it < nring ? it : nring;
+      const int used = it < kT16Stages ? it : kT16Stages;
       for (int i = 0; i < used; ++i) {
         const int c = it - 1 - i;
-        (void)mbar_wait(&full[c % nring], (c / nring) & 1);
+        (void)mbar_wait(&full[c % kT16Stages], (c / kT16Stages) & 1);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int it = 0, tcount = 0, ca = 0, na = 0;   // ca / na: A ring slot and its use count
+      int it = 0, tcount = 0;
+      const uint32_t bufcols = DOWN ? kTileN : 2 * kTileN;
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
-        if (tcount > 0 && !abort_s && !mbar_wait(&acc_empty, (tcount - 1) & 1)) {
+        const int buf = tcount & 1, use = tcount >> 1;
+        if (use > 0 && !abort_s && !mbar_wait(&acc_empty[buf], (use - 1) & 1)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
         }
         fence_after();
+        const uint32_t d0 = tmem + buf * bufcols;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % nring;
-          if (!abort_s && (!mbar_wait(&full[s], (it / nring) & 1) ||
-                           !mbar_wait(&conv_full[ca], na & 1))) {
+          const int s = it % kT16Stages, n = it / kT16Stages;
+          if (!abort_s && !mbar_wait(&conv_full[s], n & 1)) {
             record_status(ws.ctl, kStTimeout);
             abort_s = 1;
           }
           fence_after();
-          const uint32_t ag = tmem + kGuACol + ca * 64, au = ag + 32;
-          const uint32_t b0 = smem_u32(ring + (size_t)s * kGuStage);
+          unsigned char* st = smem + s * L::kStage;
+          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + L::kConv);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t acc = (ks > 0 || q > 0) ? 1u : 0u;
-            mma_f16_ts(tmem, ag + q * 8, desc_sw128(b0 + q * 32), acc);
-            mma_f16_ts(tmem + kTileN, au + q * 8, desc_sw128(b0 + q * 32), acc);
+            mma_f16(d0, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32), acc);
+            if (!DOWN)
+              mma_f16(d0 + kTileN, desc_sw128(a0 + 16384 + q * 32), desc_sw128(b0 + q * 32), acc);
           }
           commit(&empty[s]);
-          commit(&conv_empty[ca]);
-          if (++ca == kGuAStages) {
-            ca = 0;
-            ++na;
-          }
         }
-        commit(&acc_full);
+        commit(&acc_full[buf]);
       }
     }
-  } else if (warp < 2 + kT16ConvWarps) {
-    // ---------------------------------------------------------------- converters
-    // warps 2..5: gate rows, warps 6..9: up rows; a thread converts the row of its own
-    // tensor-memory lane (32 x (warp % 4) + lane) of every stage
-    const int mat = (warp - 2) >> 2, r = 32 * (warp & 3) + lane;
-    const int rr = mat * 64 + (r & 63);   // row inside the scale atom of its 64-row tile
-    const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kGuACol + mat * 32;
-    int it = 0, ca = 0, na = 0;
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- converters (warps 2..5)
+    // thread ct owns A row ct (gate/up: gate row ct and up row ct) of every stage
+    const int ct = tid - 64;
+    int it = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       for (int ks = 0; ks < nks; ++ks, ++it) {
-        const int s = it % nring;
-        if (!abort_s && (!mbar_wait(&full[s], (it / nring) & 1) ||
-                         (na > 0 && !mbar_wait(&conv_empty[ca], (na - 1) & 1)))) {
+        const int s = it % kT16Stages, n = it / kT16Stages;
+        if (!abort_s && !mbar_wait(&full[s], n & 1)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
         }
-        fence_after();
-        const unsigned char* raw = ring + (size_t)s * kGuStage + 16384;
-        const unsigned char* sf = raw + 8192 + (r >> 6) * 512;
-        const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(sf + (rr & 31) * 16 + (rr >> 5) * 4);
-        uint32_t o[32];
-        t16_dequant_row(raw + mat * 4096 + r * 32, sc4, o);
-        st32(tl + ca * 64, o);
-        fence_before();
+        unsigned char* st = smem + s * L::kStage;
+        const unsigned char* raw = st + L::kConv + L::kB;
+        const unsigned char* sf = raw + L::kRaw;
+#pragma unroll
+        for (int mat = 0; mat < (DOWN ? 1 : 2); ++mat) {
+          const uint4* src = reinterpret_cast<const uint4*>(raw + mat * 4096 + ct * 32);
+          const uint4 c0 = src[0], c1 = src[1];
+          // the row's 4 scale bytes (blocks of 16 along this stage's 64 K)
+          const int rr = DOWN ? ct : mat * 64 + (ct & 63);
+          const unsigned char* atom = sf + (DOWN ? 0 : (ct >> 6) * 512);
+          const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(atom + (rr & 31) * 16 + (rr >> 5) * 4);
+          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          unsigned char* row = st + mat * 16384 + (ct >> 3) * 1024 + (ct & 7) * 128;
+          const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {   // chunk c: elements 8c .. 8c+7 = code word c
+            const uint32_t sp = (c < 4) ? s01 : s23;
+            uint32_t f[4];
+            e2m1x8_to_f16x2x4(w[c], f);
+            uint4 o;
+            if (c & 2) {   // blocks 1 and 3 of the stage: the high half of the pair
+              o = make_uint4(hmul2_hi(f[0], sp), hmul2_hi(f[1], sp), hmul2_hi(f[2], sp),
+                             hmul2_hi(f[3], sp));
+            } else {
+              o = make_uint4(hmul2_lo(f[0], sp), hmul2_lo(f[1], sp), hmul2_lo(f[2], sp),
+                             hmul2_lo(f[3], sp));
+            }
+            *reinterpret_cast<uint4*>(row + ((c ^ (ct & 7)) << 4)) = o;
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&conv_full[ca]);
-          mbar_arrive(&empty[s]);
-        }
-        if (++ca == kGuAStages) {
-          ca = 0;
-          ++na;
-        }
+        if (lane == 0) mbar_arrive(&conv_full[s]);
       }
     }
   } else {
-    // ---------------------------------------------------------------- epilogue (last 8 warps)
-    // warp pair (w, w + 4) shares lane quadrant w & 3: columns 0..63 and 64..127
-    const int et = tid - (2 + kT16ConvWarps) * 32;   // 0..255
+    // ---------------------------------------------------------------- epilogue (warps 6..9)
+    const int et = tid - 192;               // 0..127
     const int quad = warp & 3;              // tensor-memory lanes 32*quad .. +31
     const int row = quad * 32 + lane;       // accumulator row of this thread
-    const int cbase = (et >> 7) * 64;
     int tcount = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
       const int j = t / prm.MT, mt = t % prm.MT;
+      const int buf = tcount & 1, use = tcount >> 1;
       const int e = ws.tt_expert[j];
       const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
-      // per column (slot) factor 2^s of the slot's token
-      if (et < kTileN) {
-        colfac[et] = et < nval ? ws.xfac[ws.perm[slot0 + et]] : 0.0f;
-        colmax[et] = 0u;
+      // per column (slot) factor 2^s: of the slot's token (gate/up) or of the slot (down)
+      {
+        float f = 0.0f;
+        if (et < nval) {
+          if (!DOWN) {
+            f = ws.xfac[ws.perm[slot0 + et]];
+          } else {
+            f = __int_as_float((127 + amax_shift(__uint_as_float(ws.slot_amax[slot0 + et]))) << 23);
+          }
+        }
+        colfac[et] = f;
+        if (!DOWN) colmax[et] = 0u;
       }
-      gu_epi_sync();
-      if (!abort_s && !mbar_wait(&acc_full, tcount & 1)) {
+      t16_epi_sync();
+      if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
       }
       __syncwarp();
       fence_after();
-      const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + cbase;
-      const float mg = prm.mult[e * 3 + 0], mu = prm.mult[e * 3 + 1];
-      const int irow = mt * 128 + row;
-      auto finish = [&](const uint32_t (&gr)[32], const uint32_t (&ur)[32], int c0) {
+      if (!DOWN) {
+        const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * (2 * kTileN);
+        const float mg = prm.mult[e * 3 + 0], mu = prm.mult[e * 3 + 1];
+        const int irow = mt * 128 + row;
+        for (int c0 = 0; c0 < kTileN; c0 += 32) {
+          uint32_t gr[32], ur[32];
+          ld32(tb + c0, gr);
+          ld32(tb + kTileN + c0, ur);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int col = c0 + q;
-          const float fx = colfac[col];
-          const float gv = __uint_as_float(gr[q]) * mg * fx;
-          const float uv = __uint_as_float(ur[q]) * mu * fx;
-          const uint16_t hb = f32_to_bf16_rn((gv / (1.0f + expf(-gv))) * uv);
-          const uint32_t am = __reduce_max_sync(
-              0xFFFFFFFFu, __float_as_uint(fabsf(__uint_as_float((uint32_t)hb << 16))));
-          if (col < nval) {
-            ws.h16[(size_t)(slot0 + col) * I + irow] = hb;
-            if (lane == 0) atomicMax(&colmax[col], am);
+          for (int q = 0; q < 32; ++q) {
+            const int col = c0 + q;
+            const float fx = colfac[col];
+            const float gv = __uint_as_float(gr[q]) * mg * fx;
+            const float uv = __uint_as_float(ur[q]) * mu * fx;
+            const uint16_t hb = f32_to_bf16_rn((gv / (1.0f + expf(-gv))) * uv);
+            const uint32_t am = __reduce_max_sync(
+                0xFFFFFFFFu, __float_as_uint(fabsf(__uint_as_float((uint32_t)hb << 16))));
+            if (col < nval) {
+              ws.h16[(size_t)(slot0 + col) * I + irow] = hb;
+              if (lane == 0) atomicMax(&colmax[col], am);
+            }
           }
         }
-      };
-      {
-        uint32_t gr[32], ur[32];
-        ld32(tb, gr);
-        ld32(tb + kTileN, ur);
-        finish(gr, ur, cbase);
-      }
-      {
-        uint32_t gr[32], ur[32];
-        ld32(tb + 32, gr);
-        ld32(tb + kTileN + 32, ur);
-        // every accumulator column of this warp is in registers: the next tile may start
         fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty);
-        finish(gr, ur, cbase + 32);
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        t16_epi_sync();
+        if (et < nval) atomicMax(&ws.slot_amax[slot0 + et], colmax[et]);
+      } else {
+        const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN;
+        const float md = prm.mult[e * 3 + 2];
+        uint16_t* yt = reinterpret_cast<uint16_t*>(ystage);
+        for (int c0 = 0; c0 < kTileN; c0 += 32) {
+          uint32_t r[32];
+          ld32(tb + c0, r);
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            yt[(c0 + q) * kYStride + row] =
+                f32_to_bf16_rn(__uint_as_float(r[q]) * md * colfac[c0 + q]);
+        }
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        t16_epi_sync();
+        for (int id = et; id < kTileN * (kTileM / 8); id += 128) {
+          const int col = id >> 4, r8 = id & 15;
+          if (col < nval)
+            *reinterpret_cast<uint4*>(ws.y + (size_t)(slot0 + col) * H + mt * 128 + r8 * 8) =
+                *reinterpret_cast<const uint4*>(yt + col * kYStride + r8 * 8);
+        }
       }
-      gu_epi_sync();
-      if (et < nval) atomicMax(&ws.slot_amax[slot0 + et], colmax[et]);
-      gu_epi_sync();   // colfac / colmax are reused by the next tile
+      t16_epi_sync();   // colfac / colmax / the Y tile are reused by the next tile
     }
   }
   fence_before();
@@ -919,20 +876,23 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(4 * kTileN)
+                 "r"(L::kTmemCols)
                  : "memory");
 }
 
-// Down with the operands' roles swapped: A = the h tile of one 128-slot token tile (f16, all I
-// columns, resident in shared memory while the CTA runs every 256-row weight tile of that token
-// tile), B = 256 dequantised down-weight rows x 64 K per stage, D = [slot][row] (M = 128,
-// N = 256) in tensor memory. The h tile is staged once per token tile instead of once per weight
-// tile, and each epilogue thread owns one slot, so Y rows are written directly. TMA stage: the
-// codes of the 256 rows (2 x 4 KB) and two 128-row scale-factor atoms.
+// W4A16 down GEMM with the operands' roles swapped: A = the h tile of one 128-slot token tile
+// (f16, all I columns, resident in shared memory while the CTA runs every 256-row weight tile of
+// that token tile), B = 256 dequantised down-weight rows x 64 K per stage, D = [slot][row]
+// (M = 128, N = 256) in tensor memory. The h tile is staged once per token tile instead of once
+// per weight tile, and each epilogue thread owns one slot, so Y rows are written directly.
 constexpr int kDnN = 256;
 constexpr uint32_t kIdescDn = (1u << 4) | ((uint32_t)(kDnN >> 3) << 17) |
                               ((uint32_t)(kTileM >> 4) << 24);   // f16 x f16 -> f32, 128x256
-constexpr int kDnStage = 8192 + 1024;
+constexpr int kDnConv = kDnN * 128;                 // 256 rows x 128 B (64 f16), SW128
+constexpr int kDnRaw = kDnN * 32;                   // 256 rows x 64 FP4 codes
+constexpr int kDnSf = 2 * 512;                      // two 128-row scale-factor atoms
+constexpr int kDnStage = kDnConv + kDnRaw + kDnSf;  // 41 KB, a multiple of 1 KB
+constexpr int kDnMaxStages = 3;
 
 __device__ __forceinline__ void mma_f16_dn(uint32_t d, uint64_t a, uint64_t b,
                                            uint32_t accumulate) {
@@ -945,10 +905,10 @@ __device__ __forceinline__ void mma_f16_dn(uint32_t d, uint64_t a, uint64_t b,
 
 __global__ void __launch_bounds__(kT16Threads, 1)
     k_tc16_dn(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_h,
-              TcParams prm, WsView ws, int nring) {
+              TcParams prm, WsView ws, int nst) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t full[kT16MaxRing], empty[kT16MaxRing];
-  __shared__ uint64_t conv_full[2], conv_empty[2], acc_full[2], acc_empty[2], a_full, a_empty;
+  __shared__ uint64_t full[kDnMaxStages], conv_full[kDnMaxStages], empty[kDnMaxStages];
+  __shared__ uint64_t acc_full[2], acc_empty[2], a_full, a_empty;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -956,18 +916,16 @@ __global__ void __launch_bounds__(kT16Threads, 1)
   const int H = prm.H, I = prm.I;
   const int nks = I / 64;
   unsigned char* atile = smem;                                   // [nks][128 rows x 128 B]
-  unsigned char* conv = smem + (size_t)nks * 16384;              // [2][256 rows x 128 B]
-  unsigned char* ring = conv + 2 * kT16Conv;                     // [nring][codes | sf]
+  unsigned char* stages = smem + (size_t)nks * 16384;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
-    for (int s = 0; s < nring; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kT16ConvWarps);
+      mbar_init(&conv_full[s], 4);
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&conv_full[b], kT16ConvWarps);
-      mbar_init(&conv_empty[b], 1);
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 4);
     }
@@ -1011,21 +969,20 @@ __global__ void __launch_bounds__(kT16Threads, 1)
             break;
           }
           mbar_arrive_expect_tx(&a_full, (uint32_t)nks * 16384u);
-          for (int ks = 0; ks < nks; ++ks)
-            tma_2d(atile + ks * 16384, &tm_h, ks * 128, j * 128, &a_full);
+          for (int ks = 0; ks < nks; ++ks) tma_2d(atile + ks * 16384, &tm_h, ks * 128, j * 128, &a_full);
           jprev = j;
           ++jcount;
         }
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % nring, n = it / nring;
+          const int s = it % nst, n = it / nst;
           if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
             record_status(ws.ctl, kStTimeout);
             abort_s = 1;
             break;
           }
-          unsigned char* raw = ring + (size_t)s * kDnStage;
-          unsigned char* sf = raw + 8192;
-          mbar_arrive_expect_tx(&full[s], kDnStage);
+          unsigned char* raw = stages + (size_t)s * kDnStage + kDnConv;
+          unsigned char* sf = raw + kDnRaw;
+          mbar_arrive_expect_tx(&full[s], kDnRaw + kDnSf);
           tma_2d(raw, &tm_raw, ks * 32, e * H + nt * kDnN, &full[s]);
           tma_2d(raw + 4096, &tm_raw, ks * 32, e * H + nt * kDnN + 128, &full[s]);
           for (int h2 = 0; h2 < 2; ++h2)
@@ -1034,10 +991,10 @@ __global__ void __launch_bounds__(kT16Threads, 1)
                      &full[s]);
         }
       }
-      const int used = it < nring ? it : nring;
+      const int used = it < nst ? it : nst;
       for (int i = 0; i < used; ++i) {
         const int c = it - 1 - i;
-        (void)mbar_wait(&full[c % nring], (c / nring) & 1);
+        (void)mbar_wait(&full[c % nst], (c / nst) & 1);
       }
     }
   } else if (warp == 1) {
@@ -1062,52 +1019,73 @@ __global__ void __launch_bounds__(kT16Threads, 1)
         fence_after();
         const uint32_t d0 = tmem + buf * kDnN;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int cb = it & 1;
-          if (!abort_s && !mbar_wait(&conv_full[cb], (it >> 1) & 1)) {
+          const int s = it % nst, n = it / nst;
+          if (!abort_s && !mbar_wait(&conv_full[s], n & 1)) {
             record_status(ws.ctl, kStTimeout);
             abort_s = 1;
           }
           fence_after();
           const uint32_t a0 = smem_u32(atile + ks * 16384);
-          const uint32_t b0 = smem_u32(conv + cb * kT16Conv);
+          const uint32_t b0 = smem_u32(stages + (size_t)s * kDnStage);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             mma_f16_dn(d0, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32),
                        (ks > 0 || q > 0) ? 1u : 0u);
-          commit(&conv_empty[cb]);
+          commit(&empty[s]);
         }
         commit(&acc_full[buf]);
         // the h tile may be replaced once this token tile's last MMA has read it
         if (u + 1 == u1 || (u + 1) / nts != j) commit(&a_empty);
       }
     }
-  } else if (warp < 2 + kT16ConvWarps) {
-    // ---------------------------------------------------------------- converters
-    // thread ct owns B row ct of every stage (rows 0..127: first atom, 128..255: second)
-    const int ct = tid - 64, mat = ct >> 7, r = ct & 127;
+  } else if (warp < 6) {
+    // ---------------------------------------------------------------- converters (warps 2..5)
+    // thread ct owns B rows ct and ct + 128 of every stage
+    const int ct = tid - 64;
     int it = 0;
     for (int u = u0; u < u1; ++u) {
       for (int ks = 0; ks < nks; ++ks, ++it) {
-        const int s = it % nring, cb = it & 1;
-        if (!abort_s && (!mbar_wait(&full[s], (it / nring) & 1) ||
-                         (it >= 2 && !mbar_wait(&conv_empty[cb], ((it >> 1) - 1) & 1)))) {
+        const int s = it % nst, n = it / nst;
+        if (!abort_s && !mbar_wait(&full[s], n & 1)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
         }
-        const unsigned char* raw = ring + (size_t)s * kDnStage;
-        const unsigned char* sf = raw + 8192 + mat * 512;
-        const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(sf + (r & 31) * 16 + (r >> 5) * 4);
-        t16_convert_row(raw + ct * 32, sc4, conv + cb * kT16Conv, ct);
+        unsigned char* st = stages + (size_t)s * kDnStage;
+        const unsigned char* raw = st + kDnConv;
+        const unsigned char* sf = raw + kDnRaw;
+#pragma unroll
+        for (int mat = 0; mat < 2; ++mat) {
+          const uint4* src = reinterpret_cast<const uint4*>(raw + mat * 4096 + ct * 32);
+          const uint4 c0 = src[0], c1 = src[1];
+          // the row's 4 scale bytes (blocks of 16 along this stage's 64 K)
+          const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(sf + mat * 512 + (ct & 31) * 16 +
+                                                                  (ct >> 5) * 4);
+          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          unsigned char* row = st + mat * 16384 + (ct >> 3) * 1024 + (ct & 7) * 128;
+          const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {   // chunk c: elements 8c .. 8c+7 = code word c
+            const uint32_t sp = (c < 4) ? s01 : s23;
+            uint32_t f[4];
+            e2m1x8_to_f16x2x4(w[c], f);
+            uint4 o;
+            if (c & 2) {
+              o = make_uint4(hmul2_hi(f[0], sp), hmul2_hi(f[1], sp), hmul2_hi(f[2], sp),
+                             hmul2_hi(f[3], sp));
+            } else {
+              o = make_uint4(hmul2_lo(f[0], sp), hmul2_lo(f[1], sp), hmul2_lo(f[2], sp),
+                             hmul2_lo(f[3], sp));
+            }
+            *reinterpret_cast<uint4*>(row + ((c ^ (ct & 7)) << 4)) = o;
+          }
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&conv_full[cb]);
-          mbar_arrive(&empty[s]);
-        }
+        if (lane == 0) mbar_arrive(&conv_full[s]);
       }
     }
   } else {
-    // ---------------------------------------------------------------- epilogue (last 4 warps)
+    // ---------------------------------------------------------------- epilogue (warps 6..9)
     const int quad = warp & 3;              // tensor-memory lanes 32*quad .. +31
     const int row = quad * 32 + lane;       // slot of the token tile
     int tcount = 0;
@@ -1284,28 +1262,10 @@ cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t
 
 bool tc_supported() { return encode_fn() != nullptr; }
 
-// Ring depths and dynamic shared memory of the W4A16 GEMMs (a 6 KB allowance for the static
-// shared memory and the 1 KB alignment pad); false when the down GEMM's resident h tile and two
-// TMA stages do not fit.
-bool tc16_geometry(int H, int I, int* gu_ring, int* gu_smem, int* dn_ring, int* dn_smem) {
-  if (H % tc::kDnN || I % 128) return false;
-  const int budget = 232448 - 6144 - 1024;
-  int g = budget / tc::kGuStage;
-  int d = (budget - 2 * tc::kT16Conv - (I / 64) * 16384) / tc::kDnStage;
-  if (g > tc::kT16MaxRing) g = tc::kT16MaxRing;
-  if (d > tc::kT16MaxRing) d = tc::kT16MaxRing;
-  if (g < 2 || d < 2) return false;
-  if (gu_ring) *gu_ring = g;
-  if (dn_ring) *dn_ring = d;
-  if (gu_smem) *gu_smem = g * tc::kGuStage + 1024;
-  if (dn_smem) *dn_smem = (I / 64) * 16384 + 2 * tc::kT16Conv + d * tc::kDnStage + 1024;
-  return true;
-}
-
 bool tile_path(int T, int H, int I, int mode) {
   if (T <= kNarrowT || !tc_supported()) return false;
   if (mode == 1) return H % 256 == 0 && I % 64 == 0;
-  if (mode == 0) return tc16_geometry(H, I, nullptr, nullptr, nullptr, nullptr);
+  if (mode == 0) return H % 128 == 0 && I % 128 == 0;
   return false;
 }
 
@@ -1392,6 +1352,12 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
   cudaError_t e = launch(lc, tc::k_xprep16_perm, dim3((ws.T + tc::kXqTok - 1) / tc::kXqTok),
                          dim3(64 * tc::kXqTok), 0, x, ws);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::k_tc16<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::T16<false>::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc::k_tc16<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tc::T16<true>::kSmem);
+  if (e != cudaSuccess) return e;
   tc::TcParams pg;
   pg.sfa = pk.sfa_gu;
   pg.sfb = nullptr;
@@ -1404,14 +1370,8 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
   pg.nks = H / 64;
   pg.last_k4 = 0;
   const int grid = lc.num_sms;
-  int gu_ring = 0, dn_ring = 0, gu_smem = 0, dn_smem = 0;
-  if (!tc16_geometry(H, I, &gu_ring, &gu_smem, &dn_ring, &dn_smem)) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(tc::k_tc16_gu, cudaFuncAttributeMaxDynamicSharedMemorySize, gu_smem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc::k_tc16_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, dn_smem);
-  if (e != cudaSuccess) return e;
-  e = launch(lc, tc::k_tc16_gu, dim3(grid), dim3(tc::kGuThreads), (size_t)gu_smem, m_gate, m_up,
-             m_x, pg, ws, gu_ring);
+  e = launch(lc, tc::k_tc16<false>, dim3(grid), dim3(tc::kT16Threads), tc::T16<false>::kSmem,
+             m_gate, m_up, m_x, pg, ws);
   if (e != cudaSuccess) return e;
   e = launch(lc, tc::k_hprep16, dim3(ws.NT), dim3(256), 0, ws);
   if (e != cudaSuccess) return e;
@@ -1419,8 +1379,19 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
   pd.sfa = pk.sfa_down;
   pd.MT = H / 128;
   pd.nks = I / 64;
-  return launch(lc, tc::k_tc16_dn, dim3(grid), dim3(tc::kT16Threads), (size_t)dn_smem, m_down,
-                m_h, pd, ws, dn_ring);
+  // the down GEMM with the h tile resident when it and two weight stages fit in shared memory
+  const int abytes = (I / 64) * 16384;
+  int nst = (232448 - 2048 - abytes) / tc::kDnStage;
+  if (nst > tc::kDnMaxStages) nst = tc::kDnMaxStages;
+  if (H % tc::kDnN == 0 && nst >= 2) {
+    const int smem = abytes + nst * tc::kDnStage + 1024;
+    e = cudaFuncSetAttribute(tc::k_tc16_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch(lc, tc::k_tc16_dn, dim3(grid), dim3(tc::kT16Threads), (size_t)smem, m_down, m_h,
+                  pd, ws, nst);
+  }
+  return launch(lc, tc::k_tc16<true>, dim3(grid), dim3(tc::kT16Threads), tc::T16<true>::kSmem,
+                m_down, m_down, m_h, pd, ws);
 }
 
 }  // namespace moe
