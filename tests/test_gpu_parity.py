@@ -196,11 +196,29 @@ def test_forward_tiny_workload(mode):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
-@pytest.mark.parametrize("T", [1, 3, 8, 9, 50, 203])
+@pytest.mark.parametrize("T", [1, 2, 3, 8, 9, 50, 203])
 def test_forward_ragged_shapes(T, mode):
     # several row tiles, k-blocks and token groups, with ragged tails
     H, E, k, I = 1536, 24, 4, 192
     x, wr, ex = small_layer(T, H, E, k, I, zipf=True, seed=11)
+    pack = pack_from_experts(ex)
+    run_and_check(x, wr, ex, pack, k, mode)
+    pack.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("T,H,E,k,I", [
+    (1, 768, 640, 8, 128),    # more than 512 experts (32 logits per lane), H % 512 != 0
+    (2, 768, 640, 8, 128),
+    (1, 1024, 64, 1, 128),    # a single expert per token
+    (1, 1024, 64, 16, 128),   # 16 experts per token
+    (5, 1024, 200, 6, 256),
+])
+def test_forward_narrow_call_shapes(T, H, E, k, I, mode):
+    # the one-launch narrow-call kernel (T <= 8): router dot products on CUDA cores (T <= 2) or
+    # tensor cores, the threshold top-k with 16 or 32 logits per lane, one-token groups built in
+    # the selecting warp
+    x, wr, ex = small_layer(T, H, E, k, I, seed=31 + T + k)
     pack = pack_from_experts(ex)
     run_and_check(x, wr, ex, pack, k, mode)
     pack.close()
