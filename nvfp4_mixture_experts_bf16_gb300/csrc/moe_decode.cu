@@ -956,11 +956,12 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         const int row = ht * kDnRows + warp * 16 + g + ((q2 >> 1) << 3);
         const uint16_t yb = f32_to_bf16_rn(acc[q2] * md * hfac_s[col < n ? col : 0]);
         const uint32_t yb_next = __shfl_down_sync(0xFFFFFFFFu, (uint32_t)yb, 4);
-        if (col < n) {
+        if (col < n && (g & 1) == 0) {
+          // rows (row, row + 1) as one pair: plain (4-byte store) and tagged
           const size_t slot = (size_t)(slot0 + col);
-          ws.y[slot * H + row] = yb;
-          if ((g & 1) == 0)
-            st_tag(ws.ytag + slot * (H / 2) + row / 2, (uint32_t)yb | (yb_next << 16), ep);
+          const uint32_t pair = (uint32_t)yb | (yb_next << 16);
+          *reinterpret_cast<uint32_t*>(ws.y + slot * H + row) = pair;
+          st_tag(ws.ytag + slot * (H / 2) + row / 2, pair, ep);
         }
       }
     }
