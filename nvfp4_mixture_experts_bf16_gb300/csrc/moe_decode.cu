@@ -13,17 +13,20 @@
 //
 //   1. router: each CTA copies its 3-4 router rows (TMA bulk copy, issued before waiting for
 //      the preceding kernel: the router does not depend on it) and the T activation rows, and
-//      writes its tagged logits. Then it converts the activations into the f16 (W4A16) or
-//      NVFP4-decoded (W4A4) MMA operand in its own shared memory and writes its share of the
-//      W4A4 codes.
+//      writes its tagged logits (CUDA-core dot products for one or two tokens, mma.sync for
+//      more). Then it converts the activations into the f16 (W4A16) or NVFP4-decoded (W4A4) MMA
+//      operand in its own shared memory and writes its share of the W4A4 codes; with one or two
+//      tokens the selecting warps skip that and route meanwhile.
 //   2. routing: every CTA selects the top-k of every token itself (one warp per token, from the
-//      tagged logits), sorts the T*k selections by expert and builds the expert groups in shared
-//      memory. CTA 0 publishes idx / w / counts / offsets / perm / slot_of.
+//      tagged logits, by a threshold over the lane maxima), sorts the T*k selections by expert
+//      and builds the expert groups in shared memory (one token: in the selecting warp, which
+//      also issues the CTA's first gate/up copies). CTA 0 publishes idx / w / counts / offsets /
+//      perm / slot_of after its own work.
 //   3. gate/up + SiLU*up: tasks (group, 16-row tile of I), as in the multi-kernel path; h is
 //      written plain and tagged. As soon as its last gate/up stage is free, the producer warp
 //      streams this CTA's down weights into the same shared memory.
 //   4. down: tasks (group, 128-row tile of H); a task waits only for its own group's tagged h.
-//      Each task writes Y (BF16), plain and tagged.
+//      Each task writes Y (BF16) as pairs of rows, plain and tagged.
 //   5. combine: CTA j (mod the grid) forms 128-row tile j of out once its tagged Y has arrived:
 //      the fixed-order weighted sum over each token's k experts (rank order, FP32, then BF16).
 #include "moe_internal.cuh"
