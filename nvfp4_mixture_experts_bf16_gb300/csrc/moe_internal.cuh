@@ -207,11 +207,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   return out;
 }
 
-// E4M3 scale byte broadcast to both halves of an f16x2.
-__device__ __forceinline__ uint32_t e4m3_bcast_f16x2(uint32_t byte) {
-  return e4m3x2_to_f16x2(byte * 0x0101u);
-}
-
 // a * (low half of s), a * (high half of s): the half broadcast is an operand selector of the
 // f16x2 multiply, so two rows' scales share one conversion
 __device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t s) {
@@ -223,11 +218,6 @@ __device__ __forceinline__ uint32_t hmul2_hi(uint32_t a, uint32_t s) {
   const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
                             __high2half2(*reinterpret_cast<const __half2*>(&s)));
   return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
-  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
 }
 
 // Exact decoded values.
