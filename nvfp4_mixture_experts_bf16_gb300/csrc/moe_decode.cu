@@ -62,6 +62,8 @@ struct DcGeom {
   int xop;                      // x operand rows, later the h operand rows of one group
   int xsep;                     // one token: bytes of its own activation staging row (outside
                                 // the arena, so the first weight copies can start early)
+  int redbufs;                  // gate/up K-partial buffers: 2 when that still leaves two
+                                // gate/up stages, else 1 (and a barrier after each epilogue)
   int smax, gmax;               // slots T*k, groups min(T*k, E)
   int smem;
 };
@@ -280,8 +282,10 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* arena = smem;
   unsigned char* xop = arena + geo.arena;
-  float* red = reinterpret_cast<float*>(xop + geo.xop);                 // [8 warps][2][128]
-  DcGroup* grp = reinterpret_cast<DcGroup*>(red + kDcWarps * 2 * 128);
+  // [redbufs][8 warps][2][128]: with two buffers gate/up task q's K-partials go to buffer
+  // q % 2, so the next task's warps need not wait for this task's epilogue
+  float* red = reinterpret_cast<float*>(xop + geo.xop);
+  DcGroup* grp = reinterpret_cast<DcGroup*>(red + geo.redbufs * kDcWarps * 2 * 128);
   int32_t* sel_idx = reinterpret_cast<int32_t*>(grp + geo.gmax);        // [S]
   float* sel_w = reinterpret_cast<float*>(sel_idx + geo.smax);          // [S]
   int32_t* sel_slot = reinterpret_cast<int32_t*>(sel_w + geo.smax);     // [S]
@@ -779,7 +783,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         accu[i] += accu2[i];
       }
       // partial sums of the 8 warps -> shared memory; 128 threads each finish one h element
-      float* myred = red + (size_t)(warp * 2) * 128;
+      float* redq = red + (size_t)((q - q0) & (geo.redbufs - 1)) * (kDcWarps * 2 * 128);
+      float* myred = redq + (size_t)(warp * 2) * 128;
       *reinterpret_cast<float4*>(myred + lane * 4) =
           make_float4(accg[0], accg[1], accg[2], accg[3]);
       *reinterpret_cast<float4*>(myred + 128 + lane * 4) =
@@ -794,8 +799,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         float gs = 0.0f, us = 0.0f;
 #pragma unroll
         for (int w = 0; w < kDcWarps; ++w) {
-          gs += red[(size_t)(w * 2) * 128 + e_idx];
-          us += red[(size_t)(w * 2) * 128 + 128 + e_idx];
+          gs += redq[(size_t)(w * 2) * 128 + e_idx];
+          us += redq[(size_t)(w * 2) * 128 + 128 + e_idx];
         }
         const bool cvalid = col < n;
         const float xf = cvalid ? xfac_s[group_tok(gm.toks, col)] : 0.0f;
@@ -838,7 +843,10 @@ __global__ void __launch_bounds__(kDcThreads, 1)
           }
         }
       }
-      consumer_sync(kDcCons);
+      // with two buffers no barrier here: the next task's partials go to the other buffer,
+      // and its own partial barrier comes after this epilogue in every thread (the down phase
+      // starts with one)
+      if (geo.redbufs == 1) consumer_sync(kDcCons);
     }
   }
 
@@ -1106,8 +1114,14 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   g.xsep = T == 1 ? g.rs : 0;
   const int route_bytes = (g.rows_max + (g.xsep ? 0 : T)) * g.rs;
   const int scratch = T * k * 64 * 4;  // Y pairs of one tile for the combine
-  const int fixed = g.xop + kDcWarps * 2 * 128 * 4 + g.gmax * (int)sizeof(DcGroup) +
-                    g.smax * 20 + 8 + 8 * (2 * 3 + 2 * 16 + 2) + 16 + g.xsep + kDcStatic;
+  const int red1 = kDcWarps * 2 * 128 * 4;   // one K-partial buffer
+  int fixed = g.xop + red1 + g.gmax * (int)sizeof(DcGroup) + g.smax * 20 + 8 +
+              8 * (2 * 3 + 2 * 16 + 2) + 16 + g.xsep + kDcStatic;
+  g.redbufs = 1;
+  if ((kDcSmemMax - fixed - red1) / g.gu_stage >= 2) {
+    g.redbufs = 2;
+    fixed += red1;
+  }
   const int avail = kDcSmemMax - fixed;
   g.gu_stages = avail / g.gu_stage;
   if (g.gu_stages > 3) g.gu_stages = 3;
