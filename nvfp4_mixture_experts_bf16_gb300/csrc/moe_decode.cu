@@ -1002,21 +1002,34 @@ __global__ void __launch_bounds__(kDcThreads, 1)
           const int it2 = base + tid + u * kDcCons;
           if (have[u]) ysm[it2] = data_of(w[u]);
         }
-        // words that had not arrived yet: poll them one at a time (rare)
+        // words that had not arrived yet: poll all of them together (one round trip per pass,
+        // bounded)
         uint32_t late = 0;
 #pragma unroll
         for (int u = 0; u < 8; ++u) late |= (have[u] && tag_of(w[u]) != ep) ? 1u << u : 0u;
-#pragma unroll 1
-        for (int u = 0; u < 8; ++u) {
-          if (!(late & (1u << u))) continue;
-          const int it2 = base + tid + u * kDcCons;
-          unsigned long long w1[1];
-          if (!poll_tags<1>(ws.ytag + (size_t)sel_slot[it2 >> 6] * (H / 2) + ht * 64 +
-                                (it2 & 63), ep, w1)) {
-            record_status(ws.ctl, kStTimeout);
-            abort_s = 1;
+        if (late) {
+          const uint64_t t0 = globaltimer_ns();
+          while (late) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              if (late & (1u << u)) {
+                const int it2 = base + tid + u * kDcCons;
+                w[u] = ld_tag(ws.ytag + (size_t)sel_slot[it2 >> 6] * (H / 2) + ht * 64 + (it2 & 63));
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              if ((late & (1u << u)) && tag_of(w[u]) == ep) {
+                ysm[base + tid + u * kDcCons] = data_of(w[u]);
+                late &= ~(1u << u);
+              }
+            }
+            if (late && globaltimer_ns() - t0 > kWaitLimitNs) {
+              record_status(ws.ctl, kStTimeout);
+              abort_s = 1;
+              break;
+            }
           }
-          ysm[it2] = data_of(w1[0]);
         }
       }
       consumer_sync(kDcCons);
