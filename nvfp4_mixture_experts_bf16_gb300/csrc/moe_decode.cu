@@ -496,7 +496,9 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   if (T == 1) balanced_range(k * gu_tiles, q0, q1);
   // one token: the selecting warp issues the first gate/up stages itself, right after the
   // selection (the arena holds no staged activations then, and every router row is consumed)
-  const int npre = (T == 1 && geo.xsep) ? min((q1 - q0) * geo.nkc, geo.gu_stages) : 0;
+  // (the first stage only: the CTA's later stages follow once it has landed, so that every
+  // CTA's first stage gets the memory system before anyone's second)
+  const int npre = (T == 1 && geo.xsep && q1 > q0) ? 1 : 0;
 
   // copies of gate/up stage `chunk` = (task q, k-chunk kc) of expert e into its ring slot
   auto issue_gu = [&](int chunk, int q, int kc, int e) {
@@ -678,6 +680,13 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         if (chunk < npre) continue;   // issued by the selecting warp
         const int s = chunk % geo.gu_stages, n = chunk / geo.gu_stages;
         if (n > 0 && !mbar_wait(&gempty[s], (n - 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+          break;
+        }
+        // one token: the second task's stage waits for the first to land (its only completed
+        // phase)
+        if (npre > 0 && chunk == 1 && geo.nkc == 1 && !mbar_wait(&gfull[0], 0)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
           break;
