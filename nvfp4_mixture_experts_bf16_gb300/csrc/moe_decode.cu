@@ -267,10 +267,33 @@ __device__ __forceinline__ uint32_t bmax2_abs(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ int group_tok(uint32_t toks, int c) { return (toks >> (4 * c)) & 0xF; }
 
-// Contiguous share of ntasks for this CTA (ntasks * gridDim.x < 2^31 for every valid shape).
-__device__ __forceinline__ void balanced_range(int ntasks, int& q0, int& q1) {
-  q0 = (int)(((unsigned)ntasks * blockIdx.x) / gridDim.x);
-  q1 = (int)(((unsigned)ntasks * (blockIdx.x + 1)) / gridDim.x);
+// Work split of a call. Gate/up tasks in contiguous ranges, the CTAs with one task fewer first
+// (b < ns take R tasks, the others R + 1), so the first groups are computed entirely by CTAs
+// that finish early. Up to one down task per such CTA, from those groups, is done early by
+// them (while the other CTAs run their extra gate/up task); every other down task is spread
+// over all CTAs (balanced), after the CTA's early one.
+struct DcSplit {
+  int q0, q1;     // gate/up tasks
+  int de0, de1;   // early down tasks
+  int dl0, dl1;   // late down tasks
+};
+__device__ __forceinline__ DcSplit dc_split(int U, int gu_tiles, int dn_tiles) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const int NG = U * gu_tiles, ND = U * dn_tiles;
+  const int R = NG / G, Rx = NG % G, ns = G - Rx;
+  DcSplit sp;
+  sp.q0 = b < ns ? b * R : ns * R + (b - ns) * (R + 1);
+  sp.q1 = sp.q0 + (b < ns ? R : R + 1);
+  const int eg = Rx > 0 ? (ns * R) / gu_tiles : 0;   // groups whose tasks all lie on b < ns
+  const int NE = min(eg * dn_tiles, ns), NL = ND - NE;
+  sp.de0 = sp.de1 = 0;
+  if (b < ns && NE > 0) {
+    sp.de0 = (int)((long long)NE * b / ns);
+    sp.de1 = (int)((long long)NE * (b + 1) / ns);
+  }
+  sp.dl0 = NE + (int)((long long)NL * b / G);
+  sp.dl1 = NE + (int)((long long)NL * (b + 1) / G);
+  return sp;
 }
 
 template <int NT, int MODE>
@@ -493,7 +516,11 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   const int gu_tiles = I / 16, dn_tiles = H / kDnRows;
   // this CTA's gate/up tasks [q0, q1) (one token: U = k groups, known before the routing)
   int q0 = 0, q1 = 0;
-  if (T == 1) balanced_range(k * gu_tiles, q0, q1);
+  if (T == 1) {
+    const DcSplit sp1 = dc_split(k, gu_tiles, H / kDnRows);
+    q0 = sp1.q0;
+    q1 = sp1.q1;
+  }
   // one token: the selecting warp issues the first gate/up stages itself, right after the
   // selection (the arena holds no staged activations then, and every router row is consumed)
   // (the first stage only: the CTA's later stages follow once it has landed, so that every
@@ -666,9 +693,12 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   }
   // groups and selections are final from here on (one token: since the operand barrier)
 
-  int d0, d1;
-  balanced_range(U * gu_tiles, q0, q1);
-  balanced_range(U * dn_tiles, d0, d1);
+  const DcSplit sp = dc_split(U, gu_tiles, dn_tiles);
+  q0 = sp.q0;
+  q1 = sp.q1;
+  // this CTA's down tasks, early ones first: task i of nd is q = dq(i)
+  const int nde = sp.de1 - sp.de0, nd = nde + (sp.dl1 - sp.dl0);
+  auto dq = [&](int i) { return i < nde ? sp.de0 + i : sp.dl0 + (i - nde); };
 
   if (warp == kDcWarps) {
     // ---------------- producer: gate/up tasks, then this CTA's down tasks
@@ -705,7 +735,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     }
     const uint32_t code_bytes = (uint32_t)kDnRows * (I / 2);
     int dchunk = 0;
-    for (int q = d0; q < d1 && !abort_s; ++q, ++dchunk) {
+    for (int i = 0; i < nd && !abort_s; ++i, ++dchunk) {
+      const int q = dq(i);
       const int gi = q / dn_tiles, ht = q % dn_tiles;
       const int e = grp[gi].expert;
       const int s = dchunk % geo.dn_stages, n = dchunk / geo.dn_stages;
@@ -865,7 +896,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     const uint32_t code_bytes = (uint32_t)kDnRows * (I / 2);
     int cur = -1, dchunk = 0;
     float md = 0.0f;
-    for (int q = d0; q < d1; ++q, ++dchunk) {
+    for (int i = 0; i < nd; ++i, ++dchunk) {
+      const int q = dq(i);
       const int gi = q / dn_tiles, ht = q % dn_tiles;
       const DcGroup gm = grp[gi];
       const int slot0 = gm.slot0, n = gm.n;
