@@ -27,8 +27,10 @@
 //      streams this CTA's down weights into the same shared memory.
 //   4. down: tasks (group, 128-row tile of H); a task waits only for its own group's tagged h.
 //      Each task writes Y (BF16) as pairs of rows, plain and tagged.
-//   5. combine: CTA j (mod the grid) forms 128-row tile j of out once its tagged Y has arrived:
-//      the fixed-order weighted sum over each token's k experts (rank order, FP32, then BF16).
+//   5. combine: 128-row tile j of out is formed, once its tagged Y has arrived, by the j-th CTA
+//      in the order (late down tasks, CTA index), i.e. by CTAs done with their own down tasks
+//      first: the fixed-order weighted sum over each token's k experts (rank order, FP32, then
+//      BF16).
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -276,6 +278,8 @@ struct DcSplit {
   int q0, q1;     // gate/up tasks
   int de0, de1;   // early down tasks
   int dl0, dl1;   // late down tasks
+  int crank;      // rank in the order (late down tasks, b): the combine's tile order, so that
+                  // the CTAs that finish their down tasks first form the output tiles
 };
 __device__ __forceinline__ DcSplit dc_split(int U, int gu_tiles, int dn_tiles) {
   const int G = gridDim.x, b = blockIdx.x;
@@ -293,6 +297,10 @@ __device__ __forceinline__ DcSplit dc_split(int U, int gu_tiles, int dn_tiles) {
   }
   sp.dl0 = NE + (int)((long long)NL * b / G);
   sp.dl1 = NE + (int)((long long)NL * (b + 1) / G);
+  // L = NL / G late tasks for most CTAs, L + 1 for NL % G of them; among the CTAs before b,
+  // (dl0 - NE) - L * b have L + 1
+  const int L = NL / G, nlow = G - NL % G, hi_before = (sp.dl0 - NE) - L * b;
+  sp.crank = (sp.dl1 - sp.dl0 == L) ? b - hi_before : nlow + hi_before;
   return sp;
 }
 
@@ -1019,12 +1027,13 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     }
   }
 
-  // ---------------- 5. combine: 128-row tile ht of out is formed by CTA ht (mod the grid) once
+  // ---------------- 5. combine: 128-row tile ht of out is formed by the CTA of rank ht (mod
+  // the grid) in the order (late down tasks, b) once
   // all of its Y pairs carry this epoch: the fixed-order weighted sum over each token's k
   // experts (rank order, FP32, then BF16)
   {
     uint32_t* ysm = reinterpret_cast<uint32_t*>(arena);   // [T][k][64] BF16 pairs of the tile
-    for (int ht = b; ht < dn_tiles; ht += G) {
+    for (int ht = sp.crank; ht < dn_tiles; ht += G) {
       consumer_sync(kDcCons);
       // 8 pairs per thread in flight at a time: (selection sj, pair p2) = it2 + u * 256
       for (int base = 0; base < S * 64; base += 8 * kDcCons) {
