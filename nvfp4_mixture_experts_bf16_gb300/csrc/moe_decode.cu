@@ -918,7 +918,38 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         md = __ldg(&pk.mult[gm.expert * 3 + 2]);
         const float sd = mode == 1 ? __ldg(&pk.down_in_scale[gm.expert]) : 0.0f;
         const int nent = n * ntile;
-        for (int ent = tid; ent < nent; ent += kDcCons) {
+        if (mode == 0 && n == 1 && nent <= 32) {
+          // one slot with at most 32 blocks: warp 0 polls its blocks, takes the slot's max |h|
+          // by a warp reduction and converts in registers
+          if (warp == 0) {
+            unsigned long long w[9];
+            uint32_t am = 0u;
+            if (lane < nent) {
+              if (!poll_tags<9>(ws.htag + ((size_t)slot0 * ntile + lane) * 9, ep, w)) {
+                record_status(ws.ctl, kStTimeout);
+                abort_s = 1;
+              }
+              am = data_of(w[8]);
+            }
+            am = __reduce_max_sync(0xFFFFFFFFu, am);   // non-negative floats order as bits
+            const int sh = amax_shift(__uint_as_float(am));
+            const float f = pow2f(-sh);
+            if (lane == 0) hfac_s[0] = pow2f(sh);
+            if (lane < nent) {
+              uint32_t* dst = reinterpret_cast<uint32_t*>(xop) + lane * 8;
+#pragma unroll
+              for (int p2 = 0; p2 < 8; ++p2) {
+                const uint32_t v = data_of(w[p2]);
+                const __half2 hh = __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), f),
+                                                     __fmul_rn(__uint_as_float(v & 0xFFFF0000u), f));
+                dst[p2] = *reinterpret_cast<const uint32_t*>(&hh);
+              }
+            }
+          }
+          consumer_sync(kDcCons);
+          cur = gi;
+        }
+        for (int ent = tid; ent < nent && cur != gi; ent += kDcCons) {
           const int row = ent / ntile, it = ent % ntile;
           const unsigned long long* src = ws.htag + ((size_t)(slot0 + row) * ntile + it) * 9;
           unsigned long long w[9];
@@ -955,8 +986,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
             if (it == 0) hfac_s[row] = sd;
           }
         }
-        consumer_sync(kDcCons);
-        if (mode == 0) {
+        if (cur != gi) consumer_sync(kDcCons);
+        if (mode == 0 && cur != gi) {
           for (int ent = tid; ent < nent; ent += kDcCons) {
             const int row = ent / ntile, it = ent % ntile;
             const int sh = amax_shift(__uint_as_float(hamax_s[row]));
