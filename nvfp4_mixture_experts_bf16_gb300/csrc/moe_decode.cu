@@ -398,59 +398,64 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     // h = 0, 1 (and every 512 chunks further), so that a warp's loads are 512 contiguous bytes
     // (exact BF16 products, FP32 sums), then a butterfly over the warp. Also each token's
     // max |x| over the thread's chunks.
-    float acc[kDcWarps][NT];
     float am[NT];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      am[t] = 0.0f;
+    for (int t = 0; t < NT; ++t) am[t] = 0.0f;
+    // rows in groups of 4 (the CTA holds 3-4 rows at 512 experts): no work is issued for
+    // absent rows beyond the group; one pass at least, for the max |x| (a CTA may hold no row)
+    for (int r0 = 0; r0 < (nrows > 0 ? nrows : 1); r0 += 4) {
+      float acc[4][NT];
 #pragma unroll
-      for (int r = 0; r < kDcWarps; ++r) acc[r][t] = 0.0f;
-    }
-    for (int c8 = warp * 64 + lane; c8 < H / 8; c8 += kDcCons * 2) {
-      const int o0 = c8 * 16, o1 = (c8 + 32) * 16;   // byte offsets of the two chunks
-      const bool h1 = c8 + 32 < H / 8;                  // H % 512 != 0: a last half chunk
-      float xv[NT][16];
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const uint4 u0 = lds128(xraw + (size_t)t * geo.rs + o0);
-        const uint4 u1 = h1 ? lds128(xraw + (size_t)t * geo.rs + o1) : make_uint4(0, 0, 0, 0);
-        const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        uint32_t m2 = 0u;
+        for (int t = 0; t < NT; ++t) acc[r][t] = 0.0f;
+      for (int c8 = warp * 64 + lane; c8 < H / 8; c8 += kDcCons * 2) {
+        const int o0 = c8 * 16, o1 = (c8 + 32) * 16;   // byte offsets of the two chunks
+        const bool h1 = c8 + 32 < H / 8;                  // H % 512 != 0: a last half chunk
+        float xv[NT][16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          xv[t][2 * i] = bf16_lo(wd[i]);
-          xv[t][2 * i + 1] = bf16_hi(wd[i]);
-          m2 = bmax2_abs(m2, wd[i]);
-        }
-        am[t] = fmaxf(am[t], fmaxf(bf16_lo(m2), bf16_hi(m2)));
-      }
-#pragma unroll
-      for (int r = 0; r < kDcWarps; ++r) {
-        if (r < nrows) {
-          const uint4 u0 = lds128(wrs + (size_t)r * geo.rs + o0);
-          const uint4 u1 = h1 ? lds128(wrs + (size_t)r * geo.rs + o1) : make_uint4(0, 0, 0, 0);
+        for (int t = 0; t < NT; ++t) {
+          const uint4 u0 = lds128(xraw + (size_t)t * geo.rs + o0);
+          const uint4 u1 = h1 ? lds128(xraw + (size_t)t * geo.rs + o1) : make_uint4(0, 0, 0, 0);
           const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+          uint32_t m2 = 0u;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const float w0 = bf16_lo(wd[i]), w1 = bf16_hi(wd[i]);
+            xv[t][2 * i] = bf16_lo(wd[i]);
+            xv[t][2 * i + 1] = bf16_hi(wd[i]);
+            m2 = bmax2_abs(m2, wd[i]);
+          }
+          am[t] = fmaxf(am[t], fmaxf(bf16_lo(m2), bf16_hi(m2)));
+        }
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-              acc[r][t] = fmaf(w0, xv[t][2 * i], acc[r][t]);
-              acc[r][t] = fmaf(w1, xv[t][2 * i + 1], acc[r][t]);
+        for (int r = 0; r < 4; ++r) {
+          if (r0 + r < nrows) {
+            const unsigned char* wrow = wrs + (size_t)(r0 + r) * geo.rs;
+            const uint4 u0 = lds128(wrow + o0);
+            const uint4 u1 = h1 ? lds128(wrow + o1) : make_uint4(0, 0, 0, 0);
+            const uint32_t wd[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float w0 = bf16_lo(wd[i]), w1 = bf16_hi(wd[i]);
+#pragma unroll
+              for (int t = 0; t < NT; ++t) {
+                acc[r][t] = fmaf(w0, xv[t][2 * i], acc[r][t]);
+                acc[r][t] = fmaf(w1, xv[t][2 * i + 1], acc[r][t]);
+              }
             }
           }
         }
       }
-    }
 #pragma unroll
-    for (int r = 0; r < kDcWarps; ++r) {
-      if (r < nrows) {
+      for (int r = 0; r < 4; ++r) {
+        if (r0 + r < nrows) {
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          float v = acc[r][t];
+          for (int t = 0; t < NT; ++t) {
+            float v = acc[r][t];
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-          if (lane == 0) red[(warp * 8 + r) * 8 + t] = v;
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+            if (lane == 0) red[(warp * 8 + r0 + r) * 8 + t] = v;
+          }
         }
       }
     }
