@@ -151,10 +151,10 @@ __device__ __forceinline__ void warp_select_scratch(uint32_t (&key)[V], int k, i
   if (lane < C) {
     mine = cand[lane];
     r = 0;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {   // broadcast reads; entries >= C do not count
+#pragma unroll 4
+    for (int j = 0; j < (C + 1) >> 1; ++j) {   // broadcast reads; entries >= C do not count
       const ulonglong2 q = reinterpret_cast<const ulonglong2*>(cand)[j];
-      r += (2 * j < C && q.x > mine) + (2 * j + 1 < C && q.y > mine);
+      r += (q.x > mine) + (2 * j + 1 < C && q.y > mine);
     }
   }
   __syncwarp();
@@ -581,11 +581,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       // one token: its k experts are distinct, so every selection is a group of one, and
       // the slot of selection j is its rank by expert (k shuffles, no block barrier)
       int p = 0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int ej = __shfl_sync(0xFFFFFFFFu, e_sel, j);
-        p += (j < k) && (ej < e_sel);
-      }
+#pragma unroll 4
+      for (int j = 0; j < k; ++j) p += __shfl_sync(0xFFFFFFFFu, e_sel, j) < e_sel;
       if (lane < k) {
         sel_idx[lane] = e_sel;
         sel_w[lane] = w_sel;
