@@ -16,7 +16,8 @@ precision".
 Parity status: every function is pinned by ``tests/test_oracle_pins.py`` (exhaustive format
 decode against the closed-form definition, brute-force nearest rounding, numpy float32
 arithmetic, top-k invariants and closed forms, one-hot / identical-expert / SiLU(0) special
-cases and numpy float64 matmuls). The match of ``quantize_nvfp4`` to NVIDIA's own checkpoint
+cases and numpy float64 matmuls; the shared expert by equality with a routed expert of the same
+weights, scipy's logistic function and closed-form combines). The match of ``quantize_nvfp4`` to NVIDIA's own checkpoint
 quantiser is parity unpinned: no checkpoint is available.
 """
 from __future__ import annotations
@@ -115,6 +116,12 @@ def lib():
                 [ctypes.c_void_p] * 8 + [ctypes.c_int]
             L.oracle_moe_forward.restype = ctypes.c_int
             L.oracle_moe_forward.argtypes = [ctypes.POINTER(_Inputs), ctypes.POINTER(_Outputs)]
+            L.oracle_shared_expert.restype = None
+            L.oracle_shared_expert.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 3 + \
+                [ctypes.c_void_p] * 6 + [ctypes.c_int]
+            L.oracle_moe_forward_shared.restype = ctypes.c_int
+            L.oracle_moe_forward_shared.argtypes = [ctypes.POINTER(_Inputs), ctypes.c_int] + \
+                [ctypes.c_void_p] * 3 + [ctypes.POINTER(_Outputs)] + [ctypes.c_void_p] * 3
             _lib = L
     return _lib
 
@@ -249,11 +256,40 @@ class ExpertSet:
         self.in_scale[e] = in_scale
 
 
+class SharedExpert:
+    """The BF16 shared expert of a layer (uint16 bit patterns): ``gate_up`` [2*Is, H] (rows
+    0..Is-1 gate, Is..2*Is-1 up), ``down`` [H, Is] and the gate vector ``gate`` [H]."""
+
+    def __init__(self, gate_up: np.ndarray, down: np.ndarray, gate: np.ndarray):
+        self.gate_up = _c(gate_up, np.uint16)
+        self.down = _c(down, np.uint16)
+        self.gate = _c(gate, np.uint16).reshape(-1)
+        self.Is = self.gate_up.shape[0] // 2
+        H = self.gate.shape[0]
+        assert self.gate_up.shape == (2 * self.Is, H) and self.down.shape == (H, self.Is)
+
+
+def shared_expert(x_bf16: np.ndarray, shared: SharedExpert, nthreads: int = 1) -> dict:
+    """The shared expert alone: sigma [T] (the gate), hs_bf16 [T, Is] and ys [T, H] (BF16
+    values as float64)."""
+    x = _c(x_bf16, np.uint16)
+    T, H = x.shape
+    Is = shared.Is
+    sigma = np.empty(T, np.float64)
+    hs = np.empty((T, Is), np.uint16)
+    ys = np.empty((T, H), np.float64)
+    lib().oracle_shared_expert(_ptr(x), T, H, Is, _ptr(shared.gate_up), _ptr(shared.down),
+                               _ptr(shared.gate), _ptr(sigma), _ptr(hs), _ptr(ys), int(nthreads))
+    return dict(sigma=sigma, hs_bf16=hs, ys=ys)
+
+
 def forward(x_bf16: np.ndarray, wr_bf16: np.ndarray, experts: ExpertSet, k: int, mode: int,
             nthreads: int = 1, y_keep_fp64: bool = False, amb_eps: float = 2.0 ** -14,
             want=("out_bf16", "out64", "idx", "w", "perm", "counts", "offsets", "slot_of",
-                  "logits", "abssum")) -> dict:
-    """Run the oracle forward; ``want`` names the outputs to return (see moe_oracle.cpp)."""
+                  "logits", "abssum"), shared: SharedExpert | None = None) -> dict:
+    """Run the oracle forward; ``want`` names the outputs to return (see moe_oracle.cpp). With
+    ``shared``, the shared expert's gated output is added before the final rounding (out_bf16
+    and out64 include it) and sigma, hs_bf16 and ys are returned too."""
     x = _c(x_bf16, np.uint16)
     wr = _c(wr_bf16, np.uint16)
     T, H = x.shape
@@ -289,7 +325,17 @@ def forward(x_bf16: np.ndarray, wr_bf16: np.ndarray, experts: ExpertSet, k: int,
         shp, dt = shapes[name]
         res[name] = np.zeros(shp, dt)
     outs = _Outputs(*[_ptr(res.get(n)) for n in _OUT_FIELDS])
-    rc = lib().oracle_moe_forward(ctypes.byref(inp), ctypes.byref(outs))
+    if shared is None:
+        rc = lib().oracle_moe_forward(ctypes.byref(inp), ctypes.byref(outs))
+    else:
+        assert shared.gate.shape[0] == H
+        res["sigma"] = np.empty(T, np.float64)
+        res["hs_bf16"] = np.empty((T, shared.Is), np.uint16)
+        res["ys"] = np.empty((T, H), np.float64)
+        rc = lib().oracle_moe_forward_shared(
+            ctypes.byref(inp), shared.Is, _ptr(shared.gate_up), _ptr(shared.down),
+            _ptr(shared.gate), ctypes.byref(outs), _ptr(res["sigma"]), _ptr(res["hs_bf16"]),
+            _ptr(res["ys"]))
     if rc != 0:
-        raise ValueError(f"oracle_moe_forward failed with code {rc}")
+        raise ValueError(f"oracle forward failed with code {rc}")
     return res

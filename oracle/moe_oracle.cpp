@@ -568,6 +568,88 @@ int oracle_moe_forward(const OracleMoeInputs* in, OracleMoeOutputs* out) {
   return 0;
 }
 
+// ------------------------------- the shared expert
+// The model card "Qwen3.8-Flash-Next NVIDIA NVFP4 for Infernix (bit-exact)", section "What is
+// bit-exact and what is quantized", lists shared experts among the dense projections stored
+// BF16, and a shared-expert gate stored BF16 (the MTP drafter's bullet); it gives neither shape
+// nor formula. Reading taken: the Qwen-style shared expert, a dense SwiGLU expert of
+// intermediate size Is with BF16 weights, scaled per token by the sigmoid of a BF16 gate
+// vector's dot product with x, and added to the routed sum before the final rounding:
+//   a_t     = sum_h x[t][h] * gv[h]                                  (FP64; products exact)
+//   sigma_t = 1 / (1 + exp(-a_t))
+//   g_i     = sum_h x[t][h] * Wgu[i][h],  u_i = sum_h x[t][h] * Wgu[Is + i][h]
+//   hs_i    = BF16_RNE( silu(g_i) * u_i )              (as a routed expert's h in W4A16)
+//   Ys[t][r] = BF16_RNE( sum_i hs_i * Wd[r][i] )       (as a routed expert's Y)
+// The shared expert is BF16 in both modes: W4A4 concerns the NVFP4 routed experts only.
+// sigma [T], hs_bf16 [T][Is] and ys [T][H] are outputs (ys holds the BF16 values exactly).
+// Pinned by: equality with a routed expert whose dequantised weights are the shared weights,
+// the gate against scipy's logistic function, and closed-form combines.
+void oracle_shared_expert(const uint16_t* x, int T, int H, int Is, const uint16_t* gate_up,
+                          const uint16_t* down, const uint16_t* gate_vec, double* sigma,
+                          uint16_t* hs_bf16, double* ys, int nthreads) {
+  (void)nthreads;
+  std::vector<double> gv(H);
+  for (int hh = 0; hh < H; ++hh) gv[hh] = bf16_to_double(gate_vec[hh]);
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(static)
+#endif
+  for (int t = 0; t < T; ++t) {
+    std::vector<double> xt(H), hdec(Is);
+    for (int hh = 0; hh < H; ++hh) xt[hh] = bf16_to_double(x[(size_t)t * H + hh]);
+    double a = 0.0;
+    for (int hh = 0; hh < H; ++hh) a += xt[hh] * gv[hh];
+    sigma[t] = 1.0 / (1.0 + std::exp(-a));
+    for (int i = 0; i < Is; ++i) {
+      const uint16_t* wg = gate_up + (size_t)i * H;
+      const uint16_t* wu = gate_up + (size_t)(Is + i) * H;
+      double g = 0.0, u = 0.0;
+      for (int hh = 0; hh < H; ++hh) {
+        g += xt[hh] * bf16_to_double(wg[hh]);
+        u += xt[hh] * bf16_to_double(wu[hh]);
+      }
+      const uint16_t b = double_to_bf16(g / (1.0 + std::exp(-g)) * u);
+      hdec[i] = bf16_to_double(b);
+      if (hs_bf16) hs_bf16[(size_t)t * Is + i] = b;
+    }
+    for (int r = 0; r < H; ++r) {
+      const uint16_t* wd = down + (size_t)r * Is;
+      double y = 0.0;
+      for (int i = 0; i < Is; ++i) y += hdec[i] * bf16_to_double(wd[i]);
+      ys[(size_t)t * H + r] = bf16_to_double(double_to_bf16(y));
+    }
+  }
+}
+
+// The MoE step with the shared expert: the routed step of oracle_moe_forward, then
+//   out[t][r] = BF16_RNE( sum_{j=0..k-1} w[t][j] * Y_slot(t,j)[r] + sigma_t * Ys[t][r] ),
+// the shared term added after the routed ones. out->out64 (if given) receives the sum before
+// the rounding; the other outputs are those of oracle_moe_forward.
+// Pinned by: a zero shared down matrix reproduces the routed step, and k = 1 with every routed
+// expert equal to the shared one gives BF16((1 + sigma_t) * Y).
+int oracle_moe_forward_shared(const OracleMoeInputs* in, int Is, const uint16_t* gate_up,
+                              const uint16_t* down, const uint16_t* gate_vec,
+                              OracleMoeOutputs* out, double* sigma, uint16_t* hs_bf16,
+                              double* ys) {
+  if (Is <= 0 || !gate_up || !down || !gate_vec || !sigma || !ys) return 3;
+  const int T = in->T, H = in->H;
+  std::vector<double> routed((size_t)T * H);
+  double* keep = out->out64;
+  out->out64 = routed.data();
+  const int rc = oracle_moe_forward(in, out);
+  out->out64 = keep;
+  if (rc != 0) return rc;
+  oracle_shared_expert(in->x, T, H, Is, gate_up, down, gate_vec, sigma, hs_bf16, ys, in->nthreads);
+  for (int t = 0; t < T; ++t) {
+    for (int r = 0; r < H; ++r) {
+      const size_t o = (size_t)t * H + r;
+      const double acc = routed[o] + sigma[t] * ys[o];
+      out->out_bf16[o] = double_to_bf16(acc);
+      if (out->out64) out->out64[o] = acc;
+    }
+  }
+  return 0;
+}
+
 int oracle_abi_version(void) { return 1; }
 
 }  // extern "C"

@@ -20,6 +20,9 @@ intermediate 384 are the plainest reading consistent with its ~2.6 MiB per exper
 * ``verify8_w4a4``  T=8,    same, W4A4
 * ``prefill8192``   T=8192, same, W4A4 (and W4A16 for comparison), Zipf(1.1)
 
+Shared expert (optional): BF16 gate/up [2*Is, H], down [H, Is] and gate vector [H], all
+~ N(0, 0.02); the workloads take Is = I.
+
 Value recipe: activations BF16 ~ N(0, 1); router BF16 ~ N(0, 0.02); expert weights
 ~ N(0, 0.02) rounded to BF16 and then quantised (multiplier = global amax / (6*448), block scale
 = E4M3 of block amax / (6 * multiplier)). Zipf workloads add a per-layer expert bias through a
@@ -51,6 +54,7 @@ ROUTER_STD = 0.02
 
 # tensor ids for the stream keys
 _T_X, _T_ROUTER, _T_GATE, _T_UP, _T_DOWN, _T_CAL, _T_U, _T_PERM, _T_DSCALE = range(1, 10)
+_T_SH_GU, _T_SH_DOWN, _T_SH_GATE = range(10, 13)
 _WHICH = {"gate": _T_GATE, "up": _T_UP, "down": _T_DOWN}
 
 
@@ -167,6 +171,16 @@ def down_input_scales(seed: int, layer: int, E: int) -> np.ndarray:
     """float32 [E]: A_e / 2688 with A_e ~ U[DOWN_AMAX_LO, DOWN_AMAX_HI]."""
     a = stream(seed, layer, _T_DSCALE).uniform(DOWN_AMAX_LO, DOWN_AMAX_HI, E).astype(np.float32)
     return (a / np.float32(2688.0)).astype(np.float32)
+
+
+def shared_expert_weights(seed: int, layer: int, H: int, Is: int):
+    """The BF16 shared expert of a layer: gate_up [2*Is, H] (gate rows, then up rows), down
+    [H, Is] and the gate vector [H], each ~ N(0, 0.02) rounded to BF16."""
+    gu = stream(seed, layer, _T_SH_GU).standard_normal((2 * Is, H), dtype=np.float32)
+    dn = stream(seed, layer, _T_SH_DOWN).standard_normal((H, Is), dtype=np.float32)
+    gv = stream(seed, layer, _T_SH_GATE).standard_normal(H, dtype=np.float32)
+    sd = np.float32(WEIGHT_STD)
+    return bf16_bits(gu * sd), bf16_bits(dn * sd), bf16_bits(gv * sd)
 
 
 # ------------------------------------------------------------------ device-side draws

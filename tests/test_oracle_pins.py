@@ -424,3 +424,111 @@ def test_synth_streams_are_deterministic_and_independent():
     c = synth.expert_weight(0, 3, 8, "gate", 64, 32)
     assert np.array_equal(a, b) and not np.array_equal(a, c)
     assert synth.activations(0, 0, 4, 64).shape == (4, 64)
+
+
+# ------------------------------------------------------------------ shared expert
+def _exact_bf16_expert(seed, H, I, S=2.0 ** -12):
+    """An NVFP4 expert quantised with a power-of-two multiplier S, so that every dequantised
+    weight (code * E4M3 scale * S: at most 6 significant bits) is exactly a BF16 value; returns
+    the NVFP4 matrices and the BF16 bit patterns of the dequantised gate, up and down."""
+    mats, bf = [], []
+    for which in ("gate", "up", "down"):
+        w = synth.bf16_to_f32(synth.expert_weight(seed, 0, 0, which, H, I))
+        c, s = oracle.quantize_nvfp4(w, S)
+        d = oracle.dequantize_nvfp4(c, s, S)
+        b = synth.bf16_bits(d.astype(np.float32))
+        assert np.array_equal(synth.bf16_to_f32(b).astype(np.float64), d)   # exactly BF16
+        mats.append((c, s))
+        bf.append(b)
+    return mats, bf
+
+
+def test_shared_expert_equals_routed_expert_with_the_same_weights():
+    T, H, E, k, I = 5, 256, 4, 2, 64
+    x = synth.activations(41, 0, T, H)
+    wr = synth.router_weight(41, 0, E, H)
+    (g, u, d), (gb, ub, db) = _exact_bf16_expert(41, H, I)
+    ex = oracle.ExpertSet(E, H, I)
+    S = 2.0 ** -12
+    for e in range(E):
+        ex.set(e, g, u, d, (S, S, S))
+    routed = oracle.forward(x, wr, ex, k, oracle.W4A16, want=("y", "h_bf16", "slot_of"))
+    gv = synth.shared_expert_weights(41, 0, H, I)[2]
+    sh = oracle.shared_expert(x, oracle.SharedExpert(np.vstack([gb, ub]), db, gv))
+    for t in range(T):
+        for j in range(k):
+            s = routed["slot_of"][t, j]
+            assert np.array_equal(routed["y"][s], sh["ys"][t])
+            assert np.array_equal(routed["h_bf16"][s], sh["hs_bf16"][t])
+    # gate and up rows swapped: a different expert (SiLU is not symmetric in g and u)
+    sw = oracle.shared_expert(x, oracle.SharedExpert(np.vstack([ub, gb]), db, gv))
+    assert not np.array_equal(sw["ys"], sh["ys"])
+
+
+def test_shared_expert_matches_numpy_float64_pipeline():
+    T, H, Is = 3, 128, 64
+    x = synth.activations(42, 0, T, H)
+    gu, dn, gv = synth.shared_expert_weights(42, 0, H, Is)
+    sh = oracle.shared_expert(x, oracle.SharedExpert(gu, dn, gv))
+    xf = synth.bf16_to_f32(x).astype(np.float64)
+    W = synth.bf16_to_f32(gu).astype(np.float64)
+    Wd = synth.bf16_to_f32(dn).astype(np.float64)
+    g = xf @ W[:Is].T
+    u = xf @ W[Is:].T
+    h = g * (1 / (1 + np.exp(-g))) * u
+    hb = np.array([[oracle.double_to_bf16(v) for v in row] for row in h], np.uint16)
+    assert np.array_equal(hb, sh["hs_bf16"])
+    y = synth.bf16_to_f32(hb).astype(np.float64) @ Wd.T
+    yb = np.array([[oracle.double_to_bf16(v) for v in row] for row in y], np.uint16)
+    assert np.array_equal(synth.bf16_to_f32(yb).astype(np.float64), sh["ys"])
+
+
+def test_shared_gate_is_the_logistic_function():
+    from scipy.special import expit
+    T, H, Is = 6, 128, 64
+    x = synth.activations(43, 0, T, H)
+    gu, dn, gv = synth.shared_expert_weights(43, 0, H, Is)
+    gv = synth.bf16_bits(synth.bf16_to_f32(gv) * np.float32(8.0))   # a spread of gate values
+    sh = oracle.shared_expert(x, oracle.SharedExpert(gu, dn, gv))
+    a = synth.bf16_to_f32(x).astype(np.float64) @ synth.bf16_to_f32(gv).astype(np.float64)
+    assert a.min() < -1 and a.max() > 1
+    np.testing.assert_allclose(sh["sigma"], expit(a), rtol=1e-12, atol=0)
+    zero = oracle.shared_expert(x, oracle.SharedExpert(gu, dn, np.zeros(H, np.uint16)))
+    assert np.all(zero["sigma"] == 0.5)
+
+
+def test_shared_forward_zero_down_is_the_routed_step(tiny):
+    wl, x, wr, ex = tiny
+    gu, dn, gv = synth.shared_expert_weights(44, 0, wl.H, wl.I)
+    sh = oracle.SharedExpert(gu, np.zeros_like(dn), gv)
+    for mode in (oracle.W4A16, oracle.W4A4):
+        a = oracle.forward(x, wr, ex, wl.k, mode)
+        b = oracle.forward(x, wr, ex, wl.k, mode, shared=sh)
+        assert np.all(b["ys"] == 0)
+        assert np.array_equal(a["out_bf16"], b["out_bf16"])
+        assert np.array_equal(a["idx"], b["idx"]) and np.array_equal(a["out64"], b["out64"])
+
+
+def test_shared_forward_closed_form_with_k1_and_equal_experts():
+    # k = 1 and every routed expert equal to the shared one: out = BF16((1 + sigma_t) * Y_t)
+    T, H, E, I = 4, 256, 3, 64
+    x = synth.activations(45, 0, T, H)
+    wr = synth.router_weight(45, 0, E, H)
+    (g, u, d), (gb, ub, db) = _exact_bf16_expert(45, H, I)
+    ex = oracle.ExpertSet(E, H, I)
+    S = 2.0 ** -12
+    for e in range(E):
+        ex.set(e, g, u, d, (S, S, S))
+    for gv in (np.zeros(H, np.uint16), synth.shared_expert_weights(45, 0, H, I)[2]):
+        res = oracle.forward(x, wr, ex, 1, oracle.W4A16, want=("out64", "y", "slot_of"),
+                             shared=oracle.SharedExpert(np.vstack([gb, ub]), db, gv))
+        for t in range(T):
+            y = res["y"][res["slot_of"][t, 0]]
+            assert np.array_equal(y, res["ys"][t])
+            if not gv.any():
+                assert res["sigma"][t] == 0.5
+                assert np.array_equal(res["out64"][t], 1.5 * y)   # exact: y has 8 bits
+            np.testing.assert_allclose(res["out64"][t], (1 + res["sigma"][t]) * y, rtol=1e-15,
+                                       atol=0)
+            ob = np.array([oracle.double_to_bf16(v) for v in res["out64"][t]], np.uint16)
+            assert np.array_equal(ob, res["out_bf16"][t])
