@@ -118,10 +118,10 @@ def lib():
             L.oracle_moe_forward.argtypes = [ctypes.POINTER(_Inputs), ctypes.POINTER(_Outputs)]
             L.oracle_shared_expert.restype = None
             L.oracle_shared_expert.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 3 + \
-                [ctypes.c_void_p] * 6 + [ctypes.c_int]
+                [ctypes.c_void_p] * 7 + [ctypes.c_int]
             L.oracle_moe_forward_shared.restype = ctypes.c_int
             L.oracle_moe_forward_shared.argtypes = [ctypes.POINTER(_Inputs), ctypes.c_int] + \
-                [ctypes.c_void_p] * 3 + [ctypes.POINTER(_Outputs)] + [ctypes.c_void_p] * 3
+                [ctypes.c_void_p] * 3 + [ctypes.POINTER(_Outputs)] + [ctypes.c_void_p] * 4
             _lib = L
     return _lib
 
@@ -270,17 +270,19 @@ class SharedExpert:
 
 
 def shared_expert(x_bf16: np.ndarray, shared: SharedExpert, nthreads: int = 1) -> dict:
-    """The shared expert alone: sigma [T] (the gate), hs_bf16 [T, Is] and ys [T, H] (BF16
-    values as float64)."""
+    """The shared expert alone: sigma [T] (the gate), hs_bf16 [T, Is], h64 [T, Is] (h before
+    its BF16 rounding) and ys [T, H] (the down product, unrounded)."""
     x = _c(x_bf16, np.uint16)
     T, H = x.shape
     Is = shared.Is
     sigma = np.empty(T, np.float64)
     hs = np.empty((T, Is), np.uint16)
+    h64 = np.empty((T, Is), np.float64)
     ys = np.empty((T, H), np.float64)
     lib().oracle_shared_expert(_ptr(x), T, H, Is, _ptr(shared.gate_up), _ptr(shared.down),
-                               _ptr(shared.gate), _ptr(sigma), _ptr(hs), _ptr(ys), int(nthreads))
-    return dict(sigma=sigma, hs_bf16=hs, ys=ys)
+                               _ptr(shared.gate), _ptr(sigma), _ptr(hs), _ptr(ys), _ptr(h64),
+                               int(nthreads))
+    return dict(sigma=sigma, hs_bf16=hs, h64=h64, ys=ys)
 
 
 def forward(x_bf16: np.ndarray, wr_bf16: np.ndarray, experts: ExpertSet, k: int, mode: int,
@@ -289,7 +291,8 @@ def forward(x_bf16: np.ndarray, wr_bf16: np.ndarray, experts: ExpertSet, k: int,
                   "logits", "abssum"), shared: SharedExpert | None = None) -> dict:
     """Run the oracle forward; ``want`` names the outputs to return (see moe_oracle.cpp). With
     ``shared``, the shared expert's gated output is added before the final rounding (out_bf16
-    and out64 include it) and sigma, hs_bf16 and ys are returned too."""
+    and out64 include it) and sigma, hs_bf16, hs64 (h before its rounding) and ys (unrounded)
+    are returned too."""
     x = _c(x_bf16, np.uint16)
     wr = _c(wr_bf16, np.uint16)
     T, H = x.shape
@@ -331,11 +334,12 @@ def forward(x_bf16: np.ndarray, wr_bf16: np.ndarray, experts: ExpertSet, k: int,
         assert shared.gate.shape[0] == H
         res["sigma"] = np.empty(T, np.float64)
         res["hs_bf16"] = np.empty((T, shared.Is), np.uint16)
+        res["hs64"] = np.empty((T, shared.Is), np.float64)
         res["ys"] = np.empty((T, H), np.float64)
         rc = lib().oracle_moe_forward_shared(
             ctypes.byref(inp), shared.Is, _ptr(shared.gate_up), _ptr(shared.down),
             _ptr(shared.gate), ctypes.byref(outs), _ptr(res["sigma"]), _ptr(res["hs_bf16"]),
-            _ptr(res["ys"]))
+            _ptr(res["ys"]), _ptr(res["hs64"]))
     if rc != 0:
         raise ValueError(f"oracle forward failed with code {rc}")
     return res

@@ -579,14 +579,19 @@ int oracle_moe_forward(const OracleMoeInputs* in, OracleMoeOutputs* out) {
 //   sigma_t = 1 / (1 + exp(-a_t))
 //   g_i     = sum_h x[t][h] * Wgu[i][h],  u_i = sum_h x[t][h] * Wgu[Is + i][h]
 //   hs_i    = BF16_RNE( silu(g_i) * u_i )              (as a routed expert's h in W4A16)
-//   Ys[t][r] = BF16_RNE( sum_i hs_i * Wd[r][i] )       (as a routed expert's Y)
-// The shared expert is BF16 in both modes: W4A4 concerns the NVFP4 routed experts only.
-// sigma [T], hs_bf16 [T][Is] and ys [T][H] are outputs (ys holds the BF16 values exactly).
+//   Ys[t][r] = sum_i hs_i * Wd[r][i]                   (FP64, not rounded)
+// Ys enters the combine unrounded: the card fixes no rounding of the shared expert's output,
+// and the reading with the fewest roundings keeps it until the output's own rounding (a BF16
+// rounding here would turn the last-bit differences of any FP32 evaluation of h into whole
+// BF16 steps of Ys). The shared expert is BF16 in both modes: W4A4 concerns the NVFP4 routed
+// experts only. Outputs: sigma [T], hs_bf16 [T][Is], ys [T][H]; h64 [T][Is] (optional) is
+// silu(g)*u before the BF16 rounding.
 // Pinned by: equality with a routed expert whose dequantised weights are the shared weights,
-// the gate against scipy's logistic function, and closed-form combines.
+// a numpy float64 pipeline, the gate against scipy's logistic function, and closed-form
+// combines.
 void oracle_shared_expert(const uint16_t* x, int T, int H, int Is, const uint16_t* gate_up,
                           const uint16_t* down, const uint16_t* gate_vec, double* sigma,
-                          uint16_t* hs_bf16, double* ys, int nthreads) {
+                          uint16_t* hs_bf16, double* ys, double* h64, int nthreads) {
   (void)nthreads;
   std::vector<double> gv(H);
   for (int hh = 0; hh < H; ++hh) gv[hh] = bf16_to_double(gate_vec[hh]);
@@ -607,29 +612,32 @@ void oracle_shared_expert(const uint16_t* x, int T, int H, int Is, const uint16_
         g += xt[hh] * bf16_to_double(wg[hh]);
         u += xt[hh] * bf16_to_double(wu[hh]);
       }
-      const uint16_t b = double_to_bf16(g / (1.0 + std::exp(-g)) * u);
+      const double h = g / (1.0 + std::exp(-g)) * u;
+      const uint16_t b = double_to_bf16(h);
       hdec[i] = bf16_to_double(b);
       if (hs_bf16) hs_bf16[(size_t)t * Is + i] = b;
+      if (h64) h64[(size_t)t * Is + i] = h;
     }
     for (int r = 0; r < H; ++r) {
       const uint16_t* wd = down + (size_t)r * Is;
       double y = 0.0;
       for (int i = 0; i < Is; ++i) y += hdec[i] * bf16_to_double(wd[i]);
-      ys[(size_t)t * H + r] = bf16_to_double(double_to_bf16(y));
+      ys[(size_t)t * H + r] = y;
     }
   }
 }
 
 // The MoE step with the shared expert: the routed step of oracle_moe_forward, then
-//   out[t][r] = BF16_RNE( sum_{j=0..k-1} w[t][j] * Y_slot(t,j)[r] + sigma_t * Ys[t][r] ),
+//   out[t][r] = BF16_RNE( sum_{j=0..k-1} w[t][j] * Y_slot(t,j)[r] + sigma_t * Ys[t][r] )
+// (Y BF16 as in the routed step, Ys unrounded),
 // the shared term added after the routed ones. out->out64 (if given) receives the sum before
 // the rounding; the other outputs are those of oracle_moe_forward.
 // Pinned by: a zero shared down matrix reproduces the routed step, and k = 1 with every routed
-// expert equal to the shared one gives BF16((1 + sigma_t) * Y).
+// expert equal to the shared one (down rows exact in BF16 products) gives BF16((1 + sigma_t) Y).
 int oracle_moe_forward_shared(const OracleMoeInputs* in, int Is, const uint16_t* gate_up,
                               const uint16_t* down, const uint16_t* gate_vec,
                               OracleMoeOutputs* out, double* sigma, uint16_t* hs_bf16,
-                              double* ys) {
+                              double* ys, double* h64) {
   if (Is <= 0 || !gate_up || !down || !gate_vec || !sigma || !ys) return 3;
   const int T = in->T, H = in->H;
   std::vector<double> routed((size_t)T * H);
@@ -638,7 +646,8 @@ int oracle_moe_forward_shared(const OracleMoeInputs* in, int Is, const uint16_t*
   const int rc = oracle_moe_forward(in, out);
   out->out64 = keep;
   if (rc != 0) return rc;
-  oracle_shared_expert(in->x, T, H, Is, gate_up, down, gate_vec, sigma, hs_bf16, ys, in->nthreads);
+  oracle_shared_expert(in->x, T, H, Is, gate_up, down, gate_vec, sigma, hs_bf16, ys, h64,
+                       in->nthreads);
   for (int t = 0; t < T; ++t) {
     for (int r = 0; r < H; ++r) {
       const size_t o = (size_t)t * H + r;

@@ -455,10 +455,14 @@ def test_shared_expert_equals_routed_expert_with_the_same_weights():
     routed = oracle.forward(x, wr, ex, k, oracle.W4A16, want=("y", "h_bf16", "slot_of"))
     gv = synth.shared_expert_weights(41, 0, H, I)[2]
     sh = oracle.shared_expert(x, oracle.SharedExpert(np.vstack([gb, ub]), db, gv))
+    ys_b = np.array([[oracle.double_to_bf16(v) for v in row] for row in sh["ys"]], np.uint16)
+    hs_b = np.array([[oracle.double_to_bf16(v) for v in row] for row in sh["h64"]], np.uint16)
+    assert np.array_equal(hs_b, sh["hs_bf16"])
     for t in range(T):
         for j in range(k):
             s = routed["slot_of"][t, j]
-            assert np.array_equal(routed["y"][s], sh["ys"][t])
+            # the routed Y is the BF16 rounding of the same FP64 down product
+            assert np.array_equal(synth.bf16_bits(routed["y"][s].astype(np.float32)), ys_b[t])
             assert np.array_equal(routed["h_bf16"][s], sh["hs_bf16"][t])
     # gate and up rows swapped: a different expert (SiLU is not symmetric in g and u)
     sw = oracle.shared_expert(x, oracle.SharedExpert(np.vstack([ub, gb]), db, gv))
@@ -476,11 +480,11 @@ def test_shared_expert_matches_numpy_float64_pipeline():
     g = xf @ W[:Is].T
     u = xf @ W[Is:].T
     h = g * (1 / (1 + np.exp(-g))) * u
+    np.testing.assert_allclose(sh["h64"], h, rtol=1e-12, atol=1e-15)
     hb = np.array([[oracle.double_to_bf16(v) for v in row] for row in h], np.uint16)
     assert np.array_equal(hb, sh["hs_bf16"])
     y = synth.bf16_to_f32(hb).astype(np.float64) @ Wd.T
-    yb = np.array([[oracle.double_to_bf16(v) for v in row] for row in y], np.uint16)
-    assert np.array_equal(synth.bf16_to_f32(yb).astype(np.float64), sh["ys"])
+    np.testing.assert_allclose(sh["ys"], y, rtol=1e-12, atol=1e-15)
 
 
 def test_shared_gate_is_the_logistic_function():
@@ -510,15 +514,25 @@ def test_shared_forward_zero_down_is_the_routed_step(tiny):
 
 
 def test_shared_forward_closed_form_with_k1_and_equal_experts():
-    # k = 1 and every routed expert equal to the shared one: out = BF16((1 + sigma_t) * Y_t)
+    # k = 1 and every routed expert equal to the shared one, the down rows one-hot with weight
+    # 1/8, so that Y = Ys exactly (one exact product per row): out = BF16((1 + sigma_t) * Y_t)
     T, H, E, I = 4, 256, 3, 64
     x = synth.activations(45, 0, T, H)
     wr = synth.router_weight(45, 0, E, H)
-    (g, u, d), (gb, ub, db) = _exact_bf16_expert(45, H, I)
-    ex = oracle.ExpertSet(E, H, I)
+    (g, u, _), (gb, ub, _) = _exact_bf16_expert(45, H, I)
+    cols = np.random.default_rng(45).integers(0, I, H)
+    dc = np.zeros((H, I // 2), np.uint8)
+    for r in range(H):
+        dc[r, cols[r] // 2] |= 2 << (4 * (cols[r] % 2))          # E2M1 code 2 = 1.0
+    d = (dc, np.full((H, I // 16), 0x38, np.uint8))               # E4M3 0x38 = 1.0
     S = 2.0 ** -12
+    db = np.zeros((H, I), np.uint16)
+    db[np.arange(H), cols] = synth.bf16_bits(np.float32([0.125]))[0]
+    assert np.array_equal(oracle.dequantize_nvfp4(*d, 0.125),
+                          synth.bf16_to_f32(db).astype(np.float64))
+    ex = oracle.ExpertSet(E, H, I)
     for e in range(E):
-        ex.set(e, g, u, d, (S, S, S))
+        ex.set(e, g, u, d, (S, S, 0.125))
     for gv in (np.zeros(H, np.uint16), synth.shared_expert_weights(45, 0, H, I)[2]):
         res = oracle.forward(x, wr, ex, 1, oracle.W4A16, want=("out64", "y", "slot_of"),
                              shared=oracle.SharedExpert(np.vstack([gb, ub]), db, gv))
