@@ -226,8 +226,9 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------ native arm
 class Layer:
-    def __init__(self, x, wr, pack, U):
+    def __init__(self, x, wr, pack, U, shared=None):
         self.x, self.wr, self.pack, self.U = x, wr, pack, U
+        self.shared = shared   # (gate_up, down, gate) BF16 tensors of the shared expert, or None
 
 
 def quantized_experts(seed, layer, E, H, I, device):
@@ -253,6 +254,18 @@ def quantized_experts(seed, layer, E, H, I, device):
 def dev_bf16(u16, device):
     import torch
     return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def with_shared(stack, wl, seed, device):
+    """The same layers, each with its own BF16 shared expert of intermediate size I."""
+    return [Layer(L.x, L.wr, L.pack, L.U,
+                  synth.torch_shared_expert_weights(seed, l, wl.H, wl.I, device))
+            for l, L in enumerate(stack)]
+
+
+def bytes_shared(H, Is):
+    """BF16 bytes of one shared expert: gate/up, down and the gate vector."""
+    return 2 * (2 * Is * H + H * Is + H)
 
 
 def build_stack(wl, layers, seed, device, packs=None):
@@ -288,14 +301,21 @@ def measure(wl, stack, steps, warmup, use_graph, device, clocks=None):
     import torch
     import nvfp4_mixture_experts_bf16_gb300 as moe
     s = torch.cuda.Stream(device=device)
-    ws = moe.new_workspace(moe.moe_workspace_size(stack[0].pack, wl.T, wl.k, wl.mode), device)
+    sh = stack[0].shared
+    nws = (moe.moe_workspace_size(stack[0].pack, wl.T, wl.k, wl.mode) if sh is None else
+           moe.moe_workspace_size_shared(stack[0].pack, wl.T, wl.k, wl.mode, sh[0].shape[0] // 2))
+    ws = moe.new_workspace(nws, device)
     outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in stack]
     launches = [0]
 
     def step():
         n = 0
         for L, o in zip(stack, outs):
-            moe.moe_forward(L.x, L.wr, L.pack, wl.k, wl.mode, out=o, ws=ws, stream=s)
+            if L.shared is None:
+                moe.moe_forward(L.x, L.wr, L.pack, wl.k, wl.mode, out=o, ws=ws, stream=s)
+            else:
+                moe.moe_forward_shared(L.x, L.wr, L.pack, L.shared, wl.k, wl.mode, out=o, ws=ws,
+                                       stream=s)
             n += moe.moe_last_launch_count()
         launches[0] = n
 
@@ -461,18 +481,38 @@ def run_native(args, rank, world, local_rank):
                                unique_experts=round(U2, 2),
                                hbm_gbs=round(b2 / (ms2 / layers * 1e-3) / 1e9, 1),
                                frac_hbm=round(b2 / (ms2 / layers * 1e-3) / 1e9 / pk["hbm"], 4))
-        for mode in (1, 0):
+        if wl.name == "decode1" and wl.T == 1:
+            # the same layers with a BF16 shared expert each (Is = I): two extra launches
+            st4 = with_shared(stack, wl, args.seed, device)
+            ms4, n4, _, _ = measure(wl, st4, max(3, args.steps // 2), 3, not args.no_graph, device)
+            b4 = layer_bytes + bytes_shared(wl.H, wl.I)
+            extra["decode1_shared"] = dict(
+                tokens_per_s=round(wl.T * layers / (ms4 / 1e3), 1),
+                us_per_layer=round(ms4 / layers * 1e3, 2), launches_per_layer=n4 // layers,
+                hbm_gbs=round(b4 / (ms4 / layers * 1e-3) / 1e9, 1),
+                frac_hbm=round(b4 / (ms4 / layers * 1e-3) / 1e9 / pk["hbm"], 4),
+                note="routed experts' bytes + the shared expert's BF16 bytes per layer time")
+            del st4
+        for mode, shared in ((1, False), (0, False), (1, True)):
             name = "prefill8192"
             w3 = synth.Workload(name, 8192, wl.H, wl.E, wl.k, wl.I, mode, 1, True)
             st3 = build_stack(w3, 1, args.seed, device, packs=packs[:1])
+            if shared:
+                st3 = with_shared(st3, w3, args.seed, device)
             ms3, _, _, _ = measure(w3, st3, 3, 2, False, device)
             flops = 2 * w3.T * w3.k * 3 * w3.I * w3.H
-            extra[f"prefill8192_{['w4a16', 'w4a4'][mode]}"] = dict(
+            key = f"prefill8192_{['w4a16', 'w4a4'][mode]}" + ("_shared" if shared else "")
+            extra[key] = dict(
                 tokens_per_s=round(w3.T / (ms3 / 1e3), 1), ms=round(ms3, 3),
                 expert_tflops=round(flops / (ms3 * 1e-3) / 1e12, 2),
                 note=("tcgen05 block-scaled FP4 grouped GEMMs" if mode == 1 else
                       "tcgen05 kind::f16 grouped GEMMs, weights dequantised to f16 in shared "
                       "memory"))
+            if shared:
+                sflops = 2 * w3.T * 3 * w3.I * w3.H
+                extra[key].update(shared_tflop=round(sflops / 1e12, 4), note=(
+                    "as prefill8192_w4a4, plus the BF16 shared expert (Is = I) on two tcgen05 "
+                    "BF16 GEMMs; expert_tflops counts the routed FLOPs only"))
         torch.cuda.synchronize()
 
     cpu = None

@@ -149,6 +149,37 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
                        int T, int k, moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
                        void* stream);
 
+/* The shared expert of a layer (model card "Qwen3.8-Flash-Next NVIDIA NVFP4 for Infernix
+ * (bit-exact)", section "What is bit-exact and what is quantized": shared experts and the
+ * shared-expert gate are stored BF16; the card gives no formula, and the Qwen-style form is
+ * taken). All pointers are caller-owned device memory, 16-byte aligned, BF16 bit patterns:
+ *   gate_up [2*inter][hidden]: rows 0..inter-1 are the gate projection, inter..2*inter-1 up;
+ *   down    [hidden][inter];
+ *   gate    [hidden]: the gate vector; the token's weight is sigma_t = 1/(1 + exp(-x_t . gate)).
+ * 64 <= inter <= 2048, inter % 64 == 0. The shared expert is BF16 in both modes. */
+typedef struct {
+  const uint16_t* gate_up;
+  const uint16_t* down;
+  const uint16_t* gate;
+  int inter;
+} moe_shared_expert;
+
+/* Workspace bytes moe_forward_shared needs (same zero-fill rule as moe_workspace_size). */
+moe_status moe_workspace_size_shared(const moe_expert_pack* pack, int T, int k, moe_mode mode,
+                                     int shared_inter, size_t* bytes);
+
+/* moe_forward plus the shared expert: for token t,
+ *   hs  = BF16( SiLU(Wg x_t) * (Wu x_t) ),   Ys = Wd hs   (FP32 accumulation, not rounded),
+ *   out[t] = BF16( sum_j w_j * Y_j  +  sigma_t * Ys ),  the shared term added after the routed
+ * ones in FP32. Arguments and requirements are those of moe_forward, plus `shared` (above);
+ * a null or invalid `shared` returns MOE_ERR_INVALID_ARG. The shared expert runs first, as two
+ * CUDA-core GEMV kernels for T <= 8 and as two tcgen05 BF16 GEMMs with a per-token kernel
+ * between them for larger T. ws/ws_bytes: see moe_workspace_size_shared. */
+moe_status moe_forward_shared(const uint16_t* x, const uint16_t* router_w,
+                              const moe_expert_pack* pack, const moe_shared_expert* shared, int T,
+                              int k, moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
+                              void* stream);
+
 /* Byte offsets inside a moe_forward workspace of intermediate results, for tests:
  * the per-call routing tables and the quantised activations and h of the last call. */
 typedef struct {
@@ -169,6 +200,13 @@ typedef struct {
 moe_status moe_workspace_offsets(const moe_expert_pack* pack, int T, int k, moe_mode mode,
                                  moe_ws_offsets* offsets);
 
+/* Byte offsets inside a moe_forward_shared workspace of the shared expert's intermediate
+ * results, for tests: h (uint16 BF16 [T][inter]), sigma (float [T]) and Y (float [T][hidden],
+ * before its BF16 rounding). The routed results sit at the offsets moe_workspace_offsets gives.
+ * Any output pointer may be null. */
+moe_status moe_workspace_offsets_shared(const moe_expert_pack* pack, int T, int k, moe_mode mode,
+                                        int shared_inter, size_t* h, size_t* sigma, size_t* y);
+
 /* NVFP4 quantiser Q (test hook, also usable to build checkpoints): rows x cols BF16 values
  * (device, cols % 16 == 0) -> codes [rows][cols/2] and E4M3 scales [rows][cols/16] (device),
  * with per-matrix FP32 scale S = input_scale (> 0, finite). Steps, per 16-element block:
@@ -185,12 +223,14 @@ moe_status moe_read_device_status(void* ws, void* stream, moe_status* status);
 /* Human-readable name of a status code (static storage). */
 const char* moe_status_string(moe_status status);
 
-/* Number of CUDA kernels the last moe_forward call on this host thread launched. */
+/* Number of CUDA kernels the last moe_forward / moe_forward_shared call on this host thread
+ * launched. */
 int moe_last_launch_count(void);
 
 /* Profiling hook (measurement only; not needed for computing): for the NEXT moe_forward call
  * on this host thread, record cudaEvent_t events[2i] before and events[2i+1] after stage i on
- * the call's stream, stage 0 = routing and activation preparation, 1 = gate/up + SiLU*up,
+ * the call's stream, stage 0 = routing and activation preparation (and the shared expert of
+ * moe_forward_shared), 1 = gate/up + SiLU*up,
  * 2 = down, 3 = combine (count <= 8 uses the first count/2 stages). While profiling, the
  * stages are not overlapped by programmatic dependent launch. count = 0 cancels. */
 moe_status moe_profile_next_forward(void* const* events, int count);

@@ -27,7 +27,8 @@ EXPORTED = ["moe_pack_nvfp4", "moe_pack_destroy", "moe_pack_info", "moe_pack_get
             "moe_workspace_size", "moe_route_workspace_size", "moe_route_topk", "moe_forward",
             "moe_workspace_offsets", "moe_quantize_act_nvfp4", "moe_read_device_status",
             "moe_status_string", "moe_last_launch_count", "moe_profile_next_forward",
-            "moe_route_topk_noalloc"]
+            "moe_route_topk_noalloc", "moe_workspace_size_shared", "moe_forward_shared",
+            "moe_workspace_offsets_shared"]
 
 
 class MoeError(RuntimeError):
@@ -39,6 +40,11 @@ class MoeError(RuntimeError):
 class _Matrix(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("multiplier", ctypes.c_float), ("input_scale", ctypes.c_float)]
+
+
+class _SharedExpert(ctypes.Structure):
+    _fields_ = [("gate_up", ctypes.c_void_p), ("down", ctypes.c_void_p),
+                ("gate", ctypes.c_void_p), ("inter", ctypes.c_int)]
 
 
 class _WsOffsets(ctypes.Structure):
@@ -85,6 +91,12 @@ def lib() -> ctypes.CDLL:
             L.moe_last_launch_count.argtypes = []
             L.moe_profile_next_forward.argtypes = [vp, i32]
             L.moe_route_topk_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+            L.moe_workspace_size_shared.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
+            L.moe_forward_shared.argtypes = [vp, vp, vp, ctypes.POINTER(_SharedExpert), i32, i32,
+                                             i32, vp, vp, sz, vp]
+            L.moe_workspace_offsets_shared.argtypes = [vp, i32, i32, i32, i32,
+                                                       ctypes.POINTER(sz), ctypes.POINTER(sz),
+                                                       ctypes.POINTER(sz)]
             for n in EXPORTED:
                 if n not in ("moe_status_string",):
                     getattr(L, n).restype = ctypes.c_int
@@ -248,6 +260,40 @@ def moe_forward(x, router_w, pack: Pack, k: int, mode: int, out=None, ws=None, s
         ws = new_workspace(moe_workspace_size(pack, T, k, mode), x.device)
     _check("moe_forward", lib().moe_forward(_bits(x), _bits(router_w), pack.handle, T, k, mode,
                                             _bits(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def moe_workspace_size_shared(pack: Pack, T: int, k: int, mode: int, shared_inter: int) -> int:
+    n = ctypes.c_size_t()
+    _check("moe_workspace_size_shared", lib().moe_workspace_size_shared(
+        pack.handle, T, k, mode, shared_inter, ctypes.byref(n)))
+    return n.value
+
+
+def moe_workspace_offsets_shared(pack: Pack, T: int, k: int, mode: int,
+                                 shared_inter: int) -> dict:
+    h, sg, y = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check("moe_workspace_offsets_shared", lib().moe_workspace_offsets_shared(
+        pack.handle, T, k, mode, shared_inter, ctypes.byref(h), ctypes.byref(sg), ctypes.byref(y)))
+    return dict(h=h.value, sigma=sg.value, y=y.value)
+
+
+def moe_forward_shared(x, router_w, pack: Pack, shared, k: int, mode: int, out=None, ws=None,
+                       stream=None):
+    """moe_forward plus the shared expert; ``shared`` = (gate_up [2*Is, H], down [H, Is],
+    gate [H]) BF16 CUDA tensors."""
+    import torch
+    gate_up, down, gate = shared
+    T, H = x.shape
+    Is = gate_up.shape[0] // 2
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = new_workspace(moe_workspace_size_shared(pack, T, k, mode, Is), x.device)
+    sh = _SharedExpert(_bits(gate_up).value, _bits(down).value, _bits(gate).value, Is)
+    _check("moe_forward_shared", lib().moe_forward_shared(
+        _bits(x), _bits(router_w), pack.handle, ctypes.byref(sh), T, k, mode, _bits(out),
+        _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

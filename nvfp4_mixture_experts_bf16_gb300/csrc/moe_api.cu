@@ -67,13 +67,14 @@ int num_sms_of_current_device() {
 struct WsLayout {
   size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm,
       chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, htag, ytag, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
-      xsf_atoms, hq_perm, hsf_atoms, xh_perm, hf_perm, total;
+      xsf_atoms, hq_perm, hsf_atoms, xh_perm, hf_perm, sh_hs, sh_sigma, sh_y, sh_gu, total;
   size_t slot_amax_bytes;
   int G, NT;
 };
 
-// mode: 0 W4A16, 1 W4A4, -1 routing only (no expert buffers).
-WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
+// mode: 0 W4A16, 1 W4A4, -1 routing only (no expert buffers). Is > 0 adds the shared
+// expert's buffers after everything else, so the other offsets do not depend on it.
+WsLayout ws_layout(int T, int H, int E, int k, int I, int mode, int Is = 0) {
   WsLayout L;
   const long long S = (long long)T * k;
   L.G = (int)((S + moe::kGroup - 1) / moe::kGroup + (S < E ? S : E));
@@ -118,6 +119,10 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode) {
   L.hsf_atoms = take(w4a4 ? (size_t)L.NT * (I / 64 > 0 ? I / 64 : 1) * 512 : 0);
   L.xh_perm = take(w4a16 ? P * H * 2 : 0);
   L.hf_perm = take(w4a16 ? P * I * 2 : 0);
+  L.sh_hs = take(Is > 0 ? (size_t)T * Is * 2 : 0);
+  L.sh_sigma = take(Is > 0 ? (size_t)T * 4 : 0);
+  L.sh_y = take(Is > 0 ? (size_t)T * H * 4 : 0);
+  L.sh_gu = take(Is > 0 && !narrow ? (size_t)T * 2 * Is * 4 : 0);
   L.total = o;
   return L;
 }
@@ -158,6 +163,8 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   v.hsf_atoms = b + L.hsf_atoms;
   v.xh_perm = reinterpret_cast<__half*>(b + L.xh_perm);
   v.hf_perm = reinterpret_cast<__half*>(b + L.hf_perm);
+  v.sh_y = nullptr;
+  v.sh_sigma = nullptr;
   return v;
 }
 
@@ -398,9 +405,20 @@ moe_status moe_route_topk(const uint16_t* x, const uint16_t* router_w, int T, in
   return from_cuda(e);
 }
 
-moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_expert_pack* pack,
-                       int T, int k, moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
-                       void* stream) {
+}  // extern "C"
+
+namespace {
+
+bool shared_ok(const moe_shared_expert* sh, int H) {
+  return sh && sh->gate_up && sh->down && sh->gate && aligned16(sh->gate_up) &&
+         aligned16(sh->down) && aligned16(sh->gate) && sh->inter >= 64 && sh->inter % 64 == 0 &&
+         sh->inter <= 2048 && H % 64 == 0;
+}
+
+// moe_forward, optionally with the shared expert (validated by the caller).
+moe_status forward_impl(const uint16_t* x, const uint16_t* router_w, const moe_expert_pack* pack,
+                        const moe_shared_expert* sh, int T, int k, moe_mode mode, uint16_t* out,
+                        void* ws, size_t ws_bytes, void* stream) {
   g_last_launches = 0;
   if (!x || !router_w || !pack || !out || !ws) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(out) || !aligned16(ws))
@@ -411,24 +429,42 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
   if (reinterpret_cast<const void*>(out) == reinterpret_cast<const void*>(x))
     return MOE_ERR_INVALID_ARG;
   if (mode == MOE_W4A4 && !pack->x_scale_uniform) return MOE_ERR_UNSUPPORTED;
-  const WsLayout L = ws_layout(T, H, E, k, I, (int)mode);
+  const bool narrow = T <= moe::kNarrowT;
+  if (sh && !narrow && !moe::tc_supported()) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(T, H, E, k, I, (int)mode, sh ? sh->inter : 0);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   moe::WsView v = ws_view(ws, L, T, H, E, k, I);
   moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
   const int m = (int)mode;
-  const bool narrow = T <= moe::kNarrowT;
   cudaError_t e;
   int n = 0;
-  // stage i of the profile covers: 0 routing (+ activation prep), 1 gate/up, 2 down, 3 combine
+  // stage i of the profile covers: 0 routing (+ activation prep, + the shared expert),
+  // 1 gate/up, 2 down, 3 combine
   if (g_prof_count) lc.pdl = false;
   e = prof_mark(lc.stream, 0);
+  if (sh && e == cudaSuccess) {
+    // the shared expert first: the combine (of whichever path runs) adds its term
+    unsigned char* b = static_cast<unsigned char*>(ws);
+    moe::ShView sv;
+    sv.gate_up = sh->gate_up;
+    sv.down = sh->down;
+    sv.gate = sh->gate;
+    sv.hs = reinterpret_cast<uint16_t*>(b + L.sh_hs);
+    sv.sigma = reinterpret_cast<float*>(b + L.sh_sigma);
+    sv.ys = reinterpret_cast<float*>(b + L.sh_y);
+    sv.gu = reinterpret_cast<float*>(b + L.sh_gu);
+    sv.Is = sh->inter;
+    e = moe::launch_shared(lc, x, sv, v, &n);
+    v.sh_y = sv.ys;
+    v.sh_sigma = sv.sigma;
+  }
   if (narrow && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
-    // the whole step in one persistent kernel; the profile's later stages are empty
+    // the whole routed step in one persistent kernel; the profile's later stages are empty
     if (e == cudaSuccess)
       e = moe::launch_decode(lc, pack->view, v, m, pack->x_scale, pack->x_inv6S, x, router_w, out);
     for (int i = 1; i < 8 && e == cudaSuccess; ++i) e = prof_mark(lc.stream, i);
     g_prof_count = 0;
-    g_last_launches = 1;
+    g_last_launches = n + 1;
     return from_cuda(e);
   }
   if (narrow) {
@@ -487,6 +523,47 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
   g_prof_count = 0;
   g_last_launches = n;
   return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_expert_pack* pack,
+                       int T, int k, moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
+                       void* stream) {
+  return forward_impl(x, router_w, pack, nullptr, T, k, mode, out, ws, ws_bytes, stream);
+}
+
+moe_status moe_workspace_size_shared(const moe_expert_pack* pack, int T, int k, moe_mode mode,
+                                     int shared_inter, size_t* bytes) {
+  if (!pack || !bytes || (mode != MOE_W4A16 && mode != MOE_W4A4) ||
+      !route_shape_ok(T, pack->H, pack->E, k) || shared_inter < 64 || shared_inter % 64 ||
+      shared_inter > 2048)
+    return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(T, pack->H, pack->E, k, pack->I, (int)mode, shared_inter).total;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_offsets_shared(const moe_expert_pack* pack, int T, int k, moe_mode mode,
+                                        int shared_inter, size_t* h, size_t* sigma, size_t* y) {
+  size_t bytes = 0;
+  const moe_status st = moe_workspace_size_shared(pack, T, k, mode, shared_inter, &bytes);
+  if (st != MOE_OK) return st;
+  const WsLayout L = ws_layout(T, pack->H, pack->E, k, pack->I, (int)mode, shared_inter);
+  if (h) *h = L.sh_hs;
+  if (sigma) *sigma = L.sh_sigma;
+  if (y) *y = L.sh_y;
+  return MOE_OK;
+}
+
+moe_status moe_forward_shared(const uint16_t* x, const uint16_t* router_w,
+                              const moe_expert_pack* pack, const moe_shared_expert* shared, int T,
+                              int k, moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
+                              void* stream) {
+  g_last_launches = 0;
+  if (!pack || !shared_ok(shared, pack->H)) return MOE_ERR_INVALID_ARG;
+  return forward_impl(x, router_w, pack, shared, T, k, mode, out, ws, ws_bytes, stream);
 }
 
 moe_status moe_quantize_act_nvfp4(const uint16_t* x, int rows, int cols, float input_scale,

@@ -83,7 +83,23 @@ struct WsView {
   uint8_t* hsf_atoms;  // [NT][I/64][512]
   __half* xh_perm;     // W4A16 grouped path: [128*NT][H] f16(x * 2^-s) by pslot
   __half* hf_perm;     // W4A16 grouped path: [128*NT][I] f16(h * 2^-s) by pslot
+  // shared expert (null when the call has none): its FP32 output before the BF16 rounding and
+  // its gate, read by the combines
+  const float* sh_y;      // [T][H]
+  const float* sh_sigma;  // [T]
   int T, H, E, k, I, G, NT;
+};
+
+// The shared expert of a call: caller-owned BF16 weights and workspace buffers.
+struct ShView {
+  const uint16_t* gate_up;  // [2 Is][H]: gate rows, then up rows
+  const uint16_t* down;     // [H][Is]
+  const uint16_t* gate;     // [H] gate vector
+  uint16_t* hs;             // [T][Is] BF16 h
+  float* sigma;             // [T]
+  float* ys;                // [T][H] FP32
+  float* gu;                // [T][2 Is] FP32 gate/up products (wide calls)
+  int Is;
 };
 
 // ------------------------------------------------------------------ pack view
@@ -539,6 +555,11 @@ cudaError_t launch_tc_router(const LaunchCfg& lc, const uint16_t* x, const uint1
 cudaError_t launch_unpack_scales(cudaStream_t s, const uint8_t* gu_scales,
                                  const uint8_t* down_scales, int E, int H, int I, int expert,
                                  int which, uint8_t* raw_out);
+
+// The shared expert (BF16 SwiGLU with a sigmoid gate): h, the gate and the FP32 output for the
+// combine; narrow calls on CUDA-core GEMVs, wide calls on the tcgen05 BF16 GEMM.
+cudaError_t launch_shared(const LaunchCfg& lc, const uint16_t* x, const ShView& sv,
+                          const WsView& ws, int* launches);
 
 // Dynamic shared memory the expert kernels need (host side, for validation).
 size_t gateup_smem_bytes(int H, bool x_resident, int T);

@@ -198,6 +198,19 @@ def torch_expert_weights(seed: int, layer: int, which: str, E: int, H: int, I: i
     return (w * WEIGHT_STD).to(torch.bfloat16)
 
 
+def torch_shared_expert_weights(seed: int, layer: int, H: int, Is: int, device):
+    """The shared expert's BF16 weights (gate_up [2*Is, H], down [H, Is], gate [H]) drawn on
+    ``device`` with seeded torch generators (the full-size workloads' stream)."""
+    import torch
+    out = []
+    for tid, shape in ((_T_SH_GU, (2 * Is, H)), (_T_SH_DOWN, (H, Is)), (_T_SH_GATE, (H,))):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(torch_seed(seed, layer, tid))
+        w = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+        out.append((w * WEIGHT_STD).to(torch.bfloat16))
+    return tuple(out)
+
+
 def describe() -> str:
     return ("seeded synthetic: x~N(0,1) BF16, router~N(0,0.02) BF16, experts~N(0,0.02)->BF16"
             "->NVFP4; Zipf(1.1) bias via shared direction for verify/prefill workloads")

@@ -8,8 +8,8 @@ import oracle
 import synth
 import nvfp4_mixture_experts_bf16_gb300 as moe
 from _gpu_fixtures import (GAMMA_NARROW, GAMMA_WIDE, FullLayer, check_topk, compare_outputs,
-                           dev_bf16, h_flip_allowance, host_u16, pack_from_experts, slot_map,
-                           small_layer, stable_perm, ws_array)
+                           dev_bf16, gamma, h_flip_allowance, host_u16, pack_from_experts,
+                           slot_map, small_layer, stable_perm, ws_array)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,13 +24,21 @@ def _built():
     moe.lib()
 
 
-def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None):
-    """Run moe_forward on the GPU and check every stage against the oracle."""
+def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None, shared=None):
+    """Run moe_forward (moe_forward_shared when ``shared`` = (gate_up, down, gate) BF16 arrays
+    is given) on the GPU and check every stage against the oracle."""
     T, H = x.shape
     E, I = ex.E, ex.I
     S = T * k
-    ws = moe.new_workspace(moe.moe_workspace_size(pack, T, k, mode))
-    out = moe.moe_forward(dev_bf16(x), dev_bf16(wr), pack, k, mode, ws=ws)
+    if shared is None:
+        ws = moe.new_workspace(moe.moe_workspace_size(pack, T, k, mode))
+        out = moe.moe_forward(dev_bf16(x), dev_bf16(wr), pack, k, mode, ws=ws)
+    else:
+        Is = shared[0].shape[0] // 2
+        ws = moe.new_workspace(moe.moe_workspace_size_shared(pack, T, k, mode, Is))
+        out = moe.moe_forward_shared(dev_bf16(x), dev_bf16(wr), pack,
+                                     tuple(dev_bf16(a) for a in shared), k, mode, ws=ws)
+    launches = moe.moe_last_launch_count()
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(ws) == 0
     off = moe.moe_workspace_offsets(pack, T, k, mode)
@@ -40,7 +48,9 @@ def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None):
     g_offsets = ws_array(ws, off["offsets"], (E + 1) * 4, np.int32)
     g_perm = ws_array(ws, off["perm"], S * 4, np.int32)
     g_slot_of = ws_array(ws, off["slot_of"], S * 4, np.int32).reshape(T, k)
-    ref = oracle.forward(x, wr, ex, k, mode, nthreads=nthreads, want=ALL)
+    ref = oracle.forward(x, wr, ex, k, mode, nthreads=nthreads, want=ALL,
+                         shared=None if shared is None else oracle.SharedExpert(*shared))
+    sh_allow = {} if shared is None else check_shared(ws, pack, x, shared, ref, k, mode)
 
     differ = check_topk(g_idx, g_w, ref, GAMMA_NARROW if T <= 8 else GAMMA_WIDE)
     c, o, p = stable_perm(g_idx, E)
@@ -60,7 +70,7 @@ def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None):
                               ref["xq_scales"])
     gm = slot_map(g_perm, g_offsets)
     rm = slot_map(ref["perm"], ref["offsets"])
-    allowance = {}
+    allowance = dict(sh_allow)
     flips = 0
     if mode == 0:
         gh = synth.bf16_to_f32(ws_array(ws, off["h_bf16"], S * I * 2, np.uint16).reshape(S, I))
@@ -91,7 +101,64 @@ def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None):
                 flips += f
     toks = [t for t in range(T) if t not in differ] if tokens is None else tokens
     worst = compare_outputs(host_u16(out), ref, mode, toks, allowance)
-    return dict(out=out, ws=ws, differ=differ, flips=flips, worst=worst, ref=ref, g_idx=g_idx)
+    return dict(out=out, ws=ws, differ=differ, flips=flips, worst=worst, ref=ref, g_idx=g_idx,
+                launches=launches)
+
+
+def check_shared(ws, pack, x, shared, ref, k, mode):
+    """The shared expert's intermediates against the oracle; returns, per token, the output
+    allowance of its accepted h roundings.
+
+    The gate: within the FP32 bound of its dot product. h: equal to the oracle's BF16 h, or
+    else between the BF16 roundings of h64 - win and h64 + win (rounding is monotonic), h64
+    being the oracle's unrounded h and win the FP32 error bound of the GPU's h:
+    |u| * 1.1 * dg + |SiLU(g)| * du + 8 ulp(h), with dg, du = gamma_n * sum|x * w| the FP32
+    accumulation bounds of g and u (n as for the router). Each accepted difference widens the
+    token's bound by |dh| * ||Wd[:, i]||_2, its exact effect on Ys (triangle inequality). Ys
+    (FP32): per token within 1e-4 of the oracle's norm plus that allowance."""
+    T, H = x.shape
+    Is = shared[0].shape[0] // 2
+    so = moe.moe_workspace_offsets_shared(pack, T, k, mode, Is)
+    return check_shared_arrays(
+        x, shared, ref, ws_array(ws, so["sigma"], T * 4, np.float32),
+        ws_array(ws, so["h"], T * Is * 2, np.uint16).reshape(T, Is),
+        ws_array(ws, so["y"], T * H * 4, np.float32).reshape(T, H))
+
+
+def check_shared_arrays(x, shared, ref, sig, gh_bits, gy):
+    """check_shared on host arrays: sigma [T] float32, h [T, Is] BF16 bits, Ys [T, H] float32."""
+    T, H = x.shape
+    gu, dn, gv = shared
+    Is = gu.shape[0] // 2
+    sig = np.asarray(sig, np.float64)
+    xf = synth.bf16_to_f32(x).astype(np.float64)
+    xa = np.abs(xf)
+    bound = 0.25 * gamma(GAMMA_WIDE) * (xa @ np.abs(synth.bf16_to_f32(gv).astype(np.float64)))
+    assert np.all(np.abs(sig - ref["sigma"]) <= bound + 1e-6), np.abs(sig - ref["sigma"]).max()
+    gh = synth.bf16_to_f32(gh_bits).astype(np.float64)
+    rh = synth.bf16_to_f32(ref["hs_bf16"]).astype(np.float64)
+    diff = np.nonzero(gh != rh)
+    allow = np.zeros(T)
+    if len(diff[0]):
+        W = synth.bf16_to_f32(gu).astype(np.float64)
+        wg, wu = W[:Is], W[Is:]
+        wcol = np.linalg.norm(synth.bf16_to_f32(dn).astype(np.float64), axis=0)  # ||Wd[:, i]||
+        for t, i in zip(*diff):
+            g, u = xf[t] @ wg[i], xf[t] @ wu[i]
+            dg = gamma(GAMMA_WIDE) * (xa[t] @ np.abs(wg[i]))
+            du = gamma(GAMMA_WIDE) * (xa[t] @ np.abs(wu[i]))
+            win = abs(u) * 1.1 * dg + abs(g / (1 + np.exp(-g))) * du + 8 * 2.0 ** -24 * abs(g * u)
+            h64 = ref["hs64"][t, i]
+            lo = synth.bf16_to_f32(np.uint16(oracle.double_to_bf16(h64 - win)))
+            hi = synth.bf16_to_f32(np.uint16(oracle.double_to_bf16(h64 + win)))
+            assert lo <= gh[t, i] <= hi, ("h outside the rounding of its error interval", t, i,
+                                          gh[t, i], rh[t, i], h64, win)
+            allow[t] += abs(gh[t, i] - rh[t, i]) * wcol[i]
+    gy = np.asarray(gy, np.float64)
+    for t in range(T):
+        ny = np.linalg.norm(ref["ys"][t])
+        assert np.linalg.norm(gy[t] - ref["ys"][t]) <= 1e-4 * ny + allow[t] * (1 + 1e-6) + 1e-30, t
+    return {t: float(ref["sigma"][t] * allow[t]) for t in range(T) if allow[t] > 0}
 
 
 # ------------------------------------------------------------------ quantiser
@@ -301,13 +368,19 @@ def test_forward_full_size_decode(name):
 
 
 # ------------------------------------------------------------------ full-size prefill, sampled
-@pytest.mark.parametrize("mode", [1, 0])
-def test_forward_prefill_8192_sampled(mode):
+@pytest.mark.parametrize("mode,with_shared", [(1, False), (0, False), (1, True)])
+def test_forward_prefill_8192_sampled(mode, with_shared):
     wl = synth.WORKLOADS["prefill8192"]
     lay = FullLayer(0, 0, wl.T, wl.zipf)
     T, k = wl.T, wl.k
-    ws = moe.new_workspace(moe.moe_workspace_size(lay.pack, T, k, mode))
-    out = moe.moe_forward(dev_bf16(lay.x), dev_bf16(lay.wr), lay.pack, k, mode, ws=ws)
+    shared = synth.shared_expert_weights(0, 0, lay.H, lay.I) if with_shared else None
+    if shared is None:
+        ws = moe.new_workspace(moe.moe_workspace_size(lay.pack, T, k, mode))
+        out = moe.moe_forward(dev_bf16(lay.x), dev_bf16(lay.wr), lay.pack, k, mode, ws=ws)
+    else:
+        ws = moe.new_workspace(moe.moe_workspace_size_shared(lay.pack, T, k, mode, lay.I))
+        out = moe.moe_forward_shared(dev_bf16(lay.x), dev_bf16(lay.wr), lay.pack,
+                                     tuple(dev_bf16(a) for a in shared), k, mode, ws=ws)
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(ws) == 0
     off = moe.moe_workspace_offsets(lay.pack, T, k, mode)
@@ -328,7 +401,8 @@ def test_forward_prefill_8192_sampled(mode):
     ex = lay.oracle_experts(ref_route["idx"][sample].ravel(), nthreads=16)
     ref = oracle.forward(lay.x[sample], lay.wr, ex, k, mode, nthreads=16,
                          want=("out_bf16", "out64", "idx", "perm", "offsets", "hq_codes",
-                               "hq_scales", "h_amb_elem", "h_amb_block"))
+                               "hq_scales", "h_amb_elem", "h_amb_block"),
+                         shared=None if shared is None else oracle.SharedExpert(*shared))
     allowance = {}
     if mode == 1:
         g_perm = ws_array(ws, off["perm"], T * k * 4, np.int32)
@@ -343,4 +417,87 @@ def test_forward_prefill_8192_sampled(mode):
                 allowance[i] = allowance.get(i, 0.0) + float(g_w[t, j]) * a
     got = host_u16(out)[sample]
     compare_outputs(got, ref, mode, list(range(len(sample))), allowance)
+    lay.close()
+
+
+# ------------------------------------------------------------------ shared expert
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("T", [1, 2, 5, 8, 9, 203])
+def test_forward_shared_ragged_shapes(T, mode):
+    # narrow calls: the two CUDA-core GEMVs then the one-launch routed kernel; wide calls: the
+    # two tcgen05 BF16 GEMMs with the per-token kernel between them
+    H, E, k, I = 1536, 24, 4, 192
+    x, wr, ex = small_layer(T, H, E, k, I, zipf=True, seed=11)
+    pack = pack_from_experts(ex)
+    r = run_and_check(x, wr, ex, pack, k, mode, shared=synth.shared_expert_weights(11, 0, H, I))
+    if T <= 8:
+        assert r["launches"] == 3
+    pack.close()
+
+
+@pytest.mark.parametrize("T,H,E,k,I,Is", [
+    (4, 256, 16, 2, 64, 64),      # the tiny workload's shapes, Is = I
+    (3, 1024, 64, 6, 128, 640),   # Is > 512: the down rows' units past the register-held ones
+    (40, 1024, 64, 6, 128, 640),  # the same through the tensor-core GEMMs (K = 640)
+    (2, 4096, 64, 10, 384, 384),  # decode widths (H, I, Is) with 64 experts
+])
+def test_forward_shared_shapes(T, H, E, k, I, Is):
+    x, wr, ex = small_layer(T, H, E, k, I, seed=50 + T)
+    pack = pack_from_experts(ex)
+    run_and_check(x, wr, ex, pack, k, 0, shared=synth.shared_expert_weights(50 + T, 0, H, Is))
+    pack.close()
+
+
+@pytest.mark.parametrize("T", [1, 5, 50])
+def test_forward_shared_zero_down_is_moe_forward(T):
+    # the shared term sigma * BF16(0) leaves the routed sum unchanged: bit-identical outputs
+    H, E, k, I = 512, 32, 4, 128
+    x, wr, ex = small_layer(T, H, E, k, I, seed=61)
+    pack = pack_from_experts(ex)
+    gu, dn, gv = synth.shared_expert_weights(61, 0, H, I)
+    for mode in (0, 1):
+        a = moe.moe_forward(dev_bf16(x), dev_bf16(wr), pack, k, mode).clone()
+        sh = (dev_bf16(gu), dev_bf16(np.zeros_like(dn)), dev_bf16(gv))
+        b = moe.moe_forward_shared(dev_bf16(x), dev_bf16(wr), pack, sh, k, mode).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), (T, mode)
+    pack.close()
+
+
+def test_forward_shared_twice_is_deterministic():
+    for T in (1, 8, 40):
+        x, wr, ex = small_layer(T, 512, 32, 4, 128, seed=62)
+        pack = pack_from_experts(ex)
+        sh = tuple(dev_bf16(a) for a in synth.shared_expert_weights(62, 0, 512, 128))
+        ws = moe.new_workspace(moe.moe_workspace_size_shared(pack, T, 4, 0, 128))
+        a = moe.moe_forward_shared(dev_bf16(x), dev_bf16(wr), pack, sh, 4, 0, ws=ws).clone()
+        b = moe.moe_forward_shared(dev_bf16(x), dev_bf16(wr), pack, sh, 4, 0, ws=ws).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert moe.moe_read_device_status(ws) == 0
+        pack.close()
+
+
+def test_forward_shared_rejects_bad_arguments():
+    x, wr, ex = small_layer(2, 256, 8, 2, 64)
+    pack = pack_from_experts(ex)
+    gu, dn, gv = (dev_bf16(a) for a in synth.shared_expert_weights(0, 0, 256, 64))
+    with pytest.raises(moe.MoeError):                      # inter % 64 != 0
+        moe.moe_forward_shared(dev_bf16(x), dev_bf16(wr), pack, (gu[:100], dn, gv), 2, 0)
+    with pytest.raises(moe.MoeError) as e:                  # workspace without the shared part
+        moe.moe_forward_shared(dev_bf16(x), dev_bf16(wr), pack, (gu, dn, gv), 2, 0,
+                               ws=moe.new_workspace(moe.moe_workspace_size(pack, 2, 2, 0)))
+    assert e.value.code == 6
+    pack.close()
+
+
+@pytest.mark.parametrize("name", ["decode1", "verify8_w4a4"])
+def test_forward_shared_full_size_decode(name):
+    wl = synth.WORKLOADS[name]
+    lay = FullLayer(0, 0, wl.T, wl.zipf)
+    ref_route = oracle.route(lay.x, lay.wr, wl.k, nthreads=8)
+    ex = lay.oracle_experts(ref_route["idx"].ravel())
+    r = run_and_check(lay.x, lay.wr, ex, lay.pack, wl.k, wl.mode,
+                      shared=synth.shared_expert_weights(0, 0, lay.H, lay.I))
+    assert not r["differ"] and r["launches"] == 3
     lay.close()
