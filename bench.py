@@ -56,6 +56,8 @@ def parse_args():
     p.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--shared", action="store_true",
+                   help="time the step with a BF16 shared expert per layer (Is = I)")
     return p.parse_args()
 
 
@@ -421,6 +423,8 @@ def run_native(args, rank, world, local_rank):
     pk = peaks()
     t_setup = time.time()
     stack = build_stack(wl, layers, args.seed + 1000 * rank, device)
+    if args.shared:
+        stack = with_shared(stack, wl, args.seed + 1000 * rank, device)
     setup_s = time.time() - t_setup
 
     if world > 1:
@@ -438,14 +442,23 @@ def run_native(args, rank, world, local_rank):
     U_mean = float(np.mean([L.U for L in stack]))
     gu_bytes = bytes_gateup(U_mean, wl.H, wl.I)
     dn_bytes = bytes_down(U_mean, wl.H, wl.I)
-    layer_bytes = gu_bytes + dn_bytes
+    layer_bytes = gu_bytes + dn_bytes + (bytes_shared(wl.H, wl.I) if args.shared else 0)
     layer_s = ms / layers * 1e-3
     layer_gbs = layer_bytes / layer_s / 1e9
     peak_src = (f"{pk['src']} hbm_gbs (MEASURED_PEAKS.json)" if pk["src"] == "measured"
                 else "fallback 6.8 TB/s")
     fused = launches == layers   # one launch per layer: the persistent narrow-call kernel
     stages = None
-    if fused:
+    if args.shared:
+        # the whole step (shared-expert kernels + the narrow-call kernel, or the wide path)
+        gbs = layer_bytes / layer_s / 1e9
+        roofline = dict(bound="hbm", kernel=f"whole step with the shared expert "
+                        f"({launches // layers} launches per layer)",
+                        achieved=round(gbs, 1), peak=pk["hbm"], unit="GB/s",
+                        frac=round(gbs / pk["hbm"], 4), traffic=None,
+                        algorithmic_bytes_per_launch=None,
+                        algorithmic_bytes_per_layer=int(layer_bytes), peak_source=peak_src)
+    elif fused:
         # the only kernel of the step: mean launch duration = event-timed step / launches
         dec_bytes = bytes_decode_launch(U_mean, wl.T, wl.H, wl.E, wl.I)
         gbs = dec_bytes / layer_s / 1e9
@@ -468,7 +481,7 @@ def run_native(args, rank, world, local_rank):
     e2e_ms, io_bytes = e2e_measure(wl, stack, max(3, args.steps // 2), state, device)
 
     extra = {}
-    if not args.no_extra and rank == 0:
+    if not args.no_extra and not args.shared and rank == 0:
         packs = [L.pack for L in stack]
         for name in ("verify8", "verify8_w4a4"):
             w2 = synth.WORKLOADS[name]
@@ -531,13 +544,16 @@ def run_native(args, rank, world, local_rank):
                     top_k=wl.k, inter=wl.I, mode=["W4A16", "W4A4"][wl.mode],
                     parallelism=f"replicas x{world}" if world > 1 else "single GPU",
                     l2="no flush: a step streams 48 layers x 10 experts = 1.27 GB > 129 MB L2",
-                    graph=not args.no_graph, setup_s=round(setup_s, 1)),
+                    graph=not args.no_graph, setup_s=round(setup_s, 1),
+                    shared_expert=bool(args.shared)),
         gpu_launches=launches * args.steps,
         roofline=roofline,
         layer=dict(us=round(ms / layers * 1e3, 3), launches=launches // layers,
                    stage_us=stages, hbm_gbs=round(layer_gbs, 1),
                    frac_hbm=round(layer_gbs / pk["hbm"], 4), unique_experts=U_mean,
-                   note="hbm_gbs: selected experts' bytes (U x B_e) per layer time, router excluded"),
+                   note=("hbm_gbs: selected experts' bytes (U x B_e)"
+                         + (" + the shared expert's BF16 bytes" if args.shared else "")
+                         + " per layer time, router excluded")),
         e2e=dict(value=round(world * tokens_per_step / (e2e_ms / 1e3), 2), unit="layer-tokens/s",
                  h2d_bytes_per_step=io_bytes, d2h_bytes_per_step=io_bytes),
         clocks=clk, cpu_baseline=cpu, secondary=extra)
