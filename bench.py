@@ -226,6 +226,21 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ multi-rank aggregation
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's step time (every rank gets it): replicas finish when the last does."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, ms: float) -> float:
+    """Whole-job layer-tokens/s: every rank processes tokens_per_step per step (weak scaling)."""
+    return world * tokens_per_step / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ native arm
 class Layer:
     def __init__(self, x, wr, pack, U, shared=None):
@@ -433,11 +448,9 @@ def run_native(args, rank, world, local_rank):
     ms, launches, clk, state = measure(wl, stack, args.steps, args.warmup, not args.no_graph,
                                        device, clocks)
     if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, device)
     tokens_per_step = wl.T * layers
-    value = world * tokens_per_step / (ms / 1e3)
+    value = job_throughput(world, tokens_per_step, ms)
 
     U_mean = float(np.mean([L.U for L in stack]))
     gu_bytes = bytes_gateup(U_mean, wl.H, wl.I)
