@@ -22,7 +22,8 @@ constexpr int kShThreads = 256;
 constexpr int kShWarps = kShThreads / 32;
 constexpr int kGuIdx = 3;               // intermediate indices per gate/up batch (2 rows each)
 constexpr int kGuRows = 2 * kGuIdx;
-constexpr int kGuUnits = 4;             // 16-byte units per lane and row: H <= 8192
+constexpr int kGuUnits = 2;             // 16-byte units per lane and row of one K-chunk
+constexpr int kGuChunk = kGuUnits * kShThreads;   // units of one K-chunk (4096 columns)
 constexpr int kDnRows = 4;              // down rows per warp batch
 constexpr int kDnUnits = 2;             // 16-byte units per lane and row kept in registers
 
@@ -35,9 +36,12 @@ __device__ __forceinline__ uint4 ldcg128(const void* p) {
 
 // Narrow gate/up: CTA b owns intermediate indices [j0, j1) of 0..Is, index Is being the gate
 // vector. A batch holds kGuIdx indices (gate row, up row each); every warp takes an eighth of
-// the 16-byte units of every row of the batch, so the CTA's 8 warps cover each row once.
+// the 16-byte units of every row of the batch, K in chunks of kGuChunk units, so the CTA's 8
+// warps cover each row once. With one token the kernel fits in 85 registers a thread,
+// so its CTAs are resident next to the preceding narrow-call kernel's and their weight loads
+// (issued before the wait) stream while that kernel runs.
 template <int NT>
-__global__ void __launch_bounds__(kShThreads, 1)
+__global__ void __launch_bounds__(kShThreads, NT == 1 ? 3 : 1)
     k_shared_gu_narrow(const uint16_t* __restrict__ x, ShView sv, int H) {
   extern __shared__ __align__(16) unsigned char xs[];   // [NT][H] BF16
   __shared__ float red[kShWarps][kGuRows][NT];
@@ -45,11 +49,11 @@ __global__ void __launch_bounds__(kShThreads, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Is = sv.Is, nidx = Is + 1, G = gridDim.x, b = blockIdx.x;
   const int j0 = (int)((long long)nidx * b / G), j1 = (int)((long long)nidx * (b + 1) / G);
-  const int nunits = H / 8;
+  const int nunits = H / 8, nkc = (nunits + kGuChunk - 1) / kGuChunk;
   uint4 w[kGuRows][kGuUnits];
   // row r of the batch at index jb: gate row (r even) or up row (r odd); the gate vector has
   // one row; absent rows load zeros
-  auto load_batch = [&](int jb) {
+  auto load_batch = [&](int jb, int kc) {
 #pragma unroll
     for (int r = 0; r < kGuRows; ++r) {
       const int j = jb + r / 2;
@@ -60,33 +64,35 @@ __global__ void __launch_bounds__(kShThreads, 1)
       }
 #pragma unroll
       for (int i = 0; i < kGuUnits; ++i) {
-        const int u = warp * 32 + lane + i * kShThreads;
+        const int u = kc * kGuChunk + warp * 32 + lane + i * kShThreads;
         w[r][i] = (row && u < nunits) ? ldg128(row + (size_t)u * 8) : make_uint4(0, 0, 0, 0);
       }
     }
   };
-  if (j0 < j1) load_batch(j0);   // before the wait: weights do not depend on earlier kernels
+  if (j0 < j1) load_batch(j0, 0);   // before the wait: weights do not depend on earlier kernels
   pdl_wait();
   pdl_launch_dependents();
   for (int o = tid; o < NT * nunits; o += kShThreads)
     reinterpret_cast<uint4*>(xs)[o] = ldcg128(x + (size_t)o * 8);
   __syncthreads();
   for (int jb = j0; jb < j1; jb += kGuIdx) {
-    if (jb != j0) load_batch(jb);
     float acc[kGuRows][NT];
 #pragma unroll
     for (int r = 0; r < kGuRows; ++r)
 #pragma unroll
       for (int t = 0; t < NT; ++t) acc[r][t] = 0.0f;
+    for (int kc = 0; kc < nkc; ++kc) {
+      if (jb != j0 || kc != 0) load_batch(jb, kc);
 #pragma unroll
-    for (int i = 0; i < kGuUnits; ++i) {
-      const int u = warp * 32 + lane + i * kShThreads;
-      if (u < nunits) {
+      for (int i = 0; i < kGuUnits; ++i) {
+        const int u = kc * kGuChunk + warp * 32 + lane + i * kShThreads;
+        if (u < nunits) {
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + ((size_t)t * nunits + u) * 16);
+          for (int t = 0; t < NT; ++t) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + ((size_t)t * nunits + u) * 16);
 #pragma unroll
-          for (int r = 0; r < kGuRows; ++r) acc[r][t] += dot8_bf16(w[r][i], xv);
+            for (int r = 0; r < kGuRows; ++r) acc[r][t] += dot8_bf16(w[r][i], xv);
+          }
         }
       }
     }
