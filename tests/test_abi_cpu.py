@@ -75,6 +75,13 @@ def test_argument_validation_before_any_launch(L):
     assert L.moe_pack_nvfp4(g, g, g, 1, 128, 64, None, ctypes.byref(vp())) == 1  # null codes
     assert L.moe_pack_destroy(None) == 0
     assert L.moe_read_device_status(None, None, None) == 1
+    # shared expert: a null pack or a null / invalid descriptor, before any launch
+    sh = moe._SharedExpert(16, 16, 16, 384)
+    assert L.moe_forward_shared(None, None, None, ctypes.byref(sh), 1, 1, 0, None, None, 0,
+                                None) == 1
+    assert L.moe_workspace_size_shared(None, 1, 1, 0, 384, ctypes.byref(n)) == 1
+    o = ctypes.c_size_t()
+    assert L.moe_workspace_offsets_shared(None, 1, 1, 0, 384, ctypes.byref(o), None, None) == 1
 
 
 def test_workspace_size_grows_with_tokens(L):
