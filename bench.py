@@ -243,9 +243,10 @@ def job_throughput(world: int, tokens_per_step: int, ms: float) -> float:
 
 # ------------------------------------------------------------------ native arm
 class Layer:
-    def __init__(self, x, wr, pack, U, shared=None):
+    def __init__(self, x, wr, pack, U, shared=None, xall=None):
         self.x, self.wr, self.pack, self.U = x, wr, pack, U
         self.shared = shared   # (gate_up, down, gate) BF16 tensors of the shared expert, or None
+        self.xall = xall       # [layers, T, H]: every layer's x, of which self.x is one row
 
 
 def quantized_experts(seed, layer, E, H, I, device):
@@ -276,7 +277,7 @@ def dev_bf16(u16, device):
 def with_shared(stack, wl, seed, device):
     """The same layers, each with its own BF16 shared expert of intermediate size I."""
     return [Layer(L.x, L.wr, L.pack, L.U,
-                  synth.torch_shared_expert_weights(seed, l, wl.H, wl.I, device))
+                  synth.torch_shared_expert_weights(seed, l, wl.H, wl.I, device), L.xall)
             for l, L in enumerate(stack)]
 
 
@@ -310,6 +311,11 @@ def build_stack(wl, layers, seed, device, packs=None):
         r = moe.moe_route_topk(x, wr, wl.k)
         U = int((r["counts"] > 0).sum().item())
         out.append(Layer(x, wr, pack, U))
+    # every layer's activations in one [layers, T, H] tensor (each layer's x a row of it), so a
+    # step's inputs move host->device in one copy
+    xall = torch.stack([L.x for L in out])
+    for l, L in enumerate(out):
+        L.x, L.xall = xall[l], xall
     return out
 
 
@@ -322,7 +328,8 @@ def measure(wl, stack, steps, warmup, use_graph, device, clocks=None):
     nws = (moe.moe_workspace_size(stack[0].pack, wl.T, wl.k, wl.mode) if sh is None else
            moe.moe_workspace_size_shared(stack[0].pack, wl.T, wl.k, wl.mode, sh[0].shape[0] // 2))
     ws = moe.new_workspace(nws, device)
-    outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in stack]
+    oall = torch.empty((len(stack), wl.T, wl.H), dtype=torch.bfloat16, device=device)
+    outs = list(oall)           # each layer's out is a row of one tensor (one device->host copy)
     launches = [0]
 
     def step():
@@ -365,7 +372,7 @@ def measure(wl, stack, steps, warmup, use_graph, device, clocks=None):
     status = moe.moe_read_device_status(ws, stream=s)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    return e0.elapsed_time(e1) / steps, launches[0], info, (s, ws, outs, run)
+    return e0.elapsed_time(e1) / steps, launches[0], info, (s, ws, oall, run)
 
 
 def stage_times(wl, stack, reps, device):
@@ -398,11 +405,14 @@ def stage_times(wl, stack, reps, device):
 
 def e2e_measure(wl, stack, steps, state, device):
     """Same metric through the public API with host buffers: per step, copy every layer's x
-    host->device (pinned), run the step, copy every layer's out device->host."""
+    host->device (pinned; the layers' inputs are one [layers, T, H] buffer, so one copy), run
+    the step, copy every layer's out device->host (one copy of the [layers, T, H] outputs)."""
     import torch
-    s, ws, outs, run = state
-    hx = [L.x.cpu().pin_memory() for L in stack]
-    ho = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory() for _ in stack]
+    s, ws, oall, run = state
+    xall = stack[0].xall
+    assert all(L.xall is xall for L in stack)
+    hx = xall.cpu().pin_memory()
+    ho = torch.empty(tuple(oall.shape), dtype=torch.bfloat16).pin_memory()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -410,11 +420,9 @@ def e2e_measure(wl, stack, steps, state, device):
         for it in range(steps + 2):
             if it == 2:
                 e0.record(s)
-            for L, h in zip(stack, hx):
-                L.x.copy_(h, non_blocking=True)
+            xall.copy_(hx, non_blocking=True)
             run()
-            for o, h in zip(outs, ho):
-                h.copy_(o, non_blocking=True)
+            ho.copy_(oall, non_blocking=True)
         e1.record(s)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
