@@ -125,17 +125,19 @@ moe_status moe_route_topk(const uint16_t* x, const uint16_t* router_w, int T, in
                           int32_t* perm, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_route_topk without a workspace argument, for callers that cannot allocate device memory:
- * code that runs while a stream is being captured into a CUDA graph (cudaMalloc is not allowed
- * there), runtimes whose allocator is frozen after start-up, and embedders that own no device
- * allocator. The pages have no counterpart to this entry point; it exists only for such callers.
- * Arguments, outputs and requirements are those of moe_route_topk. Its workspace is a fixed
- * 4 MiB device array inside the library, held by every GPU that loads the library until the
- * process exits; shapes whose moe_route_workspace_size exceeds 4 MiB return MOE_ERR_WORKSPACE
- * before anything is launched. No call allocates or frees memory. The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress): make that first call before any
- * stream capture. Each call clears the array's control words (cudaMemsetAsync on `stream`). All
- * calls share the one array: calls that overlap on the GPU (e.g. on two streams) race, so the
- * caller must serialise them. */
+ * runtimes whose allocator is frozen after start-up, and embedders that own no device allocator
+ * (a plugin that is handed only its input and output buffers). The pages have no counterpart to
+ * this entry point; it exists only for such callers. Arguments, outputs and requirements are
+ * those of moe_route_topk. Its workspace is a fixed 4 MiB device array inside the library, held
+ * by every GPU that loads the library until the process exits; shapes whose
+ * moe_route_workspace_size exceeds 4 MiB return MOE_ERR_WORKSPACE before anything is launched.
+ * No call allocates or frees memory. The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before any stream capture,
+ * and do not use the entry point again after a cudaDeviceReset of that device in the same
+ * process. Each call clears the array's control words (cudaMemsetAsync on `stream`) except the
+ * status word: a device-side timeout of any call stays recorded until
+ * moe_read_device_status(NULL, ...) reads and clears it. All calls share the one array: calls
+ * that overlap on the GPU (e.g. on two streams) race, so the caller must serialise them. */
 moe_status moe_route_topk_noalloc(const uint16_t* x, const uint16_t* router_w, int T, int H, int E,
                                   int k, int32_t* idx, float* w, int32_t* counts, int32_t* offsets,
                                   int32_t* perm, void* stream);
@@ -169,9 +171,9 @@ moe_status moe_workspace_size_shared(const moe_expert_pack* pack, int T, int k, 
                                      int shared_inter, size_t* bytes);
 
 /* moe_forward plus the shared expert: for token t,
- *   hs  = BF16( SiLU(Wg x_t) * (Wu x_t) ),   Ys = Wd hs   (FP32 accumulation, not rounded),
- *   out[t] = BF16( sum_j w_j * Y_j  +  sigma_t * Ys ),  the shared term added after the routed
- * ones in FP32. Arguments and requirements are those of moe_forward, plus `shared` (above);
+ *   hs  = BF16( SiLU(Wg x_t) * (Wu x_t) ),   Ys = Wd hs   (FP32 accumulation),
+ *   out[t] = BF16( sum_j w_j * Y_j  +  sigma_t * BF16(Ys) ),  the shared term added after the
+ * routed ones in FP32; Ys is rounded to BF16 like each routed expert's output Y. Arguments and requirements are those of moe_forward, plus `shared` (above);
  * a null or invalid `shared` returns MOE_ERR_INVALID_ARG. The shared expert runs first, as two
  * CUDA-core GEMV kernels for T <= 8 and as two tcgen05 BF16 GEMMs with a per-token kernel
  * between them for larger T. ws/ws_bytes: see moe_workspace_size_shared. */
@@ -202,8 +204,8 @@ moe_status moe_workspace_offsets(const moe_expert_pack* pack, int T, int k, moe_
 
 /* Byte offsets inside a moe_forward_shared workspace of the shared expert's intermediate
  * results, for tests: h (uint16 BF16 [T][inter]), sigma (float [T]) and Y (float [T][hidden],
- * before its BF16 rounding). The routed results sit at the offsets moe_workspace_offsets gives.
- * Any output pointer may be null. */
+ * before its BF16 rounding, which the combine applies). The routed results sit at the offsets
+ * moe_workspace_offsets gives. Any output pointer may be null. */
 moe_status moe_workspace_offsets_shared(const moe_expert_pack* pack, int T, int k, moe_mode mode,
                                         int shared_inter, size_t* h, size_t* sigma, size_t* y);
 
@@ -217,7 +219,8 @@ moe_status moe_quantize_act_nvfp4(const uint16_t* x, int rows, int cols, float i
                                   uint8_t* codes, uint8_t* scales, void* stream);
 
 /* Read and clear the device status word of a workspace (synchronises `stream`). *status is
- * MOE_OK or the first error a kernel recorded (MOE_ERR_TIMEOUT). */
+ * MOE_OK or the first error a kernel recorded (MOE_ERR_TIMEOUT). ws = NULL reads the status word
+ * of moe_route_topk_noalloc's fixed array on the current device. */
 moe_status moe_read_device_status(void* ws, void* stream, moe_status* status);
 
 /* Human-readable name of a status code (static storage). */

@@ -311,8 +311,11 @@ def moe_quantize_act_nvfp4(x, input_scale: float, codes=None, scales=None, strea
 
 
 def moe_read_device_status(ws, stream=None) -> int:
+    """Read and clear a workspace's device status word; ws = None reads the one of
+    moe_route_topk_noalloc's fixed array on the current device."""
     st = ctypes.c_int()
-    _check("moe_read_device_status", lib().moe_read_device_status(_ptr(ws), _stream(stream),
+    wp = ctypes.c_void_p(None) if ws is None else _ptr(ws)
+    _check("moe_read_device_status", lib().moe_read_device_status(wp, _stream(stream),
                                                                   ctypes.byref(st)))
     return st.value
 

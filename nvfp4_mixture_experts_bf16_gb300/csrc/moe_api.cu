@@ -10,6 +10,7 @@
 
 namespace moe {
 size_t route_narrow_smem_bytes(int T, int H, int E, int k);
+void* noalloc_scratch_of_current_device();
 }
 
 struct moe_expert_pack {
@@ -577,7 +578,11 @@ moe_status moe_quantize_act_nvfp4(const uint16_t* x, int rows, int cols, float i
 }
 
 moe_status moe_read_device_status(void* ws, void* stream, moe_status* status) {
-  if (!ws || !status) return MOE_ERR_INVALID_ARG;
+  if (!status) return MOE_ERR_INVALID_ARG;
+  if (!ws) {   // the fixed array of moe_route_topk_noalloc on the current device
+    ws = moe::noalloc_scratch_of_current_device();
+    if (!ws) return MOE_ERR_CUDA;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint32_t v = 0;
   uint32_t* word = static_cast<uint32_t*>(ws) + moe::kCtlStatus;

@@ -1126,12 +1126,13 @@ __global__ void __launch_bounds__(kDcThreads, 1)
           a1 += wj * __uint_as_float(v & 0xFFFF0000u);
         }
         if (ws.sh_y) {
-          // the shared expert's term, after the routed ones (written by an earlier kernel)
+          // the shared expert's term, after the routed ones (written by an earlier kernel):
+          // sigma_t * BF16(Ys), Ys rounded like a routed expert's output
           const float sg = __ldcg(ws.sh_sigma + t);
           const float2 ys = __ldcg(reinterpret_cast<const float2*>(ws.sh_y + (size_t)t * H) +
                                    ht * 64 + p2);
-          a0 += sg * ys.x;
-          a1 += sg * ys.y;
+          a0 += sg * bf16_round(ys.x);
+          a1 += sg * bf16_round(ys.y);
         }
         reinterpret_cast<uint32_t*>(out + (size_t)t * H)[ht * 64 + p2] =
             (uint32_t)f32_to_bf16_rn(a0) | ((uint32_t)f32_to_bf16_rn(a1) << 16);

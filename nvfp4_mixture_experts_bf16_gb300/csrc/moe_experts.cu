@@ -600,13 +600,14 @@ __global__ void __launch_bounds__(256) k_combine(WsView ws, uint16_t* __restrict
       }
     }
     if (ws.sh_y) {
-      // the shared expert's term, after the routed ones: sigma_t * Ys (FP32, unrounded)
+      // the shared expert's term, after the routed ones: sigma_t * BF16(Ys) (Ys is an expert
+      // output, rounded to BF16 like the routed Y)
       const float sg = __ldcg(ws.sh_sigma + t);
       const float4* ys = reinterpret_cast<const float4*>(ws.sh_y + (size_t)t * H) + 2 * r8;
       const float4 a = __ldcg(ys), b = __ldcg(ys + 1);
       const float yv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += sg * yv[q];
+      for (int q = 0; q < 8; ++q) acc[q] += sg * bf16_round(yv[q]);
     }
     uint32_t o[4];
 #pragma unroll

@@ -497,6 +497,11 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float v) {
   return *reinterpret_cast<uint16_t*>(&b);
 }
 
+// v rounded to the nearest BF16 value (ties to even), as an FP32 value
+__device__ __forceinline__ float bf16_round(float v) {
+  return __uint_as_float((uint32_t)f32_to_bf16_rn(v) << 16);
+}
+
 __device__ __forceinline__ int amax_shift(float m) {
   if (!(m > 0.0f)) return 0;
   int ex;

@@ -2,19 +2,20 @@
 // that cannot allocate device memory.
 //
 // moe_route_topk needs a caller-provided workspace. Some callers have no way to provide one:
-// code running inside a CUDA graph capture (cudaMalloc is not allowed while a stream is being
-// captured), runtimes that freeze their allocator after start-up, and embedders that own no
-// device allocator at all. moe_route_topk_noalloc serves them: its workspace is a fixed device
-// array owned by this library, so a call allocates nothing (no cudaMalloc, no cudaFree, no
-// allocating library routine).
+// runtimes that freeze their allocator after start-up, and embedders that own no device
+// allocator at all (a plugin handed only input and output buffers). moe_route_topk_noalloc
+// serves them: its workspace is a fixed device array owned by this library, so a call allocates
+// nothing (no cudaMalloc, no cudaFree, no allocating library routine).
 //
 // The array is file-scope static device memory of kNoAllocScratchBytes (4 MiB). Every GPU that
 // loads the library keeps it until the process exits. The first call on a device looks up the
-// array's device address (cudaGetSymbolAddress) and caches it; make that first call before any
-// stream capture. All calls share it, so calls whose executions overlap
-// on the GPU (for example on two streams) race and must be serialised by the caller. The array
-// keeps the previous call's contents; each call first clears the control words that must start
-// at zero.
+// array's device address (cudaGetSymbolAddress) and caches it per device ordinal; the cache
+// does not survive a cudaDeviceReset of that device in the same process. All calls share the
+// array, so calls whose executions overlap on the GPU (for example on two streams) race and
+// must be serialised by the caller. The array keeps the previous call's contents; each call
+// first clears the control words that must start at zero. The status word is not cleared: a
+// device-side timeout stays recorded until moe_read_device_status(NULL, ...) reads and clears
+// it.
 #include "../../include/moe_nvfp4.h"
 #include "moe_internal.cuh"
 
@@ -50,6 +51,16 @@ void* scratch_address(int device, cudaError_t* err) {
 
 }  // namespace
 
+namespace moe {
+// The fixed array of the current device (for reading its status word), or null.
+void* noalloc_scratch_of_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  cudaError_t e;
+  return scratch_address(dev, &e);
+}
+}  // namespace moe
+
 extern "C" {
 
 moe_status moe_route_topk_noalloc(const uint16_t* x, const uint16_t* router_w, int T, int H, int E,
@@ -64,8 +75,15 @@ moe_status moe_route_topk_noalloc(const uint16_t* x, const uint16_t* router_w, i
   cudaError_t e;
   void* ws = scratch_address(dev, &e);
   if (!ws) return MOE_ERR_CUDA;
-  // The control words (router ticket, status, counts of the call) must start at zero.
-  e = cudaMemsetAsync(ws, 0, moe::kCtlWords * 4, static_cast<cudaStream_t>(stream));
+  // The control words before and after the status word (router ticket, counts of the call)
+  // must start at zero; the status word keeps an earlier call's error until it is read.
+  static_assert(moe::kCtlStatus == 1, "control word layout");
+  unsigned char* ctl = static_cast<unsigned char*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  e = cudaMemsetAsync(ctl, 0, moe::kCtlStatus * 4, s);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(ctl + (moe::kCtlStatus + 1) * 4, 0,
+                        (moe::kCtlWords - moe::kCtlStatus - 1) * 4, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   return moe_route_topk(x, router_w, T, H, E, k, idx, w, counts, offsets, perm, ws,
                         kNoAllocScratchBytes, stream);

@@ -4,8 +4,9 @@
 // bit-exact and what is quantized", keeps the shared experts and the shared-expert gate in BF16
 // and gives no formula; the Qwen-style form is taken. For token t:
 //   sigma_t = 1 / (1 + exp(-x_t . gv)),   hs = BF16( SiLU(Wg x_t) * (Wu x_t) ),   Ys = Wd hs,
-// all products exact BF16 x BF16 accumulated in FP32. Ys stays FP32 (unrounded): the combines
-// add sigma_t * Ys after the routed terms, before the output's rounding.
+// all products exact BF16 x BF16 accumulated in FP32. Ys is stored in FP32 as computed; the
+// combines round it to BF16 (an expert output, like the routed Y) and add sigma_t * BF16(Ys)
+// after the routed terms, before the output's rounding.
 //
 // Narrow calls (T <= 8) are two CUDA-core GEMVs over the BF16 weights (6 MB gate/up, 3 MB down
 // at H = 4096, Is = 384), one CTA per SM, each row read by one CTA with 16-byte loads on

@@ -118,10 +118,13 @@ def lib():
             L.oracle_moe_forward.argtypes = [ctypes.POINTER(_Inputs), ctypes.POINTER(_Outputs)]
             L.oracle_shared_expert.restype = None
             L.oracle_shared_expert.argtypes = [ctypes.c_void_p] + [ctypes.c_int] * 3 + \
-                [ctypes.c_void_p] * 7 + [ctypes.c_int]
+                [ctypes.c_void_p] * 8 + [ctypes.c_int]
             L.oracle_moe_forward_shared.restype = ctypes.c_int
             L.oracle_moe_forward_shared.argtypes = [ctypes.POINTER(_Inputs), ctypes.c_int] + \
-                [ctypes.c_void_p] * 3 + [ctypes.POINTER(_Outputs)] + [ctypes.c_void_p] * 4
+                [ctypes.c_void_p] * 3 + [ctypes.POINTER(_Outputs)] + [ctypes.c_void_p] * 5
+            L.oracle_h_ambiguity.restype = None
+            L.oracle_h_ambiguity.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.c_double,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
             _lib = L
     return _lib
 
@@ -175,6 +178,17 @@ def quantize_nvfp4(v: np.ndarray, S: float, nthreads: int = 1):
     lib().oracle_quantize_nvfp4(_ptr(v), rows, cols, float(S), _ptr(codes), _ptr(scales),
                                 int(nthreads))
     return codes, scales
+
+
+def h_ambiguity(v16: np.ndarray, S: float, eps: float, colnorm16: np.ndarray):
+    """The W4A4 h quantiser's ambiguity for one 16-element block of FP32 h values with down
+    input scale S (see h_ambiguity in moe_oracle.cpp): (elem [16], block) output allowances."""
+    v = _c(v16, np.float32).reshape(16)
+    cn = _c(colnorm16, np.float64).reshape(16)
+    elem = np.zeros(16, np.float64)
+    block = np.zeros(1, np.float64)
+    lib().oracle_h_ambiguity(_ptr(v), float(S), float(eps), _ptr(cn), _ptr(elem), _ptr(block))
+    return elem, float(block[0])
 
 
 def quantize_block_steps(v16: np.ndarray, S: float) -> dict:
@@ -271,7 +285,8 @@ class SharedExpert:
 
 def shared_expert(x_bf16: np.ndarray, shared: SharedExpert, nthreads: int = 1) -> dict:
     """The shared expert alone: sigma [T] (the gate), hs_bf16 [T, Is], h64 [T, Is] (h before
-    its BF16 rounding) and ys [T, H] (the down product, unrounded)."""
+    its BF16 rounding), ys [T, H] (the down product rounded to BF16, as FP64 values) and ys64
+    [T, H] (the down product before that rounding)."""
     x = _c(x_bf16, np.uint16)
     T, H = x.shape
     Is = shared.Is
@@ -279,10 +294,11 @@ def shared_expert(x_bf16: np.ndarray, shared: SharedExpert, nthreads: int = 1) -
     hs = np.empty((T, Is), np.uint16)
     h64 = np.empty((T, Is), np.float64)
     ys = np.empty((T, H), np.float64)
+    ys64 = np.empty((T, H), np.float64)
     lib().oracle_shared_expert(_ptr(x), T, H, Is, _ptr(shared.gate_up), _ptr(shared.down),
-                               _ptr(shared.gate), _ptr(sigma), _ptr(hs), _ptr(ys), _ptr(h64),
-                               int(nthreads))
-    return dict(sigma=sigma, hs_bf16=hs, h64=h64, ys=ys)
+                               _ptr(shared.gate), _ptr(sigma), _ptr(hs), _ptr(ys), _ptr(ys64),
+                               _ptr(h64), int(nthreads))
+    return dict(sigma=sigma, hs_bf16=hs, h64=h64, ys=ys, ys64=ys64)
 
 
 def forward(x_bf16: np.ndarray, wr_bf16: np.ndarray, experts: ExpertSet, k: int, mode: int,
@@ -291,7 +307,8 @@ def forward(x_bf16: np.ndarray, wr_bf16: np.ndarray, experts: ExpertSet, k: int,
                   "logits", "abssum"), shared: SharedExpert | None = None) -> dict:
     """Run the oracle forward; ``want`` names the outputs to return (see moe_oracle.cpp). With
     ``shared``, the shared expert's gated output is added before the final rounding (out_bf16
-    and out64 include it) and sigma, hs_bf16, hs64 (h before its rounding) and ys (unrounded)
+    and out64 include it) and sigma, hs_bf16, hs64 (h before its rounding), ys (the down product
+    rounded to BF16) and ys64 (before that rounding)
     are returned too."""
     x = _c(x_bf16, np.uint16)
     wr = _c(wr_bf16, np.uint16)
@@ -336,10 +353,11 @@ def forward(x_bf16: np.ndarray, wr_bf16: np.ndarray, experts: ExpertSet, k: int,
         res["hs_bf16"] = np.empty((T, shared.Is), np.uint16)
         res["hs64"] = np.empty((T, shared.Is), np.float64)
         res["ys"] = np.empty((T, H), np.float64)
+        res["ys64"] = np.empty((T, H), np.float64)
         rc = lib().oracle_moe_forward_shared(
             ctypes.byref(inp), shared.Is, _ptr(shared.gate_up), _ptr(shared.down),
             _ptr(shared.gate), ctypes.byref(outs), _ptr(res["sigma"]), _ptr(res["hs_bf16"]),
-            _ptr(res["ys"]), _ptr(res["hs64"]))
+            _ptr(res["ys"]), _ptr(res["ys64"]), _ptr(res["hs64"]))
     if rc != 0:
         raise ValueError(f"oracle forward failed with code {rc}")
     return res

@@ -203,6 +203,60 @@ void dequantize_rows(const uint8_t* codes, const uint8_t* scales, int64_t rows, 
     }
 }
 
+// Ambiguity of the W4A4 h quantiser's decisions, for tests that compare the oracle's codes
+// with an FP32 evaluation of h whose values may differ from the oracle's by up to eps times the
+// block's max |h| (eps is a tolerance reading: the FP32 evaluation error of h relative to the
+// block amax). For one 16-element block v (FP32 h values) with the down input scale S:
+//   - the block scale is ambiguous when the scaled amax t = fl32(a * inv6S) and t * (1 -/+ eps)
+//     encode to different E4M3 bytes; then block = sum_i |alt_i - dec_i| * colnorm_i, alt_i
+//     being element i decoded after Q with the other scale, dec_i with the block's own scale;
+//   - element i (block scale unchanged) is ambiguous when its scaled value fl32(v_i * r) moved
+//     by -/+ eps * a * r encodes to different E2M1 codes; then elem_i = |dec(alt code) -
+//     dec(code)| * dec(sf) * S * colnorm_i, alt code being the code on the other side.
+// colnorm_i = ||Wd[:, i]||_2, the factor by which a change of h_i moves the expert's output Y.
+// Everything else is 0. Pinned by: hand-built blocks at and around E2M1 and E4M3 rounding
+// boundaries against an interval test written independently in FP64, and a brute-force
+// perturbation of single elements re-quantised with the (separately pinned) quantiser.
+void h_ambiguity(const float* vb, float S, float inv6S, double eps, const double* colnorm,
+                 double* elem, double* block) {
+  const BlockQ q = quantize_block(vb, 16, inv6S, S);
+  const double sfv = kE4M3[q.sf];
+  float a = 0.0f;
+  for (int i = 0; i < 16; ++i) a = std::max(a, std::fabs(vb[i]));
+  double dec[16];
+  for (int i = 0; i < 16; ++i) dec[i] = e2m1_value(q.q[i]) * sfv * (double)S;
+  *block = 0.0;
+  if (eps > 0) {
+    const float tlo = (float)((double)q.t * (1.0 - eps));
+    const float thi = (float)((double)q.t * (1.0 + eps));
+    const int s_lo = e4m3_encode_nonneg(tlo), s_hi = e4m3_encode_nonneg(thi);
+    if (s_lo != s_hi) {
+      const int alt = (s_lo != q.sf) ? s_lo : s_hi;
+      const double altv = kE4M3[alt];
+      const float ralt = altv == 0.0 ? 0.0f : f32_div(1.0f, f32_mul((float)altv, S));
+      double contrib = 0.0;
+      for (int i = 0; i < 16; ++i) {
+        const double dalt =
+            altv == 0.0 ? 0.0 : e2m1_value(e2m1_encode(f32_mul(vb[i], ralt))) * altv * (double)S;
+        contrib += std::fabs(dalt - dec[i]) * colnorm[i];
+      }
+      *block = contrib;
+    }
+  }
+  for (int i = 0; i < 16; ++i) {
+    elem[i] = 0.0;
+    if (eps > 0 && q.r != 0.0f) {
+      const double xs = (double)f32_mul(vb[i], q.r);
+      const double win = eps * (double)a * (double)q.r;
+      const int c_lo = e2m1_encode((float)(xs - win)), c_hi = e2m1_encode((float)(xs + win));
+      if (c_lo != c_hi) {  // a +0/-0 pair contributes 0 but is still a valid flip
+        const int alt = (c_lo != q.q[i]) ? c_lo : c_hi;
+        elem[i] = std::fabs(e2m1_value(alt) - e2m1_value(q.q[i])) * sfv * (double)S * colnorm[i];
+      }
+    }
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -266,6 +320,12 @@ float oracle_quantize_weight_bf16(const uint16_t* w, int64_t rows, int64_t cols,
 void oracle_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows,
                              int64_t cols, double mult, double* out) {
   dequantize_rows(codes, scales, rows, cols, mult, out);
+}
+
+// The W4A4 h quantiser's ambiguity for one block (see h_ambiguity; pinned there).
+void oracle_h_ambiguity(const float* v16, float S, double eps, const double* colnorm16,
+                        double* elem16, double* block) {
+  h_ambiguity(v16, S, inv6S_of(S), eps, colnorm16, elem16, block);
 }
 
 // ------------------------------- routing
@@ -481,46 +541,11 @@ int oracle_moe_forward(const OracleMoeInputs* in, OracleMoeOutputs* out) {
             for (int i = 0; i < 8; ++i)
               out->hq_codes[(size_t)slot * (I / 2) + b * 8 + i] =
                   (uint8_t)(q.q[2 * i] | (q.q[2 * i + 1] << 4));
-          // Ambiguity of the decisions, for tests that compare against an FP32 computation of h:
-          // the block scale is ambiguous if the scaled amax lies within a relative window
-          // amb_eps of an E4M3 rounding boundary; an element is ambiguous if its scaled value
-          // lies within amb_eps * (scaled block amax) of an E2M1 rounding boundary.
-          const double eps = in->amb_eps;
-          float a = 0.0f;
-          for (int i = 0; i < 16; ++i) a = std::max(a, std::fabs(vb[i]));
-          if (out->h_amb_block) {
-            double contrib = 0.0;
-            const float tlo = (float)((double)q.t * (1.0 - eps));
-            const float thi = (float)((double)q.t * (1.0 + eps));
-            int s_lo = e4m3_encode_nonneg(tlo), s_hi = e4m3_encode_nonneg(thi);
-            if (eps > 0 && s_lo != s_hi) {
-              int alt = (s_lo != q.sf) ? s_lo : s_hi;
-              double altv = kE4M3[alt];
-              float ralt = altv == 0.0 ? 0.0f : f32_div(1.0f, f32_mul((float)altv, Sd));
-              for (int i = 0; i < 16; ++i) {
-                double dalt = altv == 0.0 ? 0.0
-                    : e2m1_value(e2m1_encode(f32_mul(vb[i], ralt))) * altv * (double)Sd;
-                contrib += std::fabs(dalt - hdec[b * 16 + i]) * colnorm[b * 16 + i];
-              }
-            }
-            out->h_amb_block[(size_t)slot * (I / 16) + b] = contrib;
-          }
-          if (out->h_amb_elem) {
-            for (int i = 0; i < 16; ++i) {
-              double contrib = 0.0;
-              if (eps > 0 && q.r != 0.0f) {
-                double xs = (double)f32_mul(vb[i], q.r);
-                double win = eps * (double)a * (double)q.r;
-                int c_lo = e2m1_encode((float)(xs - win)), c_hi = e2m1_encode((float)(xs + win));
-                if (c_lo != c_hi) {  // a +0/-0 pair contributes 0 but is still a valid flip
-                  int alt = (c_lo != q.q[i]) ? c_lo : c_hi;
-                  contrib = std::fabs(e2m1_value(alt) - e2m1_value(q.q[i])) * sfv * (double)Sd *
-                            colnorm[b * 16 + i];
-                }
-              }
-              out->h_amb_elem[(size_t)slot * I + b * 16 + i] = contrib;
-            }
-          }
+          double amb_e[16], amb_b = 0.0;
+          h_ambiguity(vb, Sd, i6d, in->amb_eps, colnorm.data() + b * 16, amb_e, &amb_b);
+          if (out->h_amb_block) out->h_amb_block[(size_t)slot * (I / 16) + b] = amb_b;
+          if (out->h_amb_elem)
+            for (int i = 0; i < 16; ++i) out->h_amb_elem[(size_t)slot * I + b * 16 + i] = amb_e[i];
         }
       }
       for (int r = 0; r < H; ++r) {
@@ -579,19 +604,20 @@ int oracle_moe_forward(const OracleMoeInputs* in, OracleMoeOutputs* out) {
 //   sigma_t = 1 / (1 + exp(-a_t))
 //   g_i     = sum_h x[t][h] * Wgu[i][h],  u_i = sum_h x[t][h] * Wgu[Is + i][h]
 //   hs_i    = BF16_RNE( silu(g_i) * u_i )              (as a routed expert's h in W4A16)
-//   Ys[t][r] = sum_i hs_i * Wd[r][i]                   (FP64, not rounded)
-// Ys enters the combine unrounded: the card fixes no rounding of the shared expert's output,
-// and the reading with the fewest roundings keeps it until the output's own rounding (a BF16
-// rounding here would turn the last-bit differences of any FP32 evaluation of h into whole
-// BF16 steps of Ys). The shared expert is BF16 in both modes: W4A4 concerns the NVFP4 routed
-// experts only. Outputs: sigma [T], hs_bf16 [T][Is], ys [T][H]; h64 [T][Is] (optional) is
-// silu(g)*u before the BF16 rounding.
+//   Ys[t][r] = BF16_RNE( sum_i hs_i * Wd[r][i] )      (FP64 sum, then rounded)
+// Ys is rounded to BF16 like a routed expert's output Y: the card stores the shared expert in
+// BF16 beside the other BF16 projections, and the reading that rounds the routed Y (each
+// expert's output is a BF16 tensor) applies to it in the same way. The shared expert is BF16
+// in both modes: W4A4 concerns the NVFP4 routed experts only. Outputs: sigma [T], hs_bf16
+// [T][Is], ys [T][H] (the rounded Ys as FP64 values); optional ys64 [T][H] (the sum before its
+// rounding) and h64 [T][Is] (silu(g)*u before its rounding).
 // Pinned by: equality with a routed expert whose dequantised weights are the shared weights,
 // a numpy float64 pipeline, the gate against scipy's logistic function, and closed-form
 // combines.
 void oracle_shared_expert(const uint16_t* x, int T, int H, int Is, const uint16_t* gate_up,
                           const uint16_t* down, const uint16_t* gate_vec, double* sigma,
-                          uint16_t* hs_bf16, double* ys, double* h64, int nthreads) {
+                          uint16_t* hs_bf16, double* ys, double* ys64, double* h64,
+                          int nthreads) {
   (void)nthreads;
   std::vector<double> gv(H);
   for (int hh = 0; hh < H; ++hh) gv[hh] = bf16_to_double(gate_vec[hh]);
@@ -622,14 +648,15 @@ void oracle_shared_expert(const uint16_t* x, int T, int H, int Is, const uint16_
       const uint16_t* wd = down + (size_t)r * Is;
       double y = 0.0;
       for (int i = 0; i < Is; ++i) y += hdec[i] * bf16_to_double(wd[i]);
-      ys[(size_t)t * H + r] = y;
+      ys[(size_t)t * H + r] = bf16_to_double(double_to_bf16(y));
+      if (ys64) ys64[(size_t)t * H + r] = y;
     }
   }
 }
 
 // The MoE step with the shared expert: the routed step of oracle_moe_forward, then
 //   out[t][r] = BF16_RNE( sum_{j=0..k-1} w[t][j] * Y_slot(t,j)[r] + sigma_t * Ys[t][r] )
-// (Y BF16 as in the routed step, Ys unrounded),
+// (Y and Ys both rounded to BF16),
 // the shared term added after the routed ones. out->out64 (if given) receives the sum before
 // the rounding; the other outputs are those of oracle_moe_forward.
 // Pinned by: a zero shared down matrix reproduces the routed step, and k = 1 with every routed
@@ -637,7 +664,7 @@ void oracle_shared_expert(const uint16_t* x, int T, int H, int Is, const uint16_
 int oracle_moe_forward_shared(const OracleMoeInputs* in, int Is, const uint16_t* gate_up,
                               const uint16_t* down, const uint16_t* gate_vec,
                               OracleMoeOutputs* out, double* sigma, uint16_t* hs_bf16,
-                              double* ys, double* h64) {
+                              double* ys, double* ys64, double* h64) {
   if (Is <= 0 || !gate_up || !down || !gate_vec || !sigma || !ys) return 3;
   const int T = in->T, H = in->H;
   std::vector<double> routed((size_t)T * H);
@@ -646,7 +673,7 @@ int oracle_moe_forward_shared(const OracleMoeInputs* in, int Is, const uint16_t*
   const int rc = oracle_moe_forward(in, out);
   out->out64 = keep;
   if (rc != 0) return rc;
-  oracle_shared_expert(in->x, T, H, Is, gate_up, down, gate_vec, sigma, hs_bf16, ys, h64,
+  oracle_shared_expert(in->x, T, H, Is, gate_up, down, gate_vec, sigma, hs_bf16, ys, ys64, h64,
                        in->nthreads);
   for (int t = 0; t < T; ++t) {
     for (int r = 0; r < H; ++r) {

@@ -418,6 +418,195 @@ def test_forward_w4a4_h_codes_are_q_of_h(tiny):
     assert np.all(res["h_amb_elem"] >= 0)
 
 
+# ------------------------------------------------------------------ W4A4 h ambiguity window
+# The oracle flags the W4A4 h quantiser's decisions that an FP32 evaluation of h could take the
+# other way (values within eps * block amax of a rounding boundary) and states how far each such
+# flip moves the expert's output. The expected values below are written independently: the
+# quantiser's steps in numpy float32 with the brute-force encoders of this file, and the windows
+# as closed FP64 intervals around the formats' rounding midpoints.
+_E2M1_MAGS = [abs(_e2m1_closed(c)) for c in range(8)]
+_E2M1_MIDS = [(_E2M1_MAGS[i] + _E2M1_MAGS[i + 1]) / 2 for i in range(7)]
+_E4M3_MAGS = [_e4m3_closed(b) for b in range(0x7F)]
+_E4M3_MIDS = [(_E4M3_MAGS[b] + _E4M3_MAGS[b + 1]) / 2 for b in range(0x7E)]
+_AMB_EPS = 2.0 ** -14
+
+
+def _e2m1_brute(v):
+    c = _nearest_brute(_E2M1_MAGS, min(abs(v), 6.0), list(range(8)))
+    return c | (8 if math.copysign(1, v) < 0 else 0)
+
+
+def _q_block_ref(v, S, sf=None):
+    """The quantiser's steps in numpy float32 (sf given: with that scale instead of its own)."""
+    v = np.asarray(v, np.float32)
+    S = np.float32(S)
+    inv6S = np.float32(1) / (np.float32(6) * S)
+    a = np.float32(np.abs(v).max())
+    t = a * inv6S
+    if sf is None:
+        sf = 0x7E if t >= 448 else _nearest_brute(_E4M3_MAGS, float(t), list(range(0x7F)))
+    if _E4M3_MAGS[sf] == 0:
+        return a, t, sf, np.float32(0), [0] * 16
+    r = np.float32(1) / (np.float32(_E4M3_MAGS[sf]) * S)
+    return a, t, sf, r, [_e2m1_brute(float(v[i] * r)) for i in range(16)]
+
+
+def _dec(codes, sf, S):
+    return np.array([_e2m1_closed(c) for c in codes]) * _E4M3_MAGS[sf] * float(np.float32(S))
+
+
+def _amb_ref(v, S, eps, cn):
+    a, t, sf, r, codes = _q_block_ref(v, S)
+    dec = _dec(codes, sf, S)
+    elem = np.zeros(16)
+    if r != 0:
+        unit = _E4M3_MAGS[sf] * float(np.float32(S))
+        win = eps * float(a) * float(r)
+        for i in range(16):
+            xs = abs(float(np.float32(v[i]) * r))
+            for j, m in enumerate(_E2M1_MIDS):
+                if xs - win <= m <= xs + win:
+                    elem[i] = (_E2M1_MAGS[j + 1] - _E2M1_MAGS[j]) * unit * cn[i]
+    block = 0.0
+    for b, m in enumerate(_E4M3_MIDS):
+        if float(t) * (1 - eps) <= m <= float(t) * (1 + eps):
+            alt = b if sf == b + 1 else b + 1
+            _, _, _, _, ac = _q_block_ref(v, S, sf=alt)
+            block = float(np.sum(np.abs(_dec(ac, alt, S) - dec) * cn))
+    return elem, block
+
+
+def _near(m, f, win):
+    """A scaled value at signed distance f * win from the midpoint m."""
+    return m + f * win
+
+
+def test_h_ambiguity_constructed_elements():
+    # S = 2^-8 and a block amax of 6 * S give the scale 1.0 (0x38) and r = 256 exactly, so an
+    # element's scaled value is v * 256 and the element window is eps * 6 in scaled units
+    S = 2.0 ** -8
+    win = _AMB_EPS * 6.0
+    cn = np.linspace(1.0, 2.5, 16)          # distinct column norms: a wrong index shows
+    scaled = [6.0,                           # the amax (never flagged: no boundary above 5)
+              0.75, 2.5,                     # exactly on midpoints (ties go to even)
+              _near(1.25, 0.6, win), _near(1.75, -0.6, win), _near(3.5, 0.3, win),
+              _near(5.0, -0.8, win),         # inside the window, on either side
+              _near(0.75, 1.6, win), _near(1.25, -2.0, win), _near(3.5, 4.0, win),
+              1.0, 3.0, 0.0,                 # representable, far from every boundary
+              -_near(0.25, 0.5, win),        # negative, inside the window of 0.25
+              -_near(5.0, 1.5, win),         # negative, outside
+              _near(0.25, -0.9, win)]
+    v = np.array(scaled, np.float32) / np.float32(256)
+    assert np.array_equal(v * np.float32(256), np.array(scaled, np.float32))
+    elem, block = oracle.h_ambiguity(v, S, _AMB_EPS, cn)
+    ref_e, ref_b = _amb_ref(v, S, _AMB_EPS, cn)
+    flagged = {1, 2, 3, 4, 5, 6, 13, 15}
+    assert set(np.nonzero(ref_e)[0].tolist()) == flagged
+    np.testing.assert_allclose(elem, ref_e, rtol=1e-12, atol=0)
+    assert block == 0.0 and ref_b == 0.0
+    # closed forms of a few: |dec(alt) - dec(code)| * dec(sf) * S * colnorm
+    assert elem[1] == pytest.approx(0.5 * S * cn[1], rel=1e-12)    # 0.5 <-> 1.0
+    assert elem[2] == pytest.approx(1.0 * S * cn[2], rel=1e-12)    # 2 <-> 3
+    assert elem[6] == pytest.approx(2.0 * S * cn[6], rel=1e-12)    # 4 <-> 6
+    assert elem[13] == pytest.approx(0.5 * S * cn[13], rel=1e-12)  # -0 <-> -0.5
+
+
+def test_h_ambiguity_constructed_block_scales():
+    S = 2.0 ** -8
+    cn = np.linspace(0.5, 3.0, 16)
+    rng = np.random.default_rng(51)
+    inv6S = np.float32(1) / (np.float32(6) * np.float32(S))
+    for m, f, want in ((1.0625, 0.0, True), (1.0625, 0.5, True), (1.0625, -0.6, True),
+                       (1.0625, 3.0, False), (1.0625, -2.5, False), (27.0 / 128, 0.4, True),
+                       (100.0, -0.7, True), (100.0, 1.3, False)):
+        t_want = m * (1 + f * _AMB_EPS)
+        a = np.float32(t_want * 6.0 * S)
+        rest = (rng.uniform(-1, 1, 15) * float(a)).astype(np.float32)
+        v = np.concatenate([[a], rest]).astype(np.float32)
+        t = float(np.float32(a) * inv6S)
+        assert abs(t / t_want - 1) < 1e-6
+        elem, block = oracle.h_ambiguity(v, S, _AMB_EPS, cn)
+        ref_e, ref_b = _amb_ref(v, S, _AMB_EPS, cn)
+        assert (ref_b > 0) == want, (m, f)
+        assert block == pytest.approx(ref_b, rel=1e-12, abs=0), (m, f)
+        np.testing.assert_allclose(elem, ref_e, rtol=1e-12, atol=0)
+
+
+def test_h_ambiguity_random_blocks_near_boundaries():
+    rng = np.random.default_rng(52)
+    for it in range(300):
+        S = float(np.float32(np.exp(rng.uniform(-9, -2))))
+        v = (rng.standard_normal(16) * np.exp(rng.uniform(-2, 2))).astype(np.float32)
+        a, t, sf, r, _ = _q_block_ref(v, S)
+        if r == 0:
+            continue
+        win = _AMB_EPS * float(a) * float(r)
+        amax_i = int(np.argmax(np.abs(v)))
+        for i in range(16):   # move some elements next to an E2M1 midpoint (the amax stays)
+            if i != amax_i and rng.random() < 0.5:
+                f = rng.uniform(-2.5, 2.5)
+                if 0.9 < abs(f) < 1.1:
+                    f = 0.5 * np.sign(f)
+                m = _E2M1_MIDS[int(rng.integers(0, 7))]
+                v[i] = np.float32(np.sign(rng.standard_normal()) * _near(m, f, win) / float(r))
+        cn = rng.uniform(0.1, 4.0, 16)
+        elem, block = oracle.h_ambiguity(v, S, _AMB_EPS, cn)
+        ref_e, ref_b = _amb_ref(v, S, _AMB_EPS, cn)
+        np.testing.assert_allclose(elem, ref_e, rtol=1e-12, atol=0, err_msg=str(it))
+        assert block == pytest.approx(ref_b, rel=1e-12, abs=0), it
+
+
+def test_h_ambiguity_flags_exactly_the_codes_a_perturbation_can_change():
+    # brute force: move one element by every delta on a fine grid of [-eps*a, eps*a] and
+    # re-quantise the block with the quantiser; its code changes for some delta exactly when
+    # the oracle flags it (elements placed off the window's edges, so the grid decides)
+    S = 2.0 ** -8
+    win = _AMB_EPS * 6.0
+    cn = np.ones(16)
+    rng = np.random.default_rng(53)
+    for it in range(40):
+        scaled = [6.0] + [float(_near(_E2M1_MIDS[int(rng.integers(0, 7))],
+                                      rng.choice([-1, 1]) * rng.choice([0.0, 0.3, 0.7, 1.4, 2.5]),
+                                      win)) * float(rng.choice([-1, 1])) for _ in range(15)]
+        v = np.array(scaled, np.float32) / np.float32(256)
+        elem, _ = oracle.h_ambiguity(v, S, _AMB_EPS, cn)
+        a = float(np.abs(v).max())
+        c0, s0 = oracle.quantize_nvfp4(v[None, :], S)
+        for i in range(1, 16):
+            changed = False
+            for d in np.linspace(-_AMB_EPS * a, _AMB_EPS * a, 201):
+                w = v.copy()
+                w[i] = np.float32(float(v[i]) + d)
+                c, s = oracle.quantize_nvfp4(w[None, :], S)
+                assert s[0, 0] == s0[0, 0]
+                ci = (c[0, i // 2] >> (4 * (i % 2))) & 0xF
+                c0i = (c0[0, i // 2] >> (4 * (i % 2))) & 0xF
+                if (ci & 7) != (c0i & 7):       # a change of magnitude (not only -0 / +0)
+                    changed = True
+                    break
+            assert changed == (elem[i] > 0), (it, i, scaled[i])
+
+
+def test_forward_h_ambiguity_is_the_block_function(tiny):
+    # the forward pass reports, for every slot and block, the block function's values with the
+    # expert's down-matrix column norms
+    wl, x, wr, ex = tiny
+    res = oracle.forward(x, wr, ex, wl.k, oracle.W4A4,
+                         want=("h", "idx", "counts", "h_amb_elem", "h_amb_block"))
+    offs = np.concatenate([[0], np.cumsum(res["counts"])])
+    for s in range(wl.T * wl.k):
+        e = int(np.searchsorted(offs, s, side="right") - 1)
+        Wd = oracle.dequantize_nvfp4(ex.down[e][0], ex.down[e][1], float(ex.mult[e, 2]))
+        cn = np.sqrt((Wd ** 2).sum(axis=0))
+        hf = res["h"][s].astype(np.float32)
+        for b in range(wl.I // 16):
+            ref_e, ref_b = _amb_ref(hf[b * 16:(b + 1) * 16], float(ex.in_scale[e, 2]),
+                                    _AMB_EPS, cn[b * 16:(b + 1) * 16])
+            np.testing.assert_allclose(res["h_amb_elem"][s, b * 16:(b + 1) * 16], ref_e,
+                                       rtol=1e-9, atol=0)
+            assert res["h_amb_block"][s, b] == pytest.approx(ref_b, rel=1e-9, abs=0)
+
+
 def test_synth_streams_are_deterministic_and_independent():
     a = synth.expert_weight(0, 3, 7, "gate", 64, 32)
     b = synth.expert_weight(0, 3, 7, "gate", 64, 32)
@@ -458,6 +647,10 @@ def test_shared_expert_equals_routed_expert_with_the_same_weights():
     ys_b = np.array([[oracle.double_to_bf16(v) for v in row] for row in sh["ys"]], np.uint16)
     hs_b = np.array([[oracle.double_to_bf16(v) for v in row] for row in sh["h64"]], np.uint16)
     assert np.array_equal(hs_b, sh["hs_bf16"])
+    # Ys is the BF16 rounding of the FP64 down product, like a routed expert's Y
+    assert np.array_equal(ys_b, np.array([[oracle.double_to_bf16(v) for v in row]
+                                          for row in sh["ys64"]], np.uint16))
+    assert np.array_equal(synth.bf16_to_f32(ys_b).astype(np.float64), sh["ys"])
     for t in range(T):
         for j in range(k):
             s = routed["slot_of"][t, j]
@@ -484,7 +677,22 @@ def test_shared_expert_matches_numpy_float64_pipeline():
     hb = np.array([[oracle.double_to_bf16(v) for v in row] for row in h], np.uint16)
     assert np.array_equal(hb, sh["hs_bf16"])
     y = synth.bf16_to_f32(hb).astype(np.float64) @ Wd.T
-    np.testing.assert_allclose(sh["ys"], y, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(sh["ys64"], y, rtol=1e-12, atol=1e-15)
+    yb = np.array([[oracle.double_to_bf16(v) for v in row] for row in sh["ys64"]], np.uint16)
+    assert np.array_equal(synth.bf16_to_f32(yb).astype(np.float64), sh["ys"])
+
+
+def test_shared_forward_adds_the_rounded_ys(tiny):
+    # out64 = (the routed sum) + sigma_t * BF16(Ys), the shared term added after the routed ones
+    wl, x, wr, ex = tiny
+    sh = oracle.SharedExpert(*synth.shared_expert_weights(46, 0, wl.H, wl.I))
+    a = oracle.forward(x, wr, ex, wl.k, oracle.W4A16)
+    b = oracle.forward(x, wr, ex, wl.k, oracle.W4A16, shared=sh)
+    assert not np.array_equal(b["ys"], b["ys64"])          # the rounding changed something
+    for t in range(wl.T):
+        assert np.array_equal(b["out64"][t], a["out64"][t] + b["sigma"][t] * b["ys"][t])
+    ob = np.array([[oracle.double_to_bf16(v) for v in row] for row in b["out64"]], np.uint16)
+    assert np.array_equal(ob, b["out_bf16"])
 
 
 def test_shared_gate_is_the_logistic_function():

@@ -1,10 +1,10 @@
 """The routing entry point for callers that cannot allocate device memory
-(moe_route_topk_noalloc: code running inside a CUDA graph capture, runtimes with a frozen
-allocator, embedders without a device allocator). Its workspace is a fixed device array inside
-the library; this test checks, through the C ABI, that two calls in a row give the results of
-moe_route_topk with a caller-provided workspace, on the decode and the grouped routing paths, and
-that shapes beyond the array are refused. It is collected last so that a run stopping at the
-first failure has run every other test."""
+(moe_route_topk_noalloc: runtimes whose allocator is frozen after start-up, embedders handed
+only their input and output buffers). Its workspace is a fixed device array inside the library;
+this test checks, through the C ABI, that two calls in a row give the results of moe_route_topk
+with a caller-provided workspace, on the decode and the grouped routing paths, that the array's
+status word reads back clean, and that shapes beyond the array are refused. It is collected last
+so that a run stopping at the first failure has run every other test."""
 import numpy as np
 import pytest
 import torch
@@ -34,6 +34,8 @@ def test_noalloc_routing_matches_workspace_routing(T, H, E, k):
         # same kernels, same inputs: the weights agree to FP32 rounding (here: exactly)
         np.testing.assert_allclose(got["w"].cpu().numpy(), ref["w"].cpu().numpy(), rtol=1e-6,
                                    atol=0)
+    # the fixed array's status word (kept across calls until read): no wait gave up
+    assert moe.moe_read_device_status(None) == 0
 
 
 def test_noalloc_routing_refuses_shapes_beyond_its_array():
