@@ -217,9 +217,7 @@ def run_reference(args, rank, world):
                 n_gpus=world, steps=cb["calls"], warmup=args.warmup,
                 ms_per_step=1e3 * n_tok / cb["value"],
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
-                data="synthetic", config=dict(workload=wl.name, T=wl.T, hidden=wl.H,
-                                              experts=wl.E, top_k=wl.k, inter=wl.I,
-                                              mode=["W4A16", "W4A4"][wl.mode]),
+                data="synthetic", config=bench_config(wl, args.layers or wl.layers, world, args),
                 cpu_baseline=cb,
                 e2e=dict(value=cb["value"], unit=cb["unit"], h2d_bytes_per_step=0,
                          d2h_bytes_per_step=0))
@@ -372,43 +370,71 @@ def measure(wl, stack, steps, warmup, use_graph, device, clocks=None):
     status = moe.moe_read_device_status(ws, stream=s)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    return e0.elapsed_time(e1) / steps, launches[0], info, (s, ws, oall, run)
+    return e0.elapsed_time(e1) / steps, launches[0], info, (s, ws, oall, run, step)
 
 
-def stage_times(wl, stack, reps, device):
-    """Mean duration of each stage (route, gate/up, down, combine) per layer, from CUDA events
-    recorded around each stage on the launching stream (PDL off while profiling)."""
+def kernel_label(name):
+    """A short label of a kernel name as cudaFuncGetName returns it (mangled or not)."""
+    import re
+    if not name:
+        return "?"
+    m = re.search(r"(k_[A-Za-z0-9_]+?)(I(?:L[a-z](-?\d+)E)+E)?(?:E|v|$)", name)
+    if m is None:
+        m2 = re.search(r"(k_[A-Za-z0-9_]+)(<[^>]*>)?", name)
+        return m2.group(0) if m2 else name[:40]
+    args = re.findall(r"L[a-z](-?\d+)E", m.group(2) or "")
+    return m.group(1) + (f"<{','.join(args)}>" if args else "")
+
+
+def launch_times(wl, stack, reps, device):
+    """Mean device time of each kernel launch of one forward call (per layer), from CUDA events
+    recorded around every launch on the launching stream (programmatic dependent launch off
+    while profiling): [(kernel, ms)]."""
     import torch
     import nvfp4_mixture_experts_bf16_gb300 as moe
     s = torch.cuda.Stream(device=device)
-    ws = moe.new_workspace(moe.moe_workspace_size(stack[0].pack, wl.T, wl.k, wl.mode), device)
+    sh = stack[0].shared
+    nws = (moe.moe_workspace_size(stack[0].pack, wl.T, wl.k, wl.mode) if sh is None else
+           moe.moe_workspace_size_shared(stack[0].pack, wl.T, wl.k, wl.mode, sh[0].shape[0] // 2))
+    ws = moe.new_workspace(nws, device)
     outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device=device) for _ in stack]
-    acc = np.zeros(4)
-    n = 0
+    acc, names, n = None, None, 0
     with torch.cuda.stream(s):
         for rep in range(reps + 1):
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in stack]
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(64)] for _ in stack]
             for ev in evs:          # torch creates the CUDA event at its first record
                 for e in ev:
                     e.record(s)
+            nl = []
             for L, o, ev in zip(stack, outs, evs):
                 moe.moe_profile_next_forward(ev)
-                moe.moe_forward(L.x, L.wr, L.pack, wl.k, wl.mode, out=o, ws=ws, stream=s)
+                if L.shared is None:
+                    moe.moe_forward(L.x, L.wr, L.pack, wl.k, wl.mode, out=o, ws=ws, stream=s)
+                else:
+                    moe.moe_forward_shared(L.x, L.wr, L.pack, L.shared, wl.k, wl.mode, out=o,
+                                           ws=ws, stream=s)
+                nl.append(min(moe.moe_last_launch_count(), 32))
+            names = [kernel_label(moe.moe_profile_kernel_name(i)) for i in range(nl[-1])]
             torch.cuda.synchronize()
             if rep == 0:
                 continue  # warm-up
-            for ev in evs:
-                acc += [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(4)]
+            for ev, k in zip(evs, nl):
+                t = np.array([ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(k)])
+                acc = t if acc is None else acc + t
                 n += 1
-    return acc / n  # ms per layer
+    return list(zip(names, (acc / n).tolist()))
 
 
-def e2e_measure(wl, stack, steps, state, device):
+def e2e_measure(wl, stack, steps, state, device, use_graph=True):
     """Same metric through the public API with host buffers: per step, copy every layer's x
     host->device (pinned; the layers' inputs are one [layers, T, H] buffer, so one copy), run
-    the step, copy every layer's out device->host (one copy of the [layers, T, H] outputs)."""
+    the step (the captured graph, or with use_graph=False every moe_forward call issued from
+    the host as a caller without graphs would), copy every layer's out device->host (one copy of
+    the [layers, T, H] outputs)."""
     import torch
-    s, ws, oall, run = state
+    s, ws, oall, run, step = state
+    if not use_graph:
+        run = step
     xall = stack[0].xall
     assert all(L.xall is xall for L in stack)
     hx = xall.cpu().pin_memory()
@@ -428,6 +454,65 @@ def e2e_measure(wl, stack, steps, state, device):
     ms = e0.elapsed_time(e1) / steps
     nbytes = len(stack) * wl.T * wl.H * 2
     return ms, nbytes
+
+
+def bench_config(wl, layers, world, args):
+    """The workload description both arms print (the same dict, so the lines compare)."""
+    return dict(workload=wl.name, T=wl.T, layers=layers, hidden=wl.H, experts=wl.E, top_k=wl.k,
+                inter=wl.I, mode=["W4A16", "W4A4"][wl.mode],
+                parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                l2=("no flush: a step streams 48 layers x 10 experts = 1.27 GB > 129 MB L2"
+                    if wl.T == 1 and layers >= 48 else
+                    "no flush: a step streams more expert bytes than the 129 MB L2 holds"),
+                graph=not args.no_graph, shared_expert=bool(args.shared))
+
+
+# FP4 dense tensor peak from the measured BF16 peak and NVIDIA's nominal dense ratio for GB300
+# (FP4 13.5 PFLOP/s : BF16 2.25 PFLOP/s = 6)
+FP4_PER_BF16 = 6.0
+
+
+def prefill_roofline(w3, ms3, kernels, U, pk, shared):
+    """The prefill chunk against both of its roofs: the tensor peak of its MMA kind (FP4 for
+    W4A4, BF16/FP16 for W4A16) and HBM for the bytes it must move at least once (the touched
+    experts' NVFP4 weights, the router, x in and out out); plus the dominant kernel (live per-
+    launch CUDA events) with its own FLOPs against the same peak."""
+    H, I, T, E, k = w3.H, w3.I, w3.T, w3.E, w3.k
+    gu_flops = 2 * T * k * 2 * I * H
+    dn_flops = 2 * T * k * I * H
+    flops = gu_flops + dn_flops
+    if w3.mode == 1:
+        peak = pk["bf16"] * FP4_PER_BF16
+        src = (f"{pk['src']} bf16_tflops {pk['bf16']} x {FP4_PER_BF16:g} (nominal dense "
+               "FP4:BF16 ratio, 13.5:2.25 PFLOP/s)")
+    else:
+        peak = pk["bf16"]
+        src = f"{pk['src']} bf16_tflops (kind::f16 runs at the BF16/FP16 rate)"
+    floor = U * (bytes_gateup(1, H, I) + bytes_down(1, H, I) + 12) + E * H * 2 + 2 * T * H * 2
+    tot = sum(t for _, t in kernels) or 1.0
+    dom_name, dom_ms = max(kernels, key=lambda kv: kv[1]) if kernels else ("?", 0.0)
+    dom_flops = (gu_flops if ("<0>" in dom_name or "<false>" in dom_name) and
+                 ("k_tc_gemm" in dom_name or "k_tc16" in dom_name) and "dn" not in dom_name
+                 else dn_flops if ("k_tc_gemm<1>" in dom_name or "k_tc16_dn" in dom_name or
+                                   "k_tc16<1>" in dom_name) else None)
+    achieved = flops / (ms3 * 1e-3) / 1e12
+    r = dict(bound="hbm" if floor / (pk["hbm"] * 1e9) > flops / (peak * 1e12) else "tensor",
+             achieved=round(achieved, 1), peak=round(peak, 1), unit="TFLOP/s",
+             frac=round(achieved / peak, 4), peak_source=src,
+             flops_per_chunk=flops,
+             hbm=dict(bytes_floor=int(floor), achieved_gbs=round(floor / (ms3 * 1e-3) / 1e9, 1),
+                      peak=pk["hbm"], frac=round(floor / (ms3 * 1e-3) / 1e9 / pk["hbm"], 4),
+                      floor_ms=round(floor / (pk["hbm"] * 1e9) * 1e3, 4),
+                      note="touched experts' NVFP4 weights + router + x + out, each once"),
+             dominant=dict(kernel=dom_name, ms=round(dom_ms, 4), share=round(dom_ms / tot, 4)),
+             kernels=[dict(kernel=n, ms=round(t, 4), share=round(t / tot, 4)) for n, t in kernels],
+             kernel_timing="CUDA events around each launch, PDL off (serialised)")
+    if dom_flops:
+        kt = dom_flops / (dom_ms * 1e-3) / 1e12
+        r["dominant"].update(tflops=round(kt, 1), frac=round(kt / peak, 4))
+    if shared:
+        r["note"] = "achieved counts the routed FLOPs only"
+    return r
 
 
 def run_native(args, rank, world, local_rank):
@@ -469,7 +554,7 @@ def run_native(args, rank, world, local_rank):
     peak_src = (f"{pk['src']} hbm_gbs (MEASURED_PEAKS.json)" if pk["src"] == "measured"
                 else "fallback 6.8 TB/s")
     fused = launches == layers   # one launch per layer: the persistent narrow-call kernel
-    stages = None
+    kern = None
     if args.shared:
         # the whole step (shared-expert kernels + the narrow-call kernel, or the wide path)
         gbs = layer_bytes / layer_s / 1e9
@@ -480,26 +565,37 @@ def run_native(args, rank, world, local_rank):
                         algorithmic_bytes_per_launch=None,
                         algorithmic_bytes_per_layer=int(layer_bytes), peak_source=peak_src)
     elif fused:
-        # the only kernel of the step: mean launch duration = event-timed step / launches
+        # the only kernel of the step: mean launch duration = event-timed step / launches.
+        # achieved = the selected experts' bytes (U x B_e, each read once), the router and the
+        # activations beside it
+        exp_bytes = gu_bytes + dn_bytes + 12 * U_mean
         dec_bytes = bytes_decode_launch(U_mean, wl.T, wl.H, wl.E, wl.I)
-        gbs = dec_bytes / layer_s / 1e9
+        gbs = exp_bytes / layer_s / 1e9
+        gbs_r = dec_bytes / layer_s / 1e9
         roofline = dict(bound="hbm", kernel="k_decode (whole narrow-call step, one launch)",
                         achieved=round(gbs, 1), peak=pk["hbm"], unit="GB/s",
                         frac=round(gbs / pk["hbm"], 4),
                         traffic=committed_traffic("k_decode", wl.name),
-                        algorithmic_bytes_per_launch=int(dec_bytes),
+                        algorithmic_bytes_per_launch=int(exp_bytes),
+                        bytes_counted="selected experts' NVFP4 codes, scales and multipliers",
+                        achieved_incl_router=round(gbs_r, 1),
+                        frac_incl_router=round(gbs_r / pk["hbm"], 4),
+                        bytes_incl_router=int(dec_bytes),
                         launch_us=round(layer_s * 1e6, 3), peak_source=peak_src)
     else:
-        st = stage_times(wl, stack, reps=3, device=device)
-        gu_gbs = gu_bytes / (st[1] * 1e-3) / 1e9
-        stages = dict(route=round(st[0] * 1e3, 2), gateup=round(st[1] * 1e3, 2),
-                      down=round(st[2] * 1e3, 2), combine=round(st[3] * 1e3, 2))
-        roofline = dict(bound="hbm", kernel="k_gateup (gate/up + SiLU*up)",
-                        achieved=round(gu_gbs, 1), peak=pk["hbm"], unit="GB/s",
-                        frac=round(gu_gbs / pk["hbm"], 4),
-                        traffic=committed_traffic("k_gateup", wl.name),
-                        algorithmic_bytes_per_launch=int(gu_bytes), peak_source=peak_src)
+        kern = launch_times(wl, stack, reps=3, device=device)
+        dom, dom_ms = max(kern, key=lambda kv: kv[1])
+        tot = sum(t for _, t in kern)
+        b = gu_bytes if "gateup" in dom else (dn_bytes if "down" in dom else gu_bytes + dn_bytes)
+        kgbs = b / (dom_ms * 1e-3) / 1e9
+        roofline = dict(bound="hbm", kernel=dom, achieved=round(kgbs, 1), peak=pk["hbm"],
+                        unit="GB/s", frac=round(kgbs / pk["hbm"], 4),
+                        traffic=committed_traffic(dom.split("<")[0], wl.name),
+                        algorithmic_bytes_per_launch=int(b), launch_us=round(dom_ms * 1e3, 3),
+                        share=round(dom_ms / tot, 4), peak_source=peak_src)
     e2e_ms, io_bytes = e2e_measure(wl, stack, max(3, args.steps // 2), state, device)
+    e2e_ng_ms, _ = e2e_measure(wl, stack, max(3, args.steps // 2), state, device,
+                               use_graph=False)
 
     extra = {}
     if not args.no_extra and not args.shared and rank == 0:
@@ -534,11 +630,14 @@ def run_native(args, rank, world, local_rank):
             if shared:
                 st3 = with_shared(st3, w3, args.seed, device)
             ms3, _, _, _ = measure(w3, st3, 3, 2, False, device)
+            kern3 = launch_times(w3, st3, reps=2, device=device)
             flops = 2 * w3.T * w3.k * 3 * w3.I * w3.H
             key = f"prefill8192_{['w4a16', 'w4a4'][mode]}" + ("_shared" if shared else "")
             extra[key] = dict(
                 tokens_per_s=round(w3.T / (ms3 / 1e3), 1), ms=round(ms3, 3),
                 expert_tflops=round(flops / (ms3 * 1e-3) / 1e12, 2),
+                unique_experts=st3[0].U,
+                roofline=prefill_roofline(w3, ms3, kern3, st3[0].U, pk, shared),
                 note=("tcgen05 block-scaled FP4 grouped GEMMs" if mode == 1 else
                       "tcgen05 kind::f16 grouped GEMMs, weights dequantised to f16 in shared "
                       "memory"))
@@ -561,22 +660,23 @@ def run_native(args, rank, world, local_rank):
         steps=args.steps, warmup=args.warmup, ms_per_step=round(ms, 5), higher_is_better=True,
         scaling="weak", vs_baseline=None, dtype="nvfp4 weights, bf16/f16 operands, f32 accum",
         data="synthetic", impl="native",
-        config=dict(workload=wl.name, T=wl.T, layers=layers, hidden=wl.H, experts=wl.E,
-                    top_k=wl.k, inter=wl.I, mode=["W4A16", "W4A4"][wl.mode],
-                    parallelism=f"replicas x{world}" if world > 1 else "single GPU",
-                    l2="no flush: a step streams 48 layers x 10 experts = 1.27 GB > 129 MB L2",
-                    graph=not args.no_graph, setup_s=round(setup_s, 1),
-                    shared_expert=bool(args.shared)),
+        config=bench_config(wl, layers, world, args), setup_s=round(setup_s, 1),
         gpu_launches=launches * args.steps,
         roofline=roofline,
         layer=dict(us=round(ms / layers * 1e3, 3), launches=launches // layers,
-                   stage_us=stages, hbm_gbs=round(layer_gbs, 1),
+                   kernel_us=None if kern is None else [(n, round(t * 1e3, 2)) for n, t in kern],
+                   hbm_gbs=round(layer_gbs, 1),
                    frac_hbm=round(layer_gbs / pk["hbm"], 4), unique_experts=U_mean,
                    note=("hbm_gbs: selected experts' bytes (U x B_e)"
                          + (" + the shared expert's BF16 bytes" if args.shared else "")
                          + " per layer time, router excluded")),
         e2e=dict(value=round(world * tokens_per_step / (e2e_ms / 1e3), 2), unit="layer-tokens/s",
-                 h2d_bytes_per_step=io_bytes, d2h_bytes_per_step=io_bytes),
+                 h2d_bytes_per_step=io_bytes, d2h_bytes_per_step=io_bytes,
+                 graph=not args.no_graph,
+                 no_graph_value=round(world * tokens_per_step / (e2e_ng_ms / 1e3), 2),
+                 note=("value: the step's calls replayed from a CUDA graph between the copies; "
+                       "no_graph_value: every call issued from the host (argument checks, "
+                       "launch) inside the timed region")),
         clocks=clk, cpu_baseline=cpu, secondary=extra)
     print(json.dumps(line), flush=True)
 

@@ -230,13 +230,17 @@ const char* moe_status_string(moe_status status);
  * launched. */
 int moe_last_launch_count(void);
 
-/* Profiling hook (measurement only; not needed for computing): for the NEXT moe_forward call
- * on this host thread, record cudaEvent_t events[2i] before and events[2i+1] after stage i on
- * the call's stream, stage 0 = routing and activation preparation (and the shared expert of
- * moe_forward_shared), 1 = gate/up + SiLU*up,
- * 2 = down, 3 = combine (count <= 8 uses the first count/2 stages). While profiling, the
- * stages are not overlapped by programmatic dependent launch. count = 0 cancels. */
+/* Profiling hook (measurement only; not needed for computing): for the NEXT moe_forward or
+ * moe_forward_shared call on this host thread, record cudaEvent_t events[2i] before and
+ * events[2i+1] after its i-th kernel launch on the call's stream (count <= 64 events, i.e. up to
+ * 32 launches; later launches are not recorded). While profiling, the launches are not
+ * overlapped by programmatic dependent launch. No other entry point may be called on this
+ * thread between arming and that call. count = 0 cancels. */
 moe_status moe_profile_next_forward(void* const* events, int count);
+
+/* Name of the kernel of the i-th launch of the last profiled call (cudaFuncGetName; static
+ * storage), or NULL. */
+const char* moe_profile_kernel_name(int i);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,7 @@ EXPORTED = ["moe_pack_nvfp4", "moe_pack_destroy", "moe_pack_info", "moe_pack_get
             "moe_workspace_offsets", "moe_quantize_act_nvfp4", "moe_read_device_status",
             "moe_status_string", "moe_last_launch_count", "moe_profile_next_forward",
             "moe_route_topk_noalloc", "moe_workspace_size_shared", "moe_forward_shared",
-            "moe_workspace_offsets_shared"]
+            "moe_workspace_offsets_shared", "moe_profile_kernel_name"]
 
 
 class MoeError(RuntimeError):
@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
             L.moe_status_string.restype = ctypes.c_char_p
             L.moe_last_launch_count.argtypes = []
             L.moe_profile_next_forward.argtypes = [vp, i32]
+            L.moe_profile_kernel_name.argtypes = [i32]
             L.moe_route_topk_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
             L.moe_workspace_size_shared.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
             L.moe_forward_shared.argtypes = [vp, vp, vp, ctypes.POINTER(_SharedExpert), i32, i32,
@@ -98,8 +99,9 @@ def lib() -> ctypes.CDLL:
                                                        ctypes.POINTER(sz), ctypes.POINTER(sz),
                                                        ctypes.POINTER(sz)]
             for n in EXPORTED:
-                if n not in ("moe_status_string",):
+                if n not in ("moe_status_string", "moe_profile_kernel_name"):
                     getattr(L, n).restype = ctypes.c_int
+            L.moe_profile_kernel_name.restype = ctypes.c_char_p
             _lib = L
     return _lib
 
@@ -325,10 +327,17 @@ def moe_last_launch_count() -> int:
 
 
 def moe_profile_next_forward(events) -> None:
-    """Record torch.cuda.Event objects around the stages of the next moe_forward call (see the
-    header): events[2i] before and events[2i+1] after stage i."""
+    """Record torch.cuda.Event objects around the kernel launches of the next moe_forward /
+    moe_forward_shared call (see the header): events[2i] before and events[2i+1] after the i-th
+    launch."""
     arr = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
     _check("moe_profile_next_forward", lib().moe_profile_next_forward(arr, len(events)))
+
+
+def moe_profile_kernel_name(i: int):
+    """Kernel name of the i-th launch of the last profiled call, or None."""
+    n = lib().moe_profile_kernel_name(int(i))
+    return None if n is None else n.decode()
 
 
 def moe_status_string(code: int) -> str:

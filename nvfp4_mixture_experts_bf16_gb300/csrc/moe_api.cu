@@ -28,14 +28,19 @@ struct moe_expert_pack {
 namespace {
 
 thread_local int g_last_launches = 0;
-// One-shot profiling events for the next moe_forward on this thread: events[2i] / events[2i+1]
-// are recorded on the call's stream before / after its i-th kernel launch.
-thread_local cudaEvent_t g_prof_events[32];
-thread_local int g_prof_count = 0;
+// One-shot per-launch profiling of the next forward call on this thread (see LaunchProf), and
+// the kernels the last profiled call launched.
+thread_local moe::LaunchProf g_prof = {};
+thread_local const void* g_prof_funcs[32] = {nullptr};
+thread_local int g_prof_nfuncs = 0;
 
-cudaError_t prof_mark(cudaStream_t s, int i) {
-  if (i < g_prof_count && g_prof_events[i]) return cudaEventRecord(g_prof_events[i], s);
-  return cudaSuccess;
+// Ends a profiled call: keeps its kernel list and switches profiling off.
+void prof_finish() {
+  if (g_prof.count == 0) return;
+  g_prof_nfuncs = g_prof.next < 32 ? g_prof.next : 32;
+  for (int i = 0; i < g_prof_nfuncs; ++i) g_prof_funcs[i] = g_prof.func[i];
+  g_prof.count = 0;
+  g_prof.next = 0;
 }
 
 constexpr size_t kAlign = 256;
@@ -180,6 +185,10 @@ bool route_shape_ok(int T, int H, int E, int k) {
 
 }  // namespace
 
+namespace moe {
+LaunchProf& launch_prof() { return g_prof; }
+}  // namespace moe
+
 extern "C" {
 
 const char* moe_status_string(moe_status s) {
@@ -198,10 +207,18 @@ const char* moe_status_string(moe_status s) {
 int moe_last_launch_count(void) { return g_last_launches; }
 
 moe_status moe_profile_next_forward(void* const* events, int count) {
-  if (count < 0 || count > 32 || (count > 0 && !events)) return MOE_ERR_INVALID_ARG;
-  for (int i = 0; i < count; ++i) g_prof_events[i] = static_cast<cudaEvent_t>(events[i]);
-  g_prof_count = count;
+  if (count < 0 || count > 64 || (count > 0 && !events)) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) g_prof.ev[i] = static_cast<cudaEvent_t>(events[i]);
+  g_prof.count = count;
+  g_prof.next = 0;
   return MOE_OK;
+}
+
+const char* moe_profile_kernel_name(int i) {
+  if (i < 0 || i >= g_prof_nfuncs || !g_prof_funcs[i]) return nullptr;
+  const char* name = nullptr;
+  if (cudaFuncGetName(&name, g_prof_funcs[i]) != cudaSuccess) return nullptr;
+  return name;
 }
 
 moe_status moe_pack_nvfp4(const moe_nvfp4_matrix* gate, const moe_nvfp4_matrix* up,
@@ -439,11 +456,10 @@ moe_status forward_impl(const uint16_t* x, const uint16_t* router_w, const moe_e
   const int m = (int)mode;
   cudaError_t e;
   int n = 0;
-  // stage i of the profile covers: 0 routing (+ activation prep, + the shared expert),
-  // 1 gate/up, 2 down, 3 combine
-  if (g_prof_count) lc.pdl = false;
-  e = prof_mark(lc.stream, 0);
-  if (sh && e == cudaSuccess) {
+  // while profiling, launches are not overlapped by programmatic dependent launch
+  if (g_prof.count) lc.pdl = false;
+  e = cudaSuccess;
+  if (sh) {
     // the shared expert first: the combine (of whichever path runs) adds its term
     unsigned char* b = static_cast<unsigned char*>(ws);
     moe::ShView sv;
@@ -460,11 +476,10 @@ moe_status forward_impl(const uint16_t* x, const uint16_t* router_w, const moe_e
     v.sh_sigma = sv.sigma;
   }
   if (narrow && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
-    // the whole routed step in one persistent kernel; the profile's later stages are empty
+    // the whole routed step in one persistent kernel
     if (e == cudaSuccess)
       e = moe::launch_decode(lc, pack->view, v, m, pack->x_scale, pack->x_inv6S, x, router_w, out);
-    for (int i = 1; i < 8 && e == cudaSuccess; ++i) e = prof_mark(lc.stream, i);
-    g_prof_count = 0;
+    prof_finish();
     g_last_launches = n + 1;
     return from_cuda(e);
   }
@@ -485,8 +500,6 @@ moe_status forward_impl(const uint16_t* x, const uint16_t* router_w, const moe_e
       n += 1;
     }
   }
-  if (e == cudaSuccess) e = prof_mark(lc.stream, 1);
-  if (e == cudaSuccess) e = prof_mark(lc.stream, 2);
   if (use_tc) {
     // x operand by padded slot, gate/up, (h operand,) down on tcgen05 (stage 1 covers all)
     if (e == cudaSuccess) {
@@ -498,30 +511,23 @@ moe_status forward_impl(const uint16_t* x, const uint16_t* router_w, const moe_e
         n += 4;
       }
     }
-    if (e == cudaSuccess) e = prof_mark(lc.stream, 3);
-    if (e == cudaSuccess) e = prof_mark(lc.stream, 4);
-  } else {
+      } else {
     if (e == cudaSuccess) {
       e = moe::launch_gateup(lc, pack->view, v, m, narrow);
       n += 1;
     }
-    if (e == cudaSuccess) e = prof_mark(lc.stream, 3);
-    if (e == cudaSuccess) e = prof_mark(lc.stream, 4);
-    if (e == cudaSuccess) {
+        if (e == cudaSuccess) {
       const long long S = (long long)T * k;
       const bool h_res = narrow && S * (2LL * I + 16) <= 96 * 1024;
       e = moe::launch_down(lc, pack->view, v, m, h_res);
       n += 1;
     }
   }
-  if (e == cudaSuccess) e = prof_mark(lc.stream, 5);
-  if (e == cudaSuccess) e = prof_mark(lc.stream, 6);
   if (e == cudaSuccess) {
     e = moe::launch_combine(lc, v, out);
     n += 1;
   }
-  if (e == cudaSuccess) e = prof_mark(lc.stream, 7);
-  g_prof_count = 0;
+  prof_finish();
   g_last_launches = n;
   return from_cuda(e);
 }

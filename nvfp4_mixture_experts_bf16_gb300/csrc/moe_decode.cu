@@ -1178,21 +1178,6 @@ __global__ void __launch_bounds__(kDcThreads, 1)
                  : "memory");
 }
 
-template <typename Kern, typename... Args>
-cudaError_t launch_pdl(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
 
 }  // namespace
 
@@ -1254,7 +1239,7 @@ cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView&
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(lc, kern, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, pk, ws,
+    return launch_kernel(lc, kern, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, pk, ws,
                       geo, x, wr, xS, x_inv6S, out);
   };
   if (mode == 1) {

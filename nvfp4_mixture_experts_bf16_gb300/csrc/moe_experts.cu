@@ -698,21 +698,6 @@ __global__ void k_pack_sf_atoms(const uint8_t* __restrict__ rg, const uint8_t* _
   }
 }
 
-template <typename Kern, typename... Args>
-cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
-                   Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
 
 }  // namespace
 
@@ -735,7 +720,7 @@ cudaError_t launch_gateup(const LaunchCfg& lc, const PackView& pk, const WsView&
   const int max_tasks = ws.G * geo.tiles;
   int grid = lc.num_sms < max_tasks ? lc.num_sms : max_tasks;
   if (grid < 1) grid = 1;
-  return launch(lc, k_gateup, dim3(grid), dim3(kGuThreads), smem, pk, ws, geo, mode,
+  return launch_kernel(lc, k_gateup, dim3(grid), dim3(kGuThreads), smem, pk, ws, geo, mode,
                 x_resident ? 1 : 0);
 }
 
@@ -754,7 +739,7 @@ cudaError_t launch_down(const LaunchCfg& lc, const PackView& pk, const WsView& w
   const int max_tasks = ws.G * geo.tiles;
   int grid = lc.num_sms < max_tasks ? lc.num_sms : max_tasks;
   if (grid < 1) grid = 1;
-  return launch(lc, k_down, dim3(grid), dim3(kDnThreads), smem, pk, ws, geo, mode,
+  return launch_kernel(lc, k_down, dim3(grid), dim3(kDnThreads), smem, pk, ws, geo, mode,
                 h_resident ? 1 : 0);
 }
 
@@ -764,7 +749,7 @@ cudaError_t launch_combine(const LaunchCfg& lc, const WsView& ws, uint16_t* out)
   const long long cap = (long long)lc.num_sms * 8;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  return launch(lc, k_combine, dim3((unsigned)grid), dim3(256), 0, ws, out);
+  return launch_kernel(lc, k_combine, dim3((unsigned)grid), dim3(256), 0, ws, out);
 }
 
 cudaError_t launch_pack_scales(cudaStream_t s, const uint8_t* raw_gate, const uint8_t* raw_up,

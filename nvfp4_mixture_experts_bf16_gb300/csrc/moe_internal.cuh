@@ -517,6 +517,48 @@ struct LaunchCfg {
   bool pdl;
 };
 
+// Per-launch profiling (measurement only): while `count` > 0 on this host thread, the i-th
+// kernel launch of a call records ev[2i] before it and ev[2i+1] after it on the call's stream,
+// and its function is kept in func[i]. Defined in moe_api.cu.
+struct LaunchProf {
+  cudaEvent_t ev[64];
+  int count;            // events supplied (0: profiling off)
+  int next;             // launches seen so far in the profiled call
+  const void* func[32];
+};
+LaunchProf& launch_prof();
+
+// Every kernel of a forward call is launched here: programmatic dependent launch when lc.pdl,
+// and the profiling events above when they are active.
+template <typename Kern, typename... Args>
+cudaError_t launch_kernel(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
+                          Args... args) {
+  LaunchProf& prof = launch_prof();
+  const int i = prof.next;
+  const bool rec = 2 * i + 1 < prof.count;
+  if (rec) {
+    const cudaError_t e = cudaEventRecord(prof.ev[2 * i], lc.stream);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = lc.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (rec) {
+    if (e == cudaSuccess) e = cudaEventRecord(prof.ev[2 * i + 1], lc.stream);
+    if (i < 32) prof.func[i] = reinterpret_cast<const void*>(kern);
+  }
+  if (prof.count > 0) prof.next = i + 1;
+  return e;
+}
+
 cudaError_t launch_route_narrow(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
                                 const WsView& ws, const PackView* pk, int mode, float xS,
                                 float x_inv6S,

@@ -609,21 +609,6 @@ __global__ void __launch_bounds__(256) k_quantize_rows(const uint16_t* __restric
   }
 }
 
-template <typename Kern, typename... Args>
-cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
-                   Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
 
 }  // namespace
 
@@ -645,7 +630,7 @@ cudaError_t launch_route_narrow(const LaunchCfg& lc, const uint16_t* x, const ui
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    return launch(lc, kern, dim3(grid), dim3(256), smem, x, wr, ws, pkv, pk ? 1 : 0, mode, xS,
+    return launch_kernel(lc, kern, dim3(grid), dim3(256), smem, x, wr, ws, pkv, pk ? 1 : 0, mode, xS,
                   x_inv6S, out);
   };
   switch (ws.T) {
@@ -674,24 +659,24 @@ cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint
     e = launch_tc_router(lc, x, wr, ws);
   } else {
     dim3 gg((ws.E + kGN - 1) / kGN, (ws.T + kGM - 1) / kGM);
-    e = launch(lc, k_router_gemm, gg, dim3(256), 0, x, wr, ws);
+    e = launch_kernel(lc, k_router_gemm, gg, dim3(256), 0, x, wr, ws);
   }
   if (e != cudaSuccess) return e;
-  e = launch(lc, k_topk_wide, dim3((ws.T + 7) / 8), dim3(256), 0, ws, out);
+  e = launch_kernel(lc, k_topk_wide, dim3((ws.T + 7) / 8), dim3(256), 0, ws, out);
   if (e != cudaSuccess) return e;
   const int nchunk = (ws.T + kChunkTok - 1) / kChunkTok;
-  e = launch(lc, k_hist_wide, dim3(nchunk), dim3(256), (size_t)ws.E * 4, ws);
+  e = launch_kernel(lc, k_hist_wide, dim3(nchunk), dim3(256), (size_t)ws.E * 4, ws);
   if (e != cudaSuccess) return e;
-  e = launch(lc, k_scan_wide, dim3(1), dim3(1024), 0, ws, pkv, pk ? 1 : 0, out, nchunk);
+  e = launch_kernel(lc, k_scan_wide, dim3(1), dim3(1024), 0, ws, pkv, pk ? 1 : 0, out, nchunk);
   if (e != cudaSuccess) return e;
-  e = launch(lc, k_scatter_wide, dim3(nchunk), dim3(256), (size_t)kChunkTok * ws.k * 4, ws, out);
+  e = launch_kernel(lc, k_scatter_wide, dim3(nchunk), dim3(256), (size_t)kChunkTok * ws.k * 4, ws, out);
   if (launches) *launches += 5;
   return e;
 }
 
 cudaError_t launch_xprep_wide(const LaunchCfg& lc, const uint16_t* x, const WsView& ws, int mode,
                               float xS, float x_inv6S) {
-  return launch(lc, k_xprep_wide, dim3(ws.T), dim3(256), 0, x, ws, mode, xS, x_inv6S);
+  return launch_kernel(lc, k_xprep_wide, dim3(ws.T), dim3(256), 0, x, ws, mode, xS, x_inv6S);
 }
 
 cudaError_t launch_quantize_rows(const LaunchCfg& lc, const uint16_t* x, int rows, int cols,
@@ -701,7 +686,7 @@ cudaError_t launch_quantize_rows(const LaunchCfg& lc, const uint16_t* x, int row
   const long long cap = (long long)lc.num_sms * 16;
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
-  return launch(lc, k_quantize_rows, dim3((unsigned)grid), dim3(256), 0, x, rows, cols, S, inv6S,
+  return launch_kernel(lc, k_quantize_rows, dim3((unsigned)grid), dim3(256), 0, x, rows, cols, S, inv6S,
                 codes, scales);
 }
 

@@ -229,21 +229,6 @@ __global__ void __launch_bounds__(kShThreads)
   if (tid == 0) sv.sigma[t] = 1.0f / (1.0f + expf(-part[0]));
 }
 
-template <typename Kern, typename... Args>
-cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
-                   Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
 
 template <int NT>
 cudaError_t launch_narrow(const LaunchCfg& lc, const uint16_t* x, const ShView& sv, int H) {
@@ -252,10 +237,10 @@ cudaError_t launch_narrow(const LaunchCfg& lc, const uint16_t* x, const ShView& 
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xs_bytes);
   if (e != cudaSuccess) return e;
   const int gu_grid = lc.num_sms < sv.Is + 1 ? lc.num_sms : sv.Is + 1;
-  e = launch(lc, k_shared_gu_narrow<NT>, dim3(gu_grid), dim3(kShThreads), xs_bytes, x, sv, H);
+  e = launch_kernel(lc, k_shared_gu_narrow<NT>, dim3(gu_grid), dim3(kShThreads), xs_bytes, x, sv, H);
   if (e != cudaSuccess) return e;
   const int dn_grid = lc.num_sms < H ? lc.num_sms : H;
-  return launch(lc, k_shared_dn_narrow<NT>, dim3(dn_grid), dim3(kShThreads), hs_bytes, sv, H);
+  return launch_kernel(lc, k_shared_dn_narrow<NT>, dim3(dn_grid), dim3(kShThreads), hs_bytes, sv, H);
 }
 
 }  // namespace
@@ -284,7 +269,7 @@ cudaError_t launch_shared(const LaunchCfg& lc, const uint16_t* x, const ShView& 
   g.logits = sv.gu;
   cudaError_t e = launch_tc_router(lc, x, sv.gate_up, g);
   if (e != cudaSuccess) return e;
-  e = launch(lc, k_shared_act_wide, dim3(T), dim3(kShThreads), 0, x, sv, T, H);
+  e = launch_kernel(lc, k_shared_act_wide, dim3(T), dim3(kShThreads), 0, x, sv, T, H);
   if (e != cudaSuccess) return e;
   // down: [T][H] = hs [T][Is] . Wd [H][Is]^T
   WsView d = ws;

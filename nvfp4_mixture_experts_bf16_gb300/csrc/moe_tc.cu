@@ -1242,21 +1242,6 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t row
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Kern, typename... Args>
-cudaError_t launch(const LaunchCfg& lc, Kern kern, dim3 grid, dim3 block, size_t smem,
-                   Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = lc.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = lc.pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
 
 }  // namespace
 
@@ -1285,7 +1270,7 @@ cudaError_t launch_tc_router(const LaunchCfg& lc, const uint16_t* x, const uint1
   if (e != cudaSuccess) return e;
   const int tiles = ((ws.E + 127) / 128) * ((ws.T + 127) / 128);
   const int grid = tiles < lc.num_sms ? tiles : lc.num_sms;
-  return launch(lc, tc::k_tc_router, dim3(grid), dim3(tc::kRThreads), smem, m_w, m_x, ws);
+  return launch_kernel(lc, tc::k_tc_router, dim3(grid), dim3(tc::kRThreads), smem, m_w, m_x, ws);
 }
 
 cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
@@ -1299,7 +1284,7 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
       !make_map(&m_down, pk.down_codes, I / 2, (uint64_t)E * H, 128) ||
       !make_map(&m_h, ws.hq_perm, I / 2, P, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch(lc, tc::k_xquant_perm, dim3((ws.T + tc::kXqTok - 1) / tc::kXqTok),
+  cudaError_t e = launch_kernel(lc, tc::k_xquant_perm, dim3((ws.T + tc::kXqTok - 1) / tc::kXqTok),
                          dim3(64 * tc::kXqTok), 0, x, ws, xS, x_inv6S);
   if (e != cudaSuccess) return e;
   const size_t smem = tc_smem_bytes();
@@ -1321,7 +1306,7 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
   pg.nks = H / tc::kStageK;
   pg.last_k4 = 4;
   const int grid = lc.num_sms;
-  e = launch(lc, tc::k_tc_gemm<false>, dim3(grid), dim3(tc::kThreads), smem, m_gate, m_up, m_x, pg,
+  e = launch_kernel(lc, tc::k_tc_gemm<false>, dim3(grid), dim3(tc::kThreads), smem, m_gate, m_up, m_x, pg,
              ws);
   if (e != cudaSuccess) return e;
   tc::TcParams pd = pg;
@@ -1330,7 +1315,7 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
   pd.MT = H / 128;
   pd.nks = (I + tc::kStageK - 1) / tc::kStageK;
   pd.last_k4 = ((I % tc::kStageK) ? (I % tc::kStageK) : tc::kStageK) / 64;
-  return launch(lc, tc::k_tc_gemm<true>, dim3(grid), dim3(tc::kThreads), smem, m_down, m_down, m_h,
+  return launch_kernel(lc, tc::k_tc_gemm<true>, dim3(grid), dim3(tc::kThreads), smem, m_down, m_down, m_h,
                 pd, ws);
 }
 
@@ -1349,7 +1334,7 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
       !make_map(&m_down, pk.down_codes, I / 2, (uint64_t)E * H, 128, 32) ||
       !make_map(&m_h, ws.hf_perm, (uint64_t)I * 2, P, 128))
     return cudaErrorInvalidValue;
-  cudaError_t e = launch(lc, tc::k_xprep16_perm, dim3((ws.T + tc::kXqTok - 1) / tc::kXqTok),
+  cudaError_t e = launch_kernel(lc, tc::k_xprep16_perm, dim3((ws.T + tc::kXqTok - 1) / tc::kXqTok),
                          dim3(64 * tc::kXqTok), 0, x, ws);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc::k_tc16<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1370,10 +1355,10 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
   pg.nks = H / 64;
   pg.last_k4 = 0;
   const int grid = lc.num_sms;
-  e = launch(lc, tc::k_tc16<false>, dim3(grid), dim3(tc::kT16Threads), tc::T16<false>::kSmem,
+  e = launch_kernel(lc, tc::k_tc16<false>, dim3(grid), dim3(tc::kT16Threads), tc::T16<false>::kSmem,
              m_gate, m_up, m_x, pg, ws);
   if (e != cudaSuccess) return e;
-  e = launch(lc, tc::k_hprep16, dim3(ws.NT), dim3(256), 0, ws);
+  e = launch_kernel(lc, tc::k_hprep16, dim3(ws.NT), dim3(256), 0, ws);
   if (e != cudaSuccess) return e;
   tc::TcParams pd = pg;
   pd.sfa = pk.sfa_down;
@@ -1387,10 +1372,10 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
     const int smem = abytes + nst * tc::kDnStage + 1024;
     e = cudaFuncSetAttribute(tc::k_tc16_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch(lc, tc::k_tc16_dn, dim3(grid), dim3(tc::kT16Threads), (size_t)smem, m_down, m_h,
+    return launch_kernel(lc, tc::k_tc16_dn, dim3(grid), dim3(tc::kT16Threads), (size_t)smem, m_down, m_h,
                   pd, ws, nst);
   }
-  return launch(lc, tc::k_tc16<true>, dim3(grid), dim3(tc::kT16Threads), tc::T16<true>::kSmem,
+  return launch_kernel(lc, tc::k_tc16<true>, dim3(grid), dim3(tc::kT16Threads), tc::T16<true>::kSmem,
                 m_down, m_down, m_h, pd, ws);
 }
 
