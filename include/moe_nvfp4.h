@@ -209,6 +209,41 @@ moe_status moe_workspace_offsets(const moe_expert_pack* pack, int T, int k, moe_
 moe_status moe_workspace_offsets_shared(const moe_expert_pack* pack, int T, int k, moe_mode mode,
                                         int shared_inter, size_t* h, size_t* sigma, size_t* y);
 
+/* Workspace bytes moe_forward_layers needs for `layers` layers shaped like `pack` (same
+ * zero-fill rule as moe_workspace_size): the control words and one region per layer. */
+moe_status moe_workspace_size_layers(const moe_expert_pack* pack, int layers, int T, int k,
+                                     moe_mode mode, size_t* bytes);
+
+/* Offsets of layer `layer`'s intermediate results inside a moe_forward_layers workspace (as
+ * moe_workspace_offsets for a single call), for tests. */
+moe_status moe_workspace_offsets_layers(const moe_expert_pack* pack, int layers, int T, int k,
+                                        moe_mode mode, int layer, moe_ws_offsets* offsets);
+
+/* The MoE step of `layers` consecutive layers of a stack, chained through the residual stream:
+ * layer 0 reads x [T][H]; layer l + 1 reads x_{l+1} = BF16(x_l + out_l), layer l's input plus
+ * its output, as a decoder layer adds its MoE output to the residual stream (a reading: the
+ * pages chain the layers of the stack but print no formula; attention and norms between the
+ * MoE steps are not part of this library). The release notes "Infernix windows-2026.10.11",
+ * section "Highlights", chain the expert passes by programmatic dependent launch and the
+ * Inferno fork's README runs decode under CUDA graphs; here narrow calls (T <= 8) go further:
+ * up to 32 layers run in ONE persistent launch of the fused kernel, whose CTAs stage layer
+ * l + 1's router rows in shared memory while layer l finishes and take layer l + 1's input from
+ * layer l's output tiles as each arrives (no kernel boundary between the layers); longer
+ * stacks take one launch per 32 layers. Other shapes run the same chain as one
+ * moe_forward-style launch sequence per layer plus the residual sum.
+ *   x         device [T][H] BF16, the first layer's input.
+ *   router_w  host array of `layers` device pointers, router_w[l] [E][H] BF16.
+ *   packs     host array of `layers` packs with equal hidden, inter and expert counts.
+ *   out       device [layers][T][H] BF16: out[l] is layer l's MoE output (moe_forward of x_l);
+ *             must not overlap x.
+ * Every layer's output equals moe_forward's on the same input (bit for bit on the fused path).
+ * W4A4 requires each pack's gate/up input scales to be equal (else MOE_ERR_UNSUPPORTED).
+ * ws/ws_bytes: see moe_workspace_size_layers. */
+moe_status moe_forward_layers(const uint16_t* x, const uint16_t* const* router_w,
+                              const moe_expert_pack* const* packs, int layers, int T, int k,
+                              moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
+                              void* stream);
+
 /* NVFP4 quantiser Q (test hook, also usable to build checkpoints): rows x cols BF16 values
  * (device, cols % 16 == 0) -> codes [rows][cols/2] and E4M3 scales [rows][cols/16] (device),
  * with per-matrix FP32 scale S = input_scale (> 0, finite). Steps, per 16-element block:

@@ -28,7 +28,8 @@ EXPORTED = ["moe_pack_nvfp4", "moe_pack_destroy", "moe_pack_info", "moe_pack_get
             "moe_workspace_offsets", "moe_quantize_act_nvfp4", "moe_read_device_status",
             "moe_status_string", "moe_last_launch_count", "moe_profile_next_forward",
             "moe_route_topk_noalloc", "moe_workspace_size_shared", "moe_forward_shared",
-            "moe_workspace_offsets_shared", "moe_profile_kernel_name"]
+            "moe_workspace_offsets_shared", "moe_profile_kernel_name",
+            "moe_workspace_size_layers", "moe_workspace_offsets_layers", "moe_forward_layers"]
 
 
 class MoeError(RuntimeError):
@@ -91,6 +92,10 @@ def lib() -> ctypes.CDLL:
             L.moe_last_launch_count.argtypes = []
             L.moe_profile_next_forward.argtypes = [vp, i32]
             L.moe_profile_kernel_name.argtypes = [i32]
+            L.moe_workspace_size_layers.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
+            L.moe_workspace_offsets_layers.argtypes = [vp, i32, i32, i32, i32, i32,
+                                                       ctypes.POINTER(_WsOffsets)]
+            L.moe_forward_layers.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]
             L.moe_route_topk_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
             L.moe_workspace_size_shared.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
             L.moe_forward_shared.argtypes = [vp, vp, vp, ctypes.POINTER(_SharedExpert), i32, i32,
@@ -262,6 +267,40 @@ def moe_forward(x, router_w, pack: Pack, k: int, mode: int, out=None, ws=None, s
         ws = new_workspace(moe_workspace_size(pack, T, k, mode), x.device)
     _check("moe_forward", lib().moe_forward(_bits(x), _bits(router_w), pack.handle, T, k, mode,
                                             _bits(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def moe_workspace_size_layers(pack: Pack, layers: int, T: int, k: int, mode: int) -> int:
+    n = ctypes.c_size_t()
+    _check("moe_workspace_size_layers", lib().moe_workspace_size_layers(
+        pack.handle, layers, T, k, mode, ctypes.byref(n)))
+    return n.value
+
+
+def moe_workspace_offsets_layers(pack: Pack, layers: int, T: int, k: int, mode: int,
+                                 layer: int) -> dict:
+    o = _WsOffsets()
+    _check("moe_workspace_offsets_layers", lib().moe_workspace_offsets_layers(
+        pack.handle, layers, T, k, mode, layer, ctypes.byref(o)))
+    return {n: getattr(o, n) for n, _ in _WsOffsets._fields_}
+
+
+def moe_forward_layers(x, router_ws, packs, k: int, mode: int, out=None, ws=None, stream=None):
+    """The chained MoE step of len(packs) layers: x [T,H] BF16 is layer 0's input, layer l+1
+    reads layer l's output; returns out [layers,T,H] BF16 (out[l] = layer l's output)."""
+    import torch
+    T, H = x.shape
+    L = len(packs)
+    assert len(router_ws) == L
+    if out is None:
+        out = torch.empty((L, T, H), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = new_workspace(moe_workspace_size_layers(packs[0], L, T, k, mode), x.device)
+    rw = (ctypes.c_void_p * L)(*[_bits(w).value for w in router_ws])
+    pk = (ctypes.c_void_p * L)(*[p.handle.value if isinstance(p.handle, ctypes.c_void_p)
+                                 else p.handle for p in packs])
+    _check("moe_forward_layers", lib().moe_forward_layers(
+        _bits(x), rw, pk, L, T, k, mode, _bits(out), _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

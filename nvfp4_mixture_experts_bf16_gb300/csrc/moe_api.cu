@@ -72,7 +72,7 @@ int num_sms_of_current_device() {
 
 struct WsLayout {
   size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm,
-      chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, htag, ytag, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
+      chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, htag, ytag, otag, xres, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
       xsf_atoms, hq_perm, hsf_atoms, xh_perm, hf_perm, sh_hs, sh_sigma, sh_y, sh_gu, total;
   size_t slot_amax_bytes;
   int G, NT;
@@ -129,6 +129,10 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode, int Is = 0) {
   L.sh_sigma = take(Is > 0 ? (size_t)T * 4 : 0);
   L.sh_y = take(Is > 0 ? (size_t)T * H * 4 : 0);
   L.sh_gu = take(Is > 0 && !narrow ? (size_t)T * 2 * Is * 4 : 0);
+  // chained layers: the next layer's input (this layer's input + output) as tagged BF16 pairs
+  // (narrow calls) and plainly
+  L.otag = take(mode >= 0 && narrow ? (size_t)T * (H / 2) * 8 : 0);
+  L.xres = take(mode >= 0 ? (size_t)T * H * 2 : 0);
   L.total = o;
   return L;
 }
@@ -157,6 +161,7 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   v.y = reinterpret_cast<uint16_t*>(b + L.y);
   v.htag = reinterpret_cast<unsigned long long*>(b + L.htag);
   v.ytag = reinterpret_cast<unsigned long long*>(b + L.ytag);
+  v.otag = reinterpret_cast<unsigned long long*>(b + L.otag);
   v.T = T; v.H = H; v.E = E; v.k = k; v.I = I; v.G = L.G; v.NT = L.NT;
   const bool tc = L.NT > 0;
   v.tt_expert = tc ? reinterpret_cast<int32_t*>(b + L.tt_expert) : nullptr;
@@ -181,6 +186,22 @@ moe_status from_cuda(cudaError_t e) {
 bool route_shape_ok(int T, int H, int E, int k) {
   return T >= 1 && T <= 65536 && H >= 128 && H % 128 == 0 && H <= 8192 && E >= 1 && E <= 1024 &&
          k >= 1 && k <= E && k <= 32;
+}
+
+// Chained layers: the control words, then one region per layer laid out as a single call's
+// workspace without its control words.
+size_t layer_stride(const WsLayout& L) { return L.total - L.gmeta; }
+size_t layers_total(const WsLayout& L, int layers) { return L.gmeta + layers * layer_stride(L); }
+
+// The view of layer l's region (control words shared), as the kernels' own layer view.
+moe::WsView shift_view(moe::WsView v, size_t off) {
+  auto mv = [&](auto*& p) { moe::shift_ptr(p, off); };
+  mv(v.gmeta); mv(v.slot_amax); mv(v.logits); mv(v.idx); mv(v.w); mv(v.slot_of); mv(v.counts);
+  mv(v.offsets); mv(v.perm); mv(v.chunk_base); mv(v.xh); mv(v.xfac); mv(v.xq); mv(v.xsf);
+  mv(v.h16); mv(v.hq); mv(v.hsf); mv(v.y); mv(v.htag); mv(v.ytag); mv(v.otag); mv(v.tt_expert);
+  mv(v.tt_slot0); mv(v.tt_n); mv(v.ttbase); mv(v.xq_perm); mv(v.xsf_atoms); mv(v.hq_perm);
+  mv(v.hsf_atoms); mv(v.xh_perm); mv(v.hf_perm);
+  return v;
 }
 
 }  // namespace
@@ -433,6 +454,86 @@ bool shared_ok(const moe_shared_expert* sh, int H) {
          sh->inter <= 2048 && H % 64 == 0;
 }
 
+// The launch sequence of one call on a prepared workspace view: the shared expert first (when
+// given; its buffers at the offsets of L in the workspace at `wsb`), then the routed step on the
+// fused narrow kernel, the multi-kernel narrow path or the grouped wide path. Adds the kernels
+// launched to *n.
+cudaError_t launch_forward(moe::LaunchCfg lc, const moe_expert_pack* pack,
+                           const moe_shared_expert* sh, const WsLayout& L, unsigned char* wsb,
+                           moe::WsView v, int m, const uint16_t* x, const uint16_t* router_w,
+                           uint16_t* out, int* n) {
+  const int T = v.T, H = v.H, E = v.E, k = v.k, I = v.I;
+  const bool narrow = T <= moe::kNarrowT;
+  cudaError_t e = cudaSuccess;
+  if (sh) {
+    // the shared expert first: the combine (of whichever path runs) adds its term
+    moe::ShView sv;
+    sv.gate_up = sh->gate_up;
+    sv.down = sh->down;
+    sv.gate = sh->gate;
+    sv.hs = reinterpret_cast<uint16_t*>(wsb + L.sh_hs);
+    sv.sigma = reinterpret_cast<float*>(wsb + L.sh_sigma);
+    sv.ys = reinterpret_cast<float*>(wsb + L.sh_y);
+    sv.gu = reinterpret_cast<float*>(wsb + L.sh_gu);
+    sv.Is = sh->inter;
+    e = moe::launch_shared(lc, x, sv, v, n);
+    v.sh_y = sv.ys;
+    v.sh_sigma = sv.sigma;
+  }
+  if (narrow && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
+    // the whole routed step in one persistent kernel
+    const moe::DcLayer dl{pack->view, router_w, out, pack->x_scale, pack->x_inv6S};
+    if (e == cudaSuccess) e = moe::launch_decode(lc, &dl, 1, 0, v, m, x, nullptr);
+    *n += 1;
+    return e;
+  }
+  if (narrow) {
+    if (e == cudaSuccess)
+      e = moe::launch_route_narrow(lc, x, router_w, v, &pack->view, m, pack->x_scale,
+                                   pack->x_inv6S, v.idx, v.w, v.counts, v.offsets, v.perm);
+    *n += 1;
+  }
+  // wide calls run the tensor-core grouped path when the layout reserved its token tiles
+  const bool use_tc = !narrow && v.NT > 0;
+  if (!narrow) {
+    if (e == cudaSuccess)
+      e = moe::launch_route_wide(lc, x, router_w, v, &pack->view, v.idx, v.w, v.counts, v.offsets,
+                                 v.perm, n);
+    if (e == cudaSuccess && !use_tc) {   // the tensor-core path quantises x itself
+      e = moe::launch_xprep_wide(lc, x, v, m, pack->x_scale, pack->x_inv6S);
+      *n += 1;
+    }
+  }
+  if (use_tc) {
+    // x operand by padded slot, gate/up, (h operand,) down on tcgen05
+    if (e == cudaSuccess) {
+      if (m == 1) {
+        e = moe::launch_tc_experts(lc, pack->view, v, x, pack->x_scale, pack->x_inv6S);
+        *n += 3;
+      } else {
+        e = moe::launch_tc16_experts(lc, pack->view, v, x);
+        *n += 4;
+      }
+    }
+  } else {
+    if (e == cudaSuccess) {
+      e = moe::launch_gateup(lc, pack->view, v, m, narrow);
+      *n += 1;
+    }
+    if (e == cudaSuccess) {
+      const long long S = (long long)T * k;
+      const bool h_res = narrow && S * (2LL * I + 16) <= 96 * 1024;
+      e = moe::launch_down(lc, pack->view, v, m, h_res);
+      *n += 1;
+    }
+  }
+  if (e == cudaSuccess) {
+    e = moe::launch_combine(lc, v, out);
+    *n += 1;
+  }
+  return e;
+}
+
 // moe_forward, optionally with the shared expert (validated by the caller).
 moe_status forward_impl(const uint16_t* x, const uint16_t* router_w, const moe_expert_pack* pack,
                         const moe_shared_expert* sh, int T, int k, moe_mode mode, uint16_t* out,
@@ -453,80 +554,11 @@ moe_status forward_impl(const uint16_t* x, const uint16_t* router_w, const moe_e
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   moe::WsView v = ws_view(ws, L, T, H, E, k, I);
   moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
-  const int m = (int)mode;
-  cudaError_t e;
-  int n = 0;
   // while profiling, launches are not overlapped by programmatic dependent launch
   if (g_prof.count) lc.pdl = false;
-  e = cudaSuccess;
-  if (sh) {
-    // the shared expert first: the combine (of whichever path runs) adds its term
-    unsigned char* b = static_cast<unsigned char*>(ws);
-    moe::ShView sv;
-    sv.gate_up = sh->gate_up;
-    sv.down = sh->down;
-    sv.gate = sh->gate;
-    sv.hs = reinterpret_cast<uint16_t*>(b + L.sh_hs);
-    sv.sigma = reinterpret_cast<float*>(b + L.sh_sigma);
-    sv.ys = reinterpret_cast<float*>(b + L.sh_y);
-    sv.gu = reinterpret_cast<float*>(b + L.sh_gu);
-    sv.Is = sh->inter;
-    e = moe::launch_shared(lc, x, sv, v, &n);
-    v.sh_y = sv.ys;
-    v.sh_sigma = sv.sigma;
-  }
-  if (narrow && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
-    // the whole routed step in one persistent kernel
-    if (e == cudaSuccess)
-      e = moe::launch_decode(lc, pack->view, v, m, pack->x_scale, pack->x_inv6S, x, router_w, out);
-    prof_finish();
-    g_last_launches = n + 1;
-    return from_cuda(e);
-  }
-  if (narrow) {
-    if (e == cudaSuccess)
-      e = moe::launch_route_narrow(lc, x, router_w, v, &pack->view, m, pack->x_scale,
-                                   pack->x_inv6S, v.idx, v.w, v.counts, v.offsets, v.perm);
-    n += 1;
-  }
-  // wide calls run the tensor-core grouped path when the layout reserved its token tiles
-  const bool use_tc = !narrow && v.NT > 0;
-  if (!narrow) {
-    if (e == cudaSuccess)
-      e = moe::launch_route_wide(lc, x, router_w, v, &pack->view, v.idx, v.w, v.counts, v.offsets,
-                                 v.perm, &n);
-    if (e == cudaSuccess && !use_tc) {   // the tensor-core path quantises x itself
-      e = moe::launch_xprep_wide(lc, x, v, m, pack->x_scale, pack->x_inv6S);
-      n += 1;
-    }
-  }
-  if (use_tc) {
-    // x operand by padded slot, gate/up, (h operand,) down on tcgen05 (stage 1 covers all)
-    if (e == cudaSuccess) {
-      if (m == 1) {
-        e = moe::launch_tc_experts(lc, pack->view, v, x, pack->x_scale, pack->x_inv6S);
-        n += 3;
-      } else {
-        e = moe::launch_tc16_experts(lc, pack->view, v, x);
-        n += 4;
-      }
-    }
-      } else {
-    if (e == cudaSuccess) {
-      e = moe::launch_gateup(lc, pack->view, v, m, narrow);
-      n += 1;
-    }
-        if (e == cudaSuccess) {
-      const long long S = (long long)T * k;
-      const bool h_res = narrow && S * (2LL * I + 16) <= 96 * 1024;
-      e = moe::launch_down(lc, pack->view, v, m, h_res);
-      n += 1;
-    }
-  }
-  if (e == cudaSuccess) {
-    e = moe::launch_combine(lc, v, out);
-    n += 1;
-  }
+  int n = 0;
+  const cudaError_t e = launch_forward(lc, pack, sh, L, static_cast<unsigned char*>(ws), v,
+                                       (int)mode, x, router_w, out, &n);
   prof_finish();
   g_last_launches = n;
   return from_cuda(e);
@@ -540,6 +572,96 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
                        int T, int k, moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
                        void* stream) {
   return forward_impl(x, router_w, pack, nullptr, T, k, mode, out, ws, ws_bytes, stream);
+}
+
+moe_status moe_workspace_size_layers(const moe_expert_pack* pack, int layers, int T, int k,
+                                     moe_mode mode, size_t* bytes) {
+  if (!pack || !bytes || layers < 1 || (mode != MOE_W4A16 && mode != MOE_W4A4) ||
+      !route_shape_ok(T, pack->H, pack->E, k))
+    return MOE_ERR_INVALID_ARG;
+  *bytes = layers_total(ws_layout(T, pack->H, pack->E, k, pack->I, (int)mode), layers);
+  return MOE_OK;
+}
+
+moe_status moe_workspace_offsets_layers(const moe_expert_pack* pack, int layers, int T, int k,
+                                        moe_mode mode, int layer, moe_ws_offsets* off) {
+  if (layer < 0 || layer >= layers) return MOE_ERR_INVALID_ARG;
+  const moe_status st = moe_workspace_offsets(pack, T, k, mode, off);
+  if (st != MOE_OK) return st;
+  const size_t d = (size_t)layer *
+                   layer_stride(ws_layout(T, pack->H, pack->E, k, pack->I, (int)mode));
+  off->idx += d; off->w += d; off->counts += d; off->offsets += d; off->perm += d;
+  off->slot_of += d; off->x_codes += d; off->x_scales += d; off->h_bf16 += d; off->h_codes += d;
+  off->h_scales += d; off->y += d;
+  return MOE_OK;
+}
+
+moe_status moe_forward_layers(const uint16_t* x, const uint16_t* const* router_w,
+                              const moe_expert_pack* const* packs, int layers, int T, int k,
+                              moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
+                              void* stream) {
+  g_last_launches = 0;
+  if (!x || !router_w || !packs || !out || !ws || layers < 1) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_W4A16 && mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
+  const moe_expert_pack* p0 = packs[0];
+  if (!p0) return MOE_ERR_INVALID_ARG;
+  const int H = p0->H, E = p0->E, I = p0->I;
+  if (!route_shape_ok(T, H, E, k)) return MOE_ERR_INVALID_ARG;
+  for (int l = 0; l < layers; ++l) {
+    if (!packs[l] || !router_w[l] || !aligned16(router_w[l])) return MOE_ERR_INVALID_ARG;
+    if (packs[l]->H != H || packs[l]->E != E || packs[l]->I != I) return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_W4A4 && !packs[l]->x_scale_uniform) return MOE_ERR_UNSUPPORTED;
+  }
+  const size_t act = (size_t)T * H;   // elements of one layer's activations
+  const uint16_t* xe = x + act;
+  if (xe > out && x < out + layers * act) return MOE_ERR_INVALID_ARG;   // x overlaps out
+  const WsLayout L = ws_layout(T, H, E, k, I, (int)mode);
+  if (ws_bytes < layers_total(L, layers)) return MOE_ERR_WORKSPACE;
+  const size_t stride = layer_stride(L);
+  const moe::WsView v0 = ws_view(ws, L, T, H, E, k, I);
+  moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
+  if (g_prof.count) lc.pdl = false;
+  const int m = (int)mode;
+  cudaError_t e = cudaSuccess;
+  int n = 0;
+  unsigned char* wsb = static_cast<unsigned char*>(ws);
+  // the residual sum x + out of layer l, plainly in its region: the input of layer l + 1 when
+  // that layer starts a new launch or runs as its own launch sequence
+  auto xres_of = [&](int l) {
+    return reinterpret_cast<uint16_t*>(wsb + L.xres + (size_t)l * stride);
+  };
+  if (T <= moe::kNarrowT && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
+    // runs of up to kMaxDcLayers chained layers per launch of the fused kernel
+    moe::DcLayer dl[moe::kMaxDcLayers];
+    for (int l0 = 0; l0 < layers && e == cudaSuccess; l0 += moe::kMaxDcLayers) {
+      const int nl = layers - l0 < moe::kMaxDcLayers ? layers - l0 : moe::kMaxDcLayers;
+      for (int i = 0; i < nl; ++i) {
+        const moe_expert_pack* p = packs[l0 + i];
+        dl[i] = moe::DcLayer{p->view, router_w[l0 + i], out + (size_t)(l0 + i) * act,
+                             p->x_scale, p->x_inv6S};
+      }
+      e = moe::launch_decode(lc, dl, nl, stride, shift_view(v0, (size_t)l0 * stride), m,
+                             l0 == 0 ? x : xres_of(l0 - 1),
+                             l0 + nl < layers ? xres_of(l0 + nl - 1) : nullptr);
+      n += 1;
+    }
+  } else {
+    // the same chain as one launch sequence per layer, each in its own workspace region, and
+    // the residual sum between them
+    for (int l = 0; l < layers && e == cudaSuccess; ++l) {
+      const uint16_t* xl = l == 0 ? x : xres_of(l - 1);
+      e = launch_forward(lc, packs[l], nullptr, L, wsb, shift_view(v0, (size_t)l * stride), m,
+                         xl, router_w[l], out + (size_t)l * act, &n);
+      if (e == cudaSuccess && l + 1 < layers) {
+        e = moe::launch_residual_add(lc, xl, out + (size_t)l * act, xres_of(l), act);
+        n += 1;
+      }
+    }
+  }
+  prof_finish();
+  g_last_launches = n;
+  return from_cuda(e);
 }
 
 moe_status moe_workspace_size_shared(const moe_expert_pack* pack, int T, int k, moe_mode mode,

@@ -617,6 +617,26 @@ __global__ void __launch_bounds__(256) k_combine(WsView ws, uint16_t* __restrict
   }
 }
 
+// ------------------------------------------------------------------ residual sum
+// out[i] = BF16(a[i] + b[i]): the next input of a chained layer (its input plus its output).
+__global__ void __launch_bounds__(256) k_residual_add(const uint16_t* __restrict__ a,
+                                                     const uint16_t* __restrict__ b,
+                                                     uint16_t* __restrict__ out, size_t n8) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n8; i += (size_t)gridDim.x * 256) {
+    const uint4 va = __ldcg(reinterpret_cast<const uint4*>(a) + i);
+    const uint4 vb = __ldcg(reinterpret_cast<const uint4*>(b) + i);
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = (uint32_t)f32_to_bf16_rn(bf16_lo(wa[q]) + bf16_lo(wb[q])) |
+             ((uint32_t)f32_to_bf16_rn(bf16_hi(wa[q]) + bf16_hi(wb[q])) << 16);
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // ------------------------------------------------------------------ scale re-layout
 // checkpoint [E][rows][cols/16] -> fragment order (see PackView).
 __global__ void k_pack_scales(const uint8_t* __restrict__ rg, const uint8_t* __restrict__ ru,
@@ -750,6 +770,14 @@ cudaError_t launch_combine(const LaunchCfg& lc, const WsView& ws, uint16_t* out)
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   return launch_kernel(lc, k_combine, dim3((unsigned)grid), dim3(256), 0, ws, out);
+}
+
+cudaError_t launch_residual_add(const LaunchCfg& lc, const uint16_t* a, const uint16_t* b,
+                                uint16_t* out, size_t n) {
+  const size_t n8 = n / 8;
+  const unsigned grid = (unsigned)((n8 + 255) / 256 < (size_t)4 * lc.num_sms
+                                       ? (n8 + 255) / 256 : (size_t)4 * lc.num_sms);
+  return launch_kernel(lc, k_residual_add, dim3(grid > 0 ? grid : 1), dim3(256), 0, a, b, out, n8);
 }
 
 cudaError_t launch_pack_scales(cudaStream_t s, const uint8_t* raw_gate, const uint8_t* raw_up,
