@@ -373,6 +373,87 @@ def measure(wl, stack, steps, warmup, use_graph, device, clocks=None):
     return e0.elapsed_time(e1) / steps, launches[0], info, (s, ws, oall, run, step)
 
 
+def measure_stack(wl, stack, steps, warmup, use_graph, device, clocks=None):
+    """Time `steps` steps of the layers chained through the residual stream with
+    moe_forward_layers (layer 0 reads stack[0].x; layer l+1 reads BF16(x_l + out_l)); returns
+    per-step ms, launches per step, the clock record, the mean distinct experts per layer (from
+    each layer's counts in the workspace) and the state for the end-to-end measurement."""
+    import torch
+    import nvfp4_mixture_experts_bf16_gb300 as moe
+    s = torch.cuda.Stream(device=device)
+    L = len(stack)
+    packs = [Lr.pack for Lr in stack]
+    wrs = [Lr.wr for Lr in stack]
+    x = stack[0].x.clone()
+    out = torch.empty((L, wl.T, wl.H), dtype=torch.bfloat16, device=device)
+    ws = moe.new_workspace(moe.moe_workspace_size_layers(packs[0], L, wl.T, wl.k, wl.mode), device)
+    launches = [0]
+
+    def step():
+        moe.moe_forward_layers(x, wrs, packs, wl.k, wl.mode, out=out, ws=ws, stream=s)
+        launches[0] = moe.moe_last_launch_count()
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    U = []
+    for l in range(L):
+        off = moe.moe_workspace_offsets_layers(packs[0], L, wl.T, wl.k, wl.mode, l)
+        c = ws[off["counts"]:off["counts"] + 4 * wl.E].cpu().numpy().view(np.int32)
+        U.append(int((c > 0).sum()))
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step()
+        torch.cuda.synchronize()
+    run = graph.replay if graph is not None else step
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            run()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if clocks:
+        clocks.start()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(steps):
+            run()
+        e1.record(s)
+    torch.cuda.synchronize()
+    info = clocks.stop() if clocks else None
+    if moe.moe_read_device_status(ws, stream=s) != 0:
+        raise RuntimeError("device status after the timed region")
+    return e0.elapsed_time(e1) / steps, launches[0], info, float(np.mean(U)), \
+        (s, x, out, run, step)
+
+
+def e2e_stack(wl, L, steps, state, use_graph=True):
+    """The chained stack end to end: per step the first layer's input host->device, the step,
+    every layer's output device->host (pinned buffers)."""
+    import torch
+    s, x, out, run, step = state
+    if not use_graph:
+        run = step
+    hx = x.cpu().pin_memory()
+    ho = torch.empty(tuple(out.shape), dtype=torch.bfloat16).pin_memory()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for it in range(steps + 2):
+            if it == 2:
+                e0.record(s)
+            x.copy_(hx, non_blocking=True)
+            run()
+            ho.copy_(out, non_blocking=True)
+        e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, wl.T * wl.H * 2, L * wl.T * wl.H * 2
+
+
 def kernel_label(name):
     """A short label of a kernel name as cudaFuncGetName returns it (mangled or not)."""
     import re
@@ -611,6 +692,23 @@ def run_native(args, rank, world, local_rank):
                                unique_experts=round(U2, 2),
                                hbm_gbs=round(b2 / (ms2 / layers * 1e-3) / 1e9, 1),
                                frac_hbm=round(b2 / (ms2 / layers * 1e-3) / 1e9 / pk["hbm"], 4))
+        for name in ("decode1", "verify8", "verify8_w4a4"):
+            # the same layers chained through the residual stream in persistent launches
+            w5 = synth.WORKLOADS[name]
+            st5 = stack if name == wl.name else build_stack(w5, layers, args.seed, device,
+                                                            packs=packs)
+            ms5, n5, _, U5, _ = measure_stack(w5, st5, max(3, args.steps // 2), 3,
+                                              not args.no_graph, device)
+            b5 = bytes_gateup(U5, w5.H, w5.I) + bytes_down(U5, w5.H, w5.I) + 12 * U5
+            g5 = b5 / (ms5 / layers * 1e-3) / 1e9
+            extra[name + "_stack"] = dict(
+                tokens_per_s=round(w5.T * layers / (ms5 / 1e3), 1),
+                us_per_layer=round(ms5 / layers * 1e3, 3), launches_per_step=n5,
+                unique_experts=round(U5, 2), hbm_gbs=round(g5, 1),
+                frac_hbm=round(g5 / pk["hbm"], 4),
+                note=("moe_forward_layers: the layers chained through the residual stream "
+                      "(x_{l+1} = BF16(x_l + out_l)), one PDL-chained launch per layer, the "
+                      "residual sum written by each layer's combine"))
         if wl.name == "decode1" and wl.T == 1:
             # the same layers with a BF16 shared expert each (Is = I): two extra launches
             st4 = with_shared(stack, wl, args.seed, device)

@@ -223,21 +223,19 @@ moe_status moe_workspace_offsets_layers(const moe_expert_pack* pack, int layers,
  * layer 0 reads x [T][H]; layer l + 1 reads x_{l+1} = BF16(x_l + out_l), layer l's input plus
  * its output, as a decoder layer adds its MoE output to the residual stream (a reading: the
  * pages chain the layers of the stack but print no formula; attention and norms between the
- * MoE steps are not part of this library). The release notes "Infernix windows-2026.10.11",
- * section "Highlights", chain the expert passes by programmatic dependent launch and the
- * Inferno fork's README runs decode under CUDA graphs; here narrow calls (T <= 8) go further:
- * up to 32 layers run in ONE persistent launch of the fused kernel, whose CTAs stage layer
- * l + 1's router rows in shared memory while layer l finishes and take layer l + 1's input from
- * layer l's output tiles as each arrives (no kernel boundary between the layers); longer
- * stacks take one launch per 32 layers. Other shapes run the same chain as one
- * moe_forward-style launch sequence per layer plus the residual sum.
+ * MoE steps are not part of this library). As the release notes "Infernix windows-2026.10.11",
+ * section "Highlights", chain the expert passes by programmatic dependent launch, each layer
+ * is one launch chained to the previous one: for narrow calls (T <= 8) the fused kernel copies
+ * its router rows before it waits for the previous layer and its combine also writes the
+ * residual sum; other shapes run moe_forward's launch sequence per layer plus the residual sum.
+ * The whole call can be captured in a CUDA graph.
  *   x         device [T][H] BF16, the first layer's input.
  *   router_w  host array of `layers` device pointers, router_w[l] [E][H] BF16.
  *   packs     host array of `layers` packs with equal hidden, inter and expert counts.
  *   out       device [layers][T][H] BF16: out[l] is layer l's MoE output (moe_forward of x_l);
  *             must not overlap x.
- * Every layer's output equals moe_forward's on the same input (bit for bit on the fused path).
- * W4A4 requires each pack's gate/up input scales to be equal (else MOE_ERR_UNSUPPORTED).
+ * Every layer's output equals moe_forward's on the same input, bit for bit. W4A4 requires each
+ * pack's gate/up input scales to be equal (else MOE_ERR_UNSUPPORTED).
  * ws/ws_bytes: see moe_workspace_size_layers. */
 moe_status moe_forward_layers(const uint16_t* x, const uint16_t* const* router_w,
                               const moe_expert_pack* const* packs, int layers, int T, int k,

@@ -72,7 +72,7 @@ int num_sms_of_current_device() {
 
 struct WsLayout {
   size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm,
-      chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, htag, ytag, otag, xres, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
+      chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, htag, ytag, xres, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
       xsf_atoms, hq_perm, hsf_atoms, xh_perm, hf_perm, sh_hs, sh_sigma, sh_y, sh_gu, total;
   size_t slot_amax_bytes;
   int G, NT;
@@ -129,9 +129,7 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode, int Is = 0) {
   L.sh_sigma = take(Is > 0 ? (size_t)T * 4 : 0);
   L.sh_y = take(Is > 0 ? (size_t)T * H * 4 : 0);
   L.sh_gu = take(Is > 0 && !narrow ? (size_t)T * 2 * Is * 4 : 0);
-  // chained layers: the next layer's input (this layer's input + output) as tagged BF16 pairs
-  // (narrow calls) and plainly
-  L.otag = take(mode >= 0 && narrow ? (size_t)T * (H / 2) * 8 : 0);
+  // a layer of a chained stack: the next layer's input (this layer's input + output)
   L.xres = take(mode >= 0 ? (size_t)T * H * 2 : 0);
   L.total = o;
   return L;
@@ -161,7 +159,6 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   v.y = reinterpret_cast<uint16_t*>(b + L.y);
   v.htag = reinterpret_cast<unsigned long long*>(b + L.htag);
   v.ytag = reinterpret_cast<unsigned long long*>(b + L.ytag);
-  v.otag = reinterpret_cast<unsigned long long*>(b + L.otag);
   v.T = T; v.H = H; v.E = E; v.k = k; v.I = I; v.G = L.G; v.NT = L.NT;
   const bool tc = L.NT > 0;
   v.tt_expert = tc ? reinterpret_cast<int32_t*>(b + L.tt_expert) : nullptr;
@@ -198,7 +195,7 @@ moe::WsView shift_view(moe::WsView v, size_t off) {
   auto mv = [&](auto*& p) { moe::shift_ptr(p, off); };
   mv(v.gmeta); mv(v.slot_amax); mv(v.logits); mv(v.idx); mv(v.w); mv(v.slot_of); mv(v.counts);
   mv(v.offsets); mv(v.perm); mv(v.chunk_base); mv(v.xh); mv(v.xfac); mv(v.xq); mv(v.xsf);
-  mv(v.h16); mv(v.hq); mv(v.hsf); mv(v.y); mv(v.htag); mv(v.ytag); mv(v.otag); mv(v.tt_expert);
+  mv(v.h16); mv(v.hq); mv(v.hsf); mv(v.y); mv(v.htag); mv(v.ytag); mv(v.tt_expert);
   mv(v.tt_slot0); mv(v.tt_n); mv(v.ttbase); mv(v.xq_perm); mv(v.xsf_atoms); mv(v.hq_perm);
   mv(v.hsf_atoms); mv(v.xh_perm); mv(v.hf_perm);
   return v;
@@ -482,8 +479,9 @@ cudaError_t launch_forward(moe::LaunchCfg lc, const moe_expert_pack* pack,
   }
   if (narrow && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
     // the whole routed step in one persistent kernel
-    const moe::DcLayer dl{pack->view, router_w, out, pack->x_scale, pack->x_inv6S};
-    if (e == cudaSuccess) e = moe::launch_decode(lc, &dl, 1, 0, v, m, x, nullptr);
+    if (e == cudaSuccess)
+      e = moe::launch_decode(lc, pack->view, v, m, pack->x_scale, pack->x_inv6S, x, router_w, out,
+                             nullptr);
     *n += 1;
     return e;
   }
@@ -626,24 +624,19 @@ moe_status moe_forward_layers(const uint16_t* x, const uint16_t* const* router_w
   cudaError_t e = cudaSuccess;
   int n = 0;
   unsigned char* wsb = static_cast<unsigned char*>(ws);
-  // the residual sum x + out of layer l, plainly in its region: the input of layer l + 1 when
-  // that layer starts a new launch or runs as its own launch sequence
+  // the residual sum x + out of layer l, in its region: the input of layer l + 1
   auto xres_of = [&](int l) {
     return reinterpret_cast<uint16_t*>(wsb + L.xres + (size_t)l * stride);
   };
   if (T <= moe::kNarrowT && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
-    // runs of up to kMaxDcLayers chained layers per launch of the fused kernel
-    moe::DcLayer dl[moe::kMaxDcLayers];
-    for (int l0 = 0; l0 < layers && e == cudaSuccess; l0 += moe::kMaxDcLayers) {
-      const int nl = layers - l0 < moe::kMaxDcLayers ? layers - l0 : moe::kMaxDcLayers;
-      for (int i = 0; i < nl; ++i) {
-        const moe_expert_pack* p = packs[l0 + i];
-        dl[i] = moe::DcLayer{p->view, router_w[l0 + i], out + (size_t)(l0 + i) * act,
-                             p->x_scale, p->x_inv6S};
-      }
-      e = moe::launch_decode(lc, dl, nl, stride, shift_view(v0, (size_t)l0 * stride), m,
-                             l0 == 0 ? x : xres_of(l0 - 1),
-                             l0 + nl < layers ? xres_of(l0 + nl - 1) : nullptr);
+    // one launch of the fused kernel per layer, chained by programmatic dependent launch: each
+    // launch copies its router rows before waiting for the previous one, and its combine also
+    // writes the residual sum, the next launch's input
+    for (int l = 0; l < layers && e == cudaSuccess; ++l) {
+      const moe_expert_pack* p = packs[l];
+      e = moe::launch_decode(lc, p->view, shift_view(v0, (size_t)l * stride), m, p->x_scale,
+                             p->x_inv6S, l == 0 ? x : xres_of(l - 1), router_w[l],
+                             out + (size_t)l * act, l + 1 < layers ? xres_of(l) : nullptr);
       n += 1;
     }
   } else {

@@ -30,7 +30,8 @@
 //   5. combine: 128-row tile j of out is formed, once its tagged Y has arrived, by the j-th CTA
 //      in the order (late down tasks, CTA index), i.e. by CTAs done with their own down tasks
 //      first: the fixed-order weighted sum over each token's k experts (rank order, FP32, then
-//      BF16).
+//      BF16). A layer of a chained stack (moe_forward_layers) also writes the residual sum
+//      BF16(x + out), the next layer's input.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -304,30 +305,11 @@ __device__ __forceinline__ DcSplit dc_split(int U, int gu_tiles, int dn_tiles) {
   return sp;
 }
 
-// The layers of one launch: layer l's experts, router and output, and its W4A4 x scale. Layer
-// l + 1 reads layer l's output as its input.
-struct DcLayers {
-  DcLayer l[kMaxDcLayers];
-  size_t ws_stride;   // bytes between the per-layer workspace regions
-  uint16_t* xnext;    // [T][H]: the last layer's residual sum, when another launch continues
-  int L;
-};
-
-// The workspace view of one layer: every per-call region moved by `off` bytes (the control
-// words stay shared).
-__device__ __forceinline__ WsView layer_view(const WsView& w, size_t off) {
-  WsView v = w;
-  auto mv = [&](auto*& p) { moe::shift_ptr(p, off); };
-  mv(v.gmeta); mv(v.slot_amax); mv(v.logits); mv(v.idx); mv(v.w); mv(v.slot_of); mv(v.counts);
-  mv(v.offsets); mv(v.perm); mv(v.xh); mv(v.xfac); mv(v.xq); mv(v.xsf); mv(v.h16); mv(v.hq);
-  mv(v.hsf); mv(v.y); mv(v.htag); mv(v.ytag); mv(v.otag);
-  return v;
-}
-
 template <int NT, int MODE>
 __global__ void __launch_bounds__(kDcThreads, 1)
-    k_decode(const __grid_constant__ DcLayers layers, WsView ws0, DcGeom geo,
-             const uint16_t* __restrict__ x) {
+    k_decode(PackView pk, WsView ws, DcGeom geo, const uint16_t* __restrict__ x,
+             const uint16_t* __restrict__ wr, float xS, float x_inv6S,
+             uint16_t* __restrict__ out, uint16_t* __restrict__ xnext) {
   constexpr int mode = MODE;   // 0: W4A16, 1: W4A4 (one instantiation each: smaller code)
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* arena = smem;
@@ -339,6 +321,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   int32_t* sel_idx = reinterpret_cast<int32_t*>(grp + geo.gmax);        // [S]
   float* sel_w = reinterpret_cast<float*>(sel_idx + geo.smax);          // [S]
   int32_t* sel_slot = reinterpret_cast<int32_t*>(sel_w + geo.smax);     // [S]
+  // the selections sorted by expert (own region: the arena only ever receives TMA writes and
+  // the combine's staging, so no proxy fence is needed before the first weight copy)
   int32_t* sorted_e = sel_slot + geo.smax;                               // [S] expert of slot p
   int32_t* sorted_t = sorted_e + geo.smax;                               // [S] token of slot p
   uint64_t* bars = reinterpret_cast<uint64_t*>(
@@ -360,25 +344,13 @@ __global__ void __launch_bounds__(kDcThreads, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int T = NT;
-  const int H = ws0.H, E = ws0.E, k = ws0.k, I = ws0.I, S = T * k;
+  const int H = ws.H, E = ws.E, k = ws.k, I = ws.I, S = T * k;
   const int G = gridDim.x, b = blockIdx.x;
   const int row0 = (E * b) / G;
   const int nrows = (E * (b + 1)) / G - row0;
-  // router rows at the end of the arena: the next layer's rows land there while this layer's
-  // combine still stages its Y pairs at the arena's start (the gate/up and down rings are free
-  // by then); several tokens' raw activations just below them
-  unsigned char* wrs = arena + geo.arena - (size_t)geo.rows_max * geo.rs;  // [rows][rs bytes]
+  unsigned char* wrs = arena;                                            // [rows][rs bytes]
   unsigned char* xraw = geo.xsep ? xsep_row                              // [T][rs bytes]
-                                 : wrs - (size_t)T * geo.rs;
-  // copies of the router rows of layer l into wrs, completing on rbar
-  auto issue_router = [&](int l) {
-    if (nrows > 0) {
-      mbar_arrive_expect_tx(rbar, (uint32_t)nrows * H * 2);
-      for (int r = 0; r < nrows; ++r)
-        bulk_g2s(wrs + (size_t)r * geo.rs, layers.l[l].wr + (size_t)(row0 + r) * H,
-                 (uint32_t)H * 2, rbar);
-    }
-  };
+                                 : arena + (size_t)geo.rows_max * geo.rs;
 
   if (tid == 0) {
     for (int s = 0; s < geo.gu_stages; ++s) {
@@ -394,7 +366,11 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     fence_mbar_init();
     abort_s = 0;
     // the router rows are weights: copy them before waiting for the preceding kernel
-    issue_router(0);
+    if (nrows > 0) {
+      mbar_arrive_expect_tx(rbar, (uint32_t)nrows * H * 2);
+      for (int r = 0; r < nrows; ++r)
+        bulk_g2s(wrs + (size_t)r * geo.rs, wr + (size_t)(row0 + r) * H, (uint32_t)H * 2, rbar);
+    }
   }
   __syncthreads();
   pdl_wait();
@@ -405,62 +381,12 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       bulk_g2s(xraw + (size_t)t * geo.rs, x + (size_t)t * H, (uint32_t)H * 2, xbar);
   }
   // this call's epoch: one past the last completed call's (never 0, the zeroed workspace's tag)
-  uint32_t ep = __ldcg(&ws0.ctl[kCtlEpoch]) + 1u;
+  uint32_t ep = __ldcg(&ws.ctl[kCtlEpoch]) + 1u;
   if (ep == 0u) ep = 1u;
-  // gate/up and down chunks this CTA has staged in earlier layers (the rings' phases carry on)
-  int gu_base = 0, dn_base = 0;
-  bool router_issued = false;   // producer lane: the next layer's router rows are in flight
-
-  for (int l = 0; l < layers.L; ++l) {
-  const DcLayer& ly = layers.l[l];
-  const PackView& pk = ly.pk;
-  uint16_t* __restrict__ out = ly.out;
-  const float xS = ly.xS, x_inv6S = ly.x_inv6S;
-  const WsView ws = layer_view(ws0, (size_t)l * layers.ws_stride);
-  if (l > 0) {
-    // this layer's x is the previous layer's output: poll its tagged BF16 pairs (every thread a
-    // share, 8 words in flight) into the raw activation rows
-    const unsigned long long* src = ws.otag - layers.ws_stride / 8;
-    const int nw = T * (H / 2);
-    for (int base = tid; base < nw; base += 8 * kDcThreads) {
-      unsigned long long w8[8];
-      uint32_t late = 0;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * kDcThreads;
-        w8[u] = i < nw ? ld_tag(src + i) : 0ull;
-        if (i < nw && tag_of(w8[u]) != ep) late |= 1u << u;
-      }
-      if (late && !abort_s) {
-        const uint64_t t0 = globaltimer_ns();
-        while (late) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            if (late & (1u << u)) {
-              w8[u] = ld_tag(src + base + u * kDcThreads);
-              if (tag_of(w8[u]) == ep) late &= ~(1u << u);
-            }
-          if (late && globaltimer_ns() - t0 > kWaitLimitNs) {
-            record_status(ws.ctl, kStTimeout);
-            abort_s = 1;
-            break;
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * kDcThreads;
-        if (i < nw)
-          *reinterpret_cast<uint32_t*>(xraw + (size_t)(i / (H / 2)) * geo.rs + 4 * (i % (H / 2))) =
-              data_of(w8[u]);
-      }
-    }
-  }
-  if ((nrows > 0 && !mbar_wait(rbar, l & 1)) || (l == 0 && !mbar_wait(xbar, 0))) {
+  if ((nrows > 0 && !mbar_wait(rbar, 0)) || !mbar_wait(xbar, 0)) {
     record_status(ws.ctl, kStTimeout);
     abort_s = 1;
   }
-  __syncthreads();   // the activation rows written by every thread are complete
 
   // ---------------- 1. router rows on the tensor cores: logits[t][row0 + r] = W[r] . x[t] as one
   // m16n8k16 BF16 MMA chain per warp over an eighth of H (A = the CTA's <= 8 router rows,
@@ -676,7 +602,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
           const int q = q0 + c / geo.nkc;
           const unsigned src = __ballot_sync(0xFFFFFFFFu, lane < k && p == q / gu_tiles);
           const int e = __shfl_sync(0xFFFFFFFFu, e_sel, __ffs(src) - 1);
-          if (lane == c) issue_gu(gu_base + c, q, c % geo.nkc, e);
+          if (lane == c) issue_gu(c, q, c % geo.nkc, e);
         }
       }
     } else if (lane < k) {
@@ -786,14 +712,13 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   auto dq = [&](int i) { return i < nde ? sp.de0 + i : sp.dl0 + (i - nde); };
 
   if (warp == kDcWarps) {
-    // ---------------- producer: gate/up tasks, then this CTA's down tasks, then the next
-    // layer's router rows (lanes 1..31 wait at the layer's closing barrier)
-    if (lane == 0) {
-    int chunk = gu_base;
+    // ---------------- producer: gate/up tasks, then this CTA's down tasks
+    if (lane != 0) return;
+    int chunk = 0;
     for (int q = q0; q < q1 && !abort_s; ++q) {
       const int e = grp[q / gu_tiles].expert;
       for (int kc = 0; kc < geo.nkc; ++kc, ++chunk) {
-        if (chunk - gu_base < npre) continue;   // issued by the selecting warp
+        if (chunk < npre) continue;   // issued by the selecting warp
         const int s = chunk % geo.gu_stages, n = chunk / geo.gu_stages;
         if (n > 0 && !mbar_wait(&gempty[s], (n - 1) & 1)) {
           record_status(ws.ctl, kStTimeout);
@@ -802,8 +727,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         }
         // one token: the second task's stage waits for the first to land (its only completed
         // phase)
-        if (npre > 0 && chunk == gu_base + 1 && geo.nkc == 1 &&
-            !mbar_wait(&gfull[gu_base % geo.gu_stages], (gu_base / geo.gu_stages) & 1)) {
+        if (npre > 0 && chunk == 1 && geo.nkc == 1 && !mbar_wait(&gfull[0], 0)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
           break;
@@ -811,20 +735,17 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         issue_gu(chunk, q, kc, e);
       }
     }
-    // the arena becomes the down ring once every gate/up stage has landed and the consumers
-    // have released it (landed: after a timeout elsewhere the consumers release unread stages)
-    const int nch = chunk - gu_base;
-    const int used = nch < geo.gu_stages ? nch : geo.gu_stages;
-    for (int i = 0; i < used; ++i) {
+    // the arena becomes the down ring once the consumers have released every gate/up stage
+    const int used = chunk < geo.gu_stages ? chunk : geo.gu_stages;
+    for (int i = 0; i < used && !abort_s; ++i) {
       const int c2 = chunk - 1 - i;
-      if (!mbar_wait(&gfull[c2 % geo.gu_stages], (c2 / geo.gu_stages) & 1) ||
-          !mbar_wait(&gempty[c2 % geo.gu_stages], (c2 / geo.gu_stages) & 1)) {
+      if (!mbar_wait(&gempty[c2 % geo.gu_stages], (c2 / geo.gu_stages) & 1)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
       }
     }
     const uint32_t code_bytes = (uint32_t)kDnRows * (I / 2);
-    int dchunk = dn_base;
+    int dchunk = 0;
     for (int i = 0; i < nd && !abort_s; ++i, ++dchunk) {
       const int q = dq(i);
       const int gi = q / dn_tiles, ht = q % dn_tiles;
@@ -843,27 +764,19 @@ __global__ void __launch_bounds__(kDcThreads, 1)
                pk.down_scales + ((size_t)e * (H / 64) + 2 * (size_t)ht) * (4 * (size_t)I), 8u * I,
                &dfull[s]);
     }
-    // every down stage consumed (so no copy into this CTA's shared memory is in flight, and the
-    // arena's end is free), then the next layer's router rows
-    const int ndl = dchunk - dn_base;
-    const int dused = ndl < geo.dn_stages ? ndl : geo.dn_stages;
+    // do not leave while copies into this CTA's shared memory may still be in flight
+    const int dused = dchunk < geo.dn_stages ? dchunk : geo.dn_stages;
     for (int i = 0; i < dused; ++i) {
       const int c2 = dchunk - 1 - i;
-      if (!mbar_wait(&dfull[c2 % geo.dn_stages], (c2 / geo.dn_stages) & 1) ||
-          !mbar_wait(&dempty[c2 % geo.dn_stages], (c2 / geo.dn_stages) & 1)) {
-        record_status(ws.ctl, kStTimeout);
-        abort_s = 1;
-      }
+      (void)mbar_wait(&dfull[c2 % geo.dn_stages], (c2 / geo.dn_stages) & 1);
     }
-    router_issued = l + 1 < layers.L && !abort_s;
-    if (router_issued) issue_router(l + 1);
-    }
-    __syncwarp();
-  } else {
+    return;
+  }
+
   // ---------------- 3. gate/up + SiLU*up (consumer warps)
   const int g = lane >> 2, c = lane & 3;
   {
-    int chunk = gu_base;
+    int chunk = 0;
     const int jb_per_chunk = geo.KC / 128;
     for (int q = q0; q < q1; ++q) {
       const int gi = q / gu_tiles, it = q % gu_tiles;
@@ -992,7 +905,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   {
     const int nkb = I / 64, ntile = I / 16;
     const uint32_t code_bytes = (uint32_t)kDnRows * (I / 2);
-    int cur = -1, dchunk = dn_base;
+    int cur = -1, dchunk = 0;
     float md = 0.0f;
     for (int i = 0; i < nd; ++i, ++dchunk) {
       const int q = dq(i);
@@ -1225,18 +1138,14 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         const uint32_t pair =
             (uint32_t)f32_to_bf16_rn(a0) | ((uint32_t)f32_to_bf16_rn(a1) << 16);
         reinterpret_cast<uint32_t*>(out + (size_t)t * H)[ht * 64 + p2] = pair;
-        // chained layers: the next layer's input is this layer's input plus its output (the
-        // residual stream), BF16(x + out), tagged for the next layer, or written plainly when
-        // the next layer belongs to the next launch
-        if (l + 1 < layers.L || layers.xnext) {
+        if (xnext) {
+          // a chained layer: the next layer's input is this layer's input plus its output (the
+          // residual stream), BF16(x + out)
           const size_t w = (size_t)t * (H / 2) + ht * 64 + p2;
-          const uint32_t xv = l == 0 ? __ldg(reinterpret_cast<const uint32_t*>(x) + w)
-                                     : data_of(ld_tag(ws.otag - layers.ws_stride / 8 + w));
-          const uint32_t sum =
+          const uint32_t xv = __ldg(reinterpret_cast<const uint32_t*>(x) + w);
+          reinterpret_cast<uint32_t*>(xnext)[w] =
               (uint32_t)f32_to_bf16_rn(bf16_lo(xv) + bf16_lo(pair)) |
               ((uint32_t)f32_to_bf16_rn(bf16_hi(xv) + bf16_hi(pair)) << 16);
-          if (l + 1 < layers.L) st_tag(ws.otag + w, sum, ep);
-          else reinterpret_cast<uint32_t*>(layers.xnext)[w] = sum;
         }
       }
     }
@@ -1273,27 +1182,13 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     }
   }
 
-  }   // consumer warps
-
-  // ---------------- end of the layer: the arena's generic writes (combine staging, activation
-  // rows) are ordered before the next layer's copies into it, and every thread is done with
-  // this layer's shared memory
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncthreads();
-  gu_base += (q1 - q0) * geo.nkc;
-  dn_base += nd;
-  if (abort_s) {
-    // leaving early: the next layer's router rows must land before this CTA exits
-    if (router_issued) (void)mbar_wait(rbar, (l + 1) & 1);
-    break;
-  }
-  }   // layers
-
   // ---------------- the last CTA of the call publishes its epoch (after every CTA read it)
-  if (tid == 0 && (ticket_acq_rel(&ws0.ctl[kCtlDone]) + 1u) % (uint32_t)G == 0u)
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(&ws0.ctl[kCtlEpoch]), "r"(ep)
+  consumer_sync(kDcCons);
+  if (tid == 0 && (ticket_acq_rel(&ws.ctl[kCtlDone]) + 1u) % (uint32_t)G == 0u)
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(&ws.ctl[kCtlEpoch]), "r"(ep)
                  : "memory");
 }
+
 
 }  // namespace
 
@@ -1332,10 +1227,9 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   g.gu_stages = avail / g.gu_stage;
   if (g.gu_stages > 3) g.gu_stages = 3;
   if (g.gu_stages < 1) return false;
-  // the combine's staging at the arena's start must not meet the router rows (and raw
-  // activations) at its end: the next layer's rows land while this layer's combine runs
   int arena = g.gu_stages * g.gu_stage;
-  if (arena < route_bytes + scratch) arena = route_bytes + scratch;
+  if (arena < route_bytes) arena = route_bytes;
+  if (arena < scratch) arena = scratch;
   if (arena > avail) return false;
   g.dn_stages = arena / g.dn_stage;
   if (g.dn_stages > 16) g.dn_stages = 16;
@@ -1347,22 +1241,17 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   return true;
 }
 
-cudaError_t launch_decode(const LaunchCfg& lc, const DcLayer* layers, int L, size_t ws_stride,
-                          const WsView& ws, int mode, const uint16_t* x, uint16_t* xnext) {
+cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
+                          float xS, float x_inv6S, const uint16_t* x, const uint16_t* wr,
+                          uint16_t* out, uint16_t* xnext) {
   DcGeom geo;
-  if (L < 1 || L > kMaxDcLayers) return cudaErrorInvalidValue;
   if (!decode_geom(ws.T, ws.H, ws.E, ws.k, ws.I, lc.num_sms, &geo)) return cudaErrorInvalidValue;
-  DcLayers dl;
-  for (int l = 0; l < L; ++l) dl.l[l] = layers[l];
-  dl.L = L;
-  dl.ws_stride = ws_stride;
-  dl.xnext = xnext;
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(lc, kern, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, dl, ws,
-                         geo, x);
+    return launch_kernel(lc, kern, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, pk, ws,
+                         geo, x, wr, xS, x_inv6S, out, xnext);
   };
   if (mode == 1) {
     switch (ws.T) {

@@ -71,8 +71,6 @@ struct WsView {
   unsigned long long* htag;  // [T*k][I/16][9]: h of one 16-element block (W4A16: 8 BF16 pairs +
                              // max |h|; W4A4: code words lo, hi + scale byte)
   unsigned long long* ytag;  // [T*k][H/2]: BF16 pairs of Y
-  unsigned long long* otag;  // [T][H/2]: chained layers: BF16 pairs of the next layer's input
-                             // (this layer's input + output), tagged
   // grouped tensor-core path: token tiles of <= 128 slots of one expert; tile j occupies padded
   // rows ("pslots") 128j .. 128j+127 of the permuted operands
   int32_t* tt_expert;  // [NT]
@@ -92,7 +90,7 @@ struct WsView {
   int T, H, E, k, I, G, NT;
 };
 
-// Moves a (non-null) workspace pointer by `off` bytes: the regions of chained layers.
+// Moves a (non-null) workspace pointer by `off` bytes: the regions of a stack's layers.
 template <typename P>
 __host__ __device__ __forceinline__ void shift_ptr(P*& p, size_t off) {
   if (p) p = reinterpret_cast<P*>(reinterpret_cast<unsigned char*>(p) + off);
@@ -588,20 +586,10 @@ cudaError_t launch_combine(const LaunchCfg& lc, const WsView& ws, uint16_t* out)
 // Fused narrow-call kernel (router .. combine in one launch): whether a shape fits it, and the
 // launch.
 bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom);
-// One layer of a fused narrow call: its experts, router, output and W4A4 activation scale.
-struct DcLayer {
-  PackView pk;
-  const uint16_t* wr;
-  uint16_t* out;
-  float xS, x_inv6S;
-};
-// Layers one launch of the fused kernel runs (its parameter block holds their table).
-constexpr int kMaxDcLayers = 32;
-// L chained layers (x is layer 0's input; layer l + 1's input is BF16(layer l's input + its
-// output)), layer l using the workspace region ws + l * ws_stride (the control words shared).
-// xnext (or null): [T][H] receives the last layer's residual sum, another launch's input.
-cudaError_t launch_decode(const LaunchCfg& lc, const DcLayer* layers, int L, size_t ws_stride,
-                          const WsView& ws, int mode, const uint16_t* x, uint16_t* xnext);
+// xnext (or null): [T][H] receives BF16(x + out), the input of the next layer of a chained stack.
+cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
+                          float xS, float x_inv6S, const uint16_t* x, const uint16_t* wr,
+                          uint16_t* out, uint16_t* xnext);
 // out[i] = BF16(a[i] + b[i]) over n BF16 values (n % 8 == 0): a chained layer's next input.
 cudaError_t launch_residual_add(const LaunchCfg& lc, const uint16_t* a, const uint16_t* b,
                                 uint16_t* out, size_t n);
