@@ -38,6 +38,7 @@ _lib = None
 
 W4A16 = 0
 W4A4 = 1
+W4A8 = 2
 
 
 def build(force: bool = False) -> str:
@@ -122,6 +123,12 @@ def lib():
             L.oracle_moe_forward_shared.restype = ctypes.c_int
             L.oracle_moe_forward_shared.argtypes = [ctypes.POINTER(_Inputs), ctypes.c_int] + \
                 [ctypes.c_void_p] * 3 + [ctypes.POINTER(_Outputs)] + [ctypes.c_void_p] * 5
+            L.oracle_quantize_a8.restype = None
+            L.oracle_quantize_a8.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_float,
+                                             ctypes.c_void_p]
+            L.oracle_h8_ambiguity.restype = None
+            L.oracle_h8_ambiguity.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.c_double,
+                                              ctypes.c_void_p, ctypes.c_void_p]
             L.oracle_h_ambiguity.restype = None
             L.oracle_h_ambiguity.argtypes = [ctypes.c_void_p, ctypes.c_float, ctypes.c_double,
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
@@ -178,6 +185,24 @@ def quantize_nvfp4(v: np.ndarray, S: float, nthreads: int = 1):
     lib().oracle_quantize_nvfp4(_ptr(v), rows, cols, float(S), _ptr(codes), _ptr(scales),
                                 int(nthreads))
     return codes, scales
+
+
+def quantize_a8(v: np.ndarray, S: float) -> np.ndarray:
+    """The W4A8 activation quantiser: E4M3 bytes of float32 values with per-matrix scale S
+    (S8 = fl32(6 S), q = E4M3_RNE_satfinite(fl32(v * fl32(1 / S8))), sign kept)."""
+    v = _c(v, np.float32)
+    codes = np.empty(v.shape, np.uint8)
+    lib().oracle_quantize_a8(_ptr(v), v.size, float(S), _ptr(codes))
+    return codes
+
+
+def h8_ambiguity(v16: np.ndarray, S: float, eps: float, colnorm16: np.ndarray) -> np.ndarray:
+    """The W4A8 h quantiser's ambiguity for one 16-element block: elem [16] allowances."""
+    v = _c(v16, np.float32).reshape(16)
+    cn = _c(colnorm16, np.float64).reshape(16)
+    elem = np.zeros(16, np.float64)
+    lib().oracle_h8_ambiguity(_ptr(v), float(S), float(eps), _ptr(cn), _ptr(elem))
+    return elem
 
 
 def h_ambiguity(v16: np.ndarray, S: float, eps: float, colnorm16: np.ndarray):
@@ -336,9 +361,11 @@ def forward(x_bf16: np.ndarray, wr_bf16: np.ndarray, experts: ExpertSet, k: int,
                   offsets=((E + 1,), np.int32), perm=((S,), np.int32),
                   slot_of=((T, k), np.int32), g=((S, I), np.float64), u=((S, I), np.float64),
                   h=((S, I), np.float64), h_bf16=((S, I), np.uint16),
-                  hq_codes=((S, I // 2), np.uint8), hq_scales=((S, I // 16), np.uint8),
+                  hq_codes=((S, I if mode == 2 else I // 2), np.uint8),
+                  hq_scales=((S, I // 16), np.uint8),
                   h_amb_elem=((S, I), np.float64), h_amb_block=((S, I // 16), np.float64),
-                  y=((S, H), np.float64), xq_codes=((T, H // 2), np.uint8),
+                  y=((S, H), np.float64),
+                  xq_codes=((T, H if mode == 2 else H // 2), np.uint8),
                   xq_scales=((T, H // 16), np.uint8))
     res = {}
     for name in set(want) | {"out_bf16"}:

@@ -177,6 +177,19 @@ BlockQ quantize_block(const float* v, int n, float inv6S, float S) {
 
 inline float inv6S_of(float S) { return f32_div(1.0f, f32_mul(6.0f, S)); }
 
+// W4A8 activation quantiser (reading: the pages name an 8-bit expert-activation route but fix
+// neither format nor scaling; taken: FP8 E4M3, round to nearest even, saturating at 448, sign
+// kept, one FP32 scale per matrix from the same calibration as the NVFP4 input scale S, whose
+// calibrated amax maps onto E4M3's largest value 448 instead of 6 * 448):
+//   S8 = fl32(6 * S),  r8 = fl32(1 / S8),  q = E4M3_RNE_satfinite(fl32(v * r8)),
+//   decoded value = dec(q) * S8.
+inline float a8_scale(float S) { return f32_mul(6.0f, S); }
+inline float a8_inv(float S) { return f32_div(1.0f, a8_scale(S)); }
+int e4m3_encode_signed(float v) {
+  return (std::signbit(v) ? 0x80 : 0) | e4m3_encode_nonneg(std::fabs(v));
+}
+inline int quantize_a8(float v, float r8) { return e4m3_encode_signed(f32_mul(v, r8)); }
+
 // Quantise rows x cols values (cols a multiple of 16) into checkpoint layout:
 // codes [rows][cols/2] with the even column in the low nibble, scales [rows][cols/16].
 void quantize_rows(const float* v, int64_t rows, int64_t cols, float S, uint8_t* codes,
@@ -257,6 +270,33 @@ void h_ambiguity(const float* vb, float S, float inv6S, double eps, const double
   }
 }
 
+// The same window for the W4A8 h quantiser, element by element (there is no block scale): for a
+// 16-element block v of FP32 h values with the down input scale S, element i is ambiguous when
+// fl32(v_i * r8) moved by -/+ eps * a * r8 (a = the block's max |h|) encodes to different E4M3
+// bytes c_lo, c_hi; the window can span several codes of a small element (E4M3 steps are
+// relative to the element), so elem_i = max(|dec(c_lo) - dec(q)|, |dec(c_hi) - dec(q)|) * S8 *
+// colnorm_i, the largest move any code in the window makes. Pinned against an interval test.
+void h8_ambiguity(const float* vb, float S, double eps, const double* colnorm, double* elem) {
+  const float r8 = a8_inv(S);
+  const double S8 = (double)a8_scale(S);
+  float a = 0.0f;
+  for (int i = 0; i < 16; ++i) a = std::max(a, std::fabs(vb[i]));
+  for (int i = 0; i < 16; ++i) {
+    elem[i] = 0.0;
+    if (eps <= 0) continue;
+    const int q = quantize_a8(vb[i], r8);
+    const double xs = (double)f32_mul(vb[i], r8);
+    const double win = eps * (double)a * (double)r8;
+    const int c_lo = e4m3_encode_signed((float)(xs - win));
+    const int c_hi = e4m3_encode_signed((float)(xs + win));
+    if (c_lo != c_hi) {
+      const double d = std::max(std::fabs(e4m3_value(c_lo) - e4m3_value(q)),
+                                std::fabs(e4m3_value(c_hi) - e4m3_value(q)));
+      elem[i] = d * S8 * colnorm[i];
+    }
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -320,6 +360,18 @@ float oracle_quantize_weight_bf16(const uint16_t* w, int64_t rows, int64_t cols,
 void oracle_dequantize_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows,
                              int64_t cols, double mult, double* out) {
   dequantize_rows(codes, scales, rows, cols, mult, out);
+}
+
+// The W4A8 activation quantiser over n FP32 values with per-matrix scale S (codes: E4M3 bytes).
+void oracle_quantize_a8(const float* v, int64_t n, float S, uint8_t* codes) {
+  const float r8 = a8_inv(S);
+  for (int64_t i = 0; i < n; ++i) codes[i] = (uint8_t)quantize_a8(v[i], r8);
+}
+
+// The W4A8 h quantiser's ambiguity for one block (see h8_ambiguity).
+void oracle_h8_ambiguity(const float* v16, float S, double eps, const double* colnorm16,
+                         double* elem16) {
+  h8_ambiguity(v16, S, eps, colnorm16, elem16);
 }
 
 // The W4A4 h quantiser's ambiguity for one block (see h_ambiguity; pinned there).
@@ -393,7 +445,7 @@ void oracle_route(const uint16_t* x, const uint16_t* wr, int T, int H, int E, in
 // ------------------------------- the MoE forward
 struct OracleMoeInputs {
   int T, H, E, k, I;
-  int mode;             // 0 = W4A16, 1 = W4A4
+  int mode;             // 0 = W4A16, 1 = W4A4, 2 = W4A8
   int y_keep_fp64;      // 1: do not round Y to BF16 (the alternative reading)
   int nthreads;
   double amb_eps;       // W4A4 h-quantiser ambiguity window (relative to the block amax)
@@ -425,21 +477,24 @@ struct OracleMoeOutputs {
   double* u;              // [T*k][I]
   double* h;              // [T*k][I]  silu(g)*u in FP64
   uint16_t* h_bf16;       // [T*k][I]  W4A16: h rounded to BF16
-  uint8_t* hq_codes;      // [T*k][I/2] W4A4: Q(h) codes
+  uint8_t* hq_codes;      // [T*k][I/2] W4A4: Q(h) codes; W4A8: [T*k][I] E4M3 bytes
   uint8_t* hq_scales;     // [T*k][I/16]
-  double* h_amb_elem;     // [T*k][I]   W4A4: |dh| * ||Wd[:,i]|| if element i's code is ambiguous
+  double* h_amb_elem;     // [T*k][I]   W4A4/W4A8: |dh| * ||Wd[:,i]|| if element i is ambiguous
   double* h_amb_block;    // [T*k][I/16] W4A4: contribution bound if the block scale is ambiguous
   double* y;              // [T*k][H]  Y (after the BF16 rounding unless y_keep_fp64)
-  uint8_t* xq_codes;      // [T][H/2]  W4A4: Q(x) with the gate input scale of expert 0
+  uint8_t* xq_codes;      // [T][H/2]  W4A4: Q(x) with the gate input scale of expert 0;
+                          // W4A8: [T][H] E4M3 bytes
   uint8_t* xq_scales;     // [T][H/16]
 };
 
 // Steps (reading of the pages plus the stated readings):
 //  1-4. routing as oracle_route.
-//  5. per slot: g_i = sum_h a_h * Wg[i][h], u_i likewise, with a = x (W4A16) or a = dec(Q(x, S))
-//     using each matrix's own input scale S (W4A4); W = code*scale*multiplier. FP64.
+//  5. per slot: g_i = sum_h a_h * Wg[i][h], u_i likewise, with a = x (W4A16), a = dec(Q(x, S))
+//     (W4A4) or a = dec(E4M3(x * r8)) * S8 (W4A8), using each matrix's own input scale S;
+//     W = code*scale*multiplier. FP64.
 //  6. h_i = silu(g_i) * u_i = g_i / (1 + exp(-g_i)) * u_i, FP64.
-//  7. h -> BF16 RNE (W4A16), or h -> Q(fl32(h), S_down) decoded (W4A4).
+//  7. h -> BF16 RNE (W4A16), h -> Q(fl32(h), S_down) decoded (W4A4), or h -> E4M3 of
+//     fl32(h) under the down matrix's scale, decoded (W4A8).
 //  8. Y[r] = sum_i h_i * Wd[r][i] in FP64, then BF16 RNE (unless y_keep_fp64).
 //  9. out[t][r] = BF16_RNE( sum_{j=0..k-1} w[t][j] * Y_{slot(t,j)}[r] ), j in rank order.
 // Pinned by: one-hot weights (closed form), identical experts, SiLU(0)=0, representable-x
@@ -479,7 +534,7 @@ int oracle_moe_forward(const OracleMoeInputs* in, OracleMoeOutputs* out) {
     dequantize_rows(in->up_codes[e], in->up_scales[e], I, H, mu, Wu.data());
     dequantize_rows(in->down_codes[e], in->down_scales[e], H, I, md, Wd.data());
     std::vector<double> colnorm(I, 0.0);
-    if (in->mode == 1) {
+    if (in->mode != 0) {
       for (int i = 0; i < I; ++i) {
         double s2 = 0.0;
         for (int r = 0; r < H; ++r) s2 += Wd[(size_t)r * I + i] * Wd[(size_t)r * I + i];
@@ -504,6 +559,16 @@ int oracle_moe_forward(const OracleMoeInputs* in, OracleMoeOutputs* out) {
             au[b * 16 + i] = e2m1_value(qu.q[i]) * kE4M3[qu.sf] * (double)Su;
           }
         }
+      } else if (in->mode == 2) {
+        // W4A8: the activation is replaced by its E4M3 quantisation under each matrix's scale.
+        const float Sg = in->in_scale[e * 3 + 0], Su = in->in_scale[e * 3 + 1];
+        const float rg = a8_inv(Sg), ru = a8_inv(Su);
+        const double S8g = a8_scale(Sg), S8u = a8_scale(Su);
+        for (int hh = 0; hh < H; ++hh) {
+          const float v = (float)xt[hh];
+          ag[hh] = e4m3_value(quantize_a8(v, rg)) * S8g;
+          au[hh] = e4m3_value(quantize_a8(v, ru)) * S8u;
+        }
       } else {
         for (int hh = 0; hh < H; ++hh) ag[hh] = au[hh] = xt[hh];
       }
@@ -526,6 +591,24 @@ int oracle_moe_forward(const OracleMoeInputs* in, OracleMoeOutputs* out) {
           uint16_t b = double_to_bf16(hv[i]);
           hdec[i] = bf16_to_double(b);
           if (out->h_bf16) out->h_bf16[(size_t)slot * I + i] = b;
+        }
+      } else if (in->mode == 2) {
+        // W4A8: h -> E4M3 with the down matrix's scale, decoded
+        const float Sd = in->in_scale[e * 3 + 2];
+        const float r8 = a8_inv(Sd);
+        const double S8 = a8_scale(Sd);
+        for (int i = 0; i < I; ++i) hf[i] = (float)hv[i];
+        for (int i = 0; i < I; ++i) {
+          const int q = quantize_a8(hf[i], r8);
+          hdec[i] = e4m3_value(q) * S8;
+          if (out->hq_codes) out->hq_codes[(size_t)slot * I + i] = (uint8_t)q;
+        }
+        for (int b = 0; b < I / 16; ++b) {
+          double amb_e[16];
+          h8_ambiguity(hf.data() + b * 16, Sd, in->amb_eps, colnorm.data() + b * 16, amb_e);
+          if (out->h_amb_block) out->h_amb_block[(size_t)slot * (I / 16) + b] = 0.0;
+          if (out->h_amb_elem)
+            for (int i = 0; i < 16; ++i) out->h_amb_elem[(size_t)slot * I + b * 16 + i] = amb_e[i];
         }
       } else {
         const float Sd = in->in_scale[e * 3 + 2];
@@ -576,6 +659,10 @@ int oracle_moe_forward(const OracleMoeInputs* in, OracleMoeOutputs* out) {
   if (out->perm) std::memcpy(out->perm, perm.data(), sizeof(int32_t) * S);
   if (out->slot_of) std::memcpy(out->slot_of, slot_of.data(), sizeof(int32_t) * S);
   if (out->y) std::memcpy(out->y, Y.data(), sizeof(double) * Y.size());
+  if (in->mode == 2 && out->xq_codes) {
+    const float r8 = a8_inv(in->in_scale[0]);
+    for (size_t i = 0; i < (size_t)T * H; ++i) out->xq_codes[i] = (uint8_t)quantize_a8((float)xd[i], r8);
+  }
   if (in->mode == 1 && out->xq_codes && out->xq_scales) {
     std::vector<float> xf(H);
     const float Sg = in->in_scale[0];

@@ -607,6 +607,144 @@ def test_forward_h_ambiguity_is_the_block_function(tiny):
             assert res["h_amb_block"][s, b] == pytest.approx(ref_b, rel=1e-9, abs=0)
 
 
+# ------------------------------------------------------------------ W4A8 activations
+def _e4m3_signed_brute(v):
+    """Nearest E4M3 byte of a float (ties to the even byte, saturating at 448), sign kept."""
+    a = abs(v)
+    b = 0x7E if a >= 448 else _nearest_brute(_E4M3_MAGS, a, list(range(0x7F)))
+    return b | (0x80 if math.copysign(1, v) < 0 else 0)
+
+
+def test_a8_quantizer_matches_numpy_float32_and_brute_force():
+    rng = np.random.default_rng(61)
+    for _ in range(40):
+        S = np.float32(np.exp(rng.uniform(-10, 0)))
+        S8 = np.float32(6) * S
+        r8 = np.float32(1) / S8
+        v = (rng.standard_normal(200) * np.exp(rng.uniform(-6, 6, 200)) * 100 * S8).astype(
+            np.float32)
+        v[:4] = [0.0, -0.0, -1e-30, 1e30]
+        # scaled values on E4M3 midpoints and their neighbours
+        mids = np.array(_E4M3_MIDS[::9], np.float32)
+        v[4:4 + len(mids)] = (mids / r8).astype(np.float32)
+        got = oracle.quantize_a8(v, float(S))
+        for i in range(len(v)):
+            assert got[i] == _e4m3_signed_brute(float(v[i] * r8)), (float(v[i]), float(S))
+
+
+def test_a8_quantizer_round_trip_and_saturation():
+    rng = np.random.default_rng(62)
+    S = 2.0 ** -9 / 6          # S8 = 2^-9 exactly: dec(q) * S8 is exact in float32
+    S8 = np.float32(6) * np.float32(S)
+    assert S8 == np.float32(2.0 ** -9)
+    codes = rng.integers(0, 256, 2000)
+    codes = codes[(codes & 0x7F) != 0x7F]                       # no NaN
+    v = np.array([_e4m3_closed(int(c)) for c in codes], np.float64) * float(S8)
+    assert np.array_equal(v.astype(np.float32).astype(np.float64), v)
+    got = oracle.quantize_a8(v.astype(np.float32), S)
+    assert np.array_equal(got, codes.astype(np.uint8))
+    big = oracle.quantize_a8(np.array([1e9, -1e9, 500 * float(S8)], np.float32), S)
+    assert list(big) == [0x7E, 0xFE, 0x7E]
+
+
+def test_forward_w4a8_equals_w4a16_before_h_on_representable_x(tiny):
+    wl, _, wr, ex0 = tiny
+    rng = np.random.default_rng(63)
+    S = 2.0 ** -7 / 6          # S8 = 2^-7
+    ex = oracle.ExpertSet(wl.E, wl.H, wl.I)
+    for e in range(wl.E):
+        ex.set(e, ex0.gate[e], ex0.up[e], ex0.down[e], ex0.mult[e], (S, S, ex0.in_scale[e, 2]))
+    codes = rng.integers(0, 256, (wl.T, wl.H))
+    codes[(codes & 0x7F) == 0x7F] = 0x3C
+    xv = np.vectorize(_e4m3_closed)(codes) * 2.0 ** -7
+    x = synth.bf16_bits(xv.astype(np.float32))
+    assert np.array_equal(synth.bf16_to_f32(x).astype(np.float64), xv)   # exactly BF16
+    a = oracle.forward(x, wr, ex, wl.k, oracle.W4A16, want=("g", "u"))
+    b = oracle.forward(x, wr, ex, wl.k, oracle.W4A8, want=("g", "u", "xq_codes"))
+    assert np.array_equal(a["g"], b["g"]) and np.array_equal(a["u"], b["u"])
+    assert np.array_equal(b["xq_codes"], oracle.quantize_a8(synth.bf16_to_f32(x), S))
+
+
+def test_forward_w4a8_h_codes_and_numpy_pipeline(tiny):
+    wl, x, wr, ex = tiny
+    res = oracle.forward(x, wr, ex, wl.k, oracle.W4A8,
+                         want=("h", "g", "u", "hq_codes", "counts", "y", "out64", "idx", "w",
+                               "slot_of", "h_amb_elem", "h_amb_block"))
+    offs = np.concatenate([[0], np.cumsum(res["counts"])])
+    xf = synth.bf16_to_f32(x)
+    for s in range(wl.T * wl.k):
+        e = int(np.searchsorted(offs, s, side="right") - 1)
+        t = [tt for tt in range(wl.T) for j in range(wl.k) if res["slot_of"][tt, j] == s][0]
+        Sg, Su, Sd = (float(ex.in_scale[e, i]) for i in range(3))
+        # the activations: E4M3 under each matrix's scale, decoded (numpy float32 steps)
+        dq = lambda v, S_: np.array([_e4m3_closed(int(c)) for c in oracle.quantize_a8(v, S_)]) \
+            * float(np.float32(6) * np.float32(S_))
+        Wg = oracle.dequantize_nvfp4(ex.gate[e][0], ex.gate[e][1], float(ex.mult[e, 0]))
+        Wu = oracle.dequantize_nvfp4(ex.up[e][0], ex.up[e][1], float(ex.mult[e, 1]))
+        Wd = oracle.dequantize_nvfp4(ex.down[e][0], ex.down[e][1], float(ex.mult[e, 2]))
+        g = Wg @ dq(xf[t], Sg)
+        u = Wu @ dq(xf[t], Su)
+        np.testing.assert_allclose(res["g"][s], g, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(res["u"][s], u, rtol=1e-12, atol=1e-14)
+        hq = oracle.quantize_a8(res["h"][s].astype(np.float32), Sd)
+        assert np.array_equal(hq, res["hq_codes"][s])
+        y = Wd @ (np.array([_e4m3_closed(int(c)) for c in hq]) *
+                  float(np.float32(6) * np.float32(Sd)))
+        yb = synth.bf16_to_f32(synth.bf16_bits(y.astype(np.float64).astype(np.float32)))
+        np.testing.assert_allclose(res["y"][s], yb, rtol=2 ** -8, atol=1e-12)
+    assert np.all(res["h_amb_block"] == 0)
+
+
+def _amb8_ref(v, S, eps, cn):
+    """Independent window test: element i is flagged when a rounding midpoint lies in the closed
+    interval of scaled values it could take; its allowance is the largest move of the nearest
+    E4M3 value over that interval (at the interval's ends), times S8 and the column norm."""
+    v = np.asarray(v, np.float32)
+    S8 = np.float32(6) * np.float32(S)
+    r8 = np.float32(1) / S8
+    a = float(np.abs(v).max())
+    elem = np.zeros(16)
+    win = eps * a * float(r8)
+    for i in range(16):
+        xs = float(v[i] * r8)
+        lo, hi = abs(xs) - win, abs(xs) + win
+        if any(lo <= m <= hi for m in _E4M3_MIDS):
+            q = _e4m3_closed(_e4m3_signed_brute(xs))
+            ends = [_e4m3_closed(_e4m3_signed_brute(xs - win)),
+                    _e4m3_closed(_e4m3_signed_brute(xs + win))]
+            elem[i] = max(abs(d - q) for d in ends) * float(S8) * cn[i]
+    return elem
+
+
+def test_h8_ambiguity_constructed_and_random():
+    rng = np.random.default_rng(64)
+    for it in range(200):
+        S = float(np.float32(np.exp(rng.uniform(-9, -3))))
+        r8 = np.float32(1) / (np.float32(6) * np.float32(S))
+        v = (rng.standard_normal(16) * 50 / r8).astype(np.float32)
+        a = float(np.abs(v).max())
+        win = _AMB_EPS * a * float(r8)
+        for i in range(16):
+            if rng.random() < 0.5 and abs(v[i]) < a * 0.9:
+                m = _E4M3_MIDS[int(rng.integers(0, 0x7E))]
+                f = rng.uniform(-2.5, 2.5)
+                if 0.9 < abs(f) < 1.1:
+                    f = 0.4
+                if m + f * win < a * float(r8) * 0.95:
+                    v[i] = np.float32(np.sign(rng.standard_normal()) * (m + f * win) / float(r8))
+        cn = rng.uniform(0.1, 4.0, 16)
+        got = oracle.h8_ambiguity(v, S, _AMB_EPS, cn)
+        np.testing.assert_allclose(got, _amb8_ref(v, S, _AMB_EPS, cn), rtol=1e-12, atol=0,
+                                   err_msg=str(it))
+    # an element exactly on a midpoint (1.0625 between 0x38 and 0x39 in scaled units) is flagged
+    S = 2.0 ** -8 / 6
+    v = np.zeros(16, np.float32)
+    v[0] = np.float32(104.0 * 2.0 ** -8)     # the block amax, an E4M3 value (0x6D)
+    v[1] = np.float32(1.0625 * 2.0 ** -8)
+    got = oracle.h8_ambiguity(v, S, _AMB_EPS, np.ones(16))
+    assert got[1] == pytest.approx(0.125 * 2.0 ** -8, rel=1e-12) and got[0] == 0
+
+
 def test_synth_streams_are_deterministic_and_independent():
     a = synth.expert_weight(0, 3, 7, "gate", 64, 32)
     b = synth.expert_weight(0, 3, 7, "gate", 64, 32)
