@@ -540,7 +540,7 @@ def e2e_measure(wl, stack, steps, state, device, use_graph=True):
 def bench_config(wl, layers, world, args):
     """The workload description both arms print (the same dict, so the lines compare)."""
     return dict(workload=wl.name, T=wl.T, layers=layers, hidden=wl.H, experts=wl.E, top_k=wl.k,
-                inter=wl.I, mode=["W4A16", "W4A4"][wl.mode],
+                inter=wl.I, mode=["W4A16", "W4A4", "W4A8"][wl.mode],
                 parallelism=f"replicas x{world}" if world > 1 else "single GPU",
                 l2=("no flush: a step streams 48 layers x 10 experts = 1.27 GB > 129 MB L2"
                     if wl.T == 1 and layers >= 48 else
@@ -681,7 +681,7 @@ def run_native(args, rank, world, local_rank):
     extra = {}
     if not args.no_extra and not args.shared and rank == 0:
         packs = [L.pack for L in stack]
-        for name in ("verify8", "verify8_w4a4"):
+        for name in ("verify8", "verify8_w4a4", "verify8_w4a8"):
             w2 = synth.WORKLOADS[name]
             st2 = build_stack(w2, layers, args.seed, device, packs=packs)
             ms2, _, _, _ = measure(w2, st2, max(3, args.steps // 2), 3, not args.no_graph, device)
@@ -721,7 +721,7 @@ def run_native(args, rank, world, local_rank):
                 frac_hbm=round(b4 / (ms4 / layers * 1e-3) / 1e9 / pk["hbm"], 4),
                 note="routed experts' bytes + the shared expert's BF16 bytes per layer time")
             del st4
-        for mode, shared in ((1, False), (0, False), (1, True)):
+        for mode, shared in ((1, False), (0, False), (1, True), (2, False)):
             name = "prefill8192"
             w3 = synth.Workload(name, 8192, wl.H, wl.E, wl.k, wl.I, mode, 1, True)
             st3 = build_stack(w3, 1, args.seed, device, packs=packs[:1])
@@ -730,7 +730,7 @@ def run_native(args, rank, world, local_rank):
             ms3, _, _, _ = measure(w3, st3, 3, 2, False, device)
             kern3 = launch_times(w3, st3, reps=2, device=device)
             flops = 2 * w3.T * w3.k * 3 * w3.I * w3.H
-            key = f"prefill8192_{['w4a16', 'w4a4'][mode]}" + ("_shared" if shared else "")
+            key = f"prefill8192_{['w4a16', 'w4a4', 'w4a8'][mode]}" + ("_shared" if shared else "")
             extra[key] = dict(
                 tokens_per_s=round(w3.T / (ms3 / 1e3), 1), ms=round(ms3, 3),
                 expert_tflops=round(flops / (ms3 * 1e-3) / 1e12, 2),
@@ -738,7 +738,7 @@ def run_native(args, rank, world, local_rank):
                 roofline=prefill_roofline(w3, ms3, kern3, st3[0].U, pk, shared),
                 note=("tcgen05 block-scaled FP4 grouped GEMMs" if mode == 1 else
                       "tcgen05 kind::f16 grouped GEMMs, weights dequantised to f16 in shared "
-                      "memory"))
+                      "memory" + (", E4M3 activations decoded to f16" if mode == 2 else "")))
             if shared:
                 sflops = 2 * w3.T * 3 * w3.I * w3.H
                 extra[key].update(shared_tflop=round(sflops / 1e12, 4), note=(

@@ -54,7 +54,14 @@ typedef enum {
 
 typedef enum {
   MOE_W4A16 = 0,  /* BF16 activations on NVFP4 weights ("--a16-activations" route)          */
-  MOE_W4A4 = 1    /* activations quantised to NVFP4 with the per-matrix input scale         */
+  MOE_W4A4 = 1,   /* activations quantised to NVFP4 with the per-matrix input scale         */
+  MOE_W4A8 = 2    /* activations quantised to FP8 E4M3 ("--a8-activations" route; reading:
+                   * E4M3 round-to-nearest-even, saturating at 448, sign kept, one FP32 scale
+                   * per matrix S8 = fl32(6 S) from the matrix's input scale S, so
+                   * code = E4M3(fl32(v * fl32(1 / S8))), value = E4M3(code) * S8; x per gate/up
+                   * matrix, h with the down matrix's scale). Runs on the fused narrow-call
+                   * kernel and the wide tensor-core f16 path; other shapes return
+                   * MOE_ERR_UNSUPPORTED. */
 } moe_mode;
 
 /* Opaque, device-resident, library-owned set of one layer's routed experts. */
@@ -144,7 +151,7 @@ moe_status moe_route_topk_noalloc(const uint16_t* x, const uint16_t* router_w, i
 
 /* The whole MoE feed-forward step: out [T][H] BF16 (device) from x [T][H] BF16 and router_w
  * [E][H] BF16 (device), using the experts of `pack` in `mode`. T <= 8 runs the narrow decode
- * kernels; larger T runs the grouped (prefill) kernels. W4A4 requires every gate and up
+ * kernels; larger T runs the grouped (prefill) kernels. W4A4 and W4A8 require every gate and up
  * matrix of the pack to share one input scale (else MOE_ERR_UNSUPPORTED). out must not alias
  * x. ws/ws_bytes: see moe_workspace_size. */
 moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_expert_pack* pack,
@@ -191,10 +198,11 @@ typedef struct {
   size_t offsets;    /* int32 [E+1]       */
   size_t perm;       /* int32 [T*k]       */
   size_t slot_of;    /* int32 [T][k]: position of (t, idx[t][j]) in perm */
-  size_t x_codes;    /* uint8 [T][H/2]   (W4A4: Q(x) codes, checkpoint nibble order) */
+  size_t x_codes;    /* uint8 [T][H/2]   (W4A4: Q(x) codes, checkpoint nibble order;
+                        W4A8: [T][H] E4M3 codes) */
   size_t x_scales;   /* uint8 [T][H/16]  (W4A4: Q(x) E4M3 scales)                    */
   size_t h_bf16;     /* uint16 [T*k][I]  (W4A16: h rounded to BF16, rows = perm slots) */
-  size_t h_codes;    /* uint8 [T*k][I/2] (W4A4: Q(h) codes)                          */
+  size_t h_codes;    /* uint8 [T*k][I/2] (W4A4: Q(h) codes; W4A8: [T*k][I] E4M3 codes) */
   size_t h_scales;   /* uint8 [T*k][I/16] (W4A4: Q(h) scales)                        */
   size_t y;          /* uint16 [T*k][H]  BF16 expert outputs Y, rows = perm slots     */
 } moe_ws_offsets;

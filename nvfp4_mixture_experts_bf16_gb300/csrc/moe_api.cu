@@ -78,7 +78,7 @@ struct WsLayout {
   int G, NT;
 };
 
-// mode: 0 W4A16, 1 W4A4, -1 routing only (no expert buffers). Is > 0 adds the shared
+// mode: 0 W4A16, 1 W4A4, 2 W4A8, -1 routing only (no expert buffers). Is > 0 adds the shared
 // expert's buffers after everything else, so the other offsets do not depend on it.
 WsLayout ws_layout(int T, int H, int E, int k, int I, int mode, int Is = 0) {
   WsLayout L;
@@ -102,10 +102,10 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode, int Is = 0) {
   L.chunk_base = take(T > moe::kNarrowT ? (size_t)nchunk * E * 4 : 0);
   L.xh = take(mode >= 0 ? (size_t)T * H * 2 : 0);
   L.xfac = take(mode >= 0 ? (size_t)T * 4 : 0);
-  L.xq = take(mode == 1 ? (size_t)T * H / 2 : 0);
+  L.xq = take(mode == 1 ? (size_t)T * H / 2 : mode == 2 ? (size_t)T * H : 0);
   L.xsf = take(mode == 1 ? (size_t)T * H / 16 : 0);
   L.h16 = take(mode == 0 ? (size_t)S * I * 2 : 0);
-  L.hq = take(mode == 1 ? (size_t)S * I / 2 : 0);
+  L.hq = take(mode == 1 ? (size_t)S * I / 2 : mode == 2 ? (size_t)S * I : 0);
   L.hsf = take(mode == 1 ? (size_t)S * I / 16 : 0);
   L.y = take(mode >= 0 ? (size_t)S * H * 2 : 0);
   L.htag = take(mode >= 0 && narrow ? (size_t)S * (I / 16) * 9 * 8 : 0);
@@ -114,7 +114,7 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode, int Is = 0) {
   const bool tc = mode >= 0 && moe::tile_path(T, H, I, mode);
   L.NT = tc ? (int)((S + 127) / 128 + (S < E ? S : E)) : 0;
   const size_t P = (size_t)L.NT * 128;
-  const bool w4a4 = tc && mode == 1, w4a16 = tc && mode == 0;
+  const bool w4a4 = tc && mode == 1, w4a16 = tc && (mode == 0 || mode == 2);
   L.tt_expert = take((size_t)L.NT * 4);
   L.tt_slot0 = take((size_t)L.NT * 4);
   L.tt_n = take((size_t)L.NT * 4);
@@ -178,6 +178,15 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
 
 moe_status from_cuda(cudaError_t e) {
   return e == cudaSuccess ? MOE_OK : (e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA);
+}
+
+bool mode_ok(int mode) { return mode == MOE_W4A16 || mode == MOE_W4A4 || mode == MOE_W4A8; }
+
+// W4A8 runs on the fused narrow kernel and on the wide tcgen05 f16 path only
+bool a8_supported(int T, int H, int E, int k, int I) {
+  if (T <= moe::kNarrowT)
+    return moe::decode_geom(T, H, E, k, I, num_sms_of_current_device(), nullptr);
+  return moe::tile_path(T, H, I, 2);
 }
 
 bool route_shape_ok(int T, int H, int E, int k) {
@@ -392,7 +401,7 @@ moe_status moe_pack_get_matrix(const moe_expert_pack* pack, int expert, int whic
 
 moe_status moe_workspace_size(const moe_expert_pack* pack, int T, int k, moe_mode mode,
                               size_t* bytes) {
-  if (!pack || !bytes || (mode != MOE_W4A16 && mode != MOE_W4A4) ||
+  if (!pack || !bytes || !mode_ok(mode) ||
       !route_shape_ok(T, pack->H, pack->E, k))
     return MOE_ERR_INVALID_ARG;
   *bytes = ws_layout(T, pack->H, pack->E, k, pack->I, (int)mode).total;
@@ -407,7 +416,7 @@ moe_status moe_route_workspace_size(int T, int H, int E, int k, size_t* bytes) {
 
 moe_status moe_workspace_offsets(const moe_expert_pack* pack, int T, int k, moe_mode mode,
                                  moe_ws_offsets* off) {
-  if (!pack || !off || (mode != MOE_W4A16 && mode != MOE_W4A4) ||
+  if (!pack || !off || !mode_ok(mode) ||
       !route_shape_ok(T, pack->H, pack->E, k))
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(T, pack->H, pack->E, k, pack->I, (int)mode);
@@ -509,7 +518,7 @@ cudaError_t launch_forward(moe::LaunchCfg lc, const moe_expert_pack* pack,
         e = moe::launch_tc_experts(lc, pack->view, v, x, pack->x_scale, pack->x_inv6S);
         *n += 3;
       } else {
-        e = moe::launch_tc16_experts(lc, pack->view, v, x);
+        e = moe::launch_tc16_experts(lc, pack->view, v, x, m == 2, pack->x_scale, pack->x_inv6S);
         *n += 4;
       }
     }
@@ -540,12 +549,13 @@ moe_status forward_impl(const uint16_t* x, const uint16_t* router_w, const moe_e
   if (!x || !router_w || !pack || !out || !ws) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(out) || !aligned16(ws))
     return MOE_ERR_INVALID_ARG;
-  if (mode != MOE_W4A16 && mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
+  if (!mode_ok(mode)) return MOE_ERR_INVALID_ARG;
   const int H = pack->H, E = pack->E, I = pack->I;
   if (!route_shape_ok(T, H, E, k)) return MOE_ERR_INVALID_ARG;
   if (reinterpret_cast<const void*>(out) == reinterpret_cast<const void*>(x))
     return MOE_ERR_INVALID_ARG;
-  if (mode == MOE_W4A4 && !pack->x_scale_uniform) return MOE_ERR_UNSUPPORTED;
+  if (mode != MOE_W4A16 && !pack->x_scale_uniform) return MOE_ERR_UNSUPPORTED;
+  if (mode == MOE_W4A8 && !a8_supported(T, H, E, k, I)) return MOE_ERR_UNSUPPORTED;
   const bool narrow = T <= moe::kNarrowT;
   if (sh && !narrow && !moe::tc_supported()) return MOE_ERR_UNSUPPORTED;
   const WsLayout L = ws_layout(T, H, E, k, I, (int)mode, sh ? sh->inter : 0);
@@ -574,7 +584,7 @@ moe_status moe_forward(const uint16_t* x, const uint16_t* router_w, const moe_ex
 
 moe_status moe_workspace_size_layers(const moe_expert_pack* pack, int layers, int T, int k,
                                      moe_mode mode, size_t* bytes) {
-  if (!pack || !bytes || layers < 1 || (mode != MOE_W4A16 && mode != MOE_W4A4) ||
+  if (!pack || !bytes || layers < 1 || !mode_ok(mode) ||
       !route_shape_ok(T, pack->H, pack->E, k))
     return MOE_ERR_INVALID_ARG;
   *bytes = layers_total(ws_layout(T, pack->H, pack->E, k, pack->I, (int)mode), layers);
@@ -601,7 +611,7 @@ moe_status moe_forward_layers(const uint16_t* x, const uint16_t* const* router_w
   g_last_launches = 0;
   if (!x || !router_w || !packs || !out || !ws || layers < 1) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
-  if (mode != MOE_W4A16 && mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
+  if (!mode_ok(mode)) return MOE_ERR_INVALID_ARG;
   const moe_expert_pack* p0 = packs[0];
   if (!p0) return MOE_ERR_INVALID_ARG;
   const int H = p0->H, E = p0->E, I = p0->I;
@@ -609,8 +619,9 @@ moe_status moe_forward_layers(const uint16_t* x, const uint16_t* const* router_w
   for (int l = 0; l < layers; ++l) {
     if (!packs[l] || !router_w[l] || !aligned16(router_w[l])) return MOE_ERR_INVALID_ARG;
     if (packs[l]->H != H || packs[l]->E != E || packs[l]->I != I) return MOE_ERR_INVALID_ARG;
-    if (mode == MOE_W4A4 && !packs[l]->x_scale_uniform) return MOE_ERR_UNSUPPORTED;
+    if (mode != MOE_W4A16 && !packs[l]->x_scale_uniform) return MOE_ERR_UNSUPPORTED;
   }
+  if (mode == MOE_W4A8 && !a8_supported(T, H, E, k, I)) return MOE_ERR_UNSUPPORTED;
   const size_t act = (size_t)T * H;   // elements of one layer's activations
   const uint16_t* xe = x + act;
   if (xe > out && x < out + layers * act) return MOE_ERR_INVALID_ARG;   // x overlaps out
@@ -659,7 +670,7 @@ moe_status moe_forward_layers(const uint16_t* x, const uint16_t* const* router_w
 
 moe_status moe_workspace_size_shared(const moe_expert_pack* pack, int T, int k, moe_mode mode,
                                      int shared_inter, size_t* bytes) {
-  if (!pack || !bytes || (mode != MOE_W4A16 && mode != MOE_W4A4) ||
+  if (!pack || !bytes || !mode_ok(mode) ||
       !route_shape_ok(T, pack->H, pack->E, k) || shared_inter < 64 || shared_inter % 64 ||
       shared_inter > 2048)
     return MOE_ERR_INVALID_ARG;

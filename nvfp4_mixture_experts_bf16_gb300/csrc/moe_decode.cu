@@ -309,8 +309,10 @@ template <int NT, int MODE>
 __global__ void __launch_bounds__(kDcThreads, 1)
     k_decode(PackView pk, WsView ws, DcGeom geo, const uint16_t* __restrict__ x,
              const uint16_t* __restrict__ wr, float xS, float x_inv6S,
-             uint16_t* __restrict__ out, uint16_t* __restrict__ xnext) {
-  constexpr int mode = MODE;   // 0: W4A16, 1: W4A4 (one instantiation each: smaller code)
+             uint16_t* __restrict__ out, uint16_t* __restrict__ xnext, int a8) {
+  // 0: W4A16, 1: quantised activations (one instantiation each: smaller code): NVFP4 (W4A4), or
+  // E4M3 (W4A8) when a8 is set; both run the same f16 MMAs on exactly decoded values
+  constexpr int mode = MODE;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* arena = smem;
   unsigned char* xop = arena + geo.arena;
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
 #pragma unroll
     for (int w = 1; w < kDcWarps; ++w) m = fmaxf(m, amax_part[w * 8 + t]);
     shift_s[t] = token_shift(m);
-    xfac_s[t] = mode == 0 ? pow2f(shift_s[t]) : xS;
+    xfac_s[t] = mode == 0 ? pow2f(shift_s[t]) : (a8 ? __fmul_rn(6.0f, xS) : xS);
   }
   __syncthreads();
 
@@ -633,6 +635,17 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         const float f = pow2f(-shift_s[t]);
 #pragma unroll
         for (int i = 0; i < 16; ++i) hv[i] = __float2half_rn(__fmul_rn(v[i], f));
+      } else if (a8) {
+        // W4A8: one E4M3 code per element; the f16 operand is the code's value (exact)
+        uint32_t cw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) cw[i >> 2] |= a8_encode(v[i], x_inv6S) << (8 * (i & 3));
+        if (blk % G == b)   // this CTA's share of the published W4A8 activation codes
+          *reinterpret_cast<uint4*>(ws.xq + (size_t)t * H + bb * 16) =
+              make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        uint32_t* hw = reinterpret_cast<uint32_t*>(hv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hw[i] = e4m3x2_to_f16x2(cw[i >> 1] >> (16 * (i & 1)));
       } else {
         uint32_t codes[2];
         const uint32_t sf = quantize16(v, xS, x_inv6S, codes);
@@ -871,6 +884,17 @@ __global__ void __launch_bounds__(kDcThreads, 1)
             if ((r & 1) == 0) st_tag(htp + r / 2, (uint32_t)hb | (hb_next << 16), ep);
             if (r == 0) st_tag(htp + 8, __float_as_uint(a), ep);
           }
+        } else if (a8) {
+          // W4A8: h -> E4M3 with the down matrix's scale (i6d = fl32(1/fl32(6 sd))), one byte per
+          // element; rows 4w..4w+3 of a column (its 16 consecutive lanes) make tagged word w
+          const uint32_t q8 = a8_encode(hv, i6d);
+          uint32_t wv = q8 << (8 * (r & 3));
+          wv |= __shfl_xor_sync(0xFFFFFFFFu, wv, 1);
+          wv |= __shfl_xor_sync(0xFFFFFFFFu, wv, 2);
+          if (cvalid) {
+            ws.hq[slot * I + it * 16 + r] = static_cast<uint8_t>(q8);
+            if ((r & 3) == 0) st_tag(htp + r / 4, wv, ep);
+          }
         } else {
           // the quantiser Q of this 16-element block of h (down input scale)
           float a = fabsf(hv);
@@ -959,6 +983,11 @@ __global__ void __launch_bounds__(kDcThreads, 1)
           bool ok;
           if (mode == 0) {
             ok = poll_tags<9>(src, ep, w);
+          } else if (a8) {
+            unsigned long long w4[4];
+            ok = poll_tags<4>(src, ep, w4);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) w[q4] = w4[q4];
           } else {
             unsigned long long w3[3];
             ok = poll_tags<3>(src, ep, w3);
@@ -976,6 +1005,12 @@ __global__ void __launch_bounds__(kDcThreads, 1)
 #pragma unroll
             for (int p2 = 0; p2 < 8; ++p2) dst[p2] = data_of(w[p2]);
             atomicMax(&hamax_s[row], data_of(w[8]));
+          } else if (a8) {
+            // W4A8: the E4M3 codes' values (exact in f16); the scale fl32(6 sd) in the epilogue
+#pragma unroll
+            for (int p2 = 0; p2 < 8; ++p2)
+              dst[p2] = e4m3x2_to_f16x2(data_of(w[p2 >> 1]) >> (16 * (p2 & 1)));
+            if (it == 0) hfac_s[row] = __fmul_rn(6.0f, sd);
           } else {
             const float sv = e4m3_value_nonneg(data_of(w[2]));
             const uint32_t cw[2] = {data_of(w[0]), data_of(w[1])};
@@ -1244,6 +1279,8 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
 cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
                           float xS, float x_inv6S, const uint16_t* x, const uint16_t* wr,
                           uint16_t* out, uint16_t* xnext) {
+  const int a8 = mode == 2;
+  if (a8) mode = 1;   // W4A8 runs the quantised-activation instantiations
   DcGeom geo;
   if (!decode_geom(ws.T, ws.H, ws.E, ws.k, ws.I, lc.num_sms, &geo)) return cudaErrorInvalidValue;
   auto go = [&](auto kern) -> cudaError_t {
@@ -1251,7 +1288,7 @@ cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(lc, kern, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, pk, ws,
-                         geo, x, wr, xS, x_inv6S, out, xnext);
+                         geo, x, wr, xS, x_inv6S, out, xnext, a8);
   };
   if (mode == 1) {
     switch (ws.T) {

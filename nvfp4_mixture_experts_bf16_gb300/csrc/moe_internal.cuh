@@ -61,10 +61,10 @@ struct WsView {
   int32_t* chunk_base; // [nchunk][E] (grouped routing)
   __half* xh;          // [T][H] activations as the f16 B operand of gate/up
   float* xfac;         // [T] factor restoring xh's scale (2^shift in W4A16, S_x in W4A4)
-  uint8_t* xq;         // [T][H/2]  W4A4 activation codes
+  uint8_t* xq;         // [T][H/2]  W4A4 activation codes ([T][H] E4M3 codes in W4A8)
   uint8_t* xsf;        // [T][H/16] W4A4 activation scales
   uint16_t* h16;       // [T*k][I] W4A16 h (BF16)
-  uint8_t* hq;         // [T*k][I/2] W4A4 h codes
+  uint8_t* hq;         // [T*k][I/2] W4A4 h codes ([T*k][I] E4M3 codes in W4A8)
   uint8_t* hsf;        // [T*k][I/16] W4A4 h scales
   uint16_t* y;         // [T*k][H] BF16 expert outputs
   // fused narrow kernel: 64-bit words {data, epoch} that other CTAs poll instead of a barrier
@@ -280,6 +280,14 @@ __device__ __forceinline__ uint32_t e4m3_encode_rn(float t) {
   if (m == 8) { m = 0; ef += 1; }
   uint32_t r = (ef << 3) | m;
   return r > 0x7Eu ? 0x7Eu : r;
+}
+
+// W4A8 activation code: E4M3 of fl32(v * r8), nearest, ties to even, saturating at 448, with
+// the sign of v kept (r8 = fl32(1 / fl32(6 S)) for the matrix's FP32 input scale S, which is the
+// inv6S the packs hold; the decoded value is E4M3(code) * fl32(6 S)).
+__device__ __forceinline__ uint32_t a8_encode(float v, float r8) {
+  const float t = __fmul_rn(v, r8);
+  return e4m3_encode_rn(fabsf(t)) | ((__float_as_uint(t) >> 24) & 0x80u);
 }
 
 // Quantise 16 FP32 values with per-matrix scale S (inv6S = fl32(1/fl32(6 S))).
@@ -602,8 +610,9 @@ bool tc_supported();
 cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
                               const uint16_t* x, float xS, float x_inv6S);
 // W4A16 grouped experts on tcgen05 kind::f16 (weights dequantised in shared memory).
+// a8 = 1: W4A8 (E4M3 activations with the scale fl32(6 xS), r8 = fl32(1/fl32(6 xS))).
 cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
-                                const uint16_t* x);
+                                const uint16_t* x, int a8, float xS, float x_r8);
 // Whether a wide call runs the tensor-core grouped path (128-slot token tiles) for its mode.
 bool tile_path(int T, int H, int I, int mode);
 // Router logits of a wide call on tcgen05 (BF16 x BF16 -> FP32).

@@ -134,6 +134,7 @@ struct TcParams {
   int MT;                // m tiles per token tile
   int nks;               // stages per tile
   int last_k4;           // K steps (of 64) in the last stage
+  int a8;                // W4A16 kernels: 1 = W4A8 (E4M3 activations and h, per-matrix scales)
 };
 
 // ------------------------------------------------------------------ shared pipeline skeleton
@@ -803,6 +804,8 @@ __global__ void __launch_bounds__(kT16Threads, 1)
         if (et < nval) {
           if (!DOWN) {
             f = ws.xfac[ws.perm[slot0 + et]];
+          } else if (prm.a8) {
+            f = __fmul_rn(6.0f, prm.dscale[e]);   // W4A8: the h codes' scale fl32(6 S_down)
           } else {
             f = __int_as_float((127 + amax_shift(__uint_as_float(ws.slot_amax[slot0 + et]))) << 23);
           }
@@ -825,6 +828,21 @@ __global__ void __launch_bounds__(kT16Threads, 1)
           uint32_t gr[32], ur[32];
           ld32(tb + c0, gr);
           ld32(tb + kTileN + c0, ur);
+          if (prm.a8) {
+            // W4A8: h -> E4M3 with the down matrix's scale (dinv6 = fl32(1/fl32(6 S_down)))
+            const float r8 = prm.dinv6[e];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const int col = c0 + q;
+              const float fx = colfac[col];
+              const float gv = __uint_as_float(gr[q]) * mg * fx;
+              const float uv = __uint_as_float(ur[q]) * mu * fx;
+              if (col < nval)
+                ws.hq[(size_t)(slot0 + col) * I + irow] =
+                    static_cast<uint8_t>(a8_encode((gv / (1.0f + expf(-gv))) * uv, r8));
+            }
+            continue;
+          }
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
             const int col = c0 + q;
@@ -844,7 +862,7 @@ __global__ void __launch_bounds__(kT16Threads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
         t16_epi_sync();
-        if (et < nval) atomicMax(&ws.slot_amax[slot0 + et], colmax[et]);
+        if (!prm.a8 && et < nval) atomicMax(&ws.slot_amax[slot0 + et], colmax[et]);
       } else {
         const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN;
         const float md = prm.mult[e * 3 + 2];
@@ -1094,11 +1112,13 @@ __global__ void __launch_bounds__(kT16Threads, 1)
       const int buf = tcount & 1, use = tcount >> 1;
       const int e = ws.tt_expert[j];
       const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
-      // Y = BF16(acc * md * 2^s of the slot)
+      // Y = BF16(acc * md * 2^s of the slot), or * fl32(6 S_down) in W4A8
       float f = 0.0f;
       if (row < nval)
         f = prm.mult[e * 3 + 2] *
-            __int_as_float((127 + amax_shift(__uint_as_float(ws.slot_amax[slot0 + row]))) << 23);
+            (prm.a8 ? __fmul_rn(6.0f, prm.dscale[e])
+                    : __int_as_float((127 + amax_shift(__uint_as_float(ws.slot_amax[slot0 + row])))
+                                     << 23));
       if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
@@ -1138,7 +1158,8 @@ __global__ void __launch_bounds__(kT16Threads, 1)
 // W4A16 activations by padded slot: 64 threads per token find the token's max |x|, then write
 // f16(x * 2^-s) into each of its k slots' rows and 2^s to xfac (exact; see above).
 __global__ void __launch_bounds__(64 * kXqTok) k_xprep16_perm(const uint16_t* __restrict__ x,
-                                                              WsView ws) {
+                                                              WsView ws, int a8, float xS,
+                                                              float r8) {
   __shared__ int pslot_s[kXqTok][32];
   __shared__ float am_s[kXqTok][2];
   const int H = ws.H, k = ws.k;
@@ -1164,6 +1185,28 @@ __global__ void __launch_bounds__(64 * kXqTok) k_xprep16_perm(const uint16_t* __
   if (lane == 0) am_s[tl][q >> 5] = m;
   __syncthreads();
   if (!live) return;
+  if (a8) {
+    // W4A8: the E4M3 code of every element (published in token order) and its value as the f16
+    // operand (exact); the scale fl32(6 S) goes to xfac
+    if (q == 0) ws.xfac[t] = __fmul_rn(6.0f, xS);
+    for (int g = q; g < H / 8; g += 64) {
+      const uint4 u = reinterpret_cast<const uint4*>(x + (size_t)t * H)[g];
+      const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+      uint32_t cw[2] = {0u, 0u}, o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        cw[i >> 1] |= (a8_encode(bf16_lo(w4[i]), r8) | (a8_encode(bf16_hi(w4[i]), r8) << 8))
+                      << (16 * (i & 1));
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = e4m3x2_to_f16x2(cw[i >> 1] >> (16 * (i & 1)));
+      *reinterpret_cast<uint2*>(ws.xq + (size_t)t * H + (size_t)g * 8) = make_uint2(cw[0], cw[1]);
+      const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int jj = 0; jj < k; ++jj)
+        reinterpret_cast<uint4*>(ws.xh_perm + (size_t)pslot_s[tl][jj] * H)[g] = ov;
+    }
+    return;
+  }
   const int sh = token_shift(fmaxf(am_s[tl][0], am_s[tl][1]));
   const float f = pow2f(-sh);
   if (q == 0) ws.xfac[t] = pow2f(sh);
@@ -1183,7 +1226,7 @@ __global__ void __launch_bounds__(64 * kXqTok) k_xprep16_perm(const uint16_t* __
 }
 
 // h of every slot as the down operand by padded slot: f16(h * 2^-s), s from the slot's max |h|.
-__global__ void __launch_bounds__(256) k_hprep16(WsView ws) {
+__global__ void __launch_bounds__(256) k_hprep16(WsView ws, int a8) {
   const int I = ws.I;
   const int j = blockIdx.x;
   pdl_wait();
@@ -1191,6 +1234,17 @@ __global__ void __launch_bounds__(256) k_hprep16(WsView ws) {
   if (j >= (int)ws.ctl[kCtlTokenTiles]) return;
   const int slot0 = ws.tt_slot0[j], n = ws.tt_n[j];
   const int words = n * (I / 2);
+  if (a8) {
+    // W4A8: the E4M3 h codes' values (exact in f16); the scale is applied by the down GEMM
+    for (int i = threadIdx.x; i < words; i += 256) {
+      const int r = i / (I / 2), wd = i % (I / 2);
+      const uint32_t two = *reinterpret_cast<const uint16_t*>(ws.hq + (size_t)(slot0 + r) * I +
+                                                              2 * wd);
+      reinterpret_cast<uint32_t*>(ws.hf_perm + ((size_t)j * 128 + r) * I)[wd] =
+          e4m3x2_to_f16x2(two);
+    }
+    return;
+  }
   for (int i = threadIdx.x; i < words; i += 256) {
     const int r = i / (I / 2), wd = i % (I / 2);
     const int sh = amax_shift(__uint_as_float(ws.slot_amax[slot0 + r]));
@@ -1250,7 +1304,7 @@ bool tc_supported() { return encode_fn() != nullptr; }
 bool tile_path(int T, int H, int I, int mode) {
   if (T <= kNarrowT || !tc_supported()) return false;
   if (mode == 1) return H % 256 == 0 && I % 64 == 0;
-  if (mode == 0) return H % 128 == 0 && I % 128 == 0;
+  if (mode == 0 || mode == 2) return H % 128 == 0 && I % 128 == 0;   // kind::f16 (W4A16, W4A8)
   return false;
 }
 
@@ -1305,6 +1359,7 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
   pg.MT = I / 64;
   pg.nks = H / tc::kStageK;
   pg.last_k4 = 4;
+  pg.a8 = 0;
   const int grid = lc.num_sms;
   e = launch_kernel(lc, tc::k_tc_gemm<false>, dim3(grid), dim3(tc::kThreads), smem, m_gate, m_up, m_x, pg,
              ws);
@@ -1324,7 +1379,7 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
 namespace moe {
 
 cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const WsView& ws,
-                                const uint16_t* x) {
+                                const uint16_t* x, int a8, float xS, float x_r8) {
   const int H = pk.H, I = pk.I, E = pk.E;
   const uint64_t P = (uint64_t)ws.NT * 128;
   CUtensorMap m_gate, m_up, m_x, m_down, m_h;
@@ -1335,7 +1390,7 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
       !make_map(&m_h, ws.hf_perm, (uint64_t)I * 2, P, 128))
     return cudaErrorInvalidValue;
   cudaError_t e = launch_kernel(lc, tc::k_xprep16_perm, dim3((ws.T + tc::kXqTok - 1) / tc::kXqTok),
-                         dim3(64 * tc::kXqTok), 0, x, ws);
+                         dim3(64 * tc::kXqTok), 0, x, ws, a8, xS, x_r8);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(tc::k_tc16<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            tc::T16<false>::kSmem);
@@ -1354,11 +1409,12 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
   pg.MT = I / 128;
   pg.nks = H / 64;
   pg.last_k4 = 0;
+  pg.a8 = a8;
   const int grid = lc.num_sms;
   e = launch_kernel(lc, tc::k_tc16<false>, dim3(grid), dim3(tc::kT16Threads), tc::T16<false>::kSmem,
              m_gate, m_up, m_x, pg, ws);
   if (e != cudaSuccess) return e;
-  e = launch_kernel(lc, tc::k_hprep16, dim3(ws.NT), dim3(256), 0, ws);
+  e = launch_kernel(lc, tc::k_hprep16, dim3(ws.NT), dim3(256), 0, ws, a8);
   if (e != cudaSuccess) return e;
   tc::TcParams pd = pg;
   pd.sfa = pk.sfa_down;

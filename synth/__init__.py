@@ -76,6 +76,7 @@ WORKLOADS = {
     "decode1": Workload("decode1", 1, 4096, 512, 10, 384, 0, 48, False),
     "verify8": Workload("verify8", 8, 4096, 512, 10, 384, 0, 48, True),
     "verify8_w4a4": Workload("verify8_w4a4", 8, 4096, 512, 10, 384, 1, 48, True),
+    "verify8_w4a8": Workload("verify8_w4a8", 8, 4096, 512, 10, 384, 2, 48, True),
     "prefill8192": Workload("prefill8192", 8192, 4096, 512, 10, 384, 1, 1, True),
 }
 

@@ -73,6 +73,18 @@ def test_forward_wide_grouped_mma_sync_path(T, H, E, k, I, mode):
     pack.close()
 
 
+@pytest.mark.parametrize("T,H,I", [(3, 1152, 128), (40, 512, 192)])
+def test_forward_w4a8_outside_its_paths_is_unsupported(T, H, I):
+    # W4A8 runs on the fused narrow kernel and the tensor-core f16 path; the narrow multi-kernel
+    # path (H % 256 != 0) and the grouped mma.sync path (I % 128 != 0) refuse it
+    x, wr, ex = small_layer(T, H, 16, 2, I, seed=96)
+    pack = pack_from_experts(ex)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward(dev_bf16(x), dev_bf16(wr), pack, 2, 2)
+    assert e.value.code == 2     # MOE_ERR_UNSUPPORTED
+    pack.close()
+
+
 def test_forward_w4a4_unequal_input_scales_is_unsupported():
     T, H, E, k, I = 4, 256, 8, 2, 64
     x, wr, ex = small_layer(T, H, E, k, I, seed=95)

@@ -8,8 +8,8 @@ import oracle
 import synth
 import nvfp4_mixture_experts_bf16_gb300 as moe
 from _gpu_fixtures import (GAMMA_NARROW, GAMMA_WIDE, FullLayer, check_topk, compare_outputs,
-                           dev_bf16, gamma, h_flip_allowance, host_u16, pack_from_experts,
-                           slot_map, small_layer, stable_perm, ws_array)
+                           dev_bf16, gamma, h8_flip_allowance, h_flip_allowance, host_u16,
+                           pack_from_experts, slot_map, small_layer, stable_perm, ws_array)
 
 pytestmark = pytest.mark.gpu
 
@@ -68,6 +68,9 @@ def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None, shared=None
                               ref["xq_codes"])
         assert np.array_equal(ws_array(ws, off["x_scales"], T * H // 16, np.uint8).reshape(T, -1),
                               ref["xq_scales"])
+    if mode == 2:
+        assert np.array_equal(ws_array(ws, off["x_codes"], T * H, np.uint8).reshape(T, H),
+                              ref["xq_codes"])
     gm = slot_map(g_perm, g_offsets)
     rm = slot_map(ref["perm"], ref["offsets"])
     allowance = dict(sh_allow)
@@ -76,9 +79,11 @@ def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None, shared=None
         gh = synth.bf16_to_f32(ws_array(ws, off["h_bf16"], S * I * 2, np.uint16).reshape(S, I))
         rh = synth.bf16_to_f32(ref["h_bf16"])
         gy = synth.bf16_to_f32(ws_array(ws, off["y"], S * H * 2, np.uint16).reshape(S, H))
-    else:
+    elif mode == 1:
         gq = ws_array(ws, off["h_codes"], S * I // 2, np.uint8).reshape(S, I // 2)
         gsf = ws_array(ws, off["h_scales"], S * I // 16, np.uint8).reshape(S, I // 16)
+    else:
+        gq8 = ws_array(ws, off["h_codes"], S * I, np.uint8).reshape(S, I)
     for t in range(T):
         if t in differ:
             continue
@@ -96,7 +101,10 @@ def run_and_check(x, wr, ex, pack, k, mode, nthreads=8, tokens=None, shared=None
                 ya, yb = gy[gs].astype(np.float64), ref["y"][rs]
                 assert np.linalg.norm(ya - yb) <= 2e-3 * np.linalg.norm(yb) + 1e-30, (t, j)
             else:
-                a, f = h_flip_allowance(gq[gs], gsf[gs], ref, rs, I)
+                if mode == 1:
+                    a, f = h_flip_allowance(gq[gs], gsf[gs], ref, rs, I)
+                else:
+                    a, f = h8_flip_allowance(gq8[gs], ref, rs)
                 allowance[t] = allowance.get(t, 0.0) + float(g_w[t, j]) * a
                 flips += f
     toks = [t for t in range(T) if t not in differ] if tokens is None else tokens
@@ -262,13 +270,23 @@ def test_route_ties_go_to_lower_index():
 
 
 # ------------------------------------------------------------------ forward, small shapes
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_forward_tiny_workload(mode):
     wl = synth.WORKLOADS["tiny"]
     x, wr, ex = small_layer(wl.T, wl.H, wl.E, wl.k, wl.I)
     pack = pack_from_experts(ex)
     r = run_and_check(x, wr, ex, pack, wl.k, mode)
-    assert r["worst"] < {0: 2e-3, 1: 5e-3}[mode]
+    assert r["worst"] < {0: 2e-3, 1: 5e-3, 2: 5e-3}[mode]
+    pack.close()
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 8, 9, 50, 203])
+def test_forward_w4a8_ragged_shapes(T):
+    # W4A8 (E4M3 activations): the fused narrow kernel (T <= 8) and the tensor-core f16 path
+    H, E, k, I = 1536, 24, 4, 256
+    x, wr, ex = small_layer(T, H, E, k, I, zipf=True, seed=12)
+    pack = pack_from_experts(ex)
+    run_and_check(x, wr, ex, pack, k, 2)
     pack.close()
 
 
@@ -283,7 +301,7 @@ def test_forward_ragged_shapes(T, mode):
     pack.close()
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("T,H,E,k,I", [
     (1, 768, 640, 8, 128),    # more than 512 experts (32 logits per lane), H % 512 != 0
     (2, 768, 640, 8, 128),
@@ -301,7 +319,7 @@ def test_forward_narrow_call_shapes(T, H, E, k, I, mode):
     pack.close()
 
 
-@pytest.mark.parametrize("mode", [1, 0])
+@pytest.mark.parametrize("mode", [1, 0, 2])
 def test_forward_multi_tile_experts(mode):
     # every expert receives more than 128 slots: several token tiles per expert on the grouped
     # tensor-core path (W4A4), several 8-token groups on the grouped CUDA-core path (W4A16)
@@ -366,7 +384,7 @@ def test_forward_rejects_bad_arguments():
 
 
 # ------------------------------------------------------------------ full-size decode
-@pytest.mark.parametrize("name", ["decode1", "verify8", "verify8_w4a4"])
+@pytest.mark.parametrize("name", ["decode1", "verify8", "verify8_w4a4", "verify8_w4a8"])
 def test_forward_full_size_decode(name):
     wl = synth.WORKLOADS[name]
     lay = FullLayer(0, 0, wl.T, wl.zipf)
@@ -378,7 +396,7 @@ def test_forward_full_size_decode(name):
 
 
 # ------------------------------------------------------------------ full-size prefill, sampled
-@pytest.mark.parametrize("mode,with_shared", [(1, False), (0, False), (1, True)])
+@pytest.mark.parametrize("mode,with_shared", [(1, False), (0, False), (1, True), (2, False)])
 def test_forward_prefill_8192_sampled(mode, with_shared):
     wl = synth.WORKLOADS["prefill8192"]
     lay = FullLayer(0, 0, wl.T, wl.zipf)
@@ -405,6 +423,10 @@ def test_forward_prefill_8192_sampled(mode, with_shared):
         rc, rs = oracle.quantize_nvfp4(synth.bf16_to_f32(lay.x), lay.xs, nthreads=16)
         assert np.array_equal(ws_array(ws, off["x_codes"], T * 2048, np.uint8).reshape(T, -1), rc)
         assert np.array_equal(ws_array(ws, off["x_scales"], T * 256, np.uint8).reshape(T, -1), rs)
+    if mode == 2:
+        rc = oracle.quantize_a8(synth.bf16_to_f32(lay.x), lay.xs)
+        assert np.array_equal(ws_array(ws, off["x_codes"], T * lay.H, np.uint8).reshape(T, -1),
+                              rc)
     rng = np.random.default_rng(0)
     sample = [int(t) for t in rng.choice(T, 24, replace=False) if t not in differ]
     sample += [t for t in (0, T - 1) if t not in differ and t not in sample]
@@ -424,6 +446,16 @@ def test_forward_prefill_8192_sampled(mode, with_shared):
             for j in range(k):
                 e = int(g_idx[t, j])
                 a, _ = h_flip_allowance(gq[gm[(t, e)]], gsf[gm[(t, e)]], ref, rm[(i, e)], lay.I)
+                allowance[i] = allowance.get(i, 0.0) + float(g_w[t, j]) * a
+    if mode == 2:
+        g_perm = ws_array(ws, off["perm"], T * k * 4, np.int32)
+        gm = slot_map(g_perm, o)
+        rm = slot_map(ref["perm"], ref["offsets"])
+        gq8 = ws_array(ws, off["h_codes"], T * k * lay.I, np.uint8).reshape(T * k, -1)
+        for i, t in enumerate(sample):
+            for j in range(k):
+                e = int(g_idx[t, j])
+                a, _ = h8_flip_allowance(gq8[gm[(t, e)]], ref, rm[(i, e)])
                 allowance[i] = allowance.get(i, 0.0) + float(g_w[t, j]) * a
     got = host_u16(out)[sample]
     compare_outputs(got, ref, mode, list(range(len(sample))), allowance)
