@@ -279,6 +279,16 @@ int moe_last_launch_count(void);
  * thread between arming and that call. count = 0 cancels. */
 moe_status moe_profile_next_forward(void* const* events, int count);
 
+/* Test-only fault injection (not needed for computing; process-wide, for failure-detection
+ * tests that must not fault a GPU): skip_logits_cta >= 0 makes that CTA of the fused narrow-call
+ * kernel publish no router logits, so every CTA's wait for them runs out; wait_limit_seconds
+ * > 0 replaces that kernel's ~2 s wait bound (0 restores it; at most 10 s); the next
+ * fail_pack_allocations device allocations of moe_pack_nvfp4 fail (MOE_ERR_OOM). A call whose
+ * wait ran out finishes, records MOE_ERR_TIMEOUT in the workspace status word, and leaves the
+ * workspace to be zeroed again. moe_test_inject_faults(-1, 0, 0) switches everything off. */
+moe_status moe_test_inject_faults(int skip_logits_cta, double wait_limit_seconds,
+                                  int fail_pack_allocations);
+
 /* Name of the kernel of the i-th launch of the last profiled call (cudaFuncGetName; static
  * storage), or NULL. */
 const char* moe_profile_kernel_name(int i);

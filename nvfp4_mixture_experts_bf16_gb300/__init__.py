@@ -29,7 +29,8 @@ EXPORTED = ["moe_pack_nvfp4", "moe_pack_destroy", "moe_pack_info", "moe_pack_get
             "moe_status_string", "moe_last_launch_count", "moe_profile_next_forward",
             "moe_route_topk_noalloc", "moe_workspace_size_shared", "moe_forward_shared",
             "moe_workspace_offsets_shared", "moe_profile_kernel_name",
-            "moe_workspace_size_layers", "moe_workspace_offsets_layers", "moe_forward_layers"]
+            "moe_workspace_size_layers", "moe_workspace_offsets_layers", "moe_forward_layers",
+            "moe_test_inject_faults"]
 
 
 class MoeError(RuntimeError):
@@ -92,6 +93,7 @@ def lib() -> ctypes.CDLL:
             L.moe_last_launch_count.argtypes = []
             L.moe_profile_next_forward.argtypes = [vp, i32]
             L.moe_profile_kernel_name.argtypes = [i32]
+            L.moe_test_inject_faults.argtypes = [i32, ctypes.c_double, i32]
             L.moe_workspace_size_layers.argtypes = [vp, i32, i32, i32, i32, ctypes.POINTER(sz)]
             L.moe_workspace_offsets_layers.argtypes = [vp, i32, i32, i32, i32, i32,
                                                        ctypes.POINTER(_WsOffsets)]
@@ -371,6 +373,13 @@ def moe_profile_next_forward(events) -> None:
     launch."""
     arr = (ctypes.c_void_p * len(events))(*[ev.cuda_event for ev in events])
     _check("moe_profile_next_forward", lib().moe_profile_next_forward(arr, len(events)))
+
+
+def moe_test_inject_faults(skip_logits_cta: int = -1, wait_limit_seconds: float = 0.0,
+                           fail_pack_allocations: int = 0) -> None:
+    """Test-only fault injection (see the header); no arguments switch it off."""
+    _check("moe_test_inject_faults", lib().moe_test_inject_faults(
+        int(skip_logits_cta), float(wait_limit_seconds), int(fail_pack_allocations)))
 
 
 def moe_profile_kernel_name(i: int):

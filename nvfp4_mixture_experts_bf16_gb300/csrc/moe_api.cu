@@ -176,6 +176,17 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   return v;
 }
 
+// Device allocation of moe_pack_nvfp4; fails on request of the test fault injection.
+cudaError_t pack_alloc(void** p, size_t bytes) {
+  moe::FaultInjection& fi = moe::fault_injection();
+  if (fi.fail_pack_allocs > 0) {
+    --fi.fail_pack_allocs;
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(p, bytes);
+}
+
 moe_status from_cuda(cudaError_t e) {
   return e == cudaSuccess ? MOE_OK : (e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA);
 }
@@ -214,6 +225,10 @@ moe::WsView shift_view(moe::WsView v, size_t off) {
 
 namespace moe {
 LaunchProf& launch_prof() { return g_prof; }
+FaultInjection& fault_injection() {
+  static FaultInjection fi = {0, -1, 0};
+  return fi;
+}
 }  // namespace moe
 
 extern "C" {
@@ -238,6 +253,18 @@ moe_status moe_profile_next_forward(void* const* events, int count) {
   for (int i = 0; i < count; ++i) g_prof.ev[i] = static_cast<cudaEvent_t>(events[i]);
   g_prof.count = count;
   g_prof.next = 0;
+  return MOE_OK;
+}
+
+moe_status moe_test_inject_faults(int skip_logits_cta, double wait_limit_seconds,
+                                  int fail_pack_allocations) {
+  if (skip_logits_cta < -1 || !(wait_limit_seconds >= 0.0) || wait_limit_seconds > 10.0 ||
+      fail_pack_allocations < 0)
+    return MOE_ERR_INVALID_ARG;
+  moe::FaultInjection& fi = moe::fault_injection();
+  fi.skip_logits_cta = skip_logits_cta;
+  fi.wait_ns = (uint64_t)(wait_limit_seconds * 1e9);
+  fi.fail_pack_allocs = fail_pack_allocations;
   return MOE_OK;
 }
 
@@ -277,13 +304,13 @@ moe_status moe_pack_nvfp4(const moe_nvfp4_matrix* gate, const moe_nvfp4_matrix* 
   pk->E = E; pk->H = H; pk->I = I;
   cudaGetDevice(&pk->device);
   pk->bytes = o;
-  if (cudaMalloc(&pk->buf, o) != cudaSuccess) {
+  if (pack_alloc(reinterpret_cast<void**>(&pk->buf), o) != cudaSuccess) {
     cudaGetLastError();
     delete pk;
     return MOE_ERR_OOM;
   }
   unsigned char* raw = nullptr;
-  if (cudaMalloc(&raw, 3 * mat_scales * E) != cudaSuccess) {
+  if (pack_alloc(reinterpret_cast<void**>(&raw), 3 * mat_scales * E) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(pk->buf);
     delete pk;
@@ -487,12 +514,18 @@ cudaError_t launch_forward(moe::LaunchCfg lc, const moe_expert_pack* pack,
     v.sh_sigma = sv.sigma;
   }
   if (narrow && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
-    // the whole routed step in one persistent kernel
-    if (e == cudaSuccess)
-      e = moe::launch_decode(lc, pack->view, v, m, pack->x_scale, pack->x_inv6S, x, router_w, out,
-                             nullptr);
-    *n += 1;
-    return e;
+    // the whole routed step in one persistent kernel (unless its CTAs cannot all be resident)
+    if (e == cudaSuccess) {
+      const cudaError_t d = moe::launch_decode(lc, pack->view, v, m, pack->x_scale,
+                                               pack->x_inv6S, x, router_w, out, nullptr);
+      if (d != cudaErrorCooperativeLaunchTooLarge) {
+        *n += 1;
+        return d;
+      }
+      cudaGetLastError();
+    } else {
+      return e;
+    }
   }
   if (narrow) {
     if (e == cudaSuccess)

@@ -52,6 +52,8 @@ struct DcGroup {
 static_assert(sizeof(DcGroup) == 16, "DcGroup layout");
 
 struct DcGeom {
+  uint64_t wait_ns;             // bound of every wait (kWaitLimitNs unless a test shortens it)
+  int skip_logits_cta;          // test fault injection: this CTA publishes no logits (-1: none)
   int rows_max;                 // router rows of one CTA, at most
   int rs;                       // bytes per staged router / activation row: 2H + 16 (padded so
                                 // that 8 rows' fragment loads hit distinct banks)
@@ -180,7 +182,7 @@ __device__ __forceinline__ void warp_select_scratch(uint32_t (&key)[V], int k, i
 template <int V>
 __device__ __forceinline__ bool topk_tagged_v(const unsigned long long* row, int E, int k,
                                               int lane, uint32_t ep, int& e_out, float& w_out,
-                                              unsigned long long* cand) {
+                                              unsigned long long* cand, uint64_t limit_ns) {
   uint32_t key[V];
   uint32_t pending = 0;
   unsigned long long w[V];
@@ -209,7 +211,7 @@ __device__ __forceinline__ bool topk_tagged_v(const unsigned long long* row, int
           }
         }
       }
-      if (__any_sync(0xFFFFFFFFu, globaltimer_ns() - t0 > kWaitLimitNs)) {   // warp-uniform
+      if (__any_sync(0xFFFFFFFFu, globaltimer_ns() - t0 > limit_ns)) {   // warp-uniform
         ok = false;
         break;
       }
@@ -221,16 +223,16 @@ __device__ __forceinline__ bool topk_tagged_v(const unsigned long long* row, int
 
 __device__ __forceinline__ bool topk_tagged(const unsigned long long* row, int E, int k, int lane,
                                             uint32_t ep, int& e_out, float& w_out,
-                                            unsigned long long* cand) {
+                                            unsigned long long* cand, uint64_t limit_ns) {
   // two register widths only: every instantiation is code that each CTA fetches once per launch
-  if (E <= 512) return topk_tagged_v<16>(row, E, k, lane, ep, e_out, w_out, cand);
-  return topk_tagged_v<32>(row, E, k, lane, ep, e_out, w_out, cand);
+  if (E <= 512) return topk_tagged_v<16>(row, E, k, lane, ep, e_out, w_out, cand, limit_ns);
+  return topk_tagged_v<32>(row, E, k, lane, ep, e_out, w_out, cand, limit_ns);
 }
 
 // Polls n tagged words (bounded) until all carry epoch ep. False on timeout.
 template <int n>
 __device__ __forceinline__ bool poll_tags(const unsigned long long* p, uint32_t ep,
-                                          unsigned long long (&out)[n]) {
+                                          unsigned long long (&out)[n], uint64_t limit_ns) {
   bool all = true;
 #pragma unroll
   for (int i = 0; i < n; ++i) {
@@ -247,7 +249,7 @@ __device__ __forceinline__ bool poll_tags(const unsigned long long* p, uint32_t 
       all &= tag_of(out[i]) == ep;
     }
     if (all) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -385,7 +387,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   // this call's epoch: one past the last completed call's (never 0, the zeroed workspace's tag)
   uint32_t ep = __ldcg(&ws.ctl[kCtlEpoch]) + 1u;
   if (ep == 0u) ep = 1u;
-  if ((nrows > 0 && !mbar_wait(rbar, 0)) || !mbar_wait(xbar, 0)) {
+  if ((nrows > 0 && !mbar_wait(rbar, 0, geo.wait_ns)) || !mbar_wait(xbar, 0, geo.wait_ns)) {
     record_status(ws.ctl, kStTimeout);
     abort_s = 1;
   }
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     if (c == 0) amax_part[warp * 8 + g] = am;
   }
   __syncthreads();
-  if (tid < nrows * T) {
+  if (tid < nrows * T && b != geo.skip_logits_cta) {
     const int rl = tid / T, t = tid % T;
     float s = red[rl * 8 + t];
 #pragma unroll
@@ -575,7 +577,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
                                    ((size_t)(b % kLogitReplicas) * T + warp) * E;
     // scratch: 32 words per warp in the GEMV partials buffer (free once the logits are out)
     unsigned long long* cand = reinterpret_cast<unsigned long long*>(red) + warp * 32;
-    const bool ok = topk_tagged(lg, E, k, lane, ep, e_sel, w_sel, cand);   // warp-uniform
+    const bool ok = topk_tagged(lg, E, k, lane, ep, e_sel, w_sel, cand, geo.wait_ns);
     if (!ok && lane == 0) {
       record_status(ws.ctl, kStTimeout);
       abort_s = 1;
@@ -733,14 +735,14 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       for (int kc = 0; kc < geo.nkc; ++kc, ++chunk) {
         if (chunk < npre) continue;   // issued by the selecting warp
         const int s = chunk % geo.gu_stages, n = chunk / geo.gu_stages;
-        if (n > 0 && !mbar_wait(&gempty[s], (n - 1) & 1)) {
+        if (n > 0 && !mbar_wait(&gempty[s], (n - 1) & 1, geo.wait_ns)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
           break;
         }
         // one token: the second task's stage waits for the first to land (its only completed
         // phase)
-        if (npre > 0 && chunk == 1 && geo.nkc == 1 && !mbar_wait(&gfull[0], 0)) {
+        if (npre > 0 && chunk == 1 && geo.nkc == 1 && !mbar_wait(&gfull[0], 0, geo.wait_ns)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
           break;
@@ -750,9 +752,12 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     }
     // the arena becomes the down ring once the consumers have released every gate/up stage
     const int used = chunk < geo.gu_stages ? chunk : geo.gu_stages;
-    for (int i = 0; i < used && !abort_s; ++i) {
+    for (int i = 0; i < used; ++i) {
+      // landed (after a timeout elsewhere the consumers may release a stage they did not read)
+      // and released
       const int c2 = chunk - 1 - i;
-      if (!mbar_wait(&gempty[c2 % geo.gu_stages], (c2 / geo.gu_stages) & 1)) {
+      if (!mbar_wait(&gfull[c2 % geo.gu_stages], (c2 / geo.gu_stages) & 1, geo.wait_ns) ||
+          !mbar_wait(&gempty[c2 % geo.gu_stages], (c2 / geo.gu_stages) & 1, geo.wait_ns)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
       }
@@ -764,7 +769,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       const int gi = q / dn_tiles, ht = q % dn_tiles;
       const int e = grp[gi].expert;
       const int s = dchunk % geo.dn_stages, n = dchunk / geo.dn_stages;
-      if (n > 0 && !mbar_wait(&dempty[s], (n - 1) & 1)) {
+      if (n > 0 && !mbar_wait(&dempty[s], (n - 1) & 1, geo.wait_ns)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
         break;
@@ -781,7 +786,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     const int dused = dchunk < geo.dn_stages ? dchunk : geo.dn_stages;
     for (int i = 0; i < dused; ++i) {
       const int c2 = dchunk - 1 - i;
-      (void)mbar_wait(&dfull[c2 % geo.dn_stages], (c2 / geo.dn_stages) & 1);
+      (void)mbar_wait(&dfull[c2 % geo.dn_stages], (c2 / geo.dn_stages) & 1, geo.wait_ns);
     }
     return;
   }
@@ -808,7 +813,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       float accg2[4] = {0.f, 0.f, 0.f, 0.f}, accu2[4] = {0.f, 0.f, 0.f, 0.f};
       for (int kc = 0; kc < geo.nkc; ++kc, ++chunk) {
         const int s = chunk % geo.gu_stages, nn = chunk / geo.gu_stages;
-        if (!abort_s && !mbar_wait(&gfull[s], nn & 1)) {
+        if (!abort_s && !mbar_wait(&gfull[s], nn & 1, geo.wait_ns)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
         }
@@ -952,7 +957,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
             unsigned long long w[9];
             uint32_t am = 0u;
             if (lane < nent) {
-              if (!poll_tags<9>(ws.htag + ((size_t)slot0 * ntile + lane) * 9, ep, w)) {
+              if (!poll_tags<9>(ws.htag + ((size_t)slot0 * ntile + lane) * 9, ep, w, geo.wait_ns)) {
                 record_status(ws.ctl, kStTimeout);
                 abort_s = 1;
               }
@@ -982,15 +987,15 @@ __global__ void __launch_bounds__(kDcThreads, 1)
           unsigned long long w[9];
           bool ok;
           if (mode == 0) {
-            ok = poll_tags<9>(src, ep, w);
+            ok = poll_tags<9>(src, ep, w, geo.wait_ns);
           } else if (a8) {
             unsigned long long w4[4];
-            ok = poll_tags<4>(src, ep, w4);
+            ok = poll_tags<4>(src, ep, w4, geo.wait_ns);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) w[q4] = w4[q4];
           } else {
             unsigned long long w3[3];
-            ok = poll_tags<3>(src, ep, w3);
+            ok = poll_tags<3>(src, ep, w3, geo.wait_ns);
             w[0] = w3[0];
             w[1] = w3[1];
             w[2] = w3[2];
@@ -1045,7 +1050,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
         cur = gi;
       }
       const int s = dchunk % geo.dn_stages, nn = dchunk / geo.dn_stages;
-      if (!abort_s && !mbar_wait(&dfull[s], nn & 1)) {
+      if (!abort_s && !mbar_wait(&dfull[s], nn & 1, geo.wait_ns)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
       }
@@ -1143,7 +1148,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
                 late &= ~(1u << u);
               }
             }
-            if (late && globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (late && globaltimer_ns() - t0 > geo.wait_ns) {
               record_status(ws.ctl, kStTimeout);
               abort_s = 1;
               break;
@@ -1231,6 +1236,8 @@ __global__ void __launch_bounds__(kDcThreads, 1)
 // memory (the multi-kernel path serves such shapes).
 bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom) {
   DcGeom g{};
+  g.wait_ns = kWaitLimitNs;
+  g.skip_logits_cta = -1;
   if (T < 1 || T > kNarrowT || num_ctas < 1) return false;
   g.rows_max = (E + num_ctas - 1) / num_ctas;
   if (g.rows_max > kDcWarps) return false;
@@ -1283,10 +1290,19 @@ cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView&
   if (a8) mode = 1;   // W4A8 runs the quantised-activation instantiations
   DcGeom geo;
   if (!decode_geom(ws.T, ws.H, ws.E, ws.k, ws.I, lc.num_sms, &geo)) return cudaErrorInvalidValue;
+  const FaultInjection& fi = fault_injection();
+  if (fi.wait_ns) geo.wait_ns = fi.wait_ns;
+  geo.skip_logits_cta = fi.skip_logits_cta;
   auto go = [&](auto kern) -> cudaError_t {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, geo.smem);
     if (e != cudaSuccess) return e;
+    // the CTAs poll each other's results, so every one of them must be resident at once: one
+    // CTA per SM must fit (else the caller takes the multi-kernel path)
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDcThreads, geo.smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     return launch_kernel(lc, kern, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, pk, ws,
                          geo, x, wr, xS, x_inv6S, out, xnext, a8);
   };

@@ -174,15 +174,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase: false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait on an mbarrier phase: false after limit_ns (kWaitLimitNs unless a kernel passes
+// its own).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -626,6 +628,16 @@ cudaError_t launch_unpack_scales(cudaStream_t s, const uint8_t* gu_scales,
 // combine; narrow calls on CUDA-core GEMVs, wide calls on the tcgen05 BF16 GEMM.
 cudaError_t launch_shared(const LaunchCfg& lc, const uint16_t* x, const ShView& sv,
                           const WsView& ws, int* launches);
+
+// Test-only fault injection (host side; see moe_test_inject_faults in the C ABI): the fused
+// narrow-call kernel's wait bound and a CTA that publishes no logits, and device allocations of
+// moe_pack_nvfp4 that fail.
+struct FaultInjection {
+  uint64_t wait_ns;        // 0: the default bound kWaitLimitNs
+  int skip_logits_cta;     // -1: none
+  int fail_pack_allocs;    // the next this many allocations of moe_pack_nvfp4 fail
+};
+FaultInjection& fault_injection();
 
 // Dynamic shared memory the expert kernels need (host side, for validation).
 size_t gateup_smem_bytes(int H, bool x_resident, int T);

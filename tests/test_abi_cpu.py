@@ -88,3 +88,33 @@ def test_workspace_size_grows_with_tokens(L):
     a = moe.moe_route_workspace_size(1, 4096, 512, 10)
     b = moe.moe_route_workspace_size(8192, 4096, 512, 10)
     assert b > a > 0
+
+
+def test_fault_injection_arguments(L):
+    assert L.moe_test_inject_faults(-2, 0.0, 0) == 1          # no such CTA
+    assert L.moe_test_inject_faults(-1, -1.0, 0) == 1         # negative wait bound
+    assert L.moe_test_inject_faults(-1, 11.0, 0) == 1         # above the 10 s cap
+    assert L.moe_test_inject_faults(-1, 0.0, -1) == 1
+    assert L.moe_test_inject_faults(-1, 0.0, 0) == 0          # everything off
+
+
+def test_pack_allocation_failure_returns_oom(L):
+    # an injected failure of moe_pack_nvfp4's device allocation: MOE_ERR_OOM, no pack, and the
+    # following allocation is not affected by the spent injection
+    import numpy as np
+    E, H, I = 2, 128, 64
+    codes = np.zeros(I * H // 2, np.uint8)
+    scales = np.full(I * H // 16, 0x38, np.uint8)
+    arr = (moe._Matrix * E)()
+    for e in range(E):
+        arr[e].codes = codes.ctypes.data
+        arr[e].scales = scales.ctypes.data
+        arr[e].multiplier = 1.0
+        arr[e].input_scale = 1.0
+    out = ctypes.c_void_p(12345)
+    try:
+        assert L.moe_test_inject_faults(-1, 0.0, 1) == 0
+        assert L.moe_pack_nvfp4(arr, arr, arr, E, H, I, None, ctypes.byref(out)) == 3
+        assert out.value is None
+    finally:
+        assert L.moe_test_inject_faults(-1, 0.0, 0) == 0
