@@ -705,8 +705,10 @@ __global__ void k_pack_sf_atoms(const uint8_t* __restrict__ rg, const uint8_t* _
       const int ks = (int)(q % (H / 64)); q /= (H / 64);
       const int mt = (int)(q % (I / 64)); q /= (I / 64);
       const int e = (int)q;
-      const int row = mt * 64 + (r & 63);
-      const uint8_t* src = r < 64 ? rg : ru;
+      // rows of the atom: the 64 gate and 64 up rows of intermediate tile mt interleaved by 16
+      // (atom rows 32q .. 32q+15: gate rows mt*64 + 16q .., 32q+16 .. 32q+31: the up rows)
+      const int row = mt * 64 + (r >> 5) * 16 + (r & 15);
+      const uint8_t* src = (r & 16) ? ru : rg;
       at_gu[o] = src[((size_t)e * I + row) * (H / 16) + ks * 4 + b];
     } else {
       const int ks = (int)(q % (I / 64)); q /= (I / 64);

@@ -125,7 +125,8 @@ struct PackView {
   const float* down_inv6S;     // [E] fl32(1 / fl32(6 * S_down))
   // tensor-core scale-factor atoms (512 B = 128 rows x 4 blocks of 16; byte
   // (r % 32) * 16 + (r / 32) * 4 + b), one per (row tile, K step of 64):
-  //   sfa_gu:   [E][I/64][H/64]: rows 0..63 = gate rows 64*mt.., rows 64..127 = the up rows
+  //   sfa_gu:   [E][I/64][H/64]: the 64 gate and 64 up rows of intermediate tile mt interleaved
+  //             by 16 (rows 32q .. 32q+15: gate rows 64*mt + 16q .., 32q+16 .. +31: the up rows)
   //   sfa_down: [E][H/128][I/64]
   const uint8_t* sfa_gu;
   const uint8_t* sfa_down;

@@ -36,13 +36,22 @@ constexpr int kStageK = 256;                    // FP4 elements per stage = 128 
 constexpr int kTileBytes = kTileM * 128;        // 16 KB: one 128-row x 128-byte SW128 tile
 constexpr int kSfStage = 4 * 512;               // 4 K steps of scale-factor atoms
 constexpr int kStageBytes = 2 * kTileBytes + 2 * kSfStage;   // A, B, SFA, SFB = 36 KB
-constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;                    // two per tensor-memory lane quadrant
 constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue warps
-constexpr int kStageF = kTileN + 4;             // padded row of the epilogue staging (floats)
 constexpr int kYStride = kTileM + 8;            // padded slot column of the down staging (BF16)
-constexpr int kTmemCols = 512;
-constexpr int kSfCol = 256;                     // scale factors after two 128-column accumulators
+constexpr int kTmemCols = 256;
+constexpr int kSfCol = 128;                     // scale factors after the 128-column accumulator
+
+// Shape of the two grouped FP4 GEMMs. A CTA runs one (token tile, weight tile) unit at a time and
+// two CTAs share an SM: each CTA has one thread that issues the tensor-core instructions, and a
+// single issuing thread spends about as long issuing a K step's 8 scale-factor copies and 4 MMAs
+// as the tensor pipe takes to run them, so a second, independent issuer per SM is what keeps the
+// pipe busy. That budget (half of an SM's shared and tensor memory) gives each CTA 3 stages of
+// 36 KB and 256 tensor-memory columns: one 128-column accumulator and two sets of scale factors.
+constexpr int kStages = 3;
+constexpr int kCtasPerSm = 2;
+constexpr int kSmem = kStages * kStageBytes + 1024;
+static_assert(kCtasPerSm * (kSmem + 1024) <= 233472, "shared memory of two CTAs");
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
                             ((uint32_t)(kTileM >> 4) << 24);   // E2M1 x E2M1, UE4M3, 128x128
 
@@ -138,19 +147,21 @@ struct TcParams {
 };
 
 // ------------------------------------------------------------------ shared pipeline skeleton
-// Kernel body shared by gate/up and down: DOWN selects the operands, K and the epilogue.
+// Kernel body shared by gate/up and down: DOWN selects the operands, K and the epilogue. The MMA
+// takes the activation tile as its M side and the weight tile as its N side, so that the
+// accumulator is [slot][weight row]: one epilogue thread holds one slot's row, and for gate/up
+// that row holds the 16 gate and 16 up values of each 16-element block of h side by side (the
+// weight tile interleaves them by 16), so SiLU*up and the quantiser run inside one thread.
 template <bool DOWN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     k_tc_gemm(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
               const __grid_constant__ CUtensorMap tm_b, TcParams prm, WsView ws) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2];
+  __shared__ uint64_t full[kStages], empty[kStages], acc_full, acc_empty;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* smem = smem_raw + pad;
-  // epilogue staging: the gate and up accumulators of a tile, [128 rows][kStageF] floats
-  float* acc_s = reinterpret_cast<float*>(smem + kStages * kStageBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -158,10 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kEpiWarps);
-    }
+    mbar_init(&acc_full, 1);
+    mbar_init(&acc_empty, kEpiWarps);
     fence_mbar_init();
     abort_s = 0;
   }
@@ -201,9 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int k4 = (ks == prm.nks - 1) ? prm.last_k4 : 4;
           mbar_arrive_expect_tx(&full[s], 2 * kTileBytes + 2 * 512 * k4);
           if (!DOWN) {
-            // A = 64 gate rows over 64 up rows of intermediate tile mt
-            tma_2d(st, &tm_a0, ks * 128, e * I + mt * 64, &full[s]);
-            tma_2d(st + kTileBytes / 2, &tm_a1, ks * 128, e * I + mt * 64, &full[s]);
+            // weight tile = the 64 gate and 64 up rows of intermediate tile mt, interleaved by 16
+            // (tile rows 32q .. 32q+15: gate rows mt*64 + 16q .., 32q+16 .. 32q+31: the up rows of
+            // the same indices)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              tma_2d(st + q * 4096, &tm_a0, ks * 128, e * I + mt * 64 + 16 * q, &full[s]);
+              tma_2d(st + q * 4096 + 2048, &tm_a1, ks * 128, e * I + mt * 64 + 16 * q, &full[s]);
+            }
           } else {
             tma_2d(st, &tm_a0, ks * 128, e * H + mt * 128, &full[s]);
           }
@@ -227,13 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int it = 0, tcount = 0;
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
-        const int buf = tcount & 1, use = tcount >> 1;
-        if (use > 0 && !abort_s && !mbar_wait(&acc_empty[buf], (use - 1) & 1)) {
+        // the accumulator of the previous unit has been read by the epilogue
+        if (tcount > 0 && !abort_s && !mbar_wait(&acc_empty, (tcount - 1) & 1)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
         }
         fence_after();
-        const uint32_t dacc = tmem + buf * kTileN;
         for (int ks = 0; ks < prm.nks; ++ks, ++it) {
           const int s = it % kStages, n = it / kStages;
           if (!abort_s && !mbar_wait(&full[s], n & 1)) {
@@ -242,89 +255,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_after();
           unsigned char* st = smem + s * kStageBytes;
-          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + kTileBytes);
-          const uint32_t sfa0 = smem_u32(st + 2 * kTileBytes);
-          const uint32_t sfb0 = smem_u32(st + 2 * kTileBytes + kSfStage);
+          const uint32_t w0 = smem_u32(st), x0 = smem_u32(st + kTileBytes);
+          const uint32_t sfw0 = smem_u32(st + 2 * kTileBytes);
+          const uint32_t sfx0 = smem_u32(st + 2 * kTileBytes + kSfStage);
           const uint32_t sfcol = tmem + kSfCol + (it & 1) * 32;
           const int k4 = (ks == prm.nks - 1) ? prm.last_k4 : 4;
           for (int q = 0; q < k4; ++q) {
-            cp_sf(sfcol + 4 * q, desc_sf(sfa0 + q * 512));
-            cp_sf(sfcol + 16 + 4 * q, desc_sf(sfb0 + q * 512));
+            cp_sf(sfcol + 4 * q, desc_sf(sfx0 + q * 512));
+            cp_sf(sfcol + 16 + 4 * q, desc_sf(sfw0 + q * 512));
           }
           for (int q = 0; q < k4; ++q) {
-            mma_nvf4(dacc, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32), sfcol + 4 * q,
+            mma_nvf4(tmem, desc_sw128(x0 + q * 32), desc_sw128(w0 + q * 32), sfcol + 4 * q,
                      sfcol + 16 + 4 * q, (ks > 0 || q > 0) ? 1u : 0u);
           }
           commit(&empty[s]);
         }
-        commit(&acc_full[buf]);
+        commit(&acc_full);
       }
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..9)
     const int ew = warp - 2;              // epilogue warp 0..7
     const int quad = warp & 3;            // tensor-memory lanes 32*quad .. +31 (hardware rule)
-    const int chalf = ew >> 2;            // column half handled by this warp in the TMEM read
-    const int row = quad * 32 + lane;     // accumulator row of this thread
-    const int etid = ew * 32 + lane;      // 0..255
+    const int chalf = ew >> 2;            // columns 64*chalf .. +63 of the accumulator
+    const int col = quad * 32 + lane;     // accumulator row = slot of the token tile
     int tcount = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tcount) {
       const int j = t / prm.MT, mt = t % prm.MT;
-      const int buf = tcount & 1, use = tcount >> 1;
       // tile metadata (independent loads, issued before the wait)
       const int e = ws.tt_expert[j];
       const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
-      if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
+      if (!abort_s && !mbar_wait(&acc_full, tcount & 1)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
       }
       __syncwarp();
       fence_after();
-      const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN;
-      if (!DOWN) {
-        // accumulators -> shared memory (this warp: its 32 rows x 64 columns)
-        for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
-          uint32_t r[32];
-          ld32(tbase + c0, r);
-          float4* dst = reinterpret_cast<float4*>(acc_s + row * kStageF + c0);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-        }
-      } else {
-        // Y = BF16(acc * md), transposed into shared memory as [slot column][row] so that each
-        // slot's 128 rows leave as contiguous 16-byte stores; lanes (rows) write consecutive
-        // 2-byte words of one column, free of bank conflicts
-        const float md = prm.mult[e * 3 + 2] * prm.dscale[e];
-        uint16_t* yt = reinterpret_cast<uint16_t*>(acc_s);
-        for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 32) {
-          uint32_t r[32];
-          ld32(tbase + c0, r);
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            yt[(c0 + q) * kYStride + row] = f32_to_bf16_rn(__uint_as_float(r[q]) * md);
-        }
-      }
-      // release the accumulator buffer to the MMA warp
+      const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + chalf * 64;
+      uint32_t r0[32], r1[32];
+      ld32(tbase, r0);
+      ld32(tbase + 32, r1);
+      // both halves are in registers: the accumulator goes back to the MMA warp
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
-      epi_sync();
+      if (lane == 0) mbar_arrive(&acc_empty);
+      if (col >= nval) continue;
+      const size_t slot = (size_t)slot0 + col;
       if (!DOWN) {
-        // rows 0..63: gate rows mt*64 + i; rows 64..127: the matching up rows. A task is one
-        // 16-row NVFP4 block of h for one token: SiLU*up and the quantiser, all in one thread.
+        // columns 32q .. 32q+15: gate of the 16 indices mt*64 + 16q ..; 32q+16 .. 32q+31: up.
+        // This thread's 64 columns are blocks q = 2*chalf, 2*chalf + 1 of the tile.
         const float mg = prm.mult[e * 3 + 0] * prm.xS, mu = prm.mult[e * 3 + 1] * prm.xS;
         const float Sd = prm.dscale[e], i6 = prm.dinv6[e];
-        for (int task = etid; task < 4 * kTileN; task += kEpiWarps * 32) {
-          const int col = task % kTileN, blk = task / kTileN;   // consecutive threads: columns
-          if (col >= nval) continue;
+        const size_t pslot = (size_t)j * 128 + col;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
           float h[16];
           float a = 0.0f;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float g = acc_s[(blk * 16 + i) * kStageF + col] * mg;
-            const float u = acc_s[(64 + blk * 16 + i) * kStageF + col] * mu;
+            const float g = __uint_as_float(hb ? r1[i] : r0[i]) * mg;
+            const float u = __uint_as_float(hb ? r1[16 + i] : r0[16 + i]) * mu;
             h[i] = (g / (1.0f + expf(-g))) * u;
             a = fmaxf(a, fabsf(h[i]));
           }
@@ -338,9 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               hi |= e2m1_encode_rn(__fmul_rn(h[8 + i], rr)) << (4 * i);
             }
           }
-          const int ib = mt * 4 + blk;                 // 16-element block index along I
-          const size_t pslot = (size_t)j * 128 + col;
-          const size_t slot = (size_t)slot0 + col;
+          const int ib = mt * 4 + chalf * 2 + hb;   // 16-element block of h along I
           *reinterpret_cast<uint2*>(ws.hq_perm + pslot * (I / 2) + ib * 8) = make_uint2(lo, hi);
           *reinterpret_cast<uint2*>(ws.hq + slot * (I / 2) + ib * 8) = make_uint2(lo, hi);
           ws.hsf_atoms[((size_t)j * (I / 64) + ib / 4) * 512 + sf_atom_byte(col, ib & 3)] =
@@ -348,16 +336,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ws.hsf[slot * (I / 16) + ib] = (uint8_t)sf;
         }
       } else {
-        // Y[slot0 + col][mt*128 .. +127]: 16 chunks of 8 rows per slot, one 16-byte store each
-        const uint16_t* yt = reinterpret_cast<const uint16_t*>(acc_s);
-        for (int id = etid; id < kTileN * (kTileM / 8); id += kEpiWarps * 32) {
-          const int col = id >> 4, r8 = id & 15;
-          if (col < nval)
-            *reinterpret_cast<uint4*>(ws.y + (size_t)(slot0 + col) * H + mt * 128 + r8 * 8) =
-                *reinterpret_cast<const uint4*>(yt + col * kYStride + r8 * 8);
+        // Y[slot][mt*128 + 64*chalf ..] = BF16(acc * md): 64 consecutive BF16 of one row, as
+        // eight 16-byte stores
+        const float md = prm.mult[e * 3 + 2] * prm.dscale[e];
+        uint4* dst = reinterpret_cast<uint4*>(ws.y + slot * H + mt * 128 + chalf * 64);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i0 = (c * 8 + 2 * q) & 31;
+            const uint32_t v0 = (c < 4) ? r0[i0] : r1[i0], v1 = (c < 4) ? r0[i0 + 1] : r1[i0 + 1];
+            w[q] = (uint32_t)f32_to_bf16_rn(__uint_as_float(v0) * md) |
+                   ((uint32_t)f32_to_bf16_rn(__uint_as_float(v1) * md) << 16);
+          }
+          dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      epi_sync();   // the staging buffer is reused by the next tile
     }
   }
   fence_before();
@@ -760,7 +755,8 @@ __global__ void __launch_bounds__(kT16Threads, 1)
           const uint4* src = reinterpret_cast<const uint4*>(raw + mat * 4096 + ct * 32);
           const uint4 c0 = src[0], c1 = src[1];
           // the row's 4 scale bytes (blocks of 16 along this stage's 64 K)
-          const int rr = DOWN ? ct : mat * 64 + (ct & 63);
+          // atom rows: gate and up rows of a 64-index tile interleaved by 16
+          const int rr = DOWN ? ct : ((ct & 63) >> 4) * 32 + mat * 16 + (ct & 15);
           const unsigned char* atom = sf + (DOWN ? 0 : (ct >> 6) * 512);
           const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(atom + (rr & 31) * 16 + (rr >> 5) * 4);
           const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
@@ -1308,9 +1304,7 @@ bool tile_path(int T, int H, int I, int mode) {
   return false;
 }
 
-size_t tc_smem_bytes() {
-  return (size_t)tc::kStages * tc::kStageBytes + (size_t)tc::kTileM * tc::kStageF * 4 + 1024;
-}
+size_t tc_smem_bytes() { return (size_t)tc::kSmem; }
 
 cudaError_t launch_tc_router(const LaunchCfg& lc, const uint16_t* x, const uint16_t* wr,
                              const WsView& ws) {
@@ -1332,8 +1326,8 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
   const int H = pk.H, I = pk.I, E = pk.E;
   const uint64_t P = (uint64_t)ws.NT * 128;
   CUtensorMap m_gate, m_up, m_x, m_down, m_h;
-  if (!make_map(&m_gate, pk.gate_codes, H / 2, (uint64_t)E * I, 64) ||
-      !make_map(&m_up, pk.up_codes, H / 2, (uint64_t)E * I, 64) ||
+  if (!make_map(&m_gate, pk.gate_codes, H / 2, (uint64_t)E * I, 16) ||
+      !make_map(&m_up, pk.up_codes, H / 2, (uint64_t)E * I, 16) ||
       !make_map(&m_x, ws.xq_perm, H / 2, P, 128) ||
       !make_map(&m_down, pk.down_codes, I / 2, (uint64_t)E * H, 128) ||
       !make_map(&m_h, ws.hq_perm, I / 2, P, 128))
@@ -1360,9 +1354,9 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
   pg.nks = H / tc::kStageK;
   pg.last_k4 = 4;
   pg.a8 = 0;
-  const int grid = lc.num_sms;
-  e = launch_kernel(lc, tc::k_tc_gemm<false>, dim3(grid), dim3(tc::kThreads), smem, m_gate, m_up, m_x, pg,
-             ws);
+  const int grid = tc::kCtasPerSm * lc.num_sms;   // persistent: two CTAs per SM
+  e = launch_kernel(lc, tc::k_tc_gemm<false>, dim3(grid), dim3(tc::kThreads), smem, m_gate, m_up,
+                    m_x, pg, ws);
   if (e != cudaSuccess) return e;
   tc::TcParams pd = pg;
   pd.sfa = pk.sfa_down;
@@ -1370,8 +1364,8 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
   pd.MT = H / 128;
   pd.nks = (I + tc::kStageK - 1) / tc::kStageK;
   pd.last_k4 = ((I % tc::kStageK) ? (I % tc::kStageK) : tc::kStageK) / 64;
-  return launch_kernel(lc, tc::k_tc_gemm<true>, dim3(grid), dim3(tc::kThreads), smem, m_down, m_down, m_h,
-                pd, ws);
+  return launch_kernel(lc, tc::k_tc_gemm<true>, dim3(grid), dim3(tc::kThreads), smem, m_down,
+                       m_down, m_h, pd, ws);
 }
 
 }  // namespace moe

@@ -430,11 +430,43 @@ def test_forward_prefill_8192_sampled(mode, with_shared):
     rng = np.random.default_rng(0)
     sample = [int(t) for t in rng.choice(T, 24, replace=False) if t not in differ]
     sample += [t for t in (0, T - 1) if t not in differ and t not in sample]
+    # on purpose: tokens of the two busiest experts (more than 1000 slots, many 128-slot token
+    # tiles each): the first, middle and last slots of each, so the last (ragged) token tile of
+    # a hot expert is always compared
+    g_perm_all = ws_array(ws, off["perm"], T * k * 4, np.int32)
+    for e_hot in np.argsort(-c, kind="stable")[:2]:
+        for s_ in (o[e_hot], (o[e_hot] + o[e_hot + 1]) // 2, o[e_hot + 1] - 1):
+            t = int(g_perm_all[s_])
+            if t not in differ and t not in sample:
+                sample.append(t)
     ex = lay.oracle_experts(ref_route["idx"][sample].ravel(), nthreads=16)
     ref = oracle.forward(lay.x[sample], lay.wr, ex, k, mode, nthreads=16,
                          want=("out_bf16", "out64", "idx", "perm", "offsets", "hq_codes",
-                               "hq_scales", "h_amb_elem", "h_amb_block"),
+                               "hq_scales", "h_amb_elem", "h_amb_block", "y", "h_bf16"),
                          shared=None if shared is None else oracle.SharedExpert(*shared))
+    # every sampled slot's expert output Y (and h in W4A16) against the oracle's
+    gm_all = slot_map(g_perm_all, o)
+    rm_all = slot_map(ref["perm"], ref["offsets"])
+    gy = ws_array(ws, off["y"], T * k * lay.H * 2, np.uint16).reshape(T * k, lay.H)
+    if mode == 0:
+        gh = ws_array(ws, off["h_bf16"], T * k * lay.I * 2, np.uint16).reshape(T * k, lay.I)
+    for i, t in enumerate(sample):
+        for j in range(k):
+            e = int(g_idx[t, j])
+            gs, rs_ = gm_all[(t, e)], rm_all[(i, e)]
+            if mode == 0:
+                a = synth.bf16_to_f32(gh[gs]).astype(np.float64)
+                b = synth.bf16_to_f32(ref["h_bf16"][rs_]).astype(np.float64)
+                scale = np.sqrt(np.mean(b * b)) + 1e-30
+                assert np.all(np.abs(a - b) <= 2.0 ** -7 * np.maximum(np.abs(a), np.abs(b))
+                              + 1e-5 * scale), (t, j)
+                # Y of the slots whose h is the oracle's bit for bit: an accepted one-ulp h
+                # difference moves every element of Y, and its BF16 re-rounding amplifies that
+                # (those slots stay covered by the h check above and the output bound below)
+                if np.array_equal(gh[gs], ref["h_bf16"][rs_]):
+                    ya = synth.bf16_to_f32(gy[gs]).astype(np.float64)
+                    assert np.linalg.norm(ya - ref["y"][rs_]) <= \
+                        2e-3 * np.linalg.norm(ref["y"][rs_]), (t, j)
     allowance = {}
     if mode == 1:
         g_perm = ws_array(ws, off["perm"], T * k * 4, np.int32)
