@@ -82,6 +82,23 @@ __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x,
       : "memory");
 }
 
+// TMA tensor store of a box from shared memory (bulk-group completion), and its group waits.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {   // sources of all groups read
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {        // all groups complete
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void mma_nvf4(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa,
                                          uint32_t sfb, uint32_t accumulate) {
   asm volatile(
@@ -144,6 +161,8 @@ struct TcParams {
   int nks;               // stages per tile
   int last_k4;           // K steps (of 64) in the last stage
   int a8;                // W4A16 kernels: 1 = W4A8 (E4M3 activations and h, per-matrix scales)
+  int nsw;               // k_tc_down: weight-tile stages
+  uint32_t ustride;      // k_tc_down: shared-memory bytes of one operand tile with its scales
 };
 
 // ------------------------------------------------------------------ shared pipeline skeleton
@@ -361,6 +380,250 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
+                 : "memory");
+}
+
+// ------------------------------------------------------------------ down GEMM, resident h
+// Y[slot][row] = BF16(md * h[slot] . Wd[row]) for the W4A4 path when a token tile's h (K = I,
+// up to 768) fits in shared memory twice. Each CTA (one per SM) takes token tiles j = CTA index,
+// + grid, ... and runs the units (j, 128-row tile mt of H) of each for mt = 0 .. H/128 - 1, so the
+// h tile of j and its scale factors (in tensor memory) stay in place while the CTA streams the
+// expert's down-weight tiles; the next token tile's h loads into the other buffer meanwhile. Per
+// unit only the weight tile and its scale factors move: half the copies of a unit that restages
+// both operands. All CTAs sweep mt in the same order at about the same pace, so the CTAs holding
+// token tiles of one expert read each of its weight tiles at about the same time, once from HBM
+// and then from L2. The accumulators are double-buffered (two 128-column buffers), so the
+// epilogue of one unit overlaps the next. Each epilogue warp writes its 32 slots' Y rows into its
+// own 4 KB of shared memory (128-byte swizzled, conflict-free) and stores them with TMA, 32 or 16
+// rows per box; the rows of a ragged tile past its last 16-row box go out as plain stores.
+// Warp 0: TMA producer; warp 1: MMA issuer; warps 2..9: epilogue (as in k_tc_gemm<true>).
+constexpr int kRhMaxStages = 6;
+constexpr int kRhTmemCols = 512;
+constexpr int kRhStaging = kEpiWarps * 32 * 128;   // 32 rows x 128 bytes per epilogue warp
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_tc_down(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
+              const __grid_constant__ CUtensorMap tm_y32, const __grid_constant__ CUtensorMap tm_y16,
+              TcParams prm, WsView ws) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t full[kRhMaxStages], empty[kRhMaxStages], h_full[2], h_empty[2], acc_full[2],
+      acc_empty[2];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ volatile int abort_s;
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* smem = smem_raw + pad;
+  const int nsw = prm.nsw;
+  const uint32_t ustride = prm.ustride;
+  const int nkc = prm.nks;                 // 128-byte K chunks of a row
+  const int natoms = prm.I / 64;           // K steps of 64 = scale-factor atoms per tile
+  const uint32_t ubytes = (uint32_t)nkc * kTileBytes + (uint32_t)natoms * 512;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < nsw; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&h_full[b], 1);
+      mbar_init(&h_empty[b], 1);
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps);
+    }
+    fence_mbar_init();
+    abort_s = 0;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base_s)),
+                 "r"(kRhTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_s;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  const int MT = prm.MT, H = prm.H;
+  const int NT = (int)ws.ctl[kCtlTokenTiles];
+  // tensor memory: accumulators at columns 0 and 128, then the scale factors of the two h
+  // buffers and of the two most recent weight tiles (natoms * 4 columns each)
+  const uint32_t hsf_col = tmem + 256, wsf_col = tmem + 256 + 2 * natoms * 4;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int it = 0, hcount = 0;
+      for (int j = blockIdx.x; j < NT && !abort_s; j += gridDim.x) {
+        const int e = __ldg(&ws.tt_expert[j]);
+        const int hb = hcount & 1, hn = hcount >> 1;
+        if (hn > 0 && !mbar_wait(&h_empty[hb], (hn - 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+          break;
+        }
+        unsigned char* hs = smem + hb * ustride;
+        mbar_arrive_expect_tx(&h_full[hb], ubytes);
+        for (int c = 0; c < nkc; ++c) tma_2d(hs + c * kTileBytes, &tm_h, c * 128, j * 128, &h_full[hb]);
+        bulk_g2s(hs + nkc * kTileBytes, prm.sfb + (size_t)j * natoms * 512, natoms * 512,
+                 &h_full[hb]);
+        ++hcount;
+        for (int mt = 0; mt < MT; ++mt) {
+          const int s = it % nsw, n = it / nsw;
+          if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+            break;
+          }
+          unsigned char* st = smem + 2 * ustride + kRhStaging + s * ustride;
+          mbar_arrive_expect_tx(&full[s], ubytes);
+          for (int c = 0; c < nkc; ++c)
+            tma_2d(st + c * kTileBytes, &tm_w, c * 128, e * H + mt * 128, &full[s]);
+          bulk_g2s(st + nkc * kTileBytes, prm.sfa + ((size_t)e * MT + mt) * natoms * 512,
+                   natoms * 512, &full[s]);
+          ++it;
+        }
+      }
+      // no copy may still be in flight when the CTA exits
+      const int used = it < nsw ? it : nsw;
+      for (int i = 0; i < used; ++i) {
+        const int c = it - 1 - i;
+        (void)mbar_wait(&full[c % nsw], (c / nsw) & 1);
+      }
+      const int hused = hcount < 2 ? hcount : 2;
+      for (int i = 0; i < hused; ++i) {
+        const int c = hcount - 1 - i;
+        (void)mbar_wait(&h_full[c & 1], (c >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int it = 0, hcount = 0, tcount = 0;
+      for (int j = blockIdx.x; j < NT; j += gridDim.x) {
+        // the previous h buffer is free once the MMAs issued so far have completed
+        if (hcount > 0) commit(&h_empty[(hcount - 1) & 1]);
+        const int hb = hcount & 1;
+        if (!abort_s && !mbar_wait(&h_full[hb], (hcount >> 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        fence_after();
+        const uint32_t hsf0 = smem_u32(smem + hb * ustride + nkc * kTileBytes);
+        for (int kb = 0; kb < natoms; ++kb)
+          cp_sf(hsf_col + hb * natoms * 4 + 4 * kb, desc_sf(hsf0 + kb * 512));
+        ++hcount;
+        for (int mt = 0; mt < MT; ++mt, ++tcount) {
+          const int buf = tcount & 1, use = tcount >> 1;
+          if (use > 0 && !abort_s && !mbar_wait(&acc_empty[buf], (use - 1) & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          const int s = it % nsw, n = it / nsw;
+          if (!abort_s && !mbar_wait(&full[s], n & 1)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          fence_after();
+          unsigned char* st = smem + 2 * ustride + kRhStaging + s * ustride;
+          const uint32_t wsf = wsf_col + (tcount & 1) * natoms * 4;
+          const uint32_t wsf0 = smem_u32(st + nkc * kTileBytes);
+          for (int kb = 0; kb < natoms; ++kb) cp_sf(wsf + 4 * kb, desc_sf(wsf0 + kb * 512));
+          const uint32_t h0 = smem_u32(smem + hb * ustride), w0 = smem_u32(st);
+          const uint32_t hsf = hsf_col + hb * natoms * 4;
+          for (int kb = 0; kb < natoms; ++kb) {
+            const uint32_t off = (kb >> 2) * kTileBytes + (kb & 3) * 32;
+            mma_nvf4(tmem + buf * kTileN, desc_sw128(h0 + off), desc_sw128(w0 + off), hsf + 4 * kb,
+                     wsf + 4 * kb, kb > 0 ? 1u : 0u);
+          }
+          commit(&empty[s]);
+          commit(&acc_full[buf]);
+          ++it;
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 2..9)
+    const int ew = warp - 2;
+    const int quad = warp & 3;            // tensor-memory lanes 32*quad .. +31
+    const int chalf = ew >> 2;            // columns 64*chalf .. +63
+    const int col = quad * 32 + lane;     // accumulator row = slot of the token tile
+    unsigned char* stg = smem + 2 * ustride + ew * (32 * 128);   // this warp's Y rows
+    int tcount = 0;
+    for (int j = blockIdx.x; j < NT; j += gridDim.x) {
+      const int e = ws.tt_expert[j];
+      const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
+      for (int mt = 0; mt < MT; ++mt, ++tcount) {
+        const int buf = tcount & 1, use = tcount >> 1;
+        if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        __syncwarp();
+        fence_after();
+        const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN + chalf * 64;
+        uint32_t r0[32], r1[32];
+        ld32(tbase, r0);
+        ld32(tbase + 32, r1);
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        // this warp's slots quad*32 .. +31: nv of them are valid, the first nt go out by TMA
+        const int nv = min(max(nval - quad * 32, 0), 32);
+        const int nt = nv == 32 ? 32 : (nv & ~15);
+        if (nv == 0) continue;
+        if (nt > 0) {
+          if (lane == 0) bulk_wait_read_all();   // the previous unit's store has read the rows
+          __syncwarp();
+        }
+        // Y[slot][mt*128 + 64*chalf ..] = BF16(acc * md): 64 BF16 = 128 bytes of one slot row
+        const float md = prm.mult[e * 3 + 2] * prm.dscale[e];
+        uint4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i0 = (c * 8 + 2 * q) & 31;
+            const uint32_t v0 = (c < 4) ? r0[i0] : r1[i0], v1 = (c < 4) ? r0[i0 + 1] : r1[i0 + 1];
+            w[q] = (uint32_t)f32_to_bf16_rn(__uint_as_float(v0) * md) |
+                   ((uint32_t)f32_to_bf16_rn(__uint_as_float(v1) * md) << 16);
+          }
+          v[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (lane < nt) {
+          // row `lane` of the warp's box; 16-byte chunk c sits at c ^ (row & 7) (128-byte swizzle)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = v[c];
+        } else if (lane < nv) {
+          uint4* dst = reinterpret_cast<uint4*>(ws.y + ((size_t)slot0 + col) * H + mt * 128 +
+                                                chalf * 64);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dst[c] = v[c];
+        }
+        if (nt > 0) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(nt == 32 ? &tm_y32 : &tm_y16, stg, mt * 256 + chalf * 128,
+                         slot0 + quad * 32);
+            bulk_commit();
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();   // the stores have completed before the CTA exits
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kRhTmemCols)
                  : "memory");
 }
 
@@ -1364,6 +1627,22 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
   pd.MT = H / 128;
   pd.nks = (I + tc::kStageK - 1) / tc::kStageK;
   pd.last_k4 = ((I % tc::kStageK) ? (I % tc::kStageK) : tc::kStageK) / 64;
+  // resident-h down GEMM when two h tiles, the Y staging and two weight tiles fit in shared memory
+  pd.ustride = ((uint32_t)pd.nks * tc::kTileBytes + (uint32_t)(I / 64) * 512 + 1023u) & ~1023u;
+  const int budget = 232448 - 2048 - tc::kRhStaging;
+  const int nsw = (budget - 2 * (int)pd.ustride) / (int)pd.ustride;
+  CUtensorMap m_y32, m_y16;
+  if (I <= 1024 && nsw >= 2 &&
+      make_map(&m_y32, ws.y, (uint64_t)H * 2, (uint64_t)ws.T * ws.k, 32) &&
+      make_map(&m_y16, ws.y, (uint64_t)H * 2, (uint64_t)ws.T * ws.k, 16)) {
+    pd.nsw = nsw < tc::kRhMaxStages ? nsw : tc::kRhMaxStages;
+    const size_t smem_rd = (size_t)(2 + pd.nsw) * pd.ustride + tc::kRhStaging + 1024;
+    e = cudaFuncSetAttribute(tc::k_tc_down, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_rd);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(lc, tc::k_tc_down, dim3(lc.num_sms), dim3(tc::kThreads), smem_rd, m_down,
+                         m_h, m_y32, m_y16, pd, ws);
+  }
   return launch_kernel(lc, tc::k_tc_gemm<true>, dim3(grid), dim3(tc::kThreads), smem, m_down,
                        m_down, m_h, pd, ws);
 }

@@ -8,6 +8,8 @@ Branches (each compared with the oracle under the rules of tests/_gpu_fixtures.p
 * the wide W4A16 tensor-core path with the down GEMM's h tile re-staged (k_tc16<true>): H % 256
   != 0, or an h tile too large to stay resident (I = 1536);
 * the wide grouped mma.sync path: W4A4 with H % 256 != 0, W4A16 with I % 128 != 0;
+* the W4A4 down GEMM with the token tile's h resident (several I), and with h restaged per unit
+  (an I whose h tile does not fit twice beside two weight tiles);
 * W4A4 with unequal gate/up input scales, which the library refuses (MOE_ERR_UNSUPPORTED).
 
 Chained layers: layer l's output is layer l+1's input, every layer with its own router and
@@ -70,6 +72,20 @@ def test_forward_wide_grouped_mma_sync_path(T, H, E, k, I, mode):
     x, wr, ex = small_layer(T, H, E, k, I, seed=91 + T, zipf=True)
     pack = pack_from_experts(ex)
     run_and_check(x, wr, ex, pack, k, mode)
+    pack.close()
+
+
+@pytest.mark.parametrize("T,H,E,k,I", [
+    (300, 512, 6, 2, 320),    # h resident: 5 scale-factor atoms, 2 K chunks
+    (200, 256, 4, 2, 512),    # h resident: 8 scale-factor atoms
+    (150, 256, 4, 2, 768),    # two h tiles do not fit beside two weight tiles: h restaged per unit
+])
+def test_forward_w4a4_wide_down_variants(T, H, E, k, I):
+    # the W4A4 down GEMM keeps a token tile's h in shared memory while its CTA runs the expert's
+    # weight tiles, over ranges of units that straddle token tiles; large I restages h instead
+    x, wr, ex = small_layer(T, H, E, k, I, seed=97 + I, zipf=True)
+    pack = pack_from_experts(ex)
+    run_and_check(x, wr, ex, pack, k, 1)
     pack.close()
 
 
