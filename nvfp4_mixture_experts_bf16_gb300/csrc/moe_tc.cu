@@ -793,44 +793,96 @@ __global__ void __launch_bounds__(64 * kXqTok) k_xquant_perm(const uint16_t* __r
   }
   __syncthreads();
   if (t >= ws.T) return;
-  for (int g = q; g < H / 64; g += 64) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + (size_t)g * 64);
-    uint4 u[8];
+  // every lane of a warp runs each round (the shuffles below need all 32), whether or not its
+  // group g lies inside the row
+  for (int gb = 0; gb < H / 64; gb += 64) {
+    const int g = gb + q;
+    const bool act = g < H / 64;
+    uint32_t cw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u}, sfw = 0;
+    if (act) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H + (size_t)g * 64);
+      uint4 u[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) u[i] = src[i];
-    uint32_t cw[8], sfw = 0;
+      for (int i = 0; i < 8; ++i) u[i] = src[i];
 #pragma unroll
-    for (int blk = 0; blk < 4; ++blk) {
-      const uint32_t w8[8] = {u[2 * blk].x, u[2 * blk].y, u[2 * blk].z, u[2 * blk].w,
-                              u[2 * blk + 1].x, u[2 * blk + 1].y, u[2 * blk + 1].z,
-                              u[2 * blk + 1].w};
-      float v[16];
+      for (int blk = 0; blk < 4; ++blk) {
+        const uint32_t w8[8] = {u[2 * blk].x, u[2 * blk].y, u[2 * blk].z, u[2 * blk].w,
+                                u[2 * blk + 1].x, u[2 * blk + 1].y, u[2 * blk + 1].z,
+                                u[2 * blk + 1].w};
+        float v[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[2 * i] = bf16_lo(w8[i]);
-        v[2 * i + 1] = bf16_hi(w8[i]);
+        for (int i = 0; i < 8; ++i) {
+          v[2 * i] = bf16_lo(w8[i]);
+          v[2 * i + 1] = bf16_hi(w8[i]);
+        }
+        uint32_t c2[2];
+        const uint32_t sf = quantize16(v, xS, x_inv6S, c2);
+        cw[2 * blk] = c2[0];
+        cw[2 * blk + 1] = c2[1];
+        sfw |= sf << (8 * blk);
       }
-      uint32_t c2[2];
-      const uint32_t sf = quantize16(v, xS, x_inv6S, c2);
-      cw[2 * blk] = c2[0];
-      cw[2 * blk + 1] = c2[1];
-      sfw |= sf << (8 * blk);
     }
-    const uint4 c_lo = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    const uint4 c_hi = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-    uint4* xd = reinterpret_cast<uint4*>(ws.xq + (size_t)t * (H / 2) + (size_t)g * 32);
-    xd[0] = c_lo;
-    xd[1] = c_hi;
-    *reinterpret_cast<uint32_t*>(ws.xsf + (size_t)t * (H / 16) + (size_t)g * 4) = sfw;
+    // Lane l holds the 32 code bytes of group g; one warp covers 1 KB of the row. Two shuffle
+    // rounds give lane l the 16-byte chunks l and 32 + l of that 1 KB (groups gw + l/2 and
+    // gw + 16 + l/2), so every store below writes up to 512 contiguous bytes per warp.
+    const int lane = threadIdx.x & 31;
+    const int gw = gb + (q & ~31);           // first group of this warp
+    uint32_t ca[4], cb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo_a = __shfl_sync(0xFFFFFFFFu, cw[i], lane >> 1);
+      const uint32_t hi_a = __shfl_sync(0xFFFFFFFFu, cw[4 + i], lane >> 1);
+      const uint32_t lo_b = __shfl_sync(0xFFFFFFFFu, cw[i], 16 + (lane >> 1));
+      const uint32_t hi_b = __shfl_sync(0xFFFFFFFFu, cw[4 + i], 16 + (lane >> 1));
+      ca[i] = (lane & 1) ? hi_a : lo_a;
+      cb[i] = (lane & 1) ? hi_b : lo_b;
+    }
+    const bool okA = gw + (lane >> 1) < H / 64, okB = gw + 16 + (lane >> 1) < H / 64;
+    const uint4 va = make_uint4(ca[0], ca[1], ca[2], ca[3]);
+    const uint4 vb = make_uint4(cb[0], cb[1], cb[2], cb[3]);
+    const size_t wofs = (size_t)gw * 32;     // byte offset of this warp's 1 KB in a row
+    uint4* xd = reinterpret_cast<uint4*>(ws.xq + (size_t)t * (H / 2) + wofs);
+    if (okA) xd[lane] = va;
+    if (okB) xd[32 + lane] = vb;
+    if (act) *reinterpret_cast<uint32_t*>(ws.xsf + (size_t)t * (H / 16) + (size_t)g * 4) = sfw;
     for (int j = 0; j < k; ++j) {
-      const int row = pslot_s[tl][j], tile = row >> 7, r = row & 127;
-      uint4* pd = reinterpret_cast<uint4*>(ws.xq_perm + (size_t)row * (H / 2) + (size_t)g * 32);
-      pd[0] = c_lo;
-      pd[1] = c_hi;
-      *reinterpret_cast<uint32_t*>(ws.xsf_atoms + ((size_t)tile * (H / 64) + g) * 512 +
-                                   sf_atom_byte(r, 0)) = sfw;
+      uint4* pd = reinterpret_cast<uint4*>(ws.xq_perm + (size_t)pslot_s[tl][j] * (H / 2) + wofs);
+      if (okA) pd[lane] = va;
+      if (okB) pd[32 + lane] = vb;
     }
   }
+}
+
+// Scale-factor atoms of the permuted activations, from the token-order scales: warp (token tile
+// j, 4 groups of 64 elements) writes the 512-byte atom of each group with one 16-byte store per
+// lane; lane l's 16 bytes are the 4 scales of rows l, l + 32, l + 64, l + 96 of the tile.
+__global__ void __launch_bounds__(256) k_xsf_atoms(WsView ws) {
+  const int G = ws.H / 64;                     // atoms per tile row (a multiple of 4)
+  const int lane = threadIdx.x & 31;
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_launch_dependents();
+  const int NT = (int)ws.ctl[kCtlTokenTiles];
+  const int j = wid / (G / 4), g0 = (wid % (G / 4)) * 4;
+  if (j >= NT) return;
+  const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
+  int tok[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = lane + 32 * i;
+    tok[i] = r < nval ? ws.perm[slot0 + r] : -1;
+  }
+  // the 4 groups' scale words of a row are 16 contiguous bytes of the token-order scales
+  uint4 sv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    sv[i] = tok[i] >= 0 ? *reinterpret_cast<const uint4*>(ws.xsf + (size_t)tok[i] * (G * 4) + g0 * 4)
+                        : make_uint4(0u, 0u, 0u, 0u);
+  unsigned char* dst = ws.xsf_atoms + ((size_t)j * G + g0) * 512 + lane * 16;
+  *reinterpret_cast<uint4*>(dst) = make_uint4(sv[0].x, sv[1].x, sv[2].x, sv[3].x);
+  *reinterpret_cast<uint4*>(dst + 512) = make_uint4(sv[0].y, sv[1].y, sv[2].y, sv[3].y);
+  *reinterpret_cast<uint4*>(dst + 1024) = make_uint4(sv[0].z, sv[1].z, sv[2].z, sv[3].z);
+  *reinterpret_cast<uint4*>(dst + 1536) = make_uint4(sv[0].w, sv[1].w, sv[2].w, sv[3].w);
 }
 
 // ------------------------------------------------------------------ W4A16 grouped experts
@@ -1597,6 +1649,10 @@ cudaError_t launch_tc_experts(const LaunchCfg& lc, const PackView& pk, const WsV
     return cudaErrorInvalidValue;
   cudaError_t e = launch_kernel(lc, tc::k_xquant_perm, dim3((ws.T + tc::kXqTok - 1) / tc::kXqTok),
                          dim3(64 * tc::kXqTok), 0, x, ws, xS, x_inv6S);
+  if (e != cudaSuccess) return e;
+  // one warp per (token tile, 16 atoms); the token-tile count is an upper bound read on the device
+  const int xsf_warps = ws.NT * (H / 64 / 4);
+  e = launch_kernel(lc, tc::k_xsf_atoms, dim3((xsf_warps + 7) / 8), dim3(256), 0, ws);
   if (e != cudaSuccess) return e;
   const size_t smem = tc_smem_bytes();
   e = cudaFuncSetAttribute(tc::k_tc_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
