@@ -574,8 +574,8 @@ def prefill_roofline(w3, ms3, kernels, U, pk, shared):
     dom_name, dom_ms = max(kernels, key=lambda kv: kv[1]) if kernels else ("?", 0.0)
     dom_flops = (gu_flops if ("<0>" in dom_name or "<false>" in dom_name) and
                  ("k_tc_gemm" in dom_name or "k_tc16" in dom_name) and "dn" not in dom_name
-                 else dn_flops if ("k_tc_gemm<1>" in dom_name or "k_tc16_dn" in dom_name or
-                                   "k_tc16<1>" in dom_name) else None)
+                 else dn_flops if ("k_tc_gemm<1>" in dom_name or "k_tc_down" in dom_name or
+                                   "k_tc16_dn" in dom_name or "k_tc16<1>" in dom_name) else None)
     achieved = flops / (ms3 * 1e-3) / 1e12
     r = dict(bound="hbm" if floor / (pk["hbm"] * 1e9) > flops / (peak * 1e12) else "tensor",
              achieved=round(achieved, 1), peak=round(peak, 1), unit="TFLOP/s",
@@ -667,7 +667,9 @@ def run_native(args, rank, world, local_rank):
         kern = launch_times(wl, stack, reps=3, device=device)
         dom, dom_ms = max(kern, key=lambda kv: kv[1])
         tot = sum(t for _, t in kern)
-        b = gu_bytes if "gateup" in dom else (dn_bytes if "down" in dom else gu_bytes + dn_bytes)
+        is_gu = "gateup" in dom or (("<0>" in dom or "<false>" in dom) and "k_tc" in dom)
+        is_dn = "down" in dom or "_dn" in dom or "k_tc_gemm<1>" in dom or "k_tc16<1>" in dom
+        b = gu_bytes if is_gu else (dn_bytes if is_dn else gu_bytes + dn_bytes)
         kgbs = b / (dom_ms * 1e-3) / 1e9
         roofline = dict(bound="hbm", kernel=dom, achieved=round(kgbs, 1), peak=pk["hbm"],
                         unit="GB/s", frac=round(kgbs / pk["hbm"], 4),
