@@ -33,6 +33,7 @@
 //      BF16). A layer of a chained stack (moe_forward_layers) also writes the residual sum
 //      BF16(x + out), the next layer's input.
 #include "moe_internal.cuh"
+#include <type_traits>
 
 namespace moe {
 namespace {
@@ -87,6 +88,12 @@ __device__ __forceinline__ unsigned long long ld_tag(const unsigned long long* p
 }
 __device__ __forceinline__ uint32_t tag_of(unsigned long long v) { return (uint32_t)(v >> 32); }
 __device__ __forceinline__ uint32_t data_of(unsigned long long v) { return (uint32_t)v; }
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t* ctr) {
   uint32_t old;
@@ -526,6 +533,43 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     xfac_s[t] = mode == 0 ? pow2f(shift_s[t]) : (a8 ? __fmul_rn(6.0f, xS) : xS);
   }
   __syncthreads();
+  if (warp == kDcWarps) {
+    if (mode != 0) {
+      // W4A4 / W4A8: this CTA's share of the quantised activations (16-element blocks b,
+      // b + G, ...), written plain while the consumer warps wait for the logits. Every CTA's
+      // operand build (2b) decodes all T tokens from them instead of quantising them itself.
+      const int nb = H / 16;
+      for (int blk = b + G * lane; blk < T * nb; blk += G * 32) {
+        const int t = blk / nb, bb = blk % nb;
+        const uint4* src = reinterpret_cast<const uint4*>(xraw + (size_t)t * geo.rs + bb * 32);
+        const uint4 u0 = src[0], u1 = src[1];
+        const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[2 * i] = bf16_lo(words[i]);
+          v[2 * i + 1] = bf16_hi(words[i]);
+        }
+        if (a8) {
+          uint32_t cw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int i = 0; i < 16; ++i) cw[i >> 2] |= a8_encode(v[i], x_inv6S) << (8 * (i & 3));
+          *reinterpret_cast<uint4*>(ws.xq + (size_t)t * H + bb * 16) =
+              make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        } else {
+          uint32_t codes[2];
+          const uint32_t sf = quantize16(v, xS, x_inv6S, codes);
+          *reinterpret_cast<uint2*>(ws.xq + (size_t)t * (H / 2) + bb * 8) =
+              make_uint2(codes[0], codes[1]);
+          ws.xsf[(size_t)t * (H / 16) + bb] = static_cast<uint8_t>(sf);
+        }
+      }
+    }
+    // every launch counts its CTAs here (all modes), so the counter stays at (epoch - 1) * G
+    // at the start of a call on this workspace; the release orders the warp's share before it
+    __syncwarp();
+    if (lane == 0) (void)ticket_acq_rel(&ws.ctl[kCtlXShare]);
+  }
 
   // ---------------- 2a. top-k + softmax of every token (warp t), from the tagged logits. With
   // T <= 2 the selection runs while the other warps build the activation operand (below);
@@ -614,62 +658,111 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       sel_w[warp * k + lane] = w_sel;
     }
   };
-  if (kEarlyTopk && warp < T) select_token();
+  // the quantised modes select before building the operand: the operand's codes come from the
+  // other CTAs' tagged words, published while the logits are exchanged, and the selection's
+  // time lets them land before anyone polls (every thread polling early floods L2 with spinning
+  // loads and delays the very stores it waits for)
+  constexpr bool kSelectFirst = kEarlyTopk || MODE != 0;
+  if (kSelectFirst && warp < T) select_token();
 
   // ---------------- 2b. activation operand of every token, in this CTA's shared memory
   {
     const int nb = H / 16;
     const int t0 = kEarlyTopk ? 32 * T : 0;
-    for (int blk = tid - t0; blk < T * nb; blk += kDcThreads - t0) {
-      if (blk < 0) break;
-      const int t = blk / nb, bb = blk % nb;
-      const uint4* src = reinterpret_cast<const uint4*>(xraw + (size_t)t * geo.rs + bb * 32);
-      const uint4 u0 = src[0], u1 = src[1];
-      const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-      float v[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[2 * i] = bf16_lo(words[i]);
-        v[2 * i + 1] = bf16_hi(words[i]);
-      }
-      __half hv[16];
-      if (mode == 0) {
-        const float f = pow2f(-shift_s[t]);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) hv[i] = __float2half_rn(__fmul_rn(v[i], f));
-      } else if (a8) {
-        // W4A8: one E4M3 code per element; the f16 operand is the code's value (exact)
-        uint32_t cw[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) cw[i >> 2] |= a8_encode(v[i], x_inv6S) << (8 * (i & 3));
-        if (blk % G == b)   // this CTA's share of the published W4A8 activation codes
-          *reinterpret_cast<uint4*>(ws.xq + (size_t)t * H + bb * 16) =
-              make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        uint32_t* hw = reinterpret_cast<uint32_t*>(hv);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) hw[i] = e4m3x2_to_f16x2(cw[i >> 1] >> (16 * (i & 1)));
-      } else {
-        uint32_t codes[2];
-        const uint32_t sf = quantize16(v, xS, x_inv6S, codes);
-        if (blk % G == b) {   // this CTA's share of the published W4A4 activation codes
-          *reinterpret_cast<uint2*>(ws.xq + (size_t)t * (H / 2) + bb * 8) =
-              make_uint2(codes[0], codes[1]);
-          ws.xsf[(size_t)t * (H / 16) + bb] = static_cast<uint8_t>(sf);
-        }
-        const float sfv = e4m3_value_nonneg(sf);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          hv[i] = __float2half_rn(e2m1_value((codes[i >> 3] >> (4 * (i & 7))) & 0xF) * sfv);
-      }
-      // element 128J + 32c + 8p + q of the row is stored at 128J + 32p + 8c + q
+    const int stride = kDcThreads - t0;
+    // element 128J + 32c + 8p + q of a row is stored at 128J + 32p + 8c + q
+    auto store_op = [&](int t, int bb, const uint32_t (&hw)[8]) {
       const int J = bb >> 3, c = (bb & 7) >> 1, p0 = 2 * (bb & 1);
       unsigned char* row = xop + (size_t)t * geo.x_stride + (size_t)(J * 128 + 8 * c) * 2;
-      *reinterpret_cast<uint4*>(row + 64 * p0) = *reinterpret_cast<uint4*>(&hv[0]);
-      *reinterpret_cast<uint4*>(row + 64 * (p0 + 1)) = *reinterpret_cast<uint4*>(&hv[8]);
+      *reinterpret_cast<uint4*>(row + 64 * p0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(row + 64 * (p0 + 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    };
+    if (mode == 0) {
+      for (int blk = tid - t0; blk < T * nb; blk += stride) {
+        if (blk < 0) break;
+        const int t = blk / nb, bb = blk % nb;
+        const uint4* src = reinterpret_cast<const uint4*>(xraw + (size_t)t * geo.rs + bb * 32);
+        const uint4 u0 = src[0], u1 = src[1];
+        const uint32_t words[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        const float f = pow2f(-shift_s[t]);
+        uint32_t hw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const __half2 h2 = __halves2half2(__float2half_rn(__fmul_rn(bf16_lo(words[i]), f)),
+                                            __float2half_rn(__fmul_rn(bf16_hi(words[i]), f)));
+          hw[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        store_op(t, bb, hw);
+      }
+    } else {
+      // W4A4 / W4A8: the codes every CTA published (its share above), read once all G CTAs
+      // have counted theirs for this call; four consecutive blocks (one token) per item, all
+      // of a thread's loads issued before any is used. The f16 operand is the code's value:
+      // E2M1 x E4M3 scale has at most 6 significant bits and lies between 2^-10 and 2688 in
+      // magnitude (exact in f16); E4M3 codes are exact in f16.
+      if (tid == 0) {
+        const uint32_t target = ep * (uint32_t)G;
+        const uint64_t tw0 = globaltimer_ns();
+        while ((int32_t)(ld_acquire_u32(&ws.ctl[kCtlXShare]) - target) < 0) {
+          if (globaltimer_ns() - tw0 > geo.wait_ns) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+            break;
+          }
+        }
+      }
+      __syncthreads();
+      const int nitems = T * nb / 4;
+      constexpr int kIt = 2;   // items per thread per round
+      for (int base = tid; base < nitems; base += kIt * kDcThreads) {
+        uint4 cv[kIt][4];
+        uint32_t sfw[kIt];
+#pragma unroll
+        for (int u = 0; u < kIt; ++u) {
+          const int it = base + u * kDcThreads;
+          if (it >= nitems) break;
+          const int t = it / (nb / 4), bb = (it % (nb / 4)) * 4;
+          if (a8) {
+            const uint4* c = reinterpret_cast<const uint4*>(ws.xq + (size_t)t * H + bb * 16);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cv[u][i] = __ldcg(c + i);
+          } else {
+            const uint4* c = reinterpret_cast<const uint4*>(ws.xq + (size_t)t * (H / 2) + bb * 8);
+            cv[u][0] = __ldcg(c);
+            cv[u][1] = __ldcg(c + 1);
+            sfw[u] = __ldcg(reinterpret_cast<const uint32_t*>(ws.xsf + (size_t)t * (H / 16) + bb));
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kIt; ++u) {
+          const int it = base + u * kDcThreads;
+          if (it >= nitems) break;
+          const int t = it / (nb / 4), bb = (it % (nb / 4)) * 4;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {   // block bb + q
+            uint32_t hw[8];
+            if (a8) {
+              const uint32_t w4[4] = {cv[u][q].x, cv[u][q].y, cv[u][q].z, cv[u][q].w};
+#pragma unroll
+              for (int i = 0; i < 8; ++i) hw[i] = e4m3x2_to_f16x2(w4[i >> 1] >> (16 * (i & 1)));
+            } else {
+              const uint4 cc = cv[u][q >> 1];
+              const uint32_t lo = (q & 1) ? cc.z : cc.x, hi = (q & 1) ? cc.w : cc.y;
+              const uint32_t s2 = e4m3x2_to_f16x2((sfw[u] >> (8 * q)) & 0xFFu);
+              uint32_t f[8];
+              e2m1x8_to_f16x2x4(lo, *reinterpret_cast<uint32_t(*)[4]>(&f[0]));
+              e2m1x8_to_f16x2x4(hi, *reinterpret_cast<uint32_t(*)[4]>(&f[4]));
+#pragma unroll
+              for (int i = 0; i < 8; ++i) hw[i] = hmul2_lo(f[i], s2);
+            }
+            store_op(t, bb + q, hw);
+          }
+        }
+      }
     }
   }
   __syncthreads();
-  if (!kEarlyTopk && warp < T) select_token();
+  if (!kSelectFirst && warp < T) select_token();
 
   // ---------------- 2c. groups, in every CTA: a stable sort of the S = T*k selections by
   // expert (entry s = t*k + j goes to slot #{s' : e_s' < e_s} + #{s' < s : e_s' == e_s}) and one

@@ -34,6 +34,8 @@ enum : int {
   kCtlTokenTiles = 4,   // number of 128-slot token tiles (grouped tensor-core path)
   kCtlEpoch = 8,        // fused narrow kernel: epoch of the last completed call (tags its data)
   kCtlDone = 9,         //   CTAs finished, over all calls (the last of a call advances the epoch)
+  kCtlXShare = 10,      //   CTAs that published their share of the quantised activations, over
+                        //   all calls ((epoch - 1) * CTAs at the start of a call)
   kCtlWords = 64
 };
 
