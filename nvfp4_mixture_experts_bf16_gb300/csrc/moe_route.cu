@@ -453,26 +453,46 @@ __global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, PackView pkv, int
   const PackView* pk = has_pack ? &pkv : nullptr;
   __shared__ int32_t tot[1024 + 1];
   __shared__ int32_t wsum[32];
+  __shared__ int32_t gsum[32][33];
+  __shared__ int last_s;
   const int E = ws.E;
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();
   pdl_launch_dependents();
-  int run = 0;
-  if (e < E) {
-    // in place: chunk counts -> chunk prefixes of expert e, 16 loads in flight per round
-    int32_t* col = ws.chunk_base + e;
-    for (int c0 = 0; c0 < nchunk; c0 += 16) {
-      int v[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) v[u] = c0 + u < nchunk ? col[(size_t)(c0 + u) * E] : 0;
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        if (c0 + u < nchunk) col[(size_t)(c0 + u) * E] = run;
-        run += v[u];
+  {
+    // this block's 32 experts (lane) x 32 groups of consecutive chunks (warp): the chunk counts
+    // of each expert become its chunk prefixes in place (loads of a warp: 32 consecutive
+    // experts of one chunk, 128 contiguous bytes)
+    const int ec = blockIdx.x * 32 + lane;
+    const int cpg = (nchunk + 31) / 32;
+    const int c0 = warp * cpg, c1 = min(c0 + cpg, nchunk);
+    int32_t* col = ws.chunk_base + ec;
+    int mine = 0;
+    if (ec < E)
+      for (int c = c0; c < c1; ++c) mine += col[(size_t)c * E];
+    gsum[warp][lane] = mine;
+    __syncthreads();
+    int run = 0;
+    for (int w = 0; w < warp; ++w) run += gsum[w][lane];
+    if (ec < E) {
+      for (int c = c0; c < c1; ++c) {
+        const int v = col[(size_t)c * E];
+        col[(size_t)c * E] = run;
+        run += v;
       }
+      if (warp == 31) ws.counts[ec] = run;   // the expert's total
     }
   }
-  const int cnt_e = e < E ? run : 0;
+  // the last block to finish forms the offsets, groups and token tiles of every expert
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0)
+    last_s = atomicAdd(&ws.ctl[kCtlRouteTicket], 1u) == gridDim.x - 1 ? 1 : 0;
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  const int e = threadIdx.x;
+  const int cnt_e = e < E ? __ldcg(&ws.counts[e]) : 0;
   const int ng_e = (cnt_e + kGroup - 1) / kGroup;
   const int nt_e = (cnt_e + 127) / 128;
   // three block-wide exclusive scans: slots, token groups, 128-slot token tiles
@@ -528,6 +548,7 @@ __global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, PackView pkv, int
     out.offsets[E] = ta;
     ws.offsets[E] = ta;
     ws.ctl[kCtlGroups] = tb;
+    ws.ctl[kCtlRouteTicket] = 0u;
   }
 }
 
@@ -667,7 +688,8 @@ cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint
   const int nchunk = (ws.T + kChunkTok - 1) / kChunkTok;
   e = launch_kernel(lc, k_hist_wide, dim3(nchunk), dim3(256), (size_t)ws.E * 4, ws);
   if (e != cudaSuccess) return e;
-  e = launch_kernel(lc, k_scan_wide, dim3(1), dim3(1024), 0, ws, pkv, pk ? 1 : 0, out, nchunk);
+  e = launch_kernel(lc, k_scan_wide, dim3((ws.E + 31) / 32), dim3(1024), 0, ws, pkv, pk ? 1 : 0,
+                    out, nchunk);
   if (e != cudaSuccess) return e;
   e = launch_kernel(lc, k_scatter_wide, dim3(nchunk), dim3(256), (size_t)kChunkTok * ws.k * 4, ws, out);
   if (launches) *launches += 5;

@@ -631,7 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // logits[T][E] = x[T][H] . Wr[E][H]^T on tcgen05.mma kind::f16 (BF16 x BF16 -> FP32 in tensor
 // memory): A = 128 router rows, B = 128 tokens, K = 64 per stage (one 128-byte swizzle atom),
 // four K = 16 instructions per stage. Warp 0: TMA producer; warp 1: MMA; warps 2..5: epilogue.
-constexpr int kRStages = 4;
+// Two CTAs per SM (3 stages of 32 KB and 256 tensor-memory columns each): one thread issues a
+// CTA's 256 MMAs per tile, and a second CTA per SM is a second issuer.
+constexpr int kRStages = 3;
 constexpr int kRThreads = 192;
 constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) |
                                 ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
@@ -644,7 +646,7 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uin
       : "memory");
 }
 
-__global__ void __launch_bounds__(kRThreads, 1)
+__global__ void __launch_bounds__(kRThreads, 2)
     k_tc_router(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                 WsView ws) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1632,7 +1634,7 @@ cudaError_t launch_tc_router(const LaunchCfg& lc, const uint16_t* x, const uint1
                                        (int)smem);
   if (e != cudaSuccess) return e;
   const int tiles = ((ws.E + 127) / 128) * ((ws.T + 127) / 128);
-  const int grid = tiles < lc.num_sms ? tiles : lc.num_sms;
+  const int grid = tiles < 2 * lc.num_sms ? tiles : 2 * lc.num_sms;
   return launch_kernel(lc, tc::k_tc_router, dim3(grid), dim3(tc::kRThreads), smem, m_w, m_x, ws);
 }
 
