@@ -51,7 +51,7 @@ def parse_args():
     p.add_argument("--experts", type=int, default=None,
                    help="experts per layer (smaller packs for profiler captures)")
     p.add_argument("--seed", type=int, default=0)
-    p.add_argument("--mode", default=None, choices=["w4a16", "w4a4"],
+    p.add_argument("--mode", default=None, choices=["w4a16", "w4a4", "w4a8"],
                    help="override the workload's activation mode (profiling)")
     p.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -605,7 +605,7 @@ def run_native(args, rank, world, local_rank):
     torch.cuda.set_device(device)
     wl = synth.WORKLOADS[args.workload]
     if args.experts or args.tokens or args.mode:
-        mode = wl.mode if args.mode is None else int(args.mode == "w4a4")
+        mode = wl.mode if args.mode is None else {"w4a16": 0, "w4a4": 1, "w4a8": 2}[args.mode]
         wl = synth.Workload(wl.name, args.tokens or wl.T, wl.H, args.experts or wl.E, wl.k, wl.I,
                             mode, wl.layers, wl.zipf)
     layers = args.layers or wl.layers

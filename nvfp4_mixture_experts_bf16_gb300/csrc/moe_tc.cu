@@ -894,13 +894,28 @@ __global__ void __launch_bounds__(256) k_xsf_atoms(WsView ws) {
 //     dequantised in shared memory by converter warps from the TMA-staged FP4 codes;
 //   B (activations): x * 2^-s per token (gate/up) and BF16 h * 2^-s per slot (down), with s
 //     putting the row's max |value| in [2^14, 2^15) (exact, as in the narrow-call path);
-// the epilogues restore 2^s. Tiles: 128 weight rows x 128 padded slots, K = 64 per stage.
-// Gate/up issues two MMAs per K step (the 128 gate rows and the 128 up rows of the same
-// intermediate indices) into two accumulators, so one epilogue lane holds both g and u.
+// the epilogues restore 2^s. K = 64 per stage. Gate/up: one 128 x 256 MMA per K = 16 step, the
+// 128 slots of a token tile as M and the 128 gate and 128 up rows of an intermediate tile as N,
+// interleaved by 16 (rows 32b .. 32b+15 gate, +16 .. +31 up), so that one epilogue thread holds
+// a slot's gate and up values of a 16-element block of h side by side. Down: 128 weight rows x
+// 128 slots (or the resident-h kernel k_tc16_dn below).
 constexpr int kT16Stages = 3;
 constexpr int kT16Threads = 10 * 32;   // producer, MMA, 4 converter warps, 4 epilogue warps
 constexpr uint32_t kIdescF16 = (1u << 4) | ((uint32_t)(kTileN >> 3) << 17) |
                                ((uint32_t)(kTileM >> 4) << 24);   // f16 x f16 -> f32, 128x128
+
+// f16 x f16 -> f32, 128 x 256 (gate/up: 128 slots x 256 weight rows)
+constexpr uint32_t kIdescF16N256 = (1u << 4) | ((uint32_t)(256 >> 3) << 17) |
+                                   ((uint32_t)(kTileM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16_n256(uint32_t d, uint64_t a, uint64_t b,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(kIdescF16N256), "r"(accumulate)
+      : "memory");
+}
 
 __device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
   asm volatile(
@@ -1043,9 +1058,10 @@ __global__ void __launch_bounds__(kT16Threads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t acc = (ks > 0 || q > 0) ? 1u : 0u;
-            mma_f16(d0, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32), acc);
-            if (!DOWN)
-              mma_f16(d0 + kTileN, desc_sw128(a0 + 16384 + q * 32), desc_sw128(b0 + q * 32), acc);
+            if (DOWN)
+              mma_f16(d0, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32), acc);
+            else   // M = the 128 slots, N = the 256 gate/up weight rows
+              mma_f16_n256(d0, desc_sw128(b0 + q * 32), desc_sw128(a0 + q * 32), acc);
           }
           commit(&empty[s]);
         }
@@ -1077,7 +1093,10 @@ __global__ void __launch_bounds__(kT16Threads, 1)
           const unsigned char* atom = sf + (DOWN ? 0 : (ct >> 6) * 512);
           const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(atom + (rr & 31) * 16 + (rr >> 5) * 4);
           const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          unsigned char* row = st + mat * 16384 + (ct >> 3) * 1024 + (ct & 7) * 128;
+          // gate/up: row ct of matrix mat is row rb of the 256-row weight tile, the gate and up
+          // rows of each 16-index block side by side (rows 32b .. 32b+15 gate, +16 .. +31 up)
+          const int rb = DOWN ? ct : ((ct >> 4) * 32 + mat * 16 + (ct & 15));
+          unsigned char* row = st + (rb >> 3) * 1024 + (rb & 7) * 128;
           const uint32_t s01 = e4m3x2_to_f16x2(sc4), s23 = e4m3x2_to_f16x2(sc4 >> 16);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {   // chunk c: elements 8c .. 8c+7 = code word c
@@ -1134,48 +1153,56 @@ __global__ void __launch_bounds__(kT16Threads, 1)
       __syncwarp();
       fence_after();
       if (!DOWN) {
+        // accumulator row = slot `row` of the token tile; columns 32b .. 32b+15 are the gate and
+        // 32b+16 .. 32b+31 the up products of intermediate indices mt*128 + 16b .. +15: one
+        // tensor-memory load per 16-element block of h, SiLU*up in registers, 32 (BF16) or 16
+        // (E4M3) contiguous bytes of the slot's h row per block
         const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * (2 * kTileN);
         const float mg = prm.mult[e * 3 + 0], mu = prm.mult[e * 3 + 1];
-        const int irow = mt * 128 + row;
-        for (int c0 = 0; c0 < kTileN; c0 += 32) {
-          uint32_t gr[32], ur[32];
-          ld32(tb + c0, gr);
-          ld32(tb + kTileN + c0, ur);
+        const bool valid = row < nval;
+        const float fx = valid ? ws.xfac[ws.perm[slot0 + row]] : 0.0f;
+        const size_t hrow = (size_t)(slot0 + (valid ? row : 0)) * I + mt * 128;
+        float amax = 0.0f;
+        for (int blk = 0; blk < 8; ++blk) {
+          uint32_t r[32];
+          ld32(tb + blk * 32, r);
+          if (blk == 7) {   // every column is in registers: the buffer goes back to the MMA warp
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          }
+          float h[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float gv = __uint_as_float(r[i]) * mg * fx;
+            const float uv = __uint_as_float(r[16 + i]) * mu * fx;
+            h[i] = (gv / (1.0f + expf(-gv))) * uv;
+          }
+          if (!valid) continue;
           if (prm.a8) {
             // W4A8: h -> E4M3 with the down matrix's scale (dinv6 = fl32(1/fl32(6 S_down)))
             const float r8 = prm.dinv6[e];
+            uint32_t cw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-              const int col = c0 + q;
-              const float fx = colfac[col];
-              const float gv = __uint_as_float(gr[q]) * mg * fx;
-              const float uv = __uint_as_float(ur[q]) * mu * fx;
-              if (col < nval)
-                ws.hq[(size_t)(slot0 + col) * I + irow] =
-                    static_cast<uint8_t>(a8_encode((gv / (1.0f + expf(-gv))) * uv, r8));
-            }
-            continue;
-          }
+            for (int i = 0; i < 16; ++i) cw[i >> 2] |= a8_encode(h[i], r8) << (8 * (i & 3));
+            *reinterpret_cast<uint4*>(ws.hq + hrow + blk * 16) =
+                make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          } else {
+            uint32_t hw[8];
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int col = c0 + q;
-            const float fx = colfac[col];
-            const float gv = __uint_as_float(gr[q]) * mg * fx;
-            const float uv = __uint_as_float(ur[q]) * mu * fx;
-            const uint16_t hb = f32_to_bf16_rn((gv / (1.0f + expf(-gv))) * uv);
-            const uint32_t am = __reduce_max_sync(
-                0xFFFFFFFFu, __float_as_uint(fabsf(__uint_as_float((uint32_t)hb << 16))));
-            if (col < nval) {
-              ws.h16[(size_t)(slot0 + col) * I + irow] = hb;
-              if (lane == 0) atomicMax(&colmax[col], am);
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t lo = f32_to_bf16_rn(h[2 * i]), hi = f32_to_bf16_rn(h[2 * i + 1]);
+              hw[i] = lo | (hi << 16);
+              // |h| of the BF16 values, for the down operand's per-slot scaling
+              amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(lo << 16)),
+                                       fabsf(__uint_as_float(hi << 16))));
             }
+            uint4* dst = reinterpret_cast<uint4*>(ws.h16 + hrow + blk * 16);
+            dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           }
         }
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        t16_epi_sync();
-        if (!prm.a8 && et < nval) atomicMax(&ws.slot_amax[slot0 + et], colmax[et]);
+        if (valid && !prm.a8) atomicMax(&ws.slot_amax[slot0 + row], __float_as_uint(amax));
       } else {
         const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * kTileN;
         const float md = prm.mult[e * 3 + 2];
