@@ -344,6 +344,27 @@ def test_forward_twice_is_deterministic_and_counters_reset():
     pack.close()
 
 
+def test_forward_modes_interleaved_on_one_workspace():
+    # narrow calls of all three modes (and a wide call) share one workspace: the fused kernel's
+    # control words (epoch, CTA counters) must carry over between them, so every output equals
+    # the same call's output on a fresh workspace, and a T = 1 and a T = 8 call alternate too
+    H, E, k, I = 512, 32, 4, 128
+    x8, wr, ex = small_layer(8, H, E, k, I, seed=5)
+    pack = pack_from_experts(ex)
+    size = max(moe.moe_workspace_size(pack, T, k, m) for T in (1, 8, 40) for m in (0, 1, 2))
+    ws = moe.new_workspace(size)
+    x40 = small_layer(40, H, E, k, I, seed=5)[0]
+    calls = [(8, 0), (8, 1), (1, 2), (8, 2), (40, 1), (1, 0), (8, 1), (1, 1), (8, 0)]
+    for T, mode in calls:
+        xs = x8[:T] if T <= 8 else x40
+        got = moe.moe_forward(dev_bf16(xs), dev_bf16(wr), pack, k, mode, ws=ws).clone()
+        fresh = moe.moe_forward(dev_bf16(xs), dev_bf16(wr), pack, k, mode).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), fresh.view(torch.int16)), (T, mode)
+        assert moe.moe_read_device_status(ws) == 0, (T, mode)
+    pack.close()
+
+
 def test_forward_identical_experts_equal_one_expert():
     x, wr, ex = small_layer(4, 512, 16, 3, 128, seed=6)
     same = oracle.ExpertSet(ex.E, ex.H, ex.I)
