@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 namespace moe {
@@ -203,6 +204,50 @@ bool a8_supported(int T, int H, int E, int k, int I) {
 bool route_shape_ok(int T, int H, int E, int k) {
   return T >= 1 && T <= 65536 && H >= 128 && H % 128 == 0 && H <= 8192 && E >= 1 && E <= 1024 &&
          k >= 1 && k <= E && k <= 32;
+}
+
+// Layout of the last call on each workspace (by address). The fused narrow kernel's epoch-tagged
+// words (logits, h, Y) rely on their regions holding zeros or tagged words of earlier calls; a
+// call of another layout (shape, mode, pack dimensions, shared expert, layer count) puts other
+// data at those offsets, whose upper halves can equal a later call's epoch. So the first fused
+// call after a layout change clears its tagged regions (a memset on the call's stream).
+uint64_t layout_sig(int kind, int T, int H, int E, int k, int I, int mode, int Is, int layers) {
+  uint64_t h = 1469598103934665603ull;   // FNV-1a over the fields
+  for (long long f : {(long long)kind, (long long)T, (long long)H, (long long)E, (long long)k,
+                      (long long)I, (long long)mode, (long long)Is, (long long)layers}) {
+    h ^= (uint64_t)f;
+    h *= 1099511628211ull;
+  }
+  return h;
+}
+
+// Records sig as the workspace's layout; true when the workspace held another layout before.
+bool layout_changed(const void* ws, uint64_t sig) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, uint64_t> last;
+  std::lock_guard<std::mutex> g(mu);
+  auto it = last.find(ws);
+  if (it == last.end()) {
+    last.emplace(ws, sig);
+    return false;   // a workspace is zero-filled before its first use
+  }
+  const bool changed = it->second != sig;
+  it->second = sig;
+  return changed;
+}
+
+// Clears the tagged regions of a narrow call's layout at byte offset base of the workspace.
+cudaError_t clear_tags(unsigned char* ws, size_t base, const WsLayout& L, int T, int H, int E,
+                       int k, int I, cudaStream_t s) {
+  const size_t S = (size_t)T * k;
+  const size_t parts[3][2] = {{L.logits, (size_t)T * E * 8 * moe::kLogitReplicas},
+                              {L.htag, S * (I / 16) * 9 * 8},
+                              {L.ytag, S * (H / 2) * 8}};
+  for (const auto& p : parts) {
+    const cudaError_t e = cudaMemsetAsync(ws + base + p[0], 0, p[1], s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // Chained layers: the control words, then one region per layer laid out as a single call's
@@ -461,6 +506,7 @@ moe_status moe_route_topk(const uint16_t* x, const uint16_t* router_w, int T, in
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (!route_shape_ok(T, H, E, k)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(T, H, E, k, 0, -1);
+  (void)layout_changed(ws, layout_sig(0, T, H, E, k, 0, -1, 0, 1));
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   moe::WsView v = ws_view(ws, L, T, H, E, k, 0);
   moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
@@ -597,6 +643,11 @@ moe_status forward_impl(const uint16_t* x, const uint16_t* router_w, const moe_e
   moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
   // while profiling, launches are not overlapped by programmatic dependent launch
   if (g_prof.count) lc.pdl = false;
+  if (layout_changed(ws, layout_sig(sh ? 2 : 1, T, H, E, k, I, (int)mode, sh ? sh->inter : 0, 1)) &&
+      narrow) {
+    const cudaError_t ce = clear_tags(static_cast<unsigned char*>(ws), 0, L, T, H, E, k, I, lc.stream);
+    if (ce != cudaSuccess) return from_cuda(ce);
+  }
   int n = 0;
   const cudaError_t e = launch_forward(lc, pack, sh, L, static_cast<unsigned char*>(ws), v,
                                        (int)mode, x, router_w, out, &n);
@@ -664,6 +715,14 @@ moe_status moe_forward_layers(const uint16_t* x, const uint16_t* const* router_w
   const moe::WsView v0 = ws_view(ws, L, T, H, E, k, I);
   moe::LaunchCfg lc{static_cast<cudaStream_t>(stream), num_sms_of_current_device(), true};
   if (g_prof.count) lc.pdl = false;
+  if (layout_changed(ws, layout_sig(3, T, H, E, k, I, (int)mode, 0, layers)) &&
+      T <= moe::kNarrowT) {
+    for (int l = 0; l < layers; ++l) {
+      const cudaError_t ce = clear_tags(static_cast<unsigned char*>(ws), (size_t)l * stride, L,
+                                        T, H, E, k, I, lc.stream);
+      if (ce != cudaSuccess) return from_cuda(ce);
+    }
+  }
   const int m = (int)mode;
   cudaError_t e = cudaSuccess;
   int n = 0;

@@ -469,6 +469,110 @@ __device__ __forceinline__ void warp_select_softmax(uint32_t (&key)[V], int k, i
   w_out = ex / z;
 }
 
+// Top-k + softmax of one token by one warp, with a 32-entry shared-memory scratch (cand):
+// threshold L = the k-th largest of the 32 lane maxima (counted with multiplicity). The k lane
+// maxima >= L are k distinct logits, so every one of the top k has key >= L. L is found without
+// a sort: each lane counts the lane maxima above its own (broadcast reads of the 32 maxima from
+// the scratch), and L is the smallest lane maximum with fewer than k above it. The candidates
+// (keys >= L, about 12 of 512 for k = 10) are packed into the scratch by ballots, each
+// candidate's exact rank by (key desc, index asc) is counted against the others, and ranks < k
+// are the selection. More than 32 candidates: the redux.sync rounds of warp_select_softmax.
+template <int V>
+__device__ __forceinline__ void warp_select_scratch(uint32_t (&key)[V], int k, int lane,
+                                                    unsigned long long* cand, int& e_out,
+                                                    float& w_out) {
+  static_assert((V & (V - 1)) == 0, "V is a power of two");
+  uint32_t m[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) m[i] = key[i];
+#pragma unroll
+  for (int w = V / 2; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = m[i] > m[i + w] ? m[i] : m[i + w];
+  const uint32_t sv = m[0];
+  uint32_t* lm = reinterpret_cast<uint32_t*>(cand);
+  lm[lane] = sv;
+  __syncwarp();
+  int above = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 q = reinterpret_cast<const uint4*>(lm)[j];
+    above += (q.x > sv) + (q.y > sv) + (q.z > sv) + (q.w > sv);
+  }
+  uint32_t thr = __reduce_min_sync(0xFFFFFFFFu, above < k ? sv : 0xFFFFFFFFu);
+  if (thr == 0u) thr = 1u;   // fewer than k lanes hold logits: every logit is a candidate
+  __syncwarp();              // every lane has read the maxima before the scratch is reused
+  const unsigned lt = (1u << lane) - 1u;
+  int C = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const bool is = key[i] >= thr;
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, is);
+    const int pos = C + __popc(bal & lt);
+    // candidate word: key in the high half, ~index in the low half, so that a larger word is a
+    // larger logit, and for equal logits the lower index
+    if (is && pos < 32) cand[pos] = ((unsigned long long)key[i] << 32) | (uint32_t)~(lane + 32 * i);
+    C += __popc(bal);
+  }
+  if (C > 32) {
+    warp_select_softmax<V>(key, k, lane, e_out, w_out);
+    return;
+  }
+  __syncwarp();
+  e_out = 0;
+  float v = 0.0f;
+  int r = 32;
+  unsigned long long mine = 0ull;
+  if (lane < C) {
+    mine = cand[lane];
+    r = 0;
+#pragma unroll 4
+    for (int j = 0; j < (C + 1) >> 1; ++j) {   // broadcast reads; entries >= C do not count
+      const ulonglong2 q = reinterpret_cast<const ulonglong2*>(cand)[j];
+      r += (q.x > mine) + (2 * j + 1 < C && q.y > mine);
+    }
+  }
+  __syncwarp();
+  if (r < k) cand[r] = mine;   // cand[0..k) <- the selection in order
+  __syncwarp();
+  if (lane < k) {
+    const unsigned long long w = cand[lane];
+    e_out = (int)~(uint32_t)w;
+    v = key_logit((uint32_t)(w >> 32));
+  }
+  __syncwarp();
+  const float m0 = __shfl_sync(0xFFFFFFFFu, v, 0);
+  const float ex = lane < k ? expf(v - m0) : 0.0f;
+  float z = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
+  w_out = ex / z;
+}
+
+// The same for E <= 32 V FP32 logits in global memory (read through L2), with the shared-memory
+// scratch selection above (cand: 32 words of this warp's shared memory).
+template <int V>
+__device__ __forceinline__ void warp_topk_softmax_scratch(const float* row, int E, int k, int lane,
+                                                          unsigned long long* cand, int& e_out,
+                                                          float& w_out) {
+  uint32_t key[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? logit_key(__ldcg(row + e)) : 0u;
+  }
+  warp_select_scratch<V>(key, k, lane, cand, e_out, w_out);
+}
+
+__device__ __forceinline__ void topk_row_scratch(const float* row, int E, int k, int lane,
+                                                 unsigned long long* cand, int& e_out,
+                                                 float& w_out) {
+  if (E <= 128) warp_topk_softmax_scratch<4>(row, E, k, lane, cand, e_out, w_out);
+  else if (E <= 256) warp_topk_softmax_scratch<8>(row, E, k, lane, cand, e_out, w_out);
+  else if (E <= 512) warp_topk_softmax_scratch<16>(row, E, k, lane, cand, e_out, w_out);
+  else warp_topk_softmax_scratch<32>(row, E, k, lane, cand, e_out, w_out);
+}
+
 // The same for E <= 32 V FP32 logits in global memory (read through L2).
 template <int V>
 __device__ __forceinline__ void warp_topk_softmax(const float* row, int E, int k, int lane,

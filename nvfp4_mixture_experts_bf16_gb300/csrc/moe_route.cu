@@ -412,6 +412,7 @@ __global__ void __launch_bounds__(256) k_router_gemm(const uint16_t* __restrict_
 
 // ------------------------------------------------------------------ wide top-k
 __global__ void __launch_bounds__(256) k_topk_wide(WsView ws, RouteOut out) {
+  __shared__ unsigned long long cand[8][32];   // per-warp selection scratch
   const int E = ws.E, k = ws.k, T = ws.T;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(256) k_topk_wide(WsView ws, RouteOut out) {
   if (t >= T) return;
   int e_sel;
   float w_sel;
-  topk_row(ws.logits + (size_t)t * E, E, k, lane, e_sel, w_sel);
+  topk_row_scratch(ws.logits + (size_t)t * E, E, k, lane, cand[warp], e_sel, w_sel);
   if (lane < k) {
     out.idx[(size_t)t * k + lane] = e_sel;
     out.w[(size_t)t * k + lane] = w_sel;
