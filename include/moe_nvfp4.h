@@ -109,8 +109,11 @@ moe_status moe_pack_get_matrix(const moe_expert_pack* pack, int expert, int whic
 
 /* Workspace bytes moe_forward needs for (pack, T, k, mode). The workspace must be zero-filled
  * before its first use; every call leaves its counters at zero again, so a workspace can be
- * reused by later calls (with any T, k, mode whose size fits) without re-zeroing. After a call
- * that reported an error through the status word, zero it again. */
+ * reused by later calls (with any pack, T, k, mode whose size fits) without re-zeroing. The
+ * library records the layout of the last call on each workspace (by its start address) and,
+ * when a narrow call (T <= 8) follows a call of another layout, clears that call's
+ * synchronisation words with a memset on the call's stream first. After a call that reported an
+ * error through the status word, zero the workspace again. */
 moe_status moe_workspace_size(const moe_expert_pack* pack, int T, int k, moe_mode mode,
                               size_t* bytes);
 
