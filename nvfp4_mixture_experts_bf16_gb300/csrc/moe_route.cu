@@ -410,42 +410,37 @@ __global__ void __launch_bounds__(256) k_router_gemm(const uint16_t* __restrict_
     }
 }
 
-// ------------------------------------------------------------------ wide top-k
-__global__ void __launch_bounds__(256) k_topk_wide(WsView ws, RouteOut out) {
-  __shared__ unsigned long long cand[8][32];   // per-warp selection scratch
+// ------------------------------------------------------------------ wide top-k + histogram
+constexpr int kChunkTok = 32;
+
+// One block per chunk of 32 tokens, one warp per token: the top-k + softmax of the token, then
+// the chunk's per-expert counts (its row of chunk_base, scanned into prefixes by k_scan_wide).
+__global__ void __launch_bounds__(32 * kChunkTok) k_topk_wide(WsView ws, RouteOut out) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  int32_t* cnt = reinterpret_cast<int32_t*>(smem);   // [E]
+  __shared__ unsigned long long cand[kChunkTok][32];   // per-warp selection scratch
   const int E = ws.E, k = ws.k, T = ws.T;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();
   pdl_launch_dependents();
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  int e_sel;
-  float w_sel;
-  topk_row_scratch(ws.logits + (size_t)t * E, E, k, lane, cand[warp], e_sel, w_sel);
-  if (lane < k) {
-    out.idx[(size_t)t * k + lane] = e_sel;
-    out.w[(size_t)t * k + lane] = w_sel;
-    ws.idx[(size_t)t * k + lane] = e_sel;
-    ws.w[(size_t)t * k + lane] = w_sel;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * kChunkTok + warp;
+  if (t < T) {
+    int e_sel;
+    float w_sel;
+    topk_row_scratch(ws.logits + (size_t)t * E, E, k, lane, cand[warp], e_sel, w_sel);
+    if (lane < k) {
+      out.idx[(size_t)t * k + lane] = e_sel;
+      out.w[(size_t)t * k + lane] = w_sel;
+      ws.idx[(size_t)t * k + lane] = e_sel;
+      ws.w[(size_t)t * k + lane] = w_sel;
+      atomicAdd(&cnt[e_sel], 1);
+    }
   }
-}
-
-// ------------------------------------------------------------------ wide histogram / scan
-constexpr int kChunkTok = 32;
-
-__global__ void __launch_bounds__(256) k_hist_wide(WsView ws) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  int32_t* cnt = reinterpret_cast<int32_t*>(smem);
-  const int E = ws.E, k = ws.k, T = ws.T;
-  pdl_wait();
-  pdl_launch_dependents();
-  for (int e = threadIdx.x; e < E; e += 256) cnt[e] = 0;
   __syncthreads();
-  const int t0 = blockIdx.x * kChunkTok;
-  const int n = min(kChunkTok, T - t0) * k;
-  for (int s = threadIdx.x; s < n; s += 256) atomicAdd(&cnt[ws.idx[(size_t)t0 * k + s]], 1);
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += 256) ws.chunk_base[(size_t)blockIdx.x * E + e] = cnt[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    ws.chunk_base[(size_t)blockIdx.x * E + e] = cnt[e];
 }
 
 // One CTA of 1024 threads: per-expert chunk prefix sums, offsets, and the token groups.
@@ -684,16 +679,14 @@ cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint
     e = launch_kernel(lc, k_router_gemm, gg, dim3(256), 0, x, wr, ws);
   }
   if (e != cudaSuccess) return e;
-  e = launch_kernel(lc, k_topk_wide, dim3((ws.T + 7) / 8), dim3(256), 0, ws, out);
-  if (e != cudaSuccess) return e;
   const int nchunk = (ws.T + kChunkTok - 1) / kChunkTok;
-  e = launch_kernel(lc, k_hist_wide, dim3(nchunk), dim3(256), (size_t)ws.E * 4, ws);
+  e = launch_kernel(lc, k_topk_wide, dim3(nchunk), dim3(32 * kChunkTok), (size_t)ws.E * 4, ws, out);
   if (e != cudaSuccess) return e;
   e = launch_kernel(lc, k_scan_wide, dim3((ws.E + 31) / 32), dim3(1024), 0, ws, pkv, pk ? 1 : 0,
                     out, nchunk);
   if (e != cudaSuccess) return e;
   e = launch_kernel(lc, k_scatter_wide, dim3(nchunk), dim3(256), (size_t)kChunkTok * ws.k * 4, ws, out);
-  if (launches) *launches += 5;
+  if (launches) *launches += 4;
   return e;
 }
 

@@ -66,7 +66,7 @@ def _check_oracle(layers, xs, outs, k, mode):
                                                                   ref["abssum"][t, b]):
                 continue
             toks.append(t)
-            if mode == 1:
+            if mode in (1, 2):   # W4A4 element and block flips; W4A8 element flips
                 allow[t] = sum(ref["w"][t, j] * (ref["h_amb_elem"][ref["slot_of"][t, j]].sum() +
                                                  ref["h_amb_block"][ref["slot_of"][t, j]].sum())
                                for j in range(k))
@@ -75,7 +75,7 @@ def _check_oracle(layers, xs, outs, k, mode):
         compare_outputs(outs[l], ref, mode, toks, allow)
 
 
-@pytest.mark.parametrize("T,mode", [(1, 0), (1, 1), (2, 0), (5, 1), (8, 0)])
+@pytest.mark.parametrize("T,mode", [(1, 0), (1, 1), (2, 0), (5, 1), (8, 0), (1, 2), (6, 2)])
 def test_layers_fused_equal_single_calls_and_oracle(T, mode):
     L, H, E, k, I = 5, 512, 64, 4, 128
     layers, x0 = _stack(L, T, H, E, k, I, mode, seed=200 + T)
