@@ -940,7 +940,7 @@ struct T16 {
   static constexpr int kStage = ((kConv + kB + kRaw + kSf) + 1023) / 1024 * 1024;
   static constexpr int kTmemCols = DOWN ? 256 : 512;
   static constexpr int kYStage = kTileN * kYStride * 2;   // down: transposed BF16 Y tile
-  static constexpr int kSmem = kT16Stages * kStage + (DOWN ? kYStage : 0) + 2 * 512 + 1024;
+  static constexpr int kSmem = kT16Stages * kStage + (DOWN ? kYStage : 0) + 512 + 1024;
 };
 
 template <bool DOWN>
@@ -957,7 +957,6 @@ __global__ void __launch_bounds__(kT16Threads, 1)
   unsigned char* smem = smem_raw + pad;
   unsigned char* ystage = smem + kT16Stages * L::kStage;            // down: Y tile
   float* colfac = reinterpret_cast<float*>(ystage + (DOWN ? L::kYStage : 0));   // [128]
-  uint32_t* colmax = reinterpret_cast<uint32_t*>(colfac + kTileN);             // [128]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
@@ -1130,22 +1129,16 @@ __global__ void __launch_bounds__(kT16Threads, 1)
       const int buf = tcount & 1, use = tcount >> 1;
       const int e = ws.tt_expert[j];
       const int slot0 = ws.tt_slot0[j], nval = ws.tt_n[j];
-      // per column (slot) factor 2^s: of the slot's token (gate/up) or of the slot (down)
-      {
+      if (DOWN) {
+        // per column (slot) factor 2^s of the slot's h, or fl32(6 S_down) in W4A8
         float f = 0.0f;
-        if (et < nval) {
-          if (!DOWN) {
-            f = ws.xfac[ws.perm[slot0 + et]];
-          } else if (prm.a8) {
-            f = __fmul_rn(6.0f, prm.dscale[e]);   // W4A8: the h codes' scale fl32(6 S_down)
-          } else {
-            f = __int_as_float((127 + amax_shift(__uint_as_float(ws.slot_amax[slot0 + et]))) << 23);
-          }
-        }
+        if (et < nval)
+          f = prm.a8 ? __fmul_rn(6.0f, prm.dscale[e])
+                     : __int_as_float((127 + amax_shift(__uint_as_float(ws.slot_amax[slot0 + et])))
+                                      << 23);
         colfac[et] = f;
-        if (!DOWN) colmax[et] = 0u;
+        t16_epi_sync();
       }
-      t16_epi_sync();
       if (!abort_s && !mbar_wait(&acc_full[buf], use & 1)) {
         record_status(ws.ctl, kStTimeout);
         abort_s = 1;
@@ -1226,7 +1219,7 @@ __global__ void __launch_bounds__(kT16Threads, 1)
                 *reinterpret_cast<const uint4*>(yt + col * kYStride + r8 * 8);
         }
       }
-      t16_epi_sync();   // colfac / colmax / the Y tile are reused by the next tile
+      if (DOWN) t16_epi_sync();   // colfac and the Y tile are reused by the next tile
     }
   }
   fence_before();
