@@ -76,6 +76,7 @@ def test_forward_wide_grouped_mma_sync_path(T, H, E, k, I, mode):
 
 
 @pytest.mark.parametrize("T,H,E,k,I", [
+    (60, 256, 4, 2, 64),      # h resident: 1 K chunk and 1 scale-factor atom; one gate/up tile
     (300, 512, 6, 2, 320),    # h resident: 5 scale-factor atoms, 2 K chunks
     (200, 256, 4, 2, 512),    # h resident: 8 scale-factor atoms
     (150, 256, 4, 2, 768),    # two h tiles do not fit beside two weight tiles: h restaged per unit
