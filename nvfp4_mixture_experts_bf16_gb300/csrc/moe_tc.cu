@@ -1,27 +1,32 @@
-// moe_tc.cu — grouped NVFP4 expert GEMMs on the 5th-generation tensor cores (tcgen05) for wide
-// (prefill) calls in W4A4 mode.
+// moe_tc.cu — the wide (prefill) calls on the 5th-generation tensor cores (tcgen05): the BF16
+// router GEMM, the grouped NVFP4 expert GEMMs of the W4A4 and the W4A16/W4A8 paths, and the
+// kernels that prepare their operands.
 //
 // Model card "Qwen3.8-Flash-Next NVIDIA NVFP4 for Infernix (bit-exact)", section "What is
 // bit-exact and what is quantized": E2M1 codes with one E4M3 scale per 16 weights, an FP32
 // multiplier and an FP32 activation input scale per matrix. The Infernix README, section
 // "Activation precision", reads prompts in W4A4 on the FP4 tensor cores. Here that is
-// tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (E2M1 x E2M1, UE4M3 scale per 16), M = 128
-// weight rows, N = 128 tokens, K = 64 per instruction, FP32 accumulators in tensor memory:
+// tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (E2M1 x E2M1, UE4M3 scale per 16),
+// 128 x 128 per instruction, K = 64, FP32 accumulators in tensor memory:
 //
 //   * tokens are grouped per expert into tiles of <= 128 slots ("token tiles"), laid out in a
 //     padded permuted space (tile j = rows 128j..128j+127), so that a tile's activation codes
 //     and scale-factor atoms are contiguous;
+//   * the activation tile is the MMA's M side and the weight tile its N side, so the
+//     accumulator is [slot][weight row] and one epilogue thread holds one slot's row;
 //   * warp 0 issues TMA loads (tensor maps, 128-byte swizzle) of the weight and activation tiles
 //     and bulk copies of the scale-factor atoms into a ring of stages guarded by mbarriers;
-//   * warp 1 copies the scale factors into tensor memory (tcgen05.cp) and issues the MMAs; a
-//     commit per stage releases the stage and a commit per tile hands the accumulator to
-//   * warps 2..5, the epilogue: tensor memory -> registers, then SiLU*up and the NVFP4
-//     quantisation of h (gate/up) or the BF16 expert output Y (down). Accumulators are double
-//     buffered so the epilogue of one tile overlaps the main loop of the next.
+//     warp 1 copies the scale factors into tensor memory (tcgen05.cp) and issues the MMAs;
+//     warps 2..9 are the epilogue (tensor memory -> registers, then SiLU*up and the NVFP4
+//     quantisation of h, or the BF16 expert output Y);
+//   * one thread issues all of a CTA's tensor-core instructions, and at these tile sizes that
+//     issuing, not memory, bounds a CTA: the gate/up GEMM runs two CTAs per SM; the down GEMM
+//     keeps a token tile's h in shared and tensor memory while it runs the expert's weight
+//     tiles, and stores Y through TMA.
 //
 // Scale-factor atom (512 B, one K step of 64 for 128 rows): byte (r % 32) * 16 + (r / 32) * 4 + b
-// holds the scale of row r, 16-element block b. After tcgen05.cp.32x128b.warpx4 row m's scales
-// sit at tensor-memory lane m, column (base + m / 32), the layout the block-scaled MMA reads.
+// holds the scale of row r, 16-element block b; tcgen05.cp.32x128b.warpx4 copies it into tensor
+// memory in the layout the block-scaled MMA reads.
 #include "moe_internal.cuh"
 
 #include <cuda.h>
