@@ -43,7 +43,7 @@ constexpr int kSfStage = 4 * 512;               // 4 K steps of scale-factor ato
 constexpr int kStageBytes = 2 * kTileBytes + 2 * kSfStage;   // A, B, SFA, SFB = 36 KB
 constexpr int kEpiWarps = 8;                    // two per tensor-memory lane quadrant
 constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue warps
-constexpr int kYStride = kTileM + 8;            // padded slot column of the down staging (BF16)
+constexpr int kYStride = kTileM + 8;            // padded slot column of a transposed BF16 Y tile
 constexpr int kTmemCols = 256;
 constexpr int kSfCol = 128;                     // scale factors after the 128-column accumulator
 
@@ -1018,7 +1018,8 @@ __global__ void __launch_bounds__(kT16Threads, 1)
           if (!DOWN) {
             tma_2d(raw, &tm_a0, ks * 32, e * I + mt * 128, &full[s]);
             tma_2d(raw + 4096, &tm_a1, ks * 32, e * I + mt * 128, &full[s]);
-            // scale atoms of the two 64-row intermediate tiles (gate rows 0..63, up 64..127)
+            // scale atoms of the two 64-index intermediate tiles (each: gate and up rows
+            // interleaved by 16)
             for (int h2 = 0; h2 < 2; ++h2)
               bulk_g2s(sf + h2 * 512,
                        prm.sfa + (((size_t)e * (I / 64) + 2 * mt + h2) * (H / 64) + ks) * 512, 512,
