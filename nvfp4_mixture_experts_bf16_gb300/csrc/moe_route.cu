@@ -414,20 +414,27 @@ __global__ void __launch_bounds__(256) k_router_gemm(const uint16_t* __restrict_
 constexpr int kChunkTok = 32;
 
 // One block per chunk of 32 tokens, one warp per token: the top-k + softmax of the token, then
-// the chunk's per-expert counts (its row of chunk_base, scanned into prefixes by k_scan_wide).
+// the chunk's per-expert counts (its row of chunk_base, scanned into prefixes by k_scan_wide)
+// and each selection's rank among the chunk's earlier selections of its expert (a token selects
+// an expert at most once, so the rank is the number of earlier tokens in the chunk that
+// selected it: a popcount of the expert's token mask), kept in slot_of for k_scatter_wide.
 __global__ void __launch_bounds__(32 * kChunkTok) k_topk_wide(WsView ws, RouteOut out) {
   extern __shared__ __align__(16) unsigned char smem[];
-  int32_t* cnt = reinterpret_cast<int32_t*>(smem);   // [E]
+  int32_t* cnt = reinterpret_cast<int32_t*>(smem);                  // [E]
+  uint32_t* tmask = reinterpret_cast<uint32_t*>(cnt + ws.E);        // [E]: tokens of the chunk
   __shared__ unsigned long long cand[kChunkTok][32];   // per-warp selection scratch
   const int E = ws.E, k = ws.k, T = ws.T;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();
   pdl_launch_dependents();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    cnt[e] = 0;
+    tmask[e] = 0u;
+  }
   __syncthreads();
   const int t = blockIdx.x * kChunkTok + warp;
+  int e_sel = 0;
   if (t < T) {
-    int e_sel;
     float w_sel;
     topk_row_scratch(ws.logits + (size_t)t * E, E, k, lane, cand[warp], e_sel, w_sel);
     if (lane < k) {
@@ -436,9 +443,12 @@ __global__ void __launch_bounds__(32 * kChunkTok) k_topk_wide(WsView ws, RouteOu
       ws.idx[(size_t)t * k + lane] = e_sel;
       ws.w[(size_t)t * k + lane] = w_sel;
       atomicAdd(&cnt[e_sel], 1);
+      atomicOr(&tmask[e_sel], 1u << warp);
     }
   }
   __syncthreads();
+  if (t < T && lane < k)
+    ws.slot_of[(size_t)t * k + lane] = __popc(tmask[e_sel] & ((1u << warp) - 1u));
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     ws.chunk_base[(size_t)blockIdx.x * E + e] = cnt[e];
 }
@@ -548,26 +558,19 @@ __global__ void __launch_bounds__(1024) k_scan_wide(WsView ws, PackView pkv, int
   }
 }
 
+// Slot s = t*k + j of every token: its position in the expert-major permutation, from the
+// expert's offset, the chunk's prefix for the expert and the selection's rank in the chunk.
 __global__ void __launch_bounds__(256) k_scatter_wide(WsView ws, RouteOut out) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int E = ws.E, k = ws.k, T = ws.T;
-  int32_t* sidx = reinterpret_cast<int32_t*>(smem);  // [kChunkTok * k]
+  const int E = ws.E, k = ws.k;
   pdl_wait();
   pdl_launch_dependents();
-  const int t0 = blockIdx.x * kChunkTok;
-  const int ntok = min(kChunkTok, T - t0);
-  const int n = ntok * k;
-  for (int s = threadIdx.x; s < n; s += 256) sidx[s] = ws.idx[(size_t)t0 * k + s];
-  __syncthreads();
-  for (int s = threadIdx.x; s < n; s += 256) {
-    const int tl = s / k, e = sidx[s];
-    int rank = 0;
-    for (int s2 = 0; s2 < tl * k; ++s2) rank += (sidx[s2] == e) ? 1 : 0;
-    const int pos = ws.offsets[e] + ws.chunk_base[(size_t)blockIdx.x * E + e] + rank;
-    out.perm[pos] = t0 + tl;
-    ws.perm[pos] = t0 + tl;
-    ws.slot_of[(size_t)t0 * k + s] = pos;
-  }
+  const int s = blockIdx.x * 256 + threadIdx.x;
+  if (s >= ws.T * k) return;
+  const int t = s / k, e = ws.idx[s];
+  const int pos = ws.offsets[e] + ws.chunk_base[(size_t)(t / kChunkTok) * E + e] + ws.slot_of[s];
+  out.perm[pos] = t;
+  ws.perm[pos] = t;
+  ws.slot_of[s] = pos;
 }
 
 // ------------------------------------------------------------------ wide activation prep
@@ -680,12 +683,12 @@ cudaError_t launch_route_wide(const LaunchCfg& lc, const uint16_t* x, const uint
   }
   if (e != cudaSuccess) return e;
   const int nchunk = (ws.T + kChunkTok - 1) / kChunkTok;
-  e = launch_kernel(lc, k_topk_wide, dim3(nchunk), dim3(32 * kChunkTok), (size_t)ws.E * 4, ws, out);
+  e = launch_kernel(lc, k_topk_wide, dim3(nchunk), dim3(32 * kChunkTok), (size_t)ws.E * 8, ws, out);
   if (e != cudaSuccess) return e;
   e = launch_kernel(lc, k_scan_wide, dim3((ws.E + 31) / 32), dim3(1024), 0, ws, pkv, pk ? 1 : 0,
                     out, nchunk);
   if (e != cudaSuccess) return e;
-  e = launch_kernel(lc, k_scatter_wide, dim3(nchunk), dim3(256), (size_t)kChunkTok * ws.k * 4, ws, out);
+  e = launch_kernel(lc, k_scatter_wide, dim3((ws.T * ws.k + 255) / 256), dim3(256), 0, ws, out);
   if (launches) *launches += 4;
   return e;
 }
