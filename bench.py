@@ -585,6 +585,10 @@ def prefill_roofline(w3, ms3, kernels, U, pk, shared):
                       peak=pk["hbm"], frac=round(floor / (ms3 * 1e-3) / 1e9 / pk["hbm"], 4),
                       floor_ms=round(floor / (pk["hbm"] * 1e9) * 1e3, 4),
                       note="touched experts' NVFP4 weights + router + x + out, each once"),
+             # the chunk's time against the larger of its two floors
+             bound_ms=round(max(flops / (peak * 1e12), floor / (pk["hbm"] * 1e9)) * 1e3, 4),
+             frac_of_bound=round(max(flops / (peak * 1e12), floor / (pk["hbm"] * 1e9)) * 1e3 / ms3,
+                                 4),
              dominant=dict(kernel=dom_name, ms=round(dom_ms, 4), share=round(dom_ms / tot, 4)),
              kernels=[dict(kernel=n, ms=round(t, 4), share=round(t / tot, 4)) for n, t in kernels],
              kernel_timing="CUDA events around each launch, PDL off (serialised)")
