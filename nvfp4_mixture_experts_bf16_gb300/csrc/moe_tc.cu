@@ -100,6 +100,9 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read_all() {   // sources of all groups read
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+__device__ __forceinline__ void bulk_wait_read_but1() {  // all but the newest group read
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_all() {        // all groups complete
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -904,7 +907,8 @@ __global__ void __launch_bounds__(256) k_xsf_atoms(WsView ws) {
 // interleaved by 16 (rows 32b .. 32b+15 gate, +16 .. +31 up), so that one epilogue thread holds
 // a slot's gate and up values of a 16-element block of h side by side. Down: 128 weight rows x
 // 128 slots (or the resident-h kernel k_tc16_dn below).
-constexpr int kT16Stages = 3;
+constexpr int kT16Stages = 6;   // load stages (activation tile, FP4 codes, scale atoms)
+constexpr int kT16Conv = 2;     // dequantised weight buffers
 constexpr int kT16Threads = 10 * 32;   // producer, MMA, 4 converter warps, 4 epilogue warps
 constexpr uint32_t kIdescF16 = (1u << 4) | ((uint32_t)(kTileN >> 3) << 17) |
                                ((uint32_t)(kTileM >> 4) << 24);   // f16 x f16 -> f32, 128x128
@@ -934,19 +938,25 @@ __device__ __forceinline__ void t16_epi_sync() {  // the 4 epilogue warps
   asm volatile("bar.sync 3, 128;" ::: "memory");
 }
 
-// Per-stage layout (bytes): conv A (f16, SW128; gate/up: gate 16 KB + up 16 KB), B (16 KB),
-// raw FP4 codes (gate/up: 2 x 128 rows x 32 B), scale-factor atoms (gate/up 2, down 1).
+// Shared memory (bytes): kT16Stages load stages, each B (16 KB, SW128), the raw FP4 codes
+// (gate/up: 2 x 128 rows x 32 B) and the scale-factor atoms (gate/up 2, down 1); then kT16Conv
+// buffers of dequantised A (f16, SW128; gate/up: gate 16 KB + up 16 KB). The load ring and the
+// dequantised buffers are separate rings: a load stage is refilled once its MMAs have run,
+// without waiting for a conversion slot, so six stages of copies stay in flight while two
+// buffers alternate between the converters and the MMAs.
 template <bool DOWN>
 struct T16 {
   static constexpr int kConv = DOWN ? 16384 : 32768;
   static constexpr int kB = 16384;
   static constexpr int kRaw = DOWN ? 4096 : 8192;
   static constexpr int kSf = DOWN ? 512 : 1024;
-  static constexpr int kStage = ((kConv + kB + kRaw + kSf) + 1023) / 1024 * 1024;
+  static constexpr int kStage = ((kB + kRaw + kSf) + 1023) / 1024 * 1024;
   static constexpr int kTmemCols = DOWN ? 256 : 512;
   static constexpr int kYStage = kTileN * kYStride * 2;   // down: transposed BF16 Y tile
-  static constexpr int kSmem = kT16Stages * kStage + (DOWN ? kYStage : 0) + 512 + 1024;
+  static constexpr int kSmem =
+      kT16Stages * kStage + kT16Conv * kConv + (DOWN ? kYStage : 0) + 512 + 1024;
 };
+static_assert(T16<false>::kSmem <= 232448 && T16<true>::kSmem <= 232448, "k_tc16 shared memory");
 
 template <bool DOWN>
 __global__ void __launch_bounds__(kT16Threads, 1)
@@ -954,21 +964,26 @@ __global__ void __launch_bounds__(kT16Threads, 1)
            const __grid_constant__ CUtensorMap tm_b, TcParams prm, WsView ws) {
   using L = T16<DOWN>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t full[kT16Stages], conv_full[kT16Stages], empty[kT16Stages];
+  __shared__ uint64_t full[kT16Stages], empty[kT16Stages];
+  __shared__ uint64_t conv_full[kT16Conv], conv_empty[kT16Conv];
   __shared__ uint64_t acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* smem = smem_raw + pad;
-  unsigned char* ystage = smem + kT16Stages * L::kStage;            // down: Y tile
+  unsigned char* convb = smem + kT16Stages * L::kStage;             // dequantised A buffers
+  unsigned char* ystage = convb + kT16Conv * L::kConv;              // down: Y tile
   float* colfac = reinterpret_cast<float*>(ystage + (DOWN ? L::kYStage : 0));   // [128]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     for (int s = 0; s < kT16Stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&conv_full[s], 4);
       mbar_init(&empty[s], 1);
+    }
+    for (int c = 0; c < kT16Conv; ++c) {
+      mbar_init(&conv_full[c], 4);
+      mbar_init(&conv_empty[c], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -1011,7 +1026,7 @@ __global__ void __launch_bounds__(kT16Threads, 1)
             break;
           }
           unsigned char* st = smem + s * L::kStage;
-          unsigned char* bt = st + L::kConv;
+          unsigned char* bt = st;
           unsigned char* raw = bt + L::kB;
           unsigned char* sf = raw + L::kRaw;
           mbar_arrive_expect_tx(&full[s], L::kB + L::kRaw + L::kSf);
@@ -1052,14 +1067,15 @@ __global__ void __launch_bounds__(kT16Threads, 1)
         fence_after();
         const uint32_t d0 = tmem + buf * bufcols;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % kT16Stages, n = it / kT16Stages;
-          if (!abort_s && !mbar_wait(&conv_full[s], n & 1)) {
+          // load stage s holds B; buffer c holds the dequantised A (its converters waited for
+          // stage s to land before they signalled c)
+          const int s = it % kT16Stages, c = it % kT16Conv;
+          if (!abort_s && !mbar_wait(&conv_full[c], (it / kT16Conv) & 1)) {
             record_status(ws.ctl, kStTimeout);
             abort_s = 1;
           }
           fence_after();
-          unsigned char* st = smem + s * L::kStage;
-          const uint32_t a0 = smem_u32(st), b0 = smem_u32(st + L::kConv);
+          const uint32_t a0 = smem_u32(convb + c * L::kConv), b0 = smem_u32(smem + s * L::kStage);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t acc = (ks > 0 || q > 0) ? 1u : 0u;
@@ -1069,6 +1085,7 @@ __global__ void __launch_bounds__(kT16Threads, 1)
               mma_f16_n256(d0, desc_sw128(b0 + q * 32), desc_sw128(a0 + q * 32), acc);
           }
           commit(&empty[s]);
+          commit(&conv_empty[c]);
         }
         commit(&acc_full[buf]);
       }
@@ -1081,13 +1098,19 @@ __global__ void __launch_bounds__(kT16Threads, 1)
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       for (int ks = 0; ks < nks; ++ks, ++it) {
         const int s = it % kT16Stages, n = it / kT16Stages;
+        const int cb = it % kT16Conv, cu = it / kT16Conv;
         if (!abort_s && !mbar_wait(&full[s], n & 1)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
         }
-        unsigned char* st = smem + s * L::kStage;
-        const unsigned char* raw = st + L::kConv + L::kB;
+        // buffer cb is free once the MMAs of its previous use have run
+        if (cu > 0 && !abort_s && !mbar_wait(&conv_empty[cb], (cu - 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        const unsigned char* raw = smem + s * L::kStage + L::kB;
         const unsigned char* sf = raw + L::kRaw;
+        unsigned char* st = convb + cb * L::kConv;
 #pragma unroll
         for (int mat = 0; mat < (DOWN ? 1 : 2); ++mat) {
           const uint4* src = reinterpret_cast<const uint4*>(raw + mat * 4096 + ct * 32);
@@ -1121,7 +1144,7 @@ __global__ void __launch_bounds__(kT16Threads, 1)
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(&conv_full[s]);
+        if (lane == 0) mbar_arrive(&conv_full[cb]);
       }
     }
   } else {
@@ -1248,8 +1271,10 @@ constexpr uint32_t kIdescDn = (1u << 4) | ((uint32_t)(kDnN >> 3) << 17) |
 constexpr int kDnConv = kDnN * 128;                 // 256 rows x 128 B (64 f16), SW128
 constexpr int kDnRaw = kDnN * 32;                   // 256 rows x 64 FP4 codes
 constexpr int kDnSf = 2 * 512;                      // two 128-row scale-factor atoms
-constexpr int kDnStage = kDnConv + kDnRaw + kDnSf;  // 41 KB, a multiple of 1 KB
-constexpr int kDnMaxStages = 3;
+constexpr int kDnLStage = kDnRaw + kDnSf;          // 9 KB load stage, a multiple of 1 KB
+constexpr int kDnConvBufs = 2;                      // dequantised B buffers
+constexpr int kDnYStaging = 4 * 2 * 4096;           // per epilogue warp: two 32-row x 128 B Y boxes
+constexpr int kDnMaxStages = 8;
 
 __device__ __forceinline__ void mma_f16_dn(uint32_t d, uint64_t a, uint64_t b,
                                            uint32_t accumulate) {
@@ -1262,9 +1287,11 @@ __device__ __forceinline__ void mma_f16_dn(uint32_t d, uint64_t a, uint64_t b,
 
 __global__ void __launch_bounds__(kT16Threads, 1)
     k_tc16_dn(const __grid_constant__ CUtensorMap tm_raw, const __grid_constant__ CUtensorMap tm_h,
-              TcParams prm, WsView ws, int nst) {
+              const __grid_constant__ CUtensorMap tm_y32, const __grid_constant__ CUtensorMap tm_y16,
+              TcParams prm, WsView ws, int nst, int ybox) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t full[kDnMaxStages], conv_full[kDnMaxStages], empty[kDnMaxStages];
+  __shared__ uint64_t full[kDnMaxStages], empty[kDnMaxStages];
+  __shared__ uint64_t conv_full[kDnConvBufs], conv_empty[kDnConvBufs];
   __shared__ uint64_t acc_full[2], acc_empty[2], a_full, a_empty;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
@@ -1272,15 +1299,23 @@ __global__ void __launch_bounds__(kT16Threads, 1)
   unsigned char* smem = smem_raw + pad;
   const int H = prm.H, I = prm.I;
   const int nks = I / 64;
+  // the h tile, two dequantised weight buffers, then the ring of load stages (FP4 codes and
+  // scale atoms): a load stage is refilled once its buffer's MMAs have run, without waiting for
+  // a conversion slot, so nst stages of copies stay in flight
   unsigned char* atile = smem;                                   // [nks][128 rows x 128 B]
-  unsigned char* stages = smem + (size_t)nks * 16384;
+  unsigned char* convb = smem + (size_t)nks * 16384;             // [2][256 rows x 128 B]
+  unsigned char* stages = convb + kDnConvBufs * kDnConv;
+  unsigned char* ystg = stages + (size_t)nst * kDnLStage;       // [4 warps][2][32 rows x 128 B]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     for (int s = 0; s < nst; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&conv_full[s], 4);
       mbar_init(&empty[s], 1);
+    }
+    for (int c = 0; c < kDnConvBufs; ++c) {
+      mbar_init(&conv_full[c], 4);
+      mbar_init(&conv_empty[c], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -1337,7 +1372,7 @@ __global__ void __launch_bounds__(kT16Threads, 1)
             abort_s = 1;
             break;
           }
-          unsigned char* raw = stages + (size_t)s * kDnStage + kDnConv;
+          unsigned char* raw = stages + (size_t)s * kDnLStage;
           unsigned char* sf = raw + kDnRaw;
           mbar_arrive_expect_tx(&full[s], kDnRaw + kDnSf);
           tma_2d(raw, &tm_raw, ks * 32, e * H + nt * kDnN, &full[s]);
@@ -1376,19 +1411,20 @@ __global__ void __launch_bounds__(kT16Threads, 1)
         fence_after();
         const uint32_t d0 = tmem + buf * kDnN;
         for (int ks = 0; ks < nks; ++ks, ++it) {
-          const int s = it % nst, n = it / nst;
-          if (!abort_s && !mbar_wait(&conv_full[s], n & 1)) {
+          const int s = it % nst, c = it % kDnConvBufs;
+          if (!abort_s && !mbar_wait(&conv_full[c], (it / kDnConvBufs) & 1)) {
             record_status(ws.ctl, kStTimeout);
             abort_s = 1;
           }
           fence_after();
           const uint32_t a0 = smem_u32(atile + ks * 16384);
-          const uint32_t b0 = smem_u32(stages + (size_t)s * kDnStage);
+          const uint32_t b0 = smem_u32(convb + c * kDnConv);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             mma_f16_dn(d0, desc_sw128(a0 + q * 32), desc_sw128(b0 + q * 32),
                        (ks > 0 || q > 0) ? 1u : 0u);
           commit(&empty[s]);
+          commit(&conv_empty[c]);
         }
         commit(&acc_full[buf]);
         // the h tile may be replaced once this token tile's last MMA has read it
@@ -1403,12 +1439,18 @@ __global__ void __launch_bounds__(kT16Threads, 1)
     for (int u = u0; u < u1; ++u) {
       for (int ks = 0; ks < nks; ++ks, ++it) {
         const int s = it % nst, n = it / nst;
+        const int cb = it % kDnConvBufs, cu = it / kDnConvBufs;
         if (!abort_s && !mbar_wait(&full[s], n & 1)) {
           record_status(ws.ctl, kStTimeout);
           abort_s = 1;
         }
-        unsigned char* st = stages + (size_t)s * kDnStage;
-        const unsigned char* raw = st + kDnConv;
+        // buffer cb is free once the MMAs of its previous use have run
+        if (cu > 0 && !abort_s && !mbar_wait(&conv_empty[cb], (cu - 1) & 1)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        unsigned char* st = convb + cb * kDnConv;
+        const unsigned char* raw = stages + (size_t)s * kDnLStage;
         const unsigned char* sf = raw + kDnRaw;
 #pragma unroll
         for (int mat = 0; mat < 2; ++mat) {
@@ -1438,14 +1480,15 @@ __global__ void __launch_bounds__(kT16Threads, 1)
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(&conv_full[s]);
+        if (lane == 0) mbar_arrive(&conv_full[cb]);
       }
     }
   } else {
     // ---------------------------------------------------------------- epilogue (warps 6..9)
     const int quad = warp & 3;              // tensor-memory lanes 32*quad .. +31
     const int row = quad * 32 + lane;       // slot of the token tile
-    int tcount = 0;
+    unsigned char* stg = ystg + (warp - 6) * 8192;   // this warp's two Y boxes
+    int tcount = 0, ycount = 0;
     for (int u = u0; u < u1; ++u, ++tcount) {
       const int j = u / nts, nt = u % nts;
       const int buf = tcount & 1, use = tcount >> 1;
@@ -1465,25 +1508,63 @@ __global__ void __launch_bounds__(kT16Threads, 1)
       __syncwarp();
       fence_after();
       const uint32_t tb = tmem + ((uint32_t)(quad * 32) << 16) + buf * kDnN;
-      uint4* yrow = reinterpret_cast<uint4*>(ws.y + (size_t)(slot0 + row) * H + nt * kDnN);
-      for (int c0 = 0; c0 < kDnN; c0 += 32) {
-        uint32_t r[32];
-        ld32(tb + c0, r);
-        uint32_t o[16];
+      // this warp's slots quad*32 .. +31: nv of them are valid, the first ntm go out by TMA
+      // (32- or 16-row boxes of 64 BF16 = 128 bytes per row, staged 128-byte swizzled), the
+      // rest of a ragged tile as plain row stores (all of them when the staging did not fit:
+      // ybox = 0)
+      const int nv = min(max(nval - quad * 32, 0), 32);
+      const int ntm = !ybox ? 0 : nv == 32 ? 32 : (nv & ~15);
+      for (int c0 = 0; c0 < kDnN; c0 += 64, ++ycount) {
+        uint32_t r0[32], r1[32];
+        ld32(tb + c0, r0);
+        ld32(tb + c0 + 32, r1);
+        if (c0 + 64 == kDnN) {   // every column is in registers: the buffer goes back
+          fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        if (nv == 0) continue;
+        uint4 v[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          o[q] = (uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * q]) * f) |
-                 ((uint32_t)f32_to_bf16_rn(__uint_as_float(r[2 * q + 1]) * f) << 16);
-        if (row < nval) {
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            yrow[c0 / 8 + q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) {
+            const int i0 = (c * 8 + 2 * q) & 31;
+            const uint32_t v0 = (c < 4) ? r0[i0] : r1[i0], v1 = (c < 4) ? r0[i0 + 1] : r1[i0 + 1];
+            w[q] = (uint32_t)f32_to_bf16_rn(__uint_as_float(v0) * f) |
+                   ((uint32_t)f32_to_bf16_rn(__uint_as_float(v1) * f) << 16);
+          }
+          v[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        unsigned char* sb = stg + (ycount & 1) * 4096;
+        if (ntm > 0) {
+          if (lane == 0) bulk_wait_read_but1();   // the store that last used sb has read it
+          __syncwarp();
+        }
+        if (lane < ntm) {
+          // row `lane` of the box; 16-byte chunk c sits at c ^ (row & 7) (128-byte swizzle)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(sb + lane * 128 + ((c ^ (lane & 7)) << 4)) = v[c];
+        } else if (lane < nv) {
+          uint4* dst =
+              reinterpret_cast<uint4*>(ws.y + (size_t)(slot0 + row) * H + nt * kDnN + c0);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dst[c] = v[c];
+        }
+        if (ntm > 0) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(ntm == 32 ? &tm_y32 : &tm_y16, sb, (nt * kDnN + c0) * 2,
+                         slot0 + quad * 32);
+            bulk_commit();
+          }
         }
       }
-      fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
+    if (lane == 0) bulk_wait_all();   // the stores have completed before the CTA exits
   }
   fence_before();
   __syncthreads();
@@ -1779,14 +1860,23 @@ cudaError_t launch_tc16_experts(const LaunchCfg& lc, const PackView& pk, const W
   pd.nks = I / 64;
   // the down GEMM with the h tile resident when it and two weight stages fit in shared memory
   const int abytes = (I / 64) * 16384;
-  int nst = (232448 - 2048 - abytes) / tc::kDnStage;
+  // Y through TMA boxes when their staging fits beside two load stages, else plain row stores
+  const int room = 232448 - 2048 - abytes - tc::kDnConvBufs * tc::kDnConv;
+  int ybox = (room - tc::kDnYStaging) / tc::kDnLStage >= 2 ? 1 : 0;
+  int nst = (room - (ybox ? tc::kDnYStaging : 0)) / tc::kDnLStage;
   if (nst > tc::kDnMaxStages) nst = tc::kDnMaxStages;
+  CUtensorMap m_y32, m_y16;
+  if (ybox && !(make_map(&m_y32, ws.y, (uint64_t)H * 2, (uint64_t)ws.T * ws.k, 32) &&
+                make_map(&m_y16, ws.y, (uint64_t)H * 2, (uint64_t)ws.T * ws.k, 16)))
+    return cudaErrorInvalidValue;
+  if (!ybox) m_y32 = m_y16 = m_down;   // not read
   if (H % tc::kDnN == 0 && nst >= 2) {
-    const int smem = abytes + nst * tc::kDnStage + 1024;
+    const int smem = abytes + tc::kDnConvBufs * tc::kDnConv + nst * tc::kDnLStage +
+                     (ybox ? tc::kDnYStaging : 0) + 1024;
     e = cudaFuncSetAttribute(tc::k_tc16_dn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_kernel(lc, tc::k_tc16_dn, dim3(grid), dim3(tc::kT16Threads), (size_t)smem, m_down, m_h,
-                  pd, ws, nst);
+                  m_y32, m_y16, pd, ws, nst, ybox);
   }
   return launch_kernel(lc, tc::k_tc16<true>, dim3(grid), dim3(tc::kT16Threads), tc::T16<true>::kSmem,
                 m_down, m_down, m_h, pd, ws);

@@ -10,6 +10,9 @@ Branches (each compared with the oracle under the rules of tests/_gpu_fixtures.p
 * the wide grouped mma.sync path: W4A4 with H % 256 != 0, W4A16 with I % 128 != 0;
 * the W4A4 down GEMM with the token tile's h resident (several I), and with h restaged per unit
   (an I whose h tile does not fit twice beside two weight tiles);
+* the W4A16 / W4A8 resident-h down GEMM (k_tc16_dn) with Y stored in TMA boxes (32- and 16-row
+  boxes plus plain stores for a ragged tile's last rows) and, where the h tile leaves no room
+  for the staging (I = 512), with plain row stores only;
 * W4A4 with unequal gate/up input scales, which the library refuses (MOE_ERR_UNSUPPORTED).
 
 Chained layers: layer l's output is layer l+1's input, every layer with its own router and
@@ -87,6 +90,19 @@ def test_forward_w4a4_wide_down_variants(T, H, E, k, I):
     x, wr, ex = small_layer(T, H, E, k, I, seed=97 + I, zipf=True)
     pack = pack_from_experts(ex)
     run_and_check(x, wr, ex, pack, k, 1)
+    pack.close()
+
+
+@pytest.mark.parametrize("mode", [0, 2])
+@pytest.mark.parametrize("T,H,E,k,I", [
+    (45, 256, 3, 2, 128),     # one token tile per expert, 30 slots: 16-row box + 14 plain rows
+    (300, 512, 6, 2, 384),    # ~100 slots per expert (Zipf): 32-row boxes and ragged tails
+    (200, 256, 4, 2, 512),    # h tile of 128 KB: no room for the Y staging, plain row stores
+])
+def test_forward_w4a16_wide_down_y_stores(T, H, E, k, I, mode):
+    x, wr, ex = small_layer(T, H, E, k, I, seed=131 + I + mode, zipf=True)
+    pack = pack_from_experts(ex)
+    run_and_check(x, wr, ex, pack, k, mode)
     pack.close()
 
 
