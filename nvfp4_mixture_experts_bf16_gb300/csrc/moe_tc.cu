@@ -1264,7 +1264,11 @@ __global__ void __launch_bounds__(kT16Threads, 1)
 // (f16, all I columns, resident in shared memory while the CTA runs every 256-row weight tile of
 // that token tile), B = 256 dequantised down-weight rows x 64 K per stage, D = [slot][row]
 // (M = 128, N = 256) in tensor memory. The h tile is staged once per token tile instead of once
-// per weight tile, and each epilogue thread owns one slot, so Y rows are written directly.
+// per weight tile. Each epilogue thread owns one slot; per 64 columns an epilogue warp writes its
+// 32 slots' Y rows into a 128-byte swizzled staging box and stores the box with TMA (plain row
+// stores for a ragged tile's last rows, or for every row when the h tile leaves no room for the
+// staging). As in k_tc16, the ring of TMA load stages (codes and scale atoms) is separate from
+// the two dequantised-weight buffers.
 constexpr int kDnN = 256;
 constexpr uint32_t kIdescDn = (1u << 4) | ((uint32_t)(kDnN >> 3) << 17) |
                               ((uint32_t)(kTileM >> 4) << 24);   // f16 x f16 -> f32, 128x256
