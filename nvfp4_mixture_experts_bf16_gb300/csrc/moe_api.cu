@@ -74,7 +74,8 @@ int num_sms_of_current_device() {
 struct WsLayout {
   size_t ctl, gmeta, slot_amax, logits, idx, w, slot_of, counts, offsets, perm,
       chunk_base, xh, xfac, xq, xsf, h16, hq, hsf, y, htag, ytag, xres, tt_expert, tt_slot0, tt_n, ttbase, xq_perm,
-      xsf_atoms, hq_perm, hsf_atoms, xh_perm, hf_perm, sh_hs, sh_sigma, sh_y, sh_gu, total;
+      xsf_atoms, hq_perm, hsf_atoms, xh_perm, hf_perm, sh_hs, sh_sigma, sh_y, sh_gu, sh_tag, total;
+  size_t sh_tag_bytes;
   size_t slot_amax_bytes;
   int G, NT;
 };
@@ -130,6 +131,8 @@ WsLayout ws_layout(int T, int H, int E, int k, int I, int mode, int Is = 0) {
   L.sh_sigma = take(Is > 0 ? (size_t)T * 4 : 0);
   L.sh_y = take(Is > 0 ? (size_t)T * H * 4 : 0);
   L.sh_gu = take(Is > 0 && !narrow ? (size_t)T * 2 * Is * 4 : 0);
+  L.sh_tag_bytes = Is > 0 && narrow ? ((size_t)T * Is + T + (size_t)T * H) * 8 : 0;
+  L.sh_tag = take(L.sh_tag_bytes);
   // a layer of a chained stack: the next layer's input (this layer's input + output)
   L.xres = take(mode >= 0 ? (size_t)T * H * 2 : 0);
   L.total = o;
@@ -174,6 +177,7 @@ moe::WsView ws_view(void* ws, const WsLayout& L, int T, int H, int E, int k, int
   v.hf_perm = reinterpret_cast<__half*>(b + L.hf_perm);
   v.sh_y = nullptr;
   v.sh_sigma = nullptr;
+  v.sh_tag = L.sh_tag_bytes ? reinterpret_cast<unsigned long long*>(b + L.sh_tag) : nullptr;
   return v;
 }
 
@@ -240,9 +244,10 @@ bool layout_changed(const void* ws, uint64_t sig) {
 cudaError_t clear_tags(unsigned char* ws, size_t base, const WsLayout& L, int T, int H, int E,
                        int k, int I, cudaStream_t s) {
   const size_t S = (size_t)T * k;
-  const size_t parts[3][2] = {{L.logits, (size_t)T * E * 8 * moe::kLogitReplicas},
+  const size_t parts[4][2] = {{L.logits, (size_t)T * E * 8 * moe::kLogitReplicas},
                               {L.htag, S * (I / 16) * 9 * 8},
-                              {L.ytag, S * (H / 2) * 8}};
+                              {L.ytag, S * (H / 2) * 8},
+                              {L.sh_tag, L.sh_tag_bytes}};
   for (const auto& p : parts) {
     const cudaError_t e = cudaMemsetAsync(ws + base + p[0], 0, p[1], s);
     if (e != cudaSuccess) return e;
@@ -544,9 +549,8 @@ cudaError_t launch_forward(moe::LaunchCfg lc, const moe_expert_pack* pack,
   const int T = v.T, H = v.H, E = v.E, k = v.k, I = v.I;
   const bool narrow = T <= moe::kNarrowT;
   cudaError_t e = cudaSuccess;
+  moe::ShView sv{};
   if (sh) {
-    // the shared expert first: the combine (of whichever path runs) adds its term
-    moe::ShView sv;
     sv.gate_up = sh->gate_up;
     sv.down = sh->down;
     sv.gate = sh->gate;
@@ -555,11 +559,26 @@ cudaError_t launch_forward(moe::LaunchCfg lc, const moe_expert_pack* pack,
     sv.ys = reinterpret_cast<float*>(wsb + L.sh_y);
     sv.gu = reinterpret_cast<float*>(wsb + L.sh_gu);
     sv.Is = sh->inter;
+  }
+  const bool fused_ok = narrow && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr);
+  if (sh && fused_ok && T <= 2 && v.sh_tag) {
+    // one or two tokens: the shared expert inside the fused kernel (its weight rows stream while
+    // the router's logits are exchanged), unless the shape leaves it no room
+    const cudaError_t d = moe::launch_decode(lc, pack->view, v, m, pack->x_scale, pack->x_inv6S,
+                                             x, router_w, out, nullptr, &sv);
+    if (d != cudaErrorNotSupported && d != cudaErrorCooperativeLaunchTooLarge) {
+      *n += 1;
+      return d;
+    }
+    cudaGetLastError();
+  }
+  if (sh) {
+    // the shared expert first: the combine (of whichever path runs) adds its term
     e = moe::launch_shared(lc, x, sv, v, n);
     v.sh_y = sv.ys;
     v.sh_sigma = sv.sigma;
   }
-  if (narrow && moe::decode_geom(T, H, E, k, I, lc.num_sms, nullptr)) {
+  if (fused_ok) {
     // the whole routed step in one persistent kernel (unless its CTAs cannot all be resident)
     if (e == cudaSuccess) {
       const cudaError_t d = moe::launch_decode(lc, pack->view, v, m, pack->x_scale,

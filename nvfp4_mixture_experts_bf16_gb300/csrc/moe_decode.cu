@@ -44,6 +44,14 @@ constexpr int kDcCons = kDcWarps * 32;
 constexpr int kDnRows = 128;                      // rows of H per down task (16 per warp)
 constexpr int kDcSmemMax = 232448;                // 227 KB opt-in per block
 constexpr int kDcStatic = 1024;                   // static shared memory allowance
+constexpr int kShBatchIdx = 3;                    // shared expert: gate/up indices per batch
+constexpr int kShBatchRows = 2 * kShBatchIdx;     //   (a gate row and an up row each)
+constexpr int kShDnRows = 4;                      // shared expert: down rows per warp batch
+
+// Prefetch of bytes (a multiple of 16) at a 16-byte aligned global address into L2.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // One expert's token group (<= 8 tokens) of the current call.
 struct DcGroup {
@@ -72,6 +80,8 @@ struct DcGeom {
                                 // gate/up stages, else 1 (and a barrier after each epilogue)
   int smax, gmax;               // slots T*k, groups min(T*k, E)
   int smem;
+  int sh_off;                   // shared expert inside the kernel: arena offsets of its gate/up
+  int sh_hs;                    // rows and of its staged h
 };
 
 // Tagged words: {data in the low 32 bits, epoch of the writing call in the high 32 bits}, stored
@@ -234,11 +244,13 @@ __device__ __forceinline__ DcSplit dc_split(int U, int gu_tiles, int dn_tiles) {
   return sp;
 }
 
-template <int NT, int MODE>
+template <int NT, int MODE, bool SH>
 __global__ void __launch_bounds__(kDcThreads, 1)
     k_decode(PackView pk, WsView ws, DcGeom geo, const uint16_t* __restrict__ x,
              const uint16_t* __restrict__ wr, float xS, float x_inv6S,
-             uint16_t* __restrict__ out, uint16_t* __restrict__ xnext, int a8) {
+             uint16_t* __restrict__ out, uint16_t* __restrict__ xnext, int a8, ShView sv) {
+  // SH: the shared expert runs inside this launch (one or two tokens)
+  static_assert(!SH || NT <= 2, "the shared expert is fused for one or two tokens");
   // 0: W4A16, 1: quantised activations (one instantiation each: smaller code): NVFP4 (W4A4), or
   // E4M3 (W4A8) when a8 is set; both run the same f16 MMAs on exactly decoded values
   constexpr int mode = MODE;
@@ -264,14 +276,17 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   uint64_t* dempty = dfull + geo.dn_stages;
   uint64_t* rbar = dempty + geo.dn_stages;
   uint64_t* xbar = rbar + 1;
+  uint64_t* sbar = xbar + 1;   // the shared expert's gate/up rows (SH)
   unsigned char* xsep_row = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(xbar + 1) + 15) & ~uintptr_t(15));
+      (reinterpret_cast<uintptr_t>(sbar + 1) + 15) & ~uintptr_t(15));
   __shared__ float xfac_s[NT];
   __shared__ int shift_s[NT];
   __shared__ float hfac_s[kGroup];
   __shared__ uint32_t hamax_s[kGroup];
   __shared__ int wcount_s[kDcWarps + 1];
   __shared__ volatile int abort_s;
+  // shared expert (SH): per-warp partial sums of one batch of its gate/up rows
+  __shared__ float shp_s[SH ? (kDcWarps + 1) * kShBatchRows * NT : 1];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int T = NT;
@@ -294,6 +309,7 @@ __global__ void __launch_bounds__(kDcThreads, 1)
     }
     mbar_init(rbar, 1);
     mbar_init(xbar, 1);
+    mbar_init(sbar, 1);
     fence_mbar_init();
     abort_s = 0;
     // the router rows are weights: copy them before waiting for the preceding kernel
@@ -301,6 +317,31 @@ __global__ void __launch_bounds__(kDcThreads, 1)
       mbar_arrive_expect_tx(rbar, (uint32_t)nrows * H * 2);
       for (int r = 0; r < nrows; ++r)
         bulk_g2s(wrs + (size_t)r * geo.rs, wr + (size_t)(row0 + r) * H, (uint32_t)H * 2, rbar);
+    }
+    if constexpr (SH) {
+      // the shared expert's weights: this CTA's gate/up rows (indices [j0, j1) of 0..Is, index
+      // Is being the gate vector) into the arena past the first gate/up stage, and its down
+      // rows [r0, r1) of H towards L2 (read once its h is complete)
+      const int Is = sv.Is;
+      const int j0 = (int)((long long)(Is + 1) * b / G), j1 = (int)((long long)(Is + 1) * (b + 1) / G);
+      uint32_t bytes = 0;
+      for (int j = j0; j < j1; ++j) bytes += (j < Is ? 2u : 1u) * (uint32_t)H * 2;
+      if (bytes > 0) {
+        mbar_arrive_expect_tx(sbar, bytes);
+        unsigned char* dst = arena + geo.sh_off;
+        for (int j = j0; j < j1; ++j) {
+          const int jj = j - j0;
+          if (j < Is) {
+            bulk_g2s(dst + (size_t)(2 * jj) * H * 2, sv.gate_up + (size_t)j * H, (uint32_t)H * 2, sbar);
+            bulk_g2s(dst + (size_t)(2 * jj + 1) * H * 2, sv.gate_up + (size_t)(Is + j) * H,
+                     (uint32_t)H * 2, sbar);
+          } else {
+            bulk_g2s(dst + (size_t)(2 * jj) * H * 2, sv.gate, (uint32_t)H * 2, sbar);
+          }
+        }
+      }
+      const int r0 = (int)((long long)H * b / G), r1 = (int)((long long)H * (b + 1) / G);
+      if (r1 > r0) l2_prefetch(sv.down + (size_t)r0 * Is, (uint32_t)(r1 - r0) * Is * 2);
     }
   }
   __syncthreads();
@@ -584,6 +625,159 @@ __global__ void __launch_bounds__(kDcThreads, 1)
   // loads and delays the very stores it waits for)
   constexpr bool kSelectFirst = kEarlyTopk || MODE != 0;
   if (kSelectFirst && warp < T) select_token();
+
+  // ---------------- shared expert (SH: one or two tokens), while warps 0 .. T-1 select. The
+  // other warps form g = Wg[j] . x_t and u = Wu[j] . x_t for this CTA's indices j (FP32 sums of
+  // exact BF16 products), then hs = BF16(SiLU(g) * u), or sigma_t = 1 / (1 + exp(-gv . x_t)) for
+  // the gate vector, written plain and tagged; then, once every CTA's hs words have arrived,
+  // Ys[t][r] = Wd[r] . hs_t for this CTA's rows [r0, r1) of H (their weights loaded into
+  // registers before the wait), written plain (FP32) and tagged for the combine. The gate/up
+  // rows and the staged hs sit in the arena past the first gate/up stage, which no copy reaches
+  // before the barrier after the operand build (2b); one token's consumers wait on its first
+  // gate/up stage after that barrier anyway, so this work stays off the critical path.
+  if constexpr (SH) {
+    if (warp >= T) {
+      const int Is = sv.Is, nthr = (kDcWarps + 1 - T) * 32, i0 = tid - 32 * T;
+      const int j0 = (int)((long long)(Is + 1) * b / G), j1 = (int)((long long)(Is + 1) * (b + 1) / G);
+      const unsigned char* rows = arena + geo.sh_off;
+      const int nunits = H / 8;
+      unsigned long long* htag = ws.sh_tag;
+      unsigned long long* stag = htag + (size_t)T * Is;
+      unsigned long long* ytag = stag + T;
+      if (j1 > j0 && !mbar_wait(sbar, 0, geo.wait_ns)) {
+        record_status(ws.ctl, kStTimeout);
+        abort_s = 1;
+      }
+      for (int jb = j0; jb < j1; jb += kShBatchIdx) {
+        float acc[kShBatchRows][NT];
+#pragma unroll
+        for (int r = 0; r < kShBatchRows; ++r)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) acc[r][t] = 0.0f;
+        for (int u = i0; u < nunits; u += nthr) {
+          uint4 xv[NT];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) xv[t] = lds128(xraw + (size_t)t * geo.rs + u * 16);
+#pragma unroll
+          for (int r = 0; r < kShBatchRows; ++r) {
+            const int j = jb + r / 2;
+            if (j < j1 && (j < Is || (r & 1) == 0)) {
+              const uint4 wv =
+                  lds128(rows + (size_t)(2 * (j - j0) + (r & 1)) * H * 2 + (size_t)u * 16);
+#pragma unroll
+              for (int t = 0; t < NT; ++t) acc[r][t] += dot8_bf16(wv, xv[t]);
+            }
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kShBatchRows; ++r)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            float v = acc[r][t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+            if (lane == 0) shp_s[(warp * kShBatchRows + r) * NT + t] = v;
+          }
+        asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
+        if (i0 < kShBatchIdx * NT) {
+          const int q = i0 / NT, t = i0 % NT, j = jb + q;
+          if (j < j1) {
+            // the warps' partials in a fixed order
+            float g = 0.0f, uu = 0.0f;
+            for (int w = T; w <= kDcWarps; ++w) {
+              g += shp_s[(w * kShBatchRows + 2 * q) * NT + t];
+              uu += shp_s[(w * kShBatchRows + 2 * q + 1) * NT + t];
+            }
+            if (j < Is) {
+              const uint16_t hb = f32_to_bf16_rn(silu_mul(g, uu));
+              sv.hs[(size_t)t * Is + j] = hb;
+              st_tag(htag + (size_t)t * Is + j, hb, ep);
+            } else {
+              const float sg = 1.0f / (1.0f + expf(-g));
+              sv.sigma[t] = sg;
+              st_tag(stag + t, __float_as_uint(sg), ep);
+            }
+          }
+        }
+        asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");   // shp_s is reused
+      }
+      // down: warp wi of nw takes rows r0 + wi + nw * i, lanes the 16-byte units of a row
+      const int r0 = (int)((long long)H * b / G), r1 = (int)((long long)H * (b + 1) / G);
+      const int nw = kDcWarps + 1 - T, wi = warp - T, nu = Is / 8;
+      uint16_t* hsm = reinterpret_cast<uint16_t*>(arena + geo.sh_hs);
+      uint4 wd[kShDnRows][2];
+      auto load_rows = [&](int rb) {
+#pragma unroll
+        for (int rr = 0; rr < kShDnRows; ++rr) {
+          const int r = r0 + wi + nw * (rb + rr);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int u = lane + 32 * c;
+            wd[rr][c] = (r < r1 && u < nu)
+                            ? __ldg(reinterpret_cast<const uint4*>(sv.down + (size_t)r * Is) + u)
+                            : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      };
+      load_rows(0);
+      for (int idx = i0; idx < T * Is; idx += nthr) {
+        unsigned long long w[1];
+        if (!poll_tags<1>(htag + idx, ep, w, geo.wait_ns)) {
+          record_status(ws.ctl, kStTimeout);
+          abort_s = 1;
+        }
+        hsm[idx] = static_cast<uint16_t>(data_of(w[0]));
+      }
+      asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
+      for (int rb = 0; r0 + wi + nw * rb < r1; rb += kShDnRows) {
+        if (rb > 0) load_rows(rb);
+        float acc[kShDnRows][NT];
+#pragma unroll
+        for (int rr = 0; rr < kShDnRows; ++rr)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) acc[rr][t] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int u = lane + 32 * c;
+          if (u < nu) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const uint4 hv = lds128(reinterpret_cast<const unsigned char*>(hsm + (size_t)t * Is + u * 8));
+#pragma unroll
+              for (int rr = 0; rr < kShDnRows; ++rr) acc[rr][t] += dot8_bf16(wd[rr][c], hv);
+            }
+          }
+        }
+        // units past the register-held ones (Is > 512)
+        for (int u = 64 + lane; u < nu; u += 32) {
+#pragma unroll
+          for (int rr = 0; rr < kShDnRows; ++rr) {
+            const int r = r0 + wi + nw * (rb + rr);
+            if (r < r1) {
+              const uint4 wv = __ldg(reinterpret_cast<const uint4*>(sv.down + (size_t)r * Is) + u);
+#pragma unroll
+              for (int t = 0; t < NT; ++t)
+                acc[rr][t] += dot8_bf16(wv, lds128(reinterpret_cast<const unsigned char*>(hsm + (size_t)t * Is + u * 8)));
+            }
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < kShDnRows; ++rr) {
+          const int r = r0 + wi + nw * (rb + rr);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            float v = acc[rr][t];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+            if (lane == 0 && r < r1) {
+              sv.ys[(size_t)t * H + r] = v;
+              st_tag(ytag + (size_t)t * H + r, __float_as_uint(v), ep);
+            }
+          }
+        }
+      }
+    }
+  }
 
   // ---------------- 2b. activation operand of every token, in this CTA's shared memory
   {
@@ -1179,7 +1373,21 @@ __global__ void __launch_bounds__(kDcThreads, 1)
           a0 += wj * __uint_as_float(v << 16);
           a1 += wj * __uint_as_float(v & 0xFFFF0000u);
         }
-        if (ws.sh_y) {
+        if (SH) {
+          // the shared expert's term, after the routed ones (computed in this launch: its
+          // tagged gate and Ys words): sigma_t * BF16(Ys), Ys rounded like a routed expert's
+          // output
+          const unsigned long long* stag = ws.sh_tag + (size_t)T * sv.Is;
+          unsigned long long wy[2], wg[1];
+          if (!poll_tags<2>(stag + T + (size_t)t * H + ht * 128 + 2 * p2, ep, wy, geo.wait_ns) ||
+              !poll_tags<1>(stag + t, ep, wg, geo.wait_ns)) {
+            record_status(ws.ctl, kStTimeout);
+            abort_s = 1;
+          }
+          const float sg = __uint_as_float(data_of(wg[0]));
+          a0 += sg * bf16_round(__uint_as_float(data_of(wy[0])));
+          a1 += sg * bf16_round(__uint_as_float(data_of(wy[1])));
+        } else if (ws.sh_y) {
           // the shared expert's term, after the routed ones (written by an earlier kernel):
           // sigma_t * BF16(Ys), Ys rounded like a routed expert's output
           const float sg = __ldcg(ws.sh_sigma + t);
@@ -1251,6 +1459,8 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   DcGeom g{};
   g.wait_ns = kWaitLimitNs;
   g.skip_logits_cta = -1;
+  g.sh_off = 0;
+  g.sh_hs = 0;
   if (T < 1 || T > kNarrowT || num_ctas < 1) return false;
   g.rows_max = (E + num_ctas - 1) / num_ctas;
   if (g.rows_max > kDcWarps) return false;
@@ -1272,7 +1482,7 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
   const int scratch = T * k * 64 * 4;  // Y pairs of one tile for the combine
   const int red1 = kDcWarps * 2 * 128 * 4;   // one K-partial buffer
   int fixed = g.xop + red1 + g.gmax * (int)sizeof(DcGroup) + g.smax * 20 + 8 +
-              8 * (2 * 3 + 2 * 16 + 2) + 16 + g.xsep + kDcStatic;
+              8 * (2 * 3 + 2 * 16 + 3) + 16 + g.xsep + kDcStatic;
   g.redbufs = 1;
   if ((kDcSmemMax - fixed - red1) / g.gu_stage >= 2) {
     g.redbufs = 2;
@@ -1298,11 +1508,28 @@ bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom
 
 cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
                           float xS, float x_inv6S, const uint16_t* x, const uint16_t* wr,
-                          uint16_t* out, uint16_t* xnext) {
+                          uint16_t* out, uint16_t* xnext, const ShView* sv) {
   const int a8 = mode == 2;
   if (a8) mode = 1;   // W4A8 runs the quantised-activation instantiations
   DcGeom geo;
   if (!decode_geom(ws.T, ws.H, ws.E, ws.k, ws.I, lc.num_sms, &geo)) return cudaErrorInvalidValue;
+  ShView svv{};
+  int shf = 0;
+  if (sv) {
+    // the shared expert's gate/up rows of one CTA (2 rows of H BF16 per index) go into the
+    // arena past the first gate/up stage and the staged router / activation rows
+    if (ws.T > 2 || !ws.sh_tag || sv->Is % 64 != 0) return cudaErrorNotSupported;
+    const int idx_max = (sv->Is + 1 + lc.num_sms - 1) / lc.num_sms;
+    const int route_bytes = (geo.rows_max + (geo.xsep ? 0 : ws.T)) * geo.rs;
+    int off = geo.gu_stage > route_bytes ? geo.gu_stage : route_bytes;
+    off = (off + 127) & ~127;
+    const long long hs_off = ((long long)off + (long long)idx_max * 2 * ws.H * 2 + 15) & ~15LL;
+    if (hs_off + (long long)ws.T * sv->Is * 2 > geo.arena) return cudaErrorNotSupported;
+    geo.sh_off = off;
+    geo.sh_hs = (int)hs_off;
+    svv = *sv;
+    shf = 1;
+  }
   const FaultInjection& fi = fault_injection();
   if (fi.wait_ns) geo.wait_ns = fi.wait_ns;
   geo.skip_logits_cta = fi.skip_logits_cta;
@@ -1317,29 +1544,33 @@ cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView&
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     return launch_kernel(lc, kern, dim3(lc.num_sms), dim3(kDcThreads), (size_t)geo.smem, pk, ws,
-                         geo, x, wr, xS, x_inv6S, out, xnext, a8);
+                         geo, x, wr, xS, x_inv6S, out, xnext, a8, svv);
   };
+  if (shf) {
+    if (mode == 1) return ws.T == 1 ? go(k_decode<1, 1, true>) : go(k_decode<2, 1, true>);
+    return ws.T == 1 ? go(k_decode<1, 0, true>) : go(k_decode<2, 0, true>);
+  }
   if (mode == 1) {
     switch (ws.T) {
-      case 1: return go(k_decode<1, 1>);
-      case 2: return go(k_decode<2, 1>);
-      case 3: return go(k_decode<3, 1>);
-      case 4: return go(k_decode<4, 1>);
-      case 5: return go(k_decode<5, 1>);
-      case 6: return go(k_decode<6, 1>);
-      case 7: return go(k_decode<7, 1>);
-      default: return go(k_decode<8, 1>);
+      case 1: return go(k_decode<1, 1, false>);
+      case 2: return go(k_decode<2, 1, false>);
+      case 3: return go(k_decode<3, 1, false>);
+      case 4: return go(k_decode<4, 1, false>);
+      case 5: return go(k_decode<5, 1, false>);
+      case 6: return go(k_decode<6, 1, false>);
+      case 7: return go(k_decode<7, 1, false>);
+      default: return go(k_decode<8, 1, false>);
     }
   }
   switch (ws.T) {
-    case 1: return go(k_decode<1, 0>);
-    case 2: return go(k_decode<2, 0>);
-    case 3: return go(k_decode<3, 0>);
-    case 4: return go(k_decode<4, 0>);
-    case 5: return go(k_decode<5, 0>);
-    case 6: return go(k_decode<6, 0>);
-    case 7: return go(k_decode<7, 0>);
-    default: return go(k_decode<8, 0>);
+    case 1: return go(k_decode<1, 0, false>);
+    case 2: return go(k_decode<2, 0, false>);
+    case 3: return go(k_decode<3, 0, false>);
+    case 4: return go(k_decode<4, 0, false>);
+    case 5: return go(k_decode<5, 0, false>);
+    case 6: return go(k_decode<6, 0, false>);
+    case 7: return go(k_decode<7, 0, false>);
+    default: return go(k_decode<8, 0, false>);
   }
 }
 

@@ -89,6 +89,9 @@ struct WsView {
   // its gate, read by the combines
   const float* sh_y;      // [T][H]
   const float* sh_sigma;  // [T]
+  // narrow calls with the shared expert inside the fused kernel: tagged words of its h
+  // ([T][Is]), its gate ([T]) and its output Ys ([T][H]), in that order
+  unsigned long long* sh_tag;
   int T, H, E, k, I, G, NT;
 };
 
@@ -704,9 +707,12 @@ cudaError_t launch_combine(const LaunchCfg& lc, const WsView& ws, uint16_t* out)
 // launch.
 bool decode_geom(int T, int H, int E, int k, int I, int num_ctas, void* out_geom);
 // xnext (or null): [T][H] receives BF16(x + out), the input of the next layer of a chained stack.
+// sv (or null): the shared expert, computed inside the kernel (one or two tokens; the
+// workspace's sh_tag words and sv's hs / sigma / ys receive its intermediates).
+// cudaErrorNotSupported when it cannot be fused for the shape (the caller runs it separately).
 cudaError_t launch_decode(const LaunchCfg& lc, const PackView& pk, const WsView& ws, int mode,
                           float xS, float x_inv6S, const uint16_t* x, const uint16_t* wr,
-                          uint16_t* out, uint16_t* xnext);
+                          uint16_t* out, uint16_t* xnext, const ShView* sv = nullptr);
 // out[i] = BF16(a[i] + b[i]) over n BF16 values (n % 8 == 0): a chained layer's next input.
 cudaError_t launch_residual_add(const LaunchCfg& lc, const uint16_t* a, const uint16_t* b,
                                 uint16_t* out, size_t n);
