@@ -21,7 +21,10 @@
 //      tagged logits, by a threshold over the lane maxima), sorts the T*k selections by expert
 //      and builds the expert groups in shared memory (one token: in the selecting warp, which
 //      also issues the CTA's first gate/up copies). CTA 0 publishes idx / w / counts / offsets /
-//      perm / slot_of after its own work.
+//      perm / slot_of after its own work. With a BF16 shared expert and one or two tokens (the
+//      SH instantiations) the warps that do not select compute it meanwhile: h and its gate from
+//      this CTA's gate/up rows (copied before the wait on the preceding kernel), exchanged as
+//      tagged words, then this CTA's rows of its output Ys, tagged for the combine.
 //   3. gate/up + SiLU*up: tasks (group, 16-row tile of I), as in the multi-kernel path; h is
 //      written plain and tagged. As soon as its last gate/up stage is free, the producer warp
 //      streams this CTA's down weights into the same shared memory.
@@ -30,8 +33,8 @@
 //   5. combine: 128-row tile j of out is formed, once its tagged Y has arrived, by the j-th CTA
 //      in the order (late down tasks, CTA index), i.e. by CTAs done with their own down tasks
 //      first: the fixed-order weighted sum over each token's k experts (rank order, FP32, then
-//      BF16). A layer of a chained stack (moe_forward_layers) also writes the residual sum
-//      BF16(x + out), the next layer's input.
+//      BF16), plus sigma_t * BF16(Ys) of a shared expert. A layer of a chained stack
+//      (moe_forward_layers) also writes the residual sum BF16(x + out), the next layer's input.
 #include "moe_internal.cuh"
 #include <type_traits>
 

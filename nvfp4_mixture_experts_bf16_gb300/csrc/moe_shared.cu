@@ -8,7 +8,8 @@
 // combines round it to BF16 (an expert output, like the routed Y) and add sigma_t * BF16(Ys)
 // after the routed terms, before the output's rounding.
 //
-// Narrow calls (T <= 8) are two CUDA-core GEMVs over the BF16 weights (6 MB gate/up, 3 MB down
+// One or two tokens run the shared expert inside the fused narrow kernel (moe_decode.cu). Other
+// narrow calls (T <= 8) are two CUDA-core GEMVs over the BF16 weights (6 MB gate/up, 3 MB down
 // at H = 4096, Is = 384), one CTA per SM, each row read by one CTA with 16-byte loads on
 // consecutive lanes; a CTA issues its first weight loads before waiting on the preceding
 // kernel, so they stream while that kernel drains. Wide calls run the two products on the
