@@ -538,11 +538,16 @@ def test_forward_shared_ragged_shapes(T, mode):
     (3, 1024, 64, 6, 128, 640),   # Is > 512: the down rows' units past the register-held ones
     (40, 1024, 64, 6, 128, 640),  # the same through the tensor-core GEMMs (K = 640)
     (2, 4096, 64, 10, 384, 384),  # decode widths (H, I, Is) with 64 experts
+    (1, 1024, 64, 6, 128, 640),   # one token, inside the fused kernel, Is > 512
+    (1, 4096, 64, 10, 384, 2048),  # one token whose gate/up rows exceed the fused kernel's
+                                   # shared memory: the two separate GEMVs instead
 ])
 def test_forward_shared_shapes(T, H, E, k, I, Is):
     x, wr, ex = small_layer(T, H, E, k, I, seed=50 + T)
     pack = pack_from_experts(ex)
-    run_and_check(x, wr, ex, pack, k, 0, shared=synth.shared_expert_weights(50 + T, 0, H, Is))
+    r = run_and_check(x, wr, ex, pack, k, 0, shared=synth.shared_expert_weights(50 + T, 0, H, Is))
+    if T <= 2:
+        assert r["launches"] == (3 if Is == 2048 else 1)
     pack.close()
 
 
