@@ -184,9 +184,11 @@ moe_status moe_workspace_size_shared(const moe_expert_pack* pack, int T, int k, 
  *   hs  = BF16( SiLU(Wg x_t) * (Wu x_t) ),   Ys = Wd hs   (FP32 accumulation),
  *   out[t] = BF16( sum_j w_j * Y_j  +  sigma_t * BF16(Ys) ),  the shared term added after the
  * routed ones in FP32; Ys is rounded to BF16 like each routed expert's output Y. Arguments and requirements are those of moe_forward, plus `shared` (above);
- * a null or invalid `shared` returns MOE_ERR_INVALID_ARG. The shared expert runs first, as two
- * CUDA-core GEMV kernels for T <= 8 and as two tcgen05 BF16 GEMMs with a per-token kernel
- * between them for larger T. ws/ws_bytes: see moe_workspace_size_shared. */
+ * a null or invalid `shared` returns MOE_ERR_INVALID_ARG. For T <= 2 the shared expert is
+ * computed inside the one launch of the routed step (one launch in all) when its gate/up rows fit
+ * the kernel's shared memory; otherwise it runs first, as two CUDA-core GEMV kernels for
+ * T <= 8 and as two tcgen05 BF16 GEMMs with a per-token kernel between them for larger T.
+ * ws/ws_bytes: see moe_workspace_size_shared. */
 moe_status moe_forward_shared(const uint16_t* x, const uint16_t* router_w,
                               const moe_expert_pack* pack, const moe_shared_expert* shared, int T,
                               int k, moe_mode mode, uint16_t* out, void* ws, size_t ws_bytes,
